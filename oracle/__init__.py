@@ -1,0 +1,16 @@
+"""CPU oracle for the blockwise attention + FFN layer.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the package's ``smoke()`` check and
+the CPU-baseline leg of ``bench.py`` may import anything from here; the
+product path (the CUDA library and its Python binding) never does.
+
+* :mod:`oracle.ref` -- plain, materialised fp64 NumPy definition of the layer,
+  forward and analytic backward, plus a blockwise (online-softmax) fp64
+  variant used only to pin the definition against the method's own claim of
+  exactness.
+* :mod:`oracle.tiny` -- scalar-loop forward for tiny shapes (cross-check).
+* :mod:`oracle.accounting` -- the pages' parameter / activation / FLOP
+  accounting formulas.
+* :mod:`oracle.sampled` -- row-sampled forward and sparse-upstream-gradient
+  backward for sequence lengths where the dense oracle is too slow.
+"""

@@ -1,0 +1,80 @@
+"""The oracle's accounting formulas against the numbers the pages print."""
+import json
+import os
+
+import pytest
+
+from oracle import accounting as A
+from oracle.ref import LayerCfg
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_numbers.json")))
+
+
+def test_activation_theorem_in_sbh_units():
+    g = GOLD["activation_sbh"]
+    s, b, h, a = g["s"], g["b"], g["h"], g["a"]
+    sbh = s * b * h
+    assert A.vanilla_layer_activation_bytes(s, b, h, a) == g["vanilla"] * sbh
+    assert A.flash_layer_activation_bytes(s, b, h) == g["flash"] * sbh
+    assert A.full_checkpoint_bytes(s, b, h) == g["checkpoint"] * sbh
+    assert sum(A.theorem_items(s, b, h, a).values()) == A.vanilla_layer_activation_bytes(s, b, h, a)
+
+
+def test_worked_example_1p3b():
+    g = GOLD["worked_example_1p3b"]
+    L, h, a, V, s, b = g["L"], g["h"], g["a"], g["V"], g["s"], g["b"]
+    psi = A.gpt_model_params(L, h, V)
+    assert psi == g["psi"]
+    assert L * A.gpt_layer_params(h) == g["layers_params"]
+    assert V * h == g["embedding"]
+    assert round(12 * L * h * h / psi, 3) == g["ratio_12Lh2"]
+    gb = 1e9
+    states = A.model_state_bytes(psi) / gb
+    act = L * A.vanilla_layer_activation_bytes(s, b, h, a) / gb
+    logits = A.logits_bytes(s, b, V) / gb
+    assert round(states, 1) == g["states_gb"]
+    assert round(act, 1) == g["act_gb"]
+    assert round(logits, 1) == g["logits_gb"]
+    assert round(states + act + logits, 1) == g["total_gb"]
+    flash = L * A.flash_layer_activation_bytes(s, b, h) / gb
+    assert round(flash, 1) == g["flash_act_gb"]
+    assert round(states + flash + logits, 1) == g["flash_total_gb"]
+    ck_in = L * A.full_checkpoint_bytes(s, b, h) / gb
+    rebuilt = A.flash_layer_activation_bytes(s, b, h) / gb
+    assert round(ck_in, 1) == g["ckpt_inputs_gb"]
+    assert round(rebuilt, 1) == g["ckpt_rebuilt_gb"]
+    assert round(states + ck_in + rebuilt + logits, 1) == g["ckpt_total_gb"]
+
+
+def test_bpt_memory_terms():
+    g = GOLD["bpt_memory_terms"]
+    t = A.bpt_activation_terms(g["s"], g["b"], g["h"], g["c"])
+    assert round(t["bpt_output"] / 1e6) == g["two_bsh_millions"]
+    assert round(t["bpt_ffn_block"] / 1e6) == g["nineteen_bch_millions"]
+    assert t["flash_total"] / t["bpt_total"] == g["flash_over_bpt"]
+    # attention 2bsh vs FFN 8bsh in the FlashAttention regime: 4x
+    assert t["flash_ffn"] == 4 * t["flash_attention"]
+
+
+def test_checkpoint_every_k():
+    g = GOLD["checkpoint_every_k"]
+    assert A.checkpoint_every_k(g["L"], 1, g["c_sbh"], g["A_sbh"]) == g["M1_sbh"]
+    assert A.checkpoint_every_k(g["L"], 2, g["c_sbh"], g["A_sbh"]) == g["M2_sbh"]
+
+
+def test_step_flops_reduce_to_page_estimate():
+    # non-causal, f = 4h, H*d = h, G = 1: 3 * (24 b s h^2 + 4 b s^2 h)
+    s, h = 512, 256
+    cfg = LayerCfg(s=s, h=h, n_heads=4, n_kv_heads=4, head_dim=64, ffn_dim=4 * h, causal=False)
+    f = A.step_flops(cfg)
+    assert f["model"] == 3 * (24 * s * h * h + 4 * s * s * h)
+    # causal halves the attention part only
+    cc = LayerCfg(s=s, h=h, n_heads=4, n_kv_heads=4, head_dim=64, ffn_dim=4 * h)
+    fc = A.layer_flops(cc)
+    assert fc["attn"] * 2 == A.layer_flops(cfg)["attn"]
+
+
+@pytest.mark.parametrize("h", [256, 2048, 2560])
+def test_gpt_params_identity(h):
+    cfg = LayerCfg(s=8, h=h, n_heads=h // 64, n_kv_heads=h // 64, head_dim=64, ffn_dim=4 * h)
+    assert A.param_count(cfg) == 12 * h * h + 13 * h

@@ -1,0 +1,203 @@
+"""Python binding of libbpt (include/bpt.h): argument marshalling only.
+
+Every step of the layer runs in the CUDA library; this module turns torch
+tensors into the pointers and structs the C ABI takes.  PyTorch supplies
+device memory and streams.  There is no fallback: if the library is missing
+or fails to load, importing the binding's entry points raises.
+
+Entry points keep the C names: bpt_layer_fwd, bpt_layer_bwd,
+bpt_attn_headchunk, bpt_attention_fwd, bpt_attention_bwd,
+bpt_workspace_bytes, bpt_saved_bytes, bpt_attention_bwd_workspace_bytes,
+bpt_status_string, bpt_last_device_error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .presets import PRESETS, LayerConfig  # noqa: F401
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbpt.so")
+
+BPT_OK, BPT_EINVAL, BPT_ENOSPC, BPT_ECUDA, BPT_ETIMEOUT, BPT_EUNSUPPORTED = range(6)
+BPT_PASS_FWD, BPT_PASS_BWD, BPT_PASS_HEADCHUNK = 0, 1, 2
+BPT_FLAG_ACCUM_GRADS = 1
+
+WEIGHT_FIELDS = ("ln1_w", "ln1_b", "wq", "bq", "wk", "bk", "wv", "bv", "wo", "bo",
+                 "ln2_w", "ln2_b", "w1", "b1", "w2", "b2", "w3")
+
+
+class BptConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "b", "s", "h", "n_heads", "n_kv_heads", "head_dim", "ffn_dim",
+        "q_block", "kv_block", "ffn_block", "head_chunk", "causal", "norm", "act", "has_bias")] + \
+        [("norm_eps", ctypes.c_float), ("flags", ctypes.c_int32)]
+
+
+class BptWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_FIELDS]
+
+
+class BptGrads(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_FIELDS]
+
+
+class BptError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {bpt_status_string(status)} (status {status})")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libbpt.so (raises if it is missing: build it first with
+    ``python -m blockwise_attention_ffn_gb300.build`` or __graft_entry__.build())."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libbpt.so not built ({LIB_PATH} missing)")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        cfgp = ctypes.POINTER(BptConfig)
+        L.bpt_workspace_bytes.argtypes = [cfgp, i32]
+        L.bpt_workspace_bytes.restype = sz
+        L.bpt_saved_bytes.argtypes = [cfgp]
+        L.bpt_saved_bytes.restype = sz
+        L.bpt_layer_fwd.argtypes = [cfgp, ctypes.POINTER(BptWeights), vp, vp, vp, vp, sz, vp]
+        L.bpt_layer_fwd.restype = i32
+        L.bpt_layer_bwd.argtypes = [cfgp, ctypes.POINTER(BptWeights), vp, vp, vp, vp,
+                                    ctypes.POINTER(BptGrads), vp, sz, vp]
+        L.bpt_layer_bwd.restype = i32
+        L.bpt_attn_headchunk.argtypes = [cfgp, ctypes.POINTER(BptWeights), vp, vp, vp, vp, sz, vp]
+        L.bpt_attn_headchunk.restype = i32
+        L.bpt_attention_fwd.argtypes = [cfgp, vp, vp, vp, vp]
+        L.bpt_attention_fwd.restype = i32
+        L.bpt_attention_bwd_workspace_bytes.argtypes = [cfgp]
+        L.bpt_attention_bwd_workspace_bytes.restype = sz
+        L.bpt_attention_bwd.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.bpt_attention_bwd.restype = i32
+        L.bpt_status_string.argtypes = [i32]
+        L.bpt_status_string.restype = ctypes.c_char_p
+        L.bpt_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
+        L.bpt_last_device_error.restype = i32
+        _lib = L
+    return _lib
+
+
+# ------------------------------------------------------------------ marshalling
+
+def make_config(c) -> BptConfig:
+    """BptConfig from a LayerConfig (or any object with the same fields)."""
+    return BptConfig(c.b, c.s, c.h, c.n_heads, c.n_kv_heads, c.head_dim, c.ffn_dim, c.q_block,
+                     c.kv_block, c.ffn_block, c.head_chunk, c.causal, c.norm, c.act, c.has_bias,
+                     c.norm_eps, c.flags)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def make_weights(w: dict) -> BptWeights:
+    return BptWeights(*[(None if w.get(n) is None else w[n].data_ptr()) for n in WEIGHT_FIELDS])
+
+
+def make_grads(g: dict) -> BptGrads:
+    return BptGrads(*[(None if g.get(n) is None else g[n].data_ptr()) for n in WEIGHT_FIELDS])
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(rc, where):
+    if rc != BPT_OK:
+        raise BptError(rc, where)
+
+
+def bpt_status_string(status: int) -> str:
+    return lib().bpt_status_string(int(status)).decode()
+
+
+def bpt_workspace_bytes(cfg, pass_: int) -> int:
+    return int(lib().bpt_workspace_bytes(ctypes.byref(make_config(cfg)), int(pass_)))
+
+
+def bpt_saved_bytes(cfg) -> int:
+    return int(lib().bpt_saved_bytes(ctypes.byref(make_config(cfg))))
+
+
+def bpt_attention_bwd_workspace_bytes(cfg) -> int:
+    return int(lib().bpt_attention_bwd_workspace_bytes(ctypes.byref(make_config(cfg))))
+
+
+def bpt_layer_fwd(cfg, weights: dict, x, y, saved, ws, stream=None) -> None:
+    c = make_config(cfg)
+    w = make_weights(weights)
+    rc = lib().bpt_layer_fwd(ctypes.byref(c), ctypes.byref(w), _ptr(x), _ptr(y), _ptr(saved),
+                             _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    _check(rc, "bpt_layer_fwd")
+
+
+def bpt_layer_bwd(cfg, weights: dict, x, saved, dy, dx, grads: dict, ws, stream=None) -> None:
+    c = make_config(cfg)
+    w = make_weights(weights)
+    g = make_grads(grads)
+    rc = lib().bpt_layer_bwd(ctypes.byref(c), ctypes.byref(w), _ptr(x), _ptr(saved), _ptr(dy),
+                             _ptr(dx), ctypes.byref(g), _ptr(ws), ws.numel() * ws.element_size(),
+                             _stream(stream))
+    _check(rc, "bpt_layer_bwd")
+
+
+def bpt_attn_headchunk(cfg, weights: dict, xn, o, lse, ws, stream=None) -> None:
+    c = make_config(cfg)
+    w = make_weights(weights)
+    rc = lib().bpt_attn_headchunk(ctypes.byref(c), ctypes.byref(w), _ptr(xn), _ptr(o), _ptr(lse),
+                                  _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    _check(rc, "bpt_attn_headchunk")
+
+
+def bpt_attention_fwd(cfg, qkv, o, lse, stream=None) -> None:
+    c = make_config(cfg)
+    rc = lib().bpt_attention_fwd(ctypes.byref(c), _ptr(qkv), _ptr(o), _ptr(lse), _stream(stream))
+    _check(rc, "bpt_attention_fwd")
+
+
+def bpt_attention_bwd(cfg, qkv, o, lse, dout, dqkv, ws, stream=None) -> None:
+    c = make_config(cfg)
+    rc = lib().bpt_attention_bwd(ctypes.byref(c), _ptr(qkv), _ptr(o), _ptr(lse), _ptr(dout),
+                                 _ptr(dqkv), _ptr(ws), ws.numel() * ws.element_size(),
+                                 _stream(stream))
+    _check(rc, "bpt_attention_bwd")
+
+
+def bpt_last_device_error(stream=None):
+    """(status, detail) after synchronising the stream; clears the word."""
+    d = ctypes.c_int(0)
+    rc = lib().bpt_last_device_error(_stream(stream), ctypes.byref(d))
+    return int(rc), int(d.value)
+
+
+# ------------------------------------------------------------------ helpers
+
+def s_pad(cfg) -> int:
+    return (cfg.s + 127) // 128 * 128
+
+
+def alloc_bytes(n: int, device="cuda"):
+    """A 256-byte aligned uint8 device buffer of at least n bytes."""
+    import torch
+    return torch.empty(max(int(n), 256), dtype=torch.uint8, device=device)
+
+
+def alloc_grads(weights: dict, device="cuda") -> dict:
+    import torch
+    return {k: (None if v is None else torch.empty(v.shape, dtype=torch.float32, device=device))
+            for k, v in weights.items()}

@@ -1,0 +1,62 @@
+// attn_common.cuh -- shared-memory geometry of the attention tiles.
+//
+// A [128 rows x D] bf16 tile (Q, K, V, dO) is stored as D/CW column chunks of
+// [128 rows x CW] each, swizzled the way TMA writes them and tcgen05 reads
+// them: CW = 64 (128-byte swizzle) when D is a multiple of 64, else CW = 16
+// (32-byte swizzle).  The same chunked tile serves as a K-major operand (the
+// head dimension is the contraction: Q K^T, V dO^T) and as an MN-major operand
+// (the head dimension is N: P V, P^T dO, dS^T Q, dS K).
+#pragma once
+
+#include "ptx.cuh"
+
+namespace bpt {
+
+template <int D>
+struct TileGeom {
+  static constexpr int CW = (D % 64 == 0) ? 64 : 16;  // chunk width (elements)
+  static constexpr int SWB = CW * 2;                   // bytes per chunk row
+  static constexpr int NCH = D / CW;                   // chunks per tile
+  static constexpr int CHUNK = 128 * SWB;              // bytes per chunk
+  static constexpr int TILE = 128 * D * 2;             // bytes per tile
+  static constexpr uint32_t LAYOUT = (SWB == 128) ? 2u : 6u;  // descriptor swizzle code
+  static constexpr int TMA_SWZ = SWB;                  // swizzle bytes for the map
+
+  // K-major use: 16 columns of the head dimension starting at 16*kk
+  static __device__ __forceinline__ uint64_t kmajor(uint32_t tile, int kk) {
+    const int c = (kk * 16) / CW;
+    const int off = ((kk * 16) % CW) * 2;
+    return sdesc(tile + c * CHUNK + off, 16, 8 * SWB, LAYOUT);
+  }
+  // MN-major use (N = D): 16 rows (the contraction) starting at 16*kk
+  static __device__ __forceinline__ uint64_t mnmajor(uint32_t tile, int kk) {
+    return sdesc(tile + kk * 16 * SWB, CHUNK, 8 * SWB, LAYOUT);
+  }
+};
+
+// A [128 x 128] bf16 tile written by threads (P, P^T, dS^T): two 64-column
+// chunks of [128 rows x 128 B], 128-byte swizzle.
+struct SqTile {
+  static constexpr int BYTES = 128 * 128 * 2;
+  // byte offset of columns 8*c .. 8*c+7 of row r
+  static __device__ __forceinline__ uint32_t off(int r, int c) {
+    return (uint32_t)((c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+  }
+  // K-major use (contraction along the columns): 16 columns from 16*kk
+  static __device__ __forceinline__ uint64_t kmajor(uint32_t tile, int kk) {
+    return sdesc(tile + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, 2u);
+  }
+  // MN-major use (contraction along the rows, the columns are M or N): 16
+  // rows from 16*kk
+  static __device__ __forceinline__ uint64_t mnmajor(uint32_t tile, int kk) {
+    return sdesc(tile + kk * 16 * 128, 16384, 1024, 2u);
+  }
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+}  // namespace bpt

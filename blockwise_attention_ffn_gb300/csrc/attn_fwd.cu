@@ -1,0 +1,385 @@
+// attn_fwd.cu -- blockwise causal attention with online softmax on tcgen05.
+//
+// "Blockwise Parallel Transformer for Long Context Large Models", section 3.4,
+// "Blockwise Self-Attention with Online Softmax" and "The Nested-Loop
+// Algorithm in Detail (Algorithm 1)": for one query block, loop over the
+// key/value blocks; keep a running row max m, denominator l and numerator
+// (here O in TMEM); for each block S = Q K_j^T / sqrt(d) with the causal bias,
+// m' = max(m, rowmax S), correction exp(m - m'), l = l*corr + rowsum exp(S - m'),
+// O = O*corr + exp(S - m') V_j; finally O / l.  The log-sum-exp m + ln l of
+// every row is written for the recompute backward.
+//
+// One CTA = one 128-row query tile of one head (GQA: key/value head n / G).
+//   warp 0      TMA: the Q tile once, K/V tiles through a KVS-deep ring
+//   warp 1      TMEM owner and MMA issuer: S_j = Q K_j^T into one of two TMEM
+//               S buffers, then O += P_{j-1} V_{j-1} (P from shared memory)
+//   warps 2..5  softmax, one query row per thread: reads its S row from TMEM,
+//               masks, updates m and l, writes P (bf16) to shared memory,
+//               rescales its O row in TMEM when the max moved by more than
+//               2^8 (otherwise keeps the stale max: exact, since O and l are
+//               scaled alike), and at the end normalises and stores O.
+// The s x s score matrix never leaves TMEM/registers.
+#include <math.h>
+#include <string.h>
+
+#include "attn_common.cuh"
+#include "internal.h"
+
+namespace bpt {
+
+namespace {
+
+struct AttnFwdParams {
+  CUtensorMap map_qkv;  // 3-D {ld_qkv, s, b}, box {CW, 128, 1}
+  int s, s_pad, H, G, causal;
+  int q_col, k_col, v_col;
+  __nv_bfloat16* o;
+  long long ld_o, o_row0;
+  int o_col;
+  float* lse;
+  int H_total, lse_head0;
+  int qt_begin, n_qt, b;
+  float scale_log2;  // log2(e) / sqrt(d)
+  float scale;       // 1 / sqrt(d)
+  unsigned int* err;
+};
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x,
+                                            int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+template <int D>
+struct FwdCfg {
+  using T = TileGeom<D>;
+  static constexpr int KVS = (D <= 80) ? 3 : 2;
+  static constexpr int SMEM_TILES = T::TILE * (1 + 2 * KVS) + 2 * SqTile::BYTES;
+  static constexpr int SMEM = SMEM_TILES + 1024 + 256;
+};
+
+template <int D>
+__global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant__ AttnFwdParams p) {
+  using T = TileGeom<D>;
+  constexpr int KVS = FwdCfg<D>::KVS;
+  constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
+  constexpr uint32_t IDESC_PV = idesc_bf16(128, D, false, true);
+  constexpr float NEG_INF = -INFINITY;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sKV = sQ + T::TILE;
+  uint8_t* sP = sKV + KVS * 2 * T::TILE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * SqTile::BYTES);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_empty = kv_full + KVS;
+  uint64_t* s_full = kv_empty + KVS;
+  uint64_t* s_free = s_full + 2;
+  uint64_t* p_full = s_free + 2;
+  uint64_t* pv_done = p_full + 2;
+  uint64_t* drain = pv_done + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+
+  // tile scheduling: heaviest query tiles first, heads of one tile adjacent
+  const int hb = p.H * p.b;
+  const int qt_rev = blockIdx.x / hb;
+  const int rem = blockIdx.x % hb;
+  const int n = rem % p.H;
+  const int bi = rem / p.H;
+  const int qt = p.qt_begin + p.n_qt - 1 - qt_rev;
+  const int q0 = qt * 128;
+  const int g = n / p.G;
+  const int kv_tiles_total = (p.s + 127) / 128;
+  const int nkv = p.causal ? min(qt + 1, kv_tiles_total) : kv_tiles_total;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < KVS; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 4);
+      mbar_init(&p_full[i], 4);
+    }
+    mbar_init(pv_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) tma_prefetch(&p.map_qkv);
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t tS = tmem;        // two 128-column S buffers
+  const uint32_t tO = tmem + 256;  // D columns
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      mbar_expect_tx(q_full, T::TILE);
+#pragma unroll
+      for (int c = 0; c < T::NCH; ++c)
+        tma_load_3d(sQ + c * T::CHUNK, &p.map_qkv, q_full, p.q_col + n * D + c * T::CW, q0, bi);
+      int issued = 0;
+      for (int j = 0; j < nkv; ++j) {
+        const int st = j % KVS;
+        if (j >= KVS && !bounded_wait(&kv_empty[st], ((j / KVS) & 1) ^ 1, abort_flag, 201, p.err)) break;
+        uint8_t* sK = sKV + st * 2 * T::TILE;
+        uint8_t* sV = sK + T::TILE;
+        mbar_expect_tx(&kv_full[st], 2 * T::TILE);
+#pragma unroll
+        for (int c = 0; c < T::NCH; ++c)
+          tma_load_3d(sK + c * T::CHUNK, &p.map_qkv, &kv_full[st], p.k_col + g * D + c * T::CW, j * 128, bi);
+#pragma unroll
+        for (int c = 0; c < T::NCH; ++c)
+          tma_load_3d(sV + c * T::CHUNK, &p.map_qkv, &kv_full[st], p.v_col + g * D + c * T::CW, j * 128, bi);
+        issued = j + 1;
+      }
+      if (*abort_flag) {
+        bounded_wait(q_full, 0, abort_flag, 202, p.err);
+        for (int j = (issued > KVS ? issued - KVS : 0); j < issued; ++j)
+          mbar_try_wait(&kv_full[j % KVS], (j / KVS) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      const uint32_t uQ = smem_u32(sQ);
+      const uint32_t uKV = smem_u32(sKV);
+      const uint32_t uP = smem_u32(sP);
+      bool ok = bounded_wait(q_full, 0, abort_flag, 211, p.err);
+      auto issue_pv = [&](int i) -> bool {
+        if (!bounded_wait(&p_full[i & 1], (i >> 1) & 1, abort_flag, 212, p.err)) return false;
+        tc_fence_after();
+        const uint32_t pt = uP + (i & 1) * SqTile::BYTES;
+        const uint32_t vt = uKV + (i % KVS) * 2 * T::TILE + T::TILE;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16(tO, SqTile::kmajor(pt, kk), T::mnmajor(vt, kk), IDESC_PV, (i > 0 || kk > 0));
+        umma_commit(&kv_empty[i % KVS]);
+        umma_commit(pv_done);
+        return true;
+      };
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int st = j % KVS;
+        const int sb = j & 1;
+        if (!bounded_wait(&kv_full[st], (j / KVS) & 1, abort_flag, 213, p.err)) { ok = false; break; }
+        if (j >= 2 && !bounded_wait(&s_free[sb], ((j - 2) >> 1) & 1, abort_flag, 214, p.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t kt = uKV + st * 2 * T::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_bf16(tS + sb * 128, T::kmajor(uQ, kk), T::kmajor(kt, kk), IDESC_S, kk > 0);
+        umma_commit(&s_full[sb]);
+        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+      }
+      if (ok) ok = issue_pv(nkv - 1);
+      if (!ok) {
+        umma_commit(drain);
+        bounded_wait(drain, 0, abort_flag, 215, p.err);
+      }
+    }
+  } else {
+    // ------------------------------------------------ softmax (warps 2..5)
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int qpos = q0 + r;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const float c = p.scale_log2;
+    float m_run = NEG_INF, l_run = 0.f;
+    bool ok = true;
+    uint8_t* myP0 = sP;
+    for (int j = 0; j < nkv; ++j) {
+      const int sb = j & 1;
+      ok = bounded_wait(&s_full[sb], (j >> 1) & 1, abort_flag, 221, p.err);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      float sv[128];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t rr[32];
+        tmem_ld32(tS + lane_off + sb * 128 + q4 * 32, rr);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sv[q4 * 32 + i] = __uint_as_float(rr[i]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[sb]);
+
+      const int kv0 = j * 128;
+      const bool diag = p.causal ? (kv0 + 127 > q0) : (kv0 + 128 > p.s);
+      if (diag) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+          const int kp = kv0 + i;
+          if (kp >= p.s || (p.causal && kp > qpos)) sv[i] = NEG_INF;
+        }
+      }
+      float mx = sv[0];
+#pragma unroll
+      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, sv[i]);
+      const float m_new = fmaxf(m_run, mx);
+      const bool need = (m_new - m_run) * c > 8.f;
+      const bool rescale = __any_sync(0xffffffffu, need);
+      float alpha = 1.f;
+      if (rescale) {
+        alpha = ex2((m_run - m_new) * c);
+        m_run = m_new;
+      }
+      const float mc = m_run * c;
+      float rs = 0.f;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        sv[i] = ex2(fmaf(sv[i], c, -mc));
+        rs += sv[i];
+      }
+      l_run = l_run * alpha + rs;
+
+      if (j > 0) {
+        ok = bounded_wait(pv_done, (j - 1) & 1, abort_flag, 222, p.err);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        if (rescale) {
+#pragma unroll 1
+          for (int cc = 0; cc < D / 16; ++cc) {
+            uint32_t ro[16];
+            tmem_ld16(tO + lane_off + cc * 16, ro);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ro[i] = __float_as_uint(__uint_as_float(ro[i]) * alpha);
+            tmem_st16(tO + lane_off + cc * 16, ro);
+          }
+          tmem_st_wait();
+        }
+      }
+      // P (bf16) into the swizzled K-major tile of buffer sb
+      uint8_t* pb = myP0 + sb * SqTile::BYTES;
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch) {
+        uint4 u;
+        u.x = pack_bf16(sv[ch * 8 + 0], sv[ch * 8 + 1]);
+        u.y = pack_bf16(sv[ch * 8 + 2], sv[ch * 8 + 3]);
+        u.z = pack_bf16(sv[ch * 8 + 4], sv[ch * 8 + 5]);
+        u.w = pack_bf16(sv[ch * 8 + 6], sv[ch * 8 + 7]);
+        *reinterpret_cast<uint4*>(pb + SqTile::off(r, ch)) = u;
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[sb]);
+    }
+    if (ok) {
+      ok = bounded_wait(pv_done, (nkv - 1) & 1, abort_flag, 223, p.err);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = 1.f / l_run;
+      const bool valid = qpos < p.s;
+      __nv_bfloat16* orow = p.o + ((long long)bi * p.s + qpos - p.o_row0) * p.ld_o + p.o_col + (long long)n * D;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 16; ++cc) {
+        uint32_t ro[16];
+        tmem_ld16(tO + lane_off + cc * 16, ro);
+        if (valid) {
+          uint4 u0, u1;
+          u0.x = pack_bf16(__uint_as_float(ro[0]) * inv_l, __uint_as_float(ro[1]) * inv_l);
+          u0.y = pack_bf16(__uint_as_float(ro[2]) * inv_l, __uint_as_float(ro[3]) * inv_l);
+          u0.z = pack_bf16(__uint_as_float(ro[4]) * inv_l, __uint_as_float(ro[5]) * inv_l);
+          u0.w = pack_bf16(__uint_as_float(ro[6]) * inv_l, __uint_as_float(ro[7]) * inv_l);
+          u1.x = pack_bf16(__uint_as_float(ro[8]) * inv_l, __uint_as_float(ro[9]) * inv_l);
+          u1.y = pack_bf16(__uint_as_float(ro[10]) * inv_l, __uint_as_float(ro[11]) * inv_l);
+          u1.z = pack_bf16(__uint_as_float(ro[12]) * inv_l, __uint_as_float(ro[13]) * inv_l);
+          u1.w = pack_bf16(__uint_as_float(ro[14]) * inv_l, __uint_as_float(ro[15]) * inv_l);
+          reinterpret_cast<uint4*>(orow + cc * 16)[0] = u0;
+          reinterpret_cast<uint4*>(orow + cc * 16)[1] = u1;
+        }
+      }
+      // every row of the padded tile gets a finite value (rows past s see the
+      // zero-filled query), so the backward pass never reads garbage
+      if (p.lse)
+        p.lse[((long long)bi * p.H_total + p.lse_head0 + n) * p.s_pad + qpos] = m_run * p.scale + logf(l_run);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+int launch_fwd(AttnFwdParams& prm, int grid, cudaStream_t st) {
+  constexpr int SMEM = FwdCfg<D>::SMEM;
+  static_assert(SMEM <= 232448, "attention forward tile set exceeds shared memory");
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
+      return 3;
+    attr = true;
+  }
+  attn_fwd_kernel<D><<<grid, 192, SMEM, st>>>(prm);
+  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
+}  // namespace
+
+int make_attn_map(CUtensorMap* map, const void* qkv, int b, int s, int64_t ld, int d);
+
+int attention_fwd(const AttnShape& sh, const void* qkv, void* o, float* lse, cudaStream_t st) {
+  if (sh.q_end <= sh.q_begin) return 0;
+  AttnFwdParams prm;
+  memset(&prm, 0, sizeof(prm));
+  if (make_attn_map(&prm.map_qkv, qkv, sh.b, sh.s, sh.ld_qkv, sh.d)) return 1;
+  prm.s = sh.s;
+  prm.s_pad = (sh.s + 127) / 128 * 128;
+  prm.H = sh.H;
+  prm.G = sh.H / sh.Hkv;
+  prm.causal = sh.causal;
+  prm.q_col = (int)sh.q_col;
+  prm.k_col = (int)sh.k_col;
+  prm.v_col = (int)sh.v_col;
+  prm.o = reinterpret_cast<__nv_bfloat16*>(o);
+  prm.ld_o = sh.ld_o;
+  prm.o_row0 = sh.o_row0;
+  prm.o_col = (int)sh.o_col;
+  prm.lse = lse;
+  prm.H_total = sh.H_total;
+  prm.lse_head0 = sh.lse_head0;
+  prm.qt_begin = sh.q_begin / 128;
+  prm.n_qt = (sh.q_end + 127) / 128 - prm.qt_begin;
+  prm.b = sh.b;
+  prm.scale = 1.f / sqrtf((float)sh.d);
+  prm.scale_log2 = prm.scale * 1.4426950408889634f;
+  prm.err = device_error_word();
+  if (!prm.err) return 3;
+  const int grid = prm.n_qt * sh.H * sh.b;
+  switch (sh.d) {
+    case 64: return launch_fwd<64>(prm, grid, st);
+    case 80: return launch_fwd<80>(prm, grid, st);
+    case 96: return launch_fwd<96>(prm, grid, st);
+    case 112: return launch_fwd<112>(prm, grid, st);
+    case 128: return launch_fwd<128>(prm, grid, st);
+    default: return 5;
+  }
+}
+
+}  // namespace bpt

@@ -1,0 +1,721 @@
+// bpt_api.cu -- the C ABI (include/bpt.h): argument validation, workspace
+// planning and the launch sequences of the forward pass, the recompute
+// backward pass and the head-chunked attention.
+//
+// Forward schedule ("Blockwise Parallel Transformer for Long Context Large
+// Models", section 3.2 and Algorithm 1): N1 and the Q/K/V projection for the
+// whole sequence (they are position-wise and not part of the memory
+// optimisation); then, for every FFN block of c_f query rows: attention of
+// those rows over their key/value blocks, output projection + bias +
+// residual, N2, fc1 + activation, fc2 + bias + residual -> y.  Only a
+// c_f x f block of the FFN intermediate ever exists.
+//
+// Head-chunk mode ("Untied Ulysses ...", section 3.4 "The Core Mechanism:
+// Headwise Chunking via UPipe", restricted to one GPU): the projection and
+// attention run in H/U stages of U query heads and U/G key/value heads; the
+// stage buffer is reused and the attention output buffer is filled slice by
+// slice; the FFN blocks follow.
+//
+// Backward ("Training memory ...", section 3, full activation checkpointing:
+// rerun the forward, then the backward): N1, Q/K/V and attention are rebuilt
+// (the saved log-sum-exp is reused by the attention backward); per FFN block
+// x1, N2, fc1 are rebuilt and the FFN / N2 gradients formed; then the output
+// projection, attention (per stage) and Q/K/V gradients, and N1.
+#include <cuda_runtime.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "../../include/bpt.h"
+#include "internal.h"
+
+using namespace bpt;
+
+namespace {
+
+struct Dims {
+  int64_t b, s, h, H, Hkv, d, f, G, U, cf, s_pad, rows, n_stages;
+  bool chunked;
+  int64_t Uk;      // key/value heads per stage
+  int64_t qkv_w;   // columns of the (stage) projection buffer
+};
+
+int validate(const bpt_config* c, Dims* D) {
+  if (!c) return BPT_EINVAL;
+  if (c->b < 1 || c->s < 1 || c->h < 8 || (c->h % 8) || c->n_heads < 1 || c->n_kv_heads < 1 ||
+      (c->n_heads % c->n_kv_heads) || c->ffn_dim < 8 || (c->ffn_dim % 8))
+    return BPT_EINVAL;
+  if (c->norm != BPT_NORM_LAYER && c->norm != BPT_NORM_RMS) return BPT_EINVAL;
+  if (c->act < 0 || c->act > 2) return BPT_EINVAL;
+  if (c->has_bias != 0 && c->has_bias != 1) return BPT_EINVAL;
+  if (c->q_block <= 0 || (c->q_block % 128) || c->kv_block <= 0 || (c->kv_block % 128)) return BPT_EINVAL;
+  if (c->ffn_block < 0 || (c->ffn_block % c->q_block)) return BPT_EINVAL;
+  if (!(c->norm_eps > 0.f)) return BPT_EINVAL;
+  if (c->act == BPT_ACT_SWIGLU && (c->ffn_dim % 64)) return BPT_EINVAL;
+  if (c->flags & ~BPT_FLAG_ACCUM_GRADS) return BPT_EINVAL;
+  const int d = c->head_dim;
+  if (d != 64 && d != 80 && d != 96 && d != 112 && d != 128) return BPT_EUNSUPPORTED;
+  const int G = c->n_heads / c->n_kv_heads;
+  int U = c->head_chunk;
+  if (U == 0) U = c->n_heads;
+  if (U < 1 || (c->n_heads % U) || (U % G)) return BPT_EINVAL;
+  if ((int64_t)c->s * c->b >= (int64_t(1) << 31)) return BPT_EINVAL;
+  D->b = c->b;
+  D->s = c->s;
+  D->h = c->h;
+  D->H = c->n_heads;
+  D->Hkv = c->n_kv_heads;
+  D->d = d;
+  D->f = c->ffn_dim;
+  D->G = G;
+  D->U = U;
+  D->Uk = U / G;
+  D->chunked = U < c->n_heads;
+  D->n_stages = c->n_heads / U;
+  D->s_pad = (D->s + 127) / 128 * 128;
+  D->cf = c->ffn_block ? c->ffn_block : std::min<int64_t>(2048, D->s_pad);
+  D->cf = std::min<int64_t>(D->cf, D->s_pad);
+  D->rows = D->b * D->s;
+  D->qkv_w = (D->U + 2 * D->Uk) * d;
+  return BPT_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int check_weights(const bpt_config* c, const bpt_weights* w) {
+  if (!w) return BPT_EINVAL;
+  const void* need[] = {w->ln1_w, w->wq, w->wk, w->wv, w->wo, w->ln2_w, w->w1, w->w2};
+  for (const void* p : need)
+    if (!p || !aligned16(p)) return BPT_EINVAL;
+  if (c->norm == BPT_NORM_LAYER && (!w->ln1_b || !w->ln2_b || !aligned16(w->ln1_b) || !aligned16(w->ln2_b)))
+    return BPT_EINVAL;
+  if (c->act == BPT_ACT_SWIGLU && (!w->w3 || !aligned16(w->w3))) return BPT_EINVAL;
+  if (c->has_bias) {
+    const void* bs[] = {w->bq, w->bk, w->bv, w->bo, w->b2};
+    for (const void* p : bs)
+      if (!p || !aligned16(p)) return BPT_EINVAL;
+    if (c->act != BPT_ACT_SWIGLU && (!w->b1 || !aligned16(w->b1))) return BPT_EINVAL;
+  }
+  return BPT_OK;
+}
+
+// ---------------------------------------------------------------- workspace
+struct Carve {
+  uint8_t* base;
+  size_t off = 0;
+  explicit Carve(void* b) : base(reinterpret_cast<uint8_t*>(b)) {}
+  void* take(size_t bytes) {
+    void* p = base ? base + off : nullptr;
+    off += (bytes + 255) / 256 * 256;
+    return p;
+  }
+};
+
+struct FwdWs {
+  void *xn, *qkv, *o, *x1, *x1n, *a;
+  float* lse;
+};
+size_t plan_fwd(const Dims& D, void* base, FwdWs* w, bool need_lse) {
+  Carve c(base);
+  w->xn = c.take(D.rows * D.h * 2);
+  w->qkv = c.take(D.rows * D.qkv_w * 2);
+  w->o = c.take((D.chunked ? D.rows : D.cf) * D.H * D.d * 2);
+  w->x1 = c.take(D.cf * D.h * 2);
+  w->x1n = c.take(D.cf * D.h * 2);
+  w->a = c.take(D.cf * D.f * 2);
+  w->lse = reinterpret_cast<float*>(need_lse ? c.take(D.b * D.H * D.s_pad * 4) : nullptr);
+  return c.off;
+}
+
+struct BwdWs {
+  void *xn, *qkv, *o, *x1, *x1n, *z, *g, *u, *a, *dz, *dx1n, *dx1, *dO, *dqkv, *attn;
+  float* dxn;
+};
+AttnBwdShape stage_bwd_shape(const Dims& D, int64_t k);
+size_t plan_bwd(const Dims& D, void* base, BwdWs* w) {
+  Carve c(base);
+  const bool swiglu_like = true;  // sized for the larger (SwiGLU) case
+  (void)swiglu_like;
+  w->xn = c.take(D.rows * D.h * 2);
+  w->qkv = c.take(D.rows * D.qkv_w * 2);
+  w->o = c.take(D.rows * D.H * D.d * 2);
+  w->x1 = c.take(D.cf * D.h * 2);
+  w->x1n = c.take(D.cf * D.h * 2);
+  w->z = c.take(D.cf * D.f * 2);   // GeLU: pre-activation; SwiGLU: gate g
+  w->u = c.take(D.cf * D.f * 2);   // SwiGLU: up u
+  w->g = w->z;
+  w->a = c.take(D.cf * D.f * 2);
+  w->dz = c.take(D.cf * D.f * 2 * 2);  // GeLU: dz [cf, f]; SwiGLU: [dg | du] [cf, 2f]
+  w->dx1n = c.take(D.cf * D.h * 2);
+  w->dx1 = c.take(D.rows * D.h * 2);
+  w->dO = c.take(D.rows * D.H * D.d * 2);
+  w->dqkv = c.take(D.rows * D.qkv_w * 2);
+  w->dxn = reinterpret_cast<float*>(c.take(D.rows * D.h * 4));
+  w->attn = c.take(attention_bwd_ws_bytes(stage_bwd_shape(D, 0)));
+  return c.off;
+}
+
+size_t plan_headchunk(const Dims& D, void* base, void** qkv) {
+  Carve c(base);
+  *qkv = c.take(D.rows * D.qkv_w * 2);
+  return c.off;
+}
+
+// ---------------------------------------------------------------- pieces
+const uint8_t* bf(const void* p, int64_t elems) { return reinterpret_cast<const uint8_t*>(p) + elems * 2; }
+uint8_t* bfm(void* p, int64_t elems) { return reinterpret_cast<uint8_t*>(p) + elems * 2; }
+float* f32(void* p, int64_t elems) { return reinterpret_cast<float*>(p) + elems; }
+
+// Q/K/V of stage k (all stages = one stage when not chunked) for all rows:
+// qkv[:, 0:U d] = xn Wq[kU d : (k+1)U d]^T (+ bq), then K, V of the stage's
+// U/G key/value heads.
+int stage_qkv(const Dims& D, const bpt_weights* w, bool has_bias, const void* xn, void* qkv, int64_t k,
+              cudaStream_t st) {
+  const int64_t d = D.d, h = D.h;
+  const int64_t q0 = k * D.U * d, kv0 = k * D.Uk * d;
+  struct Piece {
+    const void* W;
+    const void* bias;
+    int64_t row0, n, col;
+  } pieces[3] = {{w->wq, w->bq, q0, D.U * d, 0},
+                 {w->wk, w->bk, kv0, D.Uk * d, D.U * d},
+                 {w->wv, w->bv, kv0, D.Uk * d, (D.U + D.Uk) * d}};
+  MatView A{xn, D.rows, h, h};
+  for (auto& pc : pieces) {
+    MatView B{bf(pc.W, pc.row0 * h), pc.n, h, h};
+    Epilogue e;
+    e.kind = EPI_BF16;
+    e.out = bfm(qkv, pc.col);
+    e.ldo = D.qkv_w;
+    e.bias = has_bias ? bf(pc.bias, pc.row0) : nullptr;
+    int64_t kseg = h;
+    int rc = gemm(D.rows, pc.n, h, A, false, &B, &kseg, 1, false, nullptr, e, st);
+    if (rc) return rc;
+  }
+  return 0;
+}
+
+AttnShape stage_attn_shape(const Dims& D, int64_t k, int causal) {
+  AttnShape a;
+  a.b = (int)D.b;
+  a.s = (int)D.s;
+  a.H = (int)D.U;
+  a.Hkv = (int)D.Uk;
+  a.d = (int)D.d;
+  a.causal = causal;
+  a.ld_qkv = D.qkv_w;
+  a.q_col = 0;
+  a.k_col = D.U * D.d;
+  a.v_col = (D.U + D.Uk) * D.d;
+  a.ld_o = D.H * D.d;
+  a.o_col = k * D.U * D.d;
+  a.H_total = (int)D.H;
+  a.lse_head0 = (int)(k * D.U);
+  a.q_begin = 0;
+  a.q_end = (int)D.s;
+  a.o_row0 = 0;
+  return a;
+}
+
+AttnBwdShape stage_bwd_shape(const Dims& D, int64_t k) {
+  AttnBwdShape s;
+  s.f = stage_attn_shape(D, k, 1);
+  s.ld_do = D.H * D.d;
+  s.do_col = k * D.U * D.d;
+  s.ld_dqkv = D.qkv_w;
+  s.dq_col = 0;
+  s.dk_col = D.U * D.d;
+  s.dv_col = (D.U + D.Uk) * D.d;
+  return s;
+}
+
+// out[M, N] (fp32, beta) = sum_i A[:, Kseg_i] B_i  with MN-major B segments;
+// one launch when the segment boundaries are multiples of 64, else one per
+// segment with accumulation.
+int gemm_kseg(int64_t M, int64_t N, const MatView& A, const MatView* B, const int64_t* ks, int nseg,
+              const Epilogue& e0, cudaStream_t st) {
+  bool ok = true;
+  int64_t K = 0;
+  for (int i = 0; i < nseg; ++i) {
+    if (i < nseg - 1 && (ks[i] % 64)) ok = false;
+    K += ks[i];
+  }
+  if (ok) return gemm(M, N, K, A, false, B, ks, nseg, true, nullptr, e0, st);
+  int64_t koff = 0;
+  for (int i = 0; i < nseg; ++i) {
+    MatView Ai{bf(A.ptr, koff), A.rows, ks[i], A.ld};
+    Epilogue e = e0;
+    if (i > 0) e.beta = 1.f;
+    int rc = gemm(M, N, ks[i], Ai, false, &B[i], &ks[i], 1, true, nullptr, e, st);
+    if (rc) return rc;
+    koff += ks[i];
+  }
+  return 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* bpt_status_string(int s) {
+  switch (s) {
+    case BPT_OK: return "ok";
+    case BPT_EINVAL: return "invalid argument (shape, divisibility, pointer or flag)";
+    case BPT_ENOSPC: return "workspace too small";
+    case BPT_ECUDA: return "CUDA call failed";
+    case BPT_ETIMEOUT: return "a bounded device wait ran out";
+    case BPT_EUNSUPPORTED: return "unsupported configuration (head_dim must be 64, 80, 96, 112 or 128)";
+    default: return "unknown status";
+  }
+}
+
+int bpt_last_device_error(void* stream, int* detail) {
+  unsigned int e[4] = {0, 0, 0, 0};
+  int rc = read_device_error(reinterpret_cast<cudaStream_t>(stream), e);
+  if (rc) {
+    if (detail) *detail = (int)e[1];
+    return BPT_ECUDA;
+  }
+  if (e[0]) {
+    if (detail) *detail = (int)e[1];
+    return BPT_ETIMEOUT;
+  }
+  if (detail) *detail = 0;
+  return BPT_OK;
+}
+
+size_t bpt_saved_bytes(const bpt_config* cfg) {
+  Dims D;
+  if (validate(cfg, &D)) return 0;
+  return (size_t)(D.b * D.H * D.s_pad * 4);
+}
+
+size_t bpt_workspace_bytes(const bpt_config* cfg, int pass) {
+  Dims D;
+  if (validate(cfg, &D)) return 0;
+  if (pass == BPT_PASS_FWD) {
+    FwdWs w;
+    return plan_fwd(D, nullptr, &w, true);
+  }
+  if (pass == BPT_PASS_BWD) {
+    BwdWs w;
+    return plan_bwd(D, nullptr, &w);
+  }
+  if (pass == BPT_PASS_HEADCHUNK) {
+    void* q;
+    return plan_headchunk(D, nullptr, &q);
+  }
+  return 0;
+}
+
+int bpt_layer_fwd(const bpt_config* cfg, const bpt_weights* w, const void* x, void* y, void* saved,
+                  void* ws, size_t ws_bytes, void* stream) {
+  Dims D;
+  int rc = validate(cfg, &D);
+  if (rc) return rc;
+  if ((rc = check_weights(cfg, w))) return rc;
+  if (!x || !y || !ws || !aligned16(x) || !aligned16(y) || !aligned16(ws) || (saved && !aligned16(saved)))
+    return BPT_EINVAL;
+  FwdWs W;
+  const size_t need = plan_fwd(D, nullptr, &W, saved == nullptr);
+  if (ws_bytes < need) return BPT_ENOSPC;
+  plan_fwd(D, ws, &W, saved == nullptr);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  float* lse = saved ? reinterpret_cast<float*>(saved) : W.lse;
+  const bool hb = cfg->has_bias != 0;
+  const int64_t h = D.h, f = D.f, Hd = D.H * D.d;
+
+  // N1 over the whole sequence
+  if ((rc = norm_fwd(D.rows, (int)h, cfg->norm, cfg->norm_eps, x, h, w->ln1_w, w->ln1_b, W.xn, h, nullptr,
+                     nullptr, st)))
+    return rc;
+  if (D.chunked) {
+    for (int64_t k = 0; k < D.n_stages; ++k) {
+      if ((rc = stage_qkv(D, w, hb, W.xn, W.qkv, k, st))) return rc;
+      AttnShape a = stage_attn_shape(D, k, cfg->causal);
+      if ((rc = attention_fwd(a, W.qkv, W.o, lse, st))) return rc;
+    }
+  } else {
+    if ((rc = stage_qkv(D, w, hb, W.xn, W.qkv, 0, st))) return rc;
+  }
+
+  for (int64_t bi = 0; bi < D.b; ++bi) {
+    for (int64_t r0 = 0; r0 < D.s; r0 += D.cf) {
+      const int64_t nr = std::min(D.cf, D.s - r0);
+      const int64_t row = bi * D.s + r0;
+      const void* oblk;
+      if (D.chunked) {
+        oblk = bf(W.o, row * Hd);
+      } else {
+        // attention of this block's query rows, all heads
+        AttnShape a = stage_attn_shape(D, 0, cfg->causal);
+        a.b = 1;
+        a.q_begin = (int)r0;
+        a.q_end = (int)(r0 + nr);
+        a.o_row0 = r0;
+        if ((rc = attention_fwd(a, bf(W.qkv, bi * D.s * D.qkv_w), W.o, lse + bi * D.H * D.s_pad, st)))
+          return rc;
+        oblk = W.o;
+      }
+      // x1 = x + O Wo^T + bo
+      {
+        MatView A{oblk, nr, Hd, Hd};
+        MatView B{w->wo, h, Hd, Hd};
+        Epilogue e;
+        e.out = W.x1;
+        e.ldo = h;
+        e.bias = hb ? w->bo : nullptr;
+        e.res = bf(x, row * h);
+        e.ldr = h;
+        if ((rc = gemm(nr, h, Hd, A, false, &B, &Hd, 1, false, nullptr, e, st))) return rc;
+      }
+      if ((rc = norm_fwd(nr, (int)h, cfg->norm, cfg->norm_eps, W.x1, h, w->ln2_w, w->ln2_b, W.x1n, h, nullptr,
+                         nullptr, st)))
+        return rc;
+      // a = act(x1n W1^T + b1)  or  silu(x1n W1^T) * (x1n W3^T)
+      {
+        MatView A{W.x1n, nr, h, h};
+        MatView B{w->w1, f, h, h};
+        Epilogue e;
+        e.out = W.a;
+        e.ldo = f;
+        if (cfg->act == BPT_ACT_SWIGLU) {
+          MatView B2{w->w3, f, h, h};
+          e.kind = EPI_SWIGLU;
+          if ((rc = gemm(nr, f, h, A, false, &B, &h, 1, false, &B2, e, st))) return rc;
+        } else {
+          e.kind = EPI_GELU;
+          e.act = cfg->act;
+          e.bias = hb ? w->b1 : nullptr;
+          if ((rc = gemm(nr, f, h, A, false, &B, &h, 1, false, nullptr, e, st))) return rc;
+        }
+      }
+      // y = x1 + a W2^T + b2
+      {
+        MatView A{W.a, nr, f, f};
+        MatView B{w->w2, h, f, f};
+        Epilogue e;
+        e.out = bfm(y, row * h);
+        e.ldo = h;
+        e.bias = hb ? w->b2 : nullptr;
+        e.res = W.x1;
+        e.ldr = h;
+        if ((rc = gemm(nr, h, f, A, false, &B, &f, 1, false, nullptr, e, st))) return rc;
+      }
+    }
+  }
+  return BPT_OK;
+}
+
+int bpt_attn_headchunk(const bpt_config* cfg, const bpt_weights* w, const void* xn, void* o, void* lse,
+                       void* ws, size_t ws_bytes, void* stream) {
+  Dims D;
+  int rc = validate(cfg, &D);
+  if (rc) return rc;
+  if (!w || !w->wq || !w->wk || !w->wv || !xn || !o || !ws) return BPT_EINVAL;
+  if (cfg->has_bias && (!w->bq || !w->bk || !w->bv)) return BPT_EINVAL;
+  if (!aligned16(xn) || !aligned16(o) || !aligned16(ws) || (lse && !aligned16(lse))) return BPT_EINVAL;
+  void* qkv;
+  if (ws_bytes < plan_headchunk(D, nullptr, &qkv)) return BPT_ENOSPC;
+  plan_headchunk(D, ws, &qkv);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  for (int64_t k = 0; k < D.n_stages; ++k) {
+    if ((rc = stage_qkv(D, w, cfg->has_bias != 0, xn, qkv, k, st))) return rc;
+    AttnShape a = stage_attn_shape(D, k, cfg->causal);
+    if ((rc = attention_fwd(a, qkv, o, reinterpret_cast<float*>(lse), st))) return rc;
+  }
+  return BPT_OK;
+}
+
+int bpt_attention_fwd(const bpt_config* cfg, const void* qkv, void* o, void* lse, void* stream) {
+  Dims D;
+  int rc = validate(cfg, &D);
+  if (rc) return rc;
+  if (!qkv || !o || !aligned16(qkv) || !aligned16(o) || (lse && !aligned16(lse))) return BPT_EINVAL;
+  Dims F = D;
+  F.U = D.H;
+  F.Uk = D.Hkv;
+  F.qkv_w = (D.H + 2 * D.Hkv) * D.d;
+  AttnShape a = stage_attn_shape(F, 0, cfg->causal);
+  return attention_fwd(a, qkv, o, reinterpret_cast<float*>(lse), reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t bpt_attention_bwd_workspace_bytes(const bpt_config* cfg) {
+  Dims D;
+  if (validate(cfg, &D)) return 0;
+  Dims F = D;
+  F.U = D.H;
+  F.Uk = D.Hkv;
+  F.qkv_w = (D.H + 2 * D.Hkv) * D.d;
+  AttnBwdShape s = stage_bwd_shape(F, 0);
+  s.f.causal = cfg->causal;
+  return attention_bwd_ws_bytes(s);
+}
+
+int bpt_attention_bwd(const bpt_config* cfg, const void* qkv, const void* o, const void* lse, const void* dout,
+                      void* dqkv, void* ws, size_t ws_bytes, void* stream) {
+  Dims D;
+  int rc = validate(cfg, &D);
+  if (rc) return rc;
+  if (!qkv || !o || !lse || !dout || !dqkv || !ws) return BPT_EINVAL;
+  if (!aligned16(qkv) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) || !aligned16(dqkv) ||
+      !aligned16(ws))
+    return BPT_EINVAL;
+  Dims F = D;
+  F.U = D.H;
+  F.Uk = D.Hkv;
+  F.qkv_w = (D.H + 2 * D.Hkv) * D.d;
+  AttnBwdShape s = stage_bwd_shape(F, 0);
+  s.f.causal = cfg->causal;
+  if (ws_bytes < attention_bwd_ws_bytes(s)) return BPT_ENOSPC;
+  return attention_bwd(s, qkv, o, reinterpret_cast<const float*>(lse), dout, dqkv, ws,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, const void* saved, const void* dy,
+                  void* dx, const bpt_grads* g, void* ws, size_t ws_bytes, void* stream) {
+  Dims D;
+  int rc = validate(cfg, &D);
+  if (rc) return rc;
+  if ((rc = check_weights(cfg, w))) return rc;
+  if (!x || !saved || !dy || !dx || !g || !ws) return BPT_EINVAL;
+  if (!aligned16(x) || !aligned16(saved) || !aligned16(dy) || !aligned16(dx) || !aligned16(ws)) return BPT_EINVAL;
+  {
+    const void* need[] = {g->ln1_w, g->wq, g->wk, g->wv, g->wo, g->ln2_w, g->w1, g->w2};
+    for (const void* p : need)
+      if (!p || !aligned16(p)) return BPT_EINVAL;
+    if (cfg->norm == BPT_NORM_LAYER && (!g->ln1_b || !g->ln2_b)) return BPT_EINVAL;
+    if (cfg->act == BPT_ACT_SWIGLU && !g->w3) return BPT_EINVAL;
+    if (cfg->has_bias && (!g->bq || !g->bk || !g->bv || !g->bo || !g->b2 ||
+                          (cfg->act != BPT_ACT_SWIGLU && !g->b1)))
+      return BPT_EINVAL;
+  }
+  BwdWs W;
+  if (ws_bytes < plan_bwd(D, nullptr, &W)) return BPT_ENOSPC;
+  plan_bwd(D, ws, &W);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const float* lse = reinterpret_cast<const float*>(saved);
+  const bool hb = cfg->has_bias != 0;
+  const bool accum = (cfg->flags & BPT_FLAG_ACCUM_GRADS) != 0;
+  const bool swiglu = cfg->act == BPT_ACT_SWIGLU;
+  const int64_t h = D.h, f = D.f, Hd = D.H * D.d, d = D.d;
+  const bool ln = cfg->norm == BPT_NORM_LAYER;
+
+  if (!accum) {
+    if (cudaMemsetAsync(g->ln1_w, 0, h * 4, st) || cudaMemsetAsync(g->ln2_w, 0, h * 4, st)) return BPT_ECUDA;
+    if (ln && (cudaMemsetAsync(g->ln1_b, 0, h * 4, st) || cudaMemsetAsync(g->ln2_b, 0, h * 4, st)))
+      return BPT_ECUDA;
+  }
+
+  // ---- recompute N1, Q/K/V and attention (the saved LSE is not rewritten)
+  if ((rc = norm_fwd(D.rows, (int)h, cfg->norm, cfg->norm_eps, x, h, w->ln1_w, w->ln1_b, W.xn, h, nullptr,
+                     nullptr, st)))
+    return rc;
+  for (int64_t k = 0; k < D.n_stages; ++k) {
+    if ((rc = stage_qkv(D, w, hb, W.xn, W.qkv, k, st))) return rc;
+    AttnShape a = stage_attn_shape(D, k, cfg->causal);
+    if ((rc = attention_fwd(a, W.qkv, W.o, nullptr, st))) return rc;
+  }
+
+  // ---- FFN blocks: rebuild x1, N2, fc1 and form the FFN / N2 gradients
+  bool first = true;
+  for (int64_t bi = 0; bi < D.b; ++bi) {
+    for (int64_t r0 = 0; r0 < D.s; r0 += D.cf) {
+      const int64_t nr = std::min(D.cf, D.s - r0);
+      const int64_t row = bi * D.s + r0;
+      const float beta = (accum || !first) ? 1.f : 0.f;
+      {
+        MatView A{bf(W.o, row * Hd), nr, Hd, Hd};
+        MatView B{w->wo, h, Hd, Hd};
+        Epilogue e;
+        e.out = W.x1;
+        e.ldo = h;
+        e.bias = hb ? w->bo : nullptr;
+        e.res = bf(x, row * h);
+        e.ldr = h;
+        if ((rc = gemm(nr, h, Hd, A, false, &B, &Hd, 1, false, nullptr, e, st))) return rc;
+      }
+      if ((rc = norm_fwd(nr, (int)h, cfg->norm, cfg->norm_eps, W.x1, h, w->ln2_w, w->ln2_b, W.x1n, h, nullptr,
+                         nullptr, st)))
+        return rc;
+      {
+        MatView A{W.x1n, nr, h, h};
+        MatView B{w->w1, f, h, h};
+        Epilogue e;
+        e.out = W.a;
+        e.ldo = f;
+        if (swiglu) {
+          MatView B2{w->w3, f, h, h};
+          e.kind = EPI_SWIGLU;
+          e.out2 = W.g;
+          e.ldo2 = f;
+          e.out3 = W.u;
+          e.ldo3 = f;
+          if ((rc = gemm(nr, f, h, A, false, &B, &h, 1, false, &B2, e, st))) return rc;
+        } else {
+          e.kind = EPI_GELU;
+          e.act = cfg->act;
+          e.bias = hb ? w->b1 : nullptr;
+          e.out2 = W.z;
+          e.ldo2 = f;
+          if ((rc = gemm(nr, f, h, A, false, &B, &h, 1, false, nullptr, e, st))) return rc;
+        }
+      }
+      const void* dyb = bf(dy, row * h);
+      // dA = dy W2, fused with the activation gradient
+      {
+        MatView A{dyb, nr, h, h};
+        MatView B{w->w2, h, f, f};  // [K = h rows, N = f cols]
+        Epilogue e;
+        if (swiglu) {
+          e.kind = EPI_SWIGLU_BWD;
+          e.aux = W.g;
+          e.ldaux = f;
+          e.aux2 = W.u;
+          e.ldaux2 = f;
+          e.out = W.dz;
+          e.ldo = 2 * f;
+          e.out2 = bfm(W.dz, f);
+          e.ldo2 = 2 * f;
+        } else {
+          e.kind = EPI_GELU_BWD;
+          e.act = cfg->act;
+          e.aux = W.z;
+          e.ldaux = f;
+          e.out = W.dz;
+          e.ldo = f;
+        }
+        if ((rc = gemm(nr, f, h, A, false, &B, &h, 1, true, nullptr, e, st))) return rc;
+      }
+      // dW2 (+)= dy^T a ; db2 (+)= colsum(dy)
+      {
+        MatView A{dyb, nr, h, h};     // MN-major: [K = rows, M = h]
+        MatView B{W.a, nr, f, f};     // MN-major: [K = rows, N = f]
+        Epilogue e;
+        e.kind = EPI_F32;
+        e.out = g->w2;
+        e.ldo = f;
+        e.beta = beta;
+        if ((rc = gemm(h, f, nr, A, true, &B, &nr, 1, true, nullptr, e, st))) return rc;
+        if (hb && (rc = colsum(nr, h, dyb, h, reinterpret_cast<float*>(g->b2), beta != 0.f, st))) return rc;
+      }
+      // dW1 (+)= dz^T x1n (SwiGLU: dWg from dg, dWu from du) ; db1
+      {
+        const int64_t ldz = swiglu ? 2 * f : f;
+        MatView B{W.x1n, nr, h, h};
+        Epilogue e;
+        e.kind = EPI_F32;
+        e.ldo = h;
+        e.beta = beta;
+        MatView A{W.dz, nr, f, ldz};
+        e.out = g->w1;
+        if ((rc = gemm(f, h, nr, A, true, &B, &nr, 1, true, nullptr, e, st))) return rc;
+        if (swiglu) {
+          MatView A2{bf(W.dz, f), nr, f, ldz};
+          e.out = g->w3;
+          if ((rc = gemm(f, h, nr, A2, true, &B, &nr, 1, true, nullptr, e, st))) return rc;
+        } else if (hb) {
+          if ((rc = colsum(nr, f, W.dz, f, reinterpret_cast<float*>(g->b1), beta != 0.f, st))) return rc;
+        }
+      }
+      // dx1n = dz W1  (SwiGLU: dg Wg + du Wu)
+      {
+        Epilogue e;
+        e.kind = EPI_BF16;
+        e.out = W.dx1n;
+        e.ldo = h;
+        if (swiglu) {
+          MatView A{W.dz, nr, 2 * f, 2 * f};
+          MatView Bs[2] = {{w->w1, f, h, h}, {w->w3, f, h, h}};
+          int64_t ks[2] = {f, f};
+          if (f % 64 == 0) {
+            if ((rc = gemm(nr, h, 2 * f, A, false, Bs, ks, 2, true, nullptr, e, st))) return rc;
+          } else {
+            return BPT_EUNSUPPORTED;
+          }
+        } else {
+          MatView A{W.dz, nr, f, f};
+          MatView B{w->w1, f, h, h};
+          if ((rc = gemm(nr, h, f, A, false, &B, &f, 1, true, nullptr, e, st))) return rc;
+        }
+      }
+      // dx1 = dy + N2^T(dx1n)
+      if ((rc = norm_bwd(nr, (int)h, cfg->norm, cfg->norm_eps, W.dx1n, 0, h, W.x1, h, w->ln2_w, dyb, h,
+                         bfm(W.dx1, row * h), h, reinterpret_cast<float*>(g->ln2_w),
+                         ln ? reinterpret_cast<float*>(g->ln2_b) : nullptr, st)))
+        return rc;
+      first = false;
+    }
+  }
+
+  // ---- output projection: dO = dx1 Wo ; dWo (+)= dx1^T O ; dbo
+  {
+    MatView A{W.dx1, D.rows, h, h};
+    MatView B{w->wo, h, Hd, Hd};  // [K = h rows, N = Hd cols]
+    Epilogue e;
+    e.out = W.dO;
+    e.ldo = Hd;
+    if ((rc = gemm(D.rows, Hd, h, A, false, &B, &h, 1, true, nullptr, e, st))) return rc;
+    MatView A2{W.dx1, D.rows, h, h};
+    MatView B2{W.o, D.rows, Hd, Hd};
+    Epilogue e2;
+    e2.kind = EPI_F32;
+    e2.out = g->wo;
+    e2.ldo = Hd;
+    e2.beta = accum ? 1.f : 0.f;
+    const int64_t K = D.rows;
+    if ((rc = gemm(h, Hd, K, A2, true, &B2, &K, 1, true, nullptr, e2, st))) return rc;
+    if (hb && (rc = colsum(D.rows, h, W.dx1, h, reinterpret_cast<float*>(g->bo), accum, st))) return rc;
+  }
+
+  // ---- attention and Q/K/V gradients, stage by stage
+  for (int64_t k = 0; k < D.n_stages; ++k) {
+    if (D.chunked && (rc = stage_qkv(D, w, hb, W.xn, W.qkv, k, st))) return rc;
+    AttnBwdShape sb = stage_bwd_shape(D, k);
+    sb.f.causal = cfg->causal;
+    if ((rc = attention_bwd(sb, W.qkv, W.o, lse, W.dO, W.dqkv, W.attn, st))) return rc;
+    const int64_t q0 = k * D.U * d, kv0 = k * D.Uk * d;
+    const int64_t nq = D.U * d, nkv = D.Uk * d;
+    // dxn (+)= dQ Wq_s + dK Wk_s + dV Wv_s
+    {
+      MatView A{W.dqkv, D.rows, D.qkv_w, D.qkv_w};
+      MatView Bs[3] = {{bf(w->wq, q0 * h), nq, h, h}, {bf(w->wk, kv0 * h), nkv, h, h}, {bf(w->wv, kv0 * h), nkv, h, h}};
+      int64_t ks[3] = {nq, nkv, nkv};
+      Epilogue e;
+      e.kind = EPI_F32;
+      e.out = W.dxn;
+      e.ldo = h;
+      e.beta = k > 0 ? 1.f : 0.f;
+      if ((rc = gemm_kseg(D.rows, h, A, Bs, ks, 3, e, st))) return rc;
+    }
+    // dWq_s, dWk_s, dWv_s (+)= dQKV_s^T xn ; biases
+    {
+      struct Piece {
+        void* G;
+        void* Gb;
+        int64_t row0, n, col;
+      } pieces[3] = {{g->wq, g->bq, q0, nq, 0}, {g->wk, g->bk, kv0, nkv, nq}, {g->wv, g->bv, kv0, nkv, nq + nkv}};
+      MatView B{W.xn, D.rows, h, h};
+      const int64_t K = D.rows;
+      for (auto& pc : pieces) {
+        MatView A{bf(W.dqkv, pc.col), D.rows, pc.n, D.qkv_w};
+        Epilogue e;
+        e.kind = EPI_F32;
+        e.out = f32(pc.G, pc.row0 * h);
+        e.ldo = h;
+        e.beta = accum ? 1.f : 0.f;
+        if ((rc = gemm(pc.n, h, K, A, true, &B, &K, 1, true, nullptr, e, st))) return rc;
+        if (hb && (rc = colsum(D.rows, pc.n, bf(W.dqkv, pc.col), D.qkv_w, f32(pc.Gb, pc.row0), accum, st)))
+          return rc;
+      }
+    }
+  }
+
+  // ---- dx = dx1 + N1^T(dxn)
+  if ((rc = norm_bwd(D.rows, (int)h, cfg->norm, cfg->norm_eps, W.dxn, 1, h, x, h, w->ln1_w, W.dx1, h, dx, h,
+                     reinterpret_cast<float*>(g->ln1_w), ln ? reinterpret_cast<float*>(g->ln1_b) : nullptr, st)))
+    return rc;
+  return BPT_OK;
+}
+
+}  // extern "C"

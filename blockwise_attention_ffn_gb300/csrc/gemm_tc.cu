@@ -1,0 +1,464 @@
+// gemm_tc.cu -- tcgen05 GEMM with fused epilogues for the layer's dense
+// contractions: the Q/K/V and output projections, the FFN's fc1 (GeLU or the
+// SwiGLU gate/up pair) and fc2, and every backward product (activation
+// gradients and fp32 weight gradients).
+//
+// One CTA computes one 128 x BN tile of C.  Warp roles:
+//   warp 0      TMA producer: K-tiles of A and B into a 4-stage smem ring
+//   warp 1      TMEM owner and single-thread MMA issuer (M=128, N=BN, K=16)
+//   warps 2..5  epilogue: TMEM -> registers (one row per thread) -> fused
+//               bias / residual / activation -> global
+// Operands are staged with 128-byte swizzle; K-major tiles are [rows x 64]
+// boxes, MN-major tiles are [64 K-rows x 64] boxes side by side.
+#include <math.h>
+#include <string.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace bpt {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int NUM_THREADS = 192;
+
+struct GemmParams {
+  CUtensorMap mapA;
+  CUtensorMap mapB[3];
+  int M, N, K;
+  int nkt;          // number of BK tiles of K
+  int seg_kt[3];    // first k-tile of segments 1 and 2 (large if absent)
+  int epi, act;
+  void* out;
+  long long ldo;
+  void* out2;
+  long long ldo2;
+  void* out3;
+  long long ldo3;
+  const __nv_bfloat16* bias;
+  const __nv_bfloat16* res;
+  long long ldr;
+  const __nv_bfloat16* aux;
+  long long ldaux;
+  const __nv_bfloat16* aux2;
+  long long ldaux2;
+  float beta;
+  unsigned int* err;
+};
+
+__device__ __forceinline__ float gelu_f(float z, int act) {
+  if (act == 0) return 0.5f * z * (1.f + erff(z * 0.70710678118654752f));
+  const float c = 0.7978845608028654f;
+  return 0.5f * z * (1.f + tanhf(c * (z + 0.044715f * z * z * z)));
+}
+__device__ __forceinline__ float gelu_grad_f(float z, int act) {
+  if (act == 0) {
+    const float phi = expf(-0.5f * z * z) * 0.3989422804014327f;
+    return 0.5f * (1.f + erff(z * 0.70710678118654752f)) + z * phi;
+  }
+  const float c = 0.7978845608028654f;
+  const float t = tanhf(c * (z + 0.044715f * z * z * z));
+  return 0.5f * (1.f + t) + 0.5f * z * (1.f - t * t) * c * (1.f + 3.f * 0.044715f * z * z);
+}
+__device__ __forceinline__ float sigmoid_f(float z) { return 1.f / (1.f + expf(-z)); }
+
+__device__ __forceinline__ void load8_bf16(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x);
+  v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
+  v[4] = bf16_lo(u.z); v[5] = bf16_hi(u.z);
+  v[6] = bf16_lo(u.w); v[7] = bf16_hi(u.w);
+}
+__device__ __forceinline__ void store8_bf16(__nv_bfloat16* p, const float (&v)[8]) {
+  uint4 u;
+  u.x = pack_bf16(v[0], v[1]);
+  u.y = pack_bf16(v[2], v[3]);
+  u.z = pack_bf16(v[4], v[5]);
+  u.w = pack_bf16(v[6], v[7]);
+  *reinterpret_cast<uint4*>(p) = u;
+}
+
+// Applies the epilogue to 8 consecutive columns n..n+7 of row m (all in range)
+// given the accumulators a (and a second accumulator b for the dual kinds).
+__device__ __forceinline__ void epi8(const GemmParams& p, int m, int n, const float (&a)[8],
+                                     const float (&b)[8]) {
+  float v[8];
+  switch (p.epi) {
+    case EPI_BF16: {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = a[j];
+      if (p.bias) {
+        float t[8];
+        load8_bf16(p.bias + n, t);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] += t[j];
+      }
+      if (p.res) {
+        float t[8];
+        load8_bf16(p.res + (long long)m * p.ldr + n, t);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] += t[j];
+      }
+      store8_bf16(reinterpret_cast<__nv_bfloat16*>(p.out) + (long long)m * p.ldo + n, v);
+      break;
+    }
+    case EPI_GELU: {
+      float z[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) z[j] = a[j];
+      if (p.bias) {
+        float t[8];
+        load8_bf16(p.bias + n, t);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) z[j] += t[j];
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = gelu_f(z[j], p.act);
+      store8_bf16(reinterpret_cast<__nv_bfloat16*>(p.out) + (long long)m * p.ldo + n, v);
+      if (p.out2) store8_bf16(reinterpret_cast<__nv_bfloat16*>(p.out2) + (long long)m * p.ldo2 + n, z);
+      break;
+    }
+    case EPI_SWIGLU: {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = a[j] * sigmoid_f(a[j]) * b[j];
+      store8_bf16(reinterpret_cast<__nv_bfloat16*>(p.out) + (long long)m * p.ldo + n, v);
+      if (p.out2) store8_bf16(reinterpret_cast<__nv_bfloat16*>(p.out2) + (long long)m * p.ldo2 + n, a);
+      if (p.out3) store8_bf16(reinterpret_cast<__nv_bfloat16*>(p.out3) + (long long)m * p.ldo3 + n, b);
+      break;
+    }
+    case EPI_GELU_BWD: {
+      float z[8];
+      load8_bf16(p.aux + (long long)m * p.ldaux + n, z);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = a[j] * gelu_grad_f(z[j], p.act);
+      store8_bf16(reinterpret_cast<__nv_bfloat16*>(p.out) + (long long)m * p.ldo + n, v);
+      break;
+    }
+    case EPI_SWIGLU_BWD: {
+      float g[8], u[8], w2[8];
+      load8_bf16(p.aux + (long long)m * p.ldaux + n, g);
+      load8_bf16(p.aux2 + (long long)m * p.ldaux2 + n, u);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float sg = sigmoid_f(g[j]);
+        v[j] = a[j] * u[j] * sg * (1.f + g[j] * (1.f - sg));
+        w2[j] = a[j] * g[j] * sg;
+      }
+      store8_bf16(reinterpret_cast<__nv_bfloat16*>(p.out) + (long long)m * p.ldo + n, v);
+      store8_bf16(reinterpret_cast<__nv_bfloat16*>(p.out2) + (long long)m * p.ldo2 + n, w2);
+      break;
+    }
+    default: {  // EPI_F32
+      float* o = reinterpret_cast<float*>(p.out) + (long long)m * p.ldo + n;
+      float4 x0 = make_float4(a[0], a[1], a[2], a[3]);
+      float4 x1 = make_float4(a[4], a[5], a[6], a[7]);
+      if (p.beta != 0.f) {
+        const float4 o0 = reinterpret_cast<const float4*>(o)[0];
+        const float4 o1 = reinterpret_cast<const float4*>(o)[1];
+        x0.x += p.beta * o0.x; x0.y += p.beta * o0.y; x0.z += p.beta * o0.z; x0.w += p.beta * o0.w;
+        x1.x += p.beta * o1.x; x1.y += p.beta * o1.y; x1.z += p.beta * o1.z; x1.w += p.beta * o1.w;
+      }
+      reinterpret_cast<float4*>(o)[0] = x0;
+      reinterpret_cast<float4*>(o)[1] = x1;
+      break;
+    }
+  }
+}
+
+// Scalar version for the ragged N tail.
+__device__ __forceinline__ void epi1(const GemmParams& p, int m, int n, float a, float b) {
+  switch (p.epi) {
+    case EPI_BF16: {
+      float v = a;
+      if (p.bias) v += __bfloat162float(p.bias[n]);
+      if (p.res) v += __bfloat162float(p.res[(long long)m * p.ldr + n]);
+      reinterpret_cast<__nv_bfloat16*>(p.out)[(long long)m * p.ldo + n] = __float2bfloat16(v);
+      break;
+    }
+    case EPI_GELU: {
+      float z = a + (p.bias ? __bfloat162float(p.bias[n]) : 0.f);
+      reinterpret_cast<__nv_bfloat16*>(p.out)[(long long)m * p.ldo + n] =
+          __float2bfloat16(gelu_f(z, p.act));
+      if (p.out2)
+        reinterpret_cast<__nv_bfloat16*>(p.out2)[(long long)m * p.ldo2 + n] = __float2bfloat16(z);
+      break;
+    }
+    case EPI_SWIGLU: {
+      reinterpret_cast<__nv_bfloat16*>(p.out)[(long long)m * p.ldo + n] =
+          __float2bfloat16(a * sigmoid_f(a) * b);
+      if (p.out2)
+        reinterpret_cast<__nv_bfloat16*>(p.out2)[(long long)m * p.ldo2 + n] = __float2bfloat16(a);
+      if (p.out3)
+        reinterpret_cast<__nv_bfloat16*>(p.out3)[(long long)m * p.ldo3 + n] = __float2bfloat16(b);
+      break;
+    }
+    case EPI_GELU_BWD: {
+      const float z = __bfloat162float(p.aux[(long long)m * p.ldaux + n]);
+      reinterpret_cast<__nv_bfloat16*>(p.out)[(long long)m * p.ldo + n] =
+          __float2bfloat16(a * gelu_grad_f(z, p.act));
+      break;
+    }
+    case EPI_SWIGLU_BWD: {
+      const float g = __bfloat162float(p.aux[(long long)m * p.ldaux + n]);
+      const float u = __bfloat162float(p.aux2[(long long)m * p.ldaux2 + n]);
+      const float sg = sigmoid_f(g);
+      reinterpret_cast<__nv_bfloat16*>(p.out)[(long long)m * p.ldo + n] =
+          __float2bfloat16(a * u * sg * (1.f + g * (1.f - sg)));
+      reinterpret_cast<__nv_bfloat16*>(p.out2)[(long long)m * p.ldo2 + n] =
+          __float2bfloat16(a * g * sg);
+      break;
+    }
+    default: {
+      float* o = reinterpret_cast<float*>(p.out) + (long long)m * p.ldo + n;
+      *o = a + (p.beta != 0.f ? p.beta * *o : 0.f);
+      break;
+    }
+  }
+}
+
+// BN: tile width (columns of C).  DUAL: BN columns of g and BN of u.
+template <int BN, bool A_MN, bool B_MN, bool DUAL>
+__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+  constexpr int B_BYTES = (DUAL ? 2 : 1) * BN * BK * 2;
+  constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr uint32_t TMEM_COLS = (DUAL ? 2 : 1) * BN <= 256 ? 256 : 512;
+  constexpr uint32_t IDESC = idesc_bf16(BM, BN, A_MN, B_MN);
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* acc_full = empty + STAGES;
+  uint64_t* drain = acc_full + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+  const int n0 = blockIdx.x * BN;
+  const int m0 = blockIdx.y * BM;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&p.mapA);
+    tma_prefetch(&p.mapB[0]);
+    if (DUAL || p.seg_kt[0] < p.nkt) tma_prefetch(&p.mapB[1]);
+    if (p.seg_kt[1] < p.nkt) tma_prefetch(&p.mapB[2]);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ producer
+      int issued = 0;
+      for (int kt = 0; kt < p.nkt; ++kt) {
+        const int s = kt % STAGES;
+        if (kt >= STAGES && !bounded_wait(&empty[s], ((kt / STAGES) & 1) ^ 1, abort_flag, 101, p.err)) break;
+        uint8_t* sa = smem + s * STAGE_BYTES;
+        uint8_t* sb = sa + A_BYTES;
+        mbar_expect_tx(&full[s], STAGE_BYTES);
+        if (!A_MN) {
+          tma_load_2d(sa, &p.mapA, &full[s], kt * BK, m0);
+        } else {
+          tma_load_2d(sa, &p.mapA, &full[s], m0, kt * BK);
+          tma_load_2d(sa + 8192, &p.mapA, &full[s], m0 + 64, kt * BK);
+        }
+        if (DUAL) {
+          tma_load_2d(sb, &p.mapB[0], &full[s], kt * BK, n0);
+          tma_load_2d(sb + BN * BK * 2, &p.mapB[1], &full[s], kt * BK, n0);
+        } else {
+          const int seg = (kt >= p.seg_kt[1]) ? 2 : (kt >= p.seg_kt[0]) ? 1 : 0;
+          const int kl = (kt - (seg == 0 ? 0 : p.seg_kt[seg - 1])) * BK;
+          if (!B_MN) {
+            tma_load_2d(sb, &p.mapB[seg], &full[s], kl, n0);
+          } else {
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c) tma_load_2d(sb + c * 8192, &p.mapB[seg], &full[s], n0 + c * 64, kl);
+          }
+        }
+        issued = kt + 1;
+      }
+      if (*abort_flag) {
+        // let every load this thread issued land before the CTA goes away
+        for (int kt = (issued > STAGES ? issued - STAGES : 0); kt < issued; ++kt)
+          bounded_wait(&full[kt % STAGES], (kt / STAGES) & 1, abort_flag, 102, p.err) ||
+              mbar_try_wait(&full[kt % STAGES], (kt / STAGES) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      const uint32_t smem_base = smem_u32(smem);
+      bool ok = true;
+      for (int kt = 0; kt < p.nkt; ++kt) {
+        const int s = kt % STAGES;
+        if (!bounded_wait(&full[s], (kt / STAGES) & 1, abort_flag, 103, p.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sa = smem_base + s * STAGE_BYTES;
+        const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint64_t ad = A_MN ? sdesc(sa + kk * 2048, 8192, 1024, 2) : sdesc(sa + kk * 32, 16, 1024, 2);
+          const uint64_t bd = B_MN ? sdesc(sb + kk * 2048, 8192, 1024, 2) : sdesc(sb + kk * 32, 16, 1024, 2);
+          umma_bf16(tmem, ad, bd, IDESC, (kt | kk) != 0);
+          if (DUAL) {
+            const uint64_t bd2 = sdesc(sb + BN * BK * 2 + kk * 32, 16, 1024, 2);
+            umma_bf16(tmem + BN, ad, bd2, IDESC, (kt | kk) != 0);
+          }
+        }
+        umma_commit(&empty[s]);
+      }
+      if (ok) {
+        umma_commit(acc_full);
+      } else {
+        umma_commit(drain);  // wait until nothing issued is still in flight
+        bounded_wait(drain, 0, abort_flag, 104, p.err) || mbar_try_wait(drain, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------ epilogue (warps 2..5)
+    const bool ok = bounded_wait(acc_full, 0, abort_flag, 105, p.err);
+    tc_fence_after();
+    if (ok) {
+      const int q = warp & 3;
+      const int row = q * 32 + lane;
+      const int m = m0 + row;
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(tbase + c * 32, ra);
+        if (DUAL) tmem_ld32(tbase + BN + c * 32, rb);
+        if (m < p.M) {
+          const int nb = n0 + c * 32;
+          if (nb + 32 <= p.N) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              float a8[8], b8[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                a8[j] = __uint_as_float(ra[g * 8 + j]);
+                b8[j] = DUAL ? __uint_as_float(rb[g * 8 + j]) : 0.f;
+              }
+              epi8(p, m, nb + g * 8, a8, b8);
+            }
+          } else {
+            for (int j = 0; j < 32 && nb + j < p.N; ++j)
+              epi1(p, m, nb + j, __uint_as_float(ra[j]), DUAL ? __uint_as_float(rb[j]) : 0.f);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+template <int BN, bool A_MN, bool B_MN, bool DUAL>
+int launch(const GemmParams& p, cudaStream_t st) {
+  constexpr int B_BYTES = (DUAL ? 2 : 1) * BN * BK * 2;
+  constexpr int SMEM = STAGES * (A_BYTES + B_BYTES) + 1024 + 256;
+  auto kern = gemm_kernel<BN, A_MN, B_MN, DUAL>;
+  static bool attr_set = false;  // per instantiation
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
+      return 3;
+    attr_set = true;
+  }
+  dim3 grid((p.N + BN - 1) / BN, (p.M + BM - 1) / BM);
+  kern<<<grid, NUM_THREADS, SMEM, st>>>(p);
+  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
+}  // namespace
+
+int gemm(int64_t M, int64_t N, int64_t K, const MatView& A, bool a_mn, const MatView* B,
+         const int64_t* b_seg_k, int nseg, bool b_mn, const MatView* B2, const Epilogue& e,
+         cudaStream_t stream) {
+  if (M <= 0 || N <= 0) return 0;
+  if (K <= 0 || nseg < 1 || nseg > 3) return 1;
+  const bool dual = (B2 != nullptr);
+  if (dual && (b_mn || nseg != 1 || a_mn)) return 1;
+  GemmParams p;
+  memset(&p, 0, sizeof(p));
+  p.M = (int)M;
+  p.N = (int)N;
+  p.K = (int)K;
+  p.nkt = (int)((K + BK - 1) / BK);
+  p.seg_kt[0] = p.seg_kt[1] = p.seg_kt[2] = 1 << 30;
+  {
+    int64_t acc = 0;
+    for (int i = 0; i < nseg; ++i) {
+      if (i < nseg - 1 && (b_seg_k[i] % BK) != 0) return 1;
+      acc += b_seg_k[i];
+      if (i < nseg - 1) p.seg_kt[i] = (int)(acc / BK);
+    }
+    if (acc != K) return 1;
+  }
+  const int BN = dual ? 128 : 256;
+  // A
+  if (!a_mn) {
+    if (make_map_2d(&p.mapA, A.ptr, A.rows, A.cols, A.ld, BK, BM, 128)) return 1;
+  } else {
+    if (make_map_2d(&p.mapA, A.ptr, A.rows, A.cols, A.ld, 64, BK, 128)) return 1;
+  }
+  for (int i = 0; i < nseg; ++i) {
+    const MatView& b = B[i];
+    if (!b_mn) {
+      if (make_map_2d(&p.mapB[i], b.ptr, b.rows, b.cols, b.ld, BK, BN, 128)) return 1;
+    } else {
+      if (make_map_2d(&p.mapB[i], b.ptr, b.rows, b.cols, b.ld, 64, BK, 128)) return 1;
+    }
+  }
+  if (dual) {
+    if (make_map_2d(&p.mapB[1], B2->ptr, B2->rows, B2->cols, B2->ld, BK, BN, 128)) return 1;
+  }
+  p.epi = e.kind;
+  p.act = e.act;
+  p.out = e.out;
+  p.ldo = e.ldo;
+  p.out2 = e.out2;
+  p.ldo2 = e.ldo2;
+  p.out3 = e.out3;
+  p.ldo3 = e.ldo3;
+  p.bias = reinterpret_cast<const __nv_bfloat16*>(e.bias);
+  p.res = reinterpret_cast<const __nv_bfloat16*>(e.res);
+  p.ldr = e.ldr;
+  p.aux = reinterpret_cast<const __nv_bfloat16*>(e.aux);
+  p.ldaux = e.ldaux;
+  p.aux2 = reinterpret_cast<const __nv_bfloat16*>(e.aux2);
+  p.ldaux2 = e.ldaux2;
+  p.beta = e.beta;
+  p.err = device_error_word();
+  if (!p.err) return 3;
+  if (dual) return launch<128, false, false, true>(p, stream);
+  if (!a_mn && !b_mn) return launch<256, false, false, false>(p, stream);
+  if (!a_mn && b_mn) return launch<256, false, true, false>(p, stream);
+  if (a_mn && b_mn) return launch<256, true, true, false>(p, stream);
+  return launch<256, true, false, false>(p, stream);
+}
+
+}  // namespace bpt

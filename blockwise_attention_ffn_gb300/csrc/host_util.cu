@@ -1,0 +1,101 @@
+// host_util.cu -- tensor-map encoding (through the driver entry point, so the
+// library needs no link-time libcuda) and the device error word.
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace bpt {
+
+__device__ unsigned int g_err[4];
+
+unsigned int* device_error_word() {
+  static unsigned int* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_err) != cudaSuccess) return nullptr;
+    addr[dev] = reinterpret_cast<unsigned int*>(p);
+  }
+  return addr[dev];
+}
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+CUtensorMapSwizzle swz(int bytes) {
+  switch (bytes) {
+    case 32: return CU_TENSOR_MAP_SWIZZLE_32B;
+    case 64: return CU_TENSOR_MAP_SWIZZLE_64B;
+    case 128: return CU_TENSOR_MAP_SWIZZLE_128B;
+    default: return CU_TENSOR_MAP_SWIZZLE_NONE;
+  }
+}
+
+}  // namespace
+
+int make_map_2d(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld,
+                uint32_t box_cols, uint32_t box_rows, int swizzle_bytes, int elem_bytes) {
+  auto fn = encode_fn();
+  if (!fn || !ptr) return 1;
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) || ((ld * elem_bytes) & 15)) return 1;
+  if (box_rows > 256 || box_cols > 256) return 1;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * (uint64_t)elem_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                  2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swz(swizzle_bytes), CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : 1;
+}
+
+// 3-D map over a packed [b, s, ld] bf16 buffer: x = column, y = row in the
+// sequence, z = sequence.  Rows past s read as zeros within each sequence.
+// box = {chunk width, 128, 1}: 64 columns with 128-byte swizzle when d is a
+// multiple of 64, else 16 columns with 32-byte swizzle.
+int make_attn_map(CUtensorMap* map, const void* qkv, int b, int s, int64_t ld, int d) {
+  auto fn = encode_fn();
+  if (!fn || !qkv) return 1;
+  if ((reinterpret_cast<uintptr_t>(qkv) & 15) || ((ld * 2) & 15)) return 1;
+  const int cw = (d % 64 == 0) ? 64 : 16;
+  cuuint64_t dims[3] = {(cuuint64_t)ld, (cuuint64_t)s, (cuuint64_t)b};
+  cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)ld * 2 * (cuuint64_t)s};
+  cuuint32_t box[3] = {(cuuint32_t)cw, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(qkv), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, cw == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_32B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : 1;
+}
+
+// Reads and clears the error word (synchronising the stream first).
+int read_device_error(cudaStream_t st, unsigned int out[4]) {
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) {
+    out[0] = 3;
+    out[1] = (unsigned)e;
+    return 3;
+  }
+  unsigned int zero[4] = {0, 0, 0, 0};
+  if (cudaMemcpyFromSymbol(out, g_err, sizeof(unsigned int) * 4) != cudaSuccess) return 3;
+  if (cudaMemcpyToSymbol(g_err, zero, sizeof(zero)) != cudaSuccess) return 3;
+  return 0;
+}
+
+}  // namespace bpt

@@ -1,0 +1,118 @@
+// internal.h -- host-side interfaces between the C ABI (bpt_api.cu) and the
+// kernel launchers.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace bpt {
+
+// Device address of this device's error word (4 x u32), or NULL.
+unsigned int* device_error_word();
+int read_device_error(cudaStream_t st, unsigned int out[4]);
+
+// ---------------------------------------------------------------- TMA maps
+// 2-D bf16 (or fp32) tensor map over a row-major matrix view [rows, cols]
+// with a leading dimension of `ld` elements.  box = {box_cols, box_rows};
+// swizzle_bytes in {0, 32, 64, 128}.  Returns 0 on success.
+int make_map_2d(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld,
+                uint32_t box_cols, uint32_t box_rows, int swizzle_bytes, int elem_bytes = 2);
+
+// ---------------------------------------------------------------- GEMM
+// C[M, N] = A[M, K] * B[N, K]^T with bf16 operands and fp32 accumulation in
+// TMEM, followed by a fused epilogue.
+//   A: K-major storage [M rows, K cols] (a_mn = false) or MN-major storage
+//      [K rows, M cols] (a_mn = true).
+//   B: up to three segments that are concatenated along K (b_seg_k[i] rows of
+//      K each), each K-major [N rows, K_i cols] or MN-major [K_i rows, N cols].
+//      Every segment but the last must hold a multiple of 64 K.
+//   dual: a second B (b2, same major/shape) whose product goes to a second
+//      accumulator; used by the SwiGLU gate/up pair.
+struct MatView {
+  const void* ptr;
+  int64_t rows, cols, ld;  // elements
+};
+
+enum EpiKind {
+  EPI_BF16 = 0,        // out = acc (+ bias[n]) (+ res[m, n])            -> bf16
+  EPI_GELU = 1,        // z = acc + bias; out = gelu(z); out2 = z (opt)  -> bf16
+  EPI_SWIGLU = 2,      // dual: out = silu(g) * u; out2 = g, out3 = u (opt) -> bf16
+  EPI_GELU_BWD = 3,    // out = acc * gelu'(aux[m, n])                   -> bf16
+  EPI_SWIGLU_BWD = 4,  // acc = dA; g = aux, u = aux2: out = dA*u*silu'(g), out2 = dA*silu(g)
+  EPI_F32 = 5,         // out = acc + beta * out                          -> fp32
+};
+
+struct Epilogue {
+  int kind = EPI_BF16;
+  int act = 0;  // gelu variant: 0 erf, 1 tanh
+  void* out = nullptr;
+  int64_t ldo = 0;
+  void* out2 = nullptr;
+  int64_t ldo2 = 0;
+  void* out3 = nullptr;
+  int64_t ldo3 = 0;
+  const void* bias = nullptr;  // bf16 [N]
+  const void* res = nullptr;   // bf16 [M, N] with ldr
+  int64_t ldr = 0;
+  const void* aux = nullptr;
+  int64_t ldaux = 0;
+  const void* aux2 = nullptr;
+  int64_t ldaux2 = 0;
+  float beta = 0.f;
+};
+
+// Returns 0 or a BPT_* status.
+int gemm(int64_t M, int64_t N, int64_t K, const MatView& A, bool a_mn, const MatView* B,
+         const int64_t* b_seg_k, int nseg, bool b_mn, const MatView* B2, const Epilogue& epi,
+         cudaStream_t stream);
+
+// ---------------------------------------------------------------- attention
+struct AttnShape {
+  int b, s, H, Hkv, d;
+  int causal;
+  // packed projection buffer [b*s, ld_qkv]: Q heads at column q_col + n*d,
+  // K heads at k_col + g*d, V heads at v_col + g*d (heads local to the call)
+  int64_t ld_qkv, q_col, k_col, v_col;
+  // output O [b*s, ld_o], head n at column o_col + n*d; LSE [b, H_total, s]
+  // at head offset lse_head0 (nullable)
+  int64_t ld_o, o_col;
+  int H_total, lse_head0;
+  // query rows processed: [q_begin, q_end) of every sequence; O row of query
+  // q of sequence bi is bi*s + q - o_row0 (o_row0 lets a caller pass a
+  // buffer that holds only the processed block)
+  int q_begin, q_end;
+  int64_t o_row0;
+};
+int attention_fwd(const AttnShape& sh, const void* qkv, void* o, float* lse, cudaStream_t st);
+
+struct AttnBwdShape {
+  AttnShape f;            // forward geometry (q_begin/q_end ignored: all rows)
+  int64_t ld_do, do_col;  // dO [b*s, ld_do], head n at do_col + n*d
+  int64_t ld_dqkv, dq_col, dk_col, dv_col;  // outputs, bf16
+};
+// ws: fp32 dQ accumulator [b*s, H*d] followed by D [b, H, s_pad] fp32
+// (s_pad = s rounded up to 128); lse is [b, H_total, s_pad].
+size_t attention_bwd_ws_bytes(const AttnBwdShape& sh);
+int attention_bwd(const AttnBwdShape& sh, const void* qkv, const void* o, const float* lse,
+                  const void* dout, void* dqkv, void* ws, cudaStream_t st);
+
+// ---------------------------------------------------------------- norms & misc
+// y = norm(x) * w (+ b), rows of width h; mean/rstd (fp32 [rows]) optional.
+int norm_fwd(int64_t rows, int h, int kind, float eps, const void* x, int64_t ldx,
+             const void* w, const void* b, void* y, int64_t ldy, float* rstd, float* mean,
+             cudaStream_t st);
+// dx = res + d/dx norm (given dy, x, w); dw/db partial sums accumulated into
+// the fp32 vectors with atomics (they must be zeroed or hold the running sum).
+// dy may be bf16 (dy_f32 = 0) or fp32 (dy_f32 = 1).
+int norm_bwd(int64_t rows, int h, int kind, float eps, const void* dy, int dy_f32, int64_t lddy,
+             const void* x, int64_t ldx, const void* w, const void* res, int64_t ldres,
+             void* dx, int64_t lddx, float* dw, float* db, cudaStream_t st);
+// out[n] (+)= sum over rows of in[row, n]  (bf16 in, fp32 out)
+int colsum(int64_t rows, int64_t n, const void* in, int64_t ld, float* out, int accumulate,
+           cudaStream_t st);
+// dst bf16 [rows, n] (ld_dst) = src fp32 [rows, n] (ld_src) * scale
+int f32_to_bf16(int64_t rows, int64_t n, const float* src, int64_t ld_src, void* dst,
+                int64_t ld_dst, float scale, cudaStream_t st);
+
+}  // namespace bpt

@@ -1,0 +1,298 @@
+// norm_misc.cu -- the memory-bound pieces of the layer: LayerNorm / RMSNorm
+// forward and backward, column sums (bias gradients), the per-row dO . O sums
+// of the attention backward, and an fp32 -> bf16 scaled copy.
+//
+// Norms follow "Training memory: model states, activations and checkpointing",
+// section 3 (pre-LN layer, LayerNorm with scale and shift; Llama-style layer
+// with RMSNorm, scale only): y = (x - mean) * rstd * w + b with the biased
+// variance, or y = x * rstd * w with rstd = 1/sqrt(mean(x^2) + eps).  One warp
+// per row, 16-byte vector accesses; rows are re-read from L1/L2 between passes.
+#include <math.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace bpt {
+
+namespace {
+
+__device__ __forceinline__ void ld8(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x);
+  v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
+  v[4] = bf16_lo(u.z); v[5] = bf16_hi(u.z);
+  v[6] = bf16_lo(u.w); v[7] = bf16_hi(u.w);
+}
+__device__ __forceinline__ void ld8f(const float* p, float (&v)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0];
+  const float4 b = reinterpret_cast<const float4*>(p)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void st8(__nv_bfloat16* p, const float (&v)[8]) {
+  uint4 u;
+  u.x = pack_bf16(v[0], v[1]);
+  u.y = pack_bf16(v[2], v[3]);
+  u.z = pack_bf16(v[4], v[5]);
+  u.w = pack_bf16(v[6], v[7]);
+  *reinterpret_cast<uint4*>(p) = u;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// mean (LayerNorm) and rstd of one row, reading it twice
+__device__ __forceinline__ void row_stats(const __nv_bfloat16* xr, int h, int kind, float eps,
+                                          float& mean, float& rstd) {
+  const int lane = threadIdx.x & 31;
+  float s = 0.f;
+  for (int c = lane * 8; c < h; c += 256) {
+    float v[8];
+    ld8(xr + c, v);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) s += (kind == 0) ? v[k] : v[k] * v[k];
+  }
+  s = warp_sum(s);
+  if (kind == 0) {
+    mean = s / h;
+    float q = 0.f;
+    for (int c = lane * 8; c < h; c += 256) {
+      float v[8];
+      ld8(xr + c, v);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float t = v[k] - mean;
+        q += t * t;
+      }
+    }
+    q = warp_sum(q);
+    rstd = rsqrtf(q / h + eps);
+  } else {
+    mean = 0.f;
+    rstd = rsqrtf(s / h + eps);
+  }
+}
+
+__global__ void norm_fwd_kernel(int64_t rows, int h, int kind, float eps, const __nv_bfloat16* x,
+                                int64_t ldx, const __nv_bfloat16* w, const __nv_bfloat16* b,
+                                __nv_bfloat16* y, int64_t ldy, float* rstd_out, float* mean_out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
+    const __nv_bfloat16* xr = x + r * ldx;
+    float mean, rstd;
+    row_stats(xr, h, kind, eps, mean, rstd);
+    for (int c = lane * 8; c < h; c += 256) {
+      float v[8], wv[8], bv[8];
+      ld8(xr + c, v);
+      ld8(w + c, wv);
+      if (b) ld8(b + c, bv);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = (v[k] - mean) * rstd * wv[k] + (b ? bv[k] : 0.f);
+      st8(y + r * ldy + c, v);
+    }
+    if (lane == 0) {
+      if (rstd_out) rstd_out[r] = rstd;
+      if (mean_out) mean_out[r] = mean;
+    }
+  }
+}
+
+// dx = res + rstd * (g - mean(g) - xhat * mean(g * xhat))    (LayerNorm)
+//    = res + rstd * (g - xhat * mean(g * xhat))              (RMSNorm)
+// with g = dy * w; dw += sum_rows dy * xhat, db += sum_rows dy.
+__global__ void norm_bwd_kernel(int64_t rows, int h, int kind, float eps, const void* dy_, int dy_f32,
+                                int64_t lddy, const __nv_bfloat16* x, int64_t ldx,
+                                const __nv_bfloat16* w, const __nv_bfloat16* res, int64_t ldres,
+                                __nv_bfloat16* dx, int64_t lddx, float* dw, float* db) {
+  extern __shared__ float red[];  // [2h]: dw and db partials of this block
+  for (int c = threadIdx.x; c < 2 * h; c += blockDim.x) red[c] = 0.f;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  auto load_dy = [&](int64_t r, int c, float (&v)[8]) {
+    if (dy_f32) ld8f(reinterpret_cast<const float*>(dy_) + r * lddy + c, v);
+    else ld8(reinterpret_cast<const __nv_bfloat16*>(dy_) + r * lddy + c, v);
+  };
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
+    const __nv_bfloat16* xr = x + r * ldx;
+    float mean, rstd;
+    row_stats(xr, h, kind, eps, mean, rstd);
+    float sg = 0.f, sgx = 0.f;
+    for (int c = lane * 8; c < h; c += 256) {
+      float v[8], wv[8], gv[8];
+      ld8(xr + c, v);
+      ld8(w + c, wv);
+      load_dy(r, c, gv);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float xh = (v[k] - mean) * rstd;
+        const float g = gv[k] * wv[k];
+        sg += g;
+        sgx += g * xh;
+        atomicAdd(&red[c + k], gv[k] * xh);
+        atomicAdd(&red[h + c + k], gv[k]);
+      }
+    }
+    sg = warp_sum(sg) / h;
+    sgx = warp_sum(sgx) / h;
+    if (kind != 0) sg = 0.f;
+    for (int c = lane * 8; c < h; c += 256) {
+      float v[8], wv[8], gv[8], rv[8];
+      ld8(xr + c, v);
+      ld8(w + c, wv);
+      load_dy(r, c, gv);
+      if (res) ld8(res + r * ldres + c, rv);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float xh = (v[k] - mean) * rstd;
+        v[k] = rstd * (gv[k] * wv[k] - sg - xh * sgx) + (res ? rv[k] : 0.f);
+      }
+      st8(dx + r * lddx + c, v);
+    }
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < h; c += blockDim.x) {
+    if (dw) atomicAdd(&dw[c], red[c]);
+    if (db) atomicAdd(&db[c], red[h + c]);
+  }
+}
+
+// out[n] += sum_r in[r, n]; 8 columns per thread, rows split over gridDim.y
+__global__ void colsum_kernel(int64_t rows, int64_t n, const __nv_bfloat16* in, int64_t ld, float* out) {
+  const int64_t c = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  if (c >= n) return;
+  const int64_t per = (rows + gridDim.y - 1) / gridDim.y;
+  const int64_t r0 = blockIdx.y * per;
+  const int64_t r1 = min(rows, r0 + per);
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int64_t r = r0; r < r1; ++r) {
+    float v[8];
+    ld8(in + r * ld + c, v);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] += v[k];
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    if (c + k < n) atomicAdd(&out[c + k], acc[k]);
+}
+
+__global__ void f32_to_bf16_kernel(int64_t rows, int64_t n, const float* src, int64_t lds,
+                                   __nv_bfloat16* dst, int64_t ldd, float scale) {
+  const int64_t per_row = n / 8;
+  const int64_t total = rows * per_row;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / per_row;
+    const int64_t c = (i % per_row) * 8;
+    float v[8];
+    ld8f(src + r * lds + c, v);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] *= scale;
+    st8(dst + r * ldd + c, v);
+  }
+}
+
+// Dsum[b, h, q] = sum_k dO[b*s + q, h*d + k] * O[b*s + q, h*d + k]  (0 for q >= s)
+__global__ void dsum_kernel(int b, int s, int s_pad, int H, int d, const __nv_bfloat16* o,
+                            int64_t ld_o, int64_t o_col, const __nv_bfloat16* dout, int64_t ld_do,
+                            int64_t do_col, float* Dsum) {
+  const int64_t total = (int64_t)b * s_pad * H;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int hn = (int)(i % H);
+    const int64_t t = i / H;
+    const int q = (int)(t % s_pad);
+    const int bi = (int)(t / s_pad);
+    float acc = 0.f;
+    if (q < s) {
+      const __nv_bfloat16* orow = o + ((int64_t)bi * s + q) * ld_o + o_col + (int64_t)hn * d;
+      const __nv_bfloat16* drow = dout + ((int64_t)bi * s + q) * ld_do + do_col + (int64_t)hn * d;
+      for (int k = 0; k < d; k += 8) {
+        float a[8], c[8];
+        ld8(orow + k, a);
+        ld8(drow + k, c);
+#pragma unroll
+        for (int m = 0; m < 8; ++m) acc += a[m] * c[m];
+      }
+    }
+    Dsum[((int64_t)bi * H + hn) * s_pad + q] = acc;
+  }
+}
+
+int grid_for(int64_t work, int per_block) {
+  int64_t g = (work + per_block - 1) / per_block;
+  if (g > 152 * 16) g = 152 * 16;
+  return (int)(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+int norm_fwd(int64_t rows, int h, int kind, float eps, const void* x, int64_t ldx, const void* w,
+             const void* b, void* y, int64_t ldy, float* rstd, float* mean, cudaStream_t st) {
+  if (rows <= 0) return 0;
+  const int threads = 256;
+  norm_fwd_kernel<<<grid_for(rows, threads / 32), threads, 0, st>>>(
+      rows, h, kind, eps, (const __nv_bfloat16*)x, ldx, (const __nv_bfloat16*)w,
+      (const __nv_bfloat16*)b, (__nv_bfloat16*)y, ldy, rstd, mean);
+  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
+int norm_bwd(int64_t rows, int h, int kind, float eps, const void* dy, int dy_f32, int64_t lddy,
+             const void* x, int64_t ldx, const void* w, const void* res, int64_t ldres, void* dx,
+             int64_t lddx, float* dw, float* db, cudaStream_t st) {
+  if (rows <= 0) return 0;
+  const int threads = 256;
+  const size_t smem = (size_t)2 * h * sizeof(float);
+  if (smem > 48 * 1024) {
+    static bool attr = false;
+    if (!attr) {
+      if (cudaFuncSetAttribute(norm_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
+          cudaSuccess)
+        return 3;
+      attr = true;
+    }
+  }
+  int grid = (int)((rows + 7) / 8);
+  if (grid > 152 * 2) grid = 152 * 2;
+  norm_bwd_kernel<<<grid, threads, smem, st>>>(rows, h, kind, eps, dy, dy_f32, lddy,
+                                               (const __nv_bfloat16*)x, ldx, (const __nv_bfloat16*)w,
+                                               (const __nv_bfloat16*)res, ldres, (__nv_bfloat16*)dx,
+                                               lddx, dw, db);
+  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
+int colsum(int64_t rows, int64_t n, const void* in, int64_t ld, float* out, int accumulate,
+           cudaStream_t st) {
+  if (!accumulate && cudaMemsetAsync(out, 0, n * sizeof(float), st) != cudaSuccess) return 3;
+  if (rows <= 0 || n <= 0) return 0;
+  const int threads = 128;
+  dim3 grid((unsigned)((n / 8 + threads - 1) / threads), 1);
+  int64_t ysplit = (rows + 255) / 256;
+  if (ysplit > 128) ysplit = 128;
+  grid.y = (unsigned)ysplit;
+  colsum_kernel<<<grid, threads, 0, st>>>(rows, n, (const __nv_bfloat16*)in, ld, out);
+  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
+int f32_to_bf16(int64_t rows, int64_t n, const float* src, int64_t ld_src, void* dst, int64_t ld_dst,
+                float scale, cudaStream_t st) {
+  if (rows <= 0 || n <= 0) return 0;
+  f32_to_bf16_kernel<<<grid_for(rows * (n / 8), 256), 256, 0, st>>>(rows, n, src, ld_src,
+                                                                     (__nv_bfloat16*)dst, ld_dst, scale);
+  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
+int attn_dsum(const AttnBwdShape& sh, const void* o, const void* dout, float* Dsum, int s_pad,
+              cudaStream_t st) {
+  const AttnShape& f = sh.f;
+  const int64_t total = (int64_t)f.b * s_pad * f.H;
+  dsum_kernel<<<grid_for(total, 256), 256, 0, st>>>(f.b, f.s, s_pad, f.H, f.d, (const __nv_bfloat16*)o,
+                                                    f.ld_o, f.o_col, (const __nv_bfloat16*)dout, sh.ld_do,
+                                                    sh.do_col, Dsum);
+  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
+}  // namespace bpt

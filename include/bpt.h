@@ -1,0 +1,189 @@
+/*
+ * bpt.h -- C ABI of libbpt: the fused blockwise attention + FFN layer
+ * (Blockwise Parallel Transformer) on one NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes is the layer these pages define:
+ *
+ *   x1 = x + Attn(N1(x)) Wo^T + bo
+ *   y  = x1 + FFN(N2(x1))
+ *   Attn, per query head n with key/value head g = floor(n / G):
+ *        softmax(Q_n K_g^T / sqrt(d) + M) V_g,   M_ij = -inf where j > i (causal)
+ *   FFN  = GeLU(z W1^T + b1) W2^T + b2           (GPT layer; act 0 erf, 1 tanh)
+ *        = (SiLU(z W1^T) * (z W3^T)) W2^T         (Llama layer, act 2; W1 gate, W3 up, W2 down)
+ *   N    = LayerNorm(gamma, beta, eps) or RMSNorm(gamma, eps)
+ *
+ *  - "Blockwise Parallel Transformer for Long Context Large Models", section
+ *    3.4: blockwise attention with online softmax ("Blockwise Self-Attention
+ *    with Online Softmax", Equation 3), the FFN applied to each finished
+ *    query block ("The FFN Memory Bottleneck and Why Fusion Is Possible"),
+ *    Algorithm 1 and the Figure 3 implementation notes (remat of each block,
+ *    causal bias per block).
+ *  - "Training memory: model states, activations and checkpointing", section
+ *    3: the pre-LN GPT layer with biases and GeLU, the Llama-style layer,
+ *    full activation checkpointing (the backward pass reruns the forward).
+ *  - "Untied Ulysses: Memory-Efficient Context Parallelism via Headwise
+ *    Chunking", section 3.4 "The Core Mechanism: Headwise Chunking via UPipe"
+ *    (U heads per stage, buffers reused, output buffer filled per stage) and
+ *    section 4.1 "The GQA Scheduling Algorithm" (query head i uses key/value
+ *    head floor(i/G)).  Only the single-GPU part: no all-to-all.
+ *
+ * Conventions
+ *  - Activations and weights are bf16, row-major.  x, y, dy, dx: [b, s, h].
+ *    Weights use the nn.Linear layout [out, in]: wq [H*d, h], wk/wv
+ *    [H_kv*d, h], wo [h, H*d], w1/w3 [f, h], w2 [h, f]; biases and norm
+ *    parameters are vectors.  A pointer a variant does not use is NULL.
+ *  - Weight gradients are fp32, same shapes.  They are overwritten unless
+ *    BPT_FLAG_ACCUM_GRADS is set, in which case they are accumulated (+=).
+ *  - Accumulation is fp32 everywhere; the log-sum-exp saved by the forward
+ *    pass is fp32 [b, H, s] in natural-log units.
+ *  - Every device pointer must be 16-byte aligned and every row length a
+ *    multiple of 8 elements.
+ *  - Ownership: the caller allocates every buffer (inputs, outputs, the
+ *    workspace whose size bpt_workspace_bytes reports).  The library never
+ *    allocates device memory.  It keeps one lazily set device error word.
+ *  - Streams: `stream` is a cudaStream_t (NULL = legacy default stream).
+ *    Every call is asynchronous on it except bpt_last_device_error.
+ *  - Errors: functions return a BPT_* status.  Arguments are validated on
+ *    the host before anything is launched; a failed launch returns
+ *    BPT_ECUDA.  Device-side waits are bounded: a wait that runs out records
+ *    BPT_ETIMEOUT in the device error word, the kernel leaves cleanly, and
+ *    bpt_last_device_error reports it.
+ */
+#ifndef BPT_H_
+#define BPT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  BPT_OK = 0,
+  BPT_EINVAL = 1,       /* shapes, divisibility, pointers or flags invalid */
+  BPT_ENOSPC = 2,       /* workspace smaller than bpt_workspace_bytes() */
+  BPT_ECUDA = 3,        /* a CUDA runtime/driver call failed */
+  BPT_ETIMEOUT = 4,     /* a bounded device wait ran out (device error word) */
+  BPT_EUNSUPPORTED = 5  /* valid but not built: e.g. head_dim not in {64,80,96,112,128} */
+};
+
+enum { BPT_NORM_LAYER = 0, BPT_NORM_RMS = 1 };
+enum { BPT_ACT_GELU_ERF = 0, BPT_ACT_GELU_TANH = 1, BPT_ACT_SWIGLU = 2 };
+enum { BPT_FLAG_ACCUM_GRADS = 1 };
+
+enum { BPT_PASS_FWD = 0, BPT_PASS_BWD = 1, BPT_PASS_HEADCHUNK = 2 };
+
+/* Shape and schedule of one layer.
+ *   b, s, h            batch, sequence length, model width
+ *   n_heads, n_kv_heads, head_dim   H, H_kv (H % H_kv == 0, G = H/H_kv), d
+ *   ffn_dim            f
+ *   q_block, kv_block  attention blocks c_q, c_kv: multiples of 128 (the
+ *                      tensor-core tile; a block of 256 is two tiles in turn)
+ *   ffn_block          rows per FFN block c_f: a multiple of q_block; 0 means
+ *                      min(2048, s rounded up to q_block)
+ *   head_chunk         U query heads per stage; U == H (or 0) means no
+ *                      chunking; H % U == 0 and U % G == 0
+ *   causal             1: key j is masked for query i when j > i
+ *   norm, act          BPT_NORM_*, BPT_ACT_*
+ *   has_bias           1: every linear has a bias (GPT); 0: none (Llama)
+ *   norm_eps           epsilon inside the norm's square root
+ *   flags              BPT_FLAG_*                                             */
+typedef struct {
+  int32_t b, s, h, n_heads, n_kv_heads, head_dim, ffn_dim;
+  int32_t q_block, kv_block, ffn_block, head_chunk;
+  int32_t causal;
+  int32_t norm;
+  int32_t act;
+  int32_t has_bias;
+  float norm_eps;
+  int32_t flags;
+} bpt_config;
+
+/* bf16 device pointers, nn.Linear [out, in]; NULL where the variant has none
+ * (ln*_b for RMSNorm, every b* when has_bias == 0, w3 unless SwiGLU). */
+typedef struct {
+  const void *ln1_w, *ln1_b, *wq, *bq, *wk, *bk, *wv, *bv, *wo, *bo;
+  const void *ln2_w, *ln2_b, *w1, *b1, *w2, *b2, *w3;
+} bpt_weights;
+
+/* fp32 device pointers with the shapes of the matching weights. */
+typedef struct {
+  void *ln1_w, *ln1_b, *wq, *bq, *wk, *bk, *wv, *bv, *wo, *bo;
+  void *ln2_w, *ln2_b, *w1, *b1, *w2, *b2, *w3;
+} bpt_grads;
+
+/* Bytes of device workspace a call needs: pass BPT_PASS_FWD for
+ * bpt_layer_fwd, BPT_PASS_BWD for bpt_layer_bwd, BPT_PASS_HEADCHUNK for
+ * bpt_attn_headchunk.  0 for an invalid config. */
+size_t bpt_workspace_bytes(const bpt_config* cfg, int pass);
+
+/* Bytes the forward pass saves for the backward pass: the log-sum-exp of
+ * every attention row, fp32 [b, H, s] (the only activation kept besides the
+ * layer input x, which the caller keeps). */
+size_t bpt_saved_bytes(const bpt_config* cfg);
+
+/* Forward pass of one layer.
+ *   x [b,s,h] bf16 in; y [b,s,h] bf16 out.
+ *   saved: bpt_saved_bytes() bytes for the backward pass, or NULL (inference).
+ *   ws/ws_bytes: workspace of at least bpt_workspace_bytes(cfg, BPT_PASS_FWD).
+ * Schedule: Q/K/V for the whole sequence (per head-chunk stage when
+ * head_chunk < H), then for each FFN block of c_f rows: attention of those
+ * query rows over their key/value blocks (online softmax, tensor cores), the
+ * output projection with bias and residual, N2, fc1 + activation and fc2 with
+ * bias and residual into y.  The s x s scores and the s x f FFN intermediate
+ * never exist; only one c_f x f block does. */
+int bpt_layer_fwd(const bpt_config* cfg, const bpt_weights* w, const void* x, void* y,
+                  void* saved, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward pass with recomputation.
+ *   x: the forward input; saved: what bpt_layer_fwd wrote; dy [b,s,h] bf16.
+ *   dx [b,s,h] bf16 out; grads: fp32 weight gradients (see BPT_FLAG_ACCUM_GRADS).
+ * The forward pass is rerun blockwise (N1, Q/K/V, attention, output
+ * projection, and per FFN block N2 and fc1) and every gradient is formed
+ * from the rebuilt blocks: attention probabilities are rebuilt from Q, K and
+ * the saved log-sum-exp tile by tile. */
+int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, const void* saved,
+                  const void* dy, void* dx, const bpt_grads* grads, void* ws, size_t ws_bytes,
+                  void* stream);
+
+/* Headwise-chunked attention on one GPU: for each of H/U stages, project the
+ * stage's U query heads and U/G key/value heads from xn (the normalised
+ * input, [b,s,h] bf16), run blockwise causal attention for those heads and
+ * write their output into o [b,s,H*d] (preallocated, filled slice by slice)
+ * and their log-sum-exp into lse [b,H,s] fp32 (nullable).  The per-stage
+ * Q/K/V buffer in the workspace is reused by every stage, so peak Q/K/V
+ * memory is 2*b*s*(U + 2U/G)*d bytes instead of 2*b*s*(H + 2H_kv)*d. */
+int bpt_attn_headchunk(const bpt_config* cfg, const bpt_weights* w, const void* xn, void* o,
+                       void* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* Attention alone on a packed projection buffer
+ *   qkv [b*s, (H + 2H_kv)*d] bf16: row t holds Q heads 0..H-1, then K heads,
+ *   then V heads (the layout the layer's projection writes),
+ *   o [b*s, H*d] bf16 out, lse [b,H,s] fp32 out (nullable).
+ * Same kernel the layer uses (BPT page section 3.4, Algorithm 1 inner loop). */
+int bpt_attention_fwd(const bpt_config* cfg, const void* qkv, void* o, void* lse, void* stream);
+
+/* Attention backward on the same packed layout.
+ *   qkv, o, lse as produced by bpt_attention_fwd; dout [b*s, H*d] bf16.
+ *   dqkv [b*s, (H + 2H_kv)*d] bf16 out (dQ, then dK, then dV; dK/dV summed
+ *   over the G query heads of each group).
+ *   ws: at least bpt_attention_bwd_workspace_bytes(cfg) bytes (fp32 dQ
+ *   accumulator and the per-row dO.O sums). */
+size_t bpt_attention_bwd_workspace_bytes(const bpt_config* cfg);
+int bpt_attention_bwd(const bpt_config* cfg, const void* qkv, const void* o, const void* lse,
+                      const void* dout, void* dqkv, void* ws, size_t ws_bytes, void* stream);
+
+/* Text of a status code (static storage). */
+const char* bpt_status_string(int status);
+
+/* Synchronises `stream`, then reads and clears the device error word.
+ * Returns BPT_OK, BPT_ETIMEOUT (a bounded wait ran out; *detail = the wait
+ * site id) or BPT_ECUDA (the synchronisation itself failed; *detail = the
+ * cudaError_t).  detail may be NULL. */
+int bpt_last_device_error(void* stream, int* detail);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BPT_H_ */

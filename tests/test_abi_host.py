@@ -1,0 +1,110 @@
+"""The C-ABI library loads on a machine without a GPU, exports every function
+include/bpt.h declares, and rejects invalid arguments on the host before it
+launches anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import blockwise_attention_ffn_gb300 as bpt
+from blockwise_attention_ffn_gb300 import presets
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def built():
+    from blockwise_attention_ffn_gb300 import build
+    build.build()
+    return bpt.lib()
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", fn)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names |= set(re.findall(r"\b(bpt_[a-z0-9_]+)\s*\(", txt))
+    return names
+
+
+def test_every_declared_symbol_is_exported(built):
+    names = _declared_functions()
+    assert {"bpt_layer_fwd", "bpt_layer_bwd", "bpt_attn_headchunk"} <= names
+    for n in names:
+        assert hasattr(built, n), n
+
+
+def test_config_struct_matches_header():
+    hdr = open(os.path.join(ROOT, "include", "bpt.h")).read()
+    body = hdr[hdr.index("typedef struct {"):hdr.index("} bpt_config;")]
+    fields = re.findall(r"\b([a-z_0-9]+)\b(?=[,;])", body.replace("int32_t", "").replace("float", ""))
+    assert fields == [f for f, _ in bpt.BptConfig._fields_]
+    assert ctypes.sizeof(bpt.BptConfig) == 4 * len(fields)
+    wbody = hdr[hdr.index("const void *ln1_w"):hdr.index("} bpt_weights;")]
+    wf = re.findall(r"\*([a-z0-9_]+)", wbody)
+    assert tuple(wf) == bpt.WEIGHT_FIELDS
+
+
+def test_status_strings(built):
+    for s in range(6):
+        assert bpt.bpt_status_string(s)
+    assert "unknown" in bpt.bpt_status_string(99)
+
+
+def test_workspace_sizes_are_host_only(built):
+    c3 = presets.C3
+    assert bpt.bpt_workspace_bytes(c3, bpt.BPT_PASS_FWD) > 0
+    assert bpt.bpt_workspace_bytes(c3, bpt.BPT_PASS_BWD) > bpt.bpt_workspace_bytes(c3, bpt.BPT_PASS_FWD)
+    assert bpt.bpt_saved_bytes(c3) == 1 * 32 * 32768 * 4
+    # invalid configs report 0 bytes
+    assert bpt.bpt_workspace_bytes(c3.with_(h=2561), 0) == 0
+    assert bpt.bpt_workspace_bytes(c3.with_(head_chunk=5), 0) == 0
+    assert bpt.bpt_workspace_bytes(c3.with_(head_dim=72), 0) == 0
+    # head chunking bounds the stage buffer: workspace shrinks with U
+    c5 = presets.C5
+    full = bpt.bpt_workspace_bytes(c5.with_(head_chunk=32), bpt.BPT_PASS_HEADCHUNK)
+    part = bpt.bpt_workspace_bytes(c5.with_(head_chunk=8), bpt.BPT_PASS_HEADCHUNK)
+    assert full == pytest.approx(4 * part, rel=1e-3)
+
+
+def _call_fwd(cfg, x=1 << 20, y=1 << 20, ws=1 << 20, wsz=1 << 40):
+    L = bpt.lib()
+    c = bpt.make_config(cfg)
+    w = bpt.BptWeights(*([1 << 20] * len(bpt.WEIGHT_FIELDS)))
+    return L.bpt_layer_fwd(ctypes.byref(c), ctypes.byref(w), x, y, None, ws, wsz, None)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(s=0), dict(h=100), dict(n_heads=5), dict(head_chunk=3), dict(q_block=64),
+    dict(ffn_block=100), dict(norm=2), dict(act=3), dict(norm_eps=0.0), dict(flags=8),
+    dict(b=0),
+])
+def test_invalid_config_rejected_before_launch(built, bad):
+    cfg = presets.C1.with_(**bad)
+    assert _call_fwd(cfg) == bpt.BPT_EINVAL
+
+
+def test_unsupported_head_dim(built):
+    assert _call_fwd(presets.C1.with_(head_dim=72, h=288)) == bpt.BPT_EUNSUPPORTED
+
+
+def test_null_and_misaligned_pointers_rejected(built):
+    assert _call_fwd(presets.C1, x=None) == bpt.BPT_EINVAL
+    assert _call_fwd(presets.C1, y=(1 << 20) + 2) == bpt.BPT_EINVAL
+
+
+def test_small_workspace_rejected(built):
+    assert _call_fwd(presets.C1, wsz=1024) == bpt.BPT_ENOSPC
+
+
+def test_missing_weight_rejected(built):
+    L = bpt.lib()
+    c = bpt.make_config(presets.C1)
+    ptrs = [1 << 20] * len(bpt.WEIGHT_FIELDS)
+    ptrs[bpt.WEIGHT_FIELDS.index("bo")] = None
+    w = bpt.BptWeights(*ptrs)
+    assert L.bpt_layer_fwd(ctypes.byref(c), ctypes.byref(w), 1 << 20, 1 << 20, None, 1 << 20,
+                           1 << 40, None) == bpt.BPT_EINVAL

@@ -1,0 +1,118 @@
+"""Attention kernels (forward and backward) against the fp64 oracle, element by
+element, on shapes that span several tiles, ragged tails, a single row,
+grouped-query heads, both masks and every supported head dimension."""
+import numpy as np
+import pytest
+import torch
+
+import blockwise_attention_ffn_gb300 as bpt
+from blockwise_attention_ffn_gb300.presets import LayerConfig
+from oracle import ref
+from tests.gpu_helpers import assert_close, to64
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [
+    # b, s, H, Hkv, d, causal
+    (1, 128, 2, 2, 64, 1),
+    (1, 300, 2, 1, 80, 1),
+    (2, 200, 2, 2, 128, 0),
+    (1, 513, 4, 2, 128, 1),
+    (1, 1, 1, 1, 64, 1),
+    (1, 384, 2, 2, 96, 1),
+    (1, 260, 2, 2, 112, 0),
+    (1, 640, 4, 1, 80, 0),
+]
+
+
+def _cfg(b, s, H, Hkv, d, causal):
+    return LayerConfig(b=b, s=s, h=H * d, n_heads=H, n_kv_heads=Hkv, head_dim=d, ffn_dim=64,
+                       causal=causal)
+
+
+def _qkv(b, s, H, Hkv, d, seed):
+    g = torch.Generator().manual_seed(seed)
+    qkv = torch.randn(b * s, (H + 2 * Hkv) * d, generator=g) * 1.5
+    return qkv.to(torch.bfloat16)
+
+
+def _split(qkv64, b, s, H, Hkv, d):
+    t = qkv64.reshape(b, s, H + 2 * Hkv, d)
+    return t[:, :, :H], t[:, :, H:H + Hkv], t[:, :, H + Hkv:]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_attention_forward(shape):
+    b, s, H, Hkv, d, causal = shape
+    cfg = _cfg(*shape)
+    qkv = _qkv(b, s, H, Hkv, d, seed=s + d)
+    o = torch.zeros(b * s, H * d, dtype=torch.bfloat16, device="cuda")
+    sp = bpt.s_pad(cfg)
+    lse = torch.zeros(b, H, sp, dtype=torch.float32, device="cuda")
+    bpt.bpt_attention_fwd(cfg, qkv.cuda(), o, lse)
+    torch.cuda.synchronize()
+    assert bpt.bpt_last_device_error()[0] == bpt.BPT_OK
+    q, k, v = _split(to64(qkv), b, s, H, Hkv, d)
+    G = H // Hkv
+    o_ref = np.empty((b, s, H, d))
+    lse_ref = np.empty((b, H, s))
+    for bi in range(b):
+        for n in range(H):
+            o_ref[bi, :, n], lse_ref[bi, n] = ref.attention_head(q[bi, :, n], k[bi, :, n // G],
+                                                                 v[bi, :, n // G], bool(causal))
+    assert_close(to64(o).reshape(b, s, H, d), o_ref, "O")
+    assert_close(to64(lse)[:, :, :s], lse_ref, "LSE", max_abs=1e-3, rel_fro=1e-5)
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_attention_backward(shape):
+    b, s, H, Hkv, d, causal = shape
+    cfg = _cfg(*shape)
+    qkv = _qkv(b, s, H, Hkv, d, seed=2 * s + d)
+    g = torch.Generator().manual_seed(7 + s)
+    dout = torch.randn(b * s, H * d, generator=g).to(torch.bfloat16)
+    qkv_d = qkv.cuda()
+    o = torch.zeros(b * s, H * d, dtype=torch.bfloat16, device="cuda")
+    sp = bpt.s_pad(cfg)
+    lse = torch.zeros(b, H, sp, dtype=torch.float32, device="cuda")
+    bpt.bpt_attention_fwd(cfg, qkv_d, o, lse)
+    dqkv = torch.full_like(qkv_d, float("nan"))
+    ws = bpt.alloc_bytes(bpt.bpt_attention_bwd_workspace_bytes(cfg))
+    bpt.bpt_attention_bwd(cfg, qkv_d, o, lse, dout.cuda(), dqkv, ws)
+    torch.cuda.synchronize()
+    assert bpt.bpt_last_device_error()[0] == bpt.BPT_OK
+    q, k, v = _split(to64(qkv), b, s, H, Hkv, d)
+    do = to64(dout).reshape(b, s, H, d)
+    G = H // Hkv
+    dq = np.zeros((b, s, H, d))
+    dk = np.zeros((b, s, Hkv, d))
+    dv = np.zeros((b, s, Hkv, d))
+    for bi in range(b):
+        for n in range(H):
+            a_, b_, c_ = ref.attention_head_backward(q[bi, :, n], k[bi, :, n // G], v[bi, :, n // G],
+                                                     do[bi, :, n], bool(causal))
+            dq[bi, :, n] += a_
+            dk[bi, :, n // G] += b_
+            dv[bi, :, n // G] += c_
+    got = to64(dqkv).reshape(b, s, H + 2 * Hkv, d)
+    assert_close(got[:, :, :H], dq, "dQ")
+    assert_close(got[:, :, H:H + Hkv], dk, "dK")
+    assert_close(got[:, :, H + Hkv:], dv, "dV")
+
+
+def test_identical_keys_give_prefix_mean():
+    """Closed form on the GPU: equal keys make causal attention the running
+    mean of the values; row 0 is V_0."""
+    b, s, H, Hkv, d = 1, 300, 2, 2, 64
+    cfg = _cfg(b, s, H, Hkv, d, 1)
+    qkv = _qkv(b, s, H, Hkv, d, seed=5).float()
+    qkv[:, H * d:(H + Hkv) * d] = qkv[0:1, H * d:(H + Hkv) * d]
+    qkv = qkv.to(torch.bfloat16)
+    o = torch.zeros(b * s, H * d, dtype=torch.bfloat16, device="cuda")
+    bpt.bpt_attention_fwd(cfg, qkv.cuda(), o, None)
+    torch.cuda.synchronize()
+    v = to64(qkv)[:, (H + Hkv) * d:].reshape(s, Hkv, d)
+    want = np.cumsum(v, 0) / np.arange(1, s + 1)[:, None, None]
+    got = to64(o).reshape(s, H, d)
+    assert_close(got, want, "prefix mean")
+    assert np.max(np.abs(got[0] - v[0])) <= 4e-3  # bf16 rounding of V_0 itself only

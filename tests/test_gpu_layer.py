@@ -1,0 +1,107 @@
+"""The whole layer (forward and recompute backward) against the fp64 oracle,
+element by element, on seeded inputs of both layer variants: GPT (LayerNorm,
+GeLU, biases) and Llama (RMSNorm, SwiGLU, no biases, grouped-query attention,
+head-chunked)."""
+import numpy as np
+import pytest
+import torch
+
+import blockwise_attention_ffn_gb300 as bpt
+from blockwise_attention_ffn_gb300.presets import C1, LayerConfig
+from oracle import ref
+from tests.gpu_helpers import (assert_close, assert_close_grad, device_inputs, run_bwd, run_fwd,
+                               to64)
+from tests.oracle_helpers import inputs_to_oracle, oracle_cfg
+
+pytestmark = pytest.mark.gpu
+
+GPT_SMALL = LayerConfig(b=1, s=300, h=256, n_heads=4, n_kv_heads=4, head_dim=64, ffn_dim=1024,
+                        ffn_block=128, name="gpt ragged")
+GPT_D80 = LayerConfig(b=1, s=520, h=320, n_heads=4, n_kv_heads=4, head_dim=80, ffn_dim=640,
+                      ffn_block=256, act=1, name="gpt d80 tanh")
+LLAMA_SMALL = LayerConfig(b=1, s=384, h=512, n_heads=8, n_kv_heads=2, head_dim=64, ffn_dim=768,
+                          head_chunk=4, norm=1, act=2, has_bias=0, name="llama gqa chunked")
+GPT_B2 = LayerConfig(b=2, s=200, h=256, n_heads=2, n_kv_heads=2, head_dim=128, ffn_dim=512,
+                     causal=0, name="gpt b2 noncausal")
+
+LAYERS = [GPT_SMALL, GPT_D80, LLAMA_SMALL, GPT_B2]
+
+
+@pytest.mark.parametrize("cfg", LAYERS, ids=lambda c: c.name)
+def test_layer_forward(cfg):
+    inp, dev = device_inputs(cfg, seed=11)
+    y, _ = run_fwd(cfg, dev)
+    o = inputs_to_oracle(inp)
+    y_ref = ref.layer_forward(o["x"], o["W"], oracle_cfg(cfg))
+    assert_close(to64(y), y_ref, "y")
+
+
+@pytest.mark.parametrize("cfg", LAYERS, ids=lambda c: c.name)
+def test_layer_backward(cfg):
+    inp, dev = device_inputs(cfg, seed=12)
+    _, saved = run_fwd(cfg, dev)
+    dx, grads = run_bwd(cfg, dev, saved)
+    o = inputs_to_oracle(inp)
+    dx_ref, g_ref = ref.layer_backward(o["x"], o["W"], o["dy"], oracle_cfg(cfg))
+    assert_close(to64(dx), dx_ref, "dx")
+    for k, v in g_ref.items():
+        assert_close_grad(to64(grads[k]), v, f"d{k}")
+
+
+def test_c1_forward_full_oracle():
+    inp, dev = device_inputs(C1, seed=C1.seed)
+    y, _ = run_fwd(C1, dev)
+    o = inputs_to_oracle(inp)
+    assert_close(to64(y), ref.layer_forward(o["x"], o["W"], oracle_cfg(C1)), "y")
+
+
+def test_headchunk_attention_matches_oracle():
+    cfg = LLAMA_SMALL
+    inp, dev = device_inputs(cfg, seed=13, with_dy=False)
+    xn = dev["x"]  # any normalised-input stand-in: the call projects whatever it gets
+    H, d = cfg.n_heads, cfg.head_dim
+    o = torch.zeros(cfg.b * cfg.s, H * d, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(cfg.b, H, bpt.s_pad(cfg), dtype=torch.float32, device="cuda")
+    ws = bpt.alloc_bytes(bpt.bpt_workspace_bytes(cfg, bpt.BPT_PASS_HEADCHUNK))
+    bpt.bpt_attn_headchunk(cfg, dev["weights"], xn, o, lse, ws)
+    torch.cuda.synchronize()
+    W = inputs_to_oracle(inp)["W"]
+    o_ref, lse_ref, _, _, _ = ref.attention_block(to64(inp["x"])[0], W, oracle_cfg(cfg))
+    assert_close(to64(o), o_ref, "O")
+    assert_close(to64(lse)[0, :, :cfg.s], lse_ref, "LSE", max_abs=2e-3, rel_fro=1e-4)
+
+
+@pytest.mark.parametrize("variant", [dict(head_chunk=2), dict(head_chunk=8), dict(ffn_block=384),
+                                     dict(ffn_block=128, q_block=128)])
+def test_schedule_invariance(variant):
+    """Head chunk U and FFN block size change the schedule, not the result."""
+    base = LLAMA_SMALL
+    _, dev = device_inputs(base, seed=14)
+    y0, s0 = run_fwd(base, dev)
+    dx0, g0 = run_bwd(base, dev, s0)
+    cfg = base.with_(**variant)
+    y1, s1 = run_fwd(cfg, dev)
+    dx1, g1 = run_bwd(cfg, dev, s1)
+    assert torch.equal(y0, y1)
+    assert_close(to64(dx1), to64(dx0), "dx", max_abs=1e-3, rel_fro=1e-4)
+    for k in g0:
+        if g0[k] is not None:
+            assert_close(to64(g1[k]), to64(g0[k]), k, max_abs=1e-3 * max(1, float(g0[k].abs().max())),
+                         rel_fro=1e-4)
+
+
+def test_accumulate_flag_adds_to_existing_gradients():
+    cfg = GPT_SMALL
+    _, dev = device_inputs(cfg, seed=15)
+    _, saved = run_fwd(cfg, dev)
+    _, g0 = run_bwd(cfg, dev, saved)
+    acc = cfg.with_(flags=bpt.BPT_FLAG_ACCUM_GRADS)
+    dx = torch.empty_like(dev["x"])
+    grads = {k: (None if v is None else v.clone()) for k, v in g0.items()}
+    ws = bpt.alloc_bytes(bpt.bpt_workspace_bytes(acc, bpt.BPT_PASS_BWD))
+    bpt.bpt_layer_bwd(acc, dev["weights"], dev["x"], saved, dev["dy"], dx, grads, ws)
+    torch.cuda.synchronize()
+    for k, v in g0.items():
+        if v is not None:
+            assert_close(to64(grads[k]), 2 * to64(v), k, max_abs=1e-3 * max(1, float(v.abs().max())),
+                         rel_fro=1e-5)

@@ -1,0 +1,415 @@
+#!/usr/bin/env python
+"""Benchmark of the fused blockwise attention + FFN layer (forward + recompute
+backward) on GB300, through the C ABI.
+
+One step = bpt_layer_fwd + bpt_layer_bwd of one layer on one batch of seeded
+synthetic input, everything resident in HBM.  Default workload: the GPT-3B
+shaped layer at s = 32768 (h 2560, 32 heads x 80, FFN 10240, GeLU, LayerNorm,
+causal) -- the configuration the headline metric is quoted on.
+
+Prints ONE JSON line (rank 0).  --impl reference times the fp64 CPU oracle
+instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused BPT layer fwd+bwd TFLOP/s and tokens/s at s=32K; % of bf16 tensor peak"
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ----------------------------------------------------------------- FLOP count
+
+def flop_counts(c) -> dict:
+    """Algorithmic FLOPs (multiply-add = 2) of one layer, causal pairs exact.
+
+    F_linear = 2 s h (H + 2 H_kv) d + 2 s H d h + 2 s h f n_mat
+    F_attn   = 4 d H * (number of unmasked query/key pairs)   (~ 2 s^2 H d)
+    forward  = F_linear + F_attn
+    executed (fwd + recompute bwd) = forward + (forward - fc2) + 2 F_linear + 2.5 F_attn
+    model    = 3 * forward"""
+    s, h, H, Hk, d, f, b = c.s, c.h, c.n_heads, c.n_kv_heads, c.head_dim, c.ffn_dim, c.b
+    n_mat = 3 if c.act == 2 else 2
+    lin = b * (2 * s * h * (H + 2 * Hk) * d + 2 * s * H * d * h + 2 * s * h * f * n_mat)
+    fc2 = b * 2 * s * f * h
+    pairs = s * (s + 1) / 2 if c.causal else s * s
+    attn = b * 4.0 * d * H * pairs
+    fwd = lin + attn
+    if not c.backward:
+        return {"forward": fwd, "executed": fwd, "model": fwd, "linear": lin, "attn": attn}
+    executed = fwd + (fwd - fc2) + 2 * lin + 2.5 * attn
+    if c.head_chunk and c.head_chunk < H:
+        # Q/K/V of every stage is projected once more for the attention backward
+        executed += b * 2 * s * h * (H + 2 * Hk) * d
+    return {"forward": fwd, "executed": executed, "model": 3 * fwd, "linear": lin, "attn": attn}
+
+
+def vanilla_activation_bytes(c) -> int:
+    """Activation bytes a vanilla (materialised, non-checkpointed) GPT layer
+    keeps: 34 sbh + 5 a s^2 b ("Training memory: model states, activations and
+    checkpointing", section 3)."""
+    return 34 * c.s * c.b * c.h + 5 * c.n_heads * c.s * c.s * c.b
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        idx = vis.split(",")[0] if vis and vis.split(",")[0].isdigit() else None
+        if idx is not None and any(r[0] == idx for r in rows):
+            rows = [r for r in rows if r[0] == idx]
+        else:
+            first = rows[0][0] if rows else None
+            rows = [r for r in rows if r[0] == first]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ----------------------------------------------------------------- helpers
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d.get("hbm_gbs", 6800.0), "bf16": d.get("bf16_tflops", 1872.7),
+                "bf16_sustained": d.get("bf16_tflops_sustained", 1702.7), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+def load_traffic() -> dict:
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
+    summary (null until a capture of the current kernel exists)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(p):
+        try:
+            return json.load(open(p))
+        except ValueError:
+            return {}
+    return {}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def describe(c) -> dict:
+    return {"workload": c.name, "b": c.b, "s": c.s, "h": c.h, "n_heads": c.n_heads,
+            "n_kv_heads": c.n_kv_heads, "head_dim": c.head_dim, "ffn_dim": c.ffn_dim,
+            "act": ["gelu-erf", "gelu-tanh", "swiglu"][c.act], "norm": ["layernorm", "rmsnorm"][c.norm],
+            "causal": bool(c.causal), "q_block": c.q_block, "kv_block": c.kv_block,
+            "ffn_block": c.ffn_block, "head_chunk": c.head_chunk or c.n_heads,
+            "pass": "fwd+bwd" if c.backward else "fwd", "seed": c.seed,
+            "l2": "no flush: every step streams inputs and buffers far larger than the 129 MB L2"}
+
+
+# ----------------------------------------------------------------- CPU oracle leg
+
+def oracle_sample(c, rows: int):
+    """The fp64 CPU oracle on the first `rows` positions of the workload
+    (same width, heads and FFN; a bounded sample)."""
+    import numpy as np
+
+    from blockwise_attention_ffn_gb300.synth import make_layer_inputs
+    from oracle import ref
+    sc = c.with_(s=rows)
+    inp = make_layer_inputs(sc, seed=c.seed, device="cpu", with_dy=c.backward)
+    W = {k: v.float().double().numpy() for k, v in inp["weights"].items() if v is not None}
+    x = inp["x"].float().double().numpy()
+    oc = ref.LayerCfg(s=rows, h=c.h, n_heads=c.n_heads, n_kv_heads=c.n_kv_heads, head_dim=c.head_dim,
+                      ffn_dim=c.ffn_dim, b=c.b, causal=bool(c.causal), norm=c.norm, act=c.act,
+                      has_bias=bool(c.has_bias), norm_eps=c.norm_eps)
+    t0 = time.perf_counter()
+    ref.layer_forward(x, W, oc)
+    if c.backward:
+        ref.layer_backward(x, W, inp["dy"].float().double().numpy(), oc)
+    dt = time.perf_counter() - t0
+    fl = flop_counts(sc)["executed"]
+    del np
+    return dt, fl, sc
+
+
+def cpu_baseline(c, rows: int) -> dict:
+    dt, fl, sc = oracle_sample(c, rows)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "seconds": dt,
+            "sample": f"fp64 NumPy oracle, forward + backward of the first {rows} positions of the "
+                      f"workload (same layer shape), {fl / 1e12:.3f} TFLOP of the same FLOP "
+                      f"definition; BLAS threads = all host cores"}
+
+
+def run_reference(args, c):
+    ws, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    times, fl = [], None
+    for i in range(args.warmup + args.steps):
+        dt, f, _ = oracle_sample(c, args.ref_rows)
+        fl = f
+        if i >= args.warmup:
+            times.append(dt)
+    t = sum(times) / len(times)
+    val = fl / t / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "config": describe(c),
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"first {args.ref_rows} positions of the workload per step"},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- GPU leg
+
+def run_gpu(args, c):
+    import torch
+    import torch.distributed as tdist
+
+    import blockwise_attention_ffn_gb300 as bpt
+    from blockwise_attention_ffn_gb300.synth import make_layer_inputs
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        tdist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    bpt.lib()
+
+    inp = make_layer_inputs(c, seed=c.seed + 101 * rank, device=dev, with_dy=c.backward)
+    W = inp["weights"]
+    x = inp["x"]
+    dy = inp.get("dy")
+    y = torch.empty_like(x)
+    saved = bpt.alloc_bytes(bpt.bpt_saved_bytes(c), dev)
+    ws_bytes = bpt.bpt_workspace_bytes(c, bpt.BPT_PASS_FWD)
+    if c.backward:
+        ws_bytes = max(ws_bytes, bpt.bpt_workspace_bytes(c, bpt.BPT_PASS_BWD))
+    torch.cuda.synchronize()
+    base_mem = torch.cuda.memory_allocated(dev)
+    ws = bpt.alloc_bytes(ws_bytes, dev)
+    dx = torch.empty_like(x)
+    grads = bpt.alloc_grads(W, dev) if c.backward else None
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        bpt.bpt_layer_fwd(c, W, x, y, saved, ws, stream)
+        if c.backward:
+            bpt.bpt_layer_bwd(c, W, x, saved, dy, dx, grads, ws, stream)
+
+    torch.cuda.reset_peak_memory_stats(dev)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st_, site = bpt.bpt_last_device_error(stream)
+    if st_ != bpt.BPT_OK:
+        raise RuntimeError(f"device error {st_} at wait site {site}")
+    peak_mem = torch.cuda.max_memory_allocated(dev)
+
+    clocks = ClockSampler()
+    if rank == 0:
+        clocks.start()
+    if world > 1:
+        tdist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        tdist.barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    clk = clocks.stop() if rank == 0 else None
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        ms = float(t.item())
+    st_, site = bpt.bpt_last_device_error(stream)
+    if st_ != bpt.BPT_OK:
+        raise RuntimeError(f"device error {st_} at wait site {site}")
+
+    fl = flop_counts(c)
+    total_fl = fl["executed"] * world
+    value = total_fl / (ms * 1e-3) / 1e12
+    peaks = load_peaks()
+
+    # per-kernel breakdown of the same step (separate profiled steps)
+    bpt.bpt_profile_enable(True)
+    nprof = max(1, min(args.steps, 3))
+    for _ in range(nprof):
+        step()
+    torch.cuda.synchronize()
+    prof = bpt.bpt_profile_collect()
+    bpt.bpt_profile_enable(False)
+    launches_per_step = sum(v["launches"] for v in prof.values()) / nprof
+    tot_ms = sum(v["ms"] for v in prof.values())
+    kernels = {}
+    for k, v in prof.items():
+        if v["launches"]:
+            kernels[k] = {"launches_per_step": v["launches"] / nprof, "ms_per_step": v["ms"] / nprof,
+                          "share": v["ms"] / tot_ms if tot_ms else None,
+                          "tflops": (v["flops"] / (v["ms"] * 1e-3) / 1e12) if v["flops"] else None,
+                          "gbs": (v["bytes"] / (v["ms"] * 1e-3) / 1e9) if v["bytes"] else None}
+    dom = max(prof, key=lambda k: prof[k]["ms"])
+    dv = prof[dom]
+    traffic = load_traffic().get(dom)
+    if dv["flops"]:
+        ach = dv["flops"] / (dv["ms"] * 1e-3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peaks["bf16_sustained"],
+                "unit": "TFLOP/s", "frac": ach / peaks["bf16_sustained"],
+                "frac_of_burst_peak": ach / peaks["bf16"],
+                "peak_note": f"{peaks['source']} bf16 sustained (kernel timed inside the long step)",
+                "per_launch_flops": dv["flops"] / dv["launches"],
+                "avg_launch_ms": dv["ms"] / dv["launches"], "traffic": traffic}
+    else:
+        ach = dv["bytes"] / (dv["ms"] * 1e-3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "peak_note": f"{peaks['source']} HBM copy bandwidth",
+                "per_launch_bytes": dv["bytes"] / dv["launches"],
+                "avg_launch_ms": dv["ms"] / dv["launches"], "traffic": traffic}
+
+    # end to end through the C ABI from pinned host buffers
+    xh = x.cpu().pin_memory()
+    dyh = dy.cpu().pin_memory() if c.backward else None
+    outh = torch.empty_like(xh).pin_memory()
+
+    def step_e2e():
+        x.copy_(xh, non_blocking=True)
+        if c.backward:
+            dy.copy_(dyh, non_blocking=True)
+        step()
+        outh.copy_(dx if c.backward else y, non_blocking=True)
+
+    for _ in range(max(1, args.warmup // 2)):
+        step_e2e()
+    torch.cuda.synchronize()
+    if world > 1:
+        tdist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step_e2e()
+    torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = xh.numel() * xh.element_size() + (dyh.numel() * dyh.element_size() if c.backward else 0)
+    d2h = outh.numel() * outh.element_size()
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) inputs, N(0,0.02) weights)",
+            "config": describe(c),
+            "flops_per_step": {"executed": fl["executed"], "model": fl["model"], "forward": fl["forward"]},
+            "tokens_per_s": c.b * c.s * world / (ms * 1e-3),
+            "model_tflops": fl["model"] * world / (ms * 1e-3) / 1e12,
+            "pct_of_bf16_peak": 100 * value / (peaks["bf16"] * world),
+            "pct_of_bf16_peak_sustained": 100 * value / (peaks["bf16_sustained"] * world),
+            "peak_source": peaks["source"],
+            "clocks": clk,
+            "e2e": {"value": total_fl / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "what": "pinned host x (and dy) copied in, fwd+bwd through the C ABI, dx copied out"},
+            "gpu_launches": int(round(launches_per_step * args.steps)),
+            "roofline": roof, "kernels": kernels,
+            "memory": {"peak_device_bytes": peak_mem, "inputs_weights_grads_bytes": base_mem,
+                       "workspace_bytes": ws_bytes, "saved_bytes": bpt.bpt_saved_bytes(c),
+                       "vanilla_layer_activation_bytes_analytic": vanilla_activation_bytes(c)},
+        }
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline(c, args.ref_rows)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        tdist.barrier()
+        tdist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="c3", help="c1..c5 (default c3, the s=32K workload)")
+    ap.add_argument("--ref-rows", type=int, default=1024,
+                    help="positions of the workload the CPU oracle runs per sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    from blockwise_attention_ffn_gb300.presets import PRESETS
+    c = PRESETS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, c)
+    return run_gpu(args, c)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

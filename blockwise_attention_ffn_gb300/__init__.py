@@ -8,7 +8,8 @@ or fails to load, importing the binding's entry points raises.
 Entry points keep the C names: bpt_layer_fwd, bpt_layer_bwd,
 bpt_attn_headchunk, bpt_attention_fwd, bpt_attention_bwd,
 bpt_workspace_bytes, bpt_saved_bytes, bpt_attention_bwd_workspace_bytes,
-bpt_status_string, bpt_last_device_error.
+bpt_status_string, bpt_last_device_error, bpt_profile_enable,
+bpt_profile_collect.
 """
 from __future__ import annotations
 
@@ -83,6 +84,11 @@ def lib() -> ctypes.CDLL:
         L.bpt_status_string.restype = ctypes.c_char_p
         L.bpt_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
         L.bpt_last_device_error.restype = i32
+        L.bpt_profile_enable.argtypes = [i32]
+        L.bpt_profile_enable.restype = i32
+        dp = ctypes.POINTER(ctypes.c_double)
+        L.bpt_profile_collect.argtypes = [i32, dp, dp, dp, ctypes.POINTER(ctypes.c_int)]
+        L.bpt_profile_collect.restype = i32
         _lib = L
     return _lib
 
@@ -183,6 +189,24 @@ def bpt_last_device_error(stream=None):
     d = ctypes.c_int(0)
     rc = lib().bpt_last_device_error(_stream(stream), ctypes.byref(d))
     return int(rc), int(d.value)
+
+
+PROF_KINDS = ("gemm", "attn_fwd", "attn_bwd", "norm", "misc")
+
+
+def bpt_profile_enable(on: bool) -> None:
+    _check(lib().bpt_profile_enable(1 if on else 0), "bpt_profile_enable")
+
+
+def bpt_profile_collect() -> dict:
+    """{kind: dict(ms=..., flops=..., bytes=..., launches=...)} since the
+    last collect (synchronises on the recorded events)."""
+    n = len(PROF_KINDS)
+    ms, fl, by = (ctypes.c_double * n)(), (ctypes.c_double * n)(), (ctypes.c_double * n)()
+    la = (ctypes.c_int * n)()
+    _check(lib().bpt_profile_collect(n, ms, fl, by, la), "bpt_profile_collect")
+    return {k: dict(ms=ms[i], flops=fl[i], bytes=by[i], launches=la[i])
+            for i, k in enumerate(PROF_KINDS)}
 
 
 # ------------------------------------------------------------------ helpers

@@ -37,6 +37,10 @@ def _compile(src: str, obj: str, extra) -> None:
 
 
 def build(force: bool = False, extra_flags=()) -> str:
+    """Compile and link libbpt.so.  BPT_DEBUG=1 in the environment adds a
+    short device-wait budget and a printf of the wait site on a timeout."""
+    if os.environ.get("BPT_DEBUG") == "1":
+        extra_flags = tuple(extra_flags) + ("-DBPT_WAIT_CYCLES=400000000LL", "-DBPT_TIMEOUT_PRINT")
     srcs = [os.path.join(CSRC, s) for s in SOURCES]
     deps = srcs + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     deps.append(os.path.join(HERE, "..", "include", "bpt.h"))

@@ -100,7 +100,8 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_kernel(const __grid_constant_
   uint64_t* ds_full = p_full + 1;
   uint64_t* dq_full = ds_full + 1;
   uint64_t* dq_free = dq_full + 1;
-  uint64_t* drain = dq_free + 1;
+  uint64_t* grp = dq_free + 1;  // compute-warp group barrier
+  uint64_t* drain = grp + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
@@ -129,6 +130,7 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_kernel(const __grid_constant_
     mbar_init(ds_full, 4);
     mbar_init(dq_full, 1);
     mbar_init(dq_free, 4);
+    mbar_init(grp, 4);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -284,7 +286,10 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_kernel(const __grid_constant_
       // the previous step's dQ bulk reductions must have finished reading the
       // staging area (it overlaps the P^T / dS^T tiles)
       bulk_wait_read0();
-      named_bar(1, 128);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(grp);
+      ok = bounded_wait(grp, t & 1, abort_flag, 325, p.err);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
 #pragma unroll
       for (int ch = 0; ch < 16; ++ch) {
         uint4 u;
@@ -354,14 +359,18 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_kernel(const __grid_constant_
       // dV and dK of this key/value tile: every MMA completed before the last
       // dq_full phase
       tc_fence_after();
-      if (kvp < p.s) {
-        __nv_bfloat16* vrow = p.dqkv + ((long long)bi * p.s + kvp) * p.ld_dqkv + p.dv_col + (long long)g * D;
-        __nv_bfloat16* krow = p.dqkv + ((long long)bi * p.s + kvp) * p.ld_dqkv + p.dk_col + (long long)g * D;
+      // the TMEM loads are warp-collective: every lane issues them, only the
+      // stores depend on the row being inside the sequence
+      const bool valid = kvp < p.s;
+      __nv_bfloat16* vrow = p.dqkv + ((long long)bi * p.s + kvp) * p.ld_dqkv + p.dv_col + (long long)g * D;
+      __nv_bfloat16* krow = p.dqkv + ((long long)bi * p.s + kvp) * p.ld_dqkv + p.dk_col + (long long)g * D;
+      const float sc = p.scale;
 #pragma unroll 1
-        for (int cc = 0; cc < D / 16; ++cc) {
-          uint32_t rv[16], rk[16];
-          tmem_ld16(tdV + lane_off + cc * 16, rv);
-          tmem_ld16(tdK + lane_off + cc * 16, rk);
+      for (int cc = 0; cc < D / 16; ++cc) {
+        uint32_t rv[16], rk[16];
+        tmem_ld16(tdV + lane_off + cc * 16, rv);
+        tmem_ld16(tdK + lane_off + cc * 16, rk);
+        if (valid) {
           uint4 v0, v1, k0, k1;
           v0.x = pack_bf16(__uint_as_float(rv[0]), __uint_as_float(rv[1]));
           v0.y = pack_bf16(__uint_as_float(rv[2]), __uint_as_float(rv[3]));
@@ -371,7 +380,6 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_kernel(const __grid_constant_
           v1.y = pack_bf16(__uint_as_float(rv[10]), __uint_as_float(rv[11]));
           v1.z = pack_bf16(__uint_as_float(rv[12]), __uint_as_float(rv[13]));
           v1.w = pack_bf16(__uint_as_float(rv[14]), __uint_as_float(rv[15]));
-          const float sc = p.scale;
           k0.x = pack_bf16(__uint_as_float(rk[0]) * sc, __uint_as_float(rk[1]) * sc);
           k0.y = pack_bf16(__uint_as_float(rk[2]) * sc, __uint_as_float(rk[3]) * sc);
           k0.z = pack_bf16(__uint_as_float(rk[4]) * sc, __uint_as_float(rk[5]) * sc);
@@ -384,14 +392,6 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_kernel(const __grid_constant_
           reinterpret_cast<uint4*>(vrow + cc * 16)[1] = v1;
           reinterpret_cast<uint4*>(krow + cc * 16)[0] = k0;
           reinterpret_cast<uint4*>(krow + cc * 16)[1] = k1;
-        }
-      } else {
-        // keep the warp converged through the aligned TMEM loads
-#pragma unroll 1
-        for (int cc = 0; cc < D / 16; ++cc) {
-          uint32_t rv[16];
-          tmem_ld16(tdV + lane_off + cc * 16, rv);
-          tmem_ld16(tdK + lane_off + cc * 16, rv);
         }
       }
     }
@@ -441,9 +441,13 @@ int attention_bwd(const AttnBwdShape& sh, const void* qkv, const void* o, const 
   const size_t dq_bytes = (size_t)f.b * f.s * f.H * f.d * 4;
   float* dq_acc = reinterpret_cast<float*>(ws);
   float* Dsum = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + ((dq_bytes + 255) / 256) * 256);
-  if (cudaMemsetAsync(dq_acc, 0, dq_bytes, st) != cudaSuccess) return 3;
-  int rc = attn_dsum(sh, o, dout, Dsum, s_pad, st);
-  if (rc) return rc;
+  int rc;
+  {
+    ProfScope prof(PROF_MISC, 0.0, (double)dq_bytes + 4.0 * f.b * f.s * f.H * f.d + 4.0 * f.b * f.H * s_pad, st);
+    if (cudaMemsetAsync(dq_acc, 0, dq_bytes, st) != cudaSuccess) return 3;
+    rc = attn_dsum(sh, o, dout, Dsum, s_pad, st);
+    if (rc) return rc;
+  }
 
   AttnBwdParams prm;
   memset(&prm, 0, sizeof(prm));
@@ -474,6 +478,10 @@ int attention_bwd(const AttnBwdShape& sh, const void* qkv, const void* o, const 
   prm.err = device_error_word();
   if (!prm.err) return 3;
   const int grid = ((f.s + 127) / 128) * f.Hkv * f.b;
+  {
+  // algorithmic work: S, dP, dV, dK, dQ over the unmasked (query, key) pairs
+  const double pairs = f.causal ? (double)f.s * (f.s + 1) / 2 : (double)f.s * f.s;
+  ProfScope prof(PROF_ATTN_BWD, 10.0 * f.d * pairs * f.H * f.b, 0.0, st);
   switch (f.d) {
     case 64: rc = launch_bwd<64>(prm, grid, st); break;
     case 80: rc = launch_bwd<80>(prm, grid, st); break;
@@ -482,8 +490,10 @@ int attention_bwd(const AttnBwdShape& sh, const void* qkv, const void* o, const 
     case 128: rc = launch_bwd<128>(prm, grid, st); break;
     default: return 5;
   }
+  }
   if (rc) return rc;
   // dQ = scale * accumulated dS K, into the bf16 gradient buffer
+  ProfScope prof(PROF_MISC, 0.0, 6.0 * f.b * f.s * f.H * f.d, st);
   return f32_to_bf16((int64_t)f.b * f.s, (int64_t)f.H * f.d, dq_acc, (int64_t)f.H * f.d,
                      reinterpret_cast<__nv_bfloat16*>(dqkv) + sh.dq_col, sh.ld_dqkv, prm.scale, st);
 }

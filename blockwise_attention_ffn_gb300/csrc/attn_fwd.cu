@@ -22,6 +22,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
+
 #include "attn_common.cuh"
 #include "internal.h"
 
@@ -372,6 +374,10 @@ int attention_fwd(const AttnShape& sh, const void* qkv, void* o, float* lse, cud
   prm.err = device_error_word();
   if (!prm.err) return 3;
   const int grid = prm.n_qt * sh.H * sh.b;
+  // algorithmic work: QK^T and PV over the unmasked (query, key) pairs
+  const double q0 = sh.q_begin, q1 = std::min(sh.q_end, sh.s);
+  const double pairs = sh.causal ? (q1 * (q1 + 1) - q0 * (q0 + 1)) / 2 : (q1 - q0) * sh.s;
+  ProfScope prof(PROF_ATTN_FWD, 4.0 * sh.d * pairs * sh.H * sh.b, 0.0, st);
   switch (sh.d) {
     case 64: return launch_fwd<64>(prm, grid, st);
     case 80: return launch_fwd<80>(prm, grid, st);

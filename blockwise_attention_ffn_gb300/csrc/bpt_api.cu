@@ -120,7 +120,7 @@ size_t plan_fwd(const Dims& D, void* base, FwdWs* w, bool need_lse) {
   w->xn = c.take(D.rows * D.h * 2);
   w->qkv = c.take(D.rows * D.qkv_w * 2);
   w->o = c.take((D.chunked ? D.rows : D.cf) * D.H * D.d * 2);
-  w->x1 = c.take(D.cf * D.h * 2);
+  w->x1 = c.take(D.cf * D.h * 4);  // fp32 residual stream
   w->x1n = c.take(D.cf * D.h * 2);
   w->a = c.take(D.cf * D.f * 2);
   w->lse = reinterpret_cast<float*>(need_lse ? c.take(D.b * D.H * D.s_pad * 4) : nullptr);
@@ -129,7 +129,7 @@ size_t plan_fwd(const Dims& D, void* base, FwdWs* w, bool need_lse) {
 
 struct BwdWs {
   void *xn, *qkv, *o, *x1, *x1n, *z, *g, *u, *a, *dz, *dx1n, *dx1, *dO, *dqkv, *attn;
-  float* dxn;
+  float *dxn, *dx1f;
 };
 AttnBwdShape stage_bwd_shape(const Dims& D, int64_t k);
 size_t plan_bwd(const Dims& D, void* base, BwdWs* w) {
@@ -139,7 +139,7 @@ size_t plan_bwd(const Dims& D, void* base, BwdWs* w) {
   w->xn = c.take(D.rows * D.h * 2);
   w->qkv = c.take(D.rows * D.qkv_w * 2);
   w->o = c.take(D.rows * D.H * D.d * 2);
-  w->x1 = c.take(D.cf * D.h * 2);
+  w->x1 = c.take(D.cf * D.h * 4);  // fp32 residual stream
   w->x1n = c.take(D.cf * D.h * 2);
   w->z = c.take(D.cf * D.f * 2);   // GeLU: pre-activation; SwiGLU: gate g
   w->u = c.take(D.cf * D.f * 2);   // SwiGLU: up u
@@ -148,6 +148,7 @@ size_t plan_bwd(const Dims& D, void* base, BwdWs* w) {
   w->dz = c.take(D.cf * D.f * 2 * 2);  // GeLU: dz [cf, f]; SwiGLU: [dg | du] [cf, 2f]
   w->dx1n = c.take(D.cf * D.h * 2);
   w->dx1 = c.take(D.rows * D.h * 2);
+  w->dx1f = reinterpret_cast<float*>(c.take(D.rows * D.h * 4));  // fp32 copy for the final residual sum
   w->dO = c.take(D.rows * D.H * D.d * 2);
   w->dqkv = c.take(D.rows * D.qkv_w * 2);
   w->dxn = reinterpret_cast<float*>(c.take(D.rows * D.h * 4));
@@ -326,8 +327,7 @@ int bpt_layer_fwd(const bpt_config* cfg, const bpt_weights* w, const void* x, vo
   const int64_t h = D.h, f = D.f, Hd = D.H * D.d;
 
   // N1 over the whole sequence
-  if ((rc = norm_fwd(D.rows, (int)h, cfg->norm, cfg->norm_eps, x, h, w->ln1_w, w->ln1_b, W.xn, h, nullptr,
-                     nullptr, st)))
+  if ((rc = norm_fwd(D.rows, (int)h, cfg->norm, cfg->norm_eps, x, 0, h, w->ln1_w, w->ln1_b, W.xn, h, st)))
     return rc;
   if (D.chunked) {
     for (int64_t k = 0; k < D.n_stages; ++k) {
@@ -362,6 +362,7 @@ int bpt_layer_fwd(const bpt_config* cfg, const bpt_weights* w, const void* x, vo
         MatView A{oblk, nr, Hd, Hd};
         MatView B{w->wo, h, Hd, Hd};
         Epilogue e;
+        e.kind = EPI_F32;  // x1 stays fp32: the residual stream is rounded once, at y
         e.out = W.x1;
         e.ldo = h;
         e.bias = hb ? w->bo : nullptr;
@@ -369,8 +370,7 @@ int bpt_layer_fwd(const bpt_config* cfg, const bpt_weights* w, const void* x, vo
         e.ldr = h;
         if ((rc = gemm(nr, h, Hd, A, false, &B, &Hd, 1, false, nullptr, e, st))) return rc;
       }
-      if ((rc = norm_fwd(nr, (int)h, cfg->norm, cfg->norm_eps, W.x1, h, w->ln2_w, w->ln2_b, W.x1n, h, nullptr,
-                         nullptr, st)))
+      if ((rc = norm_fwd(nr, (int)h, cfg->norm, cfg->norm_eps, W.x1, 1, h, w->ln2_w, w->ln2_b, W.x1n, h, st)))
         return rc;
       // a = act(x1n W1^T + b1)  or  silu(x1n W1^T) * (x1n W3^T)
       {
@@ -399,6 +399,7 @@ int bpt_layer_fwd(const bpt_config* cfg, const bpt_weights* w, const void* x, vo
         e.ldo = h;
         e.bias = hb ? w->b2 : nullptr;
         e.res = W.x1;
+        e.res_f32 = 1;
         e.ldr = h;
         if ((rc = gemm(nr, h, f, A, false, &B, &f, 1, false, nullptr, e, st))) return rc;
       }
@@ -508,8 +509,7 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
   }
 
   // ---- recompute N1, Q/K/V and attention (the saved LSE is not rewritten)
-  if ((rc = norm_fwd(D.rows, (int)h, cfg->norm, cfg->norm_eps, x, h, w->ln1_w, w->ln1_b, W.xn, h, nullptr,
-                     nullptr, st)))
+  if ((rc = norm_fwd(D.rows, (int)h, cfg->norm, cfg->norm_eps, x, 0, h, w->ln1_w, w->ln1_b, W.xn, h, st)))
     return rc;
   for (int64_t k = 0; k < D.n_stages; ++k) {
     if ((rc = stage_qkv(D, w, hb, W.xn, W.qkv, k, st))) return rc;
@@ -528,6 +528,7 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
         MatView A{bf(W.o, row * Hd), nr, Hd, Hd};
         MatView B{w->wo, h, Hd, Hd};
         Epilogue e;
+        e.kind = EPI_F32;  // x1 stays fp32: the residual stream is rounded once, at y
         e.out = W.x1;
         e.ldo = h;
         e.bias = hb ? w->bo : nullptr;
@@ -535,8 +536,7 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
         e.ldr = h;
         if ((rc = gemm(nr, h, Hd, A, false, &B, &Hd, 1, false, nullptr, e, st))) return rc;
       }
-      if ((rc = norm_fwd(nr, (int)h, cfg->norm, cfg->norm_eps, W.x1, h, w->ln2_w, w->ln2_b, W.x1n, h, nullptr,
-                         nullptr, st)))
+      if ((rc = norm_fwd(nr, (int)h, cfg->norm, cfg->norm_eps, W.x1, 1, h, w->ln2_w, w->ln2_b, W.x1n, h, st)))
         return rc;
       {
         MatView A{W.x1n, nr, h, h};
@@ -639,11 +639,13 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
           if ((rc = gemm(nr, h, f, A, false, &B, &f, 1, true, nullptr, e, st))) return rc;
         }
       }
-      // dx1 = dy + N2^T(dx1n)
-      if ((rc = norm_bwd(nr, (int)h, cfg->norm, cfg->norm_eps, W.dx1n, 0, h, W.x1, h, w->ln2_w, dyb, h,
-                         bfm(W.dx1, row * h), h, reinterpret_cast<float*>(g->ln2_w),
-                         ln ? reinterpret_cast<float*>(g->ln2_b) : nullptr, st)))
-        return rc;
+      // dx1 = dy + N2^T(dx1n), as bf16 (operand of the next products) and fp32
+      {
+        NormBwdIO io{W.dx1n, 0, h, W.x1, 1, h, dyb, 0, h, bfm(W.dx1, row * h), W.dx1f + row * h, h};
+        if ((rc = norm_bwd(nr, (int)h, cfg->norm, cfg->norm_eps, io, w->ln2_w, reinterpret_cast<float*>(g->ln2_w),
+                           ln ? reinterpret_cast<float*>(g->ln2_b) : nullptr, st)))
+          return rc;
+      }
       first = false;
     }
   }
@@ -712,9 +714,12 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
   }
 
   // ---- dx = dx1 + N1^T(dxn)
-  if ((rc = norm_bwd(D.rows, (int)h, cfg->norm, cfg->norm_eps, W.dxn, 1, h, x, h, w->ln1_w, W.dx1, h, dx, h,
-                     reinterpret_cast<float*>(g->ln1_w), ln ? reinterpret_cast<float*>(g->ln1_b) : nullptr, st)))
-    return rc;
+  {
+    NormBwdIO io{W.dxn, 1, h, x, 0, h, W.dx1f, 1, h, dx, nullptr, h};
+    if ((rc = norm_bwd(D.rows, (int)h, cfg->norm, cfg->norm_eps, io, w->ln1_w, reinterpret_cast<float*>(g->ln1_w),
+                       ln ? reinterpret_cast<float*>(g->ln1_b) : nullptr, st)))
+      return rc;
+  }
   return BPT_OK;
 }
 

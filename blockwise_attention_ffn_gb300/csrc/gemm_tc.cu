@@ -40,8 +40,9 @@ struct GemmParams {
   void* out3;
   long long ldo3;
   const __nv_bfloat16* bias;
-  const __nv_bfloat16* res;
+  const void* res;
   long long ldr;
+  int res_f32;
   const __nv_bfloat16* aux;
   long long ldaux;
   const __nv_bfloat16* aux2;
@@ -82,6 +83,22 @@ __device__ __forceinline__ void store8_bf16(__nv_bfloat16* p, const float (&v)[8
   *reinterpret_cast<uint4*>(p) = u;
 }
 
+__device__ __forceinline__ void load8_res(const GemmParams& p, int m, int n, float (&v)[8]) {
+  if (p.res_f32) {
+    const float4* r = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.res) + (long long)m * p.ldr + n);
+    const float4 a = r[0], b = r[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+    load8_bf16(reinterpret_cast<const __nv_bfloat16*>(p.res) + (long long)m * p.ldr + n, v);
+  }
+}
+__device__ __forceinline__ float load1_res(const GemmParams& p, int m, int n) {
+  const long long i = (long long)m * p.ldr + n;
+  return p.res_f32 ? reinterpret_cast<const float*>(p.res)[i]
+                   : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.res)[i]);
+}
+
 // Applies the epilogue to 8 consecutive columns n..n+7 of row m (all in range)
 // given the accumulators a (and a second accumulator b for the dual kinds).
 __device__ __forceinline__ void epi8(const GemmParams& p, int m, int n, const float (&a)[8],
@@ -99,7 +116,7 @@ __device__ __forceinline__ void epi8(const GemmParams& p, int m, int n, const fl
       }
       if (p.res) {
         float t[8];
-        load8_bf16(p.res + (long long)m * p.ldr + n, t);
+        load8_res(p, m, n, t);
 #pragma unroll
         for (int j = 0; j < 8; ++j) v[j] += t[j];
       }
@@ -154,8 +171,23 @@ __device__ __forceinline__ void epi8(const GemmParams& p, int m, int n, const fl
     }
     default: {  // EPI_F32
       float* o = reinterpret_cast<float*>(p.out) + (long long)m * p.ldo + n;
-      float4 x0 = make_float4(a[0], a[1], a[2], a[3]);
-      float4 x1 = make_float4(a[4], a[5], a[6], a[7]);
+      float t[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) t[j] = a[j];
+      if (p.bias) {
+        float bb[8];
+        load8_bf16(p.bias + n, bb);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) t[j] += bb[j];
+      }
+      if (p.res) {
+        float rr[8];
+        load8_res(p, m, n, rr);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) t[j] += rr[j];
+      }
+      float4 x0 = make_float4(t[0], t[1], t[2], t[3]);
+      float4 x1 = make_float4(t[4], t[5], t[6], t[7]);
       if (p.beta != 0.f) {
         const float4 o0 = reinterpret_cast<const float4*>(o)[0];
         const float4 o1 = reinterpret_cast<const float4*>(o)[1];
@@ -175,7 +207,7 @@ __device__ __forceinline__ void epi1(const GemmParams& p, int m, int n, float a,
     case EPI_BF16: {
       float v = a;
       if (p.bias) v += __bfloat162float(p.bias[n]);
-      if (p.res) v += __bfloat162float(p.res[(long long)m * p.ldr + n]);
+      if (p.res) v += load1_res(p, m, n);
       reinterpret_cast<__nv_bfloat16*>(p.out)[(long long)m * p.ldo + n] = __float2bfloat16(v);
       break;
     }
@@ -214,7 +246,10 @@ __device__ __forceinline__ void epi1(const GemmParams& p, int m, int n, float a,
     }
     default: {
       float* o = reinterpret_cast<float*>(p.out) + (long long)m * p.ldo + n;
-      *o = a + (p.beta != 0.f ? p.beta * *o : 0.f);
+      float v = a;
+      if (p.bias) v += __bfloat162float(p.bias[n]);
+      if (p.res) v += load1_res(p, m, n);
+      *o = v + (p.beta != 0.f ? p.beta * *o : 0.f);
       break;
     }
   }
@@ -337,7 +372,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     }
   } else {
     // ------------------------------------------------ epilogue (warps 2..5)
-    const bool ok = bounded_wait(acc_full, 0, abort_flag, 105, p.err);
+    // the TMEM loads below are warp-collective, so the decision is too
+    const bool ok = __all_sync(0xffffffffu, bounded_wait(acc_full, 0, abort_flag, 105, p.err));
     tc_fence_after();
     if (ok) {
       const int q = warp & 3;
@@ -445,8 +481,9 @@ int gemm(int64_t M, int64_t N, int64_t K, const MatView& A, bool a_mn, const Mat
   p.out3 = e.out3;
   p.ldo3 = e.ldo3;
   p.bias = reinterpret_cast<const __nv_bfloat16*>(e.bias);
-  p.res = reinterpret_cast<const __nv_bfloat16*>(e.res);
+  p.res = e.res;
   p.ldr = e.ldr;
+  p.res_f32 = e.res_f32;
   p.aux = reinterpret_cast<const __nv_bfloat16*>(e.aux);
   p.ldaux = e.ldaux;
   p.aux2 = reinterpret_cast<const __nv_bfloat16*>(e.aux2);
@@ -454,6 +491,7 @@ int gemm(int64_t M, int64_t N, int64_t K, const MatView& A, bool a_mn, const Mat
   p.beta = e.beta;
   p.err = device_error_word();
   if (!p.err) return 3;
+  ProfScope prof(PROF_GEMM, 2.0 * (double)M * (double)N * (double)K * (dual ? 2 : 1), 0.0, stream);
   if (dual) return launch<128, false, false, true>(p, stream);
   if (!a_mn && !b_mn) return launch<256, false, false, false>(p, stream);
   if (!a_mn && b_mn) return launch<256, false, true, false>(p, stream);

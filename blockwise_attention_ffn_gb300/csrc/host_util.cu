@@ -3,6 +3,11 @@
 #include <cudaTypedefs.h>
 #include <string.h>
 
+#include <mutex>
+#include <vector>
+
+#include "../../include/bpt.h"
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -20,6 +25,41 @@ unsigned int* device_error_word() {
     addr[dev] = reinterpret_cast<unsigned int*>(p);
   }
   return addr[dev];
+}
+
+namespace {
+
+struct ProfRec {
+  cudaEvent_t a = nullptr, b = nullptr;
+  int kind = 0;
+  double flops = 0, bytes = 0;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof;
+size_t g_prof_used = 0;
+
+}  // namespace
+
+ProfScope::ProfScope(int kind, double flops, double bytes, cudaStream_t s) : slot(-1), st(s) {
+  if (!g_prof_on) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (g_prof_used == g_prof.size()) {
+    ProfRec r;
+    if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) return;
+    g_prof.push_back(r);
+  }
+  slot = (int)g_prof_used++;
+  g_prof[slot].kind = kind;
+  g_prof[slot].flops = flops;
+  g_prof[slot].bytes = bytes;
+  cudaEventRecord(g_prof[slot].a, st);
+}
+
+ProfScope::~ProfScope() {
+  if (slot < 0) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  cudaEventRecord(g_prof[slot].b, st);
 }
 
 namespace {
@@ -99,3 +139,37 @@ int read_device_error(cudaStream_t st, unsigned int out[4]) {
 }
 
 }  // namespace bpt
+
+extern "C" {
+
+int bpt_profile_enable(int on) {
+  std::lock_guard<std::mutex> lk(bpt::g_prof_mu);
+  bpt::g_prof_on = on != 0;
+  bpt::g_prof_used = 0;
+  return BPT_OK;
+}
+
+int bpt_profile_collect(int nkinds, double* ms, double* flops, double* bytes, int* launches) {
+  if (nkinds < 1 || !ms || !flops || !bytes || !launches) return BPT_EINVAL;
+  std::lock_guard<std::mutex> lk(bpt::g_prof_mu);
+  for (int k = 0; k < nkinds; ++k) {
+    ms[k] = flops[k] = bytes[k] = 0;
+    launches[k] = 0;
+  }
+  for (size_t i = 0; i < bpt::g_prof_used; ++i) {
+    auto& r = bpt::g_prof[i];
+    if (cudaEventSynchronize(r.b) != cudaSuccess) return BPT_ECUDA;
+    float t = 0;
+    if (cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) return BPT_ECUDA;
+    if (r.kind < nkinds) {
+      ms[r.kind] += t;
+      flops[r.kind] += r.flops;
+      bytes[r.kind] += r.bytes;
+      launches[r.kind] += 1;
+    }
+  }
+  bpt::g_prof_used = 0;
+  return BPT_OK;
+}
+
+}  // extern "C"

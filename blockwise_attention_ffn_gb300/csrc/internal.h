@@ -8,6 +8,17 @@
 
 namespace bpt {
 
+// ---------------------------------------------------------------- profiling
+// When enabled (bpt_profile_enable), every launch is bracketed by CUDA events
+// on its stream and tagged with its kind and algorithmic work.
+enum ProfKind { PROF_GEMM = 0, PROF_ATTN_FWD = 1, PROF_ATTN_BWD = 2, PROF_NORM = 3, PROF_MISC = 4, PROF_KINDS = 5 };
+struct ProfScope {
+  ProfScope(int kind, double flops, double bytes, cudaStream_t st);
+  ~ProfScope();
+  int slot;
+  cudaStream_t st;
+};
+
 // Device address of this device's error word (4 x u32), or NULL.
 unsigned int* device_error_word();
 int read_device_error(cudaStream_t st, unsigned int out[4]);
@@ -40,7 +51,7 @@ enum EpiKind {
   EPI_SWIGLU = 2,      // dual: out = silu(g) * u; out2 = g, out3 = u (opt) -> bf16
   EPI_GELU_BWD = 3,    // out = acc * gelu'(aux[m, n])                   -> bf16
   EPI_SWIGLU_BWD = 4,  // acc = dA; g = aux, u = aux2: out = dA*u*silu'(g), out2 = dA*silu(g)
-  EPI_F32 = 5,         // out = acc + beta * out                          -> fp32
+  EPI_F32 = 5,         // out = acc (+ bias) (+ res) + beta * out        -> fp32
 };
 
 struct Epilogue {
@@ -53,8 +64,9 @@ struct Epilogue {
   void* out3 = nullptr;
   int64_t ldo3 = 0;
   const void* bias = nullptr;  // bf16 [N]
-  const void* res = nullptr;   // bf16 [M, N] with ldr
+  const void* res = nullptr;   // [M, N] with ldr: bf16, or fp32 when res_f32
   int64_t ldr = 0;
+  int res_f32 = 0;
   const void* aux = nullptr;
   int64_t ldaux = 0;
   const void* aux2 = nullptr;
@@ -98,16 +110,21 @@ int attention_bwd(const AttnBwdShape& sh, const void* qkv, const void* o, const 
                   const void* dout, void* dqkv, void* ws, cudaStream_t st);
 
 // ---------------------------------------------------------------- norms & misc
-// y = norm(x) * w (+ b), rows of width h; mean/rstd (fp32 [rows]) optional.
-int norm_fwd(int64_t rows, int h, int kind, float eps, const void* x, int64_t ldx,
-             const void* w, const void* b, void* y, int64_t ldy, float* rstd, float* mean,
-             cudaStream_t st);
+// y = norm(x) * w (+ b), rows of width h; x is bf16 or (x_f32) fp32; y bf16.
+int norm_fwd(int64_t rows, int h, int kind, float eps, const void* x, int x_f32, int64_t ldx,
+             const void* w, const void* b, void* y, int64_t ldy, cudaStream_t st);
 // dx = res + d/dx norm (given dy, x, w); dw/db partial sums accumulated into
 // the fp32 vectors with atomics (they must be zeroed or hold the running sum).
-// dy may be bf16 (dy_f32 = 0) or fp32 (dy_f32 = 1).
-int norm_bwd(int64_t rows, int h, int kind, float eps, const void* dy, int dy_f32, int64_t lddy,
-             const void* x, int64_t ldx, const void* w, const void* res, int64_t ldres,
-             void* dx, int64_t lddx, float* dw, float* db, cudaStream_t st);
+// dy, x and res are each bf16 or fp32 (the *_f32 flags); dx is written as
+// bf16 and, when dx_f32 is given, also as fp32 (same leading dimension).
+struct NormBwdIO {
+  const void* dy; int dy_f32; int64_t lddy;
+  const void* x; int x_f32; int64_t ldx;
+  const void* res; int res_f32; int64_t ldres;
+  void* dx; float* dx_f32; int64_t lddx;
+};
+int norm_bwd(int64_t rows, int h, int kind, float eps, const NormBwdIO& io, const void* w, float* dw,
+             float* db, cudaStream_t st);
 // out[n] (+)= sum over rows of in[row, n]  (bf16 in, fp32 out)
 int colsum(int64_t rows, int64_t n, const void* in, int64_t ld, float* out, int accumulate,
            cudaStream_t st);

@@ -43,14 +43,20 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// 8 consecutive values of a bf16 or fp32 row
+__device__ __forceinline__ void ld8x(const void* base, int f32, int64_t idx, float (&v)[8]) {
+  if (f32) ld8f(reinterpret_cast<const float*>(base) + idx, v);
+  else ld8(reinterpret_cast<const __nv_bfloat16*>(base) + idx, v);
+}
+
 // mean (LayerNorm) and rstd of one row, reading it twice
-__device__ __forceinline__ void row_stats(const __nv_bfloat16* xr, int h, int kind, float eps,
-                                          float& mean, float& rstd) {
+__device__ __forceinline__ void row_stats(const void* x, int x_f32, int64_t row_off, int h, int kind,
+                                          float eps, float& mean, float& rstd) {
   const int lane = threadIdx.x & 31;
   float s = 0.f;
   for (int c = lane * 8; c < h; c += 256) {
     float v[8];
-    ld8(xr + c, v);
+    ld8x(x, x_f32, row_off + c, v);
 #pragma unroll
     for (int k = 0; k < 8; ++k) s += (kind == 0) ? v[k] : v[k] * v[k];
   }
@@ -60,7 +66,7 @@ __device__ __forceinline__ void row_stats(const __nv_bfloat16* xr, int h, int ki
     float q = 0.f;
     for (int c = lane * 8; c < h; c += 256) {
       float v[8];
-      ld8(xr + c, v);
+      ld8x(x, x_f32, row_off + c, v);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const float t = v[k] - mean;
@@ -75,27 +81,22 @@ __device__ __forceinline__ void row_stats(const __nv_bfloat16* xr, int h, int ki
   }
 }
 
-__global__ void norm_fwd_kernel(int64_t rows, int h, int kind, float eps, const __nv_bfloat16* x,
+__global__ void norm_fwd_kernel(int64_t rows, int h, int kind, float eps, const void* x, int x_f32,
                                 int64_t ldx, const __nv_bfloat16* w, const __nv_bfloat16* b,
-                                __nv_bfloat16* y, int64_t ldy, float* rstd_out, float* mean_out) {
+                                __nv_bfloat16* y, int64_t ldy) {
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
-    const __nv_bfloat16* xr = x + r * ldx;
     float mean, rstd;
-    row_stats(xr, h, kind, eps, mean, rstd);
+    row_stats(x, x_f32, r * ldx, h, kind, eps, mean, rstd);
     for (int c = lane * 8; c < h; c += 256) {
       float v[8], wv[8], bv[8];
-      ld8(xr + c, v);
+      ld8x(x, x_f32, r * ldx + c, v);
       ld8(w + c, wv);
       if (b) ld8(b + c, bv);
 #pragma unroll
       for (int k = 0; k < 8; ++k) v[k] = (v[k] - mean) * rstd * wv[k] + (b ? bv[k] : 0.f);
       st8(y + r * ldy + c, v);
-    }
-    if (lane == 0) {
-      if (rstd_out) rstd_out[r] = rstd;
-      if (mean_out) mean_out[r] = mean;
     }
   }
 }
@@ -103,29 +104,22 @@ __global__ void norm_fwd_kernel(int64_t rows, int h, int kind, float eps, const 
 // dx = res + rstd * (g - mean(g) - xhat * mean(g * xhat))    (LayerNorm)
 //    = res + rstd * (g - xhat * mean(g * xhat))              (RMSNorm)
 // with g = dy * w; dw += sum_rows dy * xhat, db += sum_rows dy.
-__global__ void norm_bwd_kernel(int64_t rows, int h, int kind, float eps, const void* dy_, int dy_f32,
-                                int64_t lddy, const __nv_bfloat16* x, int64_t ldx,
-                                const __nv_bfloat16* w, const __nv_bfloat16* res, int64_t ldres,
-                                __nv_bfloat16* dx, int64_t lddx, float* dw, float* db) {
+__global__ void norm_bwd_kernel(int64_t rows, int h, int kind, float eps, NormBwdIO io,
+                                const __nv_bfloat16* w, float* dw, float* db) {
   extern __shared__ float red[];  // [2h]: dw and db partials of this block
   for (int c = threadIdx.x; c < 2 * h; c += blockDim.x) red[c] = 0.f;
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  auto load_dy = [&](int64_t r, int c, float (&v)[8]) {
-    if (dy_f32) ld8f(reinterpret_cast<const float*>(dy_) + r * lddy + c, v);
-    else ld8(reinterpret_cast<const __nv_bfloat16*>(dy_) + r * lddy + c, v);
-  };
   for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
-    const __nv_bfloat16* xr = x + r * ldx;
     float mean, rstd;
-    row_stats(xr, h, kind, eps, mean, rstd);
+    row_stats(io.x, io.x_f32, r * io.ldx, h, kind, eps, mean, rstd);
     float sg = 0.f, sgx = 0.f;
     for (int c = lane * 8; c < h; c += 256) {
       float v[8], wv[8], gv[8];
-      ld8(xr + c, v);
+      ld8x(io.x, io.x_f32, r * io.ldx + c, v);
       ld8(w + c, wv);
-      load_dy(r, c, gv);
+      ld8x(io.dy, io.dy_f32, r * io.lddy + c, gv);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const float xh = (v[k] - mean) * rstd;
@@ -141,16 +135,21 @@ __global__ void norm_bwd_kernel(int64_t rows, int h, int kind, float eps, const 
     if (kind != 0) sg = 0.f;
     for (int c = lane * 8; c < h; c += 256) {
       float v[8], wv[8], gv[8], rv[8];
-      ld8(xr + c, v);
+      ld8x(io.x, io.x_f32, r * io.ldx + c, v);
       ld8(w + c, wv);
-      load_dy(r, c, gv);
-      if (res) ld8(res + r * ldres + c, rv);
+      ld8x(io.dy, io.dy_f32, r * io.lddy + c, gv);
+      if (io.res) ld8x(io.res, io.res_f32, r * io.ldres + c, rv);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const float xh = (v[k] - mean) * rstd;
-        v[k] = rstd * (gv[k] * wv[k] - sg - xh * sgx) + (res ? rv[k] : 0.f);
+        v[k] = rstd * (gv[k] * wv[k] - sg - xh * sgx) + (io.res ? rv[k] : 0.f);
       }
-      st8(dx + r * lddx + c, v);
+      st8(reinterpret_cast<__nv_bfloat16*>(io.dx) + r * io.lddx + c, v);
+      if (io.dx_f32) {
+        float4* o = reinterpret_cast<float4*>(io.dx_f32 + r * io.lddx + c);
+        o[0] = make_float4(v[0], v[1], v[2], v[3]);
+        o[1] = make_float4(v[4], v[5], v[6], v[7]);
+      }
     }
   }
   __syncthreads();
@@ -230,22 +229,23 @@ int grid_for(int64_t work, int per_block) {
 
 }  // namespace
 
-int norm_fwd(int64_t rows, int h, int kind, float eps, const void* x, int64_t ldx, const void* w,
-             const void* b, void* y, int64_t ldy, float* rstd, float* mean, cudaStream_t st) {
+int norm_fwd(int64_t rows, int h, int kind, float eps, const void* x, int x_f32, int64_t ldx,
+             const void* w, const void* b, void* y, int64_t ldy, cudaStream_t st) {
   if (rows <= 0) return 0;
   const int threads = 256;
+  ProfScope prof(PROF_NORM, 0.0, (double)rows * h * ((x_f32 ? 4 : 2) + 2), st);
   norm_fwd_kernel<<<grid_for(rows, threads / 32), threads, 0, st>>>(
-      rows, h, kind, eps, (const __nv_bfloat16*)x, ldx, (const __nv_bfloat16*)w,
-      (const __nv_bfloat16*)b, (__nv_bfloat16*)y, ldy, rstd, mean);
+      rows, h, kind, eps, x, x_f32, ldx, (const __nv_bfloat16*)w, (const __nv_bfloat16*)b,
+      (__nv_bfloat16*)y, ldy);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 
-int norm_bwd(int64_t rows, int h, int kind, float eps, const void* dy, int dy_f32, int64_t lddy,
-             const void* x, int64_t ldx, const void* w, const void* res, int64_t ldres, void* dx,
-             int64_t lddx, float* dw, float* db, cudaStream_t st) {
+int norm_bwd(int64_t rows, int h, int kind, float eps, const NormBwdIO& io, const void* w, float* dw,
+             float* db, cudaStream_t st) {
   if (rows <= 0) return 0;
   const int threads = 256;
   const size_t smem = (size_t)2 * h * sizeof(float);
+  if (smem > 200 * 1024) return 1;
   if (smem > 48 * 1024) {
     static bool attr = false;
     if (!attr) {
@@ -257,10 +257,11 @@ int norm_bwd(int64_t rows, int h, int kind, float eps, const void* dy, int dy_f3
   }
   int grid = (int)((rows + 7) / 8);
   if (grid > 152 * 2) grid = 152 * 2;
-  norm_bwd_kernel<<<grid, threads, smem, st>>>(rows, h, kind, eps, dy, dy_f32, lddy,
-                                               (const __nv_bfloat16*)x, ldx, (const __nv_bfloat16*)w,
-                                               (const __nv_bfloat16*)res, ldres, (__nv_bfloat16*)dx,
-                                               lddx, dw, db);
+  ProfScope prof(PROF_NORM, 0.0,
+                 (double)rows * h * ((io.dy_f32 ? 4 : 2) + (io.x_f32 ? 4 : 2) + (io.res ? (io.res_f32 ? 4 : 2) : 0) + 2 +
+                                     (io.dx_f32 ? 4 : 0)),
+                 st);
+  norm_bwd_kernel<<<grid, threads, smem, st>>>(rows, h, kind, eps, io, (const __nv_bfloat16*)w, dw, db);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 
@@ -269,6 +270,7 @@ int colsum(int64_t rows, int64_t n, const void* in, int64_t ld, float* out, int 
   if (!accumulate && cudaMemsetAsync(out, 0, n * sizeof(float), st) != cudaSuccess) return 3;
   if (rows <= 0 || n <= 0) return 0;
   const int threads = 128;
+  ProfScope prof(PROF_MISC, 0.0, (double)rows * n * 2, st);
   dim3 grid((unsigned)((n / 8 + threads - 1) / threads), 1);
   int64_t ysplit = (rows + 255) / 256;
   if (ysplit > 128) ysplit = 128;

@@ -8,6 +8,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
+#include <stdio.h>
 
 namespace bpt {
 
@@ -21,6 +22,9 @@ namespace bpt {
 #endif
 
 __device__ __forceinline__ void report_timeout(unsigned int* err, int site) {
+#ifdef BPT_TIMEOUT_PRINT
+  printf("bpt: wait site %d timed out in block %d thread %d\n", site, (int)blockIdx.x, (int)threadIdx.x);
+#endif
   if (atomicCAS(&err[0], 0u, 4u) == 0u) {
     err[1] = (unsigned)site;
     err[2] = blockIdx.x;

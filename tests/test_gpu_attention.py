@@ -30,9 +30,11 @@ def _cfg(b, s, H, Hkv, d, causal):
                        causal=causal)
 
 
-def _qkv(b, s, H, Hkv, d, seed):
+def _qkv(b, s, H, Hkv, d, seed, scale=1.0):
+    """q, k, v ~ N(0, scale^2): in the layer workloads the projections of the
+    normalised input by N(0, 0.02^2) weights have unit scale at h ~ 2500."""
     g = torch.Generator().manual_seed(seed)
-    qkv = torch.randn(b * s, (H + 2 * Hkv) * d, generator=g) * 1.5
+    qkv = torch.randn(b * s, (H + 2 * Hkv) * d, generator=g) * scale
     return qkv.to(torch.bfloat16)
 
 
@@ -45,7 +47,7 @@ def _split(qkv64, b, s, H, Hkv, d):
 def test_attention_forward(shape):
     b, s, H, Hkv, d, causal = shape
     cfg = _cfg(*shape)
-    qkv = _qkv(b, s, H, Hkv, d, seed=s + d)
+    qkv = _qkv(b, s, H, Hkv, d, seed=s + d, scale=1.5)  # peakier softmax than the workloads
     o = torch.zeros(b * s, H * d, dtype=torch.bfloat16, device="cuda")
     sp = bpt.s_pad(cfg)
     lse = torch.zeros(b, H, sp, dtype=torch.float32, device="cuda")
@@ -61,7 +63,7 @@ def test_attention_forward(shape):
             o_ref[bi, :, n], lse_ref[bi, n] = ref.attention_head(q[bi, :, n], k[bi, :, n // G],
                                                                  v[bi, :, n // G], bool(causal))
     assert_close(to64(o).reshape(b, s, H, d), o_ref, "O")
-    assert_close(to64(lse)[:, :, :s], lse_ref, "LSE", max_abs=1e-3, rel_fro=1e-5)
+    assert_close(to64(lse)[:, :, :s], lse_ref, "LSE", max_abs=1e-3, rel_fro=1e-5, bf16_out=False)
 
 
 @pytest.mark.parametrize("shape", SHAPES)
@@ -95,9 +97,9 @@ def test_attention_backward(shape):
             dk[bi, :, n // G] += b_
             dv[bi, :, n // G] += c_
     got = to64(dqkv).reshape(b, s, H + 2 * Hkv, d)
-    assert_close(got[:, :, :H], dq, "dQ")
-    assert_close(got[:, :, H:H + Hkv], dk, "dK")
-    assert_close(got[:, :, H + Hkv:], dv, "dV")
+    assert_close(got[:, :, :H], dq, "dQ", grad=True)
+    assert_close(got[:, :, H:H + Hkv], dk, "dK", grad=True)
+    assert_close(got[:, :, H + Hkv:], dv, "dV", grad=True)
 
 
 def test_identical_keys_give_prefix_mean():

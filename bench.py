@@ -392,6 +392,39 @@ def run_gpu(args, c):
     return 0
 
 
+def run_one_kernel(args, c):
+    """One launch of one component at the workload's shape with a shorter
+    sequence (--seq), for profiler captures of a small case."""
+    import torch
+
+    import blockwise_attention_ffn_gb300 as bpt
+    sc = c.with_(s=args.seq)
+    H, Hk, d, s = sc.n_heads, sc.n_kv_heads, sc.head_dim, sc.s
+    g = torch.Generator(device="cuda").manual_seed(0)
+    qkv = torch.randn(sc.b * s, (H + 2 * Hk) * d, generator=g, device="cuda").to(torch.bfloat16)
+    o = torch.empty(sc.b * s, H * d, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(sc.b, H, bpt.s_pad(sc), dtype=torch.float32, device="cuda")
+    bpt.bpt_attention_fwd(sc, qkv, o, lse)
+    if args.profile_kernel == "attn_bwd":
+        dout = torch.randn(sc.b * s, H * d, generator=g, device="cuda").to(torch.bfloat16)
+        dqkv = torch.empty_like(qkv)
+        ws = bpt.alloc_bytes(bpt.bpt_attention_bwd_workspace_bytes(sc))
+        bpt.bpt_attention_bwd(sc, qkv, o, lse, dout, dqkv, ws)
+    elif args.profile_kernel == "layer":
+        from blockwise_attention_ffn_gb300.synth import make_layer_inputs
+        inp = make_layer_inputs(sc, seed=0, device="cuda", with_dy=True)
+        y = torch.empty_like(inp["x"])
+        saved = bpt.alloc_bytes(bpt.bpt_saved_bytes(sc))
+        ws = bpt.alloc_bytes(max(bpt.bpt_workspace_bytes(sc, 0), bpt.bpt_workspace_bytes(sc, 1)))
+        bpt.bpt_layer_fwd(sc, inp["weights"], inp["x"], y, saved, ws)
+        dx = torch.empty_like(inp["x"])
+        bpt.bpt_layer_bwd(sc, inp["weights"], inp["x"], saved, inp["dy"], dx, bpt.alloc_grads(inp["weights"]), ws)
+    torch.cuda.synchronize()
+    st_, site = bpt.bpt_last_device_error()
+    print(json.dumps({"profile_kernel": args.profile_kernel, "seq": args.seq, "status": st_}))
+    return 0 if st_ == bpt.BPT_OK else 1
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -402,10 +435,15 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=1024,
                     help="positions of the workload the CPU oracle runs per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-kernel", choices=["attn_fwd", "attn_bwd", "layer"], default=None,
+                    help="run one launch of this component (small case for profiler captures)")
+    ap.add_argument("--seq", type=int, default=4096, help="sequence length for --profile-kernel")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     from blockwise_attention_ffn_gb300.presets import PRESETS
     c = PRESETS[args.config]
+    if args.profile_kernel:
+        return run_one_kernel(args, c)
     if args.impl == "reference":
         return run_reference(args, c)
     return run_gpu(args, c)

@@ -6,7 +6,7 @@ device memory and streams.  There is no fallback: if the library is missing
 or fails to load, importing the binding's entry points raises.
 
 Entry points keep the C names: bpt_layer_fwd, bpt_layer_bwd,
-bpt_attn_headchunk, bpt_attention_fwd, bpt_attention_bwd,
+bpt_attn_headchunk, bpt_attention_fwd, bpt_attention_bwd, bpt_attention_bwd_noalloc,
 bpt_workspace_bytes, bpt_saved_bytes, bpt_attention_bwd_workspace_bytes,
 bpt_status_string, bpt_last_device_error, bpt_profile_enable,
 bpt_profile_collect.
@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
         L.bpt_attention_bwd_workspace_bytes.restype = sz
         L.bpt_attention_bwd.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.bpt_attention_bwd.restype = i32
+        L.bpt_attention_bwd_noalloc.argtypes = [cfgp, vp, vp, vp, vp, vp, vp]
+        L.bpt_attention_bwd_noalloc.restype = i32
         L.bpt_status_string.argtypes = [i32]
         L.bpt_status_string.restype = ctypes.c_char_p
         L.bpt_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
@@ -182,6 +184,20 @@ def bpt_attention_bwd(cfg, qkv, o, lse, dout, dqkv, ws, stream=None) -> None:
                                  _ptr(dqkv), _ptr(ws), ws.numel() * ws.element_size(),
                                  _stream(stream))
     _check(rc, "bpt_attention_bwd")
+
+
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
+
+
+def bpt_attention_bwd_noalloc(cfg, qkv, o, lse, dout, dqkv, stream=None) -> None:
+    """bpt_attention_bwd for callers that cannot allocate device memory at
+    call time: the scratch is a fixed array inside the library (at most
+    NOALLOC_SCRATCH_BYTES; larger problems raise BptError with BPT_ENOSPC).
+    Calls that overlap on the GPU share that array and race: serialise them."""
+    c = make_config(cfg)
+    rc = lib().bpt_attention_bwd_noalloc(ctypes.byref(c), _ptr(qkv), _ptr(o), _ptr(lse), _ptr(dout),
+                                         _ptr(dqkv), _stream(stream))
+    _check(rc, "bpt_attention_bwd_noalloc")
 
 
 def bpt_last_device_error(stream=None):

@@ -177,6 +177,31 @@ size_t bpt_attention_bwd_workspace_bytes(const bpt_config* cfg);
 int bpt_attention_bwd(const bpt_config* cfg, const void* qkv, const void* o, const void* lse,
                       const void* dout, void* dqkv, void* ws, size_t ws_bytes, void* stream);
 
+/* The attention backward without any device allocation by the caller.
+ * This entry point has no counterpart in the paper; it exists for callers
+ * that cannot allocate device memory when they call the library: a plugin of
+ * an inference or training engine whose enqueue step runs on a memory plan
+ * fixed in advance, a hot path that cannot afford cudaMalloc/cudaFree and
+ * the device synchronisation they may cause, or a process whose device
+ * memory is owned by another allocator.  Same arguments and results as
+ * bpt_attention_bwd minus the workspace: the scratch it needs (the fp32 dQ
+ * accumulator and the per-row dO.O sums, bpt_attention_bwd_workspace_bytes)
+ * lives in a fixed device array of BPT_NOALLOC_SCRATCH_BYTES compiled into
+ * the library, which every GPU that loads it keeps until the process exits.
+ *  - Returns BPT_ENOSPC, without launching anything, when the problem needs
+ *    more scratch than BPT_NOALLOC_SCRATCH_BYTES (4*b*s*H*d bytes plus
+ *    4*b*H*s_pad, about 64 MiB: e.g. s = 32768 with H*d = 2048 is too big).
+ *  - The first call on a device looks up the array's device address (once
+ *    per device, with that device current); make that first call before
+ *    any stream capture.
+ *  - Every call shares the one array and clears what must start at zero
+ *    itself.  Calls that overlap on the GPU (other streams or host threads
+ *    on the same device) race on it: serialise them.
+ *  - It calls no cudaMalloc, cudaFree or other allocating routine. */
+#define BPT_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+int bpt_attention_bwd_noalloc(const bpt_config* cfg, const void* qkv, const void* o, const void* lse,
+                              const void* dout, void* dqkv, void* stream);
+
 /* Opt-in launch profiler.  bpt_profile_enable(1) makes every later launch
  * of this process record a pair of CUDA events on its stream, tagged with
  * the launch's kind and its algorithmic work (FLOPs for tensor-core kernels,

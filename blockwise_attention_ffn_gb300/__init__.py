@@ -191,8 +191,9 @@ NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 def bpt_attention_bwd_noalloc(cfg, qkv, o, lse, dout, dqkv, stream=None) -> None:
     """bpt_attention_bwd for callers that cannot allocate device memory at
-    call time: the scratch is a fixed array inside the library (at most
-    NOALLOC_SCRATCH_BYTES; larger problems raise BptError with BPT_ENOSPC).
+    call time: the scratch (4*b*H*s_pad bytes of row sums) is a fixed array
+    inside the library (at most NOALLOC_SCRATCH_BYTES; larger problems raise
+    BptError with BPT_ENOSPC).
     Calls that overlap on the GPU share that array and race: serialise them."""
     c = make_config(cfg)
     rc = lib().bpt_attention_bwd_noalloc(ctypes.byref(c), _ptr(qkv), _ptr(o), _ptr(lse), _ptr(dout),

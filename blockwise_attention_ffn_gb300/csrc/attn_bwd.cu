@@ -6,22 +6,24 @@
 // S = Q K^T / sqrt(d), P = softmax(S) = exp(S - LSE), O = P V,
 //   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D) with D = rowsum(dO * O)
 //   (= rowsum(P * dP)),  dQ = dS K / sqrt(d),  dK = dS^T Q / sqrt(d).
-// The rebuild is what "Blockwise Parallel Transformer for Long Context Large
-// Models", section 3.4, "Implementation Details (Figure 3)" describes as
-// remat of each key/value block step in the backward pass.
+// The rebuild is the backward-pass remat of every key/value block step that
+// "Blockwise Parallel Transformer for Long Context Large Models", section
+// 3.4, "Implementation Details (Figure 3)" describes.
 //
-// One CTA = one 128-row key/value tile j of one key/value head g; it loops
-// over the G query heads of the group and, for each, over the query tiles
-// i >= j (causal) or all i.  dK and dV accumulate in TMEM over the whole
-// loop; each dQ_i tile is reduced into an fp32 accumulator in global memory
-// with bulk asynchronous reductions.
-//   warp 0      TMA: K_j, V_j once; Q_i, dO_i, LSE_i, D_i per step
-//   warp 1      MMA issuer: S^T = K Q^T, dP^T = V dO^T, dV += P^T dO,
-//               dK += dS^T Q, dQ = dS K
-//   warps 2..5  one key/value row per thread: P^T and dS^T (bf16) into
-//               shared memory; drain dQ (one query row per thread)
+// Two kernels, neither with atomics:
+//  * dK/dV: one CTA per 128-row key/value tile j of one key/value head; it
+//    loops over the G query heads of the group and their query tiles i >= j
+//    (causal), accumulating dK and dV in TMEM.
+//  * dQ: one CTA per 128-row query tile i of one query head; it loops over
+//    the key/value tiles j <= i, accumulating dQ in TMEM, and writes it once.
+// Both rebuild S and dP (the dQ kernel for its own tile order), so a pair of
+// tiles costs 7 tensor-core products instead of 5; in exchange no partial dQ
+// tile is ever reduced through L2 (in a one-kernel design that traffic is
+// tens of GB per step at s = 32K and bounds the whole backward pass).
 #include <math.h>
 #include <string.h>
+
+#include <algorithm>
 
 #include "attn_common.cuh"
 #include "internal.h"
@@ -38,10 +40,9 @@ struct AttnBwdParams {
   const float* lse;     // [b, H_total, s_pad] at head offset lse_head0
   const float* Dsum;    // [b, H, s_pad]
   int H_total, lse_head0;
-  float* dq_acc;        // [b*s, H*d] fp32
   __nv_bfloat16* dqkv;
   long long ld_dqkv;
-  int dk_col, dv_col;
+  int dq_col, dk_col, dv_col;
   float scale, scale_log2;
   unsigned int* err;
 };
@@ -62,46 +63,71 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// 16 TMEM fp32 columns of this thread's row -> 16 bf16 values (scaled)
+__device__ __forceinline__ void store_row16(__nv_bfloat16* dst, const uint32_t* v, float sc) {
+  uint4 a, b;
+  a.x = pack_bf16(__uint_as_float(v[0]) * sc, __uint_as_float(v[1]) * sc);
+  a.y = pack_bf16(__uint_as_float(v[2]) * sc, __uint_as_float(v[3]) * sc);
+  a.z = pack_bf16(__uint_as_float(v[4]) * sc, __uint_as_float(v[5]) * sc);
+  a.w = pack_bf16(__uint_as_float(v[6]) * sc, __uint_as_float(v[7]) * sc);
+  b.x = pack_bf16(__uint_as_float(v[8]) * sc, __uint_as_float(v[9]) * sc);
+  b.y = pack_bf16(__uint_as_float(v[10]) * sc, __uint_as_float(v[11]) * sc);
+  b.z = pack_bf16(__uint_as_float(v[12]) * sc, __uint_as_float(v[13]) * sc);
+  b.w = pack_bf16(__uint_as_float(v[14]) * sc, __uint_as_float(v[15]) * sc);
+  reinterpret_cast<uint4*>(dst)[0] = a;
+  reinterpret_cast<uint4*>(dst)[1] = b;
+}
+
+// ===========================================================================
+// dK / dV
+// ===========================================================================
+// Warps: 0 TMA, 1 MMA, 2..9 compute.  Compute warp w handles key/value row
+// (w % 4) * 32 + lane (its TMEM lane quarter) and query columns
+// [64 * grp, 64 * grp + 64) with grp = (w - 2) / 4, so every row is shared by
+// two warps and each sub-partition runs two compute warps.
+// TMEM: S^T [0,128), dP^T [128,256), dV [256, 256+D), dK [256+D, 256+2D).
+// Per step t (query tile i of query head hn):
+//   MMA: [P^T(t) in smem] dV(t); [S^T columns read] S(t+1); [dS^T(t) in smem]
+//        dP(t+1), dK(t)
+//   compute: S^T(t) -> P^T (kept in registers, bf16 copy to smem), release
+//        the S^T columns; dP^T(t) -> dS^T = P^T (dP^T - D) to smem.
+// So S(t+1) runs while the compute warps form dS^T(t), and dP(t+1) and dK(t)
+// run while they form P^T(t+1).
 template <int D>
-struct BwdCfg {
+struct DkdvCfg {
   using T = TileGeom<D>;
-  static constexpr int QS = (D >= 112) ? 1 : 2;
-  static constexpr bool DQ_SEP = (256 + 3 * D) <= 512;  // dQ has its own TMEM columns
+  static constexpr int QS = (D <= 96) ? 2 : 1;
   static constexpr int STAGE = 2 * T::TILE + 2 * 512;  // Q, dO, LSE, D
   static constexpr int SMEM = 2 * T::TILE + QS * STAGE + 2 * SqTile::BYTES + 1024 + 256;
 };
 
 template <int D>
-__global__ void __launch_bounds__(192, 1) attn_bwd_kernel(const __grid_constant__ AttnBwdParams p) {
+__global__ void __launch_bounds__(320, 1) attn_dkdv_kernel(const __grid_constant__ AttnBwdParams p) {
   using T = TileGeom<D>;
-  constexpr int QS = BwdCfg<D>::QS;
-  constexpr bool DQ_SEP = BwdCfg<D>::DQ_SEP;
-  constexpr int STAGE = BwdCfg<D>::STAGE;
-  constexpr uint32_t ID_SQ = idesc_bf16(128, 128, false, false);  // S^T, dP^T
-  constexpr uint32_t ID_KV = idesc_bf16(128, D, false, true);     // dV, dK
-  constexpr uint32_t ID_DQ = idesc_bf16(128, D, true, true);      // dQ
+  constexpr int QS = DkdvCfg<D>::QS;
+  constexpr int STAGE = DkdvCfg<D>::STAGE;
+  constexpr uint32_t ID_SQ = idesc_bf16(128, 128, false, false);
+  constexpr uint32_t ID_KV = idesc_bf16(128, D, false, true);
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem;
   uint8_t* sV = sK + T::TILE;
   uint8_t* sStage = sV + T::TILE;
-  uint8_t* sP = sStage + QS * STAGE;       // P^T tile, then dS^T tile; both reused for dQ staging
+  uint8_t* sP = sStage + QS * STAGE;
   uint8_t* sDS = sP + SqTile::BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sDS + SqTile::BYTES);
   uint64_t* kv_full = bars;
   uint64_t* qdo_full = bars + 1;
   uint64_t* qdo_empty = qdo_full + QS;
-  uint64_t* s_full = qdo_empty + QS;
-  uint64_t* s_free = s_full + 1;
-  uint64_t* dp_full = s_free + 1;
-  uint64_t* dp_free = dp_full + 1;
-  uint64_t* p_full = dp_free + 1;
-  uint64_t* ds_full = p_full + 1;
-  uint64_t* dq_full = ds_full + 1;
-  uint64_t* dq_free = dq_full + 1;
-  uint64_t* grp = dq_free + 1;  // compute-warp group barrier
-  uint64_t* drain = grp + 1;
+  uint64_t* s_full = qdo_empty + QS;  // S^T(t) in TMEM
+  uint64_t* dp_full = s_full + 1;     // dP^T(t) in TMEM
+  uint64_t* p_full = dp_full + 1;     // P^T(t) in smem (8 arrivals)
+  uint64_t* s_free = p_full + 1;      // S^T columns read (8 arrivals)
+  uint64_t* pds_full = s_free + 1;    // dS^T(t) in smem, dP^T columns read (8)
+  uint64_t* p_used = pds_full + 1;    // dV(t) done
+  uint64_t* it_done = p_used + 1;     // dK(t) done
+  uint64_t* drain = it_done + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
@@ -123,14 +149,12 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_kernel(const __grid_constant_
       mbar_init(&qdo_empty[i], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(s_free, 4);
     mbar_init(dp_full, 1);
-    mbar_init(dp_free, 4);
-    mbar_init(p_full, 4);
-    mbar_init(ds_full, 4);
-    mbar_init(dq_full, 1);
-    mbar_init(dq_free, 4);
-    mbar_init(grp, 4);
+    mbar_init(p_full, 8);
+    mbar_init(s_free, 8);
+    mbar_init(pds_full, 8);
+    mbar_init(p_used, 1);
+    mbar_init(it_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -147,11 +171,10 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_kernel(const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const uint32_t tS = tmem;               // S^T, 128 columns
-  const uint32_t tdP = tmem + 128;        // dP^T, 128 columns
-  const uint32_t tdV = tmem + 256;        // D columns
-  const uint32_t tdK = tmem + 256 + D;    // D columns
-  const uint32_t tdQ = DQ_SEP ? tmem + 256 + 2 * D : tmem;  // D columns
+  const uint32_t tS = tmem;
+  const uint32_t tdP = tmem + 128;
+  const uint32_t tdV = tmem + 256;
+  const uint32_t tdK = tmem + 256 + D;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -165,7 +188,7 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_kernel(const __grid_constant_
       int issued = 0;
       for (int t = 0; t < T_iter; ++t) {
         const int st = t % QS;
-        if (t >= QS && !bounded_wait(&qdo_empty[st], ((t / QS) & 1) ^ 1, abort_flag, 301, p.err)) break;
+        if (t >= QS && !bounded_wait(&qdo_empty[st], ((t / QS) & 1) ^ 1, abort_flag, 501, p.err)) break;
         const int hn = g * p.G + t / n_i;
         const int i = i0 + t % n_i;
         uint8_t* sQ = sStage + st * STAGE;
@@ -183,9 +206,9 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_kernel(const __grid_constant_
         issued = t + 1;
       }
       if (*abort_flag) {
-        bounded_wait(kv_full, 0, abort_flag, 302, p.err);
+        mbar_try_wait(kv_full, 0);
         for (int t = (issued > QS ? issued - QS : 0); t < issued; ++t)
-          mbar_try_wait(&qdo_full[t % QS], (t / QS) & 1);
+          bounded_wait(&qdo_full[t % QS], (t / QS) & 1, abort_flag, 502, p.err);
       }
     }
   } else if (warp == 1) {
@@ -193,206 +216,415 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_kernel(const __grid_constant_
       // ------------------------------------------------ MMA issuer
       const uint32_t uK = smem_u32(sK), uV = smem_u32(sV);
       const uint32_t uP = smem_u32(sP), uDS = smem_u32(sDS);
-      bool ok = bounded_wait(kv_full, 0, abort_flag, 311, p.err);
-      for (int t = 0; ok && t < T_iter; ++t) {
-        const int st = t % QS;
-        const uint32_t uQ = smem_u32(sStage + st * STAGE);
-        const uint32_t udO = uQ + T::TILE;
-        if (!bounded_wait(&qdo_full[st], (t / QS) & 1, abort_flag, 312, p.err)) { ok = false; break; }
-        if (t >= 1) {
-          if (DQ_SEP) {
-            if (!bounded_wait(s_free, (t - 1) & 1, abort_flag, 313, p.err)) { ok = false; break; }
-          } else {
-            if (!bounded_wait(dq_free, (t - 1) & 1, abort_flag, 314, p.err)) { ok = false; break; }
-          }
-        }
-        tc_fence_after();
+      auto stage_u = [&](int t) { return smem_u32(sStage + (t % QS) * STAGE); };
+      auto issue_s = [&](int t) {
+        const uint32_t uQ = stage_u(t);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) umma_bf16(tS, T::kmajor(uK, kk), T::kmajor(uQ, kk), ID_SQ, kk > 0);
         umma_commit(s_full);
-        if (t >= 1 && !bounded_wait(dp_free, (t - 1) & 1, abort_flag, 315, p.err)) { ok = false; break; }
-        tc_fence_after();
+      };
+      auto issue_dp = [&](int t) {
+        const uint32_t udO = stage_u(t) + T::TILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) umma_bf16(tdP, T::kmajor(uV, kk), T::kmajor(udO, kk), ID_SQ, kk > 0);
         umma_commit(dp_full);
-        // dV += P^T dO
-        if (!bounded_wait(p_full, t & 1, abort_flag, 316, p.err)) { ok = false; break; }
+      };
+      bool ok = bounded_wait(kv_full, 0, abort_flag, 511, p.err) &&
+                bounded_wait(&qdo_full[0], 0, abort_flag, 512, p.err);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        issue_dp(0);
+      }
+      for (int t = 0; ok && t < T_iter; ++t) {
+        const int st = t % QS;
+        const uint32_t uQ = stage_u(t);
+        const uint32_t udO = uQ + T::TILE;
+        const bool more = t + 1 < T_iter;
+        // dV(t) += P^T(t) dO(t)
+        if (!bounded_wait(p_full, t & 1, abort_flag, 513, p.err)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           umma_bf16(tdV, SqTile::kmajor(uP, kk), T::mnmajor(udO, kk), ID_KV, (t > 0 || kk > 0));
-        // dK += dS^T Q
-        if (!bounded_wait(ds_full, t & 1, abort_flag, 317, p.err)) { ok = false; break; }
+        umma_commit(p_used);
+        if (QS == 2 && more) {
+          // S(t+1) as soon as the S^T columns are read
+          if (!bounded_wait(s_free, t & 1, abort_flag, 514, p.err)) { ok = false; break; }
+          if (!bounded_wait(&qdo_full[(t + 1) % QS], ((t + 1) / QS) & 1, abort_flag, 515, p.err)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(t + 1);
+        }
+        if (!bounded_wait(pds_full, t & 1, abort_flag, 516, p.err)) { ok = false; break; }
         tc_fence_after();
+        if (QS == 2 && more) issue_dp(t + 1);
+        // dK(t) += dS^T(t) Q(t)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           umma_bf16(tdK, SqTile::kmajor(uDS, kk), T::mnmajor(uQ, kk), ID_KV, (t > 0 || kk > 0));
         umma_commit(&qdo_empty[st]);
-        // dQ = dS K  (the S^T columns are free: the compute warps read S^T
-        // before they published dS^T)
-        if (DQ_SEP && t >= 1 && !bounded_wait(dq_free, (t - 1) & 1, abort_flag, 318, p.err)) { ok = false; break; }
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_bf16(tdQ, SqTile::mnmajor(uDS, kk), T::mnmajor(uK, kk), ID_DQ, kk > 0);
-        umma_commit(dq_full);
+        umma_commit(it_done);
+        if (QS == 1 && more) {
+          // one Q/dO stage: the next tile loads once dK(t) is done with it
+          if (!bounded_wait(&qdo_full[(t + 1) % QS], ((t + 1) / QS) & 1, abort_flag, 517, p.err)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(t + 1);
+          issue_dp(t + 1);
+        }
       }
       if (!ok) {
         umma_commit(drain);
-        bounded_wait(drain, 0, abort_flag, 319, p.err);
+        bounded_wait(drain, 0, abort_flag, 519, p.err);
       }
     }
   } else {
-    // ------------------------------------------------ compute (warps 2..5)
+    // ------------------------------------------------ compute (warps 2..9)
     const int quarter = warp & 3;
+    const int grp = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
     const int kvp = j * 128 + r;
-    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int c0 = grp * 64;
+    const uint32_t lane_off = ((uint32_t)(quarter * 32) << 16) + c0;
     const float c = p.scale_log2;
     const float LOG2E = 1.4426950408889634f;
     bool ok = true;
     for (int t = 0; t < T_iter; ++t) {
       const int st = t % QS;
-      const int hn = g * p.G + t / n_i;
       const int i = i0 + t % n_i;
-      const int q0 = i * 128;
-      const float* sL = reinterpret_cast<const float*>(sStage + st * STAGE + 2 * T::TILE);
+      const int q0 = i * 128 + c0;
+      const float* sL = reinterpret_cast<const float*>(sStage + st * STAGE + 2 * T::TILE) + c0;
       const float* sDsum = sL + 128;
-      ok = bounded_wait(&qdo_full[st], (t / QS) & 1, abort_flag, 321, p.err) &&
-           bounded_wait(s_full, t & 1, abort_flag, 322, p.err);
+      ok = bounded_wait(&qdo_full[st], (t / QS) & 1, abort_flag, 521, p.err) &&
+           bounded_wait(s_full, t & 1, abort_flag, 522, p.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      float pv[128];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t rr[32];
-        tmem_ld32(tS + lane_off + q4 * 32, rr);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) pv[q4 * 32 + k] = __uint_as_float(rr[k]);
+      const bool edge = (p.causal && kvp > q0) || (q0 + 64 > p.s) || (kvp >= p.s);
+      // phase 1: P^T.  dV(t-1), the last reader of the P^T tile, precedes
+      // S(t) on the tensor pipe, so this wait returns at once.
+      if (t >= 1) {
+        ok = bounded_wait(p_used, (t - 1) & 1, abort_flag, 523, p.err);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       }
+      uint32_t pv[64];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) tmem_ld16_nw(tS + lane_off + q4 * 16, pv + q4 * 16);
+      tmem_wait_ld(pv);
       tc_fence_before();
       __syncwarp();
-      if (DQ_SEP && lane == 0) mbar_arrive(s_free);
-      const bool edge = (p.causal && kvp > q0) || (q0 + 128 > p.s) || (kvp >= p.s);
+      if (lane == 0) mbar_arrive(s_free);
 #pragma unroll
-      for (int k = 0; k < 128; ++k) {
-        float e = ex2(fmaf(pv[k], c, -sL[k] * LOG2E));
+      for (int k = 0; k < 64; k += 8) {
+        const float4 la = *reinterpret_cast<const float4*>(sL + k);
+        const float4 lb = *reinterpret_cast<const float4*>(sL + k + 4);
+        const float lv[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
+        float e[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) e[m] = ex2(fmaf(__uint_as_float(pv[k + m]), c, -lv[m] * LOG2E));
         if (edge) {
-          const int qp = q0 + k;
-          if (qp >= p.s || kvp >= p.s || (p.causal && kvp > qp)) e = 0.f;
-        }
-        pv[k] = e;
-      }
-      // the previous step's dQ bulk reductions must have finished reading the
-      // staging area (it overlaps the P^T / dS^T tiles)
-      bulk_wait_read0();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(grp);
-      ok = bounded_wait(grp, t & 1, abort_flag, 325, p.err);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
 #pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
-        uint4 u;
-        u.x = pack_bf16(pv[ch * 8 + 0], pv[ch * 8 + 1]);
-        u.y = pack_bf16(pv[ch * 8 + 2], pv[ch * 8 + 3]);
-        u.z = pack_bf16(pv[ch * 8 + 4], pv[ch * 8 + 5]);
-        u.w = pack_bf16(pv[ch * 8 + 6], pv[ch * 8 + 7]);
-        *reinterpret_cast<uint4*>(sP + SqTile::off(r, ch)) = u;
+          for (int m = 0; m < 8; ++m) {
+            const int qp = q0 + k + m;
+            if (qp >= p.s || kvp >= p.s || (p.causal && kvp > qp)) e[m] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < 8; ++m) pv[k + m] = __float_as_uint(e[m]);
+        *reinterpret_cast<uint4*>(sP + SqTile::off(r, grp * 8 + k / 8)) =
+            make_uint4(pack_bf16(e[0], e[1]), pack_bf16(e[2], e[3]), pack_bf16(e[4], e[5]), pack_bf16(e[6], e[7]));
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
-
-      ok = bounded_wait(dp_full, t & 1, abort_flag, 323, p.err);
+      // phase 2: dS^T = P^T (dP^T - D), once dK(t-1) released the dS^T tile
+      ok = bounded_wait(dp_full, t & 1, abort_flag, 524, p.err);
+      if (ok && t >= 1) ok = bounded_wait(it_done, (t - 1) & 1, abort_flag, 525, p.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
+      uint32_t dr[64];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t rr[32];
-        tmem_ld32(tdP + lane_off + q4 * 32, rr);
+      for (int q4 = 0; q4 < 4; ++q4) tmem_ld16_nw(tdP + lane_off + q4 * 16, dr + q4 * 16);
+      tmem_wait_ld(dr);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) pv[q4 * 32 + k] *= (__uint_as_float(rr[k]) - sDsum[q4 * 32 + k]);
+      for (int k = 0; k < 64; k += 8) {
+        const float4 da = *reinterpret_cast<const float4*>(sDsum + k);
+        const float4 db = *reinterpret_cast<const float4*>(sDsum + k + 4);
+        const float dv[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
+        float a[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) a[m] = __uint_as_float(pv[k + m]) * (__uint_as_float(dr[k + m]) - dv[m]);
+        *reinterpret_cast<uint4*>(sDS + SqTile::off(r, grp * 8 + k / 8)) =
+            make_uint4(pack_bf16(a[0], a[1]), pack_bf16(a[2], a[3]), pack_bf16(a[4], a[5]), pack_bf16(a[6], a[7]));
       }
       tc_fence_before();
+      fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(dp_free);
+      if (lane == 0) mbar_arrive(pds_full);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, bounded_wait(it_done, (T_iter - 1) & 1, abort_flag, 526, p.err));
+    if (ok) {
+      // group 0 writes dV, group 1 writes dK (TMEM loads by every lane,
+      // stores only for rows inside the sequence)
+      tc_fence_after();
+      const bool valid = kvp < p.s;
+      const uint32_t tsrc = (grp == 0 ? tdV : tdK) + ((uint32_t)(quarter * 32) << 16);
+      __nv_bfloat16* row = p.dqkv + ((long long)bi * p.s + kvp) * p.ld_dqkv +
+                           (grp == 0 ? p.dv_col : p.dk_col) + (long long)g * D;
+      const float sc = grp == 0 ? 1.f : p.scale;
+      uint32_t acc[D];
 #pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
-        uint4 u;
-        u.x = pack_bf16(pv[ch * 8 + 0], pv[ch * 8 + 1]);
-        u.y = pack_bf16(pv[ch * 8 + 2], pv[ch * 8 + 3]);
-        u.z = pack_bf16(pv[ch * 8 + 4], pv[ch * 8 + 5]);
-        u.w = pack_bf16(pv[ch * 8 + 6], pv[ch * 8 + 7]);
-        *reinterpret_cast<uint4*>(sDS + SqTile::off(r, ch)) = u;
+      for (int cc = 0; cc < D / 16; ++cc) tmem_ld16_nw(tsrc + cc * 16, acc + cc * 16);
+      tmem_wait_ld(acc);
+      if (valid) {
+#pragma unroll
+        for (int cc = 0; cc < D / 16; ++cc) store_row16(row + cc * 16, acc + cc * 16, sc);
       }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ===========================================================================
+// dQ
+// ===========================================================================
+// Warps: 0 TMA, 1 MMA, 2..9 compute (query row (w % 4) * 32 + lane, key
+// columns [64 * grp, 64 * grp + 64)).
+// TMEM: S [0,128), dP [128,256), dQ [256, 256+D).
+// Per key/value tile j: S = Q K_j^T, dP = dO V_j^T; P = exp(S - LSE) kept in
+// registers, dS = P (dP - D) into smem; dQ += dS K_j.  MMA order per step:
+// [S columns read] S(j+1); [dS(j) in smem] dP(j+1), dQ(j).
+template <int D>
+struct DqCfg {
+  using T = TileGeom<D>;
+  static constexpr int KVS = (D <= 96) ? 3 : 2;
+  static constexpr int SMEM = 2 * T::TILE + KVS * 2 * T::TILE + SqTile::BYTES + 1024 + 256;
+};
+
+template <int D>
+__global__ void __launch_bounds__(320, 1) attn_dq_kernel(const __grid_constant__ AttnBwdParams p) {
+  using T = TileGeom<D>;
+  constexpr int KVS = DqCfg<D>::KVS;
+  constexpr uint32_t ID_SQ = idesc_bf16(128, 128, false, false);
+  constexpr uint32_t ID_DQ = idesc_bf16(128, D, false, true);
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sdO = sQ + T::TILE;
+  uint8_t* sKV = sdO + T::TILE;
+  uint8_t* sDS = sKV + KVS * 2 * T::TILE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sDS + SqTile::BYTES);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_empty = kv_full + KVS;
+  uint64_t* s_full = kv_empty + KVS;  // S(j) in TMEM
+  uint64_t* dp_full = s_full + 1;     // dP(j) in TMEM
+  uint64_t* s_free = dp_full + 1;     // S columns read (8 arrivals)
+  uint64_t* ds_full = s_free + 1;     // dS(j) in smem, dP columns read (8)
+  uint64_t* dq_done = ds_full + 1;    // dQ(j) done (dS tile free)
+  uint64_t* drain = dq_done + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+  const int hb = p.H * p.b;
+  const int n_qt = (p.s + 127) / 128;
+  const int i = n_qt - 1 - (int)(blockIdx.x / hb);  // heaviest query tiles first
+  const int n = (blockIdx.x % hb) % p.H;
+  const int bi = (blockIdx.x % hb) / p.H;
+  const int g = n / p.G;
+  const int q0 = i * 128;
+  const int nkv = p.causal ? min(i + 1, n_qt) : n_qt;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int k = 0; k < KVS; ++k) {
+      mbar_init(&kv_full[k], 1);
+      mbar_init(&kv_empty[k], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(s_free, 8);
+    mbar_init(ds_full, 8);
+    mbar_init(dq_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&p.map_qkv);
+    tma_prefetch(&p.map_do);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t tS = tmem;
+  const uint32_t tdP = tmem + 128;
+  const uint32_t tdQ = tmem + 256;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      mbar_expect_tx(q_full, 2 * T::TILE);
+#pragma unroll
+      for (int c = 0; c < T::NCH; ++c) {
+        tma_load_3d(sQ + c * T::CHUNK, &p.map_qkv, q_full, p.q_col + n * D + c * T::CW, q0, bi);
+        tma_load_3d(sdO + c * T::CHUNK, &p.map_do, q_full, p.do_col + n * D + c * T::CW, q0, bi);
+      }
+      int issued = 0;
+      for (int jt = 0; jt < nkv; ++jt) {
+        const int st = jt % KVS;
+        if (jt >= KVS && !bounded_wait(&kv_empty[st], ((jt / KVS) & 1) ^ 1, abort_flag, 601, p.err)) break;
+        uint8_t* sK = sKV + st * 2 * T::TILE;
+        uint8_t* sV = sK + T::TILE;
+        mbar_expect_tx(&kv_full[st], 2 * T::TILE);
+#pragma unroll
+        for (int c = 0; c < T::NCH; ++c) {
+          tma_load_3d(sK + c * T::CHUNK, &p.map_qkv, &kv_full[st], p.k_col + g * D + c * T::CW, jt * 128, bi);
+          tma_load_3d(sV + c * T::CHUNK, &p.map_qkv, &kv_full[st], p.v_col + g * D + c * T::CW, jt * 128, bi);
+        }
+        issued = jt + 1;
+      }
+      if (*abort_flag) {
+        mbar_try_wait(q_full, 0);
+        for (int jt = (issued > KVS ? issued - KVS : 0); jt < issued; ++jt)
+          bounded_wait(&kv_full[jt % KVS], (jt / KVS) & 1, abort_flag, 602, p.err);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      const uint32_t uQ = smem_u32(sQ), udO = smem_u32(sdO);
+      const uint32_t uKV = smem_u32(sKV), uDS = smem_u32(sDS);
+      auto issue_s = [&](int jt) {
+        const uint32_t uK = uKV + (jt % KVS) * 2 * T::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) umma_bf16(tS, T::kmajor(uQ, kk), T::kmajor(uK, kk), ID_SQ, kk > 0);
+        umma_commit(s_full);
+      };
+      auto issue_dp = [&](int jt) {
+        const uint32_t uV = uKV + (jt % KVS) * 2 * T::TILE + T::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) umma_bf16(tdP, T::kmajor(udO, kk), T::kmajor(uV, kk), ID_SQ, kk > 0);
+        umma_commit(dp_full);
+      };
+      bool ok = bounded_wait(q_full, 0, abort_flag, 611, p.err) &&
+                bounded_wait(&kv_full[0], 0, abort_flag, 612, p.err);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        issue_dp(0);
+      }
+      for (int jt = 0; ok && jt < nkv; ++jt) {
+        const bool more = jt + 1 < nkv;
+        if (more) {
+          if (!bounded_wait(s_free, jt & 1, abort_flag, 613, p.err)) { ok = false; break; }
+          if (!bounded_wait(&kv_full[(jt + 1) % KVS], ((jt + 1) / KVS) & 1, abort_flag, 614, p.err)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(jt + 1);
+        }
+        if (!bounded_wait(ds_full, jt & 1, abort_flag, 615, p.err)) { ok = false; break; }
+        tc_fence_after();
+        if (more) issue_dp(jt + 1);
+        // dQ += dS(j) K_j
+        const uint32_t uK = uKV + (jt % KVS) * 2 * T::TILE;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16(tdQ, SqTile::kmajor(uDS, kk), T::mnmajor(uK, kk), ID_DQ, (jt > 0 || kk > 0));
+        umma_commit(&kv_empty[jt % KVS]);
+        umma_commit(dq_done);
+      }
+      if (!ok) {
+        umma_commit(drain);
+        bounded_wait(drain, 0, abort_flag, 619, p.err);
+      }
+    }
+  } else {
+    // ------------------------------------------------ compute (warps 2..9)
+    const int quarter = warp & 3;
+    const int grp = (warp - 2) >> 2;
+    const int r = quarter * 32 + lane;
+    const int qpos = q0 + r;
+    const int c0 = grp * 64;
+    const uint32_t lane_off = ((uint32_t)(quarter * 32) << 16) + c0;
+    const float c = p.scale_log2;
+    // this row's log-sum-exp (base 2) and dO.O sum; rows past s read the
+    // finite filler values and are masked out below
+    const float l2 = p.lse[((long long)bi * p.H_total + p.lse_head0 + n) * p.s_pad + qpos] * 1.4426950408889634f;
+    const float dsum = p.Dsum[((long long)bi * p.H + n) * p.s_pad + qpos];
+    bool ok = true;
+    for (int jt = 0; jt < nkv; ++jt) {
+      ok = bounded_wait(s_full, jt & 1, abort_flag, 621, p.err);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      const int kv0 = jt * 128 + c0;
+      const bool edge = (p.causal && kv0 + 63 > q0) || (kv0 + 64 > p.s) || (qpos >= p.s);
+      // phase 1: P = exp(S - LSE), in registers; then release the S columns
+      uint32_t pv[64];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) tmem_ld16_nw(tS + lane_off + q4 * 16, pv + q4 * 16);
+      tmem_wait_ld(pv);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free);
+#pragma unroll
+      for (int k = 0; k < 64; ++k) {
+        float e = ex2(fmaf(__uint_as_float(pv[k]), c, -l2));
+        if (edge) {
+          const int kp = kv0 + k;
+          if (kp >= p.s || qpos >= p.s || (p.causal && kp > qpos)) e = 0.f;
+        }
+        pv[k] = __float_as_uint(e);
+      }
+      // phase 2: dS = P (dP - D) into smem once dQ(j-1) released the tile
+      ok = bounded_wait(dp_full, jt & 1, abort_flag, 622, p.err);
+      if (ok && jt >= 1) ok = bounded_wait(dq_done, (jt - 1) & 1, abort_flag, 623, p.err);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t dr[64];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) tmem_ld16_nw(tdP + lane_off + q4 * 16, dr + q4 * 16);
+      tmem_wait_ld(dr);
+#pragma unroll
+      for (int k = 0; k < 64; k += 8) {
+        float a[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) a[m] = __uint_as_float(pv[k + m]) * (__uint_as_float(dr[k + m]) - dsum);
+        *reinterpret_cast<uint4*>(sDS + SqTile::off(r, grp * 8 + k / 8)) =
+            make_uint4(pack_bf16(a[0], a[1]), pack_bf16(a[2], a[3]), pack_bf16(a[4], a[5]), pack_bf16(a[6], a[7]));
+      }
+      tc_fence_before();
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full);
-
-      // drain dQ_i: TMEM lane r is query row q0 + r
-      ok = bounded_wait(dq_full, t & 1, abort_flag, 324, p.err);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      tc_fence_after();
-      float* stage = reinterpret_cast<float*>(sP) + r * D;
-#pragma unroll 1
-      for (int cc = 0; cc < D / 16; ++cc) {
-        uint32_t rr[16];
-        tmem_ld16(tdQ + lane_off + cc * 16, rr);
-        float4* dst = reinterpret_cast<float4*>(stage + cc * 16);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          dst[k] = make_float4(__uint_as_float(rr[4 * k]), __uint_as_float(rr[4 * k + 1]),
-                               __uint_as_float(rr[4 * k + 2]), __uint_as_float(rr[4 * k + 3]));
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dq_free);
-      fence_proxy_async_smem();
-      if (q0 + r < p.s) {
-        float* gdst = p.dq_acc + ((long long)bi * p.s + q0 + r) * ((long long)p.H * D) + (long long)hn * D;
-        bulk_reduce_add_f32(gdst, stage, D * 4);
-      }
-      bulk_commit();
     }
-    bulk_wait0();
+    if (ok) ok = __all_sync(0xffffffffu, bounded_wait(dq_done, (nkv - 1) & 1, abort_flag, 624, p.err));
     if (ok) {
-      // dV and dK of this key/value tile: every MMA completed before the last
-      // dq_full phase
+      // the two groups split dQ's 16-column chunks
       tc_fence_after();
-      // the TMEM loads are warp-collective: every lane issues them, only the
-      // stores depend on the row being inside the sequence
-      const bool valid = kvp < p.s;
-      __nv_bfloat16* vrow = p.dqkv + ((long long)bi * p.s + kvp) * p.ld_dqkv + p.dv_col + (long long)g * D;
-      __nv_bfloat16* krow = p.dqkv + ((long long)bi * p.s + kvp) * p.ld_dqkv + p.dk_col + (long long)g * D;
-      const float sc = p.scale;
-#pragma unroll 1
-      for (int cc = 0; cc < D / 16; ++cc) {
-        uint32_t rv[16], rk[16];
-        tmem_ld16(tdV + lane_off + cc * 16, rv);
-        tmem_ld16(tdK + lane_off + cc * 16, rk);
-        if (valid) {
-          uint4 v0, v1, k0, k1;
-          v0.x = pack_bf16(__uint_as_float(rv[0]), __uint_as_float(rv[1]));
-          v0.y = pack_bf16(__uint_as_float(rv[2]), __uint_as_float(rv[3]));
-          v0.z = pack_bf16(__uint_as_float(rv[4]), __uint_as_float(rv[5]));
-          v0.w = pack_bf16(__uint_as_float(rv[6]), __uint_as_float(rv[7]));
-          v1.x = pack_bf16(__uint_as_float(rv[8]), __uint_as_float(rv[9]));
-          v1.y = pack_bf16(__uint_as_float(rv[10]), __uint_as_float(rv[11]));
-          v1.z = pack_bf16(__uint_as_float(rv[12]), __uint_as_float(rv[13]));
-          v1.w = pack_bf16(__uint_as_float(rv[14]), __uint_as_float(rv[15]));
-          k0.x = pack_bf16(__uint_as_float(rk[0]) * sc, __uint_as_float(rk[1]) * sc);
-          k0.y = pack_bf16(__uint_as_float(rk[2]) * sc, __uint_as_float(rk[3]) * sc);
-          k0.z = pack_bf16(__uint_as_float(rk[4]) * sc, __uint_as_float(rk[5]) * sc);
-          k0.w = pack_bf16(__uint_as_float(rk[6]) * sc, __uint_as_float(rk[7]) * sc);
-          k1.x = pack_bf16(__uint_as_float(rk[8]) * sc, __uint_as_float(rk[9]) * sc);
-          k1.y = pack_bf16(__uint_as_float(rk[10]) * sc, __uint_as_float(rk[11]) * sc);
-          k1.z = pack_bf16(__uint_as_float(rk[12]) * sc, __uint_as_float(rk[13]) * sc);
-          k1.w = pack_bf16(__uint_as_float(rk[14]) * sc, __uint_as_float(rk[15]) * sc);
-          reinterpret_cast<uint4*>(vrow + cc * 16)[0] = v0;
-          reinterpret_cast<uint4*>(vrow + cc * 16)[1] = v1;
-          reinterpret_cast<uint4*>(krow + cc * 16)[0] = k0;
-          reinterpret_cast<uint4*>(krow + cc * 16)[1] = k1;
-        }
+      constexpr int NC = D / 16;
+      constexpr int NC0 = (NC + 1) / 2;
+      const int cbeg = grp == 0 ? 0 : NC0, cend = grp == 0 ? NC0 : NC;
+      const bool valid = qpos < p.s;
+      __nv_bfloat16* qrow = p.dqkv + ((long long)bi * p.s + qpos) * p.ld_dqkv + p.dq_col + (long long)n * D;
+      const uint32_t tq = tdQ + ((uint32_t)(quarter * 32) << 16);
+      for (int cc = cbeg; cc < cend; ++cc) {
+        uint32_t v[16];
+        tmem_ld16_nw(tq + cc * 16, v);
+        tmem_wait_ld(v);
+        if (valid) store_row16(qrow + cc * 16, v, p.scale);
       }
     }
   }
@@ -407,17 +639,46 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_kernel(const __grid_constant_
 }
 
 template <int D>
-int launch_bwd(AttnBwdParams& prm, int grid, cudaStream_t st) {
-  constexpr int SMEM = BwdCfg<D>::SMEM;
-  static_assert(SMEM <= 232448, "attention backward tile set exceeds shared memory");
+int launch_dkdv(AttnBwdParams& prm, int grid, cudaStream_t st) {
+  constexpr int SMEM = DkdvCfg<D>::SMEM;
+  static_assert(SMEM <= 232448, "dK/dV tile set exceeds shared memory");
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
+    if (cudaFuncSetAttribute(attn_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
       return 3;
     attr = true;
   }
-  attn_bwd_kernel<D><<<grid, 192, SMEM, st>>>(prm);
+  attn_dkdv_kernel<D><<<grid, 320, SMEM, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
+template <int D>
+int launch_dq(AttnBwdParams& prm, int grid, cudaStream_t st) {
+  constexpr int SMEM = DqCfg<D>::SMEM;
+  static_assert(SMEM <= 232448, "dQ tile set exceeds shared memory");
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(attn_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
+      return 3;
+    attr = true;
+  }
+  attn_dq_kernel<D><<<grid, 320, SMEM, st>>>(prm);
+  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
+template <int D>
+int launch_both(AttnBwdParams& prm, const AttnShape& f, cudaStream_t st) {
+  const double pairs = f.causal ? (double)f.s * (f.s + 1) / 2 : (double)f.s * f.s;
+  int rc;
+  {
+    // S, dP, dV, dK over the unmasked pairs
+    ProfScope prof(PROF_ATTN_BWD, 8.0 * f.d * pairs * f.H * f.b, 0.0, st);
+    rc = launch_dkdv<D>(prm, ((f.s + 127) / 128) * f.Hkv * f.b, st);
+  }
+  if (rc) return rc;
+  // S, dP, dQ (the first two rebuilt once more in the query-major order)
+  ProfScope prof(PROF_ATTN_BWD, 6.0 * f.d * pairs * f.H * f.b, 0.0, st);
+  return launch_dq<D>(prm, ((f.s + 127) / 128) * f.H * f.b, st);
 }
 
 }  // namespace
@@ -426,11 +687,10 @@ int make_attn_map(CUtensorMap* map, const void* qkv, int b, int s, int64_t ld, i
 int attn_dsum(const AttnBwdShape& sh, const void* o, const void* dout, float* Dsum, int s_pad,
               cudaStream_t st);
 
+// workspace: the per-row dO.O sums D [b, H, s_pad] fp32
 size_t attention_bwd_ws_bytes(const AttnBwdShape& sh) {
   const int64_t s_pad = ((int64_t)sh.f.s + 127) / 128 * 128;
-  const size_t dq = (size_t)sh.f.b * sh.f.s * sh.f.H * sh.f.d * 4;
-  const size_t dsum = (size_t)sh.f.b * sh.f.H * s_pad * 4;
-  return ((dq + 255) / 256) * 256 + dsum;
+  return (size_t)sh.f.b * sh.f.H * s_pad * 4;
 }
 
 // lse: [b, H_total, s_pad] fp32 (head offset lse_head0)
@@ -438,13 +698,10 @@ int attention_bwd(const AttnBwdShape& sh, const void* qkv, const void* o, const 
                   const void* dout, void* dqkv, void* ws, cudaStream_t st) {
   const AttnShape& f = sh.f;
   const int s_pad = (f.s + 127) / 128 * 128;
-  const size_t dq_bytes = (size_t)f.b * f.s * f.H * f.d * 4;
-  float* dq_acc = reinterpret_cast<float*>(ws);
-  float* Dsum = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + ((dq_bytes + 255) / 256) * 256);
+  float* Dsum = reinterpret_cast<float*>(ws);
   int rc;
   {
-    ProfScope prof(PROF_MISC, 0.0, (double)dq_bytes + 4.0 * f.b * f.s * f.H * f.d + 4.0 * f.b * f.H * s_pad, st);
-    if (cudaMemsetAsync(dq_acc, 0, dq_bytes, st) != cudaSuccess) return 3;
+    ProfScope prof(PROF_MISC, 0.0, 4.0 * f.b * f.s * f.H * f.d + 4.0 * f.b * f.H * s_pad, st);
     rc = attn_dsum(sh, o, dout, Dsum, s_pad, st);
     if (rc) return rc;
   }
@@ -468,34 +725,23 @@ int attention_bwd(const AttnBwdShape& sh, const void* qkv, const void* o, const 
   prm.Dsum = Dsum;
   prm.H_total = f.H_total;
   prm.lse_head0 = f.lse_head0;
-  prm.dq_acc = dq_acc;
   prm.dqkv = reinterpret_cast<__nv_bfloat16*>(dqkv);
   prm.ld_dqkv = sh.ld_dqkv;
+  prm.dq_col = (int)sh.dq_col;
   prm.dk_col = (int)sh.dk_col;
   prm.dv_col = (int)sh.dv_col;
   prm.scale = 1.f / sqrtf((float)f.d);
   prm.scale_log2 = prm.scale * 1.4426950408889634f;
   prm.err = device_error_word();
   if (!prm.err) return 3;
-  const int grid = ((f.s + 127) / 128) * f.Hkv * f.b;
-  {
-  // algorithmic work: S, dP, dV, dK, dQ over the unmasked (query, key) pairs
-  const double pairs = f.causal ? (double)f.s * (f.s + 1) / 2 : (double)f.s * f.s;
-  ProfScope prof(PROF_ATTN_BWD, 10.0 * f.d * pairs * f.H * f.b, 0.0, st);
   switch (f.d) {
-    case 64: rc = launch_bwd<64>(prm, grid, st); break;
-    case 80: rc = launch_bwd<80>(prm, grid, st); break;
-    case 96: rc = launch_bwd<96>(prm, grid, st); break;
-    case 112: rc = launch_bwd<112>(prm, grid, st); break;
-    case 128: rc = launch_bwd<128>(prm, grid, st); break;
+    case 64: return launch_both<64>(prm, f, st);
+    case 80: return launch_both<80>(prm, f, st);
+    case 96: return launch_both<96>(prm, f, st);
+    case 112: return launch_both<112>(prm, f, st);
+    case 128: return launch_both<128>(prm, f, st);
     default: return 5;
   }
-  }
-  if (rc) return rc;
-  // dQ = scale * accumulated dS K, into the bf16 gradient buffer
-  ProfScope prof(PROF_MISC, 0.0, 6.0 * f.b * f.s * f.H * f.d, st);
-  return f32_to_bf16((int64_t)f.b * f.s, (int64_t)f.H * f.d, dq_acc, (int64_t)f.H * f.d,
-                     reinterpret_cast<__nv_bfloat16*>(dqkv) + sh.dq_col, sh.ld_dqkv, prm.scale, st);
 }
 
 }  // namespace bpt

@@ -1,7 +1,7 @@
 // attn_bwd_noalloc.cu -- bpt_attention_bwd_noalloc: the attention backward
-// with its scratch (the fp32 dQ accumulator and the per-row dO . O sums)
-// in a fixed array compiled into the library, for callers that cannot
-// allocate device memory when they call us.
+// with its scratch (the fp32 per-row dO . O sums) in a fixed array compiled
+// into the library, for callers that cannot allocate device memory when they
+// call us.
 //
 // Who cannot allocate: code that must run with a device-memory plan fixed
 // ahead of time -- an inference or training engine's plugin whose enqueue
@@ -14,8 +14,8 @@
 // that loads this part of the library, for the life of the process.  Every
 // call shares it: two calls that overlap on the GPU (different streams, or
 // different host threads on one device) race on it and produce wrong results,
-// so serialise them.  A call clears what must start at zero (the dQ
-// accumulator) itself; the rest is fully overwritten.
+// so serialise them.  A call fully overwrites the part of the array it uses,
+// so nothing has to start at zero.
 #include <cuda_runtime.h>
 #include <stdint.h>
 

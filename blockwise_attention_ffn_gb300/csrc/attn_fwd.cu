@@ -213,12 +213,13 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       float sv[128];
+      {
+        uint32_t rr[128];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t rr[32];
-        tmem_ld32(tS + lane_off + sb * 128 + q4 * 32, rr);
+        for (int q4 = 0; q4 < 4; ++q4) tmem_ld32_nw(tS + lane_off + sb * 128 + q4 * 32, rr + q4 * 32);
+        tmem_wait_ld(rr);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) sv[q4 * 32 + i] = __uint_as_float(rr[i]);
+        for (int i = 0; i < 128; ++i) sv[i] = __uint_as_float(rr[i]);
       }
       tc_fence_before();
       __syncwarp();
@@ -253,21 +254,12 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
       }
       l_run = l_run * alpha + rs;
 
+      // PV(j-1) must be done before O is rescaled, and PV(j-2) (the last
+      // reader of P buffer sb) before P is overwritten; PV(j-1) covers both.
       if (j > 0) {
         ok = bounded_wait(pv_done, (j - 1) & 1, abort_flag, 222, p.err);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        if (rescale) {
-#pragma unroll 1
-          for (int cc = 0; cc < D / 16; ++cc) {
-            uint32_t ro[16];
-            tmem_ld16(tO + lane_off + cc * 16, ro);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) ro[i] = __float_as_uint(__uint_as_float(ro[i]) * alpha);
-            tmem_st16(tO + lane_off + cc * 16, ro);
-          }
-          tmem_st_wait();
-        }
       }
       // P (bf16) into the swizzled K-major tile of buffer sb
       uint8_t* pb = myP0 + sb * SqTile::BYTES;
@@ -279,6 +271,17 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
         u.z = pack_bf16(sv[ch * 8 + 4], sv[ch * 8 + 5]);
         u.w = pack_bf16(sv[ch * 8 + 6], sv[ch * 8 + 7]);
         *reinterpret_cast<uint4*>(pb + SqTile::off(r, ch)) = u;
+      }
+      if (j > 0 && rescale) {
+        uint32_t ro[D];
+#pragma unroll
+        for (int cc = 0; cc < D / 16; ++cc) tmem_ld16_nw(tO + lane_off + cc * 16, ro + cc * 16);
+        tmem_wait_ld(ro);
+#pragma unroll
+        for (int i = 0; i < D; ++i) ro[i] = __float_as_uint(__uint_as_float(ro[i]) * alpha);
+#pragma unroll
+        for (int cc = 0; cc < D / 16; ++cc) tmem_st16_nw(tO + lane_off + cc * 16, ro + cc * 16);
+        tmem_st_wait();
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -294,10 +297,13 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
       const float inv_l = 1.f / l_run;
       const bool valid = qpos < p.s;
       __nv_bfloat16* orow = p.o + ((long long)bi * p.s + qpos - p.o_row0) * p.ld_o + p.o_col + (long long)n * D;
-#pragma unroll 1
+      uint32_t oall[D];
+#pragma unroll
+      for (int cc = 0; cc < D / 16; ++cc) tmem_ld16_nw(tO + lane_off + cc * 16, oall + cc * 16);
+      tmem_wait_ld(oall);
+#pragma unroll
       for (int cc = 0; cc < D / 16; ++cc) {
-        uint32_t ro[16];
-        tmem_ld16(tO + lane_off + cc * 16, ro);
+        const uint32_t* ro = oall + cc * 16;
         if (valid) {
           uint4 u0, u1;
           u0.x = pack_bf16(__uint_as_float(ro[0]) * inv_l, __uint_as_float(ro[1]) * inv_l);

@@ -171,8 +171,11 @@ int bpt_attention_fwd(const bpt_config* cfg, const void* qkv, void* o, void* lse
  *   qkv, o, lse as produced by bpt_attention_fwd; dout [b*s, H*d] bf16.
  *   dqkv [b*s, (H + 2H_kv)*d] bf16 out (dQ, then dK, then dV; dK/dV summed
  *   over the G query heads of each group).
- *   ws: at least bpt_attention_bwd_workspace_bytes(cfg) bytes (fp32 dQ
- *   accumulator and the per-row dO.O sums). */
+ *   ws: at least bpt_attention_bwd_workspace_bytes(cfg) bytes (the fp32
+ *   per-row dO.O sums, 4*b*H*s_pad bytes).
+ * Two kernels: dK/dV with the key/value tile outermost and dQ with the query
+ * tile outermost, each accumulating in TMEM; no atomics, so the result is
+ * deterministic. */
 size_t bpt_attention_bwd_workspace_bytes(const bpt_config* cfg);
 int bpt_attention_bwd(const bpt_config* cfg, const void* qkv, const void* o, const void* lse,
                       const void* dout, void* dqkv, void* ws, size_t ws_bytes, void* stream);
@@ -184,13 +187,13 @@ int bpt_attention_bwd(const bpt_config* cfg, const void* qkv, const void* o, con
  * fixed in advance, a hot path that cannot afford cudaMalloc/cudaFree and
  * the device synchronisation they may cause, or a process whose device
  * memory is owned by another allocator.  Same arguments and results as
- * bpt_attention_bwd minus the workspace: the scratch it needs (the fp32 dQ
- * accumulator and the per-row dO.O sums, bpt_attention_bwd_workspace_bytes)
+ * bpt_attention_bwd minus the workspace: the scratch it needs (the fp32
+ * per-row dO.O sums, bpt_attention_bwd_workspace_bytes = 4*b*H*s_pad bytes)
  * lives in a fixed device array of BPT_NOALLOC_SCRATCH_BYTES compiled into
  * the library, which every GPU that loads it keeps until the process exits.
  *  - Returns BPT_ENOSPC, without launching anything, when the problem needs
- *    more scratch than BPT_NOALLOC_SCRATCH_BYTES (4*b*s*H*d bytes plus
- *    4*b*H*s_pad, about 64 MiB: e.g. s = 32768 with H*d = 2048 is too big).
+ *    more scratch than BPT_NOALLOC_SCRATCH_BYTES (64 MiB: b*H*s_pad up to
+ *    16M, e.g. 32 heads at s = 512K; 32 heads at s = 1M is too big).
  *  - The first call on a device looks up the array's device address (once
  *    per device, with that device current); make that first call before
  *    any stream capture.

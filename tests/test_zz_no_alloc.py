@@ -45,7 +45,7 @@ def test_noalloc_matches_workspace_entry_point_twice():
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch():
-    big = CFG.with_(s=32768, h=2048, n_heads=16, n_kv_heads=16, head_dim=128)
+    big = CFG.with_(s=1 << 20, h=4096, n_heads=32, n_kv_heads=8, head_dim=128)
     assert bpt.bpt_attention_bwd_workspace_bytes(big) > bpt.NOALLOC_SCRATCH_BYTES
     t = torch.empty(16, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(bpt.BptError) as e:

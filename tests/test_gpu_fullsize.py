@@ -1,0 +1,59 @@
+"""The five workloads at their full sizes, in the launch configuration the bench
+times, against the fp64 oracle:
+
+* forward: 64 sampled output rows (first, last, block boundaries and random
+  rows) computed exactly by the row-sampled oracle;
+* backward (the workloads that have one): an upstream gradient that is the
+  seeded N(0,1) gradient on 64 sampled rows and zero elsewhere, for which the
+  sparse-gradient oracle gives dx and every weight gradient exactly, so all of
+  them are compared element by element.
+"""
+import numpy as np
+import pytest
+import torch
+
+from blockwise_attention_ffn_gb300.presets import PRESETS
+from oracle import sampled
+from tests.gpu_helpers import (ATTN_GRAD_REL_FRO, assert_close, assert_close_grad, device_inputs, run_bwd,
+                               run_fwd, to64)
+from tests.oracle_helpers import inputs_to_oracle, oracle_cfg
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+def _rows(s, seed, n=64):
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, 127, 128, s // 2, s - 2, s - 1]
+    rest = rng.choice(np.arange(2, s - 2), size=n - len(fixed), replace=False)
+    return np.unique(np.concatenate([fixed, rest]))
+
+
+@pytest.mark.parametrize("name", ["c2", "c3", "c4", "c5"])
+def test_forward_sampled_rows(name):
+    cfg = PRESETS[name]
+    inp, dev = device_inputs(cfg, seed=cfg.seed, with_dy=False)
+    y, _ = run_fwd(cfg, dev)
+    rows = _rows(cfg.s, cfg.seed)
+    o = inputs_to_oracle(inp)
+    want = sampled.forward_rows(o["x"], o["W"], oracle_cfg(cfg), rows)
+    got = to64(y[0, torch.as_tensor(rows, device=y.device)])
+    assert_close(got, want, f"{name} y[rows]", rms_scale=True)
+
+
+@pytest.mark.parametrize("name", ["c3", "c4", "c5"])
+def test_backward_sparse_upstream_gradient(name):
+    cfg = PRESETS[name]
+    inp, dev = device_inputs(cfg, seed=cfg.seed)
+    rows = _rows(cfg.s, cfg.seed + 1)
+    mask = torch.zeros(cfg.s, dtype=torch.bool)
+    mask[torch.as_tensor(rows)] = True
+    dy_sparse = inp["dy"].clone()
+    dy_sparse[0, ~mask] = 0
+    _, saved = run_fwd(cfg, dev)
+    dx, grads = run_bwd(cfg, dev, saved, dy=dy_sparse.cuda())
+    o = inputs_to_oracle(inp)
+    dx_ref, g_ref = sampled.backward_sparse_dy(o["x"], o["W"], to64(inp["dy"])[0, rows], rows,
+                                               oracle_cfg(cfg))
+    assert_close(to64(dx)[0], dx_ref, f"{name} dx", grad=True, rel_fro=ATTN_GRAD_REL_FRO)
+    for k, v in g_ref.items():
+        assert_close_grad(to64(grads[k]), v, f"{name} d{k}", name=k)

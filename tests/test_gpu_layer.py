@@ -43,9 +43,9 @@ def test_layer_backward(cfg):
     dx, grads = run_bwd(cfg, dev, saved)
     o = inputs_to_oracle(inp)
     dx_ref, g_ref = ref.layer_backward(o["x"], o["W"], o["dy"], oracle_cfg(cfg))
-    assert_close(to64(dx), dx_ref, "dx")
+    assert_close(to64(dx), dx_ref, "dx", grad=True)
     for k, v in g_ref.items():
-        assert_close_grad(to64(grads[k]), v, f"d{k}")
+        assert_close_grad(to64(grads[k]), v, f"d{k}", name=k)
 
 
 def test_c1_forward_full_oracle():

@@ -676,8 +676,10 @@ int launch_both(AttnBwdParams& prm, const AttnShape& f, cudaStream_t st) {
     rc = launch_dkdv<D>(prm, ((f.s + 127) / 128) * f.Hkv * f.b, st);
   }
   if (rc) return rc;
-  // S, dP, dQ (the first two rebuilt once more in the query-major order)
-  ProfScope prof(PROF_ATTN_BWD, 6.0 * f.d * pairs * f.H * f.b, 0.0, st);
+  // dQ only: the S and dP this kernel rebuilds for its query-major order are
+  // not part of the method's algorithmic work (S, dP, dV, dK, dQ = 2.5x the
+  // forward attention), so they are not credited
+  ProfScope prof(PROF_ATTN_BWD, 2.0 * f.d * pairs * f.H * f.b, 0.0, st);
   return launch_dq<D>(prm, ((f.s + 127) / 128) * f.H * f.b, st);
 }
 

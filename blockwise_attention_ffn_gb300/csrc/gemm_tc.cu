@@ -3,11 +3,13 @@
 // SwiGLU gate/up pair) and fc2, and every backward product (activation
 // gradients and fp32 weight gradients).
 //
-// One CTA computes one 128 x BN tile of C.  Warp roles:
+// Persistent: one CTA per SM walks 128 x BN tiles of C.  Warp roles:
 //   warp 0      TMA producer: K-tiles of A and B into a 4-stage smem ring
 //   warp 1      TMEM owner and single-thread MMA issuer (M=128, N=BN, K=16)
-//   warps 2..5  epilogue: TMEM -> registers (one row per thread) -> fused
-//               bias / residual / activation -> global
+//               into one of two 256-column accumulators
+//   warps 2..9  epilogue: TMEM -> registers (one row per thread, half the
+//               columns per warp) -> fused bias / residual / activation ->
+//               global, overlapped with the next tile's main loop
 // Operands are staged with 128-byte swizzle; K-major tiles are [rows x 64]
 // boxes, MN-major tiles are [64 K-rows x 64] boxes side by side.
 #include <math.h>
@@ -24,7 +26,8 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 
 struct GemmParams {
   CUtensorMap mapA;
@@ -48,6 +51,8 @@ struct GemmParams {
   const __nv_bfloat16* aux2;
   long long ldaux2;
   float beta;
+  int mt, nt, ntiles;  // tile grid
+  int m_fast;          // walk tiles along M first
   unsigned int* err;
 };
 
@@ -255,34 +260,58 @@ __device__ __forceinline__ void epi1(const GemmParams& p, int m, int n, float a,
   }
 }
 
+// Tile origin of persistent work item `tile`.  The walk runs fastest along
+// the dimension of the smaller operand, so the CTAs in flight share that
+// operand in L2 while the larger one streams through once.
+__device__ __forceinline__ void tile_origin(const GemmParams& p, int tile, int bn, int& m0, int& n0) {
+  int mb, nb;
+  if (p.m_fast) {
+    mb = tile % p.mt;
+    nb = tile / p.mt;
+  } else {
+    nb = tile % p.nt;
+    mb = tile / p.nt;
+  }
+  m0 = mb * BM;
+  n0 = nb * bn;
+}
+
 // BN: tile width (columns of C).  DUAL: BN columns of g and BN of u.
+// Persistent: each CTA walks tiles blockIdx.x, blockIdx.x + gridDim.x, ...
+// with two TMEM accumulators, so the epilogue of one tile overlaps the main
+// loop of the next.
 template <int BN, bool A_MN, bool B_MN, bool DUAL>
 __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
   constexpr int B_BYTES = (DUAL ? 2 : 1) * BN * BK * 2;
   constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  constexpr uint32_t TMEM_COLS = (DUAL ? 2 : 1) * BN <= 256 ? 256 : 512;
+  constexpr int ACC_COLS = (DUAL ? 2 : 1) * BN;
+  static_assert(ACC_COLS == 256, "two accumulators must fill the 512 TMEM columns");
+  constexpr uint32_t TMEM_COLS = 512;
   constexpr uint32_t IDESC = idesc_bf16(BM, BN, A_MN, B_MN);
+  constexpr int EPI_COLS = BN / 2;  // columns of one accumulator half per epilogue warp
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
   uint64_t* empty = full + STAGES;
-  uint64_t* acc_full = empty + STAGES;
-  uint64_t* drain = acc_full + 1;
+  uint64_t* acc_full = empty + STAGES;  // [2]
+  uint64_t* acc_empty = acc_full + 2;   // [2]
+  uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = warp_id();
   const int lane = lane_id();
-  const int n0 = blockIdx.x * BN;
-  const int m0 = blockIdx.y * BM;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(acc_full, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], NUM_EPI_WARPS);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -305,88 +334,121 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------ producer
-      int issued = 0;
-      for (int kt = 0; kt < p.nkt; ++kt) {
-        const int s = kt % STAGES;
-        if (kt >= STAGES && !bounded_wait(&empty[s], ((kt / STAGES) & 1) ^ 1, abort_flag, 101, p.err)) break;
-        uint8_t* sa = smem + s * STAGE_BYTES;
-        uint8_t* sb = sa + A_BYTES;
-        mbar_expect_tx(&full[s], STAGE_BYTES);
-        if (!A_MN) {
-          tma_load_2d(sa, &p.mapA, &full[s], kt * BK, m0);
-        } else {
-          tma_load_2d(sa, &p.mapA, &full[s], m0, kt * BK);
-          tma_load_2d(sa + 8192, &p.mapA, &full[s], m0 + 64, kt * BK);
-        }
-        if (DUAL) {
-          tma_load_2d(sb, &p.mapB[0], &full[s], kt * BK, n0);
-          tma_load_2d(sb + BN * BK * 2, &p.mapB[1], &full[s], kt * BK, n0);
-        } else {
-          const int seg = (kt >= p.seg_kt[1]) ? 2 : (kt >= p.seg_kt[0]) ? 1 : 0;
-          const int kl = (kt - (seg == 0 ? 0 : p.seg_kt[seg - 1])) * BK;
-          if (!B_MN) {
-            tma_load_2d(sb, &p.mapB[seg], &full[s], kl, n0);
-          } else {
-#pragma unroll
-            for (int c = 0; c < BN / 64; ++c) tma_load_2d(sb + c * 8192, &p.mapB[seg], &full[s], n0 + c * 64, kl);
+      uint32_t it = 0;  // k-tiles issued, across this CTA's tiles
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.ntiles; tile += gridDim.x) {
+        int m0, n0;
+        tile_origin(p, tile, BN, m0, n0);
+        for (int kt = 0; kt < p.nkt; ++kt) {
+          const int s = it % STAGES;
+          if (it >= STAGES && !bounded_wait(&empty[s], ((it / STAGES) & 1) ^ 1, abort_flag, 101, p.err)) {
+            ok = false;
+            break;
           }
+          uint8_t* sa = smem + s * STAGE_BYTES;
+          uint8_t* sb = sa + A_BYTES;
+          mbar_expect_tx(&full[s], STAGE_BYTES);
+          if (!A_MN) {
+            tma_load_2d(sa, &p.mapA, &full[s], kt * BK, m0);
+          } else {
+            tma_load_2d(sa, &p.mapA, &full[s], m0, kt * BK);
+            tma_load_2d(sa + 8192, &p.mapA, &full[s], m0 + 64, kt * BK);
+          }
+          if (DUAL) {
+            tma_load_2d(sb, &p.mapB[0], &full[s], kt * BK, n0);
+            tma_load_2d(sb + BN * BK * 2, &p.mapB[1], &full[s], kt * BK, n0);
+          } else {
+            const int seg = (kt >= p.seg_kt[1]) ? 2 : (kt >= p.seg_kt[0]) ? 1 : 0;
+            const int kl = (kt - (seg == 0 ? 0 : p.seg_kt[seg - 1])) * BK;
+            if (!B_MN) {
+              tma_load_2d(sb, &p.mapB[seg], &full[s], kl, n0);
+            } else {
+#pragma unroll
+              for (int c = 0; c < BN / 64; ++c) tma_load_2d(sb + c * 8192, &p.mapB[seg], &full[s], n0 + c * 64, kl);
+            }
+          }
+          ++it;
         }
-        issued = kt + 1;
       }
       if (*abort_flag) {
         // let every load this thread issued land before the CTA goes away
-        for (int kt = (issued > STAGES ? issued - STAGES : 0); kt < issued; ++kt)
-          bounded_wait(&full[kt % STAGES], (kt / STAGES) & 1, abort_flag, 102, p.err) ||
-              mbar_try_wait(&full[kt % STAGES], (kt / STAGES) & 1);
+        for (uint32_t j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+          bounded_wait(&full[j % STAGES], (j / STAGES) & 1, abort_flag, 102, p.err) ||
+              mbar_try_wait(&full[j % STAGES], (j / STAGES) & 1);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
       const uint32_t smem_base = smem_u32(smem);
+      uint32_t it = 0;
+      int tc = 0;  // tiles done by this CTA
       bool ok = true;
-      for (int kt = 0; kt < p.nkt; ++kt) {
-        const int s = kt % STAGES;
-        if (!bounded_wait(&full[s], (kt / STAGES) & 1, abort_flag, 103, p.err)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t sa = smem_base + s * STAGE_BYTES;
-        const uint32_t sb = sa + A_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint64_t ad = A_MN ? sdesc(sa + kk * 2048, 8192, 1024, 2) : sdesc(sa + kk * 32, 16, 1024, 2);
-          const uint64_t bd = B_MN ? sdesc(sb + kk * 2048, 8192, 1024, 2) : sdesc(sb + kk * 32, 16, 1024, 2);
-          umma_bf16(tmem, ad, bd, IDESC, (kt | kk) != 0);
-          if (DUAL) {
-            const uint64_t bd2 = sdesc(sb + BN * BK * 2 + kk * 32, 16, 1024, 2);
-            umma_bf16(tmem + BN, ad, bd2, IDESC, (kt | kk) != 0);
-          }
+      for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++tc) {
+        const int acc = tc & 1;
+        // the epilogue must have drained this accumulator's previous tile
+        if (tc >= 2 && !bounded_wait(&acc_empty[acc], ((tc >> 1) - 1) & 1, abort_flag, 106, p.err)) {
+          ok = false;
+          break;
         }
-        umma_commit(&empty[s]);
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(acc * ACC_COLS);
+        for (int kt = 0; kt < p.nkt; ++kt) {
+          const int s = it % STAGES;
+          if (!bounded_wait(&full[s], (it / STAGES) & 1, abort_flag, 103, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_base + s * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = A_MN ? sdesc(sa + kk * 2048, 8192, 1024, 2) : sdesc(sa + kk * 32, 16, 1024, 2);
+            const uint64_t bd = B_MN ? sdesc(sb + kk * 2048, 8192, 1024, 2) : sdesc(sb + kk * 32, 16, 1024, 2);
+            umma_bf16(d, ad, bd, IDESC, (kt | kk) != 0);
+            if (DUAL) {
+              const uint64_t bd2 = sdesc(sb + BN * BK * 2 + kk * 32, 16, 1024, 2);
+              umma_bf16(d + BN, ad, bd2, IDESC, (kt | kk) != 0);
+            }
+          }
+          umma_commit(&empty[s]);
+          ++it;
+        }
+        if (!ok) break;
+        umma_commit(&acc_full[acc]);
       }
-      if (ok) {
-        umma_commit(acc_full);
-      } else {
+      if (!ok) {
         umma_commit(drain);  // wait until nothing issued is still in flight
         bounded_wait(drain, 0, abort_flag, 104, p.err) || mbar_try_wait(drain, 0);
       }
     }
   } else {
-    // ------------------------------------------------ epilogue (warps 2..5)
-    // the TMEM loads below are warp-collective, so the decision is too
-    const bool ok = __all_sync(0xffffffffu, bounded_wait(acc_full, 0, abort_flag, 105, p.err));
-    tc_fence_after();
-    if (ok) {
-      const int q = warp & 3;
-      const int row = q * 32 + lane;
+    // ------------------------------------------------ epilogue (warps 2..9)
+    // warp w reads TMEM lanes 32*(w%4)..+31 (its row quarter) and one half of
+    // the accumulator's columns
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int row = q * 32 + lane;
+    int tc = 0;
+    for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++tc) {
+      const int acc = tc & 1;
+      // the TMEM loads below are warp-collective, so the decision is too
+      const bool ok = __all_sync(0xffffffffu, bounded_wait(&acc_full[acc], (tc >> 1) & 1, abort_flag, 105, p.err));
+      if (!ok) break;
+      tc_fence_after();
+      int m0, n0;
+      tile_origin(p, tile, BN, m0, n0);
       const int m = m0 + row;
-      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
+      const uint32_t tbase = tmem + (uint32_t)(acc * ACC_COLS) + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < EPI_COLS / 32; ++c) {
+        const int col = half * EPI_COLS + c * 32;
         uint32_t ra[32], rb[32];
-        tmem_ld32(tbase + c * 32, ra);
-        if (DUAL) tmem_ld32(tbase + BN + c * 32, rb);
+        tmem_ld32(tbase + col, ra);
+        if (DUAL) tmem_ld32(tbase + BN + col, rb);
         if (m < p.M) {
-          const int nb = n0 + c * 32;
+          const int nb = n0 + col;
           if (nb + 32 <= p.N) {
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
@@ -399,11 +461,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
               epi8(p, m, nb + g * 8, a8, b8);
             }
           } else {
-            for (int j = 0; j < 32 && nb + j < p.N; ++j)
-              epi1(p, m, nb + j, __uint_as_float(ra[j]), DUAL ? __uint_as_float(rb[j]) : 0.f);
+            // unrolled so the accumulators stay in registers
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (nb + j < p.N) epi1(p, m, nb + j, __uint_as_float(ra[j]), DUAL ? __uint_as_float(rb[j]) : 0.f);
           }
         }
       }
+      // this warp's part of the accumulator has been read: hand it back
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
     }
   }
 
@@ -414,7 +482,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
 }
 
 template <int BN, bool A_MN, bool B_MN, bool DUAL>
-int launch(const GemmParams& p, cudaStream_t st) {
+int launch(GemmParams& p, cudaStream_t st) {
   constexpr int B_BYTES = (DUAL ? 2 : 1) * BN * BK * 2;
   constexpr int SMEM = STAGES * (A_BYTES + B_BYTES) + 1024 + 256;
   auto kern = gemm_kernel<BN, A_MN, B_MN, DUAL>;
@@ -424,7 +492,13 @@ int launch(const GemmParams& p, cudaStream_t st) {
       return 3;
     attr_set = true;
   }
-  dim3 grid((p.N + BN - 1) / BN, (p.M + BM - 1) / BM);
+  const int nsm = sm_count();
+  if (nsm <= 0) return 3;
+  p.mt = (p.M + BM - 1) / BM;
+  p.nt = (p.N + BN - 1) / BN;
+  p.ntiles = p.mt * p.nt;
+  p.m_fast = p.M <= p.N;
+  const int grid = p.ntiles < nsm ? p.ntiles : nsm;
   kern<<<grid, NUM_THREADS, SMEM, st>>>(p);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }

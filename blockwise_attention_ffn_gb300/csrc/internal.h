@@ -22,6 +22,8 @@ struct ProfScope {
 // Device address of this device's error word (4 x u32), or NULL.
 unsigned int* device_error_word();
 int read_device_error(cudaStream_t st, unsigned int out[4]);
+// streaming multiprocessors of the current device (0 on error), cached per device
+int sm_count();
 
 // ---------------------------------------------------------------- TMA maps
 // 2-D bf16 (or fp32) tensor map over a row-major matrix view [rows, cols]

@@ -160,22 +160,49 @@ __global__ void norm_bwd_kernel(int64_t rows, int h, int kind, float eps, NormBw
 }
 
 // out[n] += sum_r in[r, n]; 8 columns per thread, rows split over gridDim.y
-__global__ void colsum_kernel(int64_t rows, int64_t n, const __nv_bfloat16* in, int64_t ld, float* out) {
-  const int64_t c = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
-  if (c >= n) return;
-  const int64_t per = (rows + gridDim.y - 1) / gridDim.y;
-  const int64_t r0 = blockIdx.y * per;
-  const int64_t r1 = min(rows, r0 + per);
+// Column sums of a bf16 [rows x n] matrix, added atomically into fp32 out.
+// A block covers 256 columns (8 per lane of a warp) and a band of rows; its 8
+// warps take every 8th row of the band, four rows in flight at a time, and
+// combine their partial sums in shared memory so the block issues one atomic
+// per column.  n and ld are multiples of 8 (16-byte row segments).
+constexpr int COLSUM_WARPS = 8;
+__global__ void __launch_bounds__(32 * COLSUM_WARPS) colsum_kernel(int64_t rows, int64_t n, const __nv_bfloat16* in,
+                                                                   int64_t ld, int64_t band, float* out) {
+  __shared__ float part[COLSUM_WARPS][256 + 4];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t c = (int64_t)blockIdx.x * 256 + lane * 8;
+  const int64_t r0 = (int64_t)blockIdx.y * band;
+  const int64_t r1 = min(rows, r0 + band);
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  for (int64_t r = r0; r < r1; ++r) {
-    float v[8];
-    ld8(in + r * ld + c, v);
+  if (c < n) {
+    int64_t r = r0 + w;
+    for (; r + 3 * COLSUM_WARPS < r1; r += 4 * COLSUM_WARPS) {
+      float v0[8], v1[8], v2[8], v3[8];
+      ld8(in + r * ld + c, v0);
+      ld8(in + (r + COLSUM_WARPS) * ld + c, v1);
+      ld8(in + (r + 2 * COLSUM_WARPS) * ld + c, v2);
+      ld8(in + (r + 3 * COLSUM_WARPS) * ld + c, v3);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) acc[k] += v[k];
+      for (int k = 0; k < 8; ++k) acc[k] += (v0[k] + v1[k]) + (v2[k] + v3[k]);
+    }
+    for (; r < r1; r += COLSUM_WARPS) {
+      float v[8];
+      ld8(in + r * ld + c, v);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc[k] += v[k];
+    }
   }
 #pragma unroll
-  for (int k = 0; k < 8; ++k)
-    if (c + k < n) atomicAdd(&out[c + k], acc[k]);
+  for (int k = 0; k < 8; ++k) part[w][lane * 8 + k] = acc[k];
+  __syncthreads();
+  const int col = threadIdx.x;  // 256 threads, one column each
+  const int64_t gc = (int64_t)blockIdx.x * 256 + col;
+  if (gc < n) {
+    float t = 0.f;
+#pragma unroll
+    for (int i = 0; i < COLSUM_WARPS; ++i) t += part[i][col];
+    atomicAdd(&out[gc], t);
+  }
 }
 
 __global__ void f32_to_bf16_kernel(int64_t rows, int64_t n, const float* src, int64_t lds,
@@ -269,13 +296,17 @@ int colsum(int64_t rows, int64_t n, const void* in, int64_t ld, float* out, int 
            cudaStream_t st) {
   if (!accumulate && cudaMemsetAsync(out, 0, n * sizeof(float), st) != cudaSuccess) return 3;
   if (rows <= 0 || n <= 0) return 0;
-  const int threads = 128;
   ProfScope prof(PROF_MISC, 0.0, (double)rows * n * 2, st);
-  dim3 grid((unsigned)((n / 8 + threads - 1) / threads), 1);
-  int64_t ysplit = (rows + 255) / 256;
-  if (ysplit > 128) ysplit = 128;
-  grid.y = (unsigned)ysplit;
-  colsum_kernel<<<grid, threads, 0, st>>>(rows, n, (const __nv_bfloat16*)in, ld, out);
+  // about four blocks per SM in all, each band a multiple of the 8 warps' rows
+  const int nsm = sm_count();
+  const int64_t gx = (n + 255) / 256;
+  int64_t gy = (4 * (nsm > 0 ? nsm : 1) + gx - 1) / gx;
+  int64_t band = (rows + gy - 1) / gy;
+  band = (band + COLSUM_WARPS - 1) / COLSUM_WARPS * COLSUM_WARPS;
+  if (band < 4 * COLSUM_WARPS) band = 4 * COLSUM_WARPS;
+  gy = (rows + band - 1) / band;
+  dim3 grid((unsigned)gx, (unsigned)gy);
+  colsum_kernel<<<grid, 32 * COLSUM_WARPS, 0, st>>>(rows, n, (const __nv_bfloat16*)in, ld, band, out);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 

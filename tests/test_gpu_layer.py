@@ -24,7 +24,12 @@ LLAMA_SMALL = LayerConfig(b=1, s=384, h=512, n_heads=8, n_kv_heads=2, head_dim=6
 GPT_B2 = LayerConfig(b=2, s=200, h=256, n_heads=2, n_kv_heads=2, head_dim=128, ffn_dim=512,
                      causal=0, name="gpt b2 noncausal")
 
-LAYERS = [GPT_SMALL, GPT_D80, LLAMA_SMALL, GPT_B2]
+# enough tiles (fc1: 16 x 32 = 512 per FFN block) that every persistent GEMM
+# CTA walks several and reuses both of its TMEM accumulators; ragged in M and N
+GPT_MANY_TILES = LayerConfig(b=1, s=2500, h=384, n_heads=6, n_kv_heads=6, head_dim=64, ffn_dim=8192,
+                             name="gpt many tiles")
+
+LAYERS = [GPT_SMALL, GPT_D80, LLAMA_SMALL, GPT_B2, GPT_MANY_TILES]
 
 
 @pytest.mark.parametrize("cfg", LAYERS, ids=lambda c: c.name)

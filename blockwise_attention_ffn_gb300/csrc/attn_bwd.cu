@@ -133,11 +133,13 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_kernel(const __grid_constant
 
   const int warp = warp_id();
   const int lane = lane_id();
-  const int hb = p.Hkv * p.b;
-  const int j = blockIdx.x / hb;
-  const int g = (blockIdx.x % hb) % p.Hkv;
-  const int bi = (blockIdx.x % hb) / p.Hkv;
+  // head-major, heaviest key tiles (smallest j) of a KV head first, so the
+  // CTAs in flight share that head's Q/dO stream in L2
   const int nq_total = (p.s + 127) / 128;
+  const int pair = blockIdx.x / nq_total;
+  const int j = blockIdx.x % nq_total;
+  const int g = pair % p.Hkv;
+  const int bi = pair / p.Hkv;
   const int i0 = p.causal ? j : 0;
   const int n_i = nq_total - i0;
   const int T_iter = p.G * n_i;
@@ -434,11 +436,13 @@ __global__ void __launch_bounds__(320, 1) attn_dq_kernel(const __grid_constant__
 
   const int warp = warp_id();
   const int lane = lane_id();
-  const int hb = p.H * p.b;
+  // head-major, heaviest query tiles of a head first; the query heads of one
+  // KV group are adjacent, so the CTAs in flight share K/V in L2
   const int n_qt = (p.s + 127) / 128;
-  const int i = n_qt - 1 - (int)(blockIdx.x / hb);  // heaviest query tiles first
-  const int n = (blockIdx.x % hb) % p.H;
-  const int bi = (blockIdx.x % hb) / p.H;
+  const int pair = blockIdx.x / n_qt;
+  const int i = n_qt - 1 - (int)(blockIdx.x % n_qt);
+  const int n = pair % p.H;
+  const int bi = pair / p.H;
   const int g = n / p.G;
   const int q0 = i * 128;
   const int nkv = p.causal ? min(i + 1, n_qt) : n_qt;

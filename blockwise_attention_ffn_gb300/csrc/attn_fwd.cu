@@ -91,12 +91,14 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
   const int warp = warp_id();
   const int lane = lane_id();
 
-  // tile scheduling: heaviest query tiles first, heads of one tile adjacent
-  const int hb = p.H * p.b;
-  const int qt_rev = blockIdx.x / hb;
-  const int rem = blockIdx.x % hb;
-  const int n = rem % p.H;
-  const int bi = rem / p.H;
+  // tile scheduling: head-major, heaviest query tiles of a head first.  The
+  // CTAs in flight then share one or two heads' K/V (10 MB per head at
+  // s=32K, d=80), which stays in L2; tile-major order spread them over every
+  // head and re-read K/V from HBM on each wave.
+  const int pair = blockIdx.x / p.n_qt;
+  const int qt_rev = blockIdx.x % p.n_qt;
+  const int n = pair % p.H;
+  const int bi = pair / p.H;
   const int qt = p.qt_begin + p.n_qt - 1 - qt_rev;
   const int q0 = qt * 128;
   const int g = n / p.G;

@@ -13,7 +13,10 @@
 // Two kernels, neither with atomics:
 //  * dK/dV: one CTA per 128-row key/value tile j of one key/value head; it
 //    loops over the G query heads of the group and their query tiles i >= j
-//    (causal), accumulating dK and dV in TMEM.
+//    (causal), accumulating dK and dV in TMEM.  Head dims 64 and 80 keep
+//    every A operand in TMEM and split the compute warps into a P group and
+//    a dS group; 96 to 128, whose accumulators leave too little TMEM for
+//    that, use one group that forms P and dS in turn.
 //  * dQ: one CTA per 128-row query tile i of one query head; it loops over
 //    the key/value tiles j <= i, accumulating dQ in TMEM, and writes it once.
 // Both rebuild S and dP (the dQ kernel for its own tile order), so a pair of
@@ -39,6 +42,9 @@ struct AttnBwdParams {
   int q_col, k_col, v_col, do_col;
   const float* lse;     // [b, H_total, s_pad] at head offset lse_head0
   const float* Dsum;    // [b, H, s_pad]
+  const float* nl2;     // [b, H, s_pad]: -LSE * log2(e)
+  const __nv_bfloat16* qkv;  // the packed projection (K and V rows read directly)
+  long long ld_qkv;
   int H_total, lse_head0;
   __nv_bfloat16* dqkv;
   long long ld_dqkv;
@@ -393,6 +399,342 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_kernel(const __grid_constant
 }
 
 // ===========================================================================
+// dK / dV with every A operand in TMEM (head dims 64 and 80)
+// ===========================================================================
+// A 128 x 128 product with both operands in shared memory takes the whole
+// shared-memory bandwidth of the SM, and the compute warps' own shared-memory
+// loads then wait behind it.  This variant gives every product at most one
+// shared-memory operand: K and V are copied into TMEM once per CTA and serve
+// as the A operands of S^T = K Q^T and dP^T = V dO^T; P^T is written over
+// S^T and dS^T over dP^T (bf16 pairs), the A operands of dV = P^T dO and
+// dK = dS^T Q.  Shared memory holds only the Q/dO ring.
+// Warps: 0 TMA, 1 MMA, 2..9 compute.  Compute warp w owns key/value rows
+// (w % 4) * 32 + lane (its TMEM lane quarter) and query columns
+// [64h, 64h+64), h = (w - 2) / 4.  Per step it forms P^T for its columns
+// (kept in registers as bf16 pairs and stored over the first 32 of its 64
+// S^T columns), then dS^T (stored over the first 32 of its dP^T columns).
+// TMEM: S^T/P^T [0,128), dP^T/dS^T [128,256), dV [256, 256+D),
+//       dK [256+D, 256+2D), K [256+2D, 256+2.5D), V [256+2.5D, 256+3D).
+// MMA order per step t: dV(t), S(t+1), dK(t), dP(t+1).  A product that
+// overwrites the TMEM operand of the one issued before it relies on the
+// tensor pipe executing one thread's products in issue order.
+template <int D>
+struct DkdvTmCfg {
+  using T = TileGeom<D>;
+  static constexpr int QS = 4;
+  static constexpr int STAGE = 2 * T::TILE + 2 * 512;  // Q, dO, -LSE*log2(e), D
+  static constexpr int SMEM = QS * STAGE + 1024 + 256;
+  static constexpr uint32_t COL_DV = 256, COL_DK = 256 + D, COL_K = 256 + 2 * D, COL_V = 256 + 2 * D + D / 2;
+};
+
+template <int D>
+__global__ void __launch_bounds__(320, 1) attn_dkdv_tm_kernel(const __grid_constant__ AttnBwdParams p) {
+  using T = TileGeom<D>;
+  using C = DkdvTmCfg<D>;
+  constexpr int QS = C::QS;
+  constexpr int STAGE = C::STAGE;
+  static_assert(C::COL_V + D / 2 <= 512, "TMEM columns");
+  constexpr uint32_t ID_SQ = idesc_bf16(128, 128, false, false);
+  constexpr uint32_t ID_KV = idesc_bf16(128, D, false, true);
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sStage = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + QS * STAGE);
+  uint64_t* kv_ready = bars;            // K, V copied into TMEM (8 compute warps)
+  uint64_t* qdo_full = bars + 1;
+  uint64_t* qdo_empty = qdo_full + QS;
+  uint64_t* s_full = qdo_empty + QS;    // S^T(t) in TMEM
+  uint64_t* dp_full = s_full + 1;       // dP^T(t) in TMEM
+  uint64_t* p_full = dp_full + 1;       // P^T(t) written (8 compute warps)
+  uint64_t* p_used = p_full + 1;        // dV(t) done
+  uint64_t* ds_full = p_used + 1;       // dS^T(t) written (8 compute warps)
+  uint64_t* it_done = ds_full + 1;      // dK(t) done
+  uint64_t* drain = it_done + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+  // head-major, heaviest key tiles (smallest j) of a KV head first, so the
+  // CTAs in flight share that head's Q/dO stream in L2
+  const int nq_total = (p.s + 127) / 128;
+  const int pair = blockIdx.x / nq_total;
+  const int j = blockIdx.x % nq_total;
+  const int g = pair % p.Hkv;
+  const int bi = pair / p.Hkv;
+  const int i0 = p.causal ? j : 0;
+  const int n_i = nq_total - i0;
+  const int T_iter = p.G * n_i;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_ready, 8);
+    for (int i = 0; i < QS; ++i) {
+      mbar_init(&qdo_full[i], 1);
+      mbar_init(&qdo_empty[i], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(p_full, 8);
+    mbar_init(p_used, 1);
+    mbar_init(ds_full, 8);
+    mbar_init(it_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&p.map_qkv);
+    tma_prefetch(&p.map_do);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t tS = tmem;
+  const uint32_t tdP = tmem + 128;
+  const uint32_t tdV = tmem + C::COL_DV;
+  const uint32_t tdK = tmem + C::COL_DK;
+  const uint32_t tKA = tmem + C::COL_K;
+  const uint32_t tVA = tmem + C::COL_V;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      int issued = 0;
+      for (int t = 0; t < T_iter; ++t) {
+        const int st = t % QS;
+        if (t >= QS && !bounded_wait(&qdo_empty[st], ((t / QS) & 1) ^ 1, abort_flag, 571, p.err)) break;
+        const int hn = g * p.G + t / n_i;
+        const int i = i0 + t % n_i;
+        uint8_t* sQ = sStage + st * STAGE;
+        uint8_t* sdO = sQ + T::TILE;
+        uint8_t* sL = sdO + T::TILE;
+        mbar_expect_tx(&qdo_full[st], STAGE);
+#pragma unroll
+        for (int c = 0; c < T::NCH; ++c) {
+          tma_load_3d(sQ + c * T::CHUNK, &p.map_qkv, &qdo_full[st], p.q_col + hn * D + c * T::CW, i * 128, bi);
+          tma_load_3d(sdO + c * T::CHUNK, &p.map_do, &qdo_full[st], p.do_col + hn * D + c * T::CW, i * 128, bi);
+        }
+        const long long row = ((long long)bi * p.H + hn) * p.s_pad + i * 128;
+        bulk_load(sL, p.nl2 + row, 512, &qdo_full[st]);
+        bulk_load(sL + 512, p.Dsum + row, 512, &qdo_full[st]);
+        issued = t + 1;
+      }
+      if (*abort_flag) {
+        for (int t = (issued > QS ? issued - QS : 0); t < issued; ++t)
+          bounded_wait(&qdo_full[t % QS], (t / QS) & 1, abort_flag, 572, p.err);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      auto stage_u = [&](int t) { return smem_u32(sStage + (t % QS) * STAGE); };
+      auto issue_s = [&](int t) {
+        const uint32_t uQ = stage_u(t);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a(tS, tKA + kk * 8, T::kmajor(uQ, kk), ID_SQ, kk > 0);
+        umma_commit(s_full);
+      };
+      auto issue_dp = [&](int t) {
+        const uint32_t udO = stage_u(t) + T::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a(tdP, tVA + kk * 8, T::kmajor(udO, kk), ID_SQ, kk > 0);
+        umma_commit(dp_full);
+      };
+      bool ok = bounded_wait(kv_ready, 0, abort_flag, 581, p.err) &&
+                bounded_wait(&qdo_full[0], 0, abort_flag, 582, p.err);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        issue_dp(0);
+      }
+      for (int t = 0; ok && t < T_iter; ++t) {
+        const int st = t % QS;
+        const uint32_t uQ = stage_u(t);
+        const uint32_t udO = uQ + T::TILE;
+        const bool more = t + 1 < T_iter;
+        // dV(t) += P^T(t) dO(t); the P^T pairs of query columns 64h.. sit at
+        // TMEM column 64h
+        if (!bounded_spin(p_full, t & 1, abort_flag, 583, p.err)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16_tmem_a(tdV, tS + (kk >> 2) * 64 + (kk & 3) * 8, T::mnmajor(udO, kk), ID_KV, (t > 0 || kk > 0));
+        umma_commit(p_used);
+        if (more) {
+          // S(t+1) overwrites P^T(t), after dV(t) in issue order
+          if (!bounded_spin(&qdo_full[(t + 1) % QS], ((t + 1) / QS) & 1, abort_flag, 586, p.err)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(t + 1);
+        }
+        // dK(t) += dS^T(t) Q(t)
+        if (!bounded_spin(ds_full, t & 1, abort_flag, 587, p.err)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16_tmem_a(tdK, tdP + (kk >> 2) * 64 + (kk & 3) * 8, T::mnmajor(uQ, kk), ID_KV, (t > 0 || kk > 0));
+        umma_commit(&qdo_empty[st]);
+        umma_commit(it_done);
+        // dP(t+1) overwrites dS^T(t), after dK(t) in issue order
+        if (more) issue_dp(t + 1);
+      }
+      if (!ok) {
+        umma_commit(drain);
+        bounded_wait(drain, 0, abort_flag, 589, p.err);
+      }
+    }
+  } else {
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int r = quarter * 32 + lane;
+    const int kvp = j * 128 + r;
+    const int c0 = half * 64;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    {
+      // K (half 0) or V (half 1) row of this thread into TMEM as bf16 pairs;
+      // rows past the sequence are zero
+      uint32_t w[D / 2];
+      const __nv_bfloat16* src = p.qkv + ((long long)bi * p.s + kvp) * p.ld_qkv + (half ? p.v_col : p.k_col) +
+                                 (long long)g * D;
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (kvp < p.s) v = *reinterpret_cast<const uint4*>(src + c * 8);
+        w[4 * c] = v.x;
+        w[4 * c + 1] = v.y;
+        w[4 * c + 2] = v.z;
+        w[4 * c + 3] = v.w;
+      }
+      const uint32_t dst = (half ? tVA : tKA) + lane_off;
+      tmem_st32(dst, *reinterpret_cast<const uint32_t(*)[32]>(w));
+      if constexpr (D / 2 > 32) tmem_st8_nw(dst + 32, w + 32);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(kv_ready);
+    }
+    const float c = p.scale_log2;
+    bool ok = true;
+    for (int t = 0; t < T_iter; ++t) {
+      const int st = t % QS;
+      const int q0 = (i0 + t % n_i) * 128;
+      const float* sNL = reinterpret_cast<const float*>(sStage + st * STAGE + 2 * T::TILE) + c0;
+      const float* sD = reinterpret_cast<const float*>(sStage + st * STAGE + 2 * T::TILE + 512) + c0;
+      ok = bounded_wait(&qdo_full[st], (t / QS) & 1, abort_flag, 591, p.err) &&
+           bounded_wait(s_full, t & 1, abort_flag, 592, p.err);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      // ---- phase 1: P^T = exp2(S^T * scale*log2(e) - LSE*log2(e)) for the
+      // 64 columns; columns [lo, hi) of this row are unmasked
+      int lo = 0, hi = min(64, p.s - (q0 + c0));
+      if (p.causal) lo = max(0, kvp - (q0 + c0));
+      if (kvp >= p.s) lo = 64;
+      const bool edge = lo > 0 || hi < 64;
+      uint32_t sv[64];
+      tmem_ld32_nw(tS + lane_off + c0, sv);
+      tmem_ld32_nw(tS + lane_off + c0 + 32, sv + 32);
+      tmem_wait_ld(sv);
+      uint32_t pk[32];
+      if (!edge) {
+#pragma unroll
+        for (int k = 0; k < 64; k += 8) {
+          const float4 la = *reinterpret_cast<const float4*>(sNL + k);
+          const float4 lb = *reinterpret_cast<const float4*>(sNL + k + 4);
+          const float nl[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
+#pragma unroll
+          for (int m = 0; m < 4; ++m)
+            pk[k / 2 + m] = pack_bf16(ex2(fmaf(__uint_as_float(sv[k + 2 * m]), c, nl[2 * m])),
+                                      ex2(fmaf(__uint_as_float(sv[k + 2 * m + 1]), c, nl[2 * m + 1])));
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 64; k += 8) {
+          const float4 la = *reinterpret_cast<const float4*>(sNL + k);
+          const float4 lb = *reinterpret_cast<const float4*>(sNL + k + 4);
+          const float nl[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
+          float e[8];
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {
+            e[m] = ex2(fmaf(__uint_as_float(sv[k + m]), c, nl[m]));
+            if (k + m < lo || k + m >= hi) e[m] = 0.f;
+          }
+#pragma unroll
+          for (int m = 0; m < 4; ++m) pk[k / 2 + m] = pack_bf16(e[2 * m], e[2 * m + 1]);
+        }
+      }
+      tmem_st32(tS + lane_off + c0, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+      // ---- phase 2: dS^T = P^T (dP^T - D) with P^T from registers
+      ok = bounded_wait(dp_full, t & 1, abort_flag, 593, p.err);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t dr[64];
+      tmem_ld32_nw(tdP + lane_off + c0, dr);
+      tmem_ld32_nw(tdP + lane_off + c0 + 32, dr + 32);
+      tmem_wait_ld(dr);
+      uint32_t o[32];
+#pragma unroll
+      for (int k = 0; k < 64; k += 8) {
+        const float4 xa = *reinterpret_cast<const float4*>(sD + k);
+        const float4 xb = *reinterpret_cast<const float4*>(sD + k + 4);
+        const float dv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const uint32_t pw = pk[k / 2 + m];
+          o[k / 2 + m] = pack_bf16(bf16_lo(pw) * (__uint_as_float(dr[k + 2 * m]) - dv[2 * m]),
+                                   bf16_hi(pw) * (__uint_as_float(dr[k + 2 * m + 1]) - dv[2 * m + 1]));
+        }
+      }
+      tmem_st32(tdP + lane_off + c0, o);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ds_full);
+    }
+    // epilogue: half 0 writes dV, half 1 dK (TMEM loads by every lane,
+    // stores only for rows inside the sequence).  Both barriers are at most
+    // one phase ahead of the step these warps last saw complete.
+    if (ok) {
+      const bool done = half == 0 ? bounded_wait(p_used, (T_iter - 1) & 1, abort_flag, 605, p.err)
+                                  : bounded_wait(it_done, (T_iter - 1) & 1, abort_flag, 606, p.err);
+      ok = __all_sync(0xffffffffu, done);
+    }
+    if (ok) {
+      tc_fence_after();
+      const bool valid = kvp < p.s;
+      const uint32_t tsrc = (half == 0 ? tdV : tdK) + lane_off;
+      __nv_bfloat16* row = p.dqkv + ((long long)bi * p.s + kvp) * p.ld_dqkv +
+                           (half == 0 ? p.dv_col : p.dk_col) + (long long)g * D;
+      const float sc = half == 0 ? 1.f : p.scale;
+      uint32_t acc[D];
+#pragma unroll
+      for (int cc = 0; cc < D / 16; ++cc) tmem_ld16_nw(tsrc + cc * 16, acc + cc * 16);
+      tmem_wait_ld(acc);
+      if (valid) {
+#pragma unroll
+        for (int cc = 0; cc < D / 16; ++cc) store_row16(row + cc * 16, acc + cc * 16, sc);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ===========================================================================
 // dQ
 // ===========================================================================
 // Warps: 0 TMA, 1 MMA, 2..9 compute (query row (w % 4) * 32 + lane, key
@@ -657,6 +999,20 @@ int launch_dkdv(AttnBwdParams& prm, int grid, cudaStream_t st) {
 }
 
 template <int D>
+int launch_dkdv_tm(AttnBwdParams& prm, int grid, cudaStream_t st) {
+  constexpr int SMEM = DkdvTmCfg<D>::SMEM;
+  static_assert(SMEM <= 232448, "dK/dV tile set exceeds shared memory");
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(attn_dkdv_tm_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
+      return 3;
+    attr = true;
+  }
+  attn_dkdv_tm_kernel<D><<<grid, 320, SMEM, st>>>(prm);
+  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
+template <int D>
 int launch_dq(AttnBwdParams& prm, int grid, cudaStream_t st) {
   constexpr int SMEM = DqCfg<D>::SMEM;
   static_assert(SMEM <= 232448, "dQ tile set exceeds shared memory");
@@ -677,7 +1033,11 @@ int launch_both(AttnBwdParams& prm, const AttnShape& f, cudaStream_t st) {
   {
     // S, dP, dV, dK over the unmasked pairs
     ProfScope prof(PROF_ATTN_BWD, 8.0 * f.d * pairs * f.H * f.b, 0.0, st);
-    rc = launch_dkdv<D>(prm, ((f.s + 127) / 128) * f.Hkv * f.b, st);
+    const int grid = ((f.s + 127) / 128) * f.Hkv * f.b;
+    if constexpr (D <= 80)
+      rc = launch_dkdv_tm<D>(prm, grid, st);
+    else
+      rc = launch_dkdv<D>(prm, grid, st);
   }
   if (rc) return rc;
   // dQ only: the S and dP this kernel rebuilds for its query-major order are
@@ -690,13 +1050,13 @@ int launch_both(AttnBwdParams& prm, const AttnShape& f, cudaStream_t st) {
 }  // namespace
 
 int make_attn_map(CUtensorMap* map, const void* qkv, int b, int s, int64_t ld, int d);
-int attn_dsum(const AttnBwdShape& sh, const void* o, const void* dout, float* Dsum, int s_pad,
-              cudaStream_t st);
+int attn_dsum(const AttnBwdShape& sh, const void* o, const void* dout, const float* lse, float* Dsum,
+              float* NL2, int s_pad, cudaStream_t st);
 
-// workspace: the per-row dO.O sums D [b, H, s_pad] fp32
+// workspace: the per-row dO.O sums D, then -LSE*log2(e), both [b, H, s_pad] fp32
 size_t attention_bwd_ws_bytes(const AttnBwdShape& sh) {
   const int64_t s_pad = ((int64_t)sh.f.s + 127) / 128 * 128;
-  return (size_t)sh.f.b * sh.f.H * s_pad * 4;
+  return (size_t)sh.f.b * sh.f.H * s_pad * 8;
 }
 
 // lse: [b, H_total, s_pad] fp32 (head offset lse_head0)
@@ -705,10 +1065,11 @@ int attention_bwd(const AttnBwdShape& sh, const void* qkv, const void* o, const 
   const AttnShape& f = sh.f;
   const int s_pad = (f.s + 127) / 128 * 128;
   float* Dsum = reinterpret_cast<float*>(ws);
+  float* NL2 = Dsum + (size_t)f.b * f.H * s_pad;
   int rc;
   {
-    ProfScope prof(PROF_MISC, 0.0, 4.0 * f.b * f.s * f.H * f.d + 4.0 * f.b * f.H * s_pad, st);
-    rc = attn_dsum(sh, o, dout, Dsum, s_pad, st);
+    ProfScope prof(PROF_MISC, 0.0, 4.0 * f.b * f.s * f.H * f.d + 12.0 * f.b * f.H * s_pad, st);
+    rc = attn_dsum(sh, o, dout, lse, Dsum, NL2, s_pad, st);
     if (rc) return rc;
   }
 
@@ -729,6 +1090,9 @@ int attention_bwd(const AttnBwdShape& sh, const void* qkv, const void* o, const 
   prm.do_col = (int)sh.do_col;
   prm.lse = lse;
   prm.Dsum = Dsum;
+  prm.nl2 = NL2;
+  prm.qkv = reinterpret_cast<const __nv_bfloat16*>(qkv);
+  prm.ld_qkv = f.ld_qkv;
   prm.H_total = f.H_total;
   prm.lse_head0 = f.lse_head0;
   prm.dqkv = reinterpret_cast<__nv_bfloat16*>(dqkv);

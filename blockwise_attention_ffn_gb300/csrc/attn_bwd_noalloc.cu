@@ -1,5 +1,6 @@
 // attn_bwd_noalloc.cu -- bpt_attention_bwd_noalloc: the attention backward
-// with its scratch (the fp32 per-row dO . O sums) in a fixed array compiled
+// with its scratch (the fp32 per-row dO . O sums and -LSE * log2(e)) in a
+// fixed array compiled
 // into the library, for callers that cannot allocate device memory when they
 // call us.
 //

@@ -222,9 +222,12 @@ __global__ void f32_to_bf16_kernel(int64_t rows, int64_t n, const float* src, in
 }
 
 // Dsum[b, h, q] = sum_k dO[b*s + q, h*d + k] * O[b*s + q, h*d + k]  (0 for q >= s)
+// and NL2[b, h, q] = -LSE[b, h, q] * log2(e), the exponent offset of the
+// probabilities in base 2 (every padded row too)
 __global__ void dsum_kernel(int b, int s, int s_pad, int H, int d, const __nv_bfloat16* o,
                             int64_t ld_o, int64_t o_col, const __nv_bfloat16* dout, int64_t ld_do,
-                            int64_t do_col, float* Dsum) {
+                            int64_t do_col, const float* lse, int H_total, int lse_head0, float* Dsum,
+                            float* NL2) {
   const int64_t total = (int64_t)b * s_pad * H;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -245,6 +248,8 @@ __global__ void dsum_kernel(int b, int s, int s_pad, int H, int d, const __nv_bf
       }
     }
     Dsum[((int64_t)bi * H + hn) * s_pad + q] = acc;
+    NL2[((int64_t)bi * H + hn) * s_pad + q] =
+        -1.4426950408889634f * lse[((int64_t)bi * H_total + lse_head0 + hn) * s_pad + q];
   }
 }
 
@@ -318,13 +323,13 @@ int f32_to_bf16(int64_t rows, int64_t n, const float* src, int64_t ld_src, void*
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 
-int attn_dsum(const AttnBwdShape& sh, const void* o, const void* dout, float* Dsum, int s_pad,
-              cudaStream_t st) {
+int attn_dsum(const AttnBwdShape& sh, const void* o, const void* dout, const float* lse, float* Dsum,
+              float* NL2, int s_pad, cudaStream_t st) {
   const AttnShape& f = sh.f;
   const int64_t total = (int64_t)f.b * s_pad * f.H;
   dsum_kernel<<<grid_for(total, 256), 256, 0, st>>>(f.b, f.s, s_pad, f.H, f.d, (const __nv_bfloat16*)o,
                                                     f.ld_o, f.o_col, (const __nv_bfloat16*)dout, sh.ld_do,
-                                                    sh.do_col, Dsum);
+                                                    sh.do_col, lse, f.H_total, f.lse_head0, Dsum, NL2);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 

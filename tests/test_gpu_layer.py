@@ -9,8 +9,8 @@ import torch
 import blockwise_attention_ffn_gb300 as bpt
 from blockwise_attention_ffn_gb300.presets import C1, LayerConfig
 from oracle import ref
-from tests.gpu_helpers import (assert_close, assert_close_grad, device_inputs, run_bwd, run_fwd,
-                               to64)
+from tests.gpu_helpers import (assert_close, assert_close_grad, device_inputs, half_ulp_bf16, run_bwd,
+                               run_fwd, to64)
 from tests.oracle_helpers import inputs_to_oracle, oracle_cfg
 
 pytestmark = pytest.mark.gpu
@@ -91,7 +91,12 @@ def test_schedule_invariance(base, variant):
     y1, s1 = run_fwd(cfg, dev)
     dx1, g1 = run_bwd(cfg, dev, s1)
     assert torch.equal(y0, y1)
-    assert_close(to64(dx1), to64(dx0), "dx", max_abs=1e-3, rel_fro=1e-4, bf16_out=False)
+    # dx is stored in bf16 after fp32 sums whose order depends on the head
+    # chunk (the input-gradient product accumulates stage by stage), so an
+    # element may round to the neighbouring bf16 value: one ulp, no more
+    d0, d1 = to64(dx0), to64(dx1)
+    assert np.all(np.abs(d1 - d0) <= 2 * half_ulp_bf16(d0) + 1e-3), float(np.max(np.abs(d1 - d0)))
+    assert_close(d1, d0, "dx", max_abs=1e30, rel_fro=1e-4, bf16_out=False)
     for k in g0:
         if g0[k] is not None:
             assert_close(to64(g1[k]), to64(g0[k]), k, max_abs=1e-3 * max(1, float(g0[k].abs().max())),

@@ -43,8 +43,10 @@ struct AttnBwdParams {
   const float* lse;     // [b, H_total, s_pad] at head offset lse_head0
   const float* Dsum;    // [b, H, s_pad]
   const float* nl2;     // [b, H, s_pad]: -LSE * log2(e)
-  const __nv_bfloat16* qkv;  // the packed projection (K and V rows read directly)
+  const __nv_bfloat16* qkv;  // the packed projection (rows copied into TMEM directly)
   long long ld_qkv;
+  const __nv_bfloat16* dout;
+  long long ld_do;
   int H_total, lse_head0;
   __nv_bfloat16* dqkv;
   long long ld_dqkv;
@@ -737,41 +739,60 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_tm_kernel(const __grid_const
 // ===========================================================================
 // dQ
 // ===========================================================================
-// Warps: 0 TMA, 1 MMA, 2..9 compute (query row (w % 4) * 32 + lane, key
-// columns [64 * grp, 64 * grp + 64)).
-// TMEM: S [0,128), dP [128,256), dQ [256, 256+D).
-// Per key/value tile j: S = Q K_j^T, dP = dO V_j^T; P = exp(S - LSE) kept in
-// registers, dS = P (dP - D) into smem; dQ += dS K_j.  MMA order per step:
-// [S columns read] S(j+1); [dS(j) in smem] dP(j+1), dQ(j).
+// One CTA per 128-row query tile i of one query head; it loops over the
+// key/value tiles j <= i.  Every product takes its A operand from TMEM: Q
+// and dO are copied there once per CTA (the A operands of S = Q K_j^T and
+// dP = dO V_j^T) and dS is written over dP as bf16 pairs (the A operand of
+// dQ += dS K_j).  Shared memory holds only the K/V ring.
+// Warps: 0 TMA, 1 MMA, 2..9 compute.  Compute warp w owns query row
+// (w % 4) * 32 + lane and key columns [64h, 64h+64), h = (w - 2) / 4; the
+// row's log-sum-exp and dO.O sum are per-thread scalars.  P stays in
+// registers (bf16 pairs); dS goes over the first 32 of the warp's 64 dP
+// columns.
+// TMEM: S [0,128), dP/dS [128,256), dQ [256, 256+D), Q [256+D, 256+1.5D),
+//       dO [256+1.5D, 256+2D).
+// MMA order: S(j+1) once S(j) is read; dQ(j), then dP(j+1), which
+// overwrites dS(j) after dQ(j) in issue order.
 template <int D>
 struct DqCfg {
   using T = TileGeom<D>;
-  static constexpr int KVS = (D <= 96) ? 3 : 2;
-  static constexpr int SMEM = 2 * T::TILE + KVS * 2 * T::TILE + SqTile::BYTES + 1024 + 256;
+  static constexpr int KVS_FIT = (232448 - 1280) / (2 * T::TILE);
+  static constexpr int KVS = KVS_FIT > 5 ? 5 : KVS_FIT;
+  static constexpr int SMEM = KVS * 2 * T::TILE + 1024 + 256;
+  static constexpr uint32_t COL_DQ = 256, COL_Q = 256 + D, COL_DO = 256 + D + D / 2;
 };
+
+// n = D/2 consecutive 32-bit TMEM columns of this thread's lane from w
+template <int N>
+__device__ __forceinline__ void tmem_store_row(uint32_t taddr, const uint32_t* w) {
+  static_assert(N % 8 == 0 && N <= 64, "row width");
+  if constexpr (N >= 32) tmem_st32(taddr, *reinterpret_cast<const uint32_t(*)[32]>(w));
+  if constexpr (N == 64) tmem_st32(taddr + 32, *reinterpret_cast<const uint32_t(*)[32]>(w + 32));
+  if constexpr (N % 32 >= 16) tmem_st16_nw(taddr + (N / 32) * 32, w + (N / 32) * 32);
+  if constexpr (N % 16 == 8) tmem_st8_nw(taddr + (N / 16) * 16, w + (N / 16) * 16);
+}
 
 template <int D>
 __global__ void __launch_bounds__(320, 1) attn_dq_kernel(const __grid_constant__ AttnBwdParams p) {
   using T = TileGeom<D>;
-  constexpr int KVS = DqCfg<D>::KVS;
+  using C = DqCfg<D>;
+  constexpr int KVS = C::KVS;
+  static_assert(C::COL_DO + D / 2 <= 512, "TMEM columns");
   constexpr uint32_t ID_SQ = idesc_bf16(128, 128, false, false);
   constexpr uint32_t ID_DQ = idesc_bf16(128, D, false, true);
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sdO = sQ + T::TILE;
-  uint8_t* sKV = sdO + T::TILE;
-  uint8_t* sDS = sKV + KVS * 2 * T::TILE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sDS + SqTile::BYTES);
-  uint64_t* q_full = bars;
+  uint8_t* sKV = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + KVS * 2 * T::TILE);
+  uint64_t* qo_ready = bars;           // Q, dO copied into TMEM (8 compute warps)
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = kv_full + KVS;
-  uint64_t* s_full = kv_empty + KVS;  // S(j) in TMEM
-  uint64_t* dp_full = s_full + 1;     // dP(j) in TMEM
-  uint64_t* s_free = dp_full + 1;     // S columns read (8 arrivals)
-  uint64_t* ds_full = s_free + 1;     // dS(j) in smem, dP columns read (8)
-  uint64_t* dq_done = ds_full + 1;    // dQ(j) done (dS tile free)
+  uint64_t* s_full = kv_empty + KVS;   // S(j) in TMEM
+  uint64_t* s_free = s_full + 1;       // S(j) read (8 compute warps)
+  uint64_t* dp_full = s_free + 1;      // dP(j) in TMEM
+  uint64_t* ds_full = dp_full + 1;     // dS(j) written (8 compute warps)
+  uint64_t* dq_done = ds_full + 1;     // dQ(j) done
   uint64_t* drain = dq_done + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -790,24 +811,21 @@ __global__ void __launch_bounds__(320, 1) attn_dq_kernel(const __grid_constant__
   const int nkv = p.causal ? min(i + 1, n_qt) : n_qt;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    mbar_init(qo_ready, 8);
     for (int k = 0; k < KVS; ++k) {
       mbar_init(&kv_full[k], 1);
       mbar_init(&kv_empty[k], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(dp_full, 1);
     mbar_init(s_free, 8);
+    mbar_init(dp_full, 1);
     mbar_init(ds_full, 8);
     mbar_init(dq_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch(&p.map_qkv);
-    tma_prefetch(&p.map_do);
-  }
+  if (warp == 0 && lane == 0) tma_prefetch(&p.map_qkv);
   if (warp == 1) {
     tmem_alloc(tmem_holder, 512);
     tmem_relinquish();
@@ -818,17 +836,13 @@ __global__ void __launch_bounds__(320, 1) attn_dq_kernel(const __grid_constant__
   const uint32_t tmem = *tmem_holder;
   const uint32_t tS = tmem;
   const uint32_t tdP = tmem + 128;
-  const uint32_t tdQ = tmem + 256;
+  const uint32_t tdQ = tmem + C::COL_DQ;
+  const uint32_t tQA = tmem + C::COL_Q;
+  const uint32_t tOA = tmem + C::COL_DO;
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------ TMA producer
-      mbar_expect_tx(q_full, 2 * T::TILE);
-#pragma unroll
-      for (int c = 0; c < T::NCH; ++c) {
-        tma_load_3d(sQ + c * T::CHUNK, &p.map_qkv, q_full, p.q_col + n * D + c * T::CW, q0, bi);
-        tma_load_3d(sdO + c * T::CHUNK, &p.map_do, q_full, p.do_col + n * D + c * T::CW, q0, bi);
-      }
       int issued = 0;
       for (int jt = 0; jt < nkv; ++jt) {
         const int st = jt % KVS;
@@ -844,7 +858,6 @@ __global__ void __launch_bounds__(320, 1) attn_dq_kernel(const __grid_constant__
         issued = jt + 1;
       }
       if (*abort_flag) {
-        mbar_try_wait(q_full, 0);
         for (int jt = (issued > KVS ? issued - KVS : 0); jt < issued; ++jt)
           bounded_wait(&kv_full[jt % KVS], (jt / KVS) & 1, abort_flag, 602, p.err);
       }
@@ -852,21 +865,20 @@ __global__ void __launch_bounds__(320, 1) attn_dq_kernel(const __grid_constant__
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
-      const uint32_t uQ = smem_u32(sQ), udO = smem_u32(sdO);
-      const uint32_t uKV = smem_u32(sKV), uDS = smem_u32(sDS);
+      const uint32_t uKV = smem_u32(sKV);
       auto issue_s = [&](int jt) {
         const uint32_t uK = uKV + (jt % KVS) * 2 * T::TILE;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) umma_bf16(tS, T::kmajor(uQ, kk), T::kmajor(uK, kk), ID_SQ, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a(tS, tQA + kk * 8, T::kmajor(uK, kk), ID_SQ, kk > 0);
         umma_commit(s_full);
       };
       auto issue_dp = [&](int jt) {
         const uint32_t uV = uKV + (jt % KVS) * 2 * T::TILE + T::TILE;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) umma_bf16(tdP, T::kmajor(udO, kk), T::kmajor(uV, kk), ID_SQ, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a(tdP, tOA + kk * 8, T::kmajor(uV, kk), ID_SQ, kk > 0);
         umma_commit(dp_full);
       };
-      bool ok = bounded_wait(q_full, 0, abort_flag, 611, p.err) &&
+      bool ok = bounded_wait(qo_ready, 0, abort_flag, 611, p.err) &&
                 bounded_wait(&kv_full[0], 0, abort_flag, 612, p.err);
       if (ok) {
         tc_fence_after();
@@ -876,21 +888,22 @@ __global__ void __launch_bounds__(320, 1) attn_dq_kernel(const __grid_constant__
       for (int jt = 0; ok && jt < nkv; ++jt) {
         const bool more = jt + 1 < nkv;
         if (more) {
-          if (!bounded_wait(s_free, jt & 1, abort_flag, 613, p.err)) { ok = false; break; }
-          if (!bounded_wait(&kv_full[(jt + 1) % KVS], ((jt + 1) / KVS) & 1, abort_flag, 614, p.err)) { ok = false; break; }
+          if (!bounded_spin(s_free, jt & 1, abort_flag, 613, p.err)) { ok = false; break; }
+          if (!bounded_spin(&kv_full[(jt + 1) % KVS], ((jt + 1) / KVS) & 1, abort_flag, 614, p.err)) { ok = false; break; }
           tc_fence_after();
           issue_s(jt + 1);
         }
-        if (!bounded_wait(ds_full, jt & 1, abort_flag, 615, p.err)) { ok = false; break; }
+        // dQ += dS(j) K_j; the dS pairs of key columns 64h.. sit at TMEM
+        // column 128 + 64h
+        if (!bounded_spin(ds_full, jt & 1, abort_flag, 615, p.err)) { ok = false; break; }
         tc_fence_after();
-        if (more) issue_dp(jt + 1);
-        // dQ += dS(j) K_j
         const uint32_t uK = uKV + (jt % KVS) * 2 * T::TILE;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_bf16(tdQ, SqTile::kmajor(uDS, kk), T::mnmajor(uK, kk), ID_DQ, (jt > 0 || kk > 0));
+          umma_bf16_tmem_a(tdQ, tdP + (kk >> 2) * 64 + (kk & 3) * 8, T::mnmajor(uK, kk), ID_DQ, (jt > 0 || kk > 0));
         umma_commit(&kv_empty[jt % KVS]);
         umma_commit(dq_done);
+        if (more) issue_dp(jt + 1);
       }
       if (!ok) {
         umma_commit(drain);
@@ -900,72 +913,100 @@ __global__ void __launch_bounds__(320, 1) attn_dq_kernel(const __grid_constant__
   } else {
     // ------------------------------------------------ compute (warps 2..9)
     const int quarter = warp & 3;
-    const int grp = (warp - 2) >> 2;
+    const int half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
     const int qpos = q0 + r;
-    const int c0 = grp * 64;
-    const uint32_t lane_off = ((uint32_t)(quarter * 32) << 16) + c0;
+    const int c0 = half * 64;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    {
+      // Q (half 0) or dO (half 1) row of this thread into TMEM as bf16
+      // pairs; rows past the sequence are zero
+      uint32_t w[D / 2];
+      const __nv_bfloat16* src = half == 0
+          ? p.qkv + ((long long)bi * p.s + qpos) * p.ld_qkv + p.q_col + (long long)n * D
+          : p.dout + ((long long)bi * p.s + qpos) * p.ld_do + p.do_col + (long long)n * D;
+#pragma unroll
+      for (int cc = 0; cc < D / 8; ++cc) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (qpos < p.s) v = *reinterpret_cast<const uint4*>(src + cc * 8);
+        w[4 * cc] = v.x;
+        w[4 * cc + 1] = v.y;
+        w[4 * cc + 2] = v.z;
+        w[4 * cc + 3] = v.w;
+      }
+      tmem_store_row<D / 2>((half == 0 ? tQA : tOA) + lane_off, w);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qo_ready);
+    }
     const float c = p.scale_log2;
-    // this row's log-sum-exp (base 2) and dO.O sum; rows past s read the
-    // finite filler values and are masked out below
-    const float l2 = p.lse[((long long)bi * p.H_total + p.lse_head0 + n) * p.s_pad + qpos] * 1.4426950408889634f;
+    // this row's -LSE*log2(e) and dO.O sum (finite filler past the sequence)
+    const float nl = p.nl2[((long long)bi * p.H + n) * p.s_pad + qpos];
     const float dsum = p.Dsum[((long long)bi * p.H + n) * p.s_pad + qpos];
     bool ok = true;
     for (int jt = 0; jt < nkv; ++jt) {
       ok = bounded_wait(s_full, jt & 1, abort_flag, 621, p.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
+      // ---- phase 1: P = exp2(S * scale*log2(e) - LSE*log2(e)); key columns
+      // [0, hi) of this warp's 64 are unmasked
       const int kv0 = jt * 128 + c0;
-      const bool edge = (p.causal && kv0 + 63 > q0) || (kv0 + 64 > p.s) || (qpos >= p.s);
-      // phase 1: P = exp(S - LSE), in registers; then release the S columns
-      uint32_t pv[64];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) tmem_ld16_nw(tS + lane_off + q4 * 16, pv + q4 * 16);
-      tmem_wait_ld(pv);
+      int hi = min(64, p.s - kv0);
+      if (p.causal) hi = min(hi, qpos - kv0 + 1);
+      if (qpos >= p.s) hi = 0;
+      uint32_t sv[64];
+      tmem_ld32_nw(tS + lane_off + c0, sv);
+      tmem_ld32_nw(tS + lane_off + c0 + 32, sv + 32);
+      tmem_wait_ld(sv);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free);
+      uint32_t pk[32];
+      if (hi >= 64) {
 #pragma unroll
-      for (int k = 0; k < 64; ++k) {
-        float e = ex2(fmaf(__uint_as_float(pv[k]), c, -l2));
-        if (edge) {
-          const int kp = kv0 + k;
-          if (kp >= p.s || qpos >= p.s || (p.causal && kp > qpos)) e = 0.f;
+        for (int k = 0; k < 64; k += 2)
+          pk[k / 2] = pack_bf16(ex2(fmaf(__uint_as_float(sv[k]), c, nl)), ex2(fmaf(__uint_as_float(sv[k + 1]), c, nl)));
+      } else {
+#pragma unroll
+        for (int k = 0; k < 64; k += 2) {
+          const float e0 = k < hi ? ex2(fmaf(__uint_as_float(sv[k]), c, nl)) : 0.f;
+          const float e1 = k + 1 < hi ? ex2(fmaf(__uint_as_float(sv[k + 1]), c, nl)) : 0.f;
+          pk[k / 2] = pack_bf16(e0, e1);
         }
-        pv[k] = __float_as_uint(e);
       }
-      // phase 2: dS = P (dP - D) into smem once dQ(j-1) released the tile
+      // ---- phase 2: dS = P (dP - D) over this warp's dP columns
       ok = bounded_wait(dp_full, jt & 1, abort_flag, 622, p.err);
-      if (ok && jt >= 1) ok = bounded_wait(dq_done, (jt - 1) & 1, abort_flag, 623, p.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       uint32_t dr[64];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) tmem_ld16_nw(tdP + lane_off + q4 * 16, dr + q4 * 16);
+      tmem_ld32_nw(tdP + lane_off + c0, dr);
+      tmem_ld32_nw(tdP + lane_off + c0 + 32, dr + 32);
       tmem_wait_ld(dr);
+      uint32_t o[32];
 #pragma unroll
-      for (int k = 0; k < 64; k += 8) {
-        float a[8];
-#pragma unroll
-        for (int m = 0; m < 8; ++m) a[m] = __uint_as_float(pv[k + m]) * (__uint_as_float(dr[k + m]) - dsum);
-        *reinterpret_cast<uint4*>(sDS + SqTile::off(r, grp * 8 + k / 8)) =
-            make_uint4(pack_bf16(a[0], a[1]), pack_bf16(a[2], a[3]), pack_bf16(a[4], a[5]), pack_bf16(a[6], a[7]));
+      for (int k = 0; k < 64; k += 2) {
+        const uint32_t pw = pk[k / 2];
+        o[k / 2] = pack_bf16(bf16_lo(pw) * (__uint_as_float(dr[k]) - dsum),
+                             bf16_hi(pw) * (__uint_as_float(dr[k + 1]) - dsum));
       }
+      tmem_st32(tdP + lane_off + c0, o);
+      tmem_st_wait();
       tc_fence_before();
-      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full);
     }
+    // epilogue: the two halves split dQ's 16-column chunks.  dq_done is at
+    // most one phase ahead of dQ(nkv-2), which completed before dP(nkv-1).
     if (ok) ok = __all_sync(0xffffffffu, bounded_wait(dq_done, (nkv - 1) & 1, abort_flag, 624, p.err));
     if (ok) {
-      // the two groups split dQ's 16-column chunks
       tc_fence_after();
       constexpr int NC = D / 16;
       constexpr int NC0 = (NC + 1) / 2;
-      const int cbeg = grp == 0 ? 0 : NC0, cend = grp == 0 ? NC0 : NC;
+      const int cbeg = half == 0 ? 0 : NC0, cend = half == 0 ? NC0 : NC;
       const bool valid = qpos < p.s;
       __nv_bfloat16* qrow = p.dqkv + ((long long)bi * p.s + qpos) * p.ld_dqkv + p.dq_col + (long long)n * D;
-      const uint32_t tq = tdQ + ((uint32_t)(quarter * 32) << 16);
+      const uint32_t tq = tdQ + lane_off;
       for (int cc = cbeg; cc < cend; ++cc) {
         uint32_t v[16];
         tmem_ld16_nw(tq + cc * 16, v);
@@ -1093,6 +1134,8 @@ int attention_bwd(const AttnBwdShape& sh, const void* qkv, const void* o, const 
   prm.nl2 = NL2;
   prm.qkv = reinterpret_cast<const __nv_bfloat16*>(qkv);
   prm.ld_qkv = f.ld_qkv;
+  prm.dout = reinterpret_cast<const __nv_bfloat16*>(dout);
+  prm.ld_do = sh.ld_do;
   prm.H_total = f.H_total;
   prm.lse_head0 = f.lse_head0;
   prm.dqkv = reinterpret_cast<__nv_bfloat16*>(dqkv);

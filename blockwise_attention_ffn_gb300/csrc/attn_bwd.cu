@@ -71,20 +71,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
-// 16 TMEM fp32 columns of this thread's row -> 16 bf16 values (scaled)
-__device__ __forceinline__ void store_row16(__nv_bfloat16* dst, const uint32_t* v, float sc) {
-  uint4 a, b;
-  a.x = pack_bf16(__uint_as_float(v[0]) * sc, __uint_as_float(v[1]) * sc);
-  a.y = pack_bf16(__uint_as_float(v[2]) * sc, __uint_as_float(v[3]) * sc);
-  a.z = pack_bf16(__uint_as_float(v[4]) * sc, __uint_as_float(v[5]) * sc);
-  a.w = pack_bf16(__uint_as_float(v[6]) * sc, __uint_as_float(v[7]) * sc);
-  b.x = pack_bf16(__uint_as_float(v[8]) * sc, __uint_as_float(v[9]) * sc);
-  b.y = pack_bf16(__uint_as_float(v[10]) * sc, __uint_as_float(v[11]) * sc);
-  b.z = pack_bf16(__uint_as_float(v[12]) * sc, __uint_as_float(v[13]) * sc);
-  b.w = pack_bf16(__uint_as_float(v[14]) * sc, __uint_as_float(v[15]) * sc);
-  reinterpret_cast<uint4*>(dst)[0] = a;
-  reinterpret_cast<uint4*>(dst)[1] = b;
-}
 
 // ===========================================================================
 // dK / dV
@@ -762,15 +748,6 @@ struct DqCfg {
   static constexpr uint32_t COL_DQ = 256, COL_Q = 256 + D, COL_DO = 256 + D + D / 2;
 };
 
-// n = D/2 consecutive 32-bit TMEM columns of this thread's lane from w
-template <int N>
-__device__ __forceinline__ void tmem_store_row(uint32_t taddr, const uint32_t* w) {
-  static_assert(N % 8 == 0 && N <= 64, "row width");
-  if constexpr (N >= 32) tmem_st32(taddr, *reinterpret_cast<const uint32_t(*)[32]>(w));
-  if constexpr (N == 64) tmem_st32(taddr + 32, *reinterpret_cast<const uint32_t(*)[32]>(w + 32));
-  if constexpr (N % 32 >= 16) tmem_st16_nw(taddr + (N / 32) * 32, w + (N / 32) * 32);
-  if constexpr (N % 16 == 8) tmem_st8_nw(taddr + (N / 16) * 16, w + (N / 16) * 16);
-}
 
 template <int D>
 __global__ void __launch_bounds__(320, 1) attn_dq_kernel(const __grid_constant__ AttnBwdParams p) {

@@ -10,14 +10,15 @@
 // every row is written for the recompute backward.
 //
 // One CTA = one 128-row query tile of one head (GQA: key/value head n / G).
-//   warp 0      TMA: the Q tile once, K/V tiles through a KVS-deep ring
-//   warp 1      TMEM owner and MMA issuer: S_j = Q K_j^T into one of two TMEM
-//               S buffers, then O += P_{j-1} V_{j-1} (P from shared memory)
-//   warps 2..5  softmax, one query row per thread: reads its S row from TMEM,
-//               masks, updates m and l, writes P (bf16) to shared memory,
-//               rescales its O row in TMEM when the max moved by more than
-//               2^8 (otherwise keeps the stale max: exact, since O and l are
-//               scaled alike), and at the end normalises and stores O.
+//   warp 0      TMA: K/V tiles through a KVS-deep ring
+//   warp 1      TMEM owner and MMA issuer: S_{j+1} = Q K_{j+1}^T into one of
+//               two TMEM S buffers, then O += P_j V_j
+//   warps 2..5  softmax, one query row per thread: copy the Q row into TMEM
+//               once; per tile read the S row, mask, update m and l, write P
+//               (bf16 pairs) over the S buffer, rescale the O row in TMEM
+//               when the max moved by more than 2^8 (otherwise keep the
+//               stale max: exact, since O and l are scaled alike), and at
+//               the end normalise and store O.
 // The s x s score matrix never leaves TMEM/registers.
 #include <math.h>
 #include <string.h>
@@ -43,6 +44,8 @@ struct AttnFwdParams {
   int qt_begin, n_qt, b;
   float scale_log2;  // log2(e) / sqrt(d)
   float scale;       // 1 / sqrt(d)
+  const __nv_bfloat16* qkv;  // the packed projection (Q rows copied into TMEM)
+  long long ld_qkv;
   unsigned int* err;
 };
 
@@ -55,34 +58,39 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// TMEM: two 128-column S buffers [0,256), O [256, 256+D), Q [256+D, 256+1.5D).
+// Q is copied into TMEM once per CTA (the A operand of S = Q K_j^T) and each
+// P is written over its own S buffer as bf16 pairs (the A operand of
+// O += P V_j), so every product reads only its B operand from shared memory,
+// which holds just the K/V ring.
 template <int D>
 struct FwdCfg {
   using T = TileGeom<D>;
-  static constexpr int KVS = (D <= 80) ? 3 : 2;
-  static constexpr int SMEM_TILES = T::TILE * (1 + 2 * KVS) + 2 * SqTile::BYTES;
-  static constexpr int SMEM = SMEM_TILES + 1024 + 256;
+  static constexpr int KVS_FIT = (232448 - 1280) / (2 * T::TILE);
+  static constexpr int KVS = KVS_FIT > 5 ? 5 : KVS_FIT;
+  static constexpr int SMEM = KVS * 2 * T::TILE + 1024 + 256;
+  static constexpr uint32_t COL_O = 256, COL_Q = 256 + D;
 };
 
 template <int D>
 __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant__ AttnFwdParams p) {
   using T = TileGeom<D>;
-  constexpr int KVS = FwdCfg<D>::KVS;
+  using C = FwdCfg<D>;
+  constexpr int KVS = C::KVS;
+  static_assert(C::COL_Q + D / 2 <= 512, "TMEM columns");
   constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
   constexpr uint32_t IDESC_PV = idesc_bf16(128, D, false, true);
   constexpr float NEG_INF = -INFINITY;
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sKV = sQ + T::TILE;
-  uint8_t* sP = sKV + KVS * 2 * T::TILE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * SqTile::BYTES);
-  uint64_t* q_full = bars;
+  uint8_t* sKV = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + KVS * 2 * T::TILE);
+  uint64_t* q_ready = bars;            // Q copied into TMEM (4 softmax warps)
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = kv_full + KVS;
-  uint64_t* s_full = kv_empty + KVS;
-  uint64_t* s_free = s_full + 2;
-  uint64_t* p_full = s_free + 2;
+  uint64_t* s_full = kv_empty + KVS;   // [2]
+  uint64_t* p_full = s_full + 2;       // [2], 4 softmax warps
   uint64_t* pv_done = p_full + 2;
   uint64_t* drain = pv_done + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
@@ -106,14 +114,13 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
   const int nkv = p.causal ? min(qt + 1, kv_tiles_total) : kv_tiles_total;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    mbar_init(q_ready, 4);
     for (int i = 0; i < KVS; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 4);
       mbar_init(&p_full[i], 4);
     }
     mbar_init(pv_done, 1);
@@ -130,16 +137,13 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const uint32_t tS = tmem;        // two 128-column S buffers
-  const uint32_t tO = tmem + 256;  // D columns
+  const uint32_t tS = tmem;  // two 128-column S / P buffers
+  const uint32_t tO = tmem + C::COL_O;
+  const uint32_t tQA = tmem + C::COL_Q;
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------ TMA producer
-      mbar_expect_tx(q_full, T::TILE);
-#pragma unroll
-      for (int c = 0; c < T::NCH; ++c)
-        tma_load_3d(sQ + c * T::CHUNK, &p.map_qkv, q_full, p.q_col + n * D + c * T::CW, q0, bi);
       int issued = 0;
       for (int j = 0; j < nkv; ++j) {
         const int st = j % KVS;
@@ -156,44 +160,38 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
         issued = j + 1;
       }
       if (*abort_flag) {
-        bounded_wait(q_full, 0, abort_flag, 202, p.err);
         for (int j = (issued > KVS ? issued - KVS : 0); j < issued; ++j)
-          mbar_try_wait(&kv_full[j % KVS], (j / KVS) & 1);
+          bounded_wait(&kv_full[j % KVS], (j / KVS) & 1, abort_flag, 202, p.err);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
-      const uint32_t uQ = smem_u32(sQ);
+      // order: S(0); per j: S(j+1), PV(j).  S(j+1) overwrites the buffer of
+      // P(j-1) after PV(j-1) in issue order.
       const uint32_t uKV = smem_u32(sKV);
-      const uint32_t uP = smem_u32(sP);
-      bool ok = bounded_wait(q_full, 0, abort_flag, 211, p.err);
-      auto issue_pv = [&](int i) -> bool {
-        if (!bounded_wait(&p_full[i & 1], (i >> 1) & 1, abort_flag, 212, p.err)) return false;
+      auto issue_s = [&](int j) -> bool {
+        if (!bounded_spin(&kv_full[j % KVS], (j / KVS) & 1, abort_flag, 213, p.err)) return false;
         tc_fence_after();
-        const uint32_t pt = uP + (i & 1) * SqTile::BYTES;
-        const uint32_t vt = uKV + (i % KVS) * 2 * T::TILE + T::TILE;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_bf16(tO, SqTile::kmajor(pt, kk), T::mnmajor(vt, kk), IDESC_PV, (i > 0 || kk > 0));
-        umma_commit(&kv_empty[i % KVS]);
-        umma_commit(pv_done);
-        return true;
-      };
-      for (int j = 0; ok && j < nkv; ++j) {
-        const int st = j % KVS;
-        const int sb = j & 1;
-        if (!bounded_wait(&kv_full[st], (j / KVS) & 1, abort_flag, 213, p.err)) { ok = false; break; }
-        if (j >= 2 && !bounded_wait(&s_free[sb], ((j - 2) >> 1) & 1, abort_flag, 214, p.err)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t kt = uKV + st * 2 * T::TILE;
+        const uint32_t kt = uKV + (j % KVS) * 2 * T::TILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_bf16(tS + sb * 128, T::kmajor(uQ, kk), T::kmajor(kt, kk), IDESC_S, kk > 0);
-        umma_commit(&s_full[sb]);
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+          umma_bf16_tmem_a(tS + (j & 1) * 128, tQA + kk * 8, T::kmajor(kt, kk), IDESC_S, kk > 0);
+        umma_commit(&s_full[j & 1]);
+        return true;
+      };
+      bool ok = bounded_wait(q_ready, 0, abort_flag, 211, p.err) && issue_s(0);
+      for (int j = 0; ok && j < nkv; ++j) {
+        if (j + 1 < nkv && !issue_s(j + 1)) { ok = false; break; }
+        if (!bounded_spin(&p_full[j & 1], (j >> 1) & 1, abort_flag, 212, p.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t vt = uKV + (j % KVS) * 2 * T::TILE + T::TILE;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16_tmem_a(tO, tS + (j & 1) * 128 + kk * 8, T::mnmajor(vt, kk), IDESC_PV, (j > 0 || kk > 0));
+        umma_commit(&kv_empty[j % KVS]);
+        umma_commit(pv_done);
       }
-      if (ok) ok = issue_pv(nkv - 1);
       if (!ok) {
         umma_commit(drain);
         bounded_wait(drain, 0, abort_flag, 215, p.err);
@@ -205,87 +203,105 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
     const int r = quarter * 32 + lane;
     const int qpos = q0 + r;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    {
+      // this thread's Q row into TMEM as bf16 pairs (zero past the sequence)
+      uint32_t w[D / 2];
+      const __nv_bfloat16* src =
+          p.qkv + ((long long)bi * p.s + qpos) * p.ld_qkv + p.q_col + (long long)n * D;
+#pragma unroll
+      for (int cc = 0; cc < D / 8; ++cc) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (qpos < p.s) v = *reinterpret_cast<const uint4*>(src + cc * 8);
+        w[4 * cc] = v.x;
+        w[4 * cc + 1] = v.y;
+        w[4 * cc + 2] = v.z;
+        w[4 * cc + 3] = v.w;
+      }
+      tmem_store_row<D / 2>(tQA + lane_off, w);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_ready);
+    }
     const float c = p.scale_log2;
     float m_run = NEG_INF, l_run = 0.f;
     bool ok = true;
-    uint8_t* myP0 = sP;
     for (int j = 0; j < nkv; ++j) {
       const int sb = j & 1;
+      const uint32_t tb = tS + sb * 128 + lane_off;
       ok = bounded_wait(&s_full[sb], (j >> 1) & 1, abort_flag, 221, p.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      float sv[128];
-      {
-        uint32_t rr[128];
+      uint32_t sv[128];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) tmem_ld32_nw(tS + lane_off + sb * 128 + q4 * 32, rr + q4 * 32);
-        tmem_wait_ld(rr);
-#pragma unroll
-        for (int i = 0; i < 128; ++i) sv[i] = __uint_as_float(rr[i]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[sb]);
-
+      for (int q4 = 0; q4 < 4; ++q4) tmem_ld32_nw(tb + q4 * 32, sv + q4 * 32);
+      tmem_wait_ld(sv);
+      // key columns [0, hi) are unmasked
       const int kv0 = j * 128;
-      const bool diag = p.causal ? (kv0 + 127 > q0) : (kv0 + 128 > p.s);
-      if (diag) {
+      int hi = min(128, p.s - kv0);
+      if (p.causal) hi = min(hi, qpos - kv0 + 1);
+      const bool edge = hi < 128;
+      float mx = NEG_INF;
+      if (!edge) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
-          const int kp = kv0 + i;
-          if (kp >= p.s || (p.causal && kp > qpos)) sv[i] = NEG_INF;
-        }
+        for (int i = 0; i < 128; ++i) mx = fmaxf(mx, __uint_as_float(sv[i]));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i < hi) mx = fmaxf(mx, __uint_as_float(sv[i]));
       }
-      float mx = sv[0];
-#pragma unroll
-      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, sv[i]);
       const float m_new = fmaxf(m_run, mx);
       const bool need = (m_new - m_run) * c > 8.f;
       const bool rescale = __any_sync(0xffffffffu, need);
       float alpha = 1.f;
       if (rescale) {
-        alpha = ex2((m_run - m_new) * c);
+        alpha = (m_run == NEG_INF) ? 0.f : ex2((m_run - m_new) * c);
         m_run = m_new;
       }
-      const float mc = m_run * c;
+      // a row with no unmasked key yet keeps m = -inf; its exponent offset
+      // is then 0 and every P entry below is masked to zero
+      const float mc = (m_run == NEG_INF) ? 0.f : m_run * c;
       float rs = 0.f;
+      uint32_t pk[64];
+      if (!edge) {
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        sv[i] = ex2(fmaf(sv[i], c, -mc));
-        rs += sv[i];
+        for (int i = 0; i < 128; i += 2) {
+          const float e0 = ex2(fmaf(__uint_as_float(sv[i]), c, -mc));
+          const float e1 = ex2(fmaf(__uint_as_float(sv[i + 1]), c, -mc));
+          rs += e0 + e1;
+          pk[i / 2] = pack_bf16(e0, e1);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 128; i += 2) {
+          const float e0 = i < hi ? ex2(fmaf(__uint_as_float(sv[i]), c, -mc)) : 0.f;
+          const float e1 = i + 1 < hi ? ex2(fmaf(__uint_as_float(sv[i + 1]), c, -mc)) : 0.f;
+          rs += e0 + e1;
+          pk[i / 2] = pack_bf16(e0, e1);
+        }
       }
       l_run = l_run * alpha + rs;
-
-      // PV(j-1) must be done before O is rescaled, and PV(j-2) (the last
-      // reader of P buffer sb) before P is overwritten; PV(j-1) covers both.
+      // P over the first 64 columns of its own S buffer (all read above)
+      tmem_st32(tb, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+      tmem_st32(tb + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
+      // PV(j-1) must be done before O is rescaled; waiting for it every step
+      // keeps these warps within one phase of pv_done
       if (j > 0) {
         ok = bounded_wait(pv_done, (j - 1) & 1, abort_flag, 222, p.err);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
+        if (rescale) {
+          uint32_t ro[D];
+#pragma unroll
+          for (int cc = 0; cc < D / 16; ++cc) tmem_ld16_nw(tO + lane_off + cc * 16, ro + cc * 16);
+          tmem_wait_ld(ro);
+#pragma unroll
+          for (int i = 0; i < D; ++i) ro[i] = __float_as_uint(__uint_as_float(ro[i]) * alpha);
+#pragma unroll
+          for (int cc = 0; cc < D / 16; ++cc) tmem_st16_nw(tO + lane_off + cc * 16, ro + cc * 16);
+        }
       }
-      // P (bf16) into the swizzled K-major tile of buffer sb
-      uint8_t* pb = myP0 + sb * SqTile::BYTES;
-#pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
-        uint4 u;
-        u.x = pack_bf16(sv[ch * 8 + 0], sv[ch * 8 + 1]);
-        u.y = pack_bf16(sv[ch * 8 + 2], sv[ch * 8 + 3]);
-        u.z = pack_bf16(sv[ch * 8 + 4], sv[ch * 8 + 5]);
-        u.w = pack_bf16(sv[ch * 8 + 6], sv[ch * 8 + 7]);
-        *reinterpret_cast<uint4*>(pb + SqTile::off(r, ch)) = u;
-      }
-      if (j > 0 && rescale) {
-        uint32_t ro[D];
-#pragma unroll
-        for (int cc = 0; cc < D / 16; ++cc) tmem_ld16_nw(tO + lane_off + cc * 16, ro + cc * 16);
-        tmem_wait_ld(ro);
-#pragma unroll
-        for (int i = 0; i < D; ++i) ro[i] = __float_as_uint(__uint_as_float(ro[i]) * alpha);
-#pragma unroll
-        for (int cc = 0; cc < D / 16; ++cc) tmem_st16_nw(tO + lane_off + cc * 16, ro + cc * 16);
-        tmem_st_wait();
-      }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[sb]);
@@ -303,22 +319,9 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
 #pragma unroll
       for (int cc = 0; cc < D / 16; ++cc) tmem_ld16_nw(tO + lane_off + cc * 16, oall + cc * 16);
       tmem_wait_ld(oall);
+      if (valid) {
 #pragma unroll
-      for (int cc = 0; cc < D / 16; ++cc) {
-        const uint32_t* ro = oall + cc * 16;
-        if (valid) {
-          uint4 u0, u1;
-          u0.x = pack_bf16(__uint_as_float(ro[0]) * inv_l, __uint_as_float(ro[1]) * inv_l);
-          u0.y = pack_bf16(__uint_as_float(ro[2]) * inv_l, __uint_as_float(ro[3]) * inv_l);
-          u0.z = pack_bf16(__uint_as_float(ro[4]) * inv_l, __uint_as_float(ro[5]) * inv_l);
-          u0.w = pack_bf16(__uint_as_float(ro[6]) * inv_l, __uint_as_float(ro[7]) * inv_l);
-          u1.x = pack_bf16(__uint_as_float(ro[8]) * inv_l, __uint_as_float(ro[9]) * inv_l);
-          u1.y = pack_bf16(__uint_as_float(ro[10]) * inv_l, __uint_as_float(ro[11]) * inv_l);
-          u1.z = pack_bf16(__uint_as_float(ro[12]) * inv_l, __uint_as_float(ro[13]) * inv_l);
-          u1.w = pack_bf16(__uint_as_float(ro[14]) * inv_l, __uint_as_float(ro[15]) * inv_l);
-          reinterpret_cast<uint4*>(orow + cc * 16)[0] = u0;
-          reinterpret_cast<uint4*>(orow + cc * 16)[1] = u1;
-        }
+        for (int cc = 0; cc < D / 16; ++cc) store_row16(orow + cc * 16, oall + cc * 16, inv_l);
       }
       // every row of the padded tile gets a finite value (rows past s see the
       // zero-filled query), so the backward pass never reads garbage
@@ -379,6 +382,8 @@ int attention_fwd(const AttnShape& sh, const void* qkv, void* o, float* lse, cud
   prm.b = sh.b;
   prm.scale = 1.f / sqrtf((float)sh.d);
   prm.scale_log2 = prm.scale * 1.4426950408889634f;
+  prm.qkv = reinterpret_cast<const __nv_bfloat16*>(qkv);
+  prm.ld_qkv = sh.ld_qkv;
   prm.err = device_error_word();
   if (!prm.err) return 3;
   const int grid = prm.n_qt * sh.H * sh.b;

@@ -548,7 +548,7 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_tm_kernel(const __grid_const
         const bool more = t + 1 < T_iter;
         // dV(t) += P^T(t) dO(t); the P^T pairs of query columns 64h.. sit at
         // TMEM column 64h
-        if (!bounded_spin(p_full, t & 1, abort_flag, 583, p.err)) { ok = false; break; }
+        if (!bounded_wait(p_full, t & 1, abort_flag, 583, p.err)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
@@ -556,12 +556,12 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_tm_kernel(const __grid_const
         umma_commit(p_used);
         if (more) {
           // S(t+1) overwrites P^T(t), after dV(t) in issue order
-          if (!bounded_spin(&qdo_full[(t + 1) % QS], ((t + 1) / QS) & 1, abort_flag, 586, p.err)) { ok = false; break; }
+          if (!bounded_wait(&qdo_full[(t + 1) % QS], ((t + 1) / QS) & 1, abort_flag, 586, p.err)) { ok = false; break; }
           tc_fence_after();
           issue_s(t + 1);
         }
         // dK(t) += dS^T(t) Q(t)
-        if (!bounded_spin(ds_full, t & 1, abort_flag, 587, p.err)) { ok = false; break; }
+        if (!bounded_wait(ds_full, t & 1, abort_flag, 587, p.err)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
@@ -865,14 +865,14 @@ __global__ void __launch_bounds__(320, 1) attn_dq_kernel(const __grid_constant__
       for (int jt = 0; ok && jt < nkv; ++jt) {
         const bool more = jt + 1 < nkv;
         if (more) {
-          if (!bounded_spin(s_free, jt & 1, abort_flag, 613, p.err)) { ok = false; break; }
-          if (!bounded_spin(&kv_full[(jt + 1) % KVS], ((jt + 1) / KVS) & 1, abort_flag, 614, p.err)) { ok = false; break; }
+          if (!bounded_wait(s_free, jt & 1, abort_flag, 613, p.err)) { ok = false; break; }
+          if (!bounded_wait(&kv_full[(jt + 1) % KVS], ((jt + 1) / KVS) & 1, abort_flag, 614, p.err)) { ok = false; break; }
           tc_fence_after();
           issue_s(jt + 1);
         }
         // dQ += dS(j) K_j; the dS pairs of key columns 64h.. sit at TMEM
         // column 128 + 64h
-        if (!bounded_spin(ds_full, jt & 1, abort_flag, 615, p.err)) { ok = false; break; }
+        if (!bounded_wait(ds_full, jt & 1, abort_flag, 615, p.err)) { ok = false; break; }
         tc_fence_after();
         const uint32_t uK = uKV + (jt % KVS) * 2 * T::TILE;
 #pragma unroll

@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
       // P(j-1) after PV(j-1) in issue order.
       const uint32_t uKV = smem_u32(sKV);
       auto issue_s = [&](int j) -> bool {
-        if (!bounded_spin(&kv_full[j % KVS], (j / KVS) & 1, abort_flag, 213, p.err)) return false;
+        if (!bounded_wait(&kv_full[j % KVS], (j / KVS) & 1, abort_flag, 213, p.err)) return false;
         tc_fence_after();
         const uint32_t kt = uKV + (j % KVS) * 2 * T::TILE;
 #pragma unroll
@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
       bool ok = bounded_wait(q_ready, 0, abort_flag, 211, p.err) && issue_s(0);
       for (int j = 0; ok && j < nkv; ++j) {
         if (j + 1 < nkv && !issue_s(j + 1)) { ok = false; break; }
-        if (!bounded_spin(&p_full[j & 1], (j >> 1) & 1, abort_flag, 212, p.err)) { ok = false; break; }
+        if (!bounded_wait(&p_full[j & 1], (j >> 1) & 1, abort_flag, 212, p.err)) { ok = false; break; }
         tc_fence_after();
         const uint32_t vt = uKV + (j % KVS) * 2 * T::TILE + T::TILE;
 #pragma unroll

@@ -82,38 +82,6 @@ __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, vol
   }
 }
 
-// Non-blocking test of phase `parity` (the thread is never suspended).
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// bounded_wait for a single issuing thread on the critical path: polls
-// without suspending, so it resumes as soon as the phase completes (a
-// suspended try_wait can take a few hundred cycles to wake).  Same limit and
-// error reporting as bounded_wait.
-__device__ __forceinline__ bool bounded_spin(uint64_t* bar, uint32_t parity, volatile int* abort, int site,
-                                             unsigned int* err) {
-  if (mbar_test_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (true) {
-    if (mbar_test_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (clock64() - t0 > BPT_WAIT_CYCLES) {
-      report_timeout(err, site);
-      *abort = 1;
-      return false;
-    }
-  }
-}
-
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -154,6 +154,35 @@ def dist_setup():
     return ws, rank, local
 
 
+# Multi-rank host logic (one process per GPU, each a full replica of the layer
+# step on its own seeded batch: the step shards by batch with no exchange).
+
+def rank_seed(c, rank: int) -> int:
+    """Seed of this rank's synthetic batch: every replica gets different data."""
+    return c.seed + 101 * rank
+
+
+def reports(rank: int) -> bool:
+    """Only rank 0 prints the JSON line (and runs the reference arm)."""
+    return rank == 0
+
+
+def max_over_ranks(x: float, world: int, device="cpu") -> float:
+    """The slowest rank's time: the job is done when every replica is."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as tdist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank_step: float, world: int, ms: float) -> float:
+    """Whole-job TFLOP/s: the work of all ranks over the slowest rank's time."""
+    return flops_per_rank_step * world / (ms * 1e-3) / 1e12
+
+
 def describe(c) -> dict:
     return {"workload": c.name, "b": c.b, "s": c.s, "h": c.h, "n_heads": c.n_heads,
             "n_kv_heads": c.n_kv_heads, "head_dim": c.head_dim, "ffn_dim": c.ffn_dim,
@@ -201,7 +230,7 @@ def cpu_baseline(c, rows: int) -> dict:
 
 def run_reference(args, c):
     ws, rank, _ = dist_setup()
-    if rank != 0:
+    if not reports(rank):
         return 0
     times, fl = [], None
     for i in range(args.warmup + args.steps):
@@ -238,7 +267,7 @@ def run_gpu(args, c):
     dev = torch.device("cuda", local)
     bpt.lib()
 
-    inp = make_layer_inputs(c, seed=c.seed + 101 * rank, device=dev, with_dy=c.backward)
+    inp = make_layer_inputs(c, seed=rank_seed(c, rank), device=dev, with_dy=c.backward)
     W = inp["weights"]
     x = inp["x"]
     dy = inp.get("dy")
@@ -284,17 +313,13 @@ def run_gpu(args, c):
         tdist.barrier()
     ms = e0.elapsed_time(e1) / args.steps
     clk = clocks.stop() if rank == 0 else None
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     st_, site = bpt.bpt_last_device_error(stream)
     if st_ != bpt.BPT_OK:
         raise RuntimeError(f"device error {st_} at wait site {site}")
 
     fl = flop_counts(c)
-    total_fl = fl["executed"] * world
-    value = total_fl / (ms * 1e-3) / 1e12
+    value = job_throughput(fl["executed"], world, ms)
     peaks = load_peaks()
 
     # per-kernel breakdown of the same step (separate profiled steps)
@@ -354,14 +379,11 @@ def run_gpu(args, c):
         step_e2e()
     torch.cuda.synchronize()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
     h2d = xh.numel() * xh.element_size() + (dyh.numel() * dyh.element_size() if c.backward else 0)
     d2h = outh.numel() * outh.element_size()
 
-    if rank == 0:
+    if reports(rank):
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -374,7 +396,7 @@ def run_gpu(args, c):
             "pct_of_bf16_peak_sustained": 100 * value / (peaks["bf16_sustained"] * world),
             "peak_source": peaks["source"],
             "clocks": clk,
-            "e2e": {"value": total_fl / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+            "e2e": {"value": job_throughput(fl["executed"], world, e2e_ms), "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "what": "pinned host x (and dy) copied in, fwd+bwd through the C ABI, dx copied out"},
             "gpu_launches": int(round(launches_per_step * args.steps)),

@@ -3,8 +3,9 @@
 Any tensor-core implementation of the layer must round to bf16 the operands of
 its products: the normalised input xn of the Q/K/V projection, Q, K and V
 themselves, the attention output O, the gradients dx1, dO, dS and dQ/dK/dV,
-and P.  This test emulates exactly those roundings (and nothing else) around
-the exact fp64 layer and measures the relative Frobenius error of the
+and P.  This test emulates exactly those roundings around the exact fp64
+layer, plus one the kernels here add (dS is formed from the bf16 copy of P
+that also feeds dV), and measures the relative Frobenius error of the
 attention-projection weight gradients against the fp64 oracle.
 
 It shows two things the GPU parity tests rely on:
@@ -75,7 +76,7 @@ def emulated_attention_grads(cfg, seed=3):
     for n in range(H):
         gk = n // G
         Dn = (do[:, n] * O[:, n]).sum(1, keepdims=True)
-        dS = _bf(P[n] * (do[:, n] @ v[:, gk].T - Dn))
+        dS = _bf(_bf(P[n]) * (do[:, n] @ v[:, gk].T - Dn))
         dv[:, gk] += _bf(P[n]).T @ do[:, n]
         dq[:, n] = dS @ k[:, gk] / sqrt(d)
         dk[:, gk] += dS.T @ q[:, n] / sqrt(d)

@@ -730,27 +730,36 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_tm_kernel(const __grid_const
 // and dO are copied there once per CTA (the A operands of S = Q K_j^T and
 // dP = dO V_j^T) and dS is written over dP as bf16 pairs (the A operand of
 // dQ += dS K_j).  Shared memory holds only the K/V ring.
-// Warps: 0 TMA, 1 MMA, 2..9 compute.  Compute warp w owns query row
+// Warps: 0 TMA, 1 and 10 MMA issuers, 2..9 compute.  MMA issue blocks until
+// the tensor core takes the product, so one thread issuing everything would
+// put the S chain (S(j+1), needed by P) behind the dQ/dP chain (dQ(j),
+// dP(j+1), needed by dS): warp 1 issues S, warp 10 dQ and dP.  Each
+// product that overwrites a TMEM operand comes from the same thread as the
+// product reading it, after it in issue order.  Compute warp w owns query row
 // (w % 4) * 32 + lane and key columns [64h, 64h+64), h = (w - 2) / 4; the
 // row's log-sum-exp and dO.O sum are per-thread scalars.  P stays in
 // registers (bf16 pairs); dS goes over the first 32 of the warp's 64 dP
 // columns.
-// TMEM: S [0,128), dP/dS [128,256), dQ [256, 256+D), Q [256+D, 256+1.5D),
-//       dO [256+1.5D, 256+2D).
-// MMA order: S(j+1) once S(j) is read; dQ(j), then dP(j+1), which
-// overwrites dS(j) after dQ(j) in issue order.
+// TMEM: S [0,128), dP [128,256), dQ [256, 256+D), Q [256+D, 256+1.5D),
+//       dO [256+1.5D, 256+2D); head dims up to 96 keep dS in its own
+//       region [256+2D, 256+2D+64), 112 and 128 over dP.
+// Issue order: warp 1 S(j+1) once S(j) is read.  Warp 10, with a separate
+// dS region: dP(j+1) once dP(j) is read, then dQ(j) once dS(j) is written
+// (so the compute warps never wait for dP); with dS over dP: dQ(j), then
+// dP(j+1), which overwrites dS(j) after dQ(j).
 template <int D>
 struct DqCfg {
   using T = TileGeom<D>;
   static constexpr int KVS_FIT = (232448 - 1280) / (2 * T::TILE);
   static constexpr int KVS = KVS_FIT > 5 ? 5 : KVS_FIT;
   static constexpr int SMEM = KVS * 2 * T::TILE + 1024 + 256;
-  static constexpr uint32_t COL_DQ = 256, COL_Q = 256 + D, COL_DO = 256 + D + D / 2;
+  static constexpr uint32_t COL_DQ = 256, COL_Q = 256 + D, COL_DO = 256 + D + D / 2, COL_DS = 256 + 2 * D;
+  static constexpr bool SEP_DS = COL_DS + 64 <= 512;
 };
 
 
 template <int D>
-__global__ void __launch_bounds__(320, 1) attn_dq_kernel(const __grid_constant__ AttnBwdParams p) {
+__global__ void __launch_bounds__(352, 1) attn_dq_kernel(const __grid_constant__ AttnBwdParams p) {
   using T = TileGeom<D>;
   using C = DqCfg<D>;
   constexpr int KVS = C::KVS;
@@ -768,10 +777,11 @@ __global__ void __launch_bounds__(320, 1) attn_dq_kernel(const __grid_constant__
   uint64_t* s_full = kv_empty + KVS;   // S(j) in TMEM
   uint64_t* s_free = s_full + 1;       // S(j) read (8 compute warps)
   uint64_t* dp_full = s_free + 1;      // dP(j) in TMEM
-  uint64_t* ds_full = dp_full + 1;     // dS(j) written (8 compute warps)
+  uint64_t* dp_free = dp_full + 1;     // dP(j) read (8 compute warps; separate dS only)
+  uint64_t* ds_full = dp_free + 1;     // dS(j) written (8 compute warps)
   uint64_t* dq_done = ds_full + 1;     // dQ(j) done
-  uint64_t* drain = dq_done + 1;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* drain = dq_done + 1;       // [2], one per issuer
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = warp_id();
@@ -796,9 +806,11 @@ __global__ void __launch_bounds__(320, 1) attn_dq_kernel(const __grid_constant__
     mbar_init(s_full, 1);
     mbar_init(s_free, 8);
     mbar_init(dp_full, 1);
+    mbar_init(dp_free, 8);
     mbar_init(ds_full, 8);
     mbar_init(dq_done, 1);
-    mbar_init(drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -816,6 +828,8 @@ __global__ void __launch_bounds__(320, 1) attn_dq_kernel(const __grid_constant__
   const uint32_t tdQ = tmem + C::COL_DQ;
   const uint32_t tQA = tmem + C::COL_Q;
   const uint32_t tOA = tmem + C::COL_DO;
+  // dS: its own region, or over the first 32 of each warp's 64 dP columns
+  const uint32_t tDS = C::SEP_DS ? tmem + C::COL_DS : tdP;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -839,10 +853,13 @@ __global__ void __launch_bounds__(320, 1) attn_dq_kernel(const __grid_constant__
           bounded_wait(&kv_full[jt % KVS], (jt / KVS) & 1, abort_flag, 602, p.err);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 10) {
     if (lane == 0) {
-      // ------------------------------------------------ MMA issuer
+      // ------------------------------------------------ MMA issuers
       const uint32_t uKV = smem_u32(sKV);
+      const bool is_s = warp == 1;
+      bool ok = bounded_wait(qo_ready, 0, abort_flag, 611, p.err) &&
+                bounded_wait(&kv_full[0], 0, abort_flag, 612, p.err);
       auto issue_s = [&](int jt) {
         const uint32_t uK = uKV + (jt % KVS) * 2 * T::TILE;
 #pragma unroll
@@ -855,40 +872,56 @@ __global__ void __launch_bounds__(320, 1) attn_dq_kernel(const __grid_constant__
         for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a(tdP, tOA + kk * 8, T::kmajor(uV, kk), ID_SQ, kk > 0);
         umma_commit(dp_full);
       };
-      bool ok = bounded_wait(qo_ready, 0, abort_flag, 611, p.err) &&
-                bounded_wait(&kv_full[0], 0, abort_flag, 612, p.err);
       if (ok) {
         tc_fence_after();
-        issue_s(0);
-        issue_dp(0);
+        if (is_s) issue_s(0); else issue_dp(0);
       }
       for (int jt = 0; ok && jt < nkv; ++jt) {
         const bool more = jt + 1 < nkv;
-        if (more) {
+        if (is_s) {
+          // S(j+1) once the compute warps have read S(j)
+          if (!more) break;
           if (!bounded_wait(s_free, jt & 1, abort_flag, 613, p.err)) { ok = false; break; }
           if (!bounded_wait(&kv_full[(jt + 1) % KVS], ((jt + 1) / KVS) & 1, abort_flag, 614, p.err)) { ok = false; break; }
           tc_fence_after();
           issue_s(jt + 1);
-        }
-        // dQ += dS(j) K_j; the dS pairs of key columns 64h.. sit at TMEM
-        // column 128 + 64h
-        if (!bounded_wait(ds_full, jt & 1, abort_flag, 615, p.err)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t uK = uKV + (jt % KVS) * 2 * T::TILE;
+        } else {
+          if (C::SEP_DS && more) {
+            // dP(j+1) once the compute warps have read dP(j)
+            if (!bounded_wait(dp_free, jt & 1, abort_flag, 617, p.err)) { ok = false; break; }
+            if (!bounded_wait(&kv_full[(jt + 1) % KVS], ((jt + 1) / KVS) & 1, abort_flag, 616, p.err)) { ok = false; break; }
+            tc_fence_after();
+            issue_dp(jt + 1);
+          }
+          // dQ += dS(j) K_j: the dS pairs of key columns 64h.. sit at column
+          // 32h of the dS region, or at column 128 + 64h over dP
+          if (!bounded_wait(ds_full, jt & 1, abort_flag, 615, p.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t uK = uKV + (jt % KVS) * 2 * T::TILE;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_tmem_a(tdQ, tdP + (kk >> 2) * 64 + (kk & 3) * 8, T::mnmajor(uK, kk), ID_DQ, (jt > 0 || kk > 0));
-        umma_commit(&kv_empty[jt % KVS]);
-        umma_commit(dq_done);
-        if (more) issue_dp(jt + 1);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t a = C::SEP_DS ? tDS + kk * 8 : tdP + (kk >> 2) * 64 + (kk & 3) * 8;
+            umma_bf16_tmem_a(tdQ, a, T::mnmajor(uK, kk), ID_DQ, (jt > 0 || kk > 0));
+          }
+          // the last readers of stage j: S(j) (complete: the compute warps
+          // read it before forming dS(j)), dP(j) and dQ(j) (this thread)
+          umma_commit(&kv_empty[jt % KVS]);
+          umma_commit(dq_done);
+          if (!C::SEP_DS && more) {
+            if (!bounded_wait(&kv_full[(jt + 1) % KVS], ((jt + 1) / KVS) & 1, abort_flag, 616, p.err)) { ok = false; break; }
+            tc_fence_after();
+            issue_dp(jt + 1);
+          }
+        }
       }
       if (!ok) {
-        umma_commit(drain);
-        bounded_wait(drain, 0, abort_flag, 619, p.err);
+        umma_commit(&drain[is_s ? 0 : 1]);
+        bounded_wait(&drain[is_s ? 0 : 1], 0, abort_flag, 619, p.err);
       }
     }
   } else {
-    // ------------------------------------------------ compute (warps 2..9)
+    // ------------------------------------------------ compute (warps 2..9;
+    // lanes 1..31 of the issuer warps fall through to the final barrier)
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
@@ -960,6 +993,12 @@ __global__ void __launch_bounds__(320, 1) attn_dq_kernel(const __grid_constant__
       tmem_ld32_nw(tdP + lane_off + c0, dr);
       tmem_ld32_nw(tdP + lane_off + c0 + 32, dr + 32);
       tmem_wait_ld(dr);
+      if constexpr (C::SEP_DS) {
+        // dP(j+1) may now overwrite dP(j)
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(dp_free);
+      }
       uint32_t o[32];
 #pragma unroll
       for (int k = 0; k < 64; k += 2) {
@@ -967,7 +1006,18 @@ __global__ void __launch_bounds__(320, 1) attn_dq_kernel(const __grid_constant__
         o[k / 2] = pack_bf16(bf16_lo(pw) * (__uint_as_float(dr[k]) - dsum),
                              bf16_hi(pw) * (__uint_as_float(dr[k + 1]) - dsum));
       }
-      tmem_st32(tdP + lane_off + c0, o);
+      if constexpr (C::SEP_DS) {
+        // dQ(j-1) has read the previous dS; waiting every step keeps these
+        // warps within one phase of dq_done
+        if (jt >= 1) {
+          ok = bounded_wait(dq_done, (jt - 1) & 1, abort_flag, 623, p.err);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          tc_fence_after();
+        }
+        tmem_st32(tDS + lane_off + half * 32, o);
+      } else {
+        tmem_st32(tdP + lane_off + c0, o);
+      }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -1040,7 +1090,7 @@ int launch_dq(AttnBwdParams& prm, int grid, cudaStream_t st) {
       return 3;
     attr = true;
   }
-  attn_dq_kernel<D><<<grid, 320, SMEM, st>>>(prm);
+  attn_dq_kernel<D><<<grid, 352, SMEM, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 

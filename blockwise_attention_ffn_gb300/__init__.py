@@ -91,6 +91,8 @@ def lib() -> ctypes.CDLL:
         dp = ctypes.POINTER(ctypes.c_double)
         L.bpt_profile_collect.argtypes = [i32, dp, dp, dp, ctypes.POINTER(ctypes.c_int)]
         L.bpt_profile_collect.restype = i32
+        L.bpt_profile_list.argtypes = [i32, ctypes.POINTER(ctypes.c_int), dp, dp, dp]
+        L.bpt_profile_list.restype = i32
         _lib = L
     return _lib
 
@@ -224,6 +226,18 @@ def bpt_profile_collect() -> dict:
     _check(lib().bpt_profile_collect(n, ms, fl, by, la), "bpt_profile_collect")
     return {k: dict(ms=ms[i], flops=fl[i], bytes=by[i], launches=la[i])
             for i, k in enumerate(PROF_KINDS)}
+
+
+def bpt_profile_list(max_launches: int = 4096) -> list:
+    """[(kind, flops, bytes, ms)] of every launch recorded since the last
+    collect, in launch order (does not clear the record)."""
+    n = max_launches
+    kd = (ctypes.c_int * n)()
+    fl, by, ms = (ctypes.c_double * n)(), (ctypes.c_double * n)(), (ctypes.c_double * n)()
+    got = lib().bpt_profile_list(n, kd, fl, by, ms)
+    if got < 0:
+        _check(-got, "bpt_profile_list")
+    return [(PROF_KINDS[kd[i]], fl[i], by[i], ms[i]) for i in range(got)]
 
 
 # ------------------------------------------------------------------ helpers

@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 #include <vector>
 
@@ -159,6 +160,23 @@ int bpt_profile_enable(int on) {
   bpt::g_prof_on = on != 0;
   bpt::g_prof_used = 0;
   return BPT_OK;
+}
+
+int bpt_profile_list(int max, int* kind, double* flops, double* bytes, double* ms) {
+  if (max < 0 || (max > 0 && (!kind || !flops || !bytes || !ms))) return -BPT_EINVAL;
+  std::lock_guard<std::mutex> lk(bpt::g_prof_mu);
+  const int n = (int)std::min<size_t>((size_t)max, bpt::g_prof_used);
+  for (int i = 0; i < n; ++i) {
+    auto& r = bpt::g_prof[i];
+    if (cudaEventSynchronize(r.b) != cudaSuccess) return -BPT_ECUDA;
+    float t = 0;
+    if (cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) return -BPT_ECUDA;
+    kind[i] = r.kind;
+    flops[i] = r.flops;
+    bytes[i] = r.bytes;
+    ms[i] = t;
+  }
+  return n;
 }
 
 int bpt_profile_collect(int nkinds, double* ms, double* flops, double* bytes, int* launches) {

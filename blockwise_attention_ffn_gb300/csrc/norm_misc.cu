@@ -104,14 +104,22 @@ __global__ void norm_fwd_kernel(int64_t rows, int h, int kind, float eps, const 
 // dx = res + rstd * (g - mean(g) - xhat * mean(g * xhat))    (LayerNorm)
 //    = res + rstd * (g - xhat * mean(g * xhat))              (RMSNorm)
 // with g = dy * w; dw += sum_rows dy * xhat, db += sum_rows dy.
-__global__ void norm_bwd_kernel(int64_t rows, int h, int kind, float eps, NormBwdIO io,
-                                const __nv_bfloat16* w, float* dw, float* db) {
-  extern __shared__ float red[];  // [2h]: dw and db partials of this block
-  for (int c = threadIdx.x; c < 2 * h; c += blockDim.x) red[c] = 0.f;
-  __syncthreads();
+// Two phases per block, over a band of rows:
+//  1. one warp per row: the row's mean and rstd (as the forward computes
+//     them), and the two row sums of the gradient, into shared memory;
+//  2. each thread owns 8 columns (the block spans the row): for every row of
+//     the band it forms dx and accumulates dw, db in registers, so the
+//     scale/shift gradients take one global atomic per column per block and
+//     no shared-memory atomics at all.
+__global__ void __launch_bounds__(512) norm_bwd_kernel(int64_t rows, int h, int kind, float eps, NormBwdIO io,
+                                                        const __nv_bfloat16* w, float* dw, float* db,
+                                                        int64_t band) {
+  extern __shared__ float stat[];  // [band][4]: mean, rstd, mean(g), mean(g * xhat)
   const int lane = threadIdx.x & 31;
-  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
+  const int nwarp = blockDim.x >> 5;
+  const int64_t r0 = (int64_t)blockIdx.x * band;
+  const int64_t r1 = min(rows, r0 + band);
+  for (int64_t r = r0 + (threadIdx.x >> 5); r < r1; r += nwarp) {
     float mean, rstd;
     row_stats(io.x, io.x_f32, r * io.ldx, h, kind, eps, mean, rstd);
     float sg = 0.f, sgx = 0.f;
@@ -122,27 +130,39 @@ __global__ void norm_bwd_kernel(int64_t rows, int h, int kind, float eps, NormBw
       ld8x(io.dy, io.dy_f32, r * io.lddy + c, gv);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const float xh = (v[k] - mean) * rstd;
         const float g = gv[k] * wv[k];
         sg += g;
-        sgx += g * xh;
-        atomicAdd(&red[c + k], gv[k] * xh);
-        atomicAdd(&red[h + c + k], gv[k]);
+        sgx += g * (v[k] - mean) * rstd;
       }
     }
     sg = warp_sum(sg) / h;
     sgx = warp_sum(sgx) / h;
-    if (kind != 0) sg = 0.f;
-    for (int c = lane * 8; c < h; c += 256) {
-      float v[8], wv[8], gv[8], rv[8];
+    if (lane == 0) {
+      float* o = stat + (r - r0) * 4;
+      o[0] = mean;
+      o[1] = rstd;
+      o[2] = (kind == 0) ? sg : 0.f;
+      o[3] = sgx;
+    }
+  }
+  __syncthreads();
+  for (int c = threadIdx.x * 8; c < h; c += blockDim.x * 8) {
+    float wv[8], adw[8], adb[8];
+    ld8(w + c, wv);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) adw[k] = adb[k] = 0.f;
+    for (int64_t r = r0; r < r1; ++r) {
+      const float4 s4 = *reinterpret_cast<const float4*>(stat + (r - r0) * 4);
+      float v[8], gv[8], rv[8];
       ld8x(io.x, io.x_f32, r * io.ldx + c, v);
-      ld8(w + c, wv);
       ld8x(io.dy, io.dy_f32, r * io.lddy + c, gv);
       if (io.res) ld8x(io.res, io.res_f32, r * io.ldres + c, rv);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const float xh = (v[k] - mean) * rstd;
-        v[k] = rstd * (gv[k] * wv[k] - sg - xh * sgx) + (io.res ? rv[k] : 0.f);
+        const float xh = (v[k] - s4.x) * s4.y;
+        adw[k] += gv[k] * xh;
+        adb[k] += gv[k];
+        v[k] = s4.y * (gv[k] * wv[k] - s4.z - xh * s4.w) + (io.res ? rv[k] : 0.f);
       }
       st8(reinterpret_cast<__nv_bfloat16*>(io.dx) + r * io.lddx + c, v);
       if (io.dx_f32) {
@@ -151,11 +171,11 @@ __global__ void norm_bwd_kernel(int64_t rows, int h, int kind, float eps, NormBw
         o[1] = make_float4(v[4], v[5], v[6], v[7]);
       }
     }
-  }
-  __syncthreads();
-  for (int c = threadIdx.x; c < h; c += blockDim.x) {
-    if (dw) atomicAdd(&dw[c], red[c]);
-    if (db) atomicAdd(&db[c], red[h + c]);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (dw) atomicAdd(&dw[c + k], adw[k]);
+      if (db) atomicAdd(&db[c + k], adb[k]);
+    }
   }
 }
 
@@ -275,25 +295,24 @@ int norm_fwd(int64_t rows, int h, int kind, float eps, const void* x, int x_f32,
 int norm_bwd(int64_t rows, int h, int kind, float eps, const NormBwdIO& io, const void* w, float* dw,
              float* db, cudaStream_t st) {
   if (rows <= 0) return 0;
-  const int threads = 256;
-  const size_t smem = (size_t)2 * h * sizeof(float);
-  if (smem > 200 * 1024) return 1;
-  if (smem > 48 * 1024) {
-    static bool attr = false;
-    if (!attr) {
-      if (cudaFuncSetAttribute(norm_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
-          cudaSuccess)
-        return 3;
-      attr = true;
-    }
-  }
-  int grid = (int)((rows + 7) / 8);
-  if (grid > 152 * 2) grid = 152 * 2;
+  // one thread per 8 columns (a whole row per block up to h = 4096), 64..512
+  // threads
+  int threads = (h / 8 + 31) / 32 * 32;
+  if (threads < 64) threads = 64;
+  if (threads > 512) threads = 512;
+  // about two blocks per SM, bands of at least 8 rows
+  const int nsm = sm_count();
+  int64_t band = (rows + 2 * (int64_t)(nsm > 0 ? nsm : 1) - 1) / (2 * (int64_t)(nsm > 0 ? nsm : 1));
+  if (band < 8) band = 8;
+  if (band > 2048) band = 2048;
+  const int64_t grid = (rows + band - 1) / band;
+  const size_t smem = (size_t)band * 4 * sizeof(float);
   ProfScope prof(PROF_NORM, 0.0,
                  (double)rows * h * ((io.dy_f32 ? 4 : 2) + (io.x_f32 ? 4 : 2) + (io.res ? (io.res_f32 ? 4 : 2) : 0) + 2 +
                                      (io.dx_f32 ? 4 : 0)),
                  st);
-  norm_bwd_kernel<<<grid, threads, smem, st>>>(rows, h, kind, eps, io, (const __nv_bfloat16*)w, dw, db);
+  norm_bwd_kernel<<<(unsigned)grid, threads, smem, st>>>(rows, h, kind, eps, io, (const __nv_bfloat16*)w, dw, db,
+                                                         band);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 

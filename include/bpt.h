@@ -216,6 +216,13 @@ int bpt_attention_bwd_noalloc(const bpt_config* cfg, const void* qkv, const void
  * backward, 3 norms, 4 other memory-bound kernels. */
 int bpt_profile_enable(int on);
 int bpt_profile_collect(int nkinds, double* ms, double* flops, double* bytes, int* launches);
+/* The launches recorded since profiling was enabled (or last collected), in
+ * launch order: for i < the returned count (at most max), the kind, the
+ * algorithmic FLOPs and bytes credited to launch i and its device time in
+ * ms.  Synchronises on the recorded events; does not clear the record
+ * (bpt_profile_collect does).  Returns the count, or minus a status code.
+ * A diagnostic aid: the layer has no such step in the paper. */
+int bpt_profile_list(int max, int* kind, double* flops, double* bytes, double* ms);
 
 /* Text of a status code (static storage). */
 const char* bpt_status_string(int status);

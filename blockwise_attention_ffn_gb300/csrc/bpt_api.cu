@@ -233,6 +233,42 @@ AttnBwdShape stage_bwd_shape(const Dims& D, int64_t k) {
 // out[M, N] (fp32, beta) = sum_i A[:, Kseg_i] B_i  with MN-major B segments;
 // one launch when the segment boundaries are multiples of 64, else one per
 // segment with accumulation.
+// A second stream, per device and host thread, for launches that do not feed
+// the next launch of the main chain (weight gradients beside activation
+// gradients): they fill the SMs the main chain's kernels leave idle in their
+// last, partial wave.  fork: the side stream waits for all work issued on the
+// main stream so far; join: the main stream waits for all work issued on the
+// side stream so far.  Created on the first backward call of a thread on a
+// device.
+struct Side {
+  cudaStream_t s = nullptr;
+  cudaEvent_t ev[8] = {};
+  int next = 0;
+};
+
+Side* side_stream() {
+  static thread_local Side sides[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  Side& sd = sides[dev];
+  if (!sd.s) {
+    if (cudaStreamCreateWithFlags(&sd.s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    for (auto& e : sd.ev)
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+  }
+  return &sd;
+}
+
+int fork_side(cudaStream_t main, Side* sd) {
+  cudaEvent_t e = sd->ev[sd->next++ % 8];
+  return (cudaEventRecord(e, main) == cudaSuccess && cudaStreamWaitEvent(sd->s, e, 0) == cudaSuccess) ? 0 : BPT_ECUDA;
+}
+
+int join_side(cudaStream_t main, Side* sd) {
+  cudaEvent_t e = sd->ev[sd->next++ % 8];
+  return (cudaEventRecord(e, sd->s) == cudaSuccess && cudaStreamWaitEvent(main, e, 0) == cudaSuccess) ? 0 : BPT_ECUDA;
+}
+
 int gemm_kseg(int64_t M, int64_t N, const MatView& A, const MatView* B, const int64_t* ks, int nseg,
               const Epilogue& e0, cudaStream_t st) {
   bool ok = true;
@@ -495,6 +531,9 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
   if (ws_bytes < plan_bwd(D, nullptr, &W)) return BPT_ENOSPC;
   plan_bwd(D, ws, &W);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Side* sd = side_stream();
+  if (!sd) return BPT_ECUDA;
+  cudaStream_t ss = sd->s;
   const float* lse = reinterpret_cast<const float*>(saved);
   const bool hb = cfg->has_bias != 0;
   const bool accum = (cfg->flags & BPT_FLAG_ACCUM_GRADS) != 0;
@@ -536,6 +575,9 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
         e.ldr = h;
         if ((rc = gemm(nr, h, Hd, A, false, &B, &Hd, 1, false, nullptr, e, st))) return rc;
       }
+      // the previous block's weight gradients (side stream) still read x1n,
+      // a and dz, which this block now rewrites
+      if (!first && (rc = join_side(st, sd))) return rc;
       if ((rc = norm_fwd(nr, (int)h, cfg->norm, cfg->norm_eps, W.x1, 1, h, w->ln2_w, w->ln2_b, W.x1n, h, st)))
         return rc;
       {
@@ -562,6 +604,20 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
         }
       }
       const void* dyb = bf(dy, row * h);
+      // side stream: the fc2 weight gradient needs only dy and a
+      if ((rc = fork_side(st, sd))) return rc;
+      // dW2 (+)= dy^T a ; db2 (+)= colsum(dy)
+      {
+        MatView A{dyb, nr, h, h};     // MN-major: [K = rows, M = h]
+        MatView B{W.a, nr, f, f};     // MN-major: [K = rows, N = f]
+        Epilogue e;
+        e.kind = EPI_F32;
+        e.out = g->w2;
+        e.ldo = f;
+        e.beta = beta;
+        if ((rc = gemm(h, f, nr, A, true, &B, &nr, 1, true, nullptr, e, ss))) return rc;
+        if (hb && (rc = colsum(nr, h, dyb, h, reinterpret_cast<float*>(g->b2), beta != 0.f, ss))) return rc;
+      }
       // dA = dy W2, fused with the activation gradient
       {
         MatView A{dyb, nr, h, h};
@@ -587,18 +643,8 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
         }
         if ((rc = gemm(nr, f, h, A, false, &B, &h, 1, true, nullptr, e, st))) return rc;
       }
-      // dW2 (+)= dy^T a ; db2 (+)= colsum(dy)
-      {
-        MatView A{dyb, nr, h, h};     // MN-major: [K = rows, M = h]
-        MatView B{W.a, nr, f, f};     // MN-major: [K = rows, N = f]
-        Epilogue e;
-        e.kind = EPI_F32;
-        e.out = g->w2;
-        e.ldo = f;
-        e.beta = beta;
-        if ((rc = gemm(h, f, nr, A, true, &B, &nr, 1, true, nullptr, e, st))) return rc;
-        if (hb && (rc = colsum(nr, h, dyb, h, reinterpret_cast<float*>(g->b2), beta != 0.f, st))) return rc;
-      }
+      // side stream: the fc1 weight (and bias) gradients need only dz and x1n
+      if ((rc = fork_side(st, sd))) return rc;
       // dW1 (+)= dz^T x1n (SwiGLU: dWg from dg, dWu from du) ; db1
       {
         const int64_t ldz = swiglu ? 2 * f : f;
@@ -609,13 +655,13 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
         e.beta = beta;
         MatView A{W.dz, nr, f, ldz};
         e.out = g->w1;
-        if ((rc = gemm(f, h, nr, A, true, &B, &nr, 1, true, nullptr, e, st))) return rc;
+        if ((rc = gemm(f, h, nr, A, true, &B, &nr, 1, true, nullptr, e, ss))) return rc;
         if (swiglu) {
           MatView A2{bf(W.dz, f), nr, f, ldz};
           e.out = g->w3;
-          if ((rc = gemm(f, h, nr, A2, true, &B, &nr, 1, true, nullptr, e, st))) return rc;
+          if ((rc = gemm(f, h, nr, A2, true, &B, &nr, 1, true, nullptr, e, ss))) return rc;
         } else if (hb) {
-          if ((rc = colsum(nr, f, W.dz, f, reinterpret_cast<float*>(g->b1), beta != 0.f, st))) return rc;
+          if ((rc = colsum(nr, f, W.dz, f, reinterpret_cast<float*>(g->b1), beta != 0.f, ss))) return rc;
         }
       }
       // dx1n = dz W1  (SwiGLU: dg Wg + du Wu)
@@ -651,13 +697,11 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
   }
 
   // ---- output projection: dO = dx1 Wo ; dWo (+)= dx1^T O ; dbo
+  if ((rc = join_side(st, sd))) return rc;
+  if ((rc = fork_side(st, sd))) return rc;
   {
-    MatView A{W.dx1, D.rows, h, h};
-    MatView B{w->wo, h, Hd, Hd};  // [K = h rows, N = Hd cols]
-    Epilogue e;
-    e.out = W.dO;
-    e.ldo = Hd;
-    if ((rc = gemm(D.rows, Hd, h, A, false, &B, &h, 1, true, nullptr, e, st))) return rc;
+    // side stream: dWo and dbo need only dx1 and O, and run beside dO and
+    // the attention backward
     MatView A2{W.dx1, D.rows, h, h};
     MatView B2{W.o, D.rows, Hd, Hd};
     Epilogue e2;
@@ -666,13 +710,22 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
     e2.ldo = Hd;
     e2.beta = accum ? 1.f : 0.f;
     const int64_t K = D.rows;
-    if ((rc = gemm(h, Hd, K, A2, true, &B2, &K, 1, true, nullptr, e2, st))) return rc;
-    if (hb && (rc = colsum(D.rows, h, W.dx1, h, reinterpret_cast<float*>(g->bo), accum, st))) return rc;
+    if ((rc = gemm(h, Hd, K, A2, true, &B2, &K, 1, true, nullptr, e2, ss))) return rc;
+    if (hb && (rc = colsum(D.rows, h, W.dx1, h, reinterpret_cast<float*>(g->bo), accum, ss))) return rc;
+    MatView A{W.dx1, D.rows, h, h};
+    MatView B{w->wo, h, Hd, Hd};  // [K = h rows, N = Hd cols]
+    Epilogue e;
+    e.out = W.dO;
+    e.ldo = Hd;
+    if ((rc = gemm(D.rows, Hd, h, A, false, &B, &h, 1, true, nullptr, e, st))) return rc;
   }
 
   // ---- attention and Q/K/V gradients, stage by stage
   for (int64_t k = 0; k < D.n_stages; ++k) {
     if (D.chunked && (rc = stage_qkv(D, w, hb, W.xn, W.qkv, k, st))) return rc;
+    // the previous stage's weight gradients (side stream) read dqkv, which
+    // this stage's attention backward rewrites
+    if (k > 0 && (rc = join_side(st, sd))) return rc;
     AttnBwdShape sb = stage_bwd_shape(D, k);
     sb.f.causal = cfg->causal;
     if ((rc = attention_bwd(sb, W.qkv, W.o, lse, W.dO, W.dqkv, W.attn, st))) return rc;
@@ -690,7 +743,9 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
       e.beta = k > 0 ? 1.f : 0.f;
       if ((rc = gemm_kseg(D.rows, h, A, Bs, ks, 3, e, st))) return rc;
     }
-    // dWq_s, dWk_s, dWv_s (+)= dQKV_s^T xn ; biases
+    // dWq_s, dWk_s, dWv_s (+)= dQKV_s^T xn ; biases, on the side stream
+    // beside dxn
+    if ((rc = fork_side(st, sd))) return rc;
     {
       struct Piece {
         void* G;
@@ -706,8 +761,8 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
         e.out = f32(pc.G, pc.row0 * h);
         e.ldo = h;
         e.beta = accum ? 1.f : 0.f;
-        if ((rc = gemm(pc.n, h, K, A, true, &B, &K, 1, true, nullptr, e, st))) return rc;
-        if (hb && (rc = colsum(D.rows, pc.n, bf(W.dqkv, pc.col), D.qkv_w, f32(pc.Gb, pc.row0), accum, st)))
+        if ((rc = gemm(pc.n, h, K, A, true, &B, &K, 1, true, nullptr, e, ss))) return rc;
+        if (hb && (rc = colsum(D.rows, pc.n, bf(W.dqkv, pc.col), D.qkv_w, f32(pc.Gb, pc.row0), accum, ss)))
           return rc;
       }
     }
@@ -720,7 +775,9 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
                        ln ? reinterpret_cast<float*>(g->ln1_b) : nullptr, st)))
       return rc;
   }
-  return BPT_OK;
+  // everything issued on the side stream is ordered before the caller's next
+  // work on the main stream
+  return join_side(st, sd) ? BPT_ECUDA : BPT_OK;
 }
 
 }  // extern "C"

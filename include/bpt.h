@@ -145,7 +145,12 @@ int bpt_layer_fwd(const bpt_config* cfg, const bpt_weights* w, const void* x, vo
  * The forward pass is rerun blockwise (N1, Q/K/V, attention, output
  * projection, and per FFN block N2 and fc1) and every gradient is formed
  * from the rebuilt blocks: attention probabilities are rebuilt from Q, K and
- * the saved log-sum-exp tile by tile. */
+ * the saved log-sum-exp tile by tile.
+ * Weight gradients that the next launch of the chain does not need run on a
+ * second stream the library creates (one per device and host thread, on the
+ * first call) and joins back into `stream` before returning: all of the
+ * call's work is ordered before later work on `stream`.  Make the first call
+ * of a thread before capturing `stream` into a graph. */
 int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, const void* saved,
                   const void* dy, void* dx, const bpt_grads* grads, void* ws, size_t ws_bytes,
                   void* stream);

@@ -188,7 +188,7 @@ def bpt_attention_bwd(cfg, qkv, o, lse, dout, dqkv, ws, stream=None) -> None:
     _check(rc, "bpt_attention_bwd")
 
 
-NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
+NOALLOC_SCRATCH_BYTES = 192 * 1024 * 1024
 
 
 def bpt_attention_bwd_noalloc(cfg, qkv, o, lse, dout, dqkv, stream=None) -> None:

@@ -28,6 +28,7 @@
 
 #include <algorithm>
 
+#include "../../include/bpt.h"
 #include "attn_common.cuh"
 #include "internal.h"
 
@@ -38,6 +39,7 @@ namespace {
 struct AttnBwdParams {
   CUtensorMap map_qkv;  // 3-D {ld_qkv, s, b}, box {CW, 128, 1}
   CUtensorMap map_do;   // 3-D {ld_do, s, b}, box {CW, 128, 1}
+  CUtensorMap map_aux;  // 2-D {8, b*H*s_pad} bf16, box {8, 128}, no swizzle
   int s, s_pad, H, Hkv, G, causal, b;
   int q_col, k_col, v_col, do_col;
   const float* lse;     // [b, H_total, s_pad] at head offset lse_head0
@@ -396,13 +398,24 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_kernel(const __grid_constant
 // as the A operands of S^T = K Q^T and dP^T = V dO^T; P^T is written over
 // S^T and dS^T over dP^T (bf16 pairs), the A operands of dV = P^T dO and
 // dK = dS^T Q.  Shared memory holds only the Q/dO ring.
+// The per-query-column terms of the softmax gradient (-LSE and -D) enter
+// through the products too: one more contraction step multiplies a 16-column
+// chunk appended to K (1, 1, 0, ...) or V (0, 0, 1, 1, 0, ...) in TMEM with
+// the query row (hi(-LSE*sqrt(d)), lo(..), hi(-D), lo(-D), 0, ...), so S^T
+// comes out offset by -LSE*sqrt(d) and dP^T by -D: the compute warps read no
+// per-column values from shared memory, whose bandwidth the products already
+// use.  The row's 8 nonzero-capable columns arrive with the Q/dO stage
+// (16 bytes per query, unswizzled: exactly the K-major core-matrix layout);
+// the descriptor points its upper 8 columns at one shared 2 KB of zeros.
 // Warps: 0 TMA, 1 MMA, 2..9 compute.  Compute warp w owns key/value rows
 // (w % 4) * 32 + lane (its TMEM lane quarter) and query columns
 // [64h, 64h+64), h = (w - 2) / 4.  Per step it forms P^T for its columns
 // (kept in registers as bf16 pairs and stored over the first 32 of its 64
 // S^T columns), then dS^T (stored over the first 32 of its dP^T columns).
 // TMEM: S^T/P^T [0,128), dP^T/dS^T [128,256), dV [256, 256+D),
-//       dK [256+D, 256+2D), K [256+2D, 256+2.5D), V [256+2.5D, 256+3D).
+//       dK [256+D, 256+2D), K' [256+2D, 256+2.5D+8), V' [.., 256+3D+16).
+// Shared memory: QS stages of (Q, dO, the 128 query rows' 16-byte extra
+// rows), then the zeros.
 // MMA order per step t: dV(t), S(t+1), dK(t), dP(t+1).  A product that
 // overwrites the TMEM operand of the one issued before it relies on the
 // tensor pipe executing one thread's products in issue order.
@@ -410,9 +423,11 @@ template <int D>
 struct DkdvTmCfg {
   using T = TileGeom<D>;
   static constexpr int QS = 4;
-  static constexpr int STAGE = 2 * T::TILE + 2 * 512;  // Q, dO, -LSE*log2(e), D
-  static constexpr int SMEM = QS * STAGE + 1024 + 256;
-  static constexpr uint32_t COL_DV = 256, COL_DK = 256 + D, COL_K = 256 + 2 * D, COL_V = 256 + 2 * D + D / 2;
+  static constexpr int AUX = 128 * 16;                 // 128 query rows x 8 bf16
+  static constexpr int STAGE = 2 * T::TILE + AUX;      // Q, dO, extra rows
+  static constexpr int ZERO = 2048;                    // the upper 8 columns
+  static constexpr int SMEM = QS * STAGE + ZERO + 1024 + 256;
+  static constexpr uint32_t COL_DV = 256, COL_DK = 256 + D, COL_K = 256 + 2 * D, COL_V = 256 + 2 * D + D / 2 + 8;
 };
 
 template <int D>
@@ -421,14 +436,15 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_tm_kernel(const __grid_const
   using C = DkdvTmCfg<D>;
   constexpr int QS = C::QS;
   constexpr int STAGE = C::STAGE;
-  static_assert(C::COL_V + D / 2 <= 512, "TMEM columns");
+  static_assert(C::COL_V + D / 2 + 8 <= 512, "TMEM columns");
   constexpr uint32_t ID_SQ = idesc_bf16(128, 128, false, false);
   constexpr uint32_t ID_KV = idesc_bf16(128, D, false, true);
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sStage = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + QS * STAGE);
+  uint8_t* sZero = sStage + QS * STAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sZero + C::ZERO);
   uint64_t* kv_ready = bars;            // K, V copied into TMEM (8 compute warps)
   uint64_t* qdo_full = bars + 1;
   uint64_t* qdo_empty = qdo_full + QS;
@@ -474,10 +490,15 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_tm_kernel(const __grid_const
   if (warp == 0 && lane == 0) {
     tma_prefetch(&p.map_qkv);
     tma_prefetch(&p.map_do);
+    tma_prefetch(&p.map_aux);
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, 512);
     tmem_relinquish();
+  }
+  if (threadIdx.x < C::ZERO / 16) {
+    reinterpret_cast<uint4*>(sZero)[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
@@ -501,16 +522,14 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_tm_kernel(const __grid_const
         const int i = i0 + t % n_i;
         uint8_t* sQ = sStage + st * STAGE;
         uint8_t* sdO = sQ + T::TILE;
-        uint8_t* sL = sdO + T::TILE;
         mbar_expect_tx(&qdo_full[st], STAGE);
 #pragma unroll
         for (int c = 0; c < T::NCH; ++c) {
           tma_load_3d(sQ + c * T::CHUNK, &p.map_qkv, &qdo_full[st], p.q_col + hn * D + c * T::CW, i * 128, bi);
           tma_load_3d(sdO + c * T::CHUNK, &p.map_do, &qdo_full[st], p.do_col + hn * D + c * T::CW, i * 128, bi);
         }
-        const long long row = ((long long)bi * p.H + hn) * p.s_pad + i * 128;
-        bulk_load(sL, p.nl2 + row, 512, &qdo_full[st]);
-        bulk_load(sL + 512, p.Dsum + row, 512, &qdo_full[st]);
+        const int row = (bi * p.H + hn) * p.s_pad + i * 128;
+        tma_load_2d(sQ + 2 * T::TILE, &p.map_aux, &qdo_full[st], 0, row);
         issued = t + 1;
       }
       if (*abort_flag) {
@@ -522,16 +541,26 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_tm_kernel(const __grid_const
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
       auto stage_u = [&](int t) { return smem_u32(sStage + (t % QS) * STAGE); };
+      // one more contraction step each: the extra rows (8-row groups 128
+      // bytes apart, the upper 8 columns in the zeros) against the chunk
+      // appended to K resp. V
+      const uint32_t uZero = smem_u32(sZero);
+      auto aux_desc = [&](int t) {
+        const uint32_t uA = stage_u(t) + 2 * T::TILE;
+        return sdesc(uA, uZero - uA, 128, 0u);
+      };
       auto issue_s = [&](int t) {
         const uint32_t uQ = stage_u(t);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a(tS, tKA + kk * 8, T::kmajor(uQ, kk), ID_SQ, kk > 0);
+        umma_bf16_tmem_a(tS, tKA + D / 2, aux_desc(t), ID_SQ, 1);
         umma_commit(s_full);
       };
       auto issue_dp = [&](int t) {
         const uint32_t udO = stage_u(t) + T::TILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a(tdP, tVA + kk * 8, T::kmajor(udO, kk), ID_SQ, kk > 0);
+        umma_bf16_tmem_a(tdP, tVA + D / 2, aux_desc(t), ID_SQ, 1);
         umma_commit(dp_full);
       };
       bool ok = bounded_wait(kv_ready, 0, abort_flag, 581, p.err) &&
@@ -586,7 +615,7 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_tm_kernel(const __grid_const
     {
       // K (half 0) or V (half 1) row of this thread into TMEM as bf16 pairs;
       // rows past the sequence are zero
-      uint32_t w[D / 2];
+      uint32_t w[D / 2 + 8];
       const __nv_bfloat16* src = p.qkv + ((long long)bi * p.s + kvp) * p.ld_qkv + (half ? p.v_col : p.k_col) +
                                  (long long)g * D;
 #pragma unroll
@@ -598,9 +627,14 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_tm_kernel(const __grid_const
         w[4 * c + 2] = v.z;
         w[4 * c + 3] = v.w;
       }
+      // the extra chunk: K picks the (hi, lo) pair of -LSE*sqrt(d) (columns
+      // 0, 1 of the query's extra row), V that of -D (columns 2, 3)
+      w[D / 2] = half ? 0u : 0x3F803F80u;
+      w[D / 2 + 1] = half ? 0x3F803F80u : 0u;
+#pragma unroll
+      for (int c = 2; c < 8; ++c) w[D / 2 + c] = 0u;
       const uint32_t dst = (half ? tVA : tKA) + lane_off;
-      tmem_st32(dst, *reinterpret_cast<const uint32_t(*)[32]>(w));
-      if constexpr (D / 2 > 32) tmem_st8_nw(dst + 32, w + 32);
+      tmem_store_row<D / 2 + 8>(dst, w);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -611,14 +645,11 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_tm_kernel(const __grid_const
     for (int t = 0; t < T_iter; ++t) {
       const int st = t % QS;
       const int q0 = (i0 + t % n_i) * 128;
-      const float* sNL = reinterpret_cast<const float*>(sStage + st * STAGE + 2 * T::TILE) + c0;
-      const float* sD = reinterpret_cast<const float*>(sStage + st * STAGE + 2 * T::TILE + 512) + c0;
-      ok = bounded_wait(&qdo_full[st], (t / QS) & 1, abort_flag, 591, p.err) &&
-           bounded_wait(s_full, t & 1, abort_flag, 592, p.err);
+      ok = bounded_wait(s_full, t & 1, abort_flag, 592, p.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      // ---- phase 1: P^T = exp2(S^T * scale*log2(e) - LSE*log2(e)) for the
-      // 64 columns; columns [lo, hi) of this row are unmasked
+      // ---- phase 1: P^T = exp2(S'^T * scale*log2(e)) for the 64 columns
+      // (S' already offset by -LSE*sqrt(d)); columns [lo, hi) are unmasked
       int lo = 0, hi = min(64, p.s - (q0 + c0));
       if (p.causal) lo = max(0, kvp - (q0 + c0));
       if (kvp >= p.s) lo = 64;
@@ -630,29 +661,14 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_tm_kernel(const __grid_const
       uint32_t pk[32];
       if (!edge) {
 #pragma unroll
-        for (int k = 0; k < 64; k += 8) {
-          const float4 la = *reinterpret_cast<const float4*>(sNL + k);
-          const float4 lb = *reinterpret_cast<const float4*>(sNL + k + 4);
-          const float nl[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
-#pragma unroll
-          for (int m = 0; m < 4; ++m)
-            pk[k / 2 + m] = pack_bf16(ex2(fmaf(__uint_as_float(sv[k + 2 * m]), c, nl[2 * m])),
-                                      ex2(fmaf(__uint_as_float(sv[k + 2 * m + 1]), c, nl[2 * m + 1])));
-        }
+        for (int k = 0; k < 64; k += 2)
+          pk[k / 2] = pack_bf16(ex2(__uint_as_float(sv[k]) * c), ex2(__uint_as_float(sv[k + 1]) * c));
       } else {
 #pragma unroll
-        for (int k = 0; k < 64; k += 8) {
-          const float4 la = *reinterpret_cast<const float4*>(sNL + k);
-          const float4 lb = *reinterpret_cast<const float4*>(sNL + k + 4);
-          const float nl[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
-          float e[8];
-#pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            e[m] = ex2(fmaf(__uint_as_float(sv[k + m]), c, nl[m]));
-            if (k + m < lo || k + m >= hi) e[m] = 0.f;
-          }
-#pragma unroll
-          for (int m = 0; m < 4; ++m) pk[k / 2 + m] = pack_bf16(e[2 * m], e[2 * m + 1]);
+        for (int k = 0; k < 64; k += 2) {
+          const float e0 = (k < lo || k >= hi) ? 0.f : ex2(__uint_as_float(sv[k]) * c);
+          const float e1 = (k + 1 < lo || k + 1 >= hi) ? 0.f : ex2(__uint_as_float(sv[k + 1]) * c);
+          pk[k / 2] = pack_bf16(e0, e1);
         }
       }
       tmem_st32(tS + lane_off + c0, pk);
@@ -660,7 +676,8 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_tm_kernel(const __grid_const
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
-      // ---- phase 2: dS^T = P^T (dP^T - D) with P^T from registers
+      // ---- phase 2: dS^T = P^T dP'^T (dP' already offset by -D), P^T from
+      // registers
       ok = bounded_wait(dp_full, t & 1, abort_flag, 593, p.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
@@ -670,16 +687,9 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_tm_kernel(const __grid_const
       tmem_wait_ld(dr);
       uint32_t o[32];
 #pragma unroll
-      for (int k = 0; k < 64; k += 8) {
-        const float4 xa = *reinterpret_cast<const float4*>(sD + k);
-        const float4 xb = *reinterpret_cast<const float4*>(sD + k + 4);
-        const float dv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const uint32_t pw = pk[k / 2 + m];
-          o[k / 2 + m] = pack_bf16(bf16_lo(pw) * (__uint_as_float(dr[k + 2 * m]) - dv[2 * m]),
-                                   bf16_hi(pw) * (__uint_as_float(dr[k + 2 * m + 1]) - dv[2 * m + 1]));
-        }
+      for (int k = 0; k < 64; k += 2) {
+        const uint32_t pw = pk[k / 2];
+        o[k / 2] = pack_bf16(bf16_lo(pw) * __uint_as_float(dr[k]), bf16_hi(pw) * __uint_as_float(dr[k + 1]));
       }
       tmem_st32(tdP + lane_off + c0, o);
       tmem_st_wait();
@@ -1119,12 +1129,13 @@ int launch_both(AttnBwdParams& prm, const AttnShape& f, cudaStream_t st) {
 
 int make_attn_map(CUtensorMap* map, const void* qkv, int b, int s, int64_t ld, int d);
 int attn_dsum(const AttnBwdShape& sh, const void* o, const void* dout, const float* lse, float* Dsum,
-              float* NL2, int s_pad, cudaStream_t st);
+              float* NL2, void* AUX, int s_pad, cudaStream_t st);
 
-// workspace: the per-row dO.O sums D, then -LSE*log2(e), both [b, H, s_pad] fp32
+// workspace: the per-row dO.O sums D and -LSE*log2(e), both [b, H, s_pad]
+// fp32, then the dK/dV kernel's extra query rows [b, H, s_pad, 8] bf16
 size_t attention_bwd_ws_bytes(const AttnBwdShape& sh) {
   const int64_t s_pad = ((int64_t)sh.f.s + 127) / 128 * 128;
-  return (size_t)sh.f.b * sh.f.H * s_pad * 8;
+  return (size_t)sh.f.b * sh.f.H * s_pad * (8 + 16);
 }
 
 // lse: [b, H_total, s_pad] fp32 (head offset lse_head0)
@@ -1132,12 +1143,15 @@ int attention_bwd(const AttnBwdShape& sh, const void* qkv, const void* o, const 
                   const void* dout, void* dqkv, void* ws, cudaStream_t st) {
   const AttnShape& f = sh.f;
   const int s_pad = (f.s + 127) / 128 * 128;
+  const size_t nrow = (size_t)f.b * f.H * s_pad;
   float* Dsum = reinterpret_cast<float*>(ws);
-  float* NL2 = Dsum + (size_t)f.b * f.H * s_pad;
+  float* NL2 = Dsum + nrow;
+  __nv_bfloat16* AUX = reinterpret_cast<__nv_bfloat16*>(NL2 + nrow);
+  if (nrow > (size_t)INT32_MAX) return BPT_EUNSUPPORTED;  // the extra rows' TMA row coordinate
   int rc;
   {
-    ProfScope prof(PROF_MISC, 0.0, 4.0 * f.b * f.s * f.H * f.d + 12.0 * f.b * f.H * s_pad, st);
-    rc = attn_dsum(sh, o, dout, lse, Dsum, NL2, s_pad, st);
+    ProfScope prof(PROF_MISC, 0.0, 4.0 * f.b * f.s * f.H * f.d + 28.0 * f.b * f.H * s_pad, st);
+    rc = attn_dsum(sh, o, dout, lse, Dsum, NL2, AUX, s_pad, st);
     if (rc) return rc;
   }
 
@@ -1145,6 +1159,7 @@ int attention_bwd(const AttnBwdShape& sh, const void* qkv, const void* o, const 
   memset(&prm, 0, sizeof(prm));
   if (make_attn_map(&prm.map_qkv, qkv, f.b, f.s, f.ld_qkv, f.d)) return 1;
   if (make_attn_map(&prm.map_do, dout, f.b, f.s, sh.ld_do, f.d)) return 1;
+  if (make_map_2d(&prm.map_aux, AUX, nrow, 8, 8, 8, 128, 0)) return 1;
   prm.s = f.s;
   prm.s_pad = s_pad;
   prm.H = f.H;

@@ -1,7 +1,6 @@
 // attn_bwd_noalloc.cu -- bpt_attention_bwd_noalloc: the attention backward
-// with its scratch (the fp32 per-row dO . O sums and -LSE * log2(e)) in a
-// fixed array compiled
-// into the library, for callers that cannot allocate device memory when they
+// with its scratch (the per-row dO . O sums and -LSE * log2(e)) in a fixed
+// array compiled into the library, for callers that cannot allocate device memory when they
 // call us.
 //
 // Who cannot allocate: code that must run with a device-memory plan fixed

@@ -243,11 +243,22 @@ __global__ void f32_to_bf16_kernel(int64_t rows, int64_t n, const float* src, in
 
 // Dsum[b, h, q] = sum_k dO[b*s + q, h*d + k] * O[b*s + q, h*d + k]  (0 for q >= s)
 // and NL2[b, h, q] = -LSE[b, h, q] * log2(e), the exponent offset of the
-// probabilities in base 2 (every padded row too)
+// probabilities in base 2 (every padded row too), and one 8-column bf16 row
+// per (b, h, q): (hi, lo) of -LSE * sqrt(d), (hi, lo) of -D, four zeros, with
+// hi + lo the value to about 2^-16 relative.  Appended to the Q and dO rows
+// as one more contraction step against (1, 1, 0, ...) resp. (0, 0, 1, 1, ...),
+// it makes the tensor core emit S - LSE/scale and dP - D directly.
+// v as the bf16 pair (hi, lo) with hi + lo = v to about 16 significant bits
+__device__ __forceinline__ uint32_t hi_lo_pair(float v) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+  return (uint32_t)__bfloat16_as_ushort(hi) | ((uint32_t)__bfloat16_as_ushort(lo) << 16);
+}
+
 __global__ void dsum_kernel(int b, int s, int s_pad, int H, int d, const __nv_bfloat16* o,
                             int64_t ld_o, int64_t o_col, const __nv_bfloat16* dout, int64_t ld_do,
                             int64_t do_col, const float* lse, int H_total, int lse_head0, float* Dsum,
-                            float* NL2) {
+                            float* NL2, __nv_bfloat16* AUX) {
   const int64_t total = (int64_t)b * s_pad * H;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -267,9 +278,13 @@ __global__ void dsum_kernel(int b, int s, int s_pad, int H, int d, const __nv_bf
         for (int m = 0; m < 8; ++m) acc += a[m] * c[m];
       }
     }
-    Dsum[((int64_t)bi * H + hn) * s_pad + q] = acc;
-    NL2[((int64_t)bi * H + hn) * s_pad + q] =
-        -1.4426950408889634f * lse[((int64_t)bi * H_total + lse_head0 + hn) * s_pad + q];
+    const int64_t row = ((int64_t)bi * H + hn) * s_pad + q;
+    const float l = lse[((int64_t)bi * H_total + lse_head0 + hn) * s_pad + q];
+    Dsum[row] = acc;
+    NL2[row] = -1.4426950408889634f * l;
+    // the row the dK/dV products append to Q and dO: -LSE/scale (scale =
+    // 1/sqrt(d)) and -D, each as a (hi, lo) bf16 pair, then four zeros
+    reinterpret_cast<uint4*>(AUX)[row] = make_uint4(hi_lo_pair(-l * sqrtf((float)d)), hi_lo_pair(-acc), 0u, 0u);
   }
 }
 
@@ -343,12 +358,13 @@ int f32_to_bf16(int64_t rows, int64_t n, const float* src, int64_t ld_src, void*
 }
 
 int attn_dsum(const AttnBwdShape& sh, const void* o, const void* dout, const float* lse, float* Dsum,
-              float* NL2, int s_pad, cudaStream_t st) {
+              float* NL2, void* AUX, int s_pad, cudaStream_t st) {
   const AttnShape& f = sh.f;
   const int64_t total = (int64_t)f.b * s_pad * f.H;
   dsum_kernel<<<grid_for(total, 256), 256, 0, st>>>(f.b, f.s, s_pad, f.H, f.d, (const __nv_bfloat16*)o,
                                                     f.ld_o, f.o_col, (const __nv_bfloat16*)dout, sh.ld_do,
-                                                    sh.do_col, lse, f.H_total, f.lse_head0, Dsum, NL2);
+                                                    sh.do_col, lse, f.H_total, f.lse_head0, Dsum, NL2,
+                                                    (__nv_bfloat16*)AUX);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 

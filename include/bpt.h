@@ -177,7 +177,9 @@ int bpt_attention_fwd(const bpt_config* cfg, const void* qkv, void* o, void* lse
  *   dqkv [b*s, (H + 2H_kv)*d] bf16 out (dQ, then dK, then dV; dK/dV summed
  *   over the G query heads of each group).
  *   ws: at least bpt_attention_bwd_workspace_bytes(cfg) bytes (the fp32
- *   per-row dO.O sums and the per-row -LSE*log2(e), 8*b*H*s_pad bytes).
+ *   per-row dO.O sums and -LSE*log2(e), and a 16-byte row per query of
+ *   both as bf16 (hi, lo) pairs for the dK/dV products: 24*b*H*s_pad bytes).
+ *   b*H*s_pad above 2^31 - 1 returns BPT_EUNSUPPORTED.
  * Two kernels: dK/dV with the key/value tile outermost and dQ with the query
  * tile outermost, each accumulating in TMEM; no atomics, so the result is
  * deterministic. */
@@ -192,13 +194,13 @@ int bpt_attention_bwd(const bpt_config* cfg, const void* qkv, const void* o, con
  * fixed in advance, a hot path that cannot afford cudaMalloc/cudaFree and
  * the device synchronisation they may cause, or a process whose device
  * memory is owned by another allocator.  Same arguments and results as
- * bpt_attention_bwd minus the workspace: the scratch it needs (the fp32
- * per-row dO.O sums and -LSE*log2(e), bpt_attention_bwd_workspace_bytes =
- * 8*b*H*s_pad bytes)
+ * bpt_attention_bwd minus the workspace: the scratch it needs (the per-row
+ * dO.O sums and -LSE*log2(e), bpt_attention_bwd_workspace_bytes =
+ * 24*b*H*s_pad bytes)
  * lives in a fixed device array of BPT_NOALLOC_SCRATCH_BYTES compiled into
  * the library, which every GPU that loads it keeps until the process exits.
  *  - Returns BPT_ENOSPC, without launching anything, when the problem needs
- *    more scratch than BPT_NOALLOC_SCRATCH_BYTES (64 MiB: b*H*s_pad up to
+ *    more scratch than BPT_NOALLOC_SCRATCH_BYTES (192 MiB: b*H*s_pad up to
  *    8M, e.g. 32 heads at s = 256K; 32 heads at s = 512K is too big).
  *  - The first call on a device looks up the array's device address (once
  *    per device, with that device current); make that first call before
@@ -207,7 +209,7 @@ int bpt_attention_bwd(const bpt_config* cfg, const void* qkv, const void* o, con
  *    itself.  Calls that overlap on the GPU (other streams or host threads
  *    on the same device) race on it: serialise them.
  *  - It calls no cudaMalloc, cudaFree or other allocating routine. */
-#define BPT_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+#define BPT_NOALLOC_SCRATCH_BYTES (192u * 1024u * 1024u)
 int bpt_attention_bwd_noalloc(const bpt_config* cfg, const void* qkv, const void* o, const void* lse,
                               const void* dout, void* dqkv, void* stream);
 

@@ -78,6 +78,13 @@ __device__ __forceinline__ void tmem_store_row(uint32_t taddr, const uint32_t* w
   if constexpr (N % 16 == 8) tmem_st8_nw(taddr + (N / 16) * 16, w + (N / 16) * 16);
 }
 
+// max of three (sm_100 family: one instruction)
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

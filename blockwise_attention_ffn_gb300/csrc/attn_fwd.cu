@@ -58,18 +58,28 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-// TMEM: two 128-column S buffers [0,256), O [256, 256+D), Q [256+D, 256+1.5D).
-// Q is copied into TMEM once per CTA (the A operand of S = Q K_j^T) and each
-// P is written over its own S buffer as bf16 pairs (the A operand of
-// O += P V_j), so every product reads only its B operand from shared memory,
-// which holds just the K/V ring.
+// TMEM: two 128-column S buffers [0,256), O [256, 256+D+EXT), Q after it
+// (D/2 columns).  Q is copied into TMEM once per CTA (the A operand of
+// S = Q K_j^T) and each P is written over its own S buffer as bf16 pairs (the
+// A operand of O += P V_j), so every product reads only its B operand from
+// shared memory, which holds just the K/V ring.
+//
+// Row sums on the tensor core (EXT = 16): each ring stage carries, right after
+// V's column chunks, one more chunk whose every 16-byte unit is (1, 0, ..., 0)
+// in bf16, so P V reads N = D + 16 columns and writes the row sum of P (the
+// same bf16 P the numerator uses) into O's columns D and D + 8 whatever the
+// swizzle permutes.  The sum is rescaled with O, and the softmax does no
+// adds.  Not for d = 128, whose 16 KB chunks would cost a ring stage.
 template <int D>
 struct FwdCfg {
   using T = TileGeom<D>;
-  static constexpr int KVS_FIT = (232448 - 1280) / (2 * T::TILE);
+  static constexpr int EXT = (T::CW == 16 || D == 64) ? 16 : 0;
+  static constexpr int EXT_BYTES = EXT ? T::CHUNK : 0;
+  static constexpr int STAGE = 2 * T::TILE + EXT_BYTES;
+  static constexpr int KVS_FIT = (232448 - 1280) / STAGE;
   static constexpr int KVS = KVS_FIT > 5 ? 5 : KVS_FIT;
-  static constexpr int SMEM = KVS * 2 * T::TILE + 1024 + 256;
-  static constexpr uint32_t COL_O = 256, COL_Q = 256 + D;
+  static constexpr int SMEM = KVS * STAGE + 1024 + 256;
+  static constexpr uint32_t COL_O = 256, COL_Q = 256 + D + EXT;
 };
 
 template <int D>
@@ -77,15 +87,17 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
   using T = TileGeom<D>;
   using C = FwdCfg<D>;
   constexpr int KVS = C::KVS;
+  constexpr int EXT = C::EXT;
+  constexpr int STAGE = C::STAGE;
   static_assert(C::COL_Q + D / 2 <= 512, "TMEM columns");
   constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
-  constexpr uint32_t IDESC_PV = idesc_bf16(128, D, false, true);
+  constexpr uint32_t IDESC_PV = idesc_bf16(128, D + EXT, false, true);
   constexpr float NEG_INF = -INFINITY;
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sKV = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + KVS * 2 * T::TILE);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + KVS * STAGE);
   uint64_t* q_ready = bars;            // Q copied into TMEM (4 softmax warps)
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = kv_full + KVS;
@@ -133,6 +145,13 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
     tmem_alloc(tmem_holder, 512);
     tmem_relinquish();
   }
+  if constexpr (EXT > 0) {
+    // the row-sum chunk of every stage (never written by TMA)
+    constexpr int UNITS = C::EXT_BYTES / 16;
+    for (int i = threadIdx.x; i < KVS * UNITS; i += blockDim.x)
+      reinterpret_cast<uint4*>(sKV + (i / UNITS) * STAGE + 2 * T::TILE)[i % UNITS] = make_uint4(0x3F80u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -148,7 +167,7 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
       for (int j = 0; j < nkv; ++j) {
         const int st = j % KVS;
         if (j >= KVS && !bounded_wait(&kv_empty[st], ((j / KVS) & 1) ^ 1, abort_flag, 201, p.err)) break;
-        uint8_t* sK = sKV + st * 2 * T::TILE;
+        uint8_t* sK = sKV + st * STAGE;
         uint8_t* sV = sK + T::TILE;
         mbar_expect_tx(&kv_full[st], 2 * T::TILE);
 #pragma unroll
@@ -173,7 +192,7 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
       auto issue_s = [&](int j) -> bool {
         if (!bounded_wait(&kv_full[j % KVS], (j / KVS) & 1, abort_flag, 213, p.err)) return false;
         tc_fence_after();
-        const uint32_t kt = uKV + (j % KVS) * 2 * T::TILE;
+        const uint32_t kt = uKV + (j % KVS) * STAGE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           umma_bf16_tmem_a(tS + (j & 1) * 128, tQA + kk * 8, T::kmajor(kt, kk), IDESC_S, kk > 0);
@@ -185,7 +204,7 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
         if (j + 1 < nkv && !issue_s(j + 1)) { ok = false; break; }
         if (!bounded_wait(&p_full[j & 1], (j >> 1) & 1, abort_flag, 212, p.err)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t vt = uKV + (j % KVS) * 2 * T::TILE + T::TILE;
+        const uint32_t vt = uKV + (j % KVS) * STAGE + T::TILE;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           umma_bf16_tmem_a(tO, tS + (j & 1) * 128 + kk * 8, T::mnmajor(vt, kk), IDESC_PV, (j > 0 || kk > 0));
@@ -243,8 +262,18 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
       const bool edge = hi < 128;
       float mx = NEG_INF;
       if (!edge) {
+        if constexpr (EXT > 0) {
+          // two chains of three-input maxima (measured faster here; slower
+          // in the d = 128 instance, which keeps the plain chain)
+          float m2[2] = {NEG_INF, NEG_INF};
 #pragma unroll
-        for (int i = 0; i < 128; ++i) mx = fmaxf(mx, __uint_as_float(sv[i]));
+          for (int i = 0; i < 128; i += 2)
+            m2[(i >> 1) & 1] = max3f(m2[(i >> 1) & 1], __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
+          mx = fmaxf(m2[0], m2[1]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 128; ++i) mx = fmaxf(mx, __uint_as_float(sv[i]));
+        }
       } else {
 #pragma unroll
         for (int i = 0; i < 128; ++i)
@@ -268,7 +297,7 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
         for (int i = 0; i < 128; i += 2) {
           const float e0 = ex2(fmaf(__uint_as_float(sv[i]), c, -mc));
           const float e1 = ex2(fmaf(__uint_as_float(sv[i + 1]), c, -mc));
-          rs += e0 + e1;
+          if constexpr (EXT == 0) rs += e0 + e1;
           pk[i / 2] = pack_bf16(e0, e1);
         }
       } else {
@@ -276,7 +305,7 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
         for (int i = 0; i < 128; i += 2) {
           const float e0 = i < hi ? ex2(fmaf(__uint_as_float(sv[i]), c, -mc)) : 0.f;
           const float e1 = i + 1 < hi ? ex2(fmaf(__uint_as_float(sv[i + 1]), c, -mc)) : 0.f;
-          rs += e0 + e1;
+          if constexpr (EXT == 0) rs += e0 + e1;
           pk[i / 2] = pack_bf16(e0, e1);
         }
       }
@@ -291,14 +320,15 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         if (rescale) {
-          uint32_t ro[D];
+          // the row (and its row-sum columns)
+          uint32_t ro[D + EXT];
 #pragma unroll
-          for (int cc = 0; cc < D / 16; ++cc) tmem_ld16_nw(tO + lane_off + cc * 16, ro + cc * 16);
+          for (int cc = 0; cc < (D + EXT) / 16; ++cc) tmem_ld16_nw(tO + lane_off + cc * 16, ro + cc * 16);
           tmem_wait_ld(ro);
 #pragma unroll
-          for (int i = 0; i < D; ++i) ro[i] = __float_as_uint(__uint_as_float(ro[i]) * alpha);
+          for (int i = 0; i < D + EXT; ++i) ro[i] = __float_as_uint(__uint_as_float(ro[i]) * alpha);
 #pragma unroll
-          for (int cc = 0; cc < D / 16; ++cc) tmem_st16_nw(tO + lane_off + cc * 16, ro + cc * 16);
+          for (int cc = 0; cc < (D + EXT) / 16; ++cc) tmem_st16_nw(tO + lane_off + cc * 16, ro + cc * 16);
         }
       }
       tmem_st_wait();
@@ -312,13 +342,14 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
     }
     if (ok) {
       tc_fence_after();
-      const float inv_l = 1.f / l_run;
       const bool valid = qpos < p.s;
       __nv_bfloat16* orow = p.o + ((long long)bi * p.s + qpos - p.o_row0) * p.ld_o + p.o_col + (long long)n * D;
-      uint32_t oall[D];
+      uint32_t oall[D + EXT];
 #pragma unroll
-      for (int cc = 0; cc < D / 16; ++cc) tmem_ld16_nw(tO + lane_off + cc * 16, oall + cc * 16);
+      for (int cc = 0; cc < (D + EXT) / 16; ++cc) tmem_ld16_nw(tO + lane_off + cc * 16, oall + cc * 16);
       tmem_wait_ld(oall);
+      if constexpr (EXT > 0) l_run = __uint_as_float(oall[D]);
+      const float inv_l = 1.f / l_run;
       if (valid) {
 #pragma unroll
         for (int cc = 0; cc < D / 16; ++cc) store_row16(orow + cc * 16, oall + cc * 16, inv_l);

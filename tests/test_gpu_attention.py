@@ -8,7 +8,7 @@ import torch
 import blockwise_attention_ffn_gb300 as bpt
 from blockwise_attention_ffn_gb300.presets import LayerConfig
 from oracle import ref
-from tests.gpu_helpers import assert_close, to64
+from tests.gpu_helpers import LSE_MAX_ABS, LSE_REL_FRO, assert_close, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -63,7 +63,7 @@ def test_attention_forward(shape):
             o_ref[bi, :, n], lse_ref[bi, n] = ref.attention_head(q[bi, :, n], k[bi, :, n // G],
                                                                  v[bi, :, n // G], bool(causal))
     assert_close(to64(o).reshape(b, s, H, d), o_ref, "O")
-    assert_close(to64(lse)[:, :, :s], lse_ref, "LSE", max_abs=1e-3, rel_fro=1e-5, bf16_out=False)
+    assert_close(to64(lse)[:, :, :s], lse_ref, "LSE", max_abs=LSE_MAX_ABS, rel_fro=LSE_REL_FRO, bf16_out=False)
 
 
 @pytest.mark.parametrize("shape", SHAPES)

@@ -9,8 +9,8 @@ import torch
 import blockwise_attention_ffn_gb300 as bpt
 from blockwise_attention_ffn_gb300.presets import C1, LayerConfig
 from oracle import ref
-from tests.gpu_helpers import (assert_close, assert_close_grad, device_inputs, half_ulp_bf16, run_bwd,
-                               run_fwd, to64)
+from tests.gpu_helpers import (LSE_MAX_ABS, LSE_REL_FRO, assert_close, assert_close_grad, device_inputs,
+                               half_ulp_bf16, run_bwd, run_fwd, to64)
 from tests.oracle_helpers import inputs_to_oracle, oracle_cfg
 
 pytestmark = pytest.mark.gpu
@@ -73,7 +73,7 @@ def test_headchunk_attention_matches_oracle():
     W = inputs_to_oracle(inp)["W"]
     o_ref, lse_ref, _, _, _ = ref.attention_block(to64(inp["x"])[0], W, oracle_cfg(cfg))
     assert_close(to64(o), o_ref, "O")
-    assert_close(to64(lse)[0, :, :cfg.s], lse_ref, "LSE", max_abs=2e-3, rel_fro=1e-4, bf16_out=False)
+    assert_close(to64(lse)[0, :, :cfg.s], lse_ref, "LSE", max_abs=LSE_MAX_ABS, rel_fro=LSE_REL_FRO, bf16_out=False)
 
 
 @pytest.mark.parametrize("base,variant", [

@@ -658,26 +658,25 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_tm_kernel(const __grid_const
       tmem_ld32_nw(tS + lane_off + c0, sv);
       tmem_ld32_nw(tS + lane_off + c0 + 32, sv + 32);
       tmem_wait_ld(sv);
-      uint32_t pk[32];
+      // P^T in fp32 (for dS^T) and as bf16 pairs (the dV operand)
+      float pe[64];
       if (!edge) {
 #pragma unroll
-        for (int k = 0; k < 64; k += 2)
-          pk[k / 2] = pack_bf16(ex2(__uint_as_float(sv[k]) * c), ex2(__uint_as_float(sv[k + 1]) * c));
+        for (int k = 0; k < 64; ++k) pe[k] = ex2(__uint_as_float(sv[k]) * c);
       } else {
 #pragma unroll
-        for (int k = 0; k < 64; k += 2) {
-          const float e0 = (k < lo || k >= hi) ? 0.f : ex2(__uint_as_float(sv[k]) * c);
-          const float e1 = (k + 1 < lo || k + 1 >= hi) ? 0.f : ex2(__uint_as_float(sv[k + 1]) * c);
-          pk[k / 2] = pack_bf16(e0, e1);
-        }
+        for (int k = 0; k < 64; ++k) pe[k] = (k < lo || k >= hi) ? 0.f : ex2(__uint_as_float(sv[k]) * c);
       }
+      uint32_t pk[32];
+#pragma unroll
+      for (int k = 0; k < 64; k += 2) pk[k / 2] = pack_bf16(pe[k], pe[k + 1]);
       tmem_st32(tS + lane_off + c0, pk);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
       // ---- phase 2: dS^T = P^T dP'^T (dP' already offset by -D), P^T from
-      // registers
+      // registers (fp32)
       ok = bounded_wait(dp_full, t & 1, abort_flag, 593, p.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
@@ -687,10 +686,8 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_tm_kernel(const __grid_const
       tmem_wait_ld(dr);
       uint32_t o[32];
 #pragma unroll
-      for (int k = 0; k < 64; k += 2) {
-        const uint32_t pw = pk[k / 2];
-        o[k / 2] = pack_bf16(bf16_lo(pw) * __uint_as_float(dr[k]), bf16_hi(pw) * __uint_as_float(dr[k + 1]));
-      }
+      for (int k = 0; k < 64; k += 2)
+        o[k / 2] = pack_bf16(pe[k] * __uint_as_float(dr[k]), pe[k + 1] * __uint_as_float(dr[k + 1]));
       tmem_st32(tdP + lane_off + c0, o);
       tmem_st_wait();
       tc_fence_before();
@@ -982,18 +979,14 @@ __global__ void __launch_bounds__(352, 1) attn_dq_kernel(const __grid_constant__
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free);
-      uint32_t pk[32];
+      // P stays in fp32 registers: no product here reads it, only dS
+      float pe[64];
       if (hi >= 64) {
 #pragma unroll
-        for (int k = 0; k < 64; k += 2)
-          pk[k / 2] = pack_bf16(ex2(fmaf(__uint_as_float(sv[k]), c, nl)), ex2(fmaf(__uint_as_float(sv[k + 1]), c, nl)));
+        for (int k = 0; k < 64; ++k) pe[k] = ex2(fmaf(__uint_as_float(sv[k]), c, nl));
       } else {
 #pragma unroll
-        for (int k = 0; k < 64; k += 2) {
-          const float e0 = k < hi ? ex2(fmaf(__uint_as_float(sv[k]), c, nl)) : 0.f;
-          const float e1 = k + 1 < hi ? ex2(fmaf(__uint_as_float(sv[k + 1]), c, nl)) : 0.f;
-          pk[k / 2] = pack_bf16(e0, e1);
-        }
+        for (int k = 0; k < 64; ++k) pe[k] = k < hi ? ex2(fmaf(__uint_as_float(sv[k]), c, nl)) : 0.f;
       }
       // ---- phase 2: dS = P (dP - D) over this warp's dP columns
       ok = bounded_wait(dp_full, jt & 1, abort_flag, 622, p.err);
@@ -1011,11 +1004,8 @@ __global__ void __launch_bounds__(352, 1) attn_dq_kernel(const __grid_constant__
       }
       uint32_t o[32];
 #pragma unroll
-      for (int k = 0; k < 64; k += 2) {
-        const uint32_t pw = pk[k / 2];
-        o[k / 2] = pack_bf16(bf16_lo(pw) * (__uint_as_float(dr[k]) - dsum),
-                             bf16_hi(pw) * (__uint_as_float(dr[k + 1]) - dsum));
-      }
+      for (int k = 0; k < 64; k += 2)
+        o[k / 2] = pack_bf16(pe[k] * (__uint_as_float(dr[k]) - dsum), pe[k + 1] * (__uint_as_float(dr[k + 1]) - dsum));
       if constexpr (C::SEP_DS) {
         // dQ(j-1) has read the previous dS; waiting every step keeps these
         // warps within one phase of dq_done

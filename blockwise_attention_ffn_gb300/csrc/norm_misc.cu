@@ -104,77 +104,138 @@ __global__ void norm_fwd_kernel(int64_t rows, int h, int kind, float eps, const 
 // dx = res + rstd * (g - mean(g) - xhat * mean(g * xhat))    (LayerNorm)
 //    = res + rstd * (g - xhat * mean(g * xhat))              (RMSNorm)
 // with g = dy * w; dw += sum_rows dy * xhat, db += sum_rows dy.
-// Two phases per block, over a band of rows:
+// A block takes a band of rows (one band per resident block: one wave) in
+// sub-bands of two rows per warp, each in two phases:
 //  1. one warp per row: the row's mean and rstd (as the forward computes
 //     them), and the two row sums of the gradient, into shared memory;
-//  2. each thread owns 8 columns (the block spans the row): for every row of
-//     the band it forms dx and accumulates dw, db in registers, so the
-//     scale/shift gradients take one global atomic per column per block and
-//     no shared-memory atomics at all.
+//  2. each thread owns 8 columns (the block spans the row up to h = 4096):
+//     for every row of the sub-band it forms dx and accumulates dw, db in
+//     registers, so the scale/shift gradients take one global atomic per
+//     column per block and no shared-memory atomics at all.
+// Phase 2 re-reads the rows phase 1 has just read, so they come from L2.
+// The loops store through pointers the compiler must assume alias the
+// inputs, so they load a group of chunks (phase 1) or two rows (phase 2)
+// before any store: one load in flight per thread would leave HBM idle.
 __global__ void __launch_bounds__(512) norm_bwd_kernel(int64_t rows, int h, int kind, float eps, NormBwdIO io,
                                                         const __nv_bfloat16* w, float* dw, float* db,
                                                         int64_t band) {
-  extern __shared__ float stat[];  // [band][4]: mean, rstd, mean(g), mean(g * xhat)
+  extern __shared__ float stat[];  // [sub-band row][4]: mean, rstd, mean(g), mean(g * xhat)
+  constexpr int NB1 = 2;           // chunk groups of phase 1 (the accumulators stay live)
   const int lane = threadIdx.x & 31;
   const int nwarp = blockDim.x >> 5;
+  const int sub = 2 * nwarp;  // rows per sub-band: two per warp in phase 1
   const int64_t r0 = (int64_t)blockIdx.x * band;
   const int64_t r1 = min(rows, r0 + band);
-  for (int64_t r = r0 + (threadIdx.x >> 5); r < r1; r += nwarp) {
-    float mean, rstd;
-    row_stats(io.x, io.x_f32, r * io.ldx, h, kind, eps, mean, rstd);
-    float sg = 0.f, sgx = 0.f;
-    for (int c = lane * 8; c < h; c += 256) {
-      float v[8], wv[8], gv[8];
-      ld8x(io.x, io.x_f32, r * io.ldx + c, v);
-      ld8(w + c, wv);
-      ld8x(io.dy, io.dy_f32, r * io.lddy + c, gv);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float g = gv[k] * wv[k];
-        sg += g;
-        sgx += g * (v[k] - mean) * rstd;
-      }
-    }
-    sg = warp_sum(sg) / h;
-    sgx = warp_sum(sgx) / h;
-    if (lane == 0) {
-      float* o = stat + (r - r0) * 4;
-      o[0] = mean;
-      o[1] = rstd;
-      o[2] = (kind == 0) ? sg : 0.f;
-      o[3] = sgx;
-    }
-  }
-  __syncthreads();
-  for (int c = threadIdx.x * 8; c < h; c += blockDim.x * 8) {
-    float wv[8], adw[8], adb[8];
-    ld8(w + c, wv);
+  // every thread walks the same number of column groups (the barriers below)
+  const int ngroups = (h + 8 * (int)blockDim.x - 1) / (8 * (int)blockDim.x);
+  for (int gi = 0; gi < ngroups; ++gi) {
+    const int c = (gi * (int)blockDim.x + (int)threadIdx.x) * 8;
+    const bool active = c < h;
+    float adw[8], adb[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) adw[k] = adb[k] = 0.f;
-    for (int64_t r = r0; r < r1; ++r) {
-      const float4 s4 = *reinterpret_cast<const float4*>(stat + (r - r0) * 4);
-      float v[8], gv[8], rv[8];
-      ld8x(io.x, io.x_f32, r * io.ldx + c, v);
-      ld8x(io.dy, io.dy_f32, r * io.lddy + c, gv);
-      if (io.res) ld8x(io.res, io.res_f32, r * io.ldres + c, rv);
+    // sub-bands: phase 2 re-reads the rows phase 1 just read, from L2
+    for (int64_t s0 = r0; s0 < r1; s0 += sub) {
+      const int64_t s1 = min(r1, s0 + sub);
+      for (int64_t r = s0 + (threadIdx.x >> 5); r < s1; r += nwarp) {
+        // mean first (LayerNorm), then one pass over x and dy for the
+        // variance and the gradient sums: sum g*xhat = rstd * (sum g*x -
+        // mean * sum g)
+        float mean = 0.f;
+        if (kind == 0) {
+          float sx = 0.f;
+          for (int c0 = lane * 8; c0 < h; c0 += NB1 * 256) {
+            float v[NB1][8];
+#pragma unroll
+            for (int u = 0; u < NB1; ++u)
+              if (c0 + u * 256 < h) ld8x(io.x, io.x_f32, r * io.ldx + c0 + u * 256, v[u]);
+#pragma unroll
+            for (int u = 0; u < NB1; ++u)
+              if (c0 + u * 256 < h) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) sx += v[u][k];
+              }
+          }
+          mean = warp_sum(sx) / h;
+        }
+        float q = 0.f, sg = 0.f, sgx = 0.f;
+        for (int c0 = lane * 8; c0 < h; c0 += NB1 * 256) {
+          float v[NB1][8], gv[NB1][8];
+#pragma unroll
+          for (int u = 0; u < NB1; ++u)
+            if (c0 + u * 256 < h) {
+              ld8x(io.x, io.x_f32, r * io.ldx + c0 + u * 256, v[u]);
+              ld8x(io.dy, io.dy_f32, r * io.lddy + c0 + u * 256, gv[u]);
+            }
+#pragma unroll
+          for (int u = 0; u < NB1; ++u)
+            if (c0 + u * 256 < h) {
+              float w8[8];
+              ld8(w + c0 + u * 256, w8);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const float t = v[u][k] - mean;
+                const float g = gv[u][k] * w8[k];
+                q += t * t;
+                sg += g;
+                sgx += g * t;
+              }
+            }
+        }
+        q = warp_sum(q);
+        const float rstd = rsqrtf(q / h + eps);
+        sg = warp_sum(sg) / h;
+        sgx = warp_sum(sgx) * rstd / h;
+        if (lane == 0) {
+          float* o = stat + (r - s0) * 4;
+          o[0] = mean;
+          o[1] = rstd;
+          o[2] = (kind == 0) ? sg : 0.f;
+          o[3] = sgx;
+        }
+      }
+      __syncthreads();
+      if (active) {
+        // two rows per iteration, every load before any store
+        for (int64_t r = s0; r < s1; r += 2) {
+          const int nr = r + 1 < s1 ? 2 : 1;
+          float v[2][8], gv[2][8], rv[2][8], wv[8];
+          ld8(w + c, wv);  // from L1: cheaper than holding it live
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+            if (u < nr) {
+              ld8x(io.x, io.x_f32, (r + u) * io.ldx + c, v[u]);
+              ld8x(io.dy, io.dy_f32, (r + u) * io.lddy + c, gv[u]);
+              if (io.res) ld8x(io.res, io.res_f32, (r + u) * io.ldres + c, rv[u]);
+            }
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+            if (u < nr) {
+              const float4 s4 = *reinterpret_cast<const float4*>(stat + (r + u - s0) * 4);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const float xh = (v[u][k] - s4.x) * s4.y;
+                adw[k] += gv[u][k] * xh;
+                adb[k] += gv[u][k];
+                v[u][k] = s4.y * (gv[u][k] * wv[k] - s4.z - xh * s4.w) + (io.res ? rv[u][k] : 0.f);
+              }
+              st8(reinterpret_cast<__nv_bfloat16*>(io.dx) + (r + u) * io.lddx + c, v[u]);
+              if (io.dx_f32) {
+                float4* o = reinterpret_cast<float4*>(io.dx_f32 + (r + u) * io.lddx + c);
+                o[0] = make_float4(v[u][0], v[u][1], v[u][2], v[u][3]);
+                o[1] = make_float4(v[u][4], v[u][5], v[u][6], v[u][7]);
+              }
+            }
+        }
+      }
+      __syncthreads();
+    }
+    if (active) {
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const float xh = (v[k] - s4.x) * s4.y;
-        adw[k] += gv[k] * xh;
-        adb[k] += gv[k];
-        v[k] = s4.y * (gv[k] * wv[k] - s4.z - xh * s4.w) + (io.res ? rv[k] : 0.f);
+        if (dw) atomicAdd(&dw[c + k], adw[k]);
+        if (db) atomicAdd(&db[c + k], adb[k]);
       }
-      st8(reinterpret_cast<__nv_bfloat16*>(io.dx) + r * io.lddx + c, v);
-      if (io.dx_f32) {
-        float4* o = reinterpret_cast<float4*>(io.dx_f32 + r * io.lddx + c);
-        o[0] = make_float4(v[0], v[1], v[2], v[3]);
-        o[1] = make_float4(v[4], v[5], v[6], v[7]);
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      if (dw) atomicAdd(&dw[c + k], adw[k]);
-      if (db) atomicAdd(&db[c + k], adb[k]);
     }
   }
 }
@@ -315,13 +376,19 @@ int norm_bwd(int64_t rows, int h, int kind, float eps, const NormBwdIO& io, cons
   int threads = (h / 8 + 31) / 32 * 32;
   if (threads < 64) threads = 64;
   if (threads > 512) threads = 512;
-  // about two blocks per SM, bands of at least 8 rows
-  const int nsm = sm_count();
-  int64_t band = (rows + 2 * (int64_t)(nsm > 0 ? nsm : 1) - 1) / (2 * (int64_t)(nsm > 0 ? nsm : 1));
+  // one full wave: as many blocks as the SMs hold at once (registers bound
+  // it), bands of at least 8 rows
+  const int64_t nsm = sm_count() > 0 ? sm_count() : 1;
+  int per_sm = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, norm_bwd_kernel, threads, 2 * (threads / 32) * 16) !=
+          cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  int64_t band = (rows + nsm * per_sm - 1) / (nsm * per_sm);
   if (band < 8) band = 8;
   if (band > 2048) band = 2048;
   const int64_t grid = (rows + band - 1) / band;
-  const size_t smem = (size_t)band * 4 * sizeof(float);
+  const size_t smem = (size_t)2 * (threads / 32) * 4 * sizeof(float);  // one sub-band of statistics
   ProfScope prof(PROF_NORM, 0.0,
                  (double)rows * h * ((io.dy_f32 ? 4 : 2) + (io.x_f32 ? 4 : 2) + (io.res ? (io.res_f32 ? 4 : 2) : 0) + 2 +
                                      (io.dx_f32 ? 4 : 0)),

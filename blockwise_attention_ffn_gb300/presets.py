@@ -42,10 +42,10 @@ C1 = LayerConfig(name="gpt-small s=1024 h=256 4x64", b=1, s=1024, h=256, n_heads
 C2 = LayerConfig(name="gpt-1b s=8192 h=2048 16x128", b=1, s=8192, h=2048, n_heads=16, n_kv_heads=16,
                  head_dim=128, ffn_dim=8192, ffn_block=2048, seed=1)
 C3 = LayerConfig(name="gpt-3b s=32768 h=2560 32x80", b=1, s=32768, h=2560, n_heads=32, n_kv_heads=32,
-                 head_dim=80, ffn_dim=10240, ffn_block=4096, backward=True, seed=2)
+                 head_dim=80, ffn_dim=10240, ffn_block=8192, backward=True, seed=2)
 C4 = LayerConfig(name="gpt-1b long s=131072 h=2048 16x128", b=1, s=131072, h=2048, n_heads=16,
                  n_kv_heads=16, head_dim=128, ffn_dim=8192, q_block=256, kv_block=256,
-                 ffn_block=4096, backward=True, seed=3)
+                 ffn_block=8192, backward=True, seed=3)
 C5 = LayerConfig(name="llama-8b s=65536 h=4096 32q/8kv x128 U=8", b=1, s=65536, h=4096, n_heads=32,
                  n_kv_heads=8, head_dim=128, ffn_dim=14336, head_chunk=8, norm=1, act=2, has_bias=0,
                  ffn_block=4096, backward=True, seed=4)

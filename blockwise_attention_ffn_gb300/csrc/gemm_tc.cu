@@ -51,8 +51,9 @@ struct GemmParams {
   const __nv_bfloat16* aux2;
   long long ldaux2;
   float beta;
-  int mt, nt, ntiles;  // tile grid
+  int mt, nt, ntiles;  // tile grid; ntiles counts work units (tiles x ksplit)
   int m_fast;          // walk tiles along M first
+  int ksplit;          // K ranges per tile (> 1: EPI_F32 added atomically)
   unsigned int* err;
 };
 
@@ -191,6 +192,12 @@ __device__ __forceinline__ void epi8(const GemmParams& p, int m, int n, const fl
 #pragma unroll
         for (int j = 0; j < 8; ++j) t[j] += rr[j];
       }
+      if (p.ksplit > 1) {
+        // one K range's share: added in L2 (the host zeroed out when beta = 0)
+        red_add_v4(o, t[0], t[1], t[2], t[3]);
+        red_add_v4(o + 4, t[4], t[5], t[6], t[7]);
+        break;
+      }
       float4 x0 = make_float4(t[0], t[1], t[2], t[3]);
       float4 x1 = make_float4(t[4], t[5], t[6], t[7]);
       if (p.beta != 0.f) {
@@ -254,16 +261,29 @@ __device__ __forceinline__ void epi1(const GemmParams& p, int m, int n, float a,
       float v = a;
       if (p.bias) v += __bfloat162float(p.bias[n]);
       if (p.res) v += load1_res(p, m, n);
+      if (p.ksplit > 1) {
+        atomicAdd(o, v);
+        break;
+      }
       *o = v + (p.beta != 0.f ? p.beta * *o : 0.f);
       break;
     }
   }
 }
 
-// Tile origin of persistent work item `tile`.  The walk runs fastest along
-// the dimension of the smaller operand, so the CTAs in flight share that
-// operand in L2 while the larger one streams through once.
-__device__ __forceinline__ void tile_origin(const GemmParams& p, int tile, int bn, int& m0, int& n0) {
+// Tile origin of persistent work unit `unit` (tile = unit mod the tile count;
+// with a split K, the K range is unit / tile count, so the CTAs in flight
+// share a K range).  The walk runs fastest along the dimension of the smaller
+// operand, so the CTAs in flight share that operand in L2 while the larger
+// one streams through once.
+__device__ __forceinline__ void k_range(const GemmParams& p, int unit, int& kb, int& ke) {
+  const int ks = unit / (p.mt * p.nt);
+  kb = (int)((long long)p.nkt * ks / p.ksplit);
+  ke = (int)((long long)p.nkt * (ks + 1) / p.ksplit);
+}
+
+__device__ __forceinline__ void tile_origin(const GemmParams& p, int unit, int bn, int& m0, int& n0) {
+  const int tile = unit % (p.mt * p.nt);
   int mb, nb;
   if (p.m_fast) {
     mb = tile % p.mt;
@@ -337,9 +357,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       uint32_t it = 0;  // k-tiles issued, across this CTA's tiles
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < p.ntiles; tile += gridDim.x) {
-        int m0, n0;
+        int m0, n0, kb, ke;
         tile_origin(p, tile, BN, m0, n0);
-        for (int kt = 0; kt < p.nkt; ++kt) {
+        k_range(p, tile, kb, ke);
+        for (int kt = kb; kt < ke; ++kt) {
           const int s = it % STAGES;
           if (it >= STAGES && !bounded_wait(&empty[s], ((it / STAGES) & 1) ^ 1, abort_flag, 101, p.err)) {
             ok = false;
@@ -393,7 +414,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         }
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(acc * ACC_COLS);
-        for (int kt = 0; kt < p.nkt; ++kt) {
+        int kb, ke;
+        k_range(p, tile, kb, ke);
+        for (int kt = kb; kt < ke; ++kt) {
           const int s = it % STAGES;
           if (!bounded_wait(&full[s], (it / STAGES) & 1, abort_flag, 103, p.err)) {
             ok = false;
@@ -406,10 +429,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = A_MN ? sdesc(sa + kk * 2048, 8192, 1024, 2) : sdesc(sa + kk * 32, 16, 1024, 2);
             const uint64_t bd = B_MN ? sdesc(sb + kk * 2048, 8192, 1024, 2) : sdesc(sb + kk * 32, 16, 1024, 2);
-            umma_bf16(d, ad, bd, IDESC, (kt | kk) != 0);
+            const bool accum = kt != kb || kk != 0;
+            umma_bf16(d, ad, bd, IDESC, accum);
             if (DUAL) {
               const uint64_t bd2 = sdesc(sb + BN * BK * 2 + kk * 32, 16, 1024, 2);
-              umma_bf16(d + BN, ad, bd2, IDESC, (kt | kk) != 0);
+              umma_bf16(d + BN, ad, bd2, IDESC, accum);
             }
           }
           umma_commit(&empty[s]);
@@ -496,7 +520,7 @@ int launch(GemmParams& p, cudaStream_t st) {
   if (nsm <= 0) return 3;
   p.mt = (p.M + BM - 1) / BM;
   p.nt = (p.N + BN - 1) / BN;
-  p.ntiles = p.mt * p.nt;
+  p.ntiles = p.mt * p.nt * p.ksplit;
   p.m_fast = p.M <= p.N;
   const int grid = p.ntiles < nsm ? p.ntiles : nsm;
   kern<<<grid, NUM_THREADS, SMEM, st>>>(p);
@@ -566,6 +590,28 @@ int gemm(int64_t M, int64_t N, int64_t K, const MatView& A, bool a_mn, const Mat
   p.err = device_error_word();
   if (!p.err) return 3;
   ProfScope prof(PROF_GEMM, 2.0 * (double)M * (double)N * (double)K * (dual ? 2 : 1), 0.0, stream);
+  // Split K for fp32 outputs with nothing but the product (weight gradients)
+  // when whole tiles would leave the last wave of SMs mostly idle: K ranges
+  // of at least 16 k-tiles each, added atomically into out (zeroed first
+  // unless accumulating).
+  p.ksplit = 1;
+  {
+    const int nsm = sm_count();
+    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    auto fill = [&](int64_t units) { return (double)units / (double)(((units + nsm - 1) / nsm) * nsm); };
+    const bool aligned = (e.ldo % 4) == 0 && (reinterpret_cast<uintptr_t>(e.out) & 15) == 0;
+    if (!dual && e.kind == EPI_F32 && !e.bias && !e.res && (e.beta == 0.f || e.beta == 1.f) && aligned && nsm > 0 &&
+        fill(tiles) < 0.8) {
+      for (int ks = 2; ks <= 8 && p.nkt / ks >= 16; ++ks)
+        if (fill(tiles * ks) >= 0.9) {
+          p.ksplit = ks;
+          break;
+        }
+    }
+    if (p.ksplit > 1 && e.beta == 0.f) {
+      if (cudaMemset2DAsync(e.out, (size_t)e.ldo * 4, 0, (size_t)N * 4, (size_t)M, stream) != cudaSuccess) return 3;
+    }
+  }
   if (dual) return launch<128, false, false, true>(p, stream);
   if (!a_mn && !b_mn) return launch<256, false, false, false>(p, stream);
   if (!a_mn && b_mn) return launch<256, false, true, false>(p, stream);

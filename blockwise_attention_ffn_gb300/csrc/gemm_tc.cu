@@ -54,6 +54,7 @@ struct GemmParams {
   int mt, nt, ntiles;  // tile grid; ntiles counts work units (tiles x ksplit)
   int m_fast;          // walk tiles along M first
   int ksplit;          // K ranges per tile (> 1: EPI_F32 added atomically)
+  int vec32;           // every epilogue operand allows 32-byte accesses
   unsigned int* err;
 };
 
@@ -73,31 +74,105 @@ __device__ __forceinline__ float gelu_grad_f(float z, int act) {
 }
 __device__ __forceinline__ float sigmoid_f(float z) { return 1.f / (1.f + expf(-z)); }
 
-__device__ __forceinline__ void load8_bf16(const __nv_bfloat16* p, float (&v)[8]) {
-  const uint4 u = *reinterpret_cast<const uint4*>(p);
-  v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x);
-  v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
-  v[4] = bf16_lo(u.z); v[5] = bf16_hi(u.z);
-  v[6] = bf16_lo(u.w); v[7] = bf16_hi(u.w);
+// W consecutive values (W = 8: 16-byte accesses; W = 16 or 32: 32-byte
+// accesses, a whole sector per thread, for the epilogue's one-row-per-thread
+// pattern)
+__device__ __forceinline__ void ld32B(const void* p, uint32_t (&w)[8]) {
+  asm volatile("ld.global.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+               : "l"(p));
 }
-__device__ __forceinline__ void store8_bf16(__nv_bfloat16* p, const float (&v)[8]) {
-  uint4 u;
-  u.x = pack_bf16(v[0], v[1]);
-  u.y = pack_bf16(v[2], v[3]);
-  u.z = pack_bf16(v[4], v[5]);
-  u.w = pack_bf16(v[6], v[7]);
-  *reinterpret_cast<uint4*>(p) = u;
+__device__ __forceinline__ void st32B(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+template <int W>
+__device__ __forceinline__ void loadw_bf16(const __nv_bfloat16* p, float (&v)[W]) {
+  if constexpr (W == 8) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = bf16_lo(w[i]);
+      v[2 * i + 1] = bf16_hi(w[i]);
+    }
+  } else {
+    // W = 16 or 32: every 32-byte piece loaded before any is used
+    uint32_t w[W / 16][8];
+#pragma unroll
+    for (int h = 0; h < W / 16; ++h) ld32B(p + 16 * h, w[h]);
+#pragma unroll
+    for (int h = 0; h < W / 16; ++h)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        v[16 * h + 2 * i] = bf16_lo(w[h][i]);
+        v[16 * h + 2 * i + 1] = bf16_hi(w[h][i]);
+      }
+  }
+}
+template <int W>
+__device__ __forceinline__ void storew_bf16(__nv_bfloat16* p, const float (&v)[W]) {
+  if constexpr (W == 8) {
+    uint4 u;
+    u.x = pack_bf16(v[0], v[1]);
+    u.y = pack_bf16(v[2], v[3]);
+    u.z = pack_bf16(v[4], v[5]);
+    u.w = pack_bf16(v[6], v[7]);
+    *reinterpret_cast<uint4*>(p) = u;
+  } else {
+#pragma unroll
+    for (int h = 0; h < W / 16; ++h) {
+      uint32_t w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i] = pack_bf16(v[16 * h + 2 * i], v[16 * h + 2 * i + 1]);
+      st32B(p + 16 * h, w);
+    }
+  }
+}
+template <int W>
+__device__ __forceinline__ void loadw_f32(const float* p, float (&v)[W]) {
+  uint32_t w[W / 8][8];
+#pragma unroll
+  for (int h = 0; h < W / 8; ++h) {
+    if constexpr (W == 8) {
+      const float4 a = reinterpret_cast<const float4*>(p)[0];
+      const float4 b = reinterpret_cast<const float4*>(p)[1];
+      w[h][0] = __float_as_uint(a.x); w[h][1] = __float_as_uint(a.y);
+      w[h][2] = __float_as_uint(a.z); w[h][3] = __float_as_uint(a.w);
+      w[h][4] = __float_as_uint(b.x); w[h][5] = __float_as_uint(b.y);
+      w[h][6] = __float_as_uint(b.z); w[h][7] = __float_as_uint(b.w);
+    } else {
+      ld32B(p + 8 * h, w[h]);
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < W / 8; ++h)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[8 * h + i] = __uint_as_float(w[h][i]);
+}
+template <int W>
+__device__ __forceinline__ void storew_f32(float* p, const float (&v)[W]) {
+#pragma unroll
+  for (int h = 0; h < W / 8; ++h) {
+    if constexpr (W == 8) {
+      reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+      reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+    } else {
+      uint32_t w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(v[8 * h + i]);
+      st32B(p + 8 * h, w);
+    }
+  }
 }
 
-__device__ __forceinline__ void load8_res(const GemmParams& p, int m, int n, float (&v)[8]) {
-  if (p.res_f32) {
-    const float4* r = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.res) + (long long)m * p.ldr + n);
-    const float4 a = r[0], b = r[1];
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-  } else {
-    load8_bf16(reinterpret_cast<const __nv_bfloat16*>(p.res) + (long long)m * p.ldr + n, v);
-  }
+template <int W>
+__device__ __forceinline__ void loadw_res(const GemmParams& p, int m, int n, float (&v)[W]) {
+  if (p.res_f32)
+    loadw_f32<W>(reinterpret_cast<const float*>(p.res) + (long long)m * p.ldr + n, v);
+  else
+    loadw_bf16<W>(reinterpret_cast<const __nv_bfloat16*>(p.res) + (long long)m * p.ldr + n, v);
 }
 __device__ __forceinline__ float load1_res(const GemmParams& p, int m, int n) {
   const long long i = (long long)m * p.ldr + n;
@@ -105,109 +180,108 @@ __device__ __forceinline__ float load1_res(const GemmParams& p, int m, int n) {
                    : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.res)[i]);
 }
 
-// Applies the epilogue to 8 consecutive columns n..n+7 of row m (all in range)
-// given the accumulators a (and a second accumulator b for the dual kinds).
-__device__ __forceinline__ void epi8(const GemmParams& p, int m, int n, const float (&a)[8],
-                                     const float (&b)[8]) {
-  float v[8];
+// Applies the epilogue to W consecutive columns n..n+W-1 of row m (all in
+// range) given the accumulators a (and a second accumulator b for the dual
+// kinds).
+template <int W>
+__device__ __forceinline__ void epiw(const GemmParams& p, int m, int n, const float (&a)[W],
+                                     const float (&b)[W]) {
+  float v[W];
   switch (p.epi) {
     case EPI_BF16: {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = a[j];
+      for (int j = 0; j < W; ++j) v[j] = a[j];
       if (p.bias) {
-        float t[8];
-        load8_bf16(p.bias + n, t);
+        float t[W];
+        loadw_bf16<W>(p.bias + n, t);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] += t[j];
+        for (int j = 0; j < W; ++j) v[j] += t[j];
       }
       if (p.res) {
-        float t[8];
-        load8_res(p, m, n, t);
+        float t[W];
+        loadw_res<W>(p, m, n, t);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] += t[j];
+        for (int j = 0; j < W; ++j) v[j] += t[j];
       }
-      store8_bf16(reinterpret_cast<__nv_bfloat16*>(p.out) + (long long)m * p.ldo + n, v);
+      storew_bf16<W>(reinterpret_cast<__nv_bfloat16*>(p.out) + (long long)m * p.ldo + n, v);
       break;
     }
     case EPI_GELU: {
-      float z[8];
+      float z[W];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) z[j] = a[j];
+      for (int j = 0; j < W; ++j) z[j] = a[j];
       if (p.bias) {
-        float t[8];
-        load8_bf16(p.bias + n, t);
+        float t[W];
+        loadw_bf16<W>(p.bias + n, t);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) z[j] += t[j];
+        for (int j = 0; j < W; ++j) z[j] += t[j];
       }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = gelu_f(z[j], p.act);
-      store8_bf16(reinterpret_cast<__nv_bfloat16*>(p.out) + (long long)m * p.ldo + n, v);
-      if (p.out2) store8_bf16(reinterpret_cast<__nv_bfloat16*>(p.out2) + (long long)m * p.ldo2 + n, z);
+      for (int j = 0; j < W; ++j) v[j] = gelu_f(z[j], p.act);
+      storew_bf16<W>(reinterpret_cast<__nv_bfloat16*>(p.out) + (long long)m * p.ldo + n, v);
+      if (p.out2) storew_bf16<W>(reinterpret_cast<__nv_bfloat16*>(p.out2) + (long long)m * p.ldo2 + n, z);
       break;
     }
     case EPI_SWIGLU: {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = a[j] * sigmoid_f(a[j]) * b[j];
-      store8_bf16(reinterpret_cast<__nv_bfloat16*>(p.out) + (long long)m * p.ldo + n, v);
-      if (p.out2) store8_bf16(reinterpret_cast<__nv_bfloat16*>(p.out2) + (long long)m * p.ldo2 + n, a);
-      if (p.out3) store8_bf16(reinterpret_cast<__nv_bfloat16*>(p.out3) + (long long)m * p.ldo3 + n, b);
+      for (int j = 0; j < W; ++j) v[j] = a[j] * sigmoid_f(a[j]) * b[j];
+      storew_bf16<W>(reinterpret_cast<__nv_bfloat16*>(p.out) + (long long)m * p.ldo + n, v);
+      if (p.out2) storew_bf16<W>(reinterpret_cast<__nv_bfloat16*>(p.out2) + (long long)m * p.ldo2 + n, a);
+      if (p.out3) storew_bf16<W>(reinterpret_cast<__nv_bfloat16*>(p.out3) + (long long)m * p.ldo3 + n, b);
       break;
     }
     case EPI_GELU_BWD: {
-      float z[8];
-      load8_bf16(p.aux + (long long)m * p.ldaux + n, z);
+      float z[W];
+      loadw_bf16<W>(p.aux + (long long)m * p.ldaux + n, z);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = a[j] * gelu_grad_f(z[j], p.act);
-      store8_bf16(reinterpret_cast<__nv_bfloat16*>(p.out) + (long long)m * p.ldo + n, v);
+      for (int j = 0; j < W; ++j) v[j] = a[j] * gelu_grad_f(z[j], p.act);
+      storew_bf16<W>(reinterpret_cast<__nv_bfloat16*>(p.out) + (long long)m * p.ldo + n, v);
       break;
     }
     case EPI_SWIGLU_BWD: {
-      float g[8], u[8], w2[8];
-      load8_bf16(p.aux + (long long)m * p.ldaux + n, g);
-      load8_bf16(p.aux2 + (long long)m * p.ldaux2 + n, u);
+      float g[W], u[W], w2[W];
+      loadw_bf16<W>(p.aux + (long long)m * p.ldaux + n, g);
+      loadw_bf16<W>(p.aux2 + (long long)m * p.ldaux2 + n, u);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < W; ++j) {
         const float sg = sigmoid_f(g[j]);
         v[j] = a[j] * u[j] * sg * (1.f + g[j] * (1.f - sg));
         w2[j] = a[j] * g[j] * sg;
       }
-      store8_bf16(reinterpret_cast<__nv_bfloat16*>(p.out) + (long long)m * p.ldo + n, v);
-      store8_bf16(reinterpret_cast<__nv_bfloat16*>(p.out2) + (long long)m * p.ldo2 + n, w2);
+      storew_bf16<W>(reinterpret_cast<__nv_bfloat16*>(p.out) + (long long)m * p.ldo + n, v);
+      storew_bf16<W>(reinterpret_cast<__nv_bfloat16*>(p.out2) + (long long)m * p.ldo2 + n, w2);
       break;
     }
     default: {  // EPI_F32
       float* o = reinterpret_cast<float*>(p.out) + (long long)m * p.ldo + n;
-      float t[8];
+      float t[W];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) t[j] = a[j];
+      for (int j = 0; j < W; ++j) t[j] = a[j];
       if (p.bias) {
-        float bb[8];
-        load8_bf16(p.bias + n, bb);
+        float bb[W];
+        loadw_bf16<W>(p.bias + n, bb);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) t[j] += bb[j];
+        for (int j = 0; j < W; ++j) t[j] += bb[j];
       }
       if (p.res) {
-        float rr[8];
-        load8_res(p, m, n, rr);
+        float rr[W];
+        loadw_res<W>(p, m, n, rr);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) t[j] += rr[j];
+        for (int j = 0; j < W; ++j) t[j] += rr[j];
       }
       if (p.ksplit > 1) {
         // one K range's share: added in L2 (the host zeroed out when beta = 0)
-        red_add_v4(o, t[0], t[1], t[2], t[3]);
-        red_add_v4(o + 4, t[4], t[5], t[6], t[7]);
+#pragma unroll
+        for (int j = 0; j < W; j += 4) red_add_v4(o + j, t[j], t[j + 1], t[j + 2], t[j + 3]);
         break;
       }
-      float4 x0 = make_float4(t[0], t[1], t[2], t[3]);
-      float4 x1 = make_float4(t[4], t[5], t[6], t[7]);
       if (p.beta != 0.f) {
-        const float4 o0 = reinterpret_cast<const float4*>(o)[0];
-        const float4 o1 = reinterpret_cast<const float4*>(o)[1];
-        x0.x += p.beta * o0.x; x0.y += p.beta * o0.y; x0.z += p.beta * o0.z; x0.w += p.beta * o0.w;
-        x1.x += p.beta * o1.x; x1.y += p.beta * o1.y; x1.z += p.beta * o1.z; x1.w += p.beta * o1.w;
+        float ov[W];
+        loadw_f32<W>(o, ov);
+#pragma unroll
+        for (int j = 0; j < W; ++j) t[j] += p.beta * ov[j];
       }
-      reinterpret_cast<float4*>(o)[0] = x0;
-      reinterpret_cast<float4*>(o)[1] = x1;
+      storew_f32<W>(o, t);
       break;
     }
   }
@@ -474,15 +548,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         if (m < p.M) {
           const int nb = n0 + col;
           if (nb + 32 <= p.N) {
+            if (p.vec32) {
+              // whole 32-byte sectors per access (the warp's 32 rows make 32
+              // separate segments either way), and the chunk's inputs all
+              // loaded before its first store
+              float a32[32], b32[32];
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              float a8[8], b8[8];
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                a8[j] = __uint_as_float(ra[g * 8 + j]);
-                b8[j] = DUAL ? __uint_as_float(rb[g * 8 + j]) : 0.f;
+              for (int j = 0; j < 32; ++j) {
+                a32[j] = __uint_as_float(ra[j]);
+                b32[j] = DUAL ? __uint_as_float(rb[j]) : 0.f;
               }
-              epi8(p, m, nb + g * 8, a8, b8);
+              epiw<32>(p, m, nb, a32, b32);
+            } else {
+#pragma unroll
+              for (int g = 0; g < 4; ++g) {
+                float a8[8], b8[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  a8[j] = __uint_as_float(ra[g * 8 + j]);
+                  b8[j] = DUAL ? __uint_as_float(rb[g * 8 + j]) : 0.f;
+                }
+                epiw<8>(p, m, nb + g * 8, a8, b8);
+              }
             }
           } else {
             // unrolled so the accumulators stay in registers
@@ -589,6 +676,16 @@ int gemm(int64_t M, int64_t N, int64_t K, const MatView& A, bool a_mn, const Mat
   p.beta = e.beta;
   p.err = device_error_word();
   if (!p.err) return 3;
+  {
+    // 32-byte epilogue accesses need 32-byte aligned operands and row strides
+    auto ok32 = [](const void* ptr, int64_t ld, int elem) {
+      return ptr == nullptr || ((reinterpret_cast<uintptr_t>(ptr) & 31) == 0 && ((ld * elem) & 31) == 0);
+    };
+    const int out_elem = e.kind == EPI_F32 ? 4 : 2;
+    p.vec32 = ok32(e.out, e.ldo, out_elem) && ok32(e.out2, e.ldo2, 2) && ok32(e.out3, e.ldo3, 2) &&
+              ok32(e.res, e.ldr, e.res_f32 ? 4 : 2) && ok32(e.aux, e.ldaux, 2) && ok32(e.aux2, e.ldaux2, 2) &&
+              ok32(e.bias, 0, 2);
+  }
   ProfScope prof(PROF_GEMM, 2.0 * (double)M * (double)N * (double)K * (dual ? 2 : 1), 0.0, stream);
   // Split K for fp32 outputs with nothing but the product (weight gradients)
   // when whole tiles would leave the last wave of SMs mostly idle: K ranges

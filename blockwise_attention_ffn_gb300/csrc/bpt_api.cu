@@ -128,7 +128,7 @@ size_t plan_fwd(const Dims& D, void* base, FwdWs* w, bool need_lse) {
 }
 
 struct BwdWs {
-  void *xn, *qkv, *o, *x1, *x1n, *z, *g, *u, *a, *dz, *dx1n, *dx1, *dO, *dqkv, *attn;
+  void *xn, *qkv, *o, *x1, *x1n, *gd, *g, *u, *a, *dz, *dx1n, *dx1, *dO, *dqkv, *attn;
   float *dxn, *dx1f;
 };
 AttnBwdShape stage_bwd_shape(const Dims& D, int64_t k);
@@ -141,9 +141,9 @@ size_t plan_bwd(const Dims& D, void* base, BwdWs* w) {
   w->o = c.take(D.rows * D.H * D.d * 2);
   w->x1 = c.take(D.cf * D.h * 4);  // fp32 residual stream
   w->x1n = c.take(D.cf * D.h * 2);
-  w->z = c.take(D.cf * D.f * 2);   // GeLU: pre-activation; SwiGLU: gate g
+  w->gd = c.take(D.cf * D.f * 2);  // GeLU: gelu'(z) of the recompute; SwiGLU: gate g
   w->u = c.take(D.cf * D.f * 2);   // SwiGLU: up u
-  w->g = w->z;
+  w->g = w->gd;
   w->a = c.take(D.cf * D.f * 2);
   w->dz = c.take(D.cf * D.f * 2 * 2);  // GeLU: dz [cf, f]; SwiGLU: [dg | du] [cf, 2f]
   w->dx1n = c.take(D.cf * D.h * 2);
@@ -598,7 +598,7 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
           e.kind = EPI_GELU;
           e.act = cfg->act;
           e.bias = hb ? w->b1 : nullptr;
-          e.out2 = W.z;
+          e.out2 = W.gd;  // gelu'(z), which the fc2 backward multiplies by
           e.ldo2 = f;
           if ((rc = gemm(nr, f, h, A, false, &B, &h, 1, false, nullptr, e, st))) return rc;
         }
@@ -636,7 +636,7 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
         } else {
           e.kind = EPI_GELU_BWD;
           e.act = cfg->act;
-          e.aux = W.z;
+          e.aux = W.gd;
           e.ldaux = f;
           e.out = W.dz;
           e.ldo = f;
@@ -720,7 +720,14 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
     if ((rc = gemm(D.rows, Hd, h, A, false, &B, &h, 1, true, nullptr, e, st))) return rc;
   }
 
-  // ---- attention and Q/K/V gradients, stage by stage
+  // ---- attention and Q/K/V gradients, stage by stage.  The key-bias
+  // gradient is identically zero: the bias adds Q[q].bk to every logit of
+  // query row q alike (masked ones stay -inf), and softmax is invariant to
+  // such a shift, so the loss does not depend on bk.  It is written as exact
+  // zeros (left as is when accumulating) instead of summing dK, whose sum of
+  // bf16-rounded rows would be rounding noise growing like sqrt(s).
+  if (hb && !accum && cudaMemsetAsync(g->bk, 0, (size_t)(D.Hkv * D.d) * sizeof(float), st) != cudaSuccess)
+    return BPT_ECUDA;
   for (int64_t k = 0; k < D.n_stages; ++k) {
     if (D.chunked && (rc = stage_qkv(D, w, hb, W.xn, W.qkv, k, st))) return rc;
     // the previous stage's weight gradients (side stream) read dqkv, which
@@ -762,7 +769,8 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
         e.ldo = h;
         e.beta = accum ? 1.f : 0.f;
         if ((rc = gemm(pc.n, h, K, A, true, &B, &K, 1, true, nullptr, e, ss))) return rc;
-        if (hb && (rc = colsum(D.rows, pc.n, bf(W.dqkv, pc.col), D.qkv_w, f32(pc.Gb, pc.row0), accum, ss)))
+        if (hb && pc.Gb != g->bk &&
+            (rc = colsum(D.rows, pc.n, bf(W.dqkv, pc.col), D.qkv_w, f32(pc.Gb, pc.row0), accum, ss)))
           return rc;
       }
     }

@@ -63,14 +63,18 @@ __device__ __forceinline__ float gelu_f(float z, int act) {
   const float c = 0.7978845608028654f;
   return 0.5f * z * (1.f + tanhf(c * (z + 0.044715f * z * z * z)));
 }
-__device__ __forceinline__ float gelu_grad_f(float z, int act) {
+// gelu(z) and gelu'(z) sharing the erf (or tanh)
+__device__ __forceinline__ void gelu_and_grad_f(float z, int act, float& g, float& d) {
   if (act == 0) {
-    const float phi = expf(-0.5f * z * z) * 0.3989422804014327f;
-    return 0.5f * (1.f + erff(z * 0.70710678118654752f)) + z * phi;
+    const float cdf = 0.5f * (1.f + erff(z * 0.70710678118654752f));
+    g = z * cdf;
+    d = cdf + z * expf(-0.5f * z * z) * 0.3989422804014327f;
+  } else {
+    const float c = 0.7978845608028654f;
+    const float t = tanhf(c * (z + 0.044715f * z * z * z));
+    g = 0.5f * z * (1.f + t);
+    d = 0.5f * (1.f + t) + 0.5f * z * (1.f - t * t) * c * (1.f + 3.f * 0.044715f * z * z);
   }
-  const float c = 0.7978845608028654f;
-  const float t = tanhf(c * (z + 0.044715f * z * z * z));
-  return 0.5f * (1.f + t) + 0.5f * z * (1.f - t * t) * c * (1.f + 3.f * 0.044715f * z * z);
 }
 __device__ __forceinline__ float sigmoid_f(float z) { return 1.f / (1.f + expf(-z)); }
 
@@ -216,10 +220,18 @@ __device__ __forceinline__ void epiw(const GemmParams& p, int m, int n, const fl
 #pragma unroll
         for (int j = 0; j < W; ++j) z[j] += t[j];
       }
+      if (p.out2) {
+        // out2 = gelu'(z), the factor the backward multiplies dA by
+        float d[W];
 #pragma unroll
-      for (int j = 0; j < W; ++j) v[j] = gelu_f(z[j], p.act);
-      storew_bf16<W>(reinterpret_cast<__nv_bfloat16*>(p.out) + (long long)m * p.ldo + n, v);
-      if (p.out2) storew_bf16<W>(reinterpret_cast<__nv_bfloat16*>(p.out2) + (long long)m * p.ldo2 + n, z);
+        for (int j = 0; j < W; ++j) gelu_and_grad_f(z[j], p.act, v[j], d[j]);
+        storew_bf16<W>(reinterpret_cast<__nv_bfloat16*>(p.out) + (long long)m * p.ldo + n, v);
+        storew_bf16<W>(reinterpret_cast<__nv_bfloat16*>(p.out2) + (long long)m * p.ldo2 + n, d);
+      } else {
+#pragma unroll
+        for (int j = 0; j < W; ++j) v[j] = gelu_f(z[j], p.act);
+        storew_bf16<W>(reinterpret_cast<__nv_bfloat16*>(p.out) + (long long)m * p.ldo + n, v);
+      }
       break;
     }
     case EPI_SWIGLU: {
@@ -231,10 +243,10 @@ __device__ __forceinline__ void epiw(const GemmParams& p, int m, int n, const fl
       break;
     }
     case EPI_GELU_BWD: {
-      float z[W];
-      loadw_bf16<W>(p.aux + (long long)m * p.ldaux + n, z);
+      float gd[W];
+      loadw_bf16<W>(p.aux + (long long)m * p.ldaux + n, gd);
 #pragma unroll
-      for (int j = 0; j < W; ++j) v[j] = a[j] * gelu_grad_f(z[j], p.act);
+      for (int j = 0; j < W; ++j) v[j] = a[j] * gd[j];
       storew_bf16<W>(reinterpret_cast<__nv_bfloat16*>(p.out) + (long long)m * p.ldo + n, v);
       break;
     }
@@ -299,10 +311,11 @@ __device__ __forceinline__ void epi1(const GemmParams& p, int m, int n, float a,
     }
     case EPI_GELU: {
       float z = a + (p.bias ? __bfloat162float(p.bias[n]) : 0.f);
-      reinterpret_cast<__nv_bfloat16*>(p.out)[(long long)m * p.ldo + n] =
-          __float2bfloat16(gelu_f(z, p.act));
+      float g, d;
+      gelu_and_grad_f(z, p.act, g, d);
+      reinterpret_cast<__nv_bfloat16*>(p.out)[(long long)m * p.ldo + n] = __float2bfloat16(g);
       if (p.out2)
-        reinterpret_cast<__nv_bfloat16*>(p.out2)[(long long)m * p.ldo2 + n] = __float2bfloat16(z);
+        reinterpret_cast<__nv_bfloat16*>(p.out2)[(long long)m * p.ldo2 + n] = __float2bfloat16(d);
       break;
     }
     case EPI_SWIGLU: {
@@ -315,9 +328,8 @@ __device__ __forceinline__ void epi1(const GemmParams& p, int m, int n, float a,
       break;
     }
     case EPI_GELU_BWD: {
-      const float z = __bfloat162float(p.aux[(long long)m * p.ldaux + n]);
-      reinterpret_cast<__nv_bfloat16*>(p.out)[(long long)m * p.ldo + n] =
-          __float2bfloat16(a * gelu_grad_f(z, p.act));
+      const float gd = __bfloat162float(p.aux[(long long)m * p.ldaux + n]);
+      reinterpret_cast<__nv_bfloat16*>(p.out)[(long long)m * p.ldo + n] = __float2bfloat16(a * gd);
       break;
     }
     case EPI_SWIGLU_BWD: {

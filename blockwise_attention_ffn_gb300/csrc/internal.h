@@ -49,9 +49,9 @@ struct MatView {
 
 enum EpiKind {
   EPI_BF16 = 0,        // out = acc (+ bias[n]) (+ res[m, n])            -> bf16
-  EPI_GELU = 1,        // z = acc + bias; out = gelu(z); out2 = z (opt)  -> bf16
+  EPI_GELU = 1,        // z = acc + bias; out = gelu(z); out2 = gelu'(z) (opt) -> bf16
   EPI_SWIGLU = 2,      // dual: out = silu(g) * u; out2 = g, out3 = u (opt) -> bf16
-  EPI_GELU_BWD = 3,    // out = acc * gelu'(aux[m, n])                   -> bf16
+  EPI_GELU_BWD = 3,    // out = acc * aux[m, n] (aux = gelu'(z))          -> bf16
   EPI_SWIGLU_BWD = 4,  // acc = dA; g = aux, u = aux2: out = dA*u*silu'(g), out2 = dA*silu(g)
   EPI_F32 = 5,         // out = acc (+ bias) (+ res) + beta * out        -> fp32
 };

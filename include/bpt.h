@@ -142,6 +142,9 @@ int bpt_layer_fwd(const bpt_config* cfg, const bpt_weights* w, const void* x, vo
 /* Backward pass with recomputation.
  *   x: the forward input; saved: what bpt_layer_fwd wrote; dy [b,s,h] bf16.
  *   dx [b,s,h] bf16 out; grads: fp32 weight gradients (see BPT_FLAG_ACCUM_GRADS).
+ *   The key-bias gradient bk is written as exact zeros (left unchanged when
+ *   accumulating): the bias shifts every logit of a query row alike, and
+ *   softmax is invariant to that, so the gradient is identically zero.
  * The forward pass is rerun blockwise (N1, Q/K/V, attention, output
  * projection, and per FFN block N2 and fc1) and every gradient is formed
  * from the rebuilt blocks: attention probabilities are rebuilt from Q, K and

@@ -58,17 +58,41 @@ struct GemmParams {
   unsigned int* err;
 };
 
+// Phi(z) = 0.5 (1 + erf(z / sqrt 2)) and e = exp(-z^2 / 2) for the erf GeLU,
+// with erf from Abramowitz & Stegun, "Handbook of Mathematical Functions",
+// formula 7.1.26: erf(x) = 1 - (a1 t + a2 t^2 + ... + a5 t^5) exp(-x^2),
+// t = 1 / (1 + p x), x >= 0, absolute error at most 1.5e-7 (far below the
+// bf16 outputs' rounding).  exp(-x^2) at x = z / sqrt 2 is the same e the
+// derivative needs, so both come from one exp2 and one reciprocal.
+__device__ __forceinline__ void gelu_erf_parts(float z, float& cdf, float& e) {
+  const float x = fabsf(z) * 0.70710678118654752f;
+  float t;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(fmaf(0.3275911f, x, 1.f)));
+  float poly = fmaf(1.061405429f, t, -1.453152027f);
+  poly = fmaf(poly, t, 1.421413741f);
+  poly = fmaf(poly, t, -0.284496736f);
+  poly = fmaf(poly, t, 0.254829592f);
+  poly *= t;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-0.72134752044448170f * z * z));  // exp(-z^2/2)
+  const float tail = 0.5f * poly * e;  // 0.5 (1 - erf(|x|))
+  cdf = z >= 0.f ? 1.f - tail : tail;
+}
 __device__ __forceinline__ float gelu_f(float z, int act) {
-  if (act == 0) return 0.5f * z * (1.f + erff(z * 0.70710678118654752f));
+  if (act == 0) {
+    float cdf, e;
+    gelu_erf_parts(z, cdf, e);
+    return z * cdf;
+  }
   const float c = 0.7978845608028654f;
   return 0.5f * z * (1.f + tanhf(c * (z + 0.044715f * z * z * z)));
 }
 // gelu(z) and gelu'(z) sharing the erf (or tanh)
 __device__ __forceinline__ void gelu_and_grad_f(float z, int act, float& g, float& d) {
   if (act == 0) {
-    const float cdf = 0.5f * (1.f + erff(z * 0.70710678118654752f));
+    float cdf, e;
+    gelu_erf_parts(z, cdf, e);
     g = z * cdf;
-    d = cdf + z * expf(-0.5f * z * z) * 0.3989422804014327f;
+    d = fmaf(z * e, 0.3989422804014327f, cdf);  // Phi(z) + z phi(z)
   } else {
     const float c = 0.7978845608028654f;
     const float t = tanhf(c * (z + 0.044715f * z * z * z));

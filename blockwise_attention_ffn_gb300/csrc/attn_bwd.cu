@@ -407,18 +407,9 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_kernel(const __grid_constant
 // use.  The row's 8 nonzero-capable columns arrive with the Q/dO stage
 // (16 bytes per query, unswizzled: exactly the K-major core-matrix layout);
 // the descriptor points its upper 8 columns at one shared 2 KB of zeros.
-// Warps: 0 TMA, 1 MMA, 2..9 compute.  Compute warp w owns key/value rows
-// (w % 4) * 32 + lane (its TMEM lane quarter) and query columns
-// [64h, 64h+64), h = (w - 2) / 4.  Per step it forms P^T for its columns
-// (kept in registers as bf16 pairs and stored over the first 32 of its 64
-// S^T columns), then dS^T (stored over the first 32 of its dP^T columns).
-// TMEM: S^T/P^T [0,128), dP^T/dS^T [128,256), dV [256, 256+D),
-//       dK [256+D, 256+2D), K' [256+2D, 256+2.5D+8), V' [.., 256+3D+16).
-// Shared memory: QS stages of (Q, dO, the 128 query rows' 16-byte extra
-// rows), then the zeros.
-// MMA order per step t: dV(t), S(t+1), dK(t), dP(t+1).  A product that
-// overwrites the TMEM operand of the one issued before it relies on the
-// tensor pipe executing one thread's products in issue order.
+// TMEM: dV [256, 256+D), dK [256+D, 256+2D), K' [256+2D, 256+2.5D+8),
+// V' [.., 256+3D+16); shared memory: QS stages of (Q, dO, the 128 query rows'
+// 16-byte extra rows), then the zeros.
 template <int D>
 struct DkdvTmCfg {
   using T = TileGeom<D>;
@@ -430,14 +421,27 @@ struct DkdvTmCfg {
   static constexpr uint32_t COL_DV = 256, COL_DK = 256 + D, COL_K = 256 + 2 * D, COL_V = 256 + 2 * D + D / 2 + 8;
 };
 
+// A step covers 64 queries: sub-tile u is the half u % 2 of
+// stage u / 2, and its S^T and dP^T go to buffer b = u % 2 (64 columns each:
+// the same 256 columns as one 128-query buffer of each).  Compute warps 2..5
+// (group 0) take the even sub-tiles, 6..9 (group 1) the odd ones, each warp
+// its lane quarter's 32 key rows by all 64 query columns, so one group's
+// exponentials overlap the other group's products instead of alternating
+// with them.  Warp 1 issues group 0's products, warp 10 group 1's, in the
+// order S(u), dP(u), dV(u) (after P^T(u)), S(u+2), dK(u) (after dS^T(u)),
+// dP(u+2): every product that overwrites a buffer comes after its reader
+// from the same thread.  Both issuers add into dV and dK, which the compute
+// warps zero first; a stage is released once both issuers' products on it
+// are done.
+// TMEM: S^T [0,64) [64,128), dP^T [128,192) [192,256), then as above.
 template <int D>
-__global__ void __launch_bounds__(320, 1) attn_dkdv_tm_kernel(const __grid_constant__ AttnBwdParams p) {
+__global__ void __launch_bounds__(352, 1) attn_dkdv_hs_kernel(const __grid_constant__ AttnBwdParams p) {
   using T = TileGeom<D>;
   using C = DkdvTmCfg<D>;
   constexpr int QS = C::QS;
   constexpr int STAGE = C::STAGE;
   static_assert(C::COL_V + D / 2 + 8 <= 512, "TMEM columns");
-  constexpr uint32_t ID_SQ = idesc_bf16(128, 128, false, false);
+  constexpr uint32_t ID_S = idesc_bf16(128, 64, false, false);
   constexpr uint32_t ID_KV = idesc_bf16(128, D, false, true);
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -445,17 +449,16 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_tm_kernel(const __grid_const
   uint8_t* sStage = smem;
   uint8_t* sZero = sStage + QS * STAGE;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sZero + C::ZERO);
-  uint64_t* kv_ready = bars;            // K, V copied into TMEM (8 compute warps)
-  uint64_t* qdo_full = bars + 1;
-  uint64_t* qdo_empty = qdo_full + QS;
-  uint64_t* s_full = qdo_empty + QS;    // S^T(t) in TMEM
-  uint64_t* dp_full = s_full + 1;       // dP^T(t) in TMEM
-  uint64_t* p_full = dp_full + 1;       // P^T(t) written (8 compute warps)
-  uint64_t* p_used = p_full + 1;        // dV(t) done
-  uint64_t* ds_full = p_used + 1;       // dS^T(t) written (8 compute warps)
-  uint64_t* it_done = ds_full + 1;      // dK(t) done
-  uint64_t* drain = it_done + 1;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* kv_ready = bars;            // K', V' in TMEM, dV, dK zeroed (8 compute warps)
+  uint64_t* qdo_full = bars + 1;        // [QS]
+  uint64_t* qdo_empty = qdo_full + QS;  // [QS], both issuers
+  uint64_t* s_full = qdo_empty + QS;    // [2] S^T(u) in buffer u % 2
+  uint64_t* dp_full = s_full + 2;       // [2]
+  uint64_t* p_full = dp_full + 2;       // [2] P^T(u) written (4 warps of the group)
+  uint64_t* ds_full = p_full + 2;       // [2] dS^T(u) written (4 warps)
+  uint64_t* all_done = ds_full + 2;     // both issuers' last products done
+  uint64_t* drain = all_done + 1;       // [2], one per issuer
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = warp_id();
@@ -469,21 +472,23 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_tm_kernel(const __grid_const
   const int bi = pair / p.Hkv;
   const int i0 = p.causal ? j : 0;
   const int n_i = nq_total - i0;
-  const int T_iter = p.G * n_i;
+  const int T_iter = p.G * n_i;  // stages
+  const int U = 2 * T_iter;      // sub-tiles
 
   if (threadIdx.x == 0) {
     mbar_init(kv_ready, 8);
     for (int i = 0; i < QS; ++i) {
       mbar_init(&qdo_full[i], 1);
-      mbar_init(&qdo_empty[i], 1);
+      mbar_init(&qdo_empty[i], 2);
     }
-    mbar_init(s_full, 1);
-    mbar_init(dp_full, 1);
-    mbar_init(p_full, 8);
-    mbar_init(p_used, 1);
-    mbar_init(ds_full, 8);
-    mbar_init(it_done, 1);
-    mbar_init(drain, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&dp_full[b], 1);
+      mbar_init(&p_full[b], 4);
+      mbar_init(&ds_full[b], 4);
+      mbar_init(&drain[b], 1);
+    }
+    mbar_init(all_done, 2);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -504,8 +509,8 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_tm_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const uint32_t tS = tmem;
-  const uint32_t tdP = tmem + 128;
+  const uint32_t tS = tmem;          // + 64 b
+  const uint32_t tdP = tmem + 128;   // + 64 b
   const uint32_t tdV = tmem + C::COL_DV;
   const uint32_t tdK = tmem + C::COL_DK;
   const uint32_t tKA = tmem + C::COL_K;
@@ -517,7 +522,7 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_tm_kernel(const __grid_const
       int issued = 0;
       for (int t = 0; t < T_iter; ++t) {
         const int st = t % QS;
-        if (t >= QS && !bounded_wait(&qdo_empty[st], ((t / QS) & 1) ^ 1, abort_flag, 571, p.err)) break;
+        if (t >= QS && !bounded_wait(&qdo_empty[st], ((t / QS) & 1) ^ 1, abort_flag, 631, p.err)) break;
         const int hn = g * p.G + t / n_i;
         const int i = i0 + t % n_i;
         uint8_t* sQ = sStage + st * STAGE;
@@ -534,89 +539,93 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_tm_kernel(const __grid_const
       }
       if (*abort_flag) {
         for (int t = (issued > QS ? issued - QS : 0); t < issued; ++t)
-          bounded_wait(&qdo_full[t % QS], (t / QS) & 1, abort_flag, 572, p.err);
+          bounded_wait(&qdo_full[t % QS], (t / QS) & 1, abort_flag, 632, p.err);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 10) {
     if (lane == 0) {
-      // ------------------------------------------------ MMA issuer
-      auto stage_u = [&](int t) { return smem_u32(sStage + (t % QS) * STAGE); };
-      // one more contraction step each: the extra rows (8-row groups 128
-      // bytes apart, the upper 8 columns in the zeros) against the chunk
-      // appended to K resp. V
+      // ------------------------------------------------ MMA issuers
+      const int b = warp == 1 ? 0 : 1;  // this issuer's buffer and sub-tiles
       const uint32_t uZero = smem_u32(sZero);
-      auto aux_desc = [&](int t) {
-        const uint32_t uA = stage_u(t) + 2 * T::TILE;
-        return sdesc(uA, uZero - uA, 128, 0u);
-      };
-      auto issue_s = [&](int t) {
-        const uint32_t uQ = stage_u(t);
+      const uint32_t tSb = tS + 64 * b, tdPb = tdP + 64 * b;
+      // the 64 query rows of sub-tile half b start 64 b rows into every
+      // chunk of the stage's tiles (whole swizzle atoms), and 64 b rows into
+      // its extra rows
+      auto stage_u = [&](int u) { return smem_u32(sStage + ((u >> 1) % QS) * STAGE); };
+      auto issue_s = [&](int u) {
+        const uint32_t uQ = stage_u(u) + 64 * T::SWB * b;
+        const uint32_t uA = stage_u(u) + 2 * T::TILE + 64 * 16 * b;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a(tS, tKA + kk * 8, T::kmajor(uQ, kk), ID_SQ, kk > 0);
-        umma_bf16_tmem_a(tS, tKA + D / 2, aux_desc(t), ID_SQ, 1);
-        umma_commit(s_full);
+        for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a(tSb, tKA + kk * 8, T::kmajor(uQ, kk), ID_S, kk > 0);
+        umma_bf16_tmem_a(tSb, tKA + D / 2, sdesc(uA, uZero - uA, 128, 0u), ID_S, 1);
+        umma_commit(&s_full[b]);
       };
-      auto issue_dp = [&](int t) {
-        const uint32_t udO = stage_u(t) + T::TILE;
+      auto issue_dp = [&](int u) {
+        const uint32_t udO = stage_u(u) + T::TILE + 64 * T::SWB * b;
+        const uint32_t uA = stage_u(u) + 2 * T::TILE + 64 * 16 * b;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a(tdP, tVA + kk * 8, T::kmajor(udO, kk), ID_SQ, kk > 0);
-        umma_bf16_tmem_a(tdP, tVA + D / 2, aux_desc(t), ID_SQ, 1);
-        umma_commit(dp_full);
+        for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a(tdPb, tVA + kk * 8, T::kmajor(udO, kk), ID_S, kk > 0);
+        umma_bf16_tmem_a(tdPb, tVA + D / 2, sdesc(uA, uZero - uA, 128, 0u), ID_S, 1);
+        umma_commit(&dp_full[b]);
       };
-      bool ok = bounded_wait(kv_ready, 0, abort_flag, 581, p.err) &&
-                bounded_wait(&qdo_full[0], 0, abort_flag, 582, p.err);
+      auto wait_stage = [&](int u) {
+        const int t = u >> 1;
+        return bounded_wait(&qdo_full[t % QS], (t / QS) & 1, abort_flag, 641, p.err);
+      };
+      bool ok = bounded_wait(kv_ready, 0, abort_flag, 642, p.err) && wait_stage(b);
       if (ok) {
         tc_fence_after();
-        issue_s(0);
-        issue_dp(0);
+        issue_s(b);
+        issue_dp(b);
       }
-      for (int t = 0; ok && t < T_iter; ++t) {
-        const int st = t % QS;
-        const uint32_t uQ = stage_u(t);
+      for (int u = b; ok && u < U; u += 2) {
+        const int st = (u >> 1) % QS;
+        const uint32_t uQ = stage_u(u);
         const uint32_t udO = uQ + T::TILE;
-        const bool more = t + 1 < T_iter;
-        // dV(t) += P^T(t) dO(t); the P^T pairs of query columns 64h.. sit at
-        // TMEM column 64h
-        if (!bounded_wait(p_full, t & 1, abort_flag, 583, p.err)) { ok = false; break; }
+        const bool more = u + 2 < U;
+        // dV += P^T(u) dO(u): the P^T pairs sit over the first 32 columns of
+        // buffer b; dO rows 64b.. are K blocks 4b..4b+3 of the stage's tile
+        if (!bounded_wait(&p_full[b], (u >> 1) & 1, abort_flag, 643, p.err)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_tmem_a(tdV, tS + (kk >> 2) * 64 + (kk & 3) * 8, T::mnmajor(udO, kk), ID_KV, (t > 0 || kk > 0));
-        umma_commit(p_used);
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16_tmem_a(tdV, tSb + kk * 8, T::mnmajor(udO, 4 * b + kk), ID_KV, 1);
         if (more) {
-          // S(t+1) overwrites P^T(t), after dV(t) in issue order
-          if (!bounded_wait(&qdo_full[(t + 1) % QS], ((t + 1) / QS) & 1, abort_flag, 586, p.err)) { ok = false; break; }
+          // S(u+2) overwrites P^T(u), after dV(u) in issue order
+          if (!wait_stage(u + 2)) { ok = false; break; }
           tc_fence_after();
-          issue_s(t + 1);
+          issue_s(u + 2);
         }
-        // dK(t) += dS^T(t) Q(t)
-        if (!bounded_wait(ds_full, t & 1, abort_flag, 587, p.err)) { ok = false; break; }
+        // dK += dS^T(u) Q(u)
+        if (!bounded_wait(&ds_full[b], (u >> 1) & 1, abort_flag, 644, p.err)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_tmem_a(tdK, tdP + (kk >> 2) * 64 + (kk & 3) * 8, T::mnmajor(uQ, kk), ID_KV, (t > 0 || kk > 0));
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16_tmem_a(tdK, tdPb + kk * 8, T::mnmajor(uQ, 4 * b + kk), ID_KV, 1);
         umma_commit(&qdo_empty[st]);
-        umma_commit(it_done);
-        // dP(t+1) overwrites dS^T(t), after dK(t) in issue order
-        if (more) issue_dp(t + 1);
+        // dP(u+2) overwrites dS^T(u), after dK(u) in issue order
+        if (more) issue_dp(u + 2);
       }
+      if (ok) umma_commit(all_done);
       if (!ok) {
-        umma_commit(drain);
-        bounded_wait(drain, 0, abort_flag, 589, p.err);
+        umma_commit(&drain[b]);
+        bounded_wait(&drain[b], 0, abort_flag, 645, p.err);
       }
     }
   } else {
+    // ------------------------------------------------ compute (warps 2..9;
+    // lanes 1..31 of the issuer warps fall through to the final barrier)
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int b = (warp - 2) >> 2;  // group = buffer = sub-tile parity
     const int r = quarter * 32 + lane;
     const int kvp = j * 128 + r;
-    const int c0 = half * 64;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     {
-      // K (half 0) or V (half 1) row of this thread into TMEM as bf16 pairs;
-      // rows past the sequence are zero
+      // K (group 0) or V (group 1) row of this thread into TMEM as bf16
+      // pairs with the extra chunk (rows past the sequence are zero), and
+      // the group's accumulator (dV, dK) zeroed: both issuers add into it
       uint32_t w[D / 2 + 8];
-      const __nv_bfloat16* src = p.qkv + ((long long)bi * p.s + kvp) * p.ld_qkv + (half ? p.v_col : p.k_col) +
+      const __nv_bfloat16* src = p.qkv + ((long long)bi * p.s + kvp) * p.ld_qkv + (b ? p.v_col : p.k_col) +
                                  (long long)g * D;
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) {
@@ -629,34 +638,39 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_tm_kernel(const __grid_const
       }
       // the extra chunk: K picks the (hi, lo) pair of -LSE*sqrt(d) (columns
       // 0, 1 of the query's extra row), V that of -D (columns 2, 3)
-      w[D / 2] = half ? 0u : 0x3F803F80u;
-      w[D / 2 + 1] = half ? 0x3F803F80u : 0u;
+      w[D / 2] = b ? 0u : 0x3F803F80u;
+      w[D / 2 + 1] = b ? 0x3F803F80u : 0u;
 #pragma unroll
       for (int c = 2; c < 8; ++c) w[D / 2 + c] = 0u;
-      const uint32_t dst = (half ? tVA : tKA) + lane_off;
-      tmem_store_row<D / 2 + 8>(dst, w);
+      tmem_store_row<D / 2 + 8>((b ? tVA : tKA) + lane_off, w);
+      uint32_t z[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) z[c] = 0u;
+#pragma unroll
+      for (int cc = 0; cc < D / 16; ++cc) tmem_st16_nw((b ? tdK : tdV) + lane_off + cc * 16, z);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(kv_ready);
     }
     const float c = p.scale_log2;
+    const uint32_t tSb = tS + 64 * b, tdPb = tdP + 64 * b;
     bool ok = true;
-    for (int t = 0; t < T_iter; ++t) {
-      const int st = t % QS;
-      const int q0 = (i0 + t % n_i) * 128;
-      ok = bounded_wait(s_full, t & 1, abort_flag, 592, p.err);
+    for (int u = b; u < U; u += 2) {
+      const int t = u >> 1;
+      const int q0 = (i0 + t % n_i) * 128 + 64 * b;
+      ok = bounded_wait(&s_full[b], (u >> 1) & 1, abort_flag, 651, p.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      // ---- phase 1: P^T = exp2(S'^T * scale*log2(e)) for the 64 columns
-      // (S' already offset by -LSE*sqrt(d)); columns [lo, hi) are unmasked
-      int lo = 0, hi = min(64, p.s - (q0 + c0));
-      if (p.causal) lo = max(0, kvp - (q0 + c0));
+      // ---- phase 1: P^T = exp2(S'^T * scale*log2(e)) (S' offset by
+      // -LSE*sqrt(d)); query columns [lo, hi) of the 64 are unmasked
+      int lo = 0, hi = min(64, p.s - q0);
+      if (p.causal) lo = max(0, kvp - q0);
       if (kvp >= p.s) lo = 64;
       const bool edge = lo > 0 || hi < 64;
       uint32_t sv[64];
-      tmem_ld32_nw(tS + lane_off + c0, sv);
-      tmem_ld32_nw(tS + lane_off + c0 + 32, sv + 32);
+      tmem_ld32_nw(tSb + lane_off, sv);
+      tmem_ld32_nw(tSb + lane_off + 32, sv + 32);
       tmem_wait_ld(sv);
       // P^T in fp32 (for dS^T) and as bf16 pairs (the dV operand)
       float pe[64];
@@ -670,45 +684,40 @@ __global__ void __launch_bounds__(320, 1) attn_dkdv_tm_kernel(const __grid_const
       uint32_t pk[32];
 #pragma unroll
       for (int k = 0; k < 64; k += 2) pk[k / 2] = pack_bf16(pe[k], pe[k + 1]);
-      tmem_st32(tS + lane_off + c0, pk);
+      tmem_st32(tSb + lane_off, pk);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
-      // ---- phase 2: dS^T = P^T dP'^T (dP' already offset by -D), P^T from
-      // registers (fp32)
-      ok = bounded_wait(dp_full, t & 1, abort_flag, 593, p.err);
+      if (lane == 0) mbar_arrive(&p_full[b]);
+      // ---- phase 2: dS^T = P^T dP'^T (dP' offset by -D)
+      ok = bounded_wait(&dp_full[b], (u >> 1) & 1, abort_flag, 652, p.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       uint32_t dr[64];
-      tmem_ld32_nw(tdP + lane_off + c0, dr);
-      tmem_ld32_nw(tdP + lane_off + c0 + 32, dr + 32);
+      tmem_ld32_nw(tdPb + lane_off, dr);
+      tmem_ld32_nw(tdPb + lane_off + 32, dr + 32);
       tmem_wait_ld(dr);
       uint32_t o[32];
 #pragma unroll
       for (int k = 0; k < 64; k += 2)
         o[k / 2] = pack_bf16(pe[k] * __uint_as_float(dr[k]), pe[k + 1] * __uint_as_float(dr[k + 1]));
-      tmem_st32(tdP + lane_off + c0, o);
+      tmem_st32(tdPb + lane_off, o);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(ds_full);
+      if (lane == 0) mbar_arrive(&ds_full[b]);
     }
-    // epilogue: half 0 writes dV, half 1 dK (TMEM loads by every lane,
-    // stores only for rows inside the sequence).  Both barriers are at most
-    // one phase ahead of the step these warps last saw complete.
-    if (ok) {
-      const bool done = half == 0 ? bounded_wait(p_used, (T_iter - 1) & 1, abort_flag, 605, p.err)
-                                  : bounded_wait(it_done, (T_iter - 1) & 1, abort_flag, 606, p.err);
-      ok = __all_sync(0xffffffffu, done);
-    }
+    // epilogue: group 0 writes dV, group 1 dK, once both issuers' products
+    // are done (TMEM loads by every lane, stores only for rows inside the
+    // sequence)
+    if (ok) ok = __all_sync(0xffffffffu, bounded_wait(all_done, 0, abort_flag, 653, p.err));
     if (ok) {
       tc_fence_after();
       const bool valid = kvp < p.s;
-      const uint32_t tsrc = (half == 0 ? tdV : tdK) + lane_off;
+      const uint32_t tsrc = (b == 0 ? tdV : tdK) + lane_off;
       __nv_bfloat16* row = p.dqkv + ((long long)bi * p.s + kvp) * p.ld_dqkv +
-                           (half == 0 ? p.dv_col : p.dk_col) + (long long)g * D;
-      const float sc = half == 0 ? 1.f : p.scale;
+                           (b == 0 ? p.dv_col : p.dk_col) + (long long)g * D;
+      const float sc = b == 0 ? 1.f : p.scale;
       uint32_t acc[D];
 #pragma unroll
       for (int cc = 0; cc < D / 16; ++cc) tmem_ld16_nw(tsrc + cc * 16, acc + cc * 16);
@@ -1067,16 +1076,16 @@ int launch_dkdv(AttnBwdParams& prm, int grid, cudaStream_t st) {
 }
 
 template <int D>
-int launch_dkdv_tm(AttnBwdParams& prm, int grid, cudaStream_t st) {
+int launch_dkdv_hs(AttnBwdParams& prm, int grid, cudaStream_t st) {
   constexpr int SMEM = DkdvTmCfg<D>::SMEM;
   static_assert(SMEM <= 232448, "dK/dV tile set exceeds shared memory");
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(attn_dkdv_tm_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
+    if (cudaFuncSetAttribute(attn_dkdv_hs_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
       return 3;
     attr = true;
   }
-  attn_dkdv_tm_kernel<D><<<grid, 320, SMEM, st>>>(prm);
+  attn_dkdv_hs_kernel<D><<<grid, 352, SMEM, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 
@@ -1103,7 +1112,7 @@ int launch_both(AttnBwdParams& prm, const AttnShape& f, cudaStream_t st) {
     ProfScope prof(PROF_ATTN_BWD, 8.0 * f.d * pairs * f.H * f.b, 0.0, st);
     const int grid = ((f.s + 127) / 128) * f.Hkv * f.b;
     if constexpr (D <= 80)
-      rc = launch_dkdv_tm<D>(prm, grid, st);
+      rc = launch_dkdv_hs<D>(prm, grid, st);
     else
       rc = launch_dkdv<D>(prm, grid, st);
   }

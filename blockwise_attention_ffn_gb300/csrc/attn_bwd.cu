@@ -738,65 +738,56 @@ __global__ void __launch_bounds__(352, 1) attn_dkdv_hs_kernel(const __grid_const
   }
 }
 
-// ===========================================================================
-// dQ
-// ===========================================================================
-// One CTA per 128-row query tile i of one query head; it loops over the
-// key/value tiles j <= i.  Every product takes its A operand from TMEM: Q
-// and dO are copied there once per CTA (the A operands of S = Q K_j^T and
-// dP = dO V_j^T) and dS is written over dP as bf16 pairs (the A operand of
-// dQ += dS K_j).  Shared memory holds only the K/V ring.
-// Warps: 0 TMA, 1 and 10 MMA issuers, 2..9 compute.  MMA issue blocks until
-// the tensor core takes the product, so one thread issuing everything would
-// put the S chain (S(j+1), needed by P) behind the dQ/dP chain (dQ(j),
-// dP(j+1), needed by dS): warp 1 issues S, warp 10 dQ and dP.  Each
-// product that overwrites a TMEM operand comes from the same thread as the
-// product reading it, after it in issue order.  Compute warp w owns query row
-// (w % 4) * 32 + lane and key columns [64h, 64h+64), h = (w - 2) / 4; the
-// row's log-sum-exp and dO.O sum are per-thread scalars.  P stays in
-// registers (bf16 pairs); dS goes over the first 32 of the warp's 64 dP
-// columns.
-// TMEM: S [0,128), dP [128,256), dQ [256, 256+D), Q [256+D, 256+1.5D),
-//       dO [256+1.5D, 256+2D); head dims up to 96 keep dS in its own
-//       region [256+2D, 256+2D+64), 112 and 128 over dP.
-// Issue order: warp 1 S(j+1) once S(j) is read.  Warp 10, with a separate
-// dS region: dP(j+1) once dP(j) is read, then dQ(j) once dS(j) is written
-// (so the compute warps never wait for dP); with dS over dP: dQ(j), then
-// dP(j+1), which overwrites dS(j) after dQ(j).
+// Shared memory of the dQ kernel: the K/V ring.
 template <int D>
 struct DqCfg {
   using T = TileGeom<D>;
   static constexpr int KVS_FIT = (232448 - 1280) / (2 * T::TILE);
   static constexpr int KVS = KVS_FIT > 5 ? 5 : KVS_FIT;
   static constexpr int SMEM = KVS * 2 * T::TILE + 1024 + 256;
-  static constexpr uint32_t COL_DQ = 256, COL_Q = 256 + D, COL_DO = 256 + D + D / 2, COL_DS = 256 + 2 * D;
-  static constexpr bool SEP_DS = COL_DS + 64 <= 512;
 };
 
-
+// ===========================================================================
+// dQ in 64-key sub-tiles with double-buffered S and dP
+// ===========================================================================
+// One CTA per 128-row query tile of one head, looping over the key/value
+// tiles j <= i in 64-key sub-tiles: sub-tile u is the half u % 2 of tile
+// u / 2, and its S and dP go to buffer b = u % 2 (64 columns each).  Q and dO
+// sit in TMEM as the A operands of S = Q K^T and dP = dO V^T; dS goes over
+// the first 32 columns of its dP buffer as the A operand of dQ += dS K.
+// Compute warps 2..5 (group 0) take the even sub-tiles and 6..9 (group 1) the
+// odd ones, each warp its lane quarter's 32 query rows by the 64 key
+// columns; warp 1 issues group 0's products and warp 10 group 1's, in the
+// order S(u), dP(u), S(u+2) (once the group has read S(u)), dQ(u) (after
+// dS(u)), dP(u+2) (which overwrites dS(u), after dQ(u) from the same
+// thread).  Both issuers add into dQ, which group 0 zeroes first; a K/V
+// stage is released once both issuers' products on it are done.  The row's
+// log-sum-exp and dO.O sum are per-thread scalars.
+// TMEM: S [0,64) [64,128), dP [128,192) [192,256), dQ [256, 256+D),
+//       Q [256+D, 256+1.5D), dO [256+1.5D, 256+2D).
 template <int D>
-__global__ void __launch_bounds__(352, 1) attn_dq_kernel(const __grid_constant__ AttnBwdParams p) {
+__global__ void __launch_bounds__(352, 1) attn_dq_hs_kernel(const __grid_constant__ AttnBwdParams p) {
   using T = TileGeom<D>;
   using C = DqCfg<D>;
   constexpr int KVS = C::KVS;
-  static_assert(C::COL_DO + D / 2 <= 512, "TMEM columns");
-  constexpr uint32_t ID_SQ = idesc_bf16(128, 128, false, false);
+  static_assert(256 + 2 * D <= 512, "TMEM columns");
+  constexpr uint32_t ID_S = idesc_bf16(128, 64, false, false);
   constexpr uint32_t ID_DQ = idesc_bf16(128, D, false, true);
+  constexpr uint32_t COL_DQ = 256, COL_Q = 256 + D, COL_DO = 256 + D + D / 2;
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sKV = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + KVS * 2 * T::TILE);
-  uint64_t* qo_ready = bars;           // Q, dO copied into TMEM (8 compute warps)
-  uint64_t* kv_full = bars + 1;
-  uint64_t* kv_empty = kv_full + KVS;
-  uint64_t* s_full = kv_empty + KVS;   // S(j) in TMEM
-  uint64_t* s_free = s_full + 1;       // S(j) read (8 compute warps)
-  uint64_t* dp_full = s_free + 1;      // dP(j) in TMEM
-  uint64_t* dp_free = dp_full + 1;     // dP(j) read (8 compute warps; separate dS only)
-  uint64_t* ds_full = dp_free + 1;     // dS(j) written (8 compute warps)
-  uint64_t* dq_done = ds_full + 1;     // dQ(j) done
-  uint64_t* drain = dq_done + 1;       // [2], one per issuer
+  uint64_t* qo_ready = bars;           // Q, dO in TMEM and dQ zeroed (8 compute warps)
+  uint64_t* kv_full = bars + 1;        // [KVS]
+  uint64_t* kv_empty = kv_full + KVS;  // [KVS], both issuers
+  uint64_t* s_full = kv_empty + KVS;   // [2] S(u) in buffer u % 2
+  uint64_t* s_free = s_full + 2;       // [2] S(u) read (4 warps of the group)
+  uint64_t* dp_full = s_free + 2;      // [2]
+  uint64_t* ds_full = dp_full + 2;     // [2] dS(u) written (4 warps)
+  uint64_t* all_done = ds_full + 2;    // both issuers' last products done
+  uint64_t* drain = all_done + 1;      // [2], one per issuer
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
@@ -812,21 +803,22 @@ __global__ void __launch_bounds__(352, 1) attn_dq_kernel(const __grid_constant__
   const int g = n / p.G;
   const int q0 = i * 128;
   const int nkv = p.causal ? min(i + 1, n_qt) : n_qt;
+  const int U = 2 * nkv;
 
   if (threadIdx.x == 0) {
     mbar_init(qo_ready, 8);
     for (int k = 0; k < KVS; ++k) {
       mbar_init(&kv_full[k], 1);
-      mbar_init(&kv_empty[k], 1);
+      mbar_init(&kv_empty[k], 2);
     }
-    mbar_init(s_full, 1);
-    mbar_init(s_free, 8);
-    mbar_init(dp_full, 1);
-    mbar_init(dp_free, 8);
-    mbar_init(ds_full, 8);
-    mbar_init(dq_done, 1);
-    mbar_init(&drain[0], 1);
-    mbar_init(&drain[1], 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_free[b], 4);
+      mbar_init(&dp_full[b], 1);
+      mbar_init(&ds_full[b], 4);
+      mbar_init(&drain[b], 1);
+    }
+    mbar_init(all_done, 2);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -839,13 +831,11 @@ __global__ void __launch_bounds__(352, 1) attn_dq_kernel(const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const uint32_t tS = tmem;
-  const uint32_t tdP = tmem + 128;
-  const uint32_t tdQ = tmem + C::COL_DQ;
-  const uint32_t tQA = tmem + C::COL_Q;
-  const uint32_t tOA = tmem + C::COL_DO;
-  // dS: its own region, or over the first 32 of each warp's 64 dP columns
-  const uint32_t tDS = C::SEP_DS ? tmem + C::COL_DS : tdP;
+  const uint32_t tS = tmem;         // + 64 b
+  const uint32_t tdP = tmem + 128;  // + 64 b
+  const uint32_t tdQ = tmem + COL_DQ;
+  const uint32_t tQA = tmem + COL_Q;
+  const uint32_t tOA = tmem + COL_DO;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -853,7 +843,7 @@ __global__ void __launch_bounds__(352, 1) attn_dq_kernel(const __grid_constant__
       int issued = 0;
       for (int jt = 0; jt < nkv; ++jt) {
         const int st = jt % KVS;
-        if (jt >= KVS && !bounded_wait(&kv_empty[st], ((jt / KVS) & 1) ^ 1, abort_flag, 601, p.err)) break;
+        if (jt >= KVS && !bounded_wait(&kv_empty[st], ((jt / KVS) & 1) ^ 1, abort_flag, 661, p.err)) break;
         uint8_t* sK = sKV + st * 2 * T::TILE;
         uint8_t* sV = sK + T::TILE;
         mbar_expect_tx(&kv_full[st], 2 * T::TILE);
@@ -866,89 +856,81 @@ __global__ void __launch_bounds__(352, 1) attn_dq_kernel(const __grid_constant__
       }
       if (*abort_flag) {
         for (int jt = (issued > KVS ? issued - KVS : 0); jt < issued; ++jt)
-          bounded_wait(&kv_full[jt % KVS], (jt / KVS) & 1, abort_flag, 602, p.err);
+          bounded_wait(&kv_full[jt % KVS], (jt / KVS) & 1, abort_flag, 662, p.err);
       }
     }
   } else if (warp == 1 || warp == 10) {
     if (lane == 0) {
       // ------------------------------------------------ MMA issuers
+      const int b = warp == 1 ? 0 : 1;  // this issuer's buffer and sub-tiles
+      const uint32_t tSb = tS + 64 * b, tdPb = tdP + 64 * b;
       const uint32_t uKV = smem_u32(sKV);
-      const bool is_s = warp == 1;
-      bool ok = bounded_wait(qo_ready, 0, abort_flag, 611, p.err) &&
-                bounded_wait(&kv_full[0], 0, abort_flag, 612, p.err);
-      auto issue_s = [&](int jt) {
-        const uint32_t uK = uKV + (jt % KVS) * 2 * T::TILE;
+      // the 64 key rows of half b start 64 b rows into every chunk of the
+      // stage's K and V tiles (whole swizzle atoms)
+      auto uK = [&](int u) { return uKV + ((u >> 1) % KVS) * 2 * T::TILE; };
+      auto issue_s = [&](int u) {
+        const uint32_t k = uK(u) + 64 * T::SWB * b;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a(tS, tQA + kk * 8, T::kmajor(uK, kk), ID_SQ, kk > 0);
-        umma_commit(s_full);
+        for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a(tSb, tQA + kk * 8, T::kmajor(k, kk), ID_S, kk > 0);
+        umma_commit(&s_full[b]);
       };
-      auto issue_dp = [&](int jt) {
-        const uint32_t uV = uKV + (jt % KVS) * 2 * T::TILE + T::TILE;
+      auto issue_dp = [&](int u) {
+        const uint32_t v = uK(u) + T::TILE + 64 * T::SWB * b;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a(tdP, tOA + kk * 8, T::kmajor(uV, kk), ID_SQ, kk > 0);
-        umma_commit(dp_full);
+        for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a(tdPb, tOA + kk * 8, T::kmajor(v, kk), ID_S, kk > 0);
+        umma_commit(&dp_full[b]);
       };
+      auto wait_stage = [&](int u) {
+        const int jt = u >> 1;
+        return bounded_wait(&kv_full[jt % KVS], (jt / KVS) & 1, abort_flag, 671, p.err);
+      };
+      bool ok = bounded_wait(qo_ready, 0, abort_flag, 672, p.err) && wait_stage(b);
       if (ok) {
         tc_fence_after();
-        if (is_s) issue_s(0); else issue_dp(0);
+        issue_s(b);
+        issue_dp(b);
       }
-      for (int jt = 0; ok && jt < nkv; ++jt) {
-        const bool more = jt + 1 < nkv;
-        if (is_s) {
-          // S(j+1) once the compute warps have read S(j)
-          if (!more) break;
-          if (!bounded_wait(s_free, jt & 1, abort_flag, 613, p.err)) { ok = false; break; }
-          if (!bounded_wait(&kv_full[(jt + 1) % KVS], ((jt + 1) / KVS) & 1, abort_flag, 614, p.err)) { ok = false; break; }
+      for (int u = b; ok && u < U; u += 2) {
+        const int st = (u >> 1) % KVS;
+        const bool more = u + 2 < U;
+        if (more) {
+          // S(u+2) once the group has read S(u)
+          if (!bounded_wait(&s_free[b], (u >> 1) & 1, abort_flag, 673, p.err) || !wait_stage(u + 2)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          issue_s(jt + 1);
-        } else {
-          if (C::SEP_DS && more) {
-            // dP(j+1) once the compute warps have read dP(j)
-            if (!bounded_wait(dp_free, jt & 1, abort_flag, 617, p.err)) { ok = false; break; }
-            if (!bounded_wait(&kv_full[(jt + 1) % KVS], ((jt + 1) / KVS) & 1, abort_flag, 616, p.err)) { ok = false; break; }
-            tc_fence_after();
-            issue_dp(jt + 1);
-          }
-          // dQ += dS(j) K_j: the dS pairs of key columns 64h.. sit at column
-          // 32h of the dS region, or at column 128 + 64h over dP
-          if (!bounded_wait(ds_full, jt & 1, abort_flag, 615, p.err)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t uK = uKV + (jt % KVS) * 2 * T::TILE;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t a = C::SEP_DS ? tDS + kk * 8 : tdP + (kk >> 2) * 64 + (kk & 3) * 8;
-            umma_bf16_tmem_a(tdQ, a, T::mnmajor(uK, kk), ID_DQ, (jt > 0 || kk > 0));
-          }
-          // the last readers of stage j: S(j) (complete: the compute warps
-          // read it before forming dS(j)), dP(j) and dQ(j) (this thread)
-          umma_commit(&kv_empty[jt % KVS]);
-          umma_commit(dq_done);
-          if (!C::SEP_DS && more) {
-            if (!bounded_wait(&kv_full[(jt + 1) % KVS], ((jt + 1) / KVS) & 1, abort_flag, 616, p.err)) { ok = false; break; }
-            tc_fence_after();
-            issue_dp(jt + 1);
-          }
+          issue_s(u + 2);
         }
+        // dQ += dS(u) K_u: key rows 64b.. are K blocks 4b..4b+3 of the tile
+        if (!bounded_wait(&ds_full[b], (u >> 1) & 1, abort_flag, 674, p.err)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16_tmem_a(tdQ, tdPb + kk * 8, T::mnmajor(uK(u), 4 * b + kk), ID_DQ, 1);
+        umma_commit(&kv_empty[st]);
+        // dP(u+2) overwrites dS(u), after dQ(u) in issue order
+        if (more) issue_dp(u + 2);
       }
+      if (ok) umma_commit(all_done);
       if (!ok) {
-        umma_commit(&drain[is_s ? 0 : 1]);
-        bounded_wait(&drain[is_s ? 0 : 1], 0, abort_flag, 619, p.err);
+        umma_commit(&drain[b]);
+        bounded_wait(&drain[b], 0, abort_flag, 675, p.err);
       }
     }
   } else {
     // ------------------------------------------------ compute (warps 2..9;
     // lanes 1..31 of the issuer warps fall through to the final barrier)
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int b = (warp - 2) >> 2;  // group = buffer = sub-tile parity
     const int r = quarter * 32 + lane;
     const int qpos = q0 + r;
-    const int c0 = half * 64;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     {
-      // Q (half 0) or dO (half 1) row of this thread into TMEM as bf16
-      // pairs; rows past the sequence are zero
+      // Q (group 0) or dO (group 1) row of this thread into TMEM as bf16
+      // pairs (rows past the sequence are zero); group 0 also zeroes dQ
       uint32_t w[D / 2];
-      const __nv_bfloat16* src = half == 0
+      const __nv_bfloat16* src = b == 0
           ? p.qkv + ((long long)bi * p.s + qpos) * p.ld_qkv + p.q_col + (long long)n * D
           : p.dout + ((long long)bi * p.s + qpos) * p.ld_do + p.do_col + (long long)n * D;
 #pragma unroll
@@ -960,7 +942,14 @@ __global__ void __launch_bounds__(352, 1) attn_dq_kernel(const __grid_constant__
         w[4 * cc + 2] = v.z;
         w[4 * cc + 3] = v.w;
       }
-      tmem_store_row<D / 2>((half == 0 ? tQA : tOA) + lane_off, w);
+      tmem_store_row<D / 2>((b == 0 ? tQA : tOA) + lane_off, w);
+      if (b == 0) {
+        uint32_t z[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) z[k] = 0u;
+#pragma unroll
+        for (int cc = 0; cc < D / 16; ++cc) tmem_st16_nw(tdQ + lane_off + cc * 16, z);
+      }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -970,24 +959,25 @@ __global__ void __launch_bounds__(352, 1) attn_dq_kernel(const __grid_constant__
     // this row's -LSE*log2(e) and dO.O sum (finite filler past the sequence)
     const float nl = p.nl2[((long long)bi * p.H + n) * p.s_pad + qpos];
     const float dsum = p.Dsum[((long long)bi * p.H + n) * p.s_pad + qpos];
+    const uint32_t tSb = tS + 64 * b, tdPb = tdP + 64 * b;
     bool ok = true;
-    for (int jt = 0; jt < nkv; ++jt) {
-      ok = bounded_wait(s_full, jt & 1, abort_flag, 621, p.err);
+    for (int u = b; u < U; u += 2) {
+      ok = bounded_wait(&s_full[b], (u >> 1) & 1, abort_flag, 681, p.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       // ---- phase 1: P = exp2(S * scale*log2(e) - LSE*log2(e)); key columns
-      // [0, hi) of this warp's 64 are unmasked
-      const int kv0 = jt * 128 + c0;
+      // [0, hi) of the 64 are unmasked
+      const int kv0 = (u >> 1) * 128 + 64 * b;
       int hi = min(64, p.s - kv0);
       if (p.causal) hi = min(hi, qpos - kv0 + 1);
       if (qpos >= p.s) hi = 0;
       uint32_t sv[64];
-      tmem_ld32_nw(tS + lane_off + c0, sv);
-      tmem_ld32_nw(tS + lane_off + c0 + 32, sv + 32);
+      tmem_ld32_nw(tSb + lane_off, sv);
+      tmem_ld32_nw(tSb + lane_off + 32, sv + 32);
       tmem_wait_ld(sv);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(s_free);
+      if (lane == 0) mbar_arrive(&s_free[b]);
       // P stays in fp32 registers: no product here reads it, only dS
       float pe[64];
       if (hi >= 64) {
@@ -997,49 +987,32 @@ __global__ void __launch_bounds__(352, 1) attn_dq_kernel(const __grid_constant__
 #pragma unroll
         for (int k = 0; k < 64; ++k) pe[k] = k < hi ? ex2(fmaf(__uint_as_float(sv[k]), c, nl)) : 0.f;
       }
-      // ---- phase 2: dS = P (dP - D) over this warp's dP columns
-      ok = bounded_wait(dp_full, jt & 1, abort_flag, 622, p.err);
+      // ---- phase 2: dS = P (dP - D), over the first 32 columns of buffer b
+      ok = bounded_wait(&dp_full[b], (u >> 1) & 1, abort_flag, 682, p.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       uint32_t dr[64];
-      tmem_ld32_nw(tdP + lane_off + c0, dr);
-      tmem_ld32_nw(tdP + lane_off + c0 + 32, dr + 32);
+      tmem_ld32_nw(tdPb + lane_off, dr);
+      tmem_ld32_nw(tdPb + lane_off + 32, dr + 32);
       tmem_wait_ld(dr);
-      if constexpr (C::SEP_DS) {
-        // dP(j+1) may now overwrite dP(j)
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(dp_free);
-      }
       uint32_t o[32];
 #pragma unroll
       for (int k = 0; k < 64; k += 2)
         o[k / 2] = pack_bf16(pe[k] * (__uint_as_float(dr[k]) - dsum), pe[k + 1] * (__uint_as_float(dr[k + 1]) - dsum));
-      if constexpr (C::SEP_DS) {
-        // dQ(j-1) has read the previous dS; waiting every step keeps these
-        // warps within one phase of dq_done
-        if (jt >= 1) {
-          ok = bounded_wait(dq_done, (jt - 1) & 1, abort_flag, 623, p.err);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-          tc_fence_after();
-        }
-        tmem_st32(tDS + lane_off + half * 32, o);
-      } else {
-        tmem_st32(tdP + lane_off + c0, o);
-      }
+      tmem_st32(tdPb + lane_off, o);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(ds_full);
+      if (lane == 0) mbar_arrive(&ds_full[b]);
     }
-    // epilogue: the two halves split dQ's 16-column chunks.  dq_done is at
-    // most one phase ahead of dQ(nkv-2), which completed before dP(nkv-1).
-    if (ok) ok = __all_sync(0xffffffffu, bounded_wait(dq_done, (nkv - 1) & 1, abort_flag, 624, p.err));
+    // epilogue: the two groups split dQ's 16-column chunks once both
+    // issuers' products are done
+    if (ok) ok = __all_sync(0xffffffffu, bounded_wait(all_done, 0, abort_flag, 683, p.err));
     if (ok) {
       tc_fence_after();
       constexpr int NC = D / 16;
       constexpr int NC0 = (NC + 1) / 2;
-      const int cbeg = half == 0 ? 0 : NC0, cend = half == 0 ? NC0 : NC;
+      const int cbeg = b == 0 ? 0 : NC0, cend = b == 0 ? NC0 : NC;
       const bool valid = qpos < p.s;
       __nv_bfloat16* qrow = p.dqkv + ((long long)bi * p.s + qpos) * p.ld_dqkv + p.dq_col + (long long)n * D;
       const uint32_t tq = tdQ + lane_off;
@@ -1095,11 +1068,11 @@ int launch_dq(AttnBwdParams& prm, int grid, cudaStream_t st) {
   static_assert(SMEM <= 232448, "dQ tile set exceeds shared memory");
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(attn_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
+    if (cudaFuncSetAttribute(attn_dq_hs_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
       return 3;
     attr = true;
   }
-  attn_dq_kernel<D><<<grid, 352, SMEM, st>>>(prm);
+  attn_dq_hs_kernel<D><<<grid, 352, SMEM, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 

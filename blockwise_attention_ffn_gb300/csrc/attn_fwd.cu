@@ -370,6 +370,350 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
   }
 }
 
+// ---------------------------------------------------------------------------
+// Split keys (head dims 64 and 80): two independent online softmaxes per CTA.
+// The 128 keys of every K/V tile are split in two halves; softmax group b
+// (warps 2..5 for b = 0, 6..9 for b = 1) runs the whole online-softmax loop
+// over the keys 64b..64b+63 of every tile, with its own running max, its own
+// O accumulator (its row sums in O's extra columns) and its own MMA-issuing
+// warp (1 or 10).  The two partial results of a row are merged once, at the
+// end, by the log-sum-exp rule: m = max(m0, m1), O = sum_b O_b 2^((m_b - m)c)
+// / sum_b l_b 2^((m_b - m)c).  Each SM sub-partition then runs two
+// independent softmax warps over 64 columns instead of one over 128, with no
+// exchange between them before the merge.
+// TMEM: S of group b in [128b, 128b+128) as two 64-column buffers; O_b at
+// 256 + b (D + 16); Q at 256 + 2 (D + 16).
+template <int D>
+struct FwdSkCfg {
+  using T = TileGeom<D>;
+  static constexpr int EXT = FwdCfg<D>::EXT;
+  static constexpr int STAGE = FwdCfg<D>::STAGE;
+  static constexpr int RED = 2 * 128 * 4;  // [group][row] running max, for the merge
+  static constexpr int KVS_FIT = (232448 - RED - 1280) / STAGE;
+  static constexpr int KVS = KVS_FIT > 5 ? 5 : KVS_FIT;
+  static constexpr int SMEM = KVS * STAGE + RED + 1024 + 256;
+  static constexpr uint32_t COL_O = 256, OW = D + EXT, COL_Q = 256 + 2 * OW;
+};
+
+template <int D>
+__global__ void __launch_bounds__(352, 1) attn_fwd_sk_kernel(const __grid_constant__ AttnFwdParams p) {
+  using T = TileGeom<D>;
+  using C = FwdSkCfg<D>;
+  constexpr int KVS = C::KVS;
+  constexpr int EXT = C::EXT;
+  constexpr int STAGE = C::STAGE;
+  static_assert(EXT == 16, "the split-key kernel keeps its row sums in O's extra columns");
+  static_assert(C::COL_Q + D / 2 <= 512, "TMEM columns");
+  constexpr uint32_t IDESC_S = idesc_bf16(128, 64, false, false);
+  constexpr uint32_t IDESC_PV = idesc_bf16(128, D + EXT, false, true);
+  constexpr float NEG_INF = -INFINITY;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sKV = smem;
+  float* red = reinterpret_cast<float*>(sKV + KVS * STAGE);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(red) + C::RED);
+  uint64_t* q_ready = bars;             // Q copied into TMEM (group 0's 4 warps)
+  uint64_t* kv_full = bars + 1;         // [KVS]
+  uint64_t* kv_empty = kv_full + KVS;   // [KVS], both issuers
+  uint64_t* s_full = kv_empty + KVS;    // [group][buffer]
+  uint64_t* p_full = s_full + 4;        // [group][buffer], 4 warps
+  uint64_t* pv_done = p_full + 4;       // [group]
+  uint64_t* drain = pv_done + 2;        // [group]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+
+  // tile scheduling: head-major, heaviest query tiles of a head first
+  const int pair = blockIdx.x / p.n_qt;
+  const int qt_rev = blockIdx.x % p.n_qt;
+  const int n = pair % p.H;
+  const int bi = pair / p.H;
+  const int qt = p.qt_begin + p.n_qt - 1 - qt_rev;
+  const int q0 = qt * 128;
+  const int g = n / p.G;
+  const int kv_tiles_total = (p.s + 127) / 128;
+  const int nkv = p.causal ? min(qt + 1, kv_tiles_total) : kv_tiles_total;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_ready, 4);
+    for (int i = 0; i < KVS; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 2);
+    }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 4);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&pv_done[b], 1);
+      mbar_init(&drain[b], 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) tma_prefetch(&p.map_qkv);
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  {
+    // the row-sum chunk of every stage (never written by TMA)
+    constexpr int UNITS = C::T::CHUNK / 16;
+    for (int i = threadIdx.x; i < KVS * UNITS; i += blockDim.x)
+      reinterpret_cast<uint4*>(sKV + (i / UNITS) * STAGE + 2 * T::TILE)[i % UNITS] = make_uint4(0x3F80u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t tQA = tmem + C::COL_Q;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      int issued = 0;
+      for (int j = 0; j < nkv; ++j) {
+        const int st = j % KVS;
+        if (j >= KVS && !bounded_wait(&kv_empty[st], ((j / KVS) & 1) ^ 1, abort_flag, 231, p.err)) break;
+        uint8_t* sK = sKV + st * STAGE;
+        uint8_t* sV = sK + T::TILE;
+        mbar_expect_tx(&kv_full[st], 2 * T::TILE);
+#pragma unroll
+        for (int c = 0; c < T::NCH; ++c)
+          tma_load_3d(sK + c * T::CHUNK, &p.map_qkv, &kv_full[st], p.k_col + g * D + c * T::CW, j * 128, bi);
+#pragma unroll
+        for (int c = 0; c < T::NCH; ++c)
+          tma_load_3d(sV + c * T::CHUNK, &p.map_qkv, &kv_full[st], p.v_col + g * D + c * T::CW, j * 128, bi);
+        issued = j + 1;
+      }
+      if (*abort_flag) {
+        for (int j = (issued > KVS ? issued - KVS : 0); j < issued; ++j)
+          bounded_wait(&kv_full[j % KVS], (j / KVS) & 1, abort_flag, 232, p.err);
+      }
+    }
+  } else if (warp == 1 || warp == 10) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuers
+      // group b's products: S_b(j+1) = Q K_j[64b..]^T into its buffer
+      // (j+1) % 2, then O_b += P_b(j) V_j[64b..] (+ the row-sum chunk).
+      // S_b(j+1) overwrites P_b(j-1) after PV_b(j-1) from the same thread.
+      const int b = warp == 1 ? 0 : 1;
+      const uint32_t uKV = smem_u32(sKV);
+      const uint32_t tSb = tmem + 128 * b;
+      const uint32_t tOb = tmem + C::COL_O + b * C::OW;
+      auto issue_s = [&](int j) -> bool {
+        if (!bounded_wait(&kv_full[j % KVS], (j / KVS) & 1, abort_flag, 233, p.err)) return false;
+        tc_fence_after();
+        const uint32_t kt = uKV + (j % KVS) * STAGE + 64 * T::SWB * b;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_bf16_tmem_a(tSb + (j & 1) * 64, tQA + kk * 8, T::kmajor(kt, kk), IDESC_S, kk > 0);
+        umma_commit(&s_full[2 * b + (j & 1)]);
+        return true;
+      };
+      bool ok = bounded_wait(q_ready, 0, abort_flag, 234, p.err) && issue_s(0);
+      for (int j = 0; ok && j < nkv; ++j) {
+        if (j + 1 < nkv && !issue_s(j + 1)) { ok = false; break; }
+        if (!bounded_wait(&p_full[2 * b + (j & 1)], (j >> 1) & 1, abort_flag, 235, p.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t vt = uKV + (j % KVS) * STAGE + T::TILE;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16_tmem_a(tOb, tSb + (j & 1) * 64 + kk * 8, T::mnmajor(vt, 4 * b + kk), IDESC_PV, (j > 0 || kk > 0));
+        umma_commit(&kv_empty[j % KVS]);
+        umma_commit(&pv_done[b]);
+      }
+      if (!ok) {
+        umma_commit(&drain[b]);
+        bounded_wait(&drain[b], 0, abort_flag, 236, p.err);
+      }
+    }
+  } else {
+    // ------------------------------------------------ softmax (warps 2..9)
+    const int quarter = warp & 3;
+    const int b = (warp - 2) >> 2;
+    const int r = quarter * 32 + lane;
+    const int qpos = q0 + r;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t tSb = tmem + 128 * b;
+    const uint32_t tOb = tmem + C::COL_O + b * C::OW;
+    if (b == 0) {
+      // this thread's Q row into TMEM as bf16 pairs (zero past the sequence)
+      uint32_t w[D / 2];
+      const __nv_bfloat16* src =
+          p.qkv + ((long long)bi * p.s + qpos) * p.ld_qkv + p.q_col + (long long)n * D;
+#pragma unroll
+      for (int cc = 0; cc < D / 8; ++cc) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (qpos < p.s) v = *reinterpret_cast<const uint4*>(src + cc * 8);
+        w[4 * cc] = v.x;
+        w[4 * cc + 1] = v.y;
+        w[4 * cc + 2] = v.z;
+        w[4 * cc + 3] = v.w;
+      }
+      tmem_store_row<D / 2>(tQA + lane_off, w);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_ready);
+    }
+    const float c = p.scale_log2;
+    float m_run = NEG_INF;
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      const int sb = j & 1;
+      const uint32_t tb = tSb + sb * 64 + lane_off;
+      ok = bounded_wait(&s_full[2 * b + sb], (j >> 1) & 1, abort_flag, 241, p.err);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sv[64];
+      tmem_ld32_nw(tb, sv);
+      tmem_ld32_nw(tb + 32, sv + 32);
+      tmem_wait_ld(sv);
+      // this group's key columns [0, hi) of the 64 are unmasked
+      const int kv0 = j * 128 + 64 * b;
+      int hi = min(64, p.s - kv0);
+      if (p.causal) hi = min(hi, qpos - kv0 + 1);
+      const bool edge = hi < 64;
+      float mx = NEG_INF;
+      if (!edge) {
+        float m2[2] = {NEG_INF, NEG_INF};
+#pragma unroll
+        for (int i = 0; i < 64; i += 2)
+          m2[(i >> 1) & 1] = max3f(m2[(i >> 1) & 1], __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
+        mx = fmaxf(m2[0], m2[1]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          if (i < hi) mx = fmaxf(mx, __uint_as_float(sv[i]));
+      }
+      const float m_new = fmaxf(m_run, mx);
+      const bool need = (m_new - m_run) * c > 8.f;
+      const bool rescale = __any_sync(0xffffffffu, need);
+      float alpha = 1.f;
+      if (rescale) {
+        alpha = (m_run == NEG_INF) ? 0.f : ex2((m_run - m_new) * c);
+        m_run = m_new;
+      }
+      // a row with no unmasked key yet keeps m = -inf; its exponent offset
+      // is then 0 and every P entry below is masked to zero
+      const float mc = (m_run == NEG_INF) ? 0.f : m_run * c;
+      uint32_t pk[32];
+      if (!edge) {
+#pragma unroll
+        for (int i = 0; i < 64; i += 2)
+          pk[i / 2] = pack_bf16(ex2(fmaf(__uint_as_float(sv[i]), c, -mc)), ex2(fmaf(__uint_as_float(sv[i + 1]), c, -mc)));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) {
+          const float e0 = i < hi ? ex2(fmaf(__uint_as_float(sv[i]), c, -mc)) : 0.f;
+          const float e1 = i + 1 < hi ? ex2(fmaf(__uint_as_float(sv[i + 1]), c, -mc)) : 0.f;
+          pk[i / 2] = pack_bf16(e0, e1);
+        }
+      }
+      // P over the first 32 columns of its own S buffer (all read above)
+      tmem_st32(tb, pk);
+      // PV(j-1) must be done before O is rescaled; waiting for it every step
+      // keeps these warps within one phase of pv_done
+      if (j > 0) {
+        ok = bounded_wait(&pv_done[b], (j - 1) & 1, abort_flag, 242, p.err);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        if (rescale) {
+          // the row and its row-sum columns
+          uint32_t ro[D + EXT];
+#pragma unroll
+          for (int cc = 0; cc < (D + EXT) / 16; ++cc) tmem_ld16_nw(tOb + lane_off + cc * 16, ro + cc * 16);
+          tmem_wait_ld(ro);
+#pragma unroll
+          for (int i = 0; i < D + EXT; ++i) ro[i] = __float_as_uint(__uint_as_float(ro[i]) * alpha);
+#pragma unroll
+          for (int cc = 0; cc < (D + EXT) / 16; ++cc) tmem_st16_nw(tOb + lane_off + cc * 16, ro + cc * 16);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[2 * b + sb]);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, bounded_wait(&pv_done[b], (nkv - 1) & 1, abort_flag, 243, p.err));
+    // merge: both groups always reach this barrier (id 1 + quarter, the two
+    // warps of this lane quarter), which also ANDs their status
+    red[b * 128 + r] = m_run;
+    bool merge = named_bar_and(1 + quarter, 64, ok);
+    // the other group's last PV has completed too (it waited for it before
+    // the barrier; its barrier has no later phase, so this returns at once)
+    if (merge)
+      merge = __all_sync(0xffffffffu, bounded_wait(&pv_done[b ^ 1], (nkv - 1) & 1, abort_flag, 244, p.err));
+    if (merge) {
+      tc_fence_after();
+      const float m_o = red[(b ^ 1) * 128 + r];
+      const float m_self = m_run;
+      const float m = fmaxf(m_self, m_o);
+      const float a_self = (m_self == NEG_INF) ? 0.f : ex2((m_self - m) * c);
+      const float a_o = (m_o == NEG_INF) ? 0.f : ex2((m_o - m) * c);
+      const uint32_t tOo = tmem + C::COL_O + (b ^ 1) * C::OW;
+      // row sums from the extra columns of both O's
+      uint32_t ls[16], lo[16];
+      tmem_ld16_nw(tOb + lane_off + D, ls);
+      tmem_ld16_nw(tOo + lane_off + D, lo);
+      tmem_wait_ld(ls);
+      tmem_wait_ld(lo);
+      const float l = __uint_as_float(ls[0]) * a_self + __uint_as_float(lo[0]) * a_o;
+      const float inv_l = 1.f / l;
+      const float w_self = a_self * inv_l, w_o = a_o * inv_l;
+      // each group writes half of the row's 16-column chunks
+      constexpr int NC = D / 16;
+      constexpr int NC0 = (NC + 1) / 2;
+      const int cbeg = b == 0 ? 0 : NC0, cend = b == 0 ? NC0 : NC;
+      const bool valid = qpos < p.s;
+      __nv_bfloat16* orow = p.o + ((long long)bi * p.s + qpos - p.o_row0) * p.ld_o + p.o_col + (long long)n * D;
+      for (int cc = cbeg; cc < cend; ++cc) {
+        uint32_t vs[16], vo[16];
+        tmem_ld16_nw(tOb + lane_off + cc * 16, vs);
+        tmem_ld16_nw(tOo + lane_off + cc * 16, vo);
+        tmem_wait_ld(vs);
+        tmem_wait_ld(vo);
+        uint32_t vm[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          vm[k] = __float_as_uint(__uint_as_float(vs[k]) * w_self + __uint_as_float(vo[k]) * w_o);
+        if (valid) store_row16(orow + cc * 16, vm, 1.f);
+      }
+      // every row of the padded tile gets a finite value (rows past s see the
+      // zero-filled query), so the backward pass never reads garbage
+      if (b == 0 && p.lse)
+        p.lse[((long long)bi * p.H_total + p.lse_head0 + n) * p.s_pad + qpos] = m * p.scale + logf(l);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+int launch_fwd_sk(AttnFwdParams& prm, int grid, cudaStream_t st) {
+  constexpr int SMEM = FwdSkCfg<D>::SMEM;
+  static_assert(SMEM <= 232448, "attention forward tile set exceeds shared memory");
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(attn_fwd_sk_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
+      return 3;
+    attr = true;
+  }
+  attn_fwd_sk_kernel<D><<<grid, 352, SMEM, st>>>(prm);
+  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
 template <int D>
 int launch_fwd(AttnFwdParams& prm, int grid, cudaStream_t st) {
   constexpr int SMEM = FwdCfg<D>::SMEM;
@@ -423,8 +767,8 @@ int attention_fwd(const AttnShape& sh, const void* qkv, void* o, float* lse, cud
   const double pairs = sh.causal ? (q1 * (q1 + 1) - q0 * (q0 + 1)) / 2 : (q1 - q0) * sh.s;
   ProfScope prof(PROF_ATTN_FWD, 4.0 * sh.d * pairs * sh.H * sh.b, 0.0, st);
   switch (sh.d) {
-    case 64: return launch_fwd<64>(prm, grid, st);
-    case 80: return launch_fwd<80>(prm, grid, st);
+    case 64: return launch_fwd_sk<64>(prm, grid, st);
+    case 80: return launch_fwd_sk<80>(prm, grid, st);
     case 96: return launch_fwd<96>(prm, grid, st);
     case 112: return launch_fwd<112>(prm, grid, st);
     case 128: return launch_fwd<128>(prm, grid, st);

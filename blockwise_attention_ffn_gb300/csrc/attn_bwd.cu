@@ -14,11 +14,14 @@
 //  * dK/dV: one CTA per 128-row key/value tile j of one key/value head; it
 //    loops over the G query heads of the group and their query tiles i >= j
 //    (causal), accumulating dK and dV in TMEM.  Head dims 64 and 80 keep
-//    every A operand in TMEM and split the compute warps into a P group and
-//    a dS group; 96 to 128, whose accumulators leave too little TMEM for
-//    that, use one group that forms P and dS in turn.
+//    every A operand in TMEM and work in 64-query sub-tiles with
+//    double-buffered S^T and dP^T, taken alternately by two groups of
+//    compute warps with their own MMA-issuing warps; 96 to 128, whose
+//    accumulators leave too little TMEM for that, keep K, V, P^T and dS^T
+//    in shared memory and one group that forms P and dS in turn.
 //  * dQ: one CTA per 128-row query tile i of one query head; it loops over
-//    the key/value tiles j <= i, accumulating dQ in TMEM, and writes it once.
+//    the key/value tiles j <= i in 64-key sub-tiles the same way,
+//    accumulating dQ in TMEM, and writes it once.
 // Both rebuild S and dP (the dQ kernel for its own tile order), so a pair of
 // tiles costs 7 tensor-core products instead of 5; in exchange no partial dQ
 // tile is ever reduced through L2 (in a one-kernel design that traffic is

@@ -9,16 +9,22 @@
 // O = O*corr + exp(S - m') V_j; finally O / l.  The log-sum-exp m + ln l of
 // every row is written for the recompute backward.
 //
-// One CTA = one 128-row query tile of one head (GQA: key/value head n / G).
-//   warp 0      TMA: K/V tiles through a KVS-deep ring
-//   warp 1      TMEM owner and MMA issuer: S_{j+1} = Q K_{j+1}^T into one of
-//               two TMEM S buffers, then O += P_j V_j
-//   warps 2..5  softmax, one query row per thread: copy the Q row into TMEM
-//               once; per tile read the S row, mask, update m and l, write P
-//               (bf16 pairs) over the S buffer, rescale the O row in TMEM
-//               when the max moved by more than 2^8 (otherwise keep the
-//               stale max: exact, since O and l are scaled alike), and at
-//               the end normalise and store O.
+// One CTA = one 128-row query tile of one head (GQA: key/value head n / G);
+// warp 0 streams K/V tiles through a ring.  Two kernels:
+//  * head dims 64 and 80 (attn_fwd_sk_kernel): the keys of every tile are
+//    split in halves, and two groups of four softmax warps (2..5, 6..9),
+//    each with its own MMA-issuing warp (1, 10), run independent online
+//    softmaxes over their halves -- own running max, own O accumulator --
+//    merged once at the end by the log-sum-exp rule;
+//  * head dims 96 to 128 (attn_fwd_kernel), whose two O accumulators would
+//    not fit in TMEM: warp 1 issues S_{j+1} = Q K_{j+1}^T into one of two
+//    TMEM S buffers, then O += P_j V_j, and warps 2..5 do the softmax.
+// Softmax, one query row per thread: copy the Q row into TMEM once; per tile
+// read the S row, mask, update m, write P (bf16 pairs) over the S buffer,
+// rescale the O row in TMEM when the max moved by more than 2^8 (otherwise
+// keep the stale max: exact, since O and l are scaled alike); at the end
+// normalise and store O.  Up to d = 112 the row sums l come from the tensor
+// core (an extra chunk of V), else from fp32 adds.
 // The s x s score matrix never leaves TMEM/registers.
 #include <math.h>
 #include <string.h>

@@ -12,6 +12,10 @@
 //               global, overlapped with the next tile's main loop
 // Operands are staged with 128-byte swizzle; K-major tiles are [rows x 64]
 // boxes, MN-major tiles are [64 K-rows x 64] boxes side by side.
+// Work units are tiles, or tiles x K ranges for fp32 weight gradients whose
+// whole tiles would leave most of the last wave of SMs idle (each range adds
+// its share in L2).  The epilogue moves whole 32-byte sectors per thread
+// where every operand allows it.
 #include <math.h>
 #include <string.h>
 

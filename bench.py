@@ -283,10 +283,10 @@ def run_gpu(args, c):
     grads = bpt.alloc_grads(W, dev) if c.backward else None
     stream = torch.cuda.current_stream(dev)
 
-    def step():
-        bpt.bpt_layer_fwd(c, W, x, y, saved, ws, stream)
-        if c.backward:
-            bpt.bpt_layer_bwd(c, W, x, saved, dy, dx, grads, ws, stream)
+    def step(cfg=c):
+        bpt.bpt_layer_fwd(cfg, W, x, y, saved, ws, stream)
+        if cfg.backward:
+            bpt.bpt_layer_bwd(cfg, W, x, saved, dy, dx, grads, ws, stream)
 
     torch.cuda.reset_peak_memory_stats(dev)
     for _ in range(args.warmup):
@@ -322,11 +322,14 @@ def run_gpu(args, c):
     value = job_throughput(fl["executed"], world, ms)
     peaks = load_peaks()
 
-    # per-kernel breakdown of the same step (separate profiled steps)
+    # per-kernel breakdown of the same step (separate profiled steps).  These
+    # run every kernel on one stream, so that no event span also covers
+    # weight-gradient work overlapping on the backward's second stream.
+    one = c.with_(flags=c.flags | bpt.BPT_FLAG_ONE_STREAM)
     bpt.bpt_profile_enable(True)
     nprof = max(1, min(args.steps, 3))
     for _ in range(nprof):
-        step()
+        step(one)
     torch.cuda.synchronize()
     prof = bpt.bpt_profile_collect()
     bpt.bpt_profile_enable(False)

@@ -24,6 +24,7 @@ LIB_PATH = os.path.join(_HERE, "libbpt.so")
 BPT_OK, BPT_EINVAL, BPT_ENOSPC, BPT_ECUDA, BPT_ETIMEOUT, BPT_EUNSUPPORTED = range(6)
 BPT_PASS_FWD, BPT_PASS_BWD, BPT_PASS_HEADCHUNK = 0, 1, 2
 BPT_FLAG_ACCUM_GRADS = 1
+BPT_FLAG_ONE_STREAM = 2
 
 WEIGHT_FIELDS = ("ln1_w", "ln1_b", "wq", "bq", "wk", "bk", "wv", "bv", "wo", "bo",
                  "ln2_w", "ln2_b", "w1", "b1", "w2", "b2", "w3")

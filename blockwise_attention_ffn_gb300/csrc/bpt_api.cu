@@ -52,7 +52,7 @@ int validate(const bpt_config* c, Dims* D) {
   if (c->ffn_block < 0 || (c->ffn_block % c->q_block)) return BPT_EINVAL;
   if (!(c->norm_eps > 0.f)) return BPT_EINVAL;
   if (c->act == BPT_ACT_SWIGLU && (c->ffn_dim % 64)) return BPT_EINVAL;
-  if (c->flags & ~BPT_FLAG_ACCUM_GRADS) return BPT_EINVAL;
+  if (c->flags & ~(BPT_FLAG_ACCUM_GRADS | BPT_FLAG_ONE_STREAM)) return BPT_EINVAL;
   const int d = c->head_dim;
   if (d != 64 && d != 80 && d != 96 && d != 112 && d != 128) return BPT_EUNSUPPORTED;
   const int G = c->n_heads / c->n_kv_heads;
@@ -533,7 +533,12 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   Side* sd = side_stream();
   if (!sd) return BPT_ECUDA;
-  cudaStream_t ss = sd->s;
+  // With BPT_FLAG_ONE_STREAM the weight-gradient products run on the
+  // caller's stream in issue order; fork and join become no-ops.
+  const bool one = (cfg->flags & BPT_FLAG_ONE_STREAM) != 0;
+  cudaStream_t ss = one ? st : sd->s;
+  auto fork = [&]() { return one ? 0 : fork_side(st, sd); };
+  auto join = [&]() { return one ? 0 : join_side(st, sd); };
   const float* lse = reinterpret_cast<const float*>(saved);
   const bool hb = cfg->has_bias != 0;
   const bool accum = (cfg->flags & BPT_FLAG_ACCUM_GRADS) != 0;
@@ -577,7 +582,7 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
       }
       // the previous block's weight gradients (side stream) still read x1n,
       // a and dz, which this block now rewrites
-      if (!first && (rc = join_side(st, sd))) return rc;
+      if (!first && (rc = join())) return rc;
       if ((rc = norm_fwd(nr, (int)h, cfg->norm, cfg->norm_eps, W.x1, 1, h, w->ln2_w, w->ln2_b, W.x1n, h, st)))
         return rc;
       {
@@ -605,7 +610,7 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
       }
       const void* dyb = bf(dy, row * h);
       // side stream: the fc2 weight gradient needs only dy and a
-      if ((rc = fork_side(st, sd))) return rc;
+      if ((rc = fork())) return rc;
       // dW2 (+)= dy^T a ; db2 (+)= colsum(dy)
       {
         MatView A{dyb, nr, h, h};     // MN-major: [K = rows, M = h]
@@ -644,7 +649,7 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
         if ((rc = gemm(nr, f, h, A, false, &B, &h, 1, true, nullptr, e, st))) return rc;
       }
       // side stream: the fc1 weight (and bias) gradients need only dz and x1n
-      if ((rc = fork_side(st, sd))) return rc;
+      if ((rc = fork())) return rc;
       // dW1 (+)= dz^T x1n (SwiGLU: dWg from dg, dWu from du) ; db1
       {
         const int64_t ldz = swiglu ? 2 * f : f;
@@ -697,8 +702,8 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
   }
 
   // ---- output projection: dO = dx1 Wo ; dWo (+)= dx1^T O ; dbo
-  if ((rc = join_side(st, sd))) return rc;
-  if ((rc = fork_side(st, sd))) return rc;
+  if ((rc = join())) return rc;
+  if ((rc = fork())) return rc;
   {
     // side stream: dWo and dbo need only dx1 and O, and run beside dO and
     // the attention backward
@@ -732,7 +737,7 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
     if (D.chunked && (rc = stage_qkv(D, w, hb, W.xn, W.qkv, k, st))) return rc;
     // the previous stage's weight gradients (side stream) read dqkv, which
     // this stage's attention backward rewrites
-    if (k > 0 && (rc = join_side(st, sd))) return rc;
+    if (k > 0 && (rc = join())) return rc;
     AttnBwdShape sb = stage_bwd_shape(D, k);
     sb.f.causal = cfg->causal;
     if ((rc = attention_bwd(sb, W.qkv, W.o, lse, W.dO, W.dqkv, W.attn, st))) return rc;
@@ -752,7 +757,7 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
     }
     // dWq_s, dWk_s, dWv_s (+)= dQKV_s^T xn ; biases, on the side stream
     // beside dxn
-    if ((rc = fork_side(st, sd))) return rc;
+    if ((rc = fork())) return rc;
     {
       struct Piece {
         void* G;
@@ -785,7 +790,7 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
   }
   // everything issued on the side stream is ordered before the caller's next
   // work on the main stream
-  return join_side(st, sd) ? BPT_ECUDA : BPT_OK;
+  return join() ? BPT_ECUDA : BPT_OK;
 }
 
 }  // extern "C"

@@ -73,7 +73,7 @@ enum {
 
 enum { BPT_NORM_LAYER = 0, BPT_NORM_RMS = 1 };
 enum { BPT_ACT_GELU_ERF = 0, BPT_ACT_GELU_TANH = 1, BPT_ACT_SWIGLU = 2 };
-enum { BPT_FLAG_ACCUM_GRADS = 1 };
+enum { BPT_FLAG_ACCUM_GRADS = 1, BPT_FLAG_ONE_STREAM = 2 };
 
 enum { BPT_PASS_FWD = 0, BPT_PASS_BWD = 1, BPT_PASS_HEADCHUNK = 2 };
 
@@ -153,7 +153,10 @@ int bpt_layer_fwd(const bpt_config* cfg, const bpt_weights* w, const void* x, vo
  * second stream the library creates (one per device and host thread, on the
  * first call) and joins back into `stream` before returning: all of the
  * call's work is ordered before later work on `stream`.  Make the first call
- * of a thread before capturing `stream` into a graph. */
+ * of a thread before capturing `stream` into a graph.  With
+ * BPT_FLAG_ONE_STREAM in cfg->flags everything runs on `stream` in issue
+ * order instead: same results, no overlap, so that each kernel can be timed
+ * on its own. */
 int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, const void* saved,
                   const void* dy, void* dx, const bpt_grads* grads, void* ws, size_t ws_bytes,
                   void* stream);

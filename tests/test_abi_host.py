@@ -87,6 +87,15 @@ def test_invalid_config_rejected_before_launch(built, bad):
     assert _call_fwd(cfg) == bpt.BPT_EINVAL
 
 
+def test_known_flags_accepted(built):
+    """Both defined flags pass validation and leave the workspace plan alone."""
+    base = bpt.bpt_workspace_bytes(presets.C1, bpt.BPT_PASS_BWD)
+    both = presets.C1.with_(flags=bpt.BPT_FLAG_ACCUM_GRADS | bpt.BPT_FLAG_ONE_STREAM)
+    assert base > 0
+    assert bpt.bpt_workspace_bytes(both, bpt.BPT_PASS_BWD) == base
+    assert bpt.bpt_workspace_bytes(presets.C1.with_(flags=4), bpt.BPT_PASS_BWD) == 0
+
+
 def test_unsupported_head_dim(built):
     assert _call_fwd(presets.C1.with_(head_dim=72, h=288)) == bpt.BPT_EUNSUPPORTED
 

@@ -80,10 +80,11 @@ def test_headchunk_attention_matches_oracle():
     (LLAMA_SMALL, dict(head_chunk=8)), (LLAMA_SMALL, dict(ffn_block=384)),
     (LLAMA_SMALL, dict(ffn_block=128)), (GPT_SMALL, dict(head_chunk=1)),
     (GPT_SMALL, dict(head_chunk=2)), (GPT_SMALL, dict(ffn_block=256, q_block=256, kv_block=256)),
+    (LLAMA_SMALL, dict(flags=bpt.BPT_FLAG_ONE_STREAM)),
 ], ids=lambda v: v.name if hasattr(v, "name") else str(v))
 def test_schedule_invariance(base, variant):
-    """Head chunk U, FFN block and attention block sizes change the schedule,
-    not the result."""
+    """Head chunk U, FFN block, attention block sizes and running on one
+    stream change the schedule, not the result."""
     _, dev = device_inputs(base, seed=14)
     y0, s0 = run_fwd(base, dev)
     dx0, g0 = run_bwd(base, dev, s0)

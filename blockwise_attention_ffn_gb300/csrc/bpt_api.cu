@@ -252,9 +252,18 @@ Side* side_stream() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   Side& sd = sides[dev];
   if (!sd.s) {
-    if (cudaStreamCreateWithFlags(&sd.s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
-    for (auto& e : sd.ev)
-      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    // all or nothing: a half-made Side is destroyed and made again next call
+    Side n;
+    bool ok = cudaStreamCreateWithFlags(&n.s, cudaStreamNonBlocking) == cudaSuccess;
+    for (auto& e : n.ev)
+      ok = ok && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+      for (auto e : n.ev)
+        if (e) cudaEventDestroy(e);
+      if (n.s) cudaStreamDestroy(n.s);
+      return nullptr;
+    }
+    sd = n;
   }
   return &sd;
 }
@@ -546,251 +555,259 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
   const int64_t h = D.h, f = D.f, Hd = D.H * D.d, d = D.d;
   const bool ln = cfg->norm == BPT_NORM_LAYER;
 
-  if (!accum) {
-    if (cudaMemsetAsync(g->ln1_w, 0, h * 4, st) || cudaMemsetAsync(g->ln2_w, 0, h * 4, st)) return BPT_ECUDA;
-    if (ln && (cudaMemsetAsync(g->ln1_b, 0, h * 4, st) || cudaMemsetAsync(g->ln2_b, 0, h * 4, st)))
-      return BPT_ECUDA;
-  }
+  // The launch sequence; on an early error return the side stream is still
+  // joined below, so nothing it was given outlives the call unordered.
+  auto run = [&]() -> int {
+    if (!accum) {
+      if (cudaMemsetAsync(g->ln1_w, 0, h * 4, st) || cudaMemsetAsync(g->ln2_w, 0, h * 4, st)) return BPT_ECUDA;
+      if (ln && (cudaMemsetAsync(g->ln1_b, 0, h * 4, st) || cudaMemsetAsync(g->ln2_b, 0, h * 4, st)))
+        return BPT_ECUDA;
+    }
 
-  // ---- recompute N1, Q/K/V and attention (the saved LSE is not rewritten)
-  if ((rc = norm_fwd(D.rows, (int)h, cfg->norm, cfg->norm_eps, x, 0, h, w->ln1_w, w->ln1_b, W.xn, h, st)))
-    return rc;
-  for (int64_t k = 0; k < D.n_stages; ++k) {
-    if ((rc = stage_qkv(D, w, hb, W.xn, W.qkv, k, st))) return rc;
-    AttnShape a = stage_attn_shape(D, k, cfg->causal);
-    if ((rc = attention_fwd(a, W.qkv, W.o, nullptr, st))) return rc;
-  }
+    // ---- recompute N1, Q/K/V and attention (the saved LSE is not rewritten)
+    if ((rc = norm_fwd(D.rows, (int)h, cfg->norm, cfg->norm_eps, x, 0, h, w->ln1_w, w->ln1_b, W.xn, h, st)))
+      return rc;
+    for (int64_t k = 0; k < D.n_stages; ++k) {
+      if ((rc = stage_qkv(D, w, hb, W.xn, W.qkv, k, st))) return rc;
+      AttnShape a = stage_attn_shape(D, k, cfg->causal);
+      if ((rc = attention_fwd(a, W.qkv, W.o, nullptr, st))) return rc;
+    }
 
-  // ---- FFN blocks: rebuild x1, N2, fc1 and form the FFN / N2 gradients
-  bool first = true;
-  for (int64_t bi = 0; bi < D.b; ++bi) {
-    for (int64_t r0 = 0; r0 < D.s; r0 += D.cf) {
-      const int64_t nr = std::min(D.cf, D.s - r0);
-      const int64_t row = bi * D.s + r0;
-      const float beta = (accum || !first) ? 1.f : 0.f;
-      {
-        MatView A{bf(W.o, row * Hd), nr, Hd, Hd};
-        MatView B{w->wo, h, Hd, Hd};
-        Epilogue e;
-        e.kind = EPI_F32;  // x1 stays fp32: the residual stream is rounded once, at y
-        e.out = W.x1;
-        e.ldo = h;
-        e.bias = hb ? w->bo : nullptr;
-        e.res = bf(x, row * h);
-        e.ldr = h;
-        if ((rc = gemm(nr, h, Hd, A, false, &B, &Hd, 1, false, nullptr, e, st))) return rc;
-      }
-      // the previous block's weight gradients (side stream) still read x1n,
-      // a and dz, which this block now rewrites
-      if (!first && (rc = join())) return rc;
-      if ((rc = norm_fwd(nr, (int)h, cfg->norm, cfg->norm_eps, W.x1, 1, h, w->ln2_w, w->ln2_b, W.x1n, h, st)))
-        return rc;
-      {
-        MatView A{W.x1n, nr, h, h};
-        MatView B{w->w1, f, h, h};
-        Epilogue e;
-        e.out = W.a;
-        e.ldo = f;
-        if (swiglu) {
-          MatView B2{w->w3, f, h, h};
-          e.kind = EPI_SWIGLU;
-          e.out2 = W.g;
-          e.ldo2 = f;
-          e.out3 = W.u;
-          e.ldo3 = f;
-          if ((rc = gemm(nr, f, h, A, false, &B, &h, 1, false, &B2, e, st))) return rc;
-        } else {
-          e.kind = EPI_GELU;
-          e.act = cfg->act;
-          e.bias = hb ? w->b1 : nullptr;
-          e.out2 = W.gd;  // gelu'(z), which the fc2 backward multiplies by
-          e.ldo2 = f;
-          if ((rc = gemm(nr, f, h, A, false, &B, &h, 1, false, nullptr, e, st))) return rc;
+    // ---- FFN blocks: rebuild x1, N2, fc1 and form the FFN / N2 gradients
+    bool first = true;
+    for (int64_t bi = 0; bi < D.b; ++bi) {
+      for (int64_t r0 = 0; r0 < D.s; r0 += D.cf) {
+        const int64_t nr = std::min(D.cf, D.s - r0);
+        const int64_t row = bi * D.s + r0;
+        const float beta = (accum || !first) ? 1.f : 0.f;
+        {
+          MatView A{bf(W.o, row * Hd), nr, Hd, Hd};
+          MatView B{w->wo, h, Hd, Hd};
+          Epilogue e;
+          e.kind = EPI_F32;  // x1 stays fp32: the residual stream is rounded once, at y
+          e.out = W.x1;
+          e.ldo = h;
+          e.bias = hb ? w->bo : nullptr;
+          e.res = bf(x, row * h);
+          e.ldr = h;
+          if ((rc = gemm(nr, h, Hd, A, false, &B, &Hd, 1, false, nullptr, e, st))) return rc;
         }
-      }
-      const void* dyb = bf(dy, row * h);
-      // side stream: the fc2 weight gradient needs only dy and a
-      if ((rc = fork())) return rc;
-      // dW2 (+)= dy^T a ; db2 (+)= colsum(dy)
-      {
-        MatView A{dyb, nr, h, h};     // MN-major: [K = rows, M = h]
-        MatView B{W.a, nr, f, f};     // MN-major: [K = rows, N = f]
-        Epilogue e;
-        e.kind = EPI_F32;
-        e.out = g->w2;
-        e.ldo = f;
-        e.beta = beta;
-        if ((rc = gemm(h, f, nr, A, true, &B, &nr, 1, true, nullptr, e, ss))) return rc;
-        if (hb && (rc = colsum(nr, h, dyb, h, reinterpret_cast<float*>(g->b2), beta != 0.f, ss))) return rc;
-      }
-      // dA = dy W2, fused with the activation gradient
-      {
-        MatView A{dyb, nr, h, h};
-        MatView B{w->w2, h, f, f};  // [K = h rows, N = f cols]
-        Epilogue e;
-        if (swiglu) {
-          e.kind = EPI_SWIGLU_BWD;
-          e.aux = W.g;
-          e.ldaux = f;
-          e.aux2 = W.u;
-          e.ldaux2 = f;
-          e.out = W.dz;
-          e.ldo = 2 * f;
-          e.out2 = bfm(W.dz, f);
-          e.ldo2 = 2 * f;
-        } else {
-          e.kind = EPI_GELU_BWD;
-          e.act = cfg->act;
-          e.aux = W.gd;
-          e.ldaux = f;
-          e.out = W.dz;
-          e.ldo = f;
-        }
-        if ((rc = gemm(nr, f, h, A, false, &B, &h, 1, true, nullptr, e, st))) return rc;
-      }
-      // side stream: the fc1 weight (and bias) gradients need only dz and x1n
-      if ((rc = fork())) return rc;
-      // dW1 (+)= dz^T x1n (SwiGLU: dWg from dg, dWu from du) ; db1
-      {
-        const int64_t ldz = swiglu ? 2 * f : f;
-        MatView B{W.x1n, nr, h, h};
-        Epilogue e;
-        e.kind = EPI_F32;
-        e.ldo = h;
-        e.beta = beta;
-        MatView A{W.dz, nr, f, ldz};
-        e.out = g->w1;
-        if ((rc = gemm(f, h, nr, A, true, &B, &nr, 1, true, nullptr, e, ss))) return rc;
-        if (swiglu) {
-          MatView A2{bf(W.dz, f), nr, f, ldz};
-          e.out = g->w3;
-          if ((rc = gemm(f, h, nr, A2, true, &B, &nr, 1, true, nullptr, e, ss))) return rc;
-        } else if (hb) {
-          if ((rc = colsum(nr, f, W.dz, f, reinterpret_cast<float*>(g->b1), beta != 0.f, ss))) return rc;
-        }
-      }
-      // dx1n = dz W1  (SwiGLU: dg Wg + du Wu)
-      {
-        Epilogue e;
-        e.kind = EPI_BF16;
-        e.out = W.dx1n;
-        e.ldo = h;
-        if (swiglu) {
-          MatView A{W.dz, nr, 2 * f, 2 * f};
-          MatView Bs[2] = {{w->w1, f, h, h}, {w->w3, f, h, h}};
-          int64_t ks[2] = {f, f};
-          if (f % 64 == 0) {
-            if ((rc = gemm(nr, h, 2 * f, A, false, Bs, ks, 2, true, nullptr, e, st))) return rc;
-          } else {
-            return BPT_EUNSUPPORTED;
-          }
-        } else {
-          MatView A{W.dz, nr, f, f};
-          MatView B{w->w1, f, h, h};
-          if ((rc = gemm(nr, h, f, A, false, &B, &f, 1, true, nullptr, e, st))) return rc;
-        }
-      }
-      // dx1 = dy + N2^T(dx1n), as bf16 (operand of the next products) and fp32
-      {
-        NormBwdIO io{W.dx1n, 0, h, W.x1, 1, h, dyb, 0, h, bfm(W.dx1, row * h), W.dx1f + row * h, h};
-        if ((rc = norm_bwd(nr, (int)h, cfg->norm, cfg->norm_eps, io, w->ln2_w, reinterpret_cast<float*>(g->ln2_w),
-                           ln ? reinterpret_cast<float*>(g->ln2_b) : nullptr, st)))
+        // the previous block's weight gradients (side stream) still read x1n,
+        // a and dz, which this block now rewrites
+        if (!first && (rc = join())) return rc;
+        if ((rc = norm_fwd(nr, (int)h, cfg->norm, cfg->norm_eps, W.x1, 1, h, w->ln2_w, w->ln2_b, W.x1n, h, st)))
           return rc;
+        {
+          MatView A{W.x1n, nr, h, h};
+          MatView B{w->w1, f, h, h};
+          Epilogue e;
+          e.out = W.a;
+          e.ldo = f;
+          if (swiglu) {
+            MatView B2{w->w3, f, h, h};
+            e.kind = EPI_SWIGLU;
+            e.out2 = W.g;
+            e.ldo2 = f;
+            e.out3 = W.u;
+            e.ldo3 = f;
+            if ((rc = gemm(nr, f, h, A, false, &B, &h, 1, false, &B2, e, st))) return rc;
+          } else {
+            e.kind = EPI_GELU;
+            e.act = cfg->act;
+            e.bias = hb ? w->b1 : nullptr;
+            e.out2 = W.gd;  // gelu'(z), which the fc2 backward multiplies by
+            e.ldo2 = f;
+            if ((rc = gemm(nr, f, h, A, false, &B, &h, 1, false, nullptr, e, st))) return rc;
+          }
+        }
+        const void* dyb = bf(dy, row * h);
+        // side stream: the fc2 weight gradient needs only dy and a
+        if ((rc = fork())) return rc;
+        // dW2 (+)= dy^T a ; db2 (+)= colsum(dy)
+        {
+          MatView A{dyb, nr, h, h};     // MN-major: [K = rows, M = h]
+          MatView B{W.a, nr, f, f};     // MN-major: [K = rows, N = f]
+          Epilogue e;
+          e.kind = EPI_F32;
+          e.out = g->w2;
+          e.ldo = f;
+          e.beta = beta;
+          if ((rc = gemm(h, f, nr, A, true, &B, &nr, 1, true, nullptr, e, ss))) return rc;
+          if (hb && (rc = colsum(nr, h, dyb, h, reinterpret_cast<float*>(g->b2), beta != 0.f, ss))) return rc;
+        }
+        // dA = dy W2, fused with the activation gradient
+        {
+          MatView A{dyb, nr, h, h};
+          MatView B{w->w2, h, f, f};  // [K = h rows, N = f cols]
+          Epilogue e;
+          if (swiglu) {
+            e.kind = EPI_SWIGLU_BWD;
+            e.aux = W.g;
+            e.ldaux = f;
+            e.aux2 = W.u;
+            e.ldaux2 = f;
+            e.out = W.dz;
+            e.ldo = 2 * f;
+            e.out2 = bfm(W.dz, f);
+            e.ldo2 = 2 * f;
+          } else {
+            e.kind = EPI_GELU_BWD;
+            e.act = cfg->act;
+            e.aux = W.gd;
+            e.ldaux = f;
+            e.out = W.dz;
+            e.ldo = f;
+          }
+          if ((rc = gemm(nr, f, h, A, false, &B, &h, 1, true, nullptr, e, st))) return rc;
+        }
+        // side stream: the fc1 weight (and bias) gradients need only dz and x1n
+        if ((rc = fork())) return rc;
+        // dW1 (+)= dz^T x1n (SwiGLU: dWg from dg, dWu from du) ; db1
+        {
+          const int64_t ldz = swiglu ? 2 * f : f;
+          MatView B{W.x1n, nr, h, h};
+          Epilogue e;
+          e.kind = EPI_F32;
+          e.ldo = h;
+          e.beta = beta;
+          MatView A{W.dz, nr, f, ldz};
+          e.out = g->w1;
+          if ((rc = gemm(f, h, nr, A, true, &B, &nr, 1, true, nullptr, e, ss))) return rc;
+          if (swiglu) {
+            MatView A2{bf(W.dz, f), nr, f, ldz};
+            e.out = g->w3;
+            if ((rc = gemm(f, h, nr, A2, true, &B, &nr, 1, true, nullptr, e, ss))) return rc;
+          } else if (hb) {
+            if ((rc = colsum(nr, f, W.dz, f, reinterpret_cast<float*>(g->b1), beta != 0.f, ss))) return rc;
+          }
+        }
+        // dx1n = dz W1  (SwiGLU: dg Wg + du Wu)
+        {
+          Epilogue e;
+          e.kind = EPI_BF16;
+          e.out = W.dx1n;
+          e.ldo = h;
+          if (swiglu) {
+            MatView A{W.dz, nr, 2 * f, 2 * f};
+            MatView Bs[2] = {{w->w1, f, h, h}, {w->w3, f, h, h}};
+            int64_t ks[2] = {f, f};
+            if (f % 64 == 0) {
+              if ((rc = gemm(nr, h, 2 * f, A, false, Bs, ks, 2, true, nullptr, e, st))) return rc;
+            } else {
+              return BPT_EUNSUPPORTED;
+            }
+          } else {
+            MatView A{W.dz, nr, f, f};
+            MatView B{w->w1, f, h, h};
+            if ((rc = gemm(nr, h, f, A, false, &B, &f, 1, true, nullptr, e, st))) return rc;
+          }
+        }
+        // dx1 = dy + N2^T(dx1n), as bf16 (operand of the next products) and fp32
+        {
+          NormBwdIO io{W.dx1n, 0, h, W.x1, 1, h, dyb, 0, h, bfm(W.dx1, row * h), W.dx1f + row * h, h};
+          if ((rc = norm_bwd(nr, (int)h, cfg->norm, cfg->norm_eps, io, w->ln2_w, reinterpret_cast<float*>(g->ln2_w),
+                             ln ? reinterpret_cast<float*>(g->ln2_b) : nullptr, st)))
+            return rc;
+        }
+        first = false;
       }
-      first = false;
     }
-  }
 
-  // ---- output projection: dO = dx1 Wo ; dWo (+)= dx1^T O ; dbo
-  if ((rc = join())) return rc;
-  if ((rc = fork())) return rc;
-  {
-    // side stream: dWo and dbo need only dx1 and O, and run beside dO and
-    // the attention backward
-    MatView A2{W.dx1, D.rows, h, h};
-    MatView B2{W.o, D.rows, Hd, Hd};
-    Epilogue e2;
-    e2.kind = EPI_F32;
-    e2.out = g->wo;
-    e2.ldo = Hd;
-    e2.beta = accum ? 1.f : 0.f;
-    const int64_t K = D.rows;
-    if ((rc = gemm(h, Hd, K, A2, true, &B2, &K, 1, true, nullptr, e2, ss))) return rc;
-    if (hb && (rc = colsum(D.rows, h, W.dx1, h, reinterpret_cast<float*>(g->bo), accum, ss))) return rc;
-    MatView A{W.dx1, D.rows, h, h};
-    MatView B{w->wo, h, Hd, Hd};  // [K = h rows, N = Hd cols]
-    Epilogue e;
-    e.out = W.dO;
-    e.ldo = Hd;
-    if ((rc = gemm(D.rows, Hd, h, A, false, &B, &h, 1, true, nullptr, e, st))) return rc;
-  }
-
-  // ---- attention and Q/K/V gradients, stage by stage.  The key-bias
-  // gradient is identically zero: the bias adds Q[q].bk to every logit of
-  // query row q alike (masked ones stay -inf), and softmax is invariant to
-  // such a shift, so the loss does not depend on bk.  It is written as exact
-  // zeros (left as is when accumulating) instead of summing dK, whose sum of
-  // bf16-rounded rows would be rounding noise growing like sqrt(s).
-  if (hb && !accum && cudaMemsetAsync(g->bk, 0, (size_t)(D.Hkv * D.d) * sizeof(float), st) != cudaSuccess)
-    return BPT_ECUDA;
-  for (int64_t k = 0; k < D.n_stages; ++k) {
-    if (D.chunked && (rc = stage_qkv(D, w, hb, W.xn, W.qkv, k, st))) return rc;
-    // the previous stage's weight gradients (side stream) read dqkv, which
-    // this stage's attention backward rewrites
-    if (k > 0 && (rc = join())) return rc;
-    AttnBwdShape sb = stage_bwd_shape(D, k);
-    sb.f.causal = cfg->causal;
-    if ((rc = attention_bwd(sb, W.qkv, W.o, lse, W.dO, W.dqkv, W.attn, st))) return rc;
-    const int64_t q0 = k * D.U * d, kv0 = k * D.Uk * d;
-    const int64_t nq = D.U * d, nkv = D.Uk * d;
-    // dxn (+)= dQ Wq_s + dK Wk_s + dV Wv_s
-    {
-      MatView A{W.dqkv, D.rows, D.qkv_w, D.qkv_w};
-      MatView Bs[3] = {{bf(w->wq, q0 * h), nq, h, h}, {bf(w->wk, kv0 * h), nkv, h, h}, {bf(w->wv, kv0 * h), nkv, h, h}};
-      int64_t ks[3] = {nq, nkv, nkv};
-      Epilogue e;
-      e.kind = EPI_F32;
-      e.out = W.dxn;
-      e.ldo = h;
-      e.beta = k > 0 ? 1.f : 0.f;
-      if ((rc = gemm_kseg(D.rows, h, A, Bs, ks, 3, e, st))) return rc;
-    }
-    // dWq_s, dWk_s, dWv_s (+)= dQKV_s^T xn ; biases, on the side stream
-    // beside dxn
+    // ---- output projection: dO = dx1 Wo ; dWo (+)= dx1^T O ; dbo
+    if ((rc = join())) return rc;
     if ((rc = fork())) return rc;
     {
-      struct Piece {
-        void* G;
-        void* Gb;
-        int64_t row0, n, col;
-      } pieces[3] = {{g->wq, g->bq, q0, nq, 0}, {g->wk, g->bk, kv0, nkv, nq}, {g->wv, g->bv, kv0, nkv, nq + nkv}};
-      MatView B{W.xn, D.rows, h, h};
+      // side stream: dWo and dbo need only dx1 and O, and run beside dO and
+      // the attention backward
+      MatView A2{W.dx1, D.rows, h, h};
+      MatView B2{W.o, D.rows, Hd, Hd};
+      Epilogue e2;
+      e2.kind = EPI_F32;
+      e2.out = g->wo;
+      e2.ldo = Hd;
+      e2.beta = accum ? 1.f : 0.f;
       const int64_t K = D.rows;
-      for (auto& pc : pieces) {
-        MatView A{bf(W.dqkv, pc.col), D.rows, pc.n, D.qkv_w};
+      if ((rc = gemm(h, Hd, K, A2, true, &B2, &K, 1, true, nullptr, e2, ss))) return rc;
+      if (hb && (rc = colsum(D.rows, h, W.dx1, h, reinterpret_cast<float*>(g->bo), accum, ss))) return rc;
+      MatView A{W.dx1, D.rows, h, h};
+      MatView B{w->wo, h, Hd, Hd};  // [K = h rows, N = Hd cols]
+      Epilogue e;
+      e.out = W.dO;
+      e.ldo = Hd;
+      if ((rc = gemm(D.rows, Hd, h, A, false, &B, &h, 1, true, nullptr, e, st))) return rc;
+    }
+
+    // ---- attention and Q/K/V gradients, stage by stage.  The key-bias
+    // gradient is identically zero: the bias adds Q[q].bk to every logit of
+    // query row q alike (masked ones stay -inf), and softmax is invariant to
+    // such a shift, so the loss does not depend on bk.  It is written as exact
+    // zeros (left as is when accumulating) instead of summing dK, whose sum of
+    // bf16-rounded rows would be rounding noise growing like sqrt(s).
+    if (hb && !accum && cudaMemsetAsync(g->bk, 0, (size_t)(D.Hkv * D.d) * sizeof(float), st) != cudaSuccess)
+      return BPT_ECUDA;
+    for (int64_t k = 0; k < D.n_stages; ++k) {
+      if (D.chunked && (rc = stage_qkv(D, w, hb, W.xn, W.qkv, k, st))) return rc;
+      // the previous stage's weight gradients (side stream) read dqkv, which
+      // this stage's attention backward rewrites
+      if (k > 0 && (rc = join())) return rc;
+      AttnBwdShape sb = stage_bwd_shape(D, k);
+      sb.f.causal = cfg->causal;
+      if ((rc = attention_bwd(sb, W.qkv, W.o, lse, W.dO, W.dqkv, W.attn, st))) return rc;
+      const int64_t q0 = k * D.U * d, kv0 = k * D.Uk * d;
+      const int64_t nq = D.U * d, nkv = D.Uk * d;
+      // dxn (+)= dQ Wq_s + dK Wk_s + dV Wv_s
+      {
+        MatView A{W.dqkv, D.rows, D.qkv_w, D.qkv_w};
+        MatView Bs[3] = {
+            {bf(w->wq, q0 * h), nq, h, h}, {bf(w->wk, kv0 * h), nkv, h, h}, {bf(w->wv, kv0 * h), nkv, h, h}};
+        int64_t ks[3] = {nq, nkv, nkv};
         Epilogue e;
         e.kind = EPI_F32;
-        e.out = f32(pc.G, pc.row0 * h);
+        e.out = W.dxn;
         e.ldo = h;
-        e.beta = accum ? 1.f : 0.f;
-        if ((rc = gemm(pc.n, h, K, A, true, &B, &K, 1, true, nullptr, e, ss))) return rc;
-        if (hb && pc.Gb != g->bk &&
-            (rc = colsum(D.rows, pc.n, bf(W.dqkv, pc.col), D.qkv_w, f32(pc.Gb, pc.row0), accum, ss)))
-          return rc;
+        e.beta = k > 0 ? 1.f : 0.f;
+        if ((rc = gemm_kseg(D.rows, h, A, Bs, ks, 3, e, st))) return rc;
+      }
+      // dWq_s, dWk_s, dWv_s (+)= dQKV_s^T xn ; biases, on the side stream
+      // beside dxn
+      if ((rc = fork())) return rc;
+      {
+        struct Piece {
+          void* G;
+          void* Gb;
+          int64_t row0, n, col;
+        } pieces[3] = {{g->wq, g->bq, q0, nq, 0}, {g->wk, g->bk, kv0, nkv, nq}, {g->wv, g->bv, kv0, nkv, nq + nkv}};
+        MatView B{W.xn, D.rows, h, h};
+        const int64_t K = D.rows;
+        for (auto& pc : pieces) {
+          MatView A{bf(W.dqkv, pc.col), D.rows, pc.n, D.qkv_w};
+          Epilogue e;
+          e.kind = EPI_F32;
+          e.out = f32(pc.G, pc.row0 * h);
+          e.ldo = h;
+          e.beta = accum ? 1.f : 0.f;
+          if ((rc = gemm(pc.n, h, K, A, true, &B, &K, 1, true, nullptr, e, ss))) return rc;
+          if (hb && pc.Gb != g->bk &&
+              (rc = colsum(D.rows, pc.n, bf(W.dqkv, pc.col), D.qkv_w, f32(pc.Gb, pc.row0), accum, ss)))
+            return rc;
+        }
       }
     }
-  }
 
-  // ---- dx = dx1 + N1^T(dxn)
-  {
-    NormBwdIO io{W.dxn, 1, h, x, 0, h, W.dx1f, 1, h, dx, nullptr, h};
-    if ((rc = norm_bwd(D.rows, (int)h, cfg->norm, cfg->norm_eps, io, w->ln1_w, reinterpret_cast<float*>(g->ln1_w),
-                       ln ? reinterpret_cast<float*>(g->ln1_b) : nullptr, st)))
-      return rc;
-  }
+    // ---- dx = dx1 + N1^T(dxn)
+    {
+      NormBwdIO io{W.dxn, 1, h, x, 0, h, W.dx1f, 1, h, dx, nullptr, h};
+      if ((rc = norm_bwd(D.rows, (int)h, cfg->norm, cfg->norm_eps, io, w->ln1_w, reinterpret_cast<float*>(g->ln1_w),
+                         ln ? reinterpret_cast<float*>(g->ln1_b) : nullptr, st)))
+        return rc;
+    }
+    return BPT_OK;
+  };
+  rc = run();
   // everything issued on the side stream is ordered before the caller's next
   // work on the main stream
-  return join() ? BPT_ECUDA : BPT_OK;
+  const int jr = join();
+  return rc ? rc : (jr ? BPT_ECUDA : BPT_OK);
 }
 
 }  // extern "C"

@@ -4,6 +4,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -48,15 +49,16 @@ struct ProfRec {
   double flops = 0, bytes = 0;
 };
 std::mutex g_prof_mu;
-bool g_prof_on = false;
+std::atomic<bool> g_prof_on{false};  // read without the lock on every launch
 std::vector<ProfRec> g_prof;
 size_t g_prof_used = 0;
 
 }  // namespace
 
 ProfScope::ProfScope(int kind, double flops, double bytes, cudaStream_t s) : slot(-1), st(s) {
-  if (!g_prof_on) return;
+  if (!g_prof_on.load(std::memory_order_relaxed)) return;
   std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof_on.load(std::memory_order_relaxed)) return;
   if (g_prof_used == g_prof.size()) {
     ProfRec r;
     if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) return;

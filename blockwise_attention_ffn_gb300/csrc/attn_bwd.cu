@@ -13,12 +13,11 @@
 // Two kernels, neither with atomics:
 //  * dK/dV: one CTA per 128-row key/value tile j of one key/value head; it
 //    loops over the G query heads of the group and their query tiles i >= j
-//    (causal), accumulating dK and dV in TMEM.  Head dims 64 and 80 keep
-//    every A operand in TMEM and work in 64-query sub-tiles with
-//    double-buffered S^T and dP^T, taken alternately by two groups of
-//    compute warps with their own MMA-issuing warps; 96 to 128, whose
-//    accumulators leave too little TMEM for that, keep K, V, P^T and dS^T
-//    in shared memory and one group that forms P and dS in turn.
+//    (causal), accumulating dK and dV in TMEM.  It works in 64-query
+//    sub-tiles with double-buffered S^T and dP^T, taken alternately by two
+//    groups of compute warps with their own MMA-issuing warps.  K and V are
+//    TMEM operands for head dims 64 and 80; for 96 to 128, whose
+//    accumulators leave no TMEM for them, they stay in shared memory.
 //  * dQ: one CTA per 128-row query tile i of one query head; it loops over
 //    the key/value tiles j <= i in 64-key sub-tiles the same way,
 //    accumulating dQ in TMEM, and writes it once.
@@ -68,359 +67,51 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
 
 
 // ===========================================================================
 // dK / dV
 // ===========================================================================
-// Warps: 0 TMA, 1 MMA, 2..9 compute.  Compute warp w handles key/value row
-// (w % 4) * 32 + lane (its TMEM lane quarter) and query columns
-// [64 * grp, 64 * grp + 64) with grp = (w - 2) / 4, so every row is shared by
-// two warps and each sub-partition runs two compute warps.
-// TMEM: S^T [0,128), dP^T [128,256), dV [256, 256+D), dK [256+D, 256+2D).
-// Per step t (query tile i of query head hn):
-//   MMA: [P^T(t) in smem] dV(t); [S^T columns read] S(t+1); [dS^T(t) in smem]
-//        dP(t+1), dK(t)
-//   compute: S^T(t) -> P^T (kept in registers, bf16 copy to smem), release
-//        the S^T columns; dP^T(t) -> dS^T = P^T (dP^T - D) to smem.
-// So S(t+1) runs while the compute warps form dS^T(t), and dP(t+1) and dK(t)
-// run while they form P^T(t+1).
-template <int D>
-struct DkdvCfg {
-  using T = TileGeom<D>;
-  static constexpr int QS = (D <= 96) ? 2 : 1;
-  static constexpr int STAGE = 2 * T::TILE + 2 * 512;  // Q, dO, LSE, D
-  static constexpr int SMEM = 2 * T::TILE + QS * STAGE + 2 * SqTile::BYTES + 1024 + 256;
-};
-
-template <int D>
-__global__ void __launch_bounds__(320, 1) attn_dkdv_kernel(const __grid_constant__ AttnBwdParams p) {
-  using T = TileGeom<D>;
-  constexpr int QS = DkdvCfg<D>::QS;
-  constexpr int STAGE = DkdvCfg<D>::STAGE;
-  constexpr uint32_t ID_SQ = idesc_bf16(128, 128, false, false);
-  constexpr uint32_t ID_KV = idesc_bf16(128, D, false, true);
-
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sK = smem;
-  uint8_t* sV = sK + T::TILE;
-  uint8_t* sStage = sV + T::TILE;
-  uint8_t* sP = sStage + QS * STAGE;
-  uint8_t* sDS = sP + SqTile::BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sDS + SqTile::BYTES);
-  uint64_t* kv_full = bars;
-  uint64_t* qdo_full = bars + 1;
-  uint64_t* qdo_empty = qdo_full + QS;
-  uint64_t* s_full = qdo_empty + QS;  // S^T(t) in TMEM
-  uint64_t* dp_full = s_full + 1;     // dP^T(t) in TMEM
-  uint64_t* p_full = dp_full + 1;     // P^T(t) in smem (8 arrivals)
-  uint64_t* s_free = p_full + 1;      // S^T columns read (8 arrivals)
-  uint64_t* pds_full = s_free + 1;    // dS^T(t) in smem, dP^T columns read (8)
-  uint64_t* p_used = pds_full + 1;    // dV(t) done
-  uint64_t* it_done = p_used + 1;     // dK(t) done
-  uint64_t* drain = it_done + 1;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-
-  const int warp = warp_id();
-  const int lane = lane_id();
-  // head-major, heaviest key tiles (smallest j) of a KV head first, so the
-  // CTAs in flight share that head's Q/dO stream in L2
-  const int nq_total = (p.s + 127) / 128;
-  const int pair = blockIdx.x / nq_total;
-  const int j = blockIdx.x % nq_total;
-  const int g = pair % p.Hkv;
-  const int bi = pair / p.Hkv;
-  const int i0 = p.causal ? j : 0;
-  const int n_i = nq_total - i0;
-  const int T_iter = p.G * n_i;
-
-  if (threadIdx.x == 0) {
-    mbar_init(kv_full, 1);
-    for (int i = 0; i < QS; ++i) {
-      mbar_init(&qdo_full[i], 1);
-      mbar_init(&qdo_empty[i], 1);
-    }
-    mbar_init(s_full, 1);
-    mbar_init(dp_full, 1);
-    mbar_init(p_full, 8);
-    mbar_init(s_free, 8);
-    mbar_init(pds_full, 8);
-    mbar_init(p_used, 1);
-    mbar_init(it_done, 1);
-    mbar_init(drain, 1);
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch(&p.map_qkv);
-    tma_prefetch(&p.map_do);
-  }
-  if (warp == 1) {
-    tmem_alloc(tmem_holder, 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_holder;
-  const uint32_t tS = tmem;
-  const uint32_t tdP = tmem + 128;
-  const uint32_t tdV = tmem + 256;
-  const uint32_t tdK = tmem + 256 + D;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------ TMA producer
-      mbar_expect_tx(kv_full, 2 * T::TILE);
-#pragma unroll
-      for (int c = 0; c < T::NCH; ++c) {
-        tma_load_3d(sK + c * T::CHUNK, &p.map_qkv, kv_full, p.k_col + g * D + c * T::CW, j * 128, bi);
-        tma_load_3d(sV + c * T::CHUNK, &p.map_qkv, kv_full, p.v_col + g * D + c * T::CW, j * 128, bi);
-      }
-      int issued = 0;
-      for (int t = 0; t < T_iter; ++t) {
-        const int st = t % QS;
-        if (t >= QS && !bounded_wait(&qdo_empty[st], ((t / QS) & 1) ^ 1, abort_flag, 501, p.err)) break;
-        const int hn = g * p.G + t / n_i;
-        const int i = i0 + t % n_i;
-        uint8_t* sQ = sStage + st * STAGE;
-        uint8_t* sdO = sQ + T::TILE;
-        uint8_t* sL = sdO + T::TILE;
-        mbar_expect_tx(&qdo_full[st], STAGE);
-#pragma unroll
-        for (int c = 0; c < T::NCH; ++c) {
-          tma_load_3d(sQ + c * T::CHUNK, &p.map_qkv, &qdo_full[st], p.q_col + hn * D + c * T::CW, i * 128, bi);
-          tma_load_3d(sdO + c * T::CHUNK, &p.map_do, &qdo_full[st], p.do_col + hn * D + c * T::CW, i * 128, bi);
-        }
-        bulk_load(sL, p.lse + ((long long)bi * p.H_total + p.lse_head0 + hn) * p.s_pad + i * 128, 512,
-                  &qdo_full[st]);
-        bulk_load(sL + 512, p.Dsum + ((long long)bi * p.H + hn) * p.s_pad + i * 128, 512, &qdo_full[st]);
-        issued = t + 1;
-      }
-      if (*abort_flag) {
-        mbar_try_wait(kv_full, 0);
-        for (int t = (issued > QS ? issued - QS : 0); t < issued; ++t)
-          bounded_wait(&qdo_full[t % QS], (t / QS) & 1, abort_flag, 502, p.err);
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------ MMA issuer
-      const uint32_t uK = smem_u32(sK), uV = smem_u32(sV);
-      const uint32_t uP = smem_u32(sP), uDS = smem_u32(sDS);
-      auto stage_u = [&](int t) { return smem_u32(sStage + (t % QS) * STAGE); };
-      auto issue_s = [&](int t) {
-        const uint32_t uQ = stage_u(t);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) umma_bf16(tS, T::kmajor(uK, kk), T::kmajor(uQ, kk), ID_SQ, kk > 0);
-        umma_commit(s_full);
-      };
-      auto issue_dp = [&](int t) {
-        const uint32_t udO = stage_u(t) + T::TILE;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) umma_bf16(tdP, T::kmajor(uV, kk), T::kmajor(udO, kk), ID_SQ, kk > 0);
-        umma_commit(dp_full);
-      };
-      bool ok = bounded_wait(kv_full, 0, abort_flag, 511, p.err) &&
-                bounded_wait(&qdo_full[0], 0, abort_flag, 512, p.err);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-        issue_dp(0);
-      }
-      for (int t = 0; ok && t < T_iter; ++t) {
-        const int st = t % QS;
-        const uint32_t uQ = stage_u(t);
-        const uint32_t udO = uQ + T::TILE;
-        const bool more = t + 1 < T_iter;
-        // dV(t) += P^T(t) dO(t)
-        if (!bounded_wait(p_full, t & 1, abort_flag, 513, p.err)) { ok = false; break; }
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_bf16(tdV, SqTile::kmajor(uP, kk), T::mnmajor(udO, kk), ID_KV, (t > 0 || kk > 0));
-        umma_commit(p_used);
-        if (QS == 2 && more) {
-          // S(t+1) as soon as the S^T columns are read
-          if (!bounded_wait(s_free, t & 1, abort_flag, 514, p.err)) { ok = false; break; }
-          if (!bounded_wait(&qdo_full[(t + 1) % QS], ((t + 1) / QS) & 1, abort_flag, 515, p.err)) { ok = false; break; }
-          tc_fence_after();
-          issue_s(t + 1);
-        }
-        if (!bounded_wait(pds_full, t & 1, abort_flag, 516, p.err)) { ok = false; break; }
-        tc_fence_after();
-        if (QS == 2 && more) issue_dp(t + 1);
-        // dK(t) += dS^T(t) Q(t)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_bf16(tdK, SqTile::kmajor(uDS, kk), T::mnmajor(uQ, kk), ID_KV, (t > 0 || kk > 0));
-        umma_commit(&qdo_empty[st]);
-        umma_commit(it_done);
-        if (QS == 1 && more) {
-          // one Q/dO stage: the next tile loads once dK(t) is done with it
-          if (!bounded_wait(&qdo_full[(t + 1) % QS], ((t + 1) / QS) & 1, abort_flag, 517, p.err)) { ok = false; break; }
-          tc_fence_after();
-          issue_s(t + 1);
-          issue_dp(t + 1);
-        }
-      }
-      if (!ok) {
-        umma_commit(drain);
-        bounded_wait(drain, 0, abort_flag, 519, p.err);
-      }
-    }
-  } else {
-    // ------------------------------------------------ compute (warps 2..9)
-    const int quarter = warp & 3;
-    const int grp = (warp - 2) >> 2;
-    const int r = quarter * 32 + lane;
-    const int kvp = j * 128 + r;
-    const int c0 = grp * 64;
-    const uint32_t lane_off = ((uint32_t)(quarter * 32) << 16) + c0;
-    const float c = p.scale_log2;
-    const float LOG2E = 1.4426950408889634f;
-    bool ok = true;
-    for (int t = 0; t < T_iter; ++t) {
-      const int st = t % QS;
-      const int i = i0 + t % n_i;
-      const int q0 = i * 128 + c0;
-      const float* sL = reinterpret_cast<const float*>(sStage + st * STAGE + 2 * T::TILE) + c0;
-      const float* sDsum = sL + 128;
-      ok = bounded_wait(&qdo_full[st], (t / QS) & 1, abort_flag, 521, p.err) &&
-           bounded_wait(s_full, t & 1, abort_flag, 522, p.err);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      tc_fence_after();
-      const bool edge = (p.causal && kvp > q0) || (q0 + 64 > p.s) || (kvp >= p.s);
-      // phase 1: P^T.  dV(t-1), the last reader of the P^T tile, precedes
-      // S(t) on the tensor pipe, so this wait returns at once.
-      if (t >= 1) {
-        ok = bounded_wait(p_used, (t - 1) & 1, abort_flag, 523, p.err);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      }
-      uint32_t pv[64];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) tmem_ld16_nw(tS + lane_off + q4 * 16, pv + q4 * 16);
-      tmem_wait_ld(pv);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_free);
-#pragma unroll
-      for (int k = 0; k < 64; k += 8) {
-        const float4 la = *reinterpret_cast<const float4*>(sL + k);
-        const float4 lb = *reinterpret_cast<const float4*>(sL + k + 4);
-        const float lv[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
-        float e[8];
-#pragma unroll
-        for (int m = 0; m < 8; ++m) e[m] = ex2(fmaf(__uint_as_float(pv[k + m]), c, -lv[m] * LOG2E));
-        if (edge) {
-#pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            const int qp = q0 + k + m;
-            if (qp >= p.s || kvp >= p.s || (p.causal && kvp > qp)) e[m] = 0.f;
-          }
-        }
-#pragma unroll
-        for (int m = 0; m < 8; ++m) pv[k + m] = __float_as_uint(e[m]);
-        *reinterpret_cast<uint4*>(sP + SqTile::off(r, grp * 8 + k / 8)) =
-            make_uint4(pack_bf16(e[0], e[1]), pack_bf16(e[2], e[3]), pack_bf16(e[4], e[5]), pack_bf16(e[6], e[7]));
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
-      // phase 2: dS^T = P^T (dP^T - D), once dK(t-1) released the dS^T tile
-      ok = bounded_wait(dp_full, t & 1, abort_flag, 524, p.err);
-      if (ok && t >= 1) ok = bounded_wait(it_done, (t - 1) & 1, abort_flag, 525, p.err);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t dr[64];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) tmem_ld16_nw(tdP + lane_off + q4 * 16, dr + q4 * 16);
-      tmem_wait_ld(dr);
-#pragma unroll
-      for (int k = 0; k < 64; k += 8) {
-        const float4 da = *reinterpret_cast<const float4*>(sDsum + k);
-        const float4 db = *reinterpret_cast<const float4*>(sDsum + k + 4);
-        const float dv[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
-        float a[8];
-#pragma unroll
-        for (int m = 0; m < 8; ++m) a[m] = __uint_as_float(pv[k + m]) * (__uint_as_float(dr[k + m]) - dv[m]);
-        *reinterpret_cast<uint4*>(sDS + SqTile::off(r, grp * 8 + k / 8)) =
-            make_uint4(pack_bf16(a[0], a[1]), pack_bf16(a[2], a[3]), pack_bf16(a[4], a[5]), pack_bf16(a[6], a[7]));
-      }
-      tc_fence_before();
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(pds_full);
-    }
-    if (ok) ok = __all_sync(0xffffffffu, bounded_wait(it_done, (T_iter - 1) & 1, abort_flag, 526, p.err));
-    if (ok) {
-      // group 0 writes dV, group 1 writes dK (TMEM loads by every lane,
-      // stores only for rows inside the sequence)
-      tc_fence_after();
-      const bool valid = kvp < p.s;
-      const uint32_t tsrc = (grp == 0 ? tdV : tdK) + ((uint32_t)(quarter * 32) << 16);
-      __nv_bfloat16* row = p.dqkv + ((long long)bi * p.s + kvp) * p.ld_dqkv +
-                           (grp == 0 ? p.dv_col : p.dk_col) + (long long)g * D;
-      const float sc = grp == 0 ? 1.f : p.scale;
-      uint32_t acc[D];
-#pragma unroll
-      for (int cc = 0; cc < D / 16; ++cc) tmem_ld16_nw(tsrc + cc * 16, acc + cc * 16);
-      tmem_wait_ld(acc);
-      if (valid) {
-#pragma unroll
-        for (int cc = 0; cc < D / 16; ++cc) store_row16(row + cc * 16, acc + cc * 16, sc);
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 1) {
-    __syncwarp();
-    tmem_dealloc(tmem, 512);
-  }
-}
-
-// ===========================================================================
-// dK / dV with every A operand in TMEM (head dims 64 and 80)
-// ===========================================================================
 // A 128 x 128 product with both operands in shared memory takes the whole
 // shared-memory bandwidth of the SM, and the compute warps' own shared-memory
-// loads then wait behind it.  This variant gives every product at most one
-// shared-memory operand: K and V are copied into TMEM once per CTA and serve
-// as the A operands of S^T = K Q^T and dP^T = V dO^T; P^T is written over
-// S^T and dS^T over dP^T (bf16 pairs), the A operands of dV = P^T dO and
-// dK = dS^T Q.  Shared memory holds only the Q/dO ring.
+// loads then wait behind it.  So P^T is written over S^T and dS^T over dP^T
+// in TMEM (bf16 pairs), the A operands of dV = P^T dO and dK = dS^T Q, and
+// the compute warps touch no shared memory at all.  For head dims 64 and 80
+// K and V are also copied into TMEM once per CTA as the A operands of
+// S^T = K Q^T and dP^T = V dO^T, so no product has more than one
+// shared-memory operand.  For 96 to 128, dV and dK take 2D TMEM columns and
+// the double-buffered S^T and dP^T the other 256, so K and V stay in shared
+// memory (loaded once per CTA) and those two products read both operands
+// from there.
 // The per-query-column terms of the softmax gradient (-LSE and -D) enter
 // through the products too: one more contraction step multiplies a 16-column
-// chunk appended to K (1, 1, 0, ...) or V (0, 0, 1, 1, 0, ...) in TMEM with
-// the query row (hi(-LSE*sqrt(d)), lo(..), hi(-D), lo(-D), 0, ...), so S^T
-// comes out offset by -LSE*sqrt(d) and dP^T by -D: the compute warps read no
-// per-column values from shared memory, whose bandwidth the products already
-// use.  The row's 8 nonzero-capable columns arrive with the Q/dO stage
-// (16 bytes per query, unswizzled: exactly the K-major core-matrix layout);
-// the descriptor points its upper 8 columns at one shared 2 KB of zeros.
-// TMEM: dV [256, 256+D), dK [256+D, 256+2D), K' [256+2D, 256+2.5D+8),
-// V' [.., 256+3D+16); shared memory: QS stages of (Q, dO, the 128 query rows'
+// chunk appended to K (1, 1, 0, ...) or V (0, 0, 1, 1, 0, ...) with the query
+// row (hi(-LSE*sqrt(d)), lo(..), hi(-D), lo(-D), 0, ...), so S^T comes out
+// offset by -LSE*sqrt(d) and dP^T by -D: the compute warps read no
+// per-column values from shared memory.  The row's 8 nonzero-capable columns
+// arrive with the Q/dO stage (16 bytes per query, unswizzled: exactly the
+// K-major core-matrix layout); the descriptor points its upper 8 columns at
+// one shared 2 KB of zeros.  K's and V's own extra chunks sit in TMEM beside
+// them, or (head dims above 80) in shared memory in the same unswizzled
+// layout, written by the compute warps.
+// TMEM: dV [256, 256+D), dK [256+D, 256+2D), and for head dims 64 and 80
+// K' [256+2D, 256+2.5D+8), V' [.., 256+3D+16).  Shared memory: (above 80) K,
+// V and their extra chunks, then QS stages of (Q, dO, the 128 query rows'
 // 16-byte extra rows), then the zeros.
 template <int D>
 struct DkdvTmCfg {
   using T = TileGeom<D>;
-  static constexpr int QS = 4;
-  static constexpr int AUX = 128 * 16;                 // 128 query rows x 8 bf16
+  // K and V are TMEM operands where their columns fit beside dV and dK (head
+  // dims up to 80); above that they stay in shared memory, with their extra
+  // chunks
+  static constexpr bool KV_TMEM = D <= 80;
+  static constexpr int AUX = 128 * 16;                 // 128 rows x 8 bf16
+  static constexpr int KV = KV_TMEM ? 0 : 2 * T::TILE + 2 * AUX;  // K, V, K extra, V extra
   static constexpr int STAGE = 2 * T::TILE + AUX;      // Q, dO, extra rows
   static constexpr int ZERO = 2048;                    // the upper 8 columns
-  static constexpr int SMEM = QS * STAGE + ZERO + 1024 + 256;
+  static constexpr int QS_FIT = (232448 - KV - ZERO - 1024 - 256) / STAGE;
+  static constexpr int QS = QS_FIT > 4 ? 4 : QS_FIT;
+  static constexpr int SMEM = KV + QS * STAGE + ZERO + 1024 + 256;
   static constexpr uint32_t COL_DV = 256, COL_DK = 256 + D, COL_K = 256 + 2 * D, COL_V = 256 + 2 * D + D / 2 + 8;
 };
 
@@ -443,16 +134,19 @@ __global__ void __launch_bounds__(352, 1) attn_dkdv_hs_kernel(const __grid_const
   using C = DkdvTmCfg<D>;
   constexpr int QS = C::QS;
   constexpr int STAGE = C::STAGE;
-  static_assert(C::COL_V + D / 2 + 8 <= 512, "TMEM columns");
+  static_assert(C::COL_DK + D <= 512, "TMEM columns");
+  static_assert(!C::KV_TMEM || C::COL_V + D / 2 + 8 <= 512, "TMEM columns");
+  static_assert(QS >= 2, "Q/dO ring");
   constexpr uint32_t ID_S = idesc_bf16(128, 64, false, false);
   constexpr uint32_t ID_KV = idesc_bf16(128, D, false, true);
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sStage = smem;
+  uint8_t* sKV = smem;                  // K, V, their extra chunks (head dims above 80)
+  uint8_t* sStage = smem + C::KV;
   uint8_t* sZero = sStage + QS * STAGE;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sZero + C::ZERO);
-  uint64_t* kv_ready = bars;            // K', V' in TMEM, dV, dK zeroed (8 compute warps)
+  uint64_t* kv_ready = bars;            // K', V' in place, dV, dK zeroed (8 compute warps)
   uint64_t* qdo_full = bars + 1;        // [QS]
   uint64_t* qdo_empty = qdo_full + QS;  // [QS], both issuers
   uint64_t* s_full = qdo_empty + QS;    // [2] S^T(u) in buffer u % 2
@@ -461,7 +155,8 @@ __global__ void __launch_bounds__(352, 1) attn_dkdv_hs_kernel(const __grid_const
   uint64_t* ds_full = p_full + 2;       // [2] dS^T(u) written (4 warps)
   uint64_t* all_done = ds_full + 2;     // both issuers' last products done
   uint64_t* drain = all_done + 1;       // [2], one per issuer
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 2);
+  uint64_t* kv_full = drain + 2;        // K, V tiles landed (shared-memory variant)
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(kv_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = warp_id();
@@ -492,6 +187,7 @@ __global__ void __launch_bounds__(352, 1) attn_dkdv_hs_kernel(const __grid_const
       mbar_init(&drain[b], 1);
     }
     mbar_init(all_done, 2);
+    mbar_init(kv_full, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -522,6 +218,15 @@ __global__ void __launch_bounds__(352, 1) attn_dkdv_hs_kernel(const __grid_const
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------ TMA producer
+      if constexpr (!C::KV_TMEM) {
+        mbar_expect_tx(kv_full, 2 * T::TILE);
+#pragma unroll
+        for (int c = 0; c < T::NCH; ++c) {
+          tma_load_3d(sKV + c * T::CHUNK, &p.map_qkv, kv_full, p.k_col + g * D + c * T::CW, j * 128, bi);
+          tma_load_3d(sKV + T::TILE + c * T::CHUNK, &p.map_qkv, kv_full, p.v_col + g * D + c * T::CW, j * 128,
+                      bi);
+        }
+      }
       int issued = 0;
       for (int t = 0; t < T_iter; ++t) {
         const int st = t % QS;
@@ -541,8 +246,9 @@ __global__ void __launch_bounds__(352, 1) attn_dkdv_hs_kernel(const __grid_const
         issued = t + 1;
       }
       if (*abort_flag) {
+        if constexpr (!C::KV_TMEM) drain_wait(kv_full, 0);
         for (int t = (issued > QS ? issued - QS : 0); t < issued; ++t)
-          bounded_wait(&qdo_full[t % QS], (t / QS) & 1, abort_flag, 632, p.err);
+          drain_wait(&qdo_full[t % QS], (t / QS) & 1);
       }
     }
   } else if (warp == 1 || warp == 10) {
@@ -555,27 +261,46 @@ __global__ void __launch_bounds__(352, 1) attn_dkdv_hs_kernel(const __grid_const
       // chunk of the stage's tiles (whole swizzle atoms), and 64 b rows into
       // its extra rows
       auto stage_u = [&](int u) { return smem_u32(sStage + ((u >> 1) % QS) * STAGE); };
+      // K, V and their extra chunks in shared memory (head dims above 80):
+      // the extra chunk is 128 rows of 16 bytes, K-major core matrices
+      // without swizzle, its upper 8 columns the zeros
+      const uint32_t uK = smem_u32(sKV), uV = uK + T::TILE;
+      const uint32_t uKx = uK + 2 * T::TILE, uVx = uKx + C::AUX;
       auto issue_s = [&](int u) {
         const uint32_t uQ = stage_u(u) + 64 * T::SWB * b;
         const uint32_t uA = stage_u(u) + 2 * T::TILE + 64 * 16 * b;
+        if constexpr (C::KV_TMEM) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a(tSb, tKA + kk * 8, T::kmajor(uQ, kk), ID_S, kk > 0);
-        umma_bf16_tmem_a(tSb, tKA + D / 2, sdesc(uA, uZero - uA, 128, 0u), ID_S, 1);
+          for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a(tSb, tKA + kk * 8, T::kmajor(uQ, kk), ID_S, kk > 0);
+          umma_bf16_tmem_a(tSb, tKA + D / 2, sdesc(uA, uZero - uA, 128, 0u), ID_S, 1);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) umma_bf16(tSb, T::kmajor(uK, kk), T::kmajor(uQ, kk), ID_S, kk > 0);
+          umma_bf16(tSb, sdesc(uKx, uZero - uKx, 128, 0u), sdesc(uA, uZero - uA, 128, 0u), ID_S, 1);
+        }
         umma_commit(&s_full[b]);
       };
       auto issue_dp = [&](int u) {
         const uint32_t udO = stage_u(u) + T::TILE + 64 * T::SWB * b;
         const uint32_t uA = stage_u(u) + 2 * T::TILE + 64 * 16 * b;
+        if constexpr (C::KV_TMEM) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a(tdPb, tVA + kk * 8, T::kmajor(udO, kk), ID_S, kk > 0);
-        umma_bf16_tmem_a(tdPb, tVA + D / 2, sdesc(uA, uZero - uA, 128, 0u), ID_S, 1);
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_bf16_tmem_a(tdPb, tVA + kk * 8, T::kmajor(udO, kk), ID_S, kk > 0);
+          umma_bf16_tmem_a(tdPb, tVA + D / 2, sdesc(uA, uZero - uA, 128, 0u), ID_S, 1);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) umma_bf16(tdPb, T::kmajor(uV, kk), T::kmajor(udO, kk), ID_S, kk > 0);
+          umma_bf16(tdPb, sdesc(uVx, uZero - uVx, 128, 0u), sdesc(uA, uZero - uA, 128, 0u), ID_S, 1);
+        }
         umma_commit(&dp_full[b]);
       };
       auto wait_stage = [&](int u) {
         const int t = u >> 1;
         return bounded_wait(&qdo_full[t % QS], (t / QS) & 1, abort_flag, 641, p.err);
       };
-      bool ok = bounded_wait(kv_ready, 0, abort_flag, 642, p.err) && wait_stage(b);
+      bool ok = bounded_wait(kv_ready, 0, abort_flag, 642, p.err) &&
+                (C::KV_TMEM || bounded_wait(kv_full, 0, abort_flag, 646, p.err)) && wait_stage(b);
       if (ok) {
         tc_fence_after();
         issue_s(b);
@@ -612,7 +337,7 @@ __global__ void __launch_bounds__(352, 1) attn_dkdv_hs_kernel(const __grid_const
       if (ok) umma_commit(all_done);
       if (!ok) {
         umma_commit(&drain[b]);
-        bounded_wait(&drain[b], 0, abort_flag, 645, p.err);
+        drain_wait(&drain[b], 0);
       }
     }
   } else {
@@ -623,7 +348,24 @@ __global__ void __launch_bounds__(352, 1) attn_dkdv_hs_kernel(const __grid_const
     const int r = quarter * 32 + lane;
     const int kvp = j * 128 + r;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    {
+    if constexpr (!C::KV_TMEM) {
+      // the extra chunk of this thread's K row (group 0: 1, 1 in columns 0,
+      // 1) or V row (group 1: in columns 2, 3), which pick the (hi, lo)
+      // pairs of the query's extra row; and the group's accumulator (dV,
+      // dK) zeroed: both issuers add into it
+      reinterpret_cast<uint4*>(sKV + 2 * T::TILE + b * C::AUX)[r] =
+          b ? make_uint4(0u, 0x3F803F80u, 0u, 0u) : make_uint4(0x3F803F80u, 0u, 0u, 0u);
+      fence_proxy_async_smem();
+      uint32_t z[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) z[c] = 0u;
+#pragma unroll
+      for (int cc = 0; cc < D / 16; ++cc) tmem_st16_nw((b ? tdK : tdV) + lane_off + cc * 16, z);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(kv_ready);
+    } else {
       // K (group 0) or V (group 1) row of this thread into TMEM as bf16
       // pairs with the extra chunk (rows past the sequence are zero), and
       // the group's accumulator (dV, dK) zeroed: both issuers add into it
@@ -721,13 +463,22 @@ __global__ void __launch_bounds__(352, 1) attn_dkdv_hs_kernel(const __grid_const
       __nv_bfloat16* row = p.dqkv + ((long long)bi * p.s + kvp) * p.ld_dqkv +
                            (b == 0 ? p.dv_col : p.dk_col) + (long long)g * D;
       const float sc = b == 0 ? 1.f : p.scale;
-      uint32_t acc[D];
+      if constexpr (D <= 80) {
+        uint32_t acc[D];
 #pragma unroll
-      for (int cc = 0; cc < D / 16; ++cc) tmem_ld16_nw(tsrc + cc * 16, acc + cc * 16);
-      tmem_wait_ld(acc);
-      if (valid) {
+        for (int cc = 0; cc < D / 16; ++cc) tmem_ld16_nw(tsrc + cc * 16, acc + cc * 16);
+        tmem_wait_ld(acc);
+        if (valid) {
 #pragma unroll
-        for (int cc = 0; cc < D / 16; ++cc) store_row16(row + cc * 16, acc + cc * 16, sc);
+          for (int cc = 0; cc < D / 16; ++cc) store_row16(row + cc * 16, acc + cc * 16, sc);
+        }
+      } else {
+        for (int cc = 0; cc < D / 16; ++cc) {
+          uint32_t v[16];
+          tmem_ld16_nw(tsrc + cc * 16, v);
+          tmem_wait_ld(v);
+          if (valid) store_row16(row + cc * 16, v, sc);
+        }
       }
     }
   }
@@ -859,7 +610,7 @@ __global__ void __launch_bounds__(352, 1) attn_dq_hs_kernel(const __grid_constan
       }
       if (*abort_flag) {
         for (int jt = (issued > KVS ? issued - KVS : 0); jt < issued; ++jt)
-          bounded_wait(&kv_full[jt % KVS], (jt / KVS) & 1, abort_flag, 662, p.err);
+          drain_wait(&kv_full[jt % KVS], (jt / KVS) & 1);
       }
     }
   } else if (warp == 1 || warp == 10) {
@@ -918,7 +669,7 @@ __global__ void __launch_bounds__(352, 1) attn_dq_hs_kernel(const __grid_constan
       if (ok) umma_commit(all_done);
       if (!ok) {
         umma_commit(&drain[b]);
-        bounded_wait(&drain[b], 0, abort_flag, 675, p.err);
+        drain_wait(&drain[b], 0);
       }
     }
   } else {
@@ -1038,20 +789,6 @@ __global__ void __launch_bounds__(352, 1) attn_dq_hs_kernel(const __grid_constan
 }
 
 template <int D>
-int launch_dkdv(AttnBwdParams& prm, int grid, cudaStream_t st) {
-  constexpr int SMEM = DkdvCfg<D>::SMEM;
-  static_assert(SMEM <= 232448, "dK/dV tile set exceeds shared memory");
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(attn_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
-      return 3;
-    attr = true;
-  }
-  attn_dkdv_kernel<D><<<grid, 320, SMEM, st>>>(prm);
-  return cudaGetLastError() == cudaSuccess ? 0 : 3;
-}
-
-template <int D>
 int launch_dkdv_hs(AttnBwdParams& prm, int grid, cudaStream_t st) {
   constexpr int SMEM = DkdvTmCfg<D>::SMEM;
   static_assert(SMEM <= 232448, "dK/dV tile set exceeds shared memory");
@@ -1087,10 +824,7 @@ int launch_both(AttnBwdParams& prm, const AttnShape& f, cudaStream_t st) {
     // S, dP, dV, dK over the unmasked pairs
     ProfScope prof(PROF_ATTN_BWD, 8.0 * f.d * pairs * f.H * f.b, 0.0, st);
     const int grid = ((f.s + 127) / 128) * f.Hkv * f.b;
-    if constexpr (D <= 80)
-      rc = launch_dkdv_hs<D>(prm, grid, st);
-    else
-      rc = launch_dkdv<D>(prm, grid, st);
+    rc = launch_dkdv_hs<D>(prm, grid, st);
   }
   if (rc) return rc;
   // dQ only: the S and dP this kernel rebuilds for its query-major order are

@@ -34,25 +34,6 @@ struct TileGeom {
   }
 };
 
-// A [128 x 128] bf16 tile written by threads (P, P^T, dS^T): two 64-column
-// chunks of [128 rows x 128 B], 128-byte swizzle.
-struct SqTile {
-  static constexpr int BYTES = 128 * 128 * 2;
-  // byte offset of columns 8*c .. 8*c+7 of row r
-  static __device__ __forceinline__ uint32_t off(int r, int c) {
-    return (uint32_t)((c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-  }
-  // K-major use (contraction along the columns): 16 columns from 16*kk
-  static __device__ __forceinline__ uint64_t kmajor(uint32_t tile, int kk) {
-    return sdesc(tile + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, 2u);
-  }
-  // MN-major use (contraction along the rows, the columns are M or N): 16
-  // rows from 16*kk
-  static __device__ __forceinline__ uint64_t mnmajor(uint32_t tile, int kk) {
-    return sdesc(tile + kk * 16 * 128, 16384, 1024, 2u);
-  }
-};
-
 // 16 TMEM fp32 columns of this thread's row -> 16 bf16 values (scaled)
 __device__ __forceinline__ void store_row16(__nv_bfloat16* dst, const uint32_t* v, float sc) {
   uint4 a, b;

@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
       }
       if (*abort_flag) {
         for (int j = (issued > KVS ? issued - KVS : 0); j < issued; ++j)
-          bounded_wait(&kv_full[j % KVS], (j / KVS) & 1, abort_flag, 202, p.err);
+          drain_wait(&kv_full[j % KVS], (j / KVS) & 1);
       }
     }
   } else if (warp == 1) {
@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
       }
       if (!ok) {
         umma_commit(drain);
-        bounded_wait(drain, 0, abort_flag, 215, p.err);
+        drain_wait(drain, 0);
       }
     }
   } else {
@@ -498,7 +498,7 @@ __global__ void __launch_bounds__(352, 1) attn_fwd_sk_kernel(const __grid_consta
       }
       if (*abort_flag) {
         for (int j = (issued > KVS ? issued - KVS : 0); j < issued; ++j)
-          bounded_wait(&kv_full[j % KVS], (j / KVS) & 1, abort_flag, 232, p.err);
+          drain_wait(&kv_full[j % KVS], (j / KVS) & 1);
       }
     }
   } else if (warp == 1 || warp == 10) {
@@ -535,7 +535,7 @@ __global__ void __launch_bounds__(352, 1) attn_fwd_sk_kernel(const __grid_consta
       }
       if (!ok) {
         umma_commit(&drain[b]);
-        bounded_wait(&drain[b], 0, abort_flag, 236, p.err);
+        drain_wait(&drain[b], 0);
       }
     }
   } else {

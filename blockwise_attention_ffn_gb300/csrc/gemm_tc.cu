@@ -508,8 +508,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       if (*abort_flag) {
         // let every load this thread issued land before the CTA goes away
         for (uint32_t j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
-          bounded_wait(&full[j % STAGES], (j / STAGES) & 1, abort_flag, 102, p.err) ||
-              mbar_try_wait(&full[j % STAGES], (j / STAGES) & 1);
+          drain_wait(&full[j % STAGES], (j / STAGES) & 1);
       }
     }
   } else if (warp == 1) {
@@ -558,7 +557,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       }
       if (!ok) {
         umma_commit(drain);  // wait until nothing issued is still in flight
-        bounded_wait(drain, 0, abort_flag, 104, p.err) || mbar_try_wait(drain, 0);
+        drain_wait(drain, 0);
       }
     }
   } else {

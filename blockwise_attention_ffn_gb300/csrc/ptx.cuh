@@ -82,6 +82,17 @@ __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, vol
   }
 }
 
+// Waits for phase `parity` of `bar` on the way out of an aborted kernel:
+// copies and products already issued must land before the shared memory or
+// TMEM they use is released, so unlike bounded_wait this ignores *abort.  It
+// still gives up after BPT_WAIT_CYCLES (the failure is already recorded).
+__device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > BPT_WAIT_CYCLES) return false;
+  return true;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -792,12 +792,8 @@ template <int D>
 int launch_dkdv_hs(AttnBwdParams& prm, int grid, cudaStream_t st) {
   constexpr int SMEM = DkdvTmCfg<D>::SMEM;
   static_assert(SMEM <= 232448, "dK/dV tile set exceeds shared memory");
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(attn_dkdv_hs_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
-      return 3;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};  // devices whose limit is set
+  if (smem_limit_once(reinterpret_cast<const void*>(attn_dkdv_hs_kernel<D>), SMEM, &attr)) return 3;
   attn_dkdv_hs_kernel<D><<<grid, 352, SMEM, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
@@ -806,12 +802,8 @@ template <int D>
 int launch_dq(AttnBwdParams& prm, int grid, cudaStream_t st) {
   constexpr int SMEM = DqCfg<D>::SMEM;
   static_assert(SMEM <= 232448, "dQ tile set exceeds shared memory");
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(attn_dq_hs_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
-      return 3;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};  // devices whose limit is set
+  if (smem_limit_once(reinterpret_cast<const void*>(attn_dq_hs_kernel<D>), SMEM, &attr)) return 3;
   attn_dq_hs_kernel<D><<<grid, 352, SMEM, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }

@@ -710,12 +710,8 @@ template <int D>
 int launch_fwd_sk(AttnFwdParams& prm, int grid, cudaStream_t st) {
   constexpr int SMEM = FwdSkCfg<D>::SMEM;
   static_assert(SMEM <= 232448, "attention forward tile set exceeds shared memory");
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(attn_fwd_sk_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
-      return 3;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};  // devices whose limit is set
+  if (smem_limit_once(reinterpret_cast<const void*>(attn_fwd_sk_kernel<D>), SMEM, &attr)) return 3;
   attn_fwd_sk_kernel<D><<<grid, 352, SMEM, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
@@ -724,12 +720,8 @@ template <int D>
 int launch_fwd(AttnFwdParams& prm, int grid, cudaStream_t st) {
   constexpr int SMEM = FwdCfg<D>::SMEM;
   static_assert(SMEM <= 232448, "attention forward tile set exceeds shared memory");
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
-      return 3;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};  // devices whose limit is set
+  if (smem_limit_once(reinterpret_cast<const void*>(attn_fwd_kernel<D>), SMEM, &attr)) return 3;
   attn_fwd_kernel<D><<<grid, 192, SMEM, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }

@@ -636,12 +636,8 @@ int launch(GemmParams& p, cudaStream_t st) {
   constexpr int B_BYTES = (DUAL ? 2 : 1) * BN * BK * 2;
   constexpr int SMEM = STAGES * (A_BYTES + B_BYTES) + 1024 + 256;
   auto kern = gemm_kernel<BN, A_MN, B_MN, DUAL>;
-  static bool attr_set = false;  // per instantiation
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
-      return 3;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr{0};  // per instantiation: devices whose limit is set
+  if (smem_limit_once(reinterpret_cast<const void*>(kern), SMEM, &attr)) return 3;
   const int nsm = sm_count();
   if (nsm <= 0) return 3;
   p.mt = (p.M + BM - 1) / BM;

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace bpt {
 
 // ---------------------------------------------------------------- profiling
@@ -24,6 +26,20 @@ unsigned int* device_error_word();
 int read_device_error(cudaStream_t st, unsigned int out[4]);
 // streaming multiprocessors of the current device (0 on error), cached per device
 int sm_count();
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per device (the attribute belongs to the kernel's instance in
+// that device's context).  `done` is the caller's per-kernel bit mask of
+// devices already set.  Returns 0 on success, 3 (BPT_ECUDA) on failure.
+inline int smem_limit_once(const void* kernel, int bytes, std::atomic<uint64_t>* done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 3;
+  const uint64_t bit = uint64_t(1) << dev;
+  if (done->load(std::memory_order_acquire) & bit) return 0;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return 3;
+  done->fetch_or(bit, std::memory_order_release);
+  return 0;
+}
 
 // ---------------------------------------------------------------- TMA maps
 // 2-D bf16 (or fp32) tensor map over a row-major matrix view [rows, cols]

@@ -78,3 +78,34 @@ def test_step_flops_reduce_to_page_estimate():
 def test_gpt_params_identity(h):
     cfg = LayerCfg(s=8, h=h, n_heads=h // 64, n_kv_heads=h // 64, head_dim=64, ffn_dim=4 * h)
     assert A.param_count(cfg) == 12 * h * h + 13 * h
+
+
+@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c4", "c5"])
+def test_bench_flop_count_matches_oracle_accounting(name):
+    """The bench's FLOP count (the headline metric's numerator) against the
+    oracle's page-pinned formulas.  The bench counts causal pairs exactly,
+    s (s + 1) / 2 per head instead of s^2 / 2, so the attention terms differ by
+    a factor (1 + 1/s); the head-chunked workload also re-projects Q/K/V for
+    the backward, an executed extra the oracle's step estimate does not have."""
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    from blockwise_attention_ffn_gb300.presets import PRESETS
+    from tests.oracle_helpers import oracle_cfg
+    c = PRESETS[name]
+    got = bench.flop_counts(c)
+    want = A.step_flops(oracle_cfg(c))
+    exact = 1 + 1 / c.s
+    assert got["linear"] == want["linear"]
+    assert got["attn"] == pytest.approx(want["attn"] * exact, rel=1e-12)
+    assert got["forward"] == pytest.approx(want["linear"] + want["attn"] * exact, rel=1e-12)
+    if not c.backward:
+        assert got["executed"] == got["forward"]
+        return
+    assert got["model"] == pytest.approx(3 * got["forward"], rel=1e-12)
+    extra = 0
+    if c.head_chunk and c.head_chunk < c.n_heads:
+        extra = want["qkv"]
+    want_exec = (2 * want["forward"] - want["fc2"] + 2 * want["linear"] + 2.5 * want["attn"]
+                 + (2 + 2.5) * want["attn"] * (exact - 1) + extra)
+    assert got["executed"] == pytest.approx(want_exec, rel=1e-12)

@@ -117,3 +117,15 @@ def test_missing_weight_rejected(built):
     w = bpt.BptWeights(*ptrs)
     assert L.bpt_layer_fwd(ctypes.byref(c), ctypes.byref(w), 1 << 20, 1 << 20, None, 1 << 20,
                            1 << 40, None) == bpt.BPT_EINVAL
+
+
+def test_attention_rows_beyond_int32_unsupported(built):
+    """b * H * s_pad past 2^31 - 1 would overflow the extra rows' TMA row
+    coordinate: the attention backward refuses it before any launch."""
+    L = bpt.lib()
+    s = (1 << 24) + 128                      # 128 heads x s_pad = 2^31 + 2^14
+    cfg = presets.C1.with_(s=s, h=8192, n_heads=128, n_kv_heads=128, head_dim=64, ffn_dim=8192)
+    c = bpt.make_config(cfg)
+    p = 1 << 20
+    rc = L.bpt_attention_bwd(ctypes.byref(c), p, p, p, p, p, p, 1 << 62, None)
+    assert rc == bpt.BPT_EUNSUPPORTED

@@ -119,3 +119,44 @@ def test_accumulate_flag_adds_to_existing_gradients():
         if v is not None:
             assert_close(to64(grads[k]), 2 * to64(v), k, max_abs=1e-3 * max(1, float(v.abs().max())),
                          rel_fro=1e-5, bf16_out=False)
+
+
+def causal_prefix_mean(v, n_heads, n_kv_heads, d):
+    """O of uniform causal attention: row i of query head n is the mean of
+    rows 0..i of its key/value head n // G (v: [s, H_kv * d])."""
+    g = n_heads // n_kv_heads
+    cum = np.cumsum(v, axis=0) / np.arange(1, v.shape[0] + 1)[:, None]
+    return np.concatenate([cum[:, (n // g) * d:(n // g + 1) * d] for n in range(n_heads)], axis=1)
+
+
+def test_zero_query_projection_gives_uniform_causal_attention():
+    """Wq = 0 makes every score zero, so each query attends uniformly to its
+    causal prefix: O_i = mean of V_0..V_i and LSE_i = ln(i + 1).  A closed
+    form that needs no oracle; grouped-query heads and head chunks included."""
+    cfg = LLAMA_SMALL
+    inp, dev = device_inputs(cfg, seed=16, with_dy=False)
+    dev["weights"]["wq"].zero_()
+    H, d = cfg.n_heads, cfg.head_dim
+    o = torch.zeros(cfg.b * cfg.s, H * d, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(cfg.b, H, bpt.s_pad(cfg), dtype=torch.float32, device="cuda")
+    ws = bpt.alloc_bytes(bpt.bpt_workspace_bytes(cfg, bpt.BPT_PASS_HEADCHUNK))
+    bpt.bpt_attn_headchunk(cfg, dev["weights"], dev["x"], o, lse, ws)
+    torch.cuda.synchronize()
+    v = to64(inp["x"])[0] @ to64(inp["weights"]["wv"]).T
+    assert_close(to64(o), causal_prefix_mean(v, H, cfg.n_kv_heads, d), "O")
+    want_lse = np.tile(np.log(np.arange(1, cfg.s + 1, dtype=np.float64)), (H, 1))
+    assert_close(to64(lse)[0, :, :cfg.s], want_lse, "LSE", max_abs=LSE_MAX_ABS, rel_fro=LSE_REL_FRO,
+                 bf16_out=False)
+
+
+def test_zero_output_projection_and_fc1_leave_residual_plus_b2():
+    """Wo = bo = 0 removes the attention branch and W1 = b1 = 0 makes the
+    FFN GeLU(0) W2^T + b2 = b2, so y = x + b2: the fp32 residual sum rounded
+    once to bf16.  Every other element of the layer still runs."""
+    cfg = GPT_SMALL
+    inp, dev = device_inputs(cfg, seed=17, with_dy=False)
+    for k in ("wo", "bo", "w1", "b1"):
+        dev["weights"][k].zero_()
+    y, _ = run_fwd(cfg, dev)
+    want = to64(inp["x"]) + to64(inp["weights"]["b2"])
+    assert_close(to64(y), want, "y", max_abs=1e-6)

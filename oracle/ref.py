@@ -38,7 +38,17 @@ Readings of points the pages leave open (each is listed with its reason in the
 design notes): GeLU defaults to the erf form (act=0) with the tanh form as
 act=1 and SwiGLU as act=2; the score scale is 1/sqrt(head_dim); the causal mask
 keeps the diagonal; RMSNorm eps defaults to 1e-5 like LayerNorm; variance is
-the biased 1/h form; no dropout (p = 0); no positional encoding.
+the biased 1/h form; no dropout (p = 0); no positional encoding unless
+``rope_base`` is set.
+
+Rotary position embedding (``rope_base`` > 0, off by default): "Untied
+Ulysses: Memory-Efficient Context Parallelism via Headwise Chunking" lists
+fused RoPE among the per-layer kernels of its Llama runs and notes the fp32
+cast it needs, without giving the rotation.  Reading: the standard rotary
+embedding in the half-split layout Llama checkpoints use -- element i of a
+query or key head is paired with element i + d/2, and the pair at sequence
+position p is rotated by the angle p * base^(-2i/d) -- applied to Q and K
+after their projection (and bias), before the scores.
 """
 from __future__ import annotations
 
@@ -73,6 +83,7 @@ class LayerCfg:
     act: int = ACT_GELU_ERF
     has_bias: bool = True
     norm_eps: float = 1e-5
+    rope_base: float = 0.0  # 0: no positional encoding
 
     @property
     def group(self) -> int:
@@ -161,6 +172,29 @@ def norm_backward(dy, xhat, rstd, w, cfg: LayerCfg):
 
 
 # ----------------------------------------------------------------------------
+# rotary position embedding
+# ----------------------------------------------------------------------------
+
+def rope_freqs(d, base):
+    """Angular frequency of pair i (elements i and i + d/2): base^(-2i/d)."""
+    return base ** (-2.0 * np.arange(d // 2, dtype=F64) / d)
+
+
+def rope(x, base, inverse=False):
+    """Rotate every (i, i + d/2) pair of x [s, n, d] (row p = position p) by
+    the angle p * base^(-2i/d); inverse=True rotates by the negated angle,
+    which is the transpose of the rotation and so also its gradient."""
+    s_, _, d = x.shape
+    ang = np.arange(s_, dtype=F64)[:, None] * rope_freqs(d, base)[None, :]
+    c = np.cos(ang)[:, None, :]
+    sn = np.sin(ang)[:, None, :]
+    if inverse:
+        sn = -sn
+    a, b = x[..., : d // 2], x[..., d // 2:]
+    return np.concatenate([a * c - b * sn, a * sn + b * c], axis=-1)
+
+
+# ----------------------------------------------------------------------------
 # attention, materialised per head (rows processed in chunks so that an s x s
 # matrix for the whole sequence is never held at once; every chunk is the full
 # textbook softmax over its rows)
@@ -243,6 +277,9 @@ def attention_block(xn, W, cfg: LayerCfg):
     q = _split_heads(_lin(xn, W["wq"], W.get("bq")), H, d)
     k = _split_heads(_lin(xn, W["wk"], W.get("bk")), Hk, d)
     v = _split_heads(_lin(xn, W["wv"], W.get("bv")), Hk, d)
+    if cfg.rope_base:
+        q = rope(q, cfg.rope_base)
+        k = rope(k, cfg.rope_base)
     o = np.empty_like(q)
     lse = np.empty((H, xn.shape[0]), F64)
     for n in range(H):
@@ -335,6 +372,10 @@ def layer_backward(x, W, dy, cfg: LayerCfg):
             dq[:, n] += a_
             dk[:, gk] += b_
             dv[:, gk] += c_
+        if cfg.rope_base:
+            # back through the rotation (the cache holds the rotated q, k)
+            dq = rope(dq, cfg.rope_base, inverse=True)
+            dk = rope(dk, cfg.rope_base, inverse=True)
         dq = dq.reshape(dq.shape[0], -1)
         dk = dk.reshape(dk.shape[0], -1)
         dv = dv.reshape(dv.shape[0], -1)
@@ -393,6 +434,9 @@ def bpt_layer_forward(x, W, cfg: LayerCfg, c_q, c_kv):
         q = _split_heads(_lin(xn, W["wq"], W.get("bq")), H, d)
         k = _split_heads(_lin(xn, W["wk"], W.get("bk")), Hk, d)
         v = _split_heads(_lin(xn, W["wv"], W.get("bv")), Hk, d)
+        if cfg.rope_base:
+            q = rope(q, cfg.rope_base)
+            k = rope(k, cfg.rope_base)
         s_ = xb.shape[0]
         for q0 in range(0, s_, c_q):
             q1 = min(s_, q0 + c_q)

@@ -7,7 +7,9 @@ Python floats and explicit loops so that no array broadcasting, reshaping or
 library call is shared with the NumPy version.  Sources: "Training memory:
 model states, activations and checkpointing", section 3 (the layer and its
 parameters); "Blockwise Parallel Transformer for Long Context Large Models",
-section 3.4 (scaled dot-product attention, causal bias).
+section 3.4 (scaled dot-product attention, causal bias).  With a nonzero
+``rope_base`` the query and key heads are rotated as :func:`oracle.ref.rope`
+describes, pair by pair with ``math.cos`` / ``math.sin``.
 """
 from __future__ import annotations
 
@@ -49,6 +51,19 @@ def _silu(z):
     return z / (1.0 + math.exp(-z))
 
 
+def _rope_row(row, pos, nheads, d, base):
+    """Rotate element i of every head with element i + d/2 by pos * base^(-2i/d)."""
+    out = list(row)
+    half = d // 2
+    for n in range(nheads):
+        for i in range(half):
+            ang = pos * math.pow(base, -2.0 * i / d)
+            a, b = row[n * d + i], row[n * d + half + i]
+            out[n * d + i] = a * math.cos(ang) - b * math.sin(ang)
+            out[n * d + half + i] = a * math.sin(ang) + b * math.cos(ang)
+    return out
+
+
 def layer_forward(x, W, cfg):
     """x: nested list [b][s][h]; W: dict of nested lists (nn.Linear [out][in]);
     cfg: object with the oracle.ref.LayerCfg fields.  Returns nested list y."""
@@ -61,6 +76,10 @@ def layer_forward(x, W, cfg):
         q = [_matvec(W["wq"], xn[t], W.get("bq")) for t in range(s)]
         k = [_matvec(W["wk"], xn[t], W.get("bk")) for t in range(s)]
         v = [_matvec(W["wv"], xn[t], W.get("bv")) for t in range(s)]
+        base = getattr(cfg, "rope_base", 0.0)
+        if base:
+            q = [_rope_row(q[t], t, H, d, base) for t in range(s)]
+            k = [_rope_row(k[t], t, Hk, d, base) for t in range(s)]
         yb = []
         for i in range(s):
             o = [0.0] * (H * d)

@@ -5,7 +5,9 @@ residual, bias or norm term (parameter count, autograd, finite differences,
 FFN-zero invariant), a wrong scale or mask (identical keys, library
 attention), a wrong sign or transposed operand in the backward (finite
 differences, autograd), or broken online-softmax bookkeeping (blockwise ==
-vanilla, kv-order permutation)."""
+vanilla, kv-order permutation), and for the rotary embedding a wrong pairing,
+sign or frequency (complex-rotation form, offset-only scores) or a missing
+rotation in the backward (finite differences)."""
 import json
 import os
 
@@ -26,6 +28,8 @@ def _cfgs_small():
         LayerCfg(s=29, h=32, n_heads=4, n_kv_heads=2, head_dim=8, ffn_dim=40, norm=1, act=2,
                  has_bias=False),
         LayerCfg(s=21, h=24, n_heads=2, n_kv_heads=1, head_dim=12, ffn_dim=40, act=1, b=2),
+        LayerCfg(s=29, h=32, n_heads=4, n_kv_heads=2, head_dim=8, ffn_dim=40, norm=1, act=2,
+                 has_bias=False, rope_base=10000.0),
     ]
 
 
@@ -130,6 +134,50 @@ def test_norms_match_their_definition():
     assert np.allclose((y * y).mean(1), (x * x).mean(1) / ((x * x).mean(1) + 1e-5), atol=1e-12)
 
 
+# -------------------------------------------------- rotary position embedding
+
+@pytest.mark.parametrize("d,base", [(2, 10000.0), (8, 10000.0), (16, 500000.0), (12, 7.0)])
+def test_rope_is_a_complex_rotation(d, base):
+    """Element i and i + d/2 as the real and imaginary part of one complex
+    number, position p multiplies it by exp(j p base^(-2i/d)): position 0 is
+    the identity and every pair keeps its length."""
+    rng = np.random.default_rng(20)
+    s, n = 23, 3
+    x = rng.standard_normal((s, n, d))
+    z = x[..., : d // 2] + 1j * x[..., d // 2:]
+    freq = base ** (-np.arange(0, d, 2) / d)
+    w = z * np.exp(1j * np.arange(s)[:, None, None] * freq[None, None, :])
+    got = ref.rope(x, base)
+    assert np.max(np.abs(got[..., : d // 2] - w.real)) < 1e-12
+    assert np.max(np.abs(got[..., d // 2:] - w.imag)) < 1e-12
+    assert np.array_equal(got[0], x[0])
+    pair_len = np.hypot(got[..., : d // 2], got[..., d // 2:])
+    assert np.max(np.abs(pair_len - np.abs(z))) < 1e-12
+
+
+def test_rope_scores_depend_on_the_offset_only():
+    """With the same query and key vector at every position, the rotated
+    score q_m . k_n depends on m - n alone (the relative-position property)."""
+    rng = np.random.default_rng(21)
+    s, d = 19, 8
+    q = np.tile(rng.standard_normal((1, 1, d)), (s, 1, 1))
+    k = np.tile(rng.standard_normal((1, 1, d)), (s, 1, 1))
+    S = ref.rope(q, 100.0)[:, 0] @ ref.rope(k, 100.0)[:, 0].T
+    for off in range(-s + 1, s):
+        diag = np.diagonal(S, offset=off)
+        assert np.max(np.abs(diag - diag[0])) < 1e-12
+    assert np.ptp(np.diagonal(S, 0)) < 1e-12 and abs(S[1, 0] - S[0, 0]) > 1e-3
+
+
+def test_rope_inverse_is_its_transpose():
+    rng = np.random.default_rng(22)
+    x, y = rng.standard_normal((2, 17, 2, 8))
+    assert np.max(np.abs(ref.rope(ref.rope(x, 50.0), 50.0, inverse=True) - x)) < 1e-12
+    lhs = np.sum(ref.rope(x, 50.0) * y)
+    rhs = np.sum(x * ref.rope(y, 50.0, inverse=True))
+    assert abs(lhs - rhs) < 1e-10
+
+
 # -------------------------------------------------- scalar-loop cross-check
 
 @pytest.mark.parametrize("cfg", [
@@ -137,6 +185,8 @@ def test_norms_match_their_definition():
     LayerCfg(s=6, h=8, n_heads=2, n_kv_heads=1, head_dim=4, ffn_dim=12, norm=1, act=2,
              has_bias=False),
     LayerCfg(s=4, h=8, n_heads=2, n_kv_heads=2, head_dim=4, ffn_dim=12, act=1, causal=False, b=2),
+    LayerCfg(s=7, h=8, n_heads=2, n_kv_heads=1, head_dim=4, ffn_dim=12, norm=1, act=2,
+             has_bias=False, rope_base=10.0),
 ])
 def test_scalar_loop_oracle_matches(cfg):
     x, W, _ = rand_layer(cfg, seed=9)
@@ -169,9 +219,10 @@ def _fd_check(cfg, seed):
             Wm = dict(W); Wm[name] = w.copy(); Wm[name][idx] -= eps
             fd[idx] = (loss(x, Wp) - loss(x, Wm)) / (2 * eps)
         assert np.linalg.norm(fd - grads[name]) <= 1e-6 * np.linalg.norm(grads[name]) + 1e-9, name
-    if "bk" in grads:
+    if "bk" in grads and not cfg.rope_base:
         # softmax is shift-invariant along a row, so a bias added to every key
-        # cannot change the output: its gradient is exactly zero
+        # cannot change the output: its gradient is exactly zero (not so once
+        # the rotary embedding turns the bias differently at every position)
         assert np.max(np.abs(grads["bk"])) < 1e-12
 
 
@@ -180,6 +231,7 @@ def _fd_check(cfg, seed):
     LayerCfg(s=5, h=8, n_heads=2, n_kv_heads=2, head_dim=4, ffn_dim=12, causal=False, act=1),
     LayerCfg(s=6, h=8, n_heads=2, n_kv_heads=1, head_dim=4, ffn_dim=12, norm=1, act=2,
              has_bias=False),
+    LayerCfg(s=6, h=8, n_heads=2, n_kv_heads=1, head_dim=4, ffn_dim=12, rope_base=10.0),
 ])
 def test_backward_matches_finite_differences(cfg):
     _fd_check(cfg, seed=10)

@@ -322,6 +322,31 @@ def run_gpu(args, c):
     value = job_throughput(fl["executed"], world, ms)
     peaks = load_peaks()
 
+    # the two passes timed on their own, the same way (forward: K forward
+    # calls; backward: K backward calls on the log-sum-exp the last forward
+    # saved).  Supplementary: a failure here is reported, not raised.
+    passes = None
+    if c.backward:
+        try:
+            p0, p1, p2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            torch.cuda.synchronize()
+            p0.record(stream)
+            for _ in range(args.steps):
+                bpt.bpt_layer_fwd(c, W, x, y, saved, ws, stream)
+            p1.record(stream)
+            for _ in range(args.steps):
+                bpt.bpt_layer_bwd(c, W, x, saved, dy, dx, grads, ws, stream)
+            p2.record(stream)
+            torch.cuda.synchronize()
+            fwd_ms = max_over_ranks(p0.elapsed_time(p1) / args.steps, world, dev)
+            bwd_ms = max_over_ranks(p1.elapsed_time(p2) / args.steps, world, dev)
+            passes = {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+                      "fwd_tflops": job_throughput(fl["forward"], world, fwd_ms),
+                      "bwd_tflops": job_throughput(fl["executed"] - fl["forward"], world, bwd_ms),
+                      "note": "each pass timed alone over the same K calls; the step above runs both"}
+        except Exception as e:  # noqa: BLE001 - reported in the line
+            passes = {"error": repr(e)}
+
     # per-kernel breakdown of the same step (separate profiled steps).  These
     # run every kernel on one stream, so that no event span also covers
     # weight-gradient work overlapping on the backward's second stream.
@@ -403,7 +428,7 @@ def run_gpu(args, c):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "what": "pinned host x (and dy) copied in, fwd+bwd through the C ABI, dx copied out"},
             "gpu_launches": int(round(launches_per_step * args.steps)),
-            "roofline": roof, "kernels": kernels,
+            "roofline": roof, "kernels": kernels, "passes": passes,
             "memory": {"peak_device_bytes": peak_mem, "inputs_weights_grads_bytes": base_mem,
                        "workspace_bytes": ws_bytes, "saved_bytes": bpt.bpt_saved_bytes(c),
                        "vanilla_layer_activation_bytes_analytic": vanilla_activation_bytes(c)},

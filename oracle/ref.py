@@ -180,12 +180,14 @@ def rope_freqs(d, base):
     return base ** (-2.0 * np.arange(d // 2, dtype=F64) / d)
 
 
-def rope(x, base, inverse=False):
-    """Rotate every (i, i + d/2) pair of x [s, n, d] (row p = position p) by
-    the angle p * base^(-2i/d); inverse=True rotates by the negated angle,
-    which is the transpose of the rotation and so also its gradient."""
+def rope(x, base, inverse=False, positions=None):
+    """Rotate every (i, i + d/2) pair of x [s, n, d] by the angle
+    p * base^(-2i/d), p the row's position (row index, or ``positions``);
+    inverse=True rotates by the negated angle, which is the transpose of the
+    rotation and so also its gradient."""
     s_, _, d = x.shape
-    ang = np.arange(s_, dtype=F64)[:, None] * rope_freqs(d, base)[None, :]
+    p = np.arange(s_, dtype=F64) if positions is None else np.asarray(positions, F64)
+    ang = p[:, None] * rope_freqs(d, base)[None, :]
     c = np.cos(ang)[:, None, :]
     sn = np.sin(ang)[:, None, :]
     if inverse:

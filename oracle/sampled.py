@@ -15,6 +15,10 @@ take too long, two exact reductions of the same definition as
   only; and every weight gradient and dx follow exactly from those sparse
   pieces.  Nothing is approximated: the result equals the dense analytic
   backward of :func:`oracle.ref.layer_backward` for that dy.
+
+With ``rope_base`` set, query rows are rotated at their own positions and
+key rows at theirs, as :func:`oracle.ref.rope` defines, and the gradients go
+back through the transposed rotation.
 """
 from __future__ import annotations
 
@@ -23,7 +27,7 @@ from math import sqrt
 import numpy as np
 
 from .ref import (ACT_SWIGLU, F64, LayerCfg, _as64, _lin, ffn_forward, gelu_grad, norm_backward,
-                  norm_forward, silu, silu_grad)
+                  norm_forward, rope, silu, silu_grad)
 
 
 def _proj(xn, W, name, bias):
@@ -53,6 +57,9 @@ def forward_rows(x, W, cfg: LayerCfg, rows, batch=0):
     k = _proj(xn, W, "wk", "bk").reshape(s_, Hk, d)
     v = _proj(xn, W, "wv", "bv").reshape(s_, Hk, d)
     q = _proj(xn[rows], W, "wq", "bq").reshape(len(rows), H, d)
+    if cfg.rope_base:
+        k = rope(k, cfg.rope_base)
+        q = rope(q, cfg.rope_base, positions=rows)
     o = np.empty((len(rows), H, d), F64)
     for n in range(H):
         o[:, n], _ = _attn_rows(q[:, n], rows, k[:, n // G], v[:, n // G], cfg.causal, s_)
@@ -80,6 +87,9 @@ def backward_sparse_dy(x, W, dy_rows, rows, cfg: LayerCfg, batch=0):
     k = _proj(xn, W64, "wk", "bk").reshape(s_, Hk, d)
     v = _proj(xn, W64, "wv", "bv").reshape(s_, Hk, d)
     q = _proj(xn[rows], W64, "wq", "bq").reshape(R, H, d)
+    if cfg.rope_base:
+        k = rope(k, cfg.rope_base)
+        q = rope(q, cfg.rope_base, positions=rows)
     o = np.empty((R, H, d), F64)
     P = [None] * H
     for n in range(H):
@@ -135,6 +145,9 @@ def backward_sparse_dy(x, W, dy_rows, rows, cfg: LayerCfg, batch=0):
         dv[:, gk] += Pn.T @ do[:, n]
         dq[:, n] = dS @ k[:, gk] / sqrt(d)
         dk[:, gk] += dS.T @ q[:, n] / sqrt(d)
+    if cfg.rope_base:
+        dq = rope(dq, cfg.rope_base, inverse=True, positions=rows)
+        dk = rope(dk, cfg.rope_base, inverse=True)
     dqf = dq.reshape(R, H * d)
     dkf = dk.reshape(s_, Hk * d)
     dvf = dv.reshape(s_, Hk * d)

@@ -12,6 +12,9 @@ from tests.oracle_helpers import rand_layer
     LayerCfg(s=64, h=32, n_heads=4, n_kv_heads=2, head_dim=8, ffn_dim=48, norm=1, act=2,
              has_bias=False),
     LayerCfg(s=50, h=32, n_heads=4, n_kv_heads=4, head_dim=8, ffn_dim=64, causal=False, act=1),
+    LayerCfg(s=72, h=32, n_heads=4, n_kv_heads=2, head_dim=8, ffn_dim=48, norm=1, act=2,
+             has_bias=False, rope_base=500000.0),
+    LayerCfg(s=40, h=32, n_heads=4, n_kv_heads=4, head_dim=8, ffn_dim=64, rope_base=10.0),
 ])
 def test_sampled_forward_and_sparse_backward(cfg):
     x, W, dy = rand_layer(cfg, seed=12)

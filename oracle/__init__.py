@@ -13,4 +13,8 @@ product path (the CUDA library and its Python binding) never does.
   accounting formulas.
 * :mod:`oracle.sampled` -- row-sampled forward and sparse-upstream-gradient
   backward for sequence lengths where the dense oracle is too slow.
+* :mod:`oracle.lm_loss` -- the language-model loss after the last layer
+  (mean token cross-entropy through the vocabulary projection) and its
+  position- and vocabulary-blocked forms, for the blockwise-loss row that
+  comes next.
 """

@@ -134,8 +134,7 @@ struct BwdWs {
 AttnBwdShape stage_bwd_shape(const Dims& D, int64_t k);
 size_t plan_bwd(const Dims& D, void* base, BwdWs* w) {
   Carve c(base);
-  const bool swiglu_like = true;  // sized for the larger (SwiGLU) case
-  (void)swiglu_like;
+  // the FFN block buffers are sized for the larger (SwiGLU) case
   w->xn = c.take(D.rows * D.h * 2);
   w->qkv = c.take(D.rows * D.qkv_w * 2);
   w->o = c.take(D.rows * D.H * D.d * 2);

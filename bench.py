@@ -147,6 +147,19 @@ def load_traffic() -> dict:
     return {}
 
 
+# A rank that dies (or never arrives) must not leave the others waiting in a
+# collective forever: every collective of the bench's process group gives up
+# after this many seconds and raises.
+PG_TIMEOUT_S = 600
+
+
+def init_group(backend: str, timeout_s: float = PG_TIMEOUT_S):
+    import datetime
+
+    import torch.distributed as tdist
+    tdist.init_process_group(backend, timeout=datetime.timedelta(seconds=timeout_s))
+
+
 def dist_setup():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -262,7 +275,7 @@ def run_gpu(args, c):
 
     world, rank, local = dist_setup()
     if world > 1:
-        tdist.init_process_group("nccl")
+        init_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     bpt.lib()

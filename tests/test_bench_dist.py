@@ -74,3 +74,43 @@ def test_single_rank_needs_no_process_group():
     import bench
     assert bench.max_over_ranks(12.5, 1) == 12.5
     assert bench.job_throughput(2e12, 1, 10.0) == pytest.approx(200.0)
+
+
+def _failing_worker(rank, world, port, out_dir, mode):
+    """Rank 1 fails before the timing barrier -- it exits, or it stalls past
+    the group's timeout without joining; rank 0 must get an error from that
+    barrier within the (short) timeout instead of waiting."""
+    import time
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import bench
+    bench.init_group("gloo", timeout_s=5)
+    if rank == 1:
+        if mode == "stall":
+            time.sleep(8)    # never joins within the 5 s timeout
+        os._exit(3)          # the simulated failure: no barrier, no clean shutdown
+    t0 = time.perf_counter()
+    try:
+        tdist.barrier()
+        outcome = "returned"
+    except Exception as e:  # noqa: BLE001 - any error is the detection
+        outcome = type(e).__name__
+    with open(os.path.join(out_dir, "r0.json"), "w") as f:
+        json.dump({"outcome": outcome, "seconds": time.perf_counter() - t0}, f)
+    os._exit(0)
+
+
+@pytest.mark.parametrize("mode", ["exit", "stall"])
+def test_failed_rank_is_detected_within_the_timeout(tmp_path, mode):
+    world = 2
+    ctx = mp.get_context("spawn")
+    port = _free_port()
+    procs = [ctx.Process(target=_failing_worker, args=(r, world, port, str(tmp_path), mode)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert not p.is_alive(), "a rank hung"
+    res = json.load(open(tmp_path / "r0.json"))
+    assert res["outcome"] != "returned", res
+    assert res["seconds"] < 12, res

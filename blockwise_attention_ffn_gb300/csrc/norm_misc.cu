@@ -349,9 +349,13 @@ __global__ void dsum_kernel(int b, int s, int s_pad, int H, int d, const __nv_bf
   }
 }
 
+// blocks for a grid-stride loop over `work` items: enough for the work, at
+// most 16 per SM of the current device
 int grid_for(int64_t work, int per_block) {
+  const int nsm = sm_count();
+  const int64_t cap = (int64_t)(nsm > 0 ? nsm : 152) * 16;
   int64_t g = (work + per_block - 1) / per_block;
-  if (g > 152 * 16) g = 152 * 16;
+  if (g > cap) g = cap;
   return (int)(g < 1 ? 1 : g);
 }
 

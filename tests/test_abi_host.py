@@ -129,3 +129,31 @@ def test_attention_rows_beyond_int32_unsupported(built):
     p = 1 << 20
     rc = L.bpt_attention_bwd(ctypes.byref(c), p, p, p, p, p, p, 1 << 62, None)
     assert rc == bpt.BPT_EUNSUPPORTED
+
+
+def test_noalloc_entry_rejects_on_the_host(built):
+    """bpt_attention_bwd_noalloc classifies its arguments before touching the
+    device: bad pointers, bad configs and problems beyond its fixed scratch."""
+    L = bpt.lib()
+    p, odd = 1 << 20, (1 << 20) + 2
+    ok = bpt.make_config(presets.C1)
+    assert L.bpt_attention_bwd_noalloc(ctypes.byref(ok), None, p, p, p, p, None) == bpt.BPT_EINVAL
+    assert L.bpt_attention_bwd_noalloc(ctypes.byref(ok), p, p, p, odd, p, None) == bpt.BPT_EINVAL
+    bad = bpt.make_config(presets.C1.with_(q_block=64))
+    assert L.bpt_attention_bwd_noalloc(ctypes.byref(bad), p, p, p, p, p, None) == bpt.BPT_EINVAL
+    odd_d = bpt.make_config(presets.C1.with_(head_dim=72, h=288))
+    assert L.bpt_attention_bwd_noalloc(ctypes.byref(odd_d), p, p, p, p, p, None) == bpt.BPT_EUNSUPPORTED
+    big = presets.C1.with_(s=1 << 20, h=4096, n_heads=32, n_kv_heads=8, head_dim=128)
+    assert bpt.bpt_attention_bwd_workspace_bytes(big) > bpt.NOALLOC_SCRATCH_BYTES
+    cb = bpt.make_config(big)
+    assert L.bpt_attention_bwd_noalloc(ctypes.byref(cb), p, p, p, p, p, None) == bpt.BPT_ENOSPC
+
+
+def test_attention_entries_reject_bad_pointers_on_the_host(built):
+    L = bpt.lib()
+    c = bpt.make_config(presets.C1)
+    p, odd = 1 << 20, (1 << 20) + 2
+    assert L.bpt_attention_fwd(ctypes.byref(c), None, p, p, None) == bpt.BPT_EINVAL
+    assert L.bpt_attention_fwd(ctypes.byref(c), p, odd, p, None) == bpt.BPT_EINVAL
+    assert L.bpt_attention_bwd(ctypes.byref(c), p, p, p, p, p, p, 1024, None) == bpt.BPT_ENOSPC
+    assert L.bpt_attention_bwd(ctypes.byref(c), p, p, p, p, None, p, 1 << 40, None) == bpt.BPT_EINVAL

@@ -157,3 +157,31 @@ def test_attention_entries_reject_bad_pointers_on_the_host(built):
     assert L.bpt_attention_fwd(ctypes.byref(c), p, odd, p, None) == bpt.BPT_EINVAL
     assert L.bpt_attention_bwd(ctypes.byref(c), p, p, p, p, p, p, 1024, None) == bpt.BPT_ENOSPC
     assert L.bpt_attention_bwd(ctypes.byref(c), p, p, p, p, None, p, 1 << 40, None) == bpt.BPT_EINVAL
+
+
+def test_backward_and_headchunk_reject_missing_buffers(built):
+    L = bpt.lib()
+    c = bpt.make_config(presets.C1)
+    p = 1 << 20
+    w = bpt.BptWeights(*([p] * len(bpt.WEIGHT_FIELDS)))
+    g = bpt.BptGrads(*([p] * len(bpt.WEIGHT_FIELDS)))
+    args = (ctypes.byref(c), ctypes.byref(w), p, p, p, p, ctypes.byref(g), p, 1 << 40, None)
+    # every argument present but the workspace too small: ENOSPC, so the
+    # pointer checks below are what reject
+    small = list(args)
+    small[8] = 1024
+    assert L.bpt_layer_bwd(*small) == bpt.BPT_ENOSPC
+    for i in (2, 3, 4, 5, 7):                     # x, saved, dy, dx, ws
+        a = list(args)
+        a[i] = None
+        assert L.bpt_layer_bwd(*a) == bpt.BPT_EINVAL, i
+    gp = [p] * len(bpt.WEIGHT_FIELDS)
+    gp[bpt.WEIGHT_FIELDS.index("w1")] = None      # a weight gradient the layer has
+    a = list(args)
+    a[6] = ctypes.byref(bpt.BptGrads(*gp))
+    assert L.bpt_layer_bwd(*a) == bpt.BPT_EINVAL
+    wp = [p] * len(bpt.WEIGHT_FIELDS)
+    wp[bpt.WEIGHT_FIELDS.index("wk")] = None
+    assert L.bpt_attn_headchunk(ctypes.byref(c), ctypes.byref(bpt.BptWeights(*wp)), p, p, None, p, 1 << 40,
+                                None) == bpt.BPT_EINVAL
+    assert L.bpt_attn_headchunk(ctypes.byref(c), ctypes.byref(w), p, p, None, p, 1024, None) == bpt.BPT_ENOSPC

@@ -185,3 +185,19 @@ def test_backward_and_headchunk_reject_missing_buffers(built):
     assert L.bpt_attn_headchunk(ctypes.byref(c), ctypes.byref(bpt.BptWeights(*wp)), p, p, None, p, 1 << 40,
                                 None) == bpt.BPT_EINVAL
     assert L.bpt_attn_headchunk(ctypes.byref(c), ctypes.byref(w), p, p, None, p, 1024, None) == bpt.BPT_ENOSPC
+
+
+def test_profiler_calls_on_the_host(built):
+    """With nothing recorded the profiler needs no device: enable, list and
+    collect return empty results; bad arguments are rejected."""
+    L = bpt.lib()
+    bpt.bpt_profile_enable(True)
+    assert bpt.bpt_profile_list() == []
+    assert all(v["launches"] == 0 and v["ms"] == 0 for v in bpt.bpt_profile_collect().values())
+    bpt.bpt_profile_enable(False)
+    n = ctypes.c_double * 1
+    assert L.bpt_profile_collect(0, n(), n(), n(), (ctypes.c_int * 1)()) == bpt.BPT_EINVAL
+    assert L.bpt_profile_collect(1, None, n(), n(), (ctypes.c_int * 1)()) == bpt.BPT_EINVAL
+    assert L.bpt_profile_list(-1, None, None, None, None) == -bpt.BPT_EINVAL
+    assert L.bpt_profile_list(4, None, None, None, None) == -bpt.BPT_EINVAL
+    assert L.bpt_profile_list(0, None, None, None, None) == 0

@@ -447,7 +447,7 @@ def run_gpu(args, c):
                        "vanilla_layer_activation_bytes_analytic": vanilla_activation_bytes(c)},
         }
         if not args.no_cpu_baseline and world == 1:
-            line["cpu_baseline"] = cpu_baseline(c, args.ref_rows)
+            line["cpu_baseline"] = cpu_baseline(c, min(args.cpu_rows, c.s))
         print(json.dumps(line), flush=True)
     if world > 1:
         tdist.barrier()
@@ -496,7 +496,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="c3", help="c1..c5 (default c3, the s=32K workload)")
     ap.add_argument("--ref-rows", type=int, default=1024,
-                    help="positions of the workload the CPU oracle runs per sample")
+                    help="positions of the workload the CPU oracle runs per step of --impl reference")
+    ap.add_argument("--cpu-rows", type=int, default=4096,
+                    help="positions of the workload (at most s) in the cpu_baseline sample of the "
+                         "GPU run: about 10-15 s of fp64 work on 16 host cores at the s=32K workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-kernel", choices=["attn_fwd", "attn_bwd", "layer"], default=None,
                     help="run one launch of this component (small case for profiler captures)")

@@ -87,6 +87,8 @@ def lib() -> ctypes.CDLL:
         L.bpt_status_string.restype = ctypes.c_char_p
         L.bpt_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
         L.bpt_last_device_error.restype = i32
+        L.bpt_watchdog_selftest.argtypes = [vp]
+        L.bpt_watchdog_selftest.restype = i32
         L.bpt_profile_enable.argtypes = [i32]
         L.bpt_profile_enable.restype = i32
         dp = ctypes.POINTER(ctypes.c_double)
@@ -209,6 +211,16 @@ def bpt_last_device_error(stream=None):
     d = ctypes.c_int(0)
     rc = lib().bpt_last_device_error(_stream(stream), ctypes.byref(d))
     return int(rc), int(d.value)
+
+
+BPT_WATCHDOG_SELFTEST_SITE = 900
+
+
+def bpt_watchdog_selftest(stream=None) -> None:
+    """Launch the watchdog self-test: a wait on a barrier nothing signals runs
+    out after about 2 s and is recorded as (BPT_ETIMEOUT,
+    BPT_WATCHDOG_SELFTEST_SITE), which bpt_last_device_error() then reads."""
+    _check(lib().bpt_watchdog_selftest(_stream(stream)), "bpt_watchdog_selftest")
 
 
 PROF_KINDS = ("gemm", "attn_fwd", "attn_bwd", "norm", "misc")

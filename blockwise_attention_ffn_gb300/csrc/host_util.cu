@@ -139,6 +139,22 @@ int make_attn_map(CUtensorMap* map, const void* qkv, int b, int s, int64_t ld, i
   return r == CUDA_SUCCESS ? 0 : 1;
 }
 
+// Watchdog self-test.  One thread waits, through the same bounded_wait every
+// kernel of the library uses, on an mbarrier that nothing ever arrives at.
+// The wait gives up after BPT_WAIT_CYCLES SM cycles, records `site` in the
+// error word and returns; the kernel then leaves normally, so the context
+// stays usable.  Nothing is faulted: the stall is a barrier nobody signals.
+__global__ void watchdog_selftest_kernel(unsigned int* err, int site) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  bounded_wait(&bar, 0, &abort_flag, site, err);
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(&bar)) : "memory");
+}
+
 // Reads and clears the error word (synchronising the stream first).
 int read_device_error(cudaStream_t st, unsigned int out[4]) {
   cudaError_t e = cudaStreamSynchronize(st);
@@ -156,6 +172,14 @@ int read_device_error(cudaStream_t st, unsigned int out[4]) {
 }  // namespace bpt
 
 extern "C" {
+
+int bpt_watchdog_selftest(void* stream) {
+  unsigned int* err = bpt::device_error_word();
+  if (!err) return BPT_ECUDA;
+  bpt::watchdog_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      err, BPT_WATCHDOG_SELFTEST_SITE);
+  return cudaGetLastError() == cudaSuccess ? BPT_OK : BPT_ECUDA;
+}
 
 int bpt_profile_enable(int on) {
   std::lock_guard<std::mutex> lk(bpt::g_prof_mu);

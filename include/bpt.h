@@ -246,6 +246,19 @@ const char* bpt_status_string(int status);
  * cudaError_t).  detail may be NULL. */
 int bpt_last_device_error(void* stream, int* detail);
 
+/* Watchdog self-test: exercises the device-side wait limit without faulting
+ * anything.  Launches one CTA whose single thread waits, through the same
+ * bounded wait every kernel of the library uses, on an mbarrier that nothing
+ * arrives at.  After the wait limit (about 4e9 SM cycles, some 2 s) it
+ * records BPT_ETIMEOUT with wait site BPT_WATCHDOG_SELFTEST_SITE in the
+ * device error word and returns normally; bpt_last_device_error then
+ * reports (BPT_ETIMEOUT, BPT_WATCHDOG_SELFTEST_SITE) and clears the word,
+ * and later calls run as usual.  Asynchronous on `stream`.  Returns BPT_OK,
+ * or BPT_ECUDA if there is no device or the launch fails.  A diagnostic
+ * aid: the paper has no such step. */
+#define BPT_WATCHDOG_SELFTEST_SITE 900
+int bpt_watchdog_selftest(void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -48,6 +48,19 @@ def test_config_struct_matches_header():
     assert tuple(wf) == bpt.WEIGHT_FIELDS
 
 
+def test_watchdog_selftest_site_matches_header(built):
+    hdr = open(os.path.join(ROOT, "include", "bpt.h")).read()
+    m = re.search(r"#define BPT_WATCHDOG_SELFTEST_SITE (\d+)", hdr)
+    assert m and int(m.group(1)) == bpt.BPT_WATCHDOG_SELFTEST_SITE
+
+
+def test_watchdog_selftest_without_a_device_launches_nothing(built):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present: the GPU test covers the self-test")
+    assert built.bpt_watchdog_selftest(None) == bpt.BPT_ECUDA
+
+
 def test_status_strings(built):
     for s in range(6):
         assert bpt.bpt_status_string(s)

@@ -17,4 +17,10 @@ product path (the CUDA library and its Python binding) never does.
   (mean token cross-entropy through the vocabulary projection) and its
   position- and vocabulary-blocked forms, for the blockwise-loss row that
   comes next.
+* :mod:`oracle.stack` -- a stack of layers trained with a checkpoint every k
+  layers (the multi-layer row that comes next).
+* :mod:`oracle.sharded` -- one layer sharded by sequence position over P
+  ranks (zigzag rows, K/V all-gather, dK/dV reduce-scatter, weight-gradient
+  all-reduce), with the collectives passed in; the tests run it on gloo
+  ranks on CPU.
 """

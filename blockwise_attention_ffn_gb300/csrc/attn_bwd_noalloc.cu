@@ -19,6 +19,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/bpt.h"
 
 namespace {
@@ -30,22 +32,22 @@ static __device__ __align__(256) unsigned char g_attn_bwd_scratch[BPT_NOALLOC_SC
 // stand-in), so the address is looked up once per device, with that device
 // current, and cached.
 void* scratch_on_current_device(int* status) {
-  static void* addr[64] = {nullptr};
+  static std::atomic<void*> addr[64];  // host threads may race here; all store the same value
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
     *status = BPT_ECUDA;
     return nullptr;
   }
-  if (!addr[dev]) {
-    void* p = nullptr;
+  void* p = addr[dev].load(std::memory_order_acquire);
+  if (!p) {
     if (cudaGetSymbolAddress(&p, g_attn_bwd_scratch) != cudaSuccess || !p) {
       *status = BPT_ECUDA;
       return nullptr;
     }
-    addr[dev] = p;
+    addr[dev].store(p, std::memory_order_release);
   }
   *status = BPT_OK;
-  return addr[dev];
+  return p;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }

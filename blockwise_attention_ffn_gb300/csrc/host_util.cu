@@ -17,28 +17,32 @@ namespace bpt {
 
 __device__ unsigned int g_err[4];
 
+// The per-device caches below are atomics: host threads may call the library
+// concurrently, and each would store the same value.
 unsigned int* device_error_word() {
-  static unsigned int* addr[64] = {nullptr};
+  static std::atomic<unsigned int*> addr[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!addr[dev]) {
+  unsigned int* a = addr[dev].load(std::memory_order_acquire);
+  if (!a) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_err) != cudaSuccess) return nullptr;
-    addr[dev] = reinterpret_cast<unsigned int*>(p);
+    a = reinterpret_cast<unsigned int*>(p);
+    addr[dev].store(a, std::memory_order_release);
   }
-  return addr[dev];
+  return a;
 }
 
 int sm_count() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (!cached[dev]) {
-    int n = 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (!n) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 namespace {
@@ -80,7 +84,8 @@ ProfScope::~ProfScope() {
 namespace {
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> cached{nullptr};
+  PFN_cuTensorMapEncodeTiled_v12000 fn = cached.load(std::memory_order_acquire);
   if (!fn) {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -89,6 +94,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
         q != cudaDriverEntryPointSuccess)
       return nullptr;
     fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    cached.store(fn, std::memory_order_release);
   }
   return fn;
 }

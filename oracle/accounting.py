@@ -103,6 +103,30 @@ def bpt_activation_terms(s, b, h, c) -> dict:
     }
 
 
+def ulysses_attention_peak_bytes(S, C, H, d) -> int:
+    """12 (S/C) H d_head bytes: the full-head Q, K, V of a device's S/C rows
+    (6 bytes per row, head and dimension) and all-to-all buffers of the same
+    size ("Untied Ulysses ...", "Where Prior Approaches Fall Short", the
+    DS-Ulysses paragraph)."""
+    return 12 * (S // C) * H * d
+
+
+def upipe_stage_peak_bytes(S, C, U, d) -> int:
+    """12 (S/C) U d_head bytes: the same buffers for the U heads of one stage,
+    reused stage after stage (same page, "The Core Mechanism: Headwise
+    Chunking via UPipe")."""
+    return 12 * (S // C) * U * d
+
+
+def upipe_one_gpu_qkv_bytes(S, U, G, d, b=1) -> int:
+    """One GPU (C = 1) has no all-to-all, so a stage holds only its
+    projections: 2 bytes x S x (U query heads + U/G key and U/G value heads)
+    x d_head.  With G = 1 this is the Q/K/V half (6 S U d) of the page's
+    12 S U d; with grouped queries the key/value heads of the stage's U/G
+    groups are made once."""
+    return 2 * b * S * (U + 2 * (U // G)) * d
+
+
 def logits_bytes(s, b, V) -> int:
     """fp32 logits: 4 sbV (same page, "The logits")."""
     return 4 * s * b * V

@@ -61,6 +61,18 @@ def test_watchdog_selftest_without_a_device_launches_nothing(built):
     assert built.bpt_watchdog_selftest(None) == bpt.BPT_ECUDA
 
 
+@pytest.mark.parametrize("U", [8, 16, 32])
+def test_headchunk_workspace_is_one_stage_of_projections(built, U):
+    """The head-chunk call's workspace is one stage's Q/K/V buffer, the
+    one-GPU form of the headwise-chunking page's per-stage peak: it scales
+    with U, not with the number of heads."""
+    from oracle import accounting
+    c = presets.C5.with_(head_chunk=U)
+    G = c.n_heads // c.n_kv_heads
+    want = accounting.upipe_one_gpu_qkv_bytes(c.s, U, G, c.head_dim, b=c.b)
+    assert bpt.bpt_workspace_bytes(c, bpt.BPT_PASS_HEADCHUNK) == (want + 255) // 256 * 256
+
+
 def test_status_strings(built):
     for s in range(6):
         assert bpt.bpt_status_string(s)

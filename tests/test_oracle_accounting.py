@@ -56,6 +56,26 @@ def test_bpt_memory_terms():
     assert t["flash_ffn"] == 4 * t["flash_attention"]
 
 
+def test_upipe_stage_memory_against_the_pages_numbers():
+    g = GOLD["upipe_memory"]
+    S, d = 1 << 20, 128
+    q = g["qwen3_32b"]
+    uly = A.ulysses_attention_peak_bytes(S, q["C"], q["H"], d)
+    up = A.upipe_stage_peak_bytes(S, q["C"], q["U"], d)
+    assert uly == q["ulysses_S_dhead"] * S * d
+    assert up == q["upipe_S_dhead"] * S * d
+    assert 1 - up / uly == q["reduction"]
+    f = g["figure3_example"]
+    assert A.upipe_stage_peak_bytes(S, f["C"], f["U"], d) == \
+        f["upipe_over_ulysses"] * A.ulysses_attention_peak_bytes(S, f["C"], f["H"], d)
+    # one GPU: no all-to-all buffers, so a stage of U heads (no grouping)
+    # holds the Q/K/V half of the page's 12 S U d
+    for U in (1, 2, 8):
+        assert 2 * A.upipe_one_gpu_qkv_bytes(S, U, 1, d) == A.upipe_stage_peak_bytes(S, 1, U, d)
+    # grouped queries: U query heads share U/G key/value heads
+    assert A.upipe_one_gpu_qkv_bytes(S, 8, 4, d) == 2 * S * (8 + 2 + 2) * d
+
+
 def test_checkpoint_every_k():
     g = GOLD["checkpoint_every_k"]
     assert A.checkpoint_every_k(g["L"], 1, g["c_sbh"], g["A_sbh"]) == g["M1_sbh"]

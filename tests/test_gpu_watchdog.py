@@ -24,8 +24,9 @@ def test_a_wait_that_runs_out_is_reported_and_the_context_survives():
     st, site = bpt.bpt_last_device_error()  # synchronises
     waited = time.perf_counter() - t0
     assert (st, site) == (bpt.BPT_ETIMEOUT, bpt.BPT_WATCHDOG_SELFTEST_SITE)
-    # the limit is 4e9 SM cycles: at most 2.07 GHz, so at least 1.9 s
-    assert waited >= 1.0, waited
+    # the limit is 4e9 SM cycles (4e8 in a BPT_DEBUG=1 build): at the
+    # 2.07 GHz maximum clock at least 1.9 s (0.19 s), so the wait really ran
+    assert waited >= 0.1, waited
     # reading cleared the word
     assert bpt.bpt_last_device_error() == (bpt.BPT_OK, 0)
 

@@ -48,6 +48,7 @@ int validate(const bpt_config* c, Dims* D) {
   if (c->norm != BPT_NORM_LAYER && c->norm != BPT_NORM_RMS) return BPT_EINVAL;
   if (c->act < 0 || c->act > 2) return BPT_EINVAL;
   if (c->has_bias != 0 && c->has_bias != 1) return BPT_EINVAL;
+  if (c->causal != 0 && c->causal != 1) return BPT_EINVAL;
   if (c->q_block <= 0 || (c->q_block % 128) || c->kv_block <= 0 || (c->kv_block % 128)) return BPT_EINVAL;
   if (c->ffn_block < 0 || (c->ffn_block % c->q_block)) return BPT_EINVAL;
   if (!(c->norm_eps > 0.f)) return BPT_EINVAL;

@@ -87,9 +87,11 @@ enum { BPT_PASS_FWD = 0, BPT_PASS_BWD = 1, BPT_PASS_HEADCHUNK = 2 };
  *                      min(2048, s rounded up to q_block)
  *   head_chunk         U query heads per stage; U == H (or 0) means no
  *                      chunking; H % U == 0 and U % G == 0
- *   causal             1: key j is masked for query i when j > i
+ *   causal             1: key j is masked for query i when j > i; 0: no mask
+ *                      (any other value is rejected)
  *   norm, act          BPT_NORM_*, BPT_ACT_*
  *   has_bias           1: every linear has a bias (GPT); 0: none (Llama)
+ *                      (any other value is rejected)
  *   norm_eps           epsilon inside the norm's square root
  *   flags              BPT_FLAG_*                                             */
 typedef struct {

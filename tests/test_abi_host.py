@@ -105,7 +105,7 @@ def _call_fwd(cfg, x=1 << 20, y=1 << 20, ws=1 << 20, wsz=1 << 40):
 @pytest.mark.parametrize("bad", [
     dict(s=0), dict(h=100), dict(n_heads=5), dict(head_chunk=3), dict(q_block=64),
     dict(ffn_block=100), dict(norm=2), dict(act=3), dict(norm_eps=0.0), dict(flags=8),
-    dict(b=0),
+    dict(b=0), dict(causal=2), dict(has_bias=2), dict(n_kv_heads=0),
 ])
 def test_invalid_config_rejected_before_launch(built, bad):
     cfg = presets.C1.with_(**bad)

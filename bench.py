@@ -221,7 +221,7 @@ def oracle_sample(c, rows: int):
     x = inp["x"].float().double().numpy()
     oc = ref.LayerCfg(s=rows, h=c.h, n_heads=c.n_heads, n_kv_heads=c.n_kv_heads, head_dim=c.head_dim,
                       ffn_dim=c.ffn_dim, b=c.b, causal=bool(c.causal), norm=c.norm, act=c.act,
-                      has_bias=bool(c.has_bias), norm_eps=c.norm_eps)
+                      has_bias=bool(c.has_bias), norm_eps=c.norm_eps, rope_base=float(c.rope_base))
     t0 = time.perf_counter()
     ref.layer_forward(x, W, oc)
     if c.backward:

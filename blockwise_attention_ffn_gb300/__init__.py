@@ -34,7 +34,7 @@ class BptConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "b", "s", "h", "n_heads", "n_kv_heads", "head_dim", "ffn_dim",
         "q_block", "kv_block", "ffn_block", "head_chunk", "causal", "norm", "act", "has_bias")] + \
-        [("norm_eps", ctypes.c_float), ("flags", ctypes.c_int32)]
+        [("norm_eps", ctypes.c_float), ("flags", ctypes.c_int32), ("rope_base", ctypes.c_float)]
 
 
 class BptWeights(ctypes.Structure):
@@ -106,7 +106,7 @@ def make_config(c) -> BptConfig:
     """BptConfig from a LayerConfig (or any object with the same fields)."""
     return BptConfig(c.b, c.s, c.h, c.n_heads, c.n_kv_heads, c.head_dim, c.ffn_dim, c.q_block,
                      c.kv_block, c.ffn_block, c.head_chunk, c.causal, c.norm, c.act, c.has_bias,
-                     c.norm_eps, c.flags)
+                     c.norm_eps, c.flags, float(getattr(c, "rope_base", 0.0)))
 
 
 def _ptr(t):

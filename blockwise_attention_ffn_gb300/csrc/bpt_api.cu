@@ -38,6 +38,7 @@ struct Dims {
   bool chunked;
   int64_t Uk;      // key/value heads per stage
   int64_t qkv_w;   // columns of the (stage) projection buffer
+  float rope;      // rotary embedding base (0: none)
 };
 
 int validate(const bpt_config* c, Dims* D) {
@@ -49,6 +50,7 @@ int validate(const bpt_config* c, Dims* D) {
   if (c->act < 0 || c->act > 2) return BPT_EINVAL;
   if (c->has_bias != 0 && c->has_bias != 1) return BPT_EINVAL;
   if (c->causal != 0 && c->causal != 1) return BPT_EINVAL;
+  if (c->rope_base != 0.f && !(c->rope_base > 1.f && c->rope_base < 3.0e38f)) return BPT_EINVAL;
   if (c->q_block <= 0 || (c->q_block % 128) || c->kv_block <= 0 || (c->kv_block % 128)) return BPT_EINVAL;
   if (c->ffn_block < 0 || (c->ffn_block % c->q_block)) return BPT_EINVAL;
   if (!(c->norm_eps > 0.f)) return BPT_EINVAL;
@@ -78,6 +80,7 @@ int validate(const bpt_config* c, Dims* D) {
   D->cf = std::min<int64_t>(D->cf, D->s_pad);
   D->rows = D->b * D->s;
   D->qkv_w = (D->U + 2 * D->Uk) * d;
+  D->rope = c->rope_base;
   return BPT_OK;
 }
 
@@ -169,7 +172,8 @@ float* f32(void* p, int64_t elems) { return reinterpret_cast<float*>(p) + elems;
 
 // Q/K/V of stage k (all stages = one stage when not chunked) for all rows:
 // qkv[:, 0:U d] = xn Wq[kU d : (k+1)U d]^T (+ bq), then K, V of the stage's
-// U/G key/value heads.
+// U/G key/value heads.  With rotary embedding, the stage's query and key
+// heads (adjacent columns) are then rotated at their rows' positions.
 int stage_qkv(const Dims& D, const bpt_weights* w, bool has_bias, const void* xn, void* qkv, int64_t k,
               cudaStream_t st) {
   const int64_t d = D.d, h = D.h;
@@ -193,6 +197,7 @@ int stage_qkv(const Dims& D, const bpt_weights* w, bool has_bias, const void* xn
     int rc = gemm(D.rows, pc.n, h, A, false, &B, &kseg, 1, false, nullptr, e, st);
     if (rc) return rc;
   }
+  if (D.rope != 0.f) return rope_apply(D.rows, (int)D.s, qkv, D.qkv_w, 0, (int)(D.U + D.Uk), (int)d, D.rope, 0, st);
   return 0;
 }
 
@@ -737,13 +742,18 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
       if ((rc = gemm(D.rows, Hd, h, A, false, &B, &h, 1, true, nullptr, e, st))) return rc;
     }
 
-    // ---- attention and Q/K/V gradients, stage by stage.  The key-bias
-    // gradient is identically zero: the bias adds Q[q].bk to every logit of
-    // query row q alike (masked ones stay -inf), and softmax is invariant to
-    // such a shift, so the loss does not depend on bk.  It is written as exact
-    // zeros (left as is when accumulating) instead of summing dK, whose sum of
-    // bf16-rounded rows would be rounding noise growing like sqrt(s).
-    if (hb && !accum && cudaMemsetAsync(g->bk, 0, (size_t)(D.Hkv * D.d) * sizeof(float), st) != cudaSuccess)
+    // ---- attention and Q/K/V gradients, stage by stage.  Without rotary
+    // embedding the key-bias gradient is identically zero: the bias adds
+    // Q[q].bk to every logit of query row q alike (masked ones stay -inf),
+    // and softmax is invariant to such a shift, so the loss does not depend
+    // on bk.  It is then written as exact zeros (left as is when
+    // accumulating) instead of summing dK, whose sum of bf16-rounded rows
+    // would be rounding noise growing like sqrt(s).  A rotation after the
+    // bias makes the added logit depend on the key's position, so with
+    // rotary embedding dbk is the column sum of dK like the other biases.
+    const bool rope = D.rope != 0.f;
+    if (hb && !accum && !rope &&
+        cudaMemsetAsync(g->bk, 0, (size_t)(D.Hkv * D.d) * sizeof(float), st) != cudaSuccess)
       return BPT_ECUDA;
     for (int64_t k = 0; k < D.n_stages; ++k) {
       if (D.chunked && (rc = stage_qkv(D, w, hb, W.xn, W.qkv, k, st))) return rc;
@@ -753,6 +763,9 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
       AttnBwdShape sb = stage_bwd_shape(D, k);
       sb.f.causal = cfg->causal;
       if ((rc = attention_bwd(sb, W.qkv, W.o, lse, W.dO, W.dqkv, W.attn, st))) return rc;
+      // dQ, dK are gradients of the rotated heads: turn them back
+      if (rope && (rc = rope_apply(D.rows, (int)D.s, W.dqkv, D.qkv_w, 0, (int)(D.U + D.Uk), (int)d, D.rope, 1, st)))
+        return rc;
       const int64_t q0 = k * D.U * d, kv0 = k * D.Uk * d;
       const int64_t nq = D.U * d, nkv = D.Uk * d;
       // dxn (+)= dQ Wq_s + dK Wk_s + dV Wv_s
@@ -787,7 +800,7 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
           e.ldo = h;
           e.beta = accum ? 1.f : 0.f;
           if ((rc = gemm(pc.n, h, K, A, true, &B, &K, 1, true, nullptr, e, ss))) return rc;
-          if (hb && pc.Gb != g->bk &&
+          if (hb && (pc.Gb != g->bk || rope) &&
               (rc = colsum(D.rows, pc.n, bf(W.dqkv, pc.col), D.qkv_w, f32(pc.Gb, pc.row0), accum, ss)))
             return rc;
         }

@@ -146,6 +146,12 @@ int norm_bwd(int64_t rows, int h, int kind, float eps, const NormBwdIO& io, cons
 // out[n] (+)= sum over rows of in[row, n]  (bf16 in, fp32 out)
 int colsum(int64_t rows, int64_t n, const void* in, int64_t ld, float* out, int accumulate,
            cudaStream_t st);
+// Rotary position embedding in place: n_heads heads of d columns from column
+// col0 of bf16 buf [rows, ld], row r at position r % s, pair (i, i + d/2)
+// turned by (r % s) * base^(-2i/d) (inverse: by minus that).  d % 4 == 0,
+// d <= 128.
+int rope_apply(int64_t rows, int s, void* buf, int64_t ld, int col0, int n_heads, int d, float base, int inverse,
+               cudaStream_t st);
 // dst bf16 [rows, n] (ld_dst) = src fp32 [rows, n] (ld_src) * scale
 int f32_to_bf16(int64_t rows, int64_t n, const float* src, int64_t ld_src, void* dst,
                 int64_t ld_dst, float scale, cudaStream_t st);

@@ -349,6 +349,55 @@ __global__ void dsum_kernel(int b, int s, int s_pad, int H, int d, const __nv_bf
   }
 }
 
+
+// Rotary position embedding ("Untied Ulysses ...", "Composability with Other
+// Memory Optimizations": fused RoPE, rotated in place without an fp32 copy of
+// Q and K), in place, on n_heads consecutive heads of d
+// columns starting at column col0 of a row-major bf16 buffer [rows, ld]
+// (rows = b*s; the position of row r is r % s).  Element i of a head is
+// paired with element i + d/2 and the pair turns by the angle p * theta[i],
+// theta[i] = base^(-2i/d) (computed on the host in double); inverse turns by
+// the negated angle: the transpose of the rotation, hence its gradient.
+// The angle is formed and reduced to [-pi, pi] in double -- p * theta reaches
+// 1.3e5 rad at s = 128K, where a float product would carry ~4e-3 rad of
+// error -- and only its sine and cosine are taken in float.  One thread per
+// row and pair of consecutive elements (i, i+1): a bf16x2 load and store per
+// half of every head.
+struct RopeTheta {
+  double t[64];
+};
+
+__global__ void rope_kernel(int64_t rows, int s, __nv_bfloat16* buf, int64_t ld, int col0, int n_heads, int d,
+                            const __grid_constant__ RopeTheta th, int inverse) {
+  const int half = d / 2;
+  const int per_row = half / 2;
+  const int64_t total = rows * per_row;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = idx / per_row;
+    const int i = (int)(idx % per_row) * 2;
+    const double p = (double)(r % s);
+    float c[2], sn[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const double a = p * th.t[i + u];
+      const double k = rint(a * 0.15915494309189535);  // turns: a / (2 pi)
+      const float red = (float)fma(-k, 6.283185307179586, a);
+      sincosf(red, &sn[u], &c[u]);
+      if (inverse) sn[u] = -sn[u];
+    }
+    __nv_bfloat16* row = buf + r * ld + col0 + i;
+    for (int hd = 0; hd < n_heads; ++hd) {
+      __nv_bfloat162* pa = reinterpret_cast<__nv_bfloat162*>(row + (int64_t)hd * d);
+      __nv_bfloat162* pb = reinterpret_cast<__nv_bfloat162*>(row + (int64_t)hd * d + half);
+      const float2 a = __bfloat1622float2(*pa);
+      const float2 b = __bfloat1622float2(*pb);
+      *pa = __floats2bfloat162_rn(a.x * c[0] - b.x * sn[0], a.y * c[1] - b.y * sn[1]);
+      *pb = __floats2bfloat162_rn(a.x * sn[0] + b.x * c[0], a.y * sn[1] + b.y * c[1]);
+    }
+  }
+}
+
 // blocks for a grid-stride loop over `work` items: enough for the work, at
 // most 16 per SM of the current device
 int grid_for(int64_t work, int per_block) {
@@ -436,6 +485,18 @@ int attn_dsum(const AttnBwdShape& sh, const void* o, const void* dout, const flo
                                                     f.ld_o, f.o_col, (const __nv_bfloat16*)dout, sh.ld_do,
                                                     sh.do_col, lse, f.H_total, f.lse_head0, Dsum, NL2,
                                                     (__nv_bfloat16*)AUX);
+  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
+int rope_apply(int64_t rows, int s, void* buf, int64_t ld, int col0, int n_heads, int d, float base, int inverse,
+               cudaStream_t st) {
+  if (rows <= 0 || n_heads <= 0) return 0;
+  if (d % 4 || d > 128 || s <= 0 || !(base > 1.f)) return 1;
+  RopeTheta th;
+  for (int i = 0; i < 64; ++i) th.t[i] = i < d / 2 ? pow((double)base, -2.0 * i / d) : 0.0;
+  ProfScope prof(PROF_MISC, 0.0, (double)rows * n_heads * d * 2 * 2, st);
+  rope_kernel<<<grid_for(rows * (d / 4), 256), 256, 0, st>>>(rows, s, (__nv_bfloat16*)buf, ld, col0, n_heads, d, th,
+                                                             inverse);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 

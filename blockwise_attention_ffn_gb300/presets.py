@@ -29,6 +29,7 @@ class LayerConfig:
     has_bias: int = 1
     norm_eps: float = 1e-5
     flags: int = 0
+    rope_base: float = 0.0  # rotary position embedding base; 0 = none
     name: str = ""
     backward: bool = False  # the workload includes the backward pass
     seed: int = 0

@@ -93,7 +93,18 @@ enum { BPT_PASS_FWD = 0, BPT_PASS_BWD = 1, BPT_PASS_HEADCHUNK = 2 };
  *   has_bias           1: every linear has a bias (GPT); 0: none (Llama)
  *                      (any other value is rejected)
  *   norm_eps           epsilon inside the norm's square root
- *   flags              BPT_FLAG_*                                             */
+ *   flags              BPT_FLAG_*
+ *   rope_base          rotary position embedding ("Untied Ulysses ...",
+ *                      "Composability with Other Memory Optimizations": fused
+ *                      RoPE, rotated in place with no fp32 copy; the page
+ *                      does not state the rotation, this is the standard
+ *                      half-split one): 0 = none; else > 1, and Q and K are
+ *                      rotated after their projection (and bias): element i
+ *                      of a head is paired with i + d/2 and the pair at
+ *                      position p (the row's index within its sequence)
+ *                      turns by p * rope_base^(-2i/d).  The layer calls and
+ *                      bpt_attn_headchunk apply it; the attention-only calls
+ *                      take Q/K as given.                                    */
 typedef struct {
   int32_t b, s, h, n_heads, n_kv_heads, head_dim, ffn_dim;
   int32_t q_block, kv_block, ffn_block, head_chunk;
@@ -103,6 +114,7 @@ typedef struct {
   int32_t has_bias;
   float norm_eps;
   int32_t flags;
+  float rope_base;
 } bpt_config;
 
 /* bf16 device pointers, nn.Linear [out, in]; NULL where the variant has none

@@ -36,4 +36,5 @@ def oracle_cfg(c) -> LayerCfg:
     """LayerCfg from any object with the library config's field names."""
     return LayerCfg(s=c.s, h=c.h, n_heads=c.n_heads, n_kv_heads=c.n_kv_heads,
                     head_dim=c.head_dim, ffn_dim=c.ffn_dim, b=c.b, causal=bool(c.causal),
-                    norm=c.norm, act=c.act, has_bias=bool(c.has_bias), norm_eps=c.norm_eps)
+                    norm=c.norm, act=c.act, has_bias=bool(c.has_bias), norm_eps=c.norm_eps,
+                    rope_base=float(getattr(c, "rope_base", 0.0)))

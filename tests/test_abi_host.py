@@ -106,6 +106,7 @@ def _call_fwd(cfg, x=1 << 20, y=1 << 20, ws=1 << 20, wsz=1 << 40):
     dict(s=0), dict(h=100), dict(n_heads=5), dict(head_chunk=3), dict(q_block=64),
     dict(ffn_block=100), dict(norm=2), dict(act=3), dict(norm_eps=0.0), dict(flags=8),
     dict(b=0), dict(causal=2), dict(has_bias=2), dict(n_kv_heads=0),
+    dict(rope_base=0.5), dict(rope_base=-10000.0), dict(rope_base=float("nan")), dict(rope_base=float("inf")),
 ])
 def test_invalid_config_rejected_before_launch(built, bad):
     cfg = presets.C1.with_(**bad)
@@ -119,6 +120,14 @@ def test_known_flags_accepted(built):
     assert base > 0
     assert bpt.bpt_workspace_bytes(both, bpt.BPT_PASS_BWD) == base
     assert bpt.bpt_workspace_bytes(presets.C1.with_(flags=4), bpt.BPT_PASS_BWD) == 0
+
+
+def test_rope_base_accepted_and_plan_unchanged(built):
+    """Rotary embedding works in place on the projection buffer: it needs no
+    workspace of its own."""
+    for p in (bpt.BPT_PASS_FWD, bpt.BPT_PASS_BWD, bpt.BPT_PASS_HEADCHUNK):
+        for c in (presets.C1, presets.C5):
+            assert bpt.bpt_workspace_bytes(c.with_(rope_base=10000.0), p) == bpt.bpt_workspace_bytes(c, p) > 0
 
 
 def test_unsupported_head_dim(built):

@@ -203,7 +203,8 @@ def describe(c) -> dict:
             "causal": bool(c.causal), "q_block": c.q_block, "kv_block": c.kv_block,
             "ffn_block": c.ffn_block, "head_chunk": c.head_chunk or c.n_heads,
             "pass": "fwd+bwd" if c.backward else "fwd", "seed": c.seed,
-            "l2": "no flush: every step streams inputs and buffers far larger than the 129 MB L2"}
+            "l2": "no flush: every step streams inputs and buffers far larger than the 129 MB L2",
+            **({"rope_base": c.rope_base} if c.rope_base else {})}
 
 
 # ----------------------------------------------------------------- CPU oracle leg
@@ -501,6 +502,8 @@ def main():
                     help="positions of the workload (at most s) in the cpu_baseline sample of the "
                          "GPU run: about 10-15 s of fp64 work on 16 host cores at the s=32K workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rope-base", type=float, default=0.0,
+                    help="rotary position embedding base for the layer (0: none, the workloads' setting)")
     ap.add_argument("--profile-kernel", choices=["attn_fwd", "attn_bwd", "layer"], default=None,
                     help="run one launch of this component (small case for profiler captures)")
     ap.add_argument("--seq", type=int, default=4096, help="sequence length for --profile-kernel")
@@ -508,6 +511,8 @@ def main():
     args.warmup = max(3, args.warmup)
     from blockwise_attention_ffn_gb300.presets import PRESETS
     c = PRESETS[args.config]
+    if args.rope_base:
+        c = c.with_(rope_base=args.rope_base)
     if args.profile_kernel:
         return run_one_kernel(args, c)
     if args.impl == "reference":

@@ -136,3 +136,92 @@ def test_zigzag_rows_partition_the_sequence_with_equal_causal_work(P):
         c = s // P
         contiguous = [sharded.causal_pairs(np.arange(r * c, (r + 1) * c)) for r in range(P)]
         assert len(set(contiguous)) == P
+
+
+class ThreadComm:
+    """Ranks as threads of one process; `broken` plants a mistake in one
+    collective: 'gather' hands each rank only its own K/V, 'reduce' skips the
+    sum over ranks (each rank keeps its own partial dK/dV and weight
+    gradients)."""
+
+    def __init__(self, rank, world, box, barrier, broken=None):
+        self.rank, self.world, self.box, self.barrier, self.broken = rank, world, box, barrier, broken
+
+    def _exchange(self, a):
+        self.barrier.wait()
+        self.box[self.rank] = np.array(a, np.float64, copy=True)
+        self.barrier.wait()
+        got = [self.box[r] for r in range(self.world)]
+        self.barrier.wait()
+        return got
+
+    def all_gather(self, a):
+        got = self._exchange(a)
+        return [got[self.rank]] if self.broken == "gather" else got
+
+    def all_reduce(self, a):
+        got = self._exchange(a)
+        return got[self.rank] if self.broken == "reduce" else np.sum(got, axis=0)
+
+
+def _run_threads(cfg, world, broken, seed, backward=True):
+    import threading
+    x, W, dy = rand_layer(cfg, seed=seed)
+    # a rank that fails breaks the barrier for the others instead of leaving
+    # them waiting
+    box, barrier, out, errs = {}, threading.Barrier(world, timeout=60), {}, []
+
+    def work(r):
+        try:
+            comm = ThreadComm(r, world, box, barrier, broken)
+            pos = sharded.zigzag_rows(cfg.s, world, r)
+            y = sharded.rank_layer_forward(x[:, pos], pos, W, cfg, comm)
+            dx, g = (sharded.rank_layer_backward(x[:, pos], pos, W, dy[:, pos], cfg, comm) if backward
+                     else (np.zeros_like(y), {}))
+            out[r] = (pos, y, dx, g)
+        except Exception as e:  # noqa: BLE001 - re-raised below
+            errs.append(e)
+            barrier.abort()
+
+    ts = [threading.Thread(target=work, args=(r,)) for r in range(world)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    if errs:
+        raise errs[0]
+    y = np.zeros((cfg.b, cfg.s, cfg.h))
+    dx = np.zeros_like(y)
+    for pos, yr, dxr, _ in out.values():
+        y[:, pos] = yr
+        dx[:, pos] = dxr
+    return (x, W, dy), y, dx, out[0][3]
+
+
+def _rel(a, b):
+    return np.linalg.norm(a - b) / np.linalg.norm(b)
+
+
+@pytest.mark.parametrize("world", [2, 4])
+def test_thread_ranks_equal_the_unsharded_layer(world):
+    cfg = CASES["gpt causal"]
+    (x, W, dy), y, dx, g0 = _run_threads(cfg, world, None, seed=95)
+    _close(y, ref.layer_forward(x, W, cfg), "y")
+    dx_ref, g_ref = ref.layer_backward(x, W, dy, cfg)
+    _close(dx, dx_ref, "dx")
+    for k, v in g_ref.items():
+        _close(g0[k], v, k)
+
+
+def test_planted_exchange_mistakes_are_caught():
+    """Without the K/V all-gather the forward is wrong; without the sum over
+    ranks the backward is wrong: both exchanges are needed, and the pins
+    above would see either one missing."""
+    cfg = CASES["gpt causal"]
+    (x, W, dy), y, _, _ = _run_threads(cfg, 2, "gather", seed=96, backward=False)
+    assert _rel(y, ref.layer_forward(x, W, cfg)) > 1e-3
+    (x, W, dy), y, dx, g0 = _run_threads(cfg, 2, "reduce", seed=97)
+    _close(y, ref.layer_forward(x, W, cfg), "y")  # the forward needs no sum
+    dx_ref, g_ref = ref.layer_backward(x, W, dy, cfg)
+    assert _rel(dx, dx_ref) > 1e-3
+    assert _rel(g0["wq"], g_ref["wq"]) > 1e-3

@@ -448,7 +448,12 @@ def run_gpu(args, c):
                        "vanilla_layer_activation_bytes_analytic": vanilla_activation_bytes(c)},
         }
         if not args.no_cpu_baseline and world == 1:
-            line["cpu_baseline"] = cpu_baseline(c, min(args.cpu_rows, c.s))
+            # a reported baseline, not the measurement: a failure here must not
+            # cost the line
+            try:
+                line["cpu_baseline"] = cpu_baseline(c, min(args.cpu_rows, c.s))
+            except Exception as e:  # noqa: BLE001 - reported in the line
+                line["cpu_baseline"] = {"error": repr(e), "kind": "oracle"}
         print(json.dumps(line), flush=True)
     if world > 1:
         tdist.barrier()

@@ -235,3 +235,27 @@ def test_profiler_calls_on_the_host(built):
     assert L.bpt_profile_list(-1, None, None, None, None) == -bpt.BPT_EINVAL
     assert L.bpt_profile_list(4, None, None, None, None) == -bpt.BPT_EINVAL
     assert L.bpt_profile_list(0, None, None, None, None) == 0
+
+
+def test_product_never_reaches_the_oracle():
+    """The package and its CUDA sources import, load or name nothing under
+    oracle/: the oracle is test infrastructure, never a fallback."""
+    pkg = os.path.join(ROOT, "blockwise_attention_ffn_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        if "_build" in dirpath or "__pycache__" in dirpath:
+            continue
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                txt = open(os.path.join(dirpath, fn)).read()
+                assert not re.search(r"^\s*(from|import)\s+oracle\b", txt, flags=re.M), fn
+                assert "oracle/" not in txt and "oracle." not in txt, fn
+
+
+def test_missing_library_raises(monkeypatch):
+    """No silent fallback: without libbpt.so the binding refuses to run."""
+    monkeypatch.setattr(bpt, "_lib", None)
+    monkeypatch.setattr(bpt, "LIB_PATH", os.path.join(ROOT, "no-such-dir", "libbpt.so"))
+    with pytest.raises(RuntimeError):
+        bpt.lib()
+    with pytest.raises(RuntimeError):
+        bpt.bpt_workspace_bytes(presets.C1, bpt.BPT_PASS_FWD)

@@ -114,3 +114,26 @@ def test_failed_rank_is_detected_within_the_timeout(tmp_path, mode):
     res = json.load(open(tmp_path / "r0.json"))
     assert res["outcome"] != "returned", res
     assert res["seconds"] < 12, res
+
+
+def test_reference_arm_line_carries_the_contract_keys(monkeypatch, capsys):
+    """One rank: the oracle arm prints one JSON line with the keys of the
+    bench contract, its own cpu_baseline and an e2e with no copies."""
+    import argparse
+
+    import bench
+    from blockwise_attention_ffn_gb300.presets import C3
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    monkeypatch.setenv("RANK", "0")
+    args = argparse.Namespace(gpus=1, steps=1, warmup=3, ref_rows=32)
+    assert bench.run_reference(args, C3) == 0
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["value"] > 0
+    assert d["config"]["workload"] == C3.name
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0

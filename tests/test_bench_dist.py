@@ -9,7 +9,6 @@ import socket
 import sys
 
 import pytest
-import torch
 import torch.distributed as tdist
 import torch.multiprocessing as mp
 

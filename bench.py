@@ -233,13 +233,31 @@ def oracle_sample(c, rows: int):
     return dt, fl, sc
 
 
+def blas_threads() -> int:
+    """Threads the oracle's BLAS runs on: what the BLAS library reports when
+    threadpoolctl is installed, else the usual environment limits, else every
+    host core."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:  # noqa: BLE001 - fall back to the environment
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        v = os.environ.get(var, "")
+        if v.isdigit() and int(v) > 0:
+            return min(int(v), os.cpu_count() or int(v))
+    return os.cpu_count() or 1
+
+
 def cpu_baseline(c, rows: int) -> dict:
     dt, fl, sc = oracle_sample(c, rows)
-    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
             "seconds": dt,
             "sample": f"fp64 NumPy oracle, forward + backward of the first {rows} positions of the "
                       f"workload (same layer shape), {fl / 1e12:.3f} TFLOP of the same FLOP "
-                      f"definition; BLAS threads = all host cores"}
+                      f"definition; cores = the BLAS threads"}
 
 
 def run_reference(args, c):
@@ -258,7 +276,7 @@ def run_reference(args, c):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic", "config": describe(c),
-            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
                              "sample": f"first {args.ref_rows} positions of the workload per step"},
             "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

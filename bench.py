@@ -255,7 +255,7 @@ def cpu_baseline(c, rows: int) -> dict:
     dt, fl, sc = oracle_sample(c, rows)
     return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
             "seconds": dt,
-            "sample": f"fp64 NumPy oracle, forward + backward of the first {rows} positions of the "
+            "sample": f"fp64 NumPy oracle, {'forward + backward' if c.backward else 'forward'} of the first {rows} positions of the "
                       f"workload (same layer shape), {fl / 1e12:.3f} TFLOP of the same FLOP "
                       f"definition; cores = the BLAS threads"}
 

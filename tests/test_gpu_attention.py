@@ -118,3 +118,29 @@ def test_identical_keys_give_prefix_mean():
     got = to64(o).reshape(s, H, d)
     assert_close(got, want, "prefix mean")
     assert np.max(np.abs(got[0] - v[0])) <= 4e-3  # bf16 rounding of V_0 itself only
+
+
+@pytest.mark.parametrize("shape", [(1, 640, 4, 1, 80, 0), (2, 200, 2, 2, 128, 0)])
+def test_noncausal_key_order_does_not_matter(shape):
+    """Without the mask the keys form a set: permuting the key/value rows
+    (across tiles and within them) changes only the order of the online
+    softmax's blocks, not the result (GPU against GPU, each within the
+    acceptance bound of the exact value)."""
+    b, s, H, Hkv, d, causal = shape
+    cfg = _cfg(*shape)
+    qkv = _qkv(b, s, H, Hkv, d, seed=s + d + 1, scale=1.5)
+    perm = torch.randperm(s, generator=torch.Generator().manual_seed(s))
+    t = qkv.reshape(b, s, H + 2 * Hkv, d).clone()
+    t[:, :, H:] = t[:, perm, H:]
+    qkv_p = t.reshape(b * s, -1)
+    outs = []
+    for x in (qkv, qkv_p):
+        o = torch.zeros(b * s, H * d, dtype=torch.bfloat16, device="cuda")
+        lse = torch.zeros(b, H, bpt.s_pad(cfg), dtype=torch.float32, device="cuda")
+        bpt.bpt_attention_fwd(cfg, x.cuda(), o, lse)
+        torch.cuda.synchronize()
+        assert bpt.bpt_last_device_error()[0] == bpt.BPT_OK
+        outs.append((to64(o), to64(lse)[:, :, :s]))
+    assert_close(outs[1][0], outs[0][0], "O, keys permuted")
+    assert_close(outs[1][1], outs[0][1], "LSE, keys permuted", max_abs=2 * LSE_MAX_ABS, rel_fro=2 * LSE_REL_FRO,
+                 bf16_out=False)

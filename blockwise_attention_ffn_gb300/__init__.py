@@ -8,8 +8,10 @@ or fails to load, importing the binding's entry points raises.
 Entry points keep the C names: bpt_layer_fwd, bpt_layer_bwd,
 bpt_attn_headchunk, bpt_attention_fwd, bpt_attention_bwd, bpt_attention_bwd_noalloc,
 bpt_workspace_bytes, bpt_saved_bytes, bpt_attention_bwd_workspace_bytes,
-bpt_status_string, bpt_last_device_error, bpt_profile_enable,
-bpt_profile_collect.
+bpt_status_string, bpt_last_device_error, bpt_watchdog_selftest,
+bpt_profile_enable, bpt_profile_collect, bpt_profile_list.  The layer stack
+with a checkpoint every k layers is in :mod:`.stack` (a scheduler over
+bpt_layer_fwd / bpt_layer_bwd).
 """
 from __future__ import annotations
 

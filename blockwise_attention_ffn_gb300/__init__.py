@@ -8,7 +8,7 @@ or fails to load, importing the binding's entry points raises.
 Entry points keep the C names: bpt_layer_fwd, bpt_layer_bwd,
 bpt_attn_headchunk, bpt_attention_fwd, bpt_attention_bwd, bpt_attention_bwd_noalloc,
 bpt_workspace_bytes, bpt_saved_bytes, bpt_attention_bwd_workspace_bytes,
-bpt_status_string, bpt_last_device_error, bpt_watchdog_selftest,
+bpt_status_string, bpt_last_device_error, bpt_check_device_range, bpt_watchdog_selftest,
 bpt_profile_enable, bpt_profile_collect, bpt_profile_list.  The layer stack
 with a checkpoint every k layers is in :mod:`.stack` (a scheduler over
 bpt_layer_fwd / bpt_layer_bwd).
@@ -27,6 +27,8 @@ BPT_OK, BPT_EINVAL, BPT_ENOSPC, BPT_ECUDA, BPT_ETIMEOUT, BPT_EUNSUPPORTED = rang
 BPT_PASS_FWD, BPT_PASS_BWD, BPT_PASS_HEADCHUNK = 0, 1, 2
 BPT_FLAG_ACCUM_GRADS = 1
 BPT_FLAG_ONE_STREAM = 2
+BPT_FLAG_DETERMINISTIC = 4
+BPT_FLAG_DEBUG_CHECKS = 8
 
 WEIGHT_FIELDS = ("ln1_w", "ln1_b", "wq", "bq", "wk", "bk", "wv", "bv", "wo", "bo",
                  "ln2_w", "ln2_b", "w1", "b1", "w2", "b2", "w3")
@@ -89,6 +91,8 @@ def lib() -> ctypes.CDLL:
         L.bpt_status_string.restype = ctypes.c_char_p
         L.bpt_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
         L.bpt_last_device_error.restype = i32
+        L.bpt_check_device_range.argtypes = [vp, sz]
+        L.bpt_check_device_range.restype = i32
         L.bpt_watchdog_selftest.argtypes = [vp]
         L.bpt_watchdog_selftest.restype = i32
         L.bpt_profile_enable.argtypes = [i32]
@@ -198,14 +202,21 @@ NOALLOC_SCRATCH_BYTES = 192 * 1024 * 1024
 
 def bpt_attention_bwd_noalloc(cfg, qkv, o, lse, dout, dqkv, stream=None) -> None:
     """bpt_attention_bwd for callers that cannot allocate device memory at
-    call time: the scratch (4*b*H*s_pad bytes of row sums) is a fixed array
-    inside the library (at most NOALLOC_SCRATCH_BYTES; larger problems raise
-    BptError with BPT_ENOSPC).
+    call time: the scratch (bpt_attention_bwd_workspace_bytes(cfg) =
+    24*b*H*s_pad bytes: the fp32 dO.O sums and -LSE*log2(e), and a 16-byte
+    bf16 row of both per query) is a fixed array inside the library (at most
+    NOALLOC_SCRATCH_BYTES; larger problems raise BptError with BPT_ENOSPC).
     Calls that overlap on the GPU share that array and race: serialise them."""
     c = make_config(cfg)
     rc = lib().bpt_attention_bwd_noalloc(ctypes.byref(c), _ptr(qkv), _ptr(o), _ptr(lse), _ptr(dout),
                                          _ptr(dqkv), _stream(stream))
     _check(rc, "bpt_attention_bwd_noalloc")
+
+
+def bpt_check_device_range(ptr: int, nbytes: int) -> int:
+    """BPT_OK if [ptr, ptr + nbytes) lies inside one device allocation of the
+    current device, else BPT_EINVAL (launches nothing)."""
+    return int(lib().bpt_check_device_range(ctypes.c_void_p(ptr), int(nbytes)))
 
 
 def bpt_last_device_error(stream=None):

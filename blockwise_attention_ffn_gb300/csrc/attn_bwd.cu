@@ -56,6 +56,7 @@ struct AttnBwdParams {
   long long ld_dqkv;
   int dq_col, dk_col, dv_col;
   float scale, scale_log2;
+  int one_issuer;  // fixed-order mode: warp 1 issues both groups' products
   unsigned int* err;
 };
 
@@ -252,14 +253,16 @@ __global__ void __launch_bounds__(352, 1) attn_dkdv_hs_kernel(const __grid_const
       }
     }
   } else if (warp == 1 || warp == 10) {
-    if (lane == 0) {
+    // one issuer (fixed-order mode): warp 1 issues every sub-tile's products
+    // in sub-tile order, so dV and dK take their products in a fixed order
+    if (lane == 0 && !(p.one_issuer && warp == 10)) {
       // ------------------------------------------------ MMA issuers
-      const int b = warp == 1 ? 0 : 1;  // this issuer's buffer and sub-tiles
+      const int b0 = warp == 1 ? 0 : 1;  // this issuer's first sub-tile
+      const int ustep = p.one_issuer ? 1 : 2;
       const uint32_t uZero = smem_u32(sZero);
-      const uint32_t tSb = tS + 64 * b, tdPb = tdP + 64 * b;
       // the 64 query rows of sub-tile half b start 64 b rows into every
       // chunk of the stage's tiles (whole swizzle atoms), and 64 b rows into
-      // its extra rows
+      // its extra rows; sub-tile u uses buffer b = u % 2
       auto stage_u = [&](int u) { return smem_u32(sStage + ((u >> 1) % QS) * STAGE); };
       // K, V and their extra chunks in shared memory (head dims above 80):
       // the extra chunk is 128 rows of 16 bytes, K-major core matrices
@@ -267,6 +270,8 @@ __global__ void __launch_bounds__(352, 1) attn_dkdv_hs_kernel(const __grid_const
       const uint32_t uK = smem_u32(sKV), uV = uK + T::TILE;
       const uint32_t uKx = uK + 2 * T::TILE, uVx = uKx + C::AUX;
       auto issue_s = [&](int u) {
+        const int b = u & 1;
+        const uint32_t tSb = tS + 64 * b;
         const uint32_t uQ = stage_u(u) + 64 * T::SWB * b;
         const uint32_t uA = stage_u(u) + 2 * T::TILE + 64 * 16 * b;
         if constexpr (C::KV_TMEM) {
@@ -281,6 +286,8 @@ __global__ void __launch_bounds__(352, 1) attn_dkdv_hs_kernel(const __grid_const
         umma_commit(&s_full[b]);
       };
       auto issue_dp = [&](int u) {
+        const int b = u & 1;
+        const uint32_t tdPb = tdP + 64 * b;
         const uint32_t udO = stage_u(u) + T::TILE + 64 * T::SWB * b;
         const uint32_t uA = stage_u(u) + 2 * T::TILE + 64 * 16 * b;
         if constexpr (C::KV_TMEM) {
@@ -300,13 +307,18 @@ __global__ void __launch_bounds__(352, 1) attn_dkdv_hs_kernel(const __grid_const
         return bounded_wait(&qdo_full[t % QS], (t / QS) & 1, abort_flag, 641, p.err);
       };
       bool ok = bounded_wait(kv_ready, 0, abort_flag, 642, p.err) &&
-                (C::KV_TMEM || bounded_wait(kv_full, 0, abort_flag, 646, p.err)) && wait_stage(b);
+                (C::KV_TMEM || bounded_wait(kv_full, 0, abort_flag, 646, p.err)) && wait_stage(b0);
       if (ok) {
         tc_fence_after();
-        issue_s(b);
-        issue_dp(b);
+        // sub-tiles 0 and 1 share stage 0 (U is even)
+        for (int u = b0; u < 2; u += ustep) {
+          issue_s(u);
+          issue_dp(u);
+        }
       }
-      for (int u = b; ok && u < U; u += 2) {
+      for (int u = b0; ok && u < U; u += ustep) {
+        const int b = u & 1;
+        const uint32_t tSb = tS + 64 * b, tdPb = tdP + 64 * b;
         const int st = (u >> 1) % QS;
         const uint32_t uQ = stage_u(u);
         const uint32_t udO = uQ + T::TILE;
@@ -334,10 +346,14 @@ __global__ void __launch_bounds__(352, 1) attn_dkdv_hs_kernel(const __grid_const
         // dP(u+2) overwrites dS^T(u), after dK(u) in issue order
         if (more) issue_dp(u + 2);
       }
-      if (ok) umma_commit(all_done);
+      if (ok) {
+        // all_done counts two commits: one per issuer, or both from one
+        umma_commit(all_done);
+        if (p.one_issuer) umma_commit(all_done);
+      }
       if (!ok) {
-        umma_commit(&drain[b]);
-        drain_wait(&drain[b], 0);
+        umma_commit(&drain[b0]);
+        drain_wait(&drain[b0], 0);
       }
     }
   } else {
@@ -614,21 +630,28 @@ __global__ void __launch_bounds__(352, 1) attn_dq_hs_kernel(const __grid_constan
       }
     }
   } else if (warp == 1 || warp == 10) {
-    if (lane == 0) {
+    // one issuer (fixed-order mode): warp 1 issues every sub-tile's products
+    // in sub-tile order, so dQ takes its products in a fixed order
+    if (lane == 0 && !(p.one_issuer && warp == 10)) {
       // ------------------------------------------------ MMA issuers
-      const int b = warp == 1 ? 0 : 1;  // this issuer's buffer and sub-tiles
-      const uint32_t tSb = tS + 64 * b, tdPb = tdP + 64 * b;
+      const int b0 = warp == 1 ? 0 : 1;  // this issuer's first sub-tile
+      const int ustep = p.one_issuer ? 1 : 2;
       const uint32_t uKV = smem_u32(sKV);
       // the 64 key rows of half b start 64 b rows into every chunk of the
-      // stage's K and V tiles (whole swizzle atoms)
+      // stage's K and V tiles (whole swizzle atoms); sub-tile u uses buffer
+      // b = u % 2
       auto uK = [&](int u) { return uKV + ((u >> 1) % KVS) * 2 * T::TILE; };
       auto issue_s = [&](int u) {
+        const int b = u & 1;
+        const uint32_t tSb = tS + 64 * b;
         const uint32_t k = uK(u) + 64 * T::SWB * b;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a(tSb, tQA + kk * 8, T::kmajor(k, kk), ID_S, kk > 0);
         umma_commit(&s_full[b]);
       };
       auto issue_dp = [&](int u) {
+        const int b = u & 1;
+        const uint32_t tdPb = tdP + 64 * b;
         const uint32_t v = uK(u) + T::TILE + 64 * T::SWB * b;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a(tdPb, tOA + kk * 8, T::kmajor(v, kk), ID_S, kk > 0);
@@ -638,13 +661,18 @@ __global__ void __launch_bounds__(352, 1) attn_dq_hs_kernel(const __grid_constan
         const int jt = u >> 1;
         return bounded_wait(&kv_full[jt % KVS], (jt / KVS) & 1, abort_flag, 671, p.err);
       };
-      bool ok = bounded_wait(qo_ready, 0, abort_flag, 672, p.err) && wait_stage(b);
+      bool ok = bounded_wait(qo_ready, 0, abort_flag, 672, p.err) && wait_stage(b0);
       if (ok) {
         tc_fence_after();
-        issue_s(b);
-        issue_dp(b);
+        // sub-tiles 0 and 1 share stage 0 (U is even)
+        for (int u = b0; u < 2; u += ustep) {
+          issue_s(u);
+          issue_dp(u);
+        }
       }
-      for (int u = b; ok && u < U; u += 2) {
+      for (int u = b0; ok && u < U; u += ustep) {
+        const int b = u & 1;
+        const uint32_t tdPb = tdP + 64 * b;
         const int st = (u >> 1) % KVS;
         const bool more = u + 2 < U;
         if (more) {
@@ -666,10 +694,14 @@ __global__ void __launch_bounds__(352, 1) attn_dq_hs_kernel(const __grid_constan
         // dP(u+2) overwrites dS(u), after dQ(u) in issue order
         if (more) issue_dp(u + 2);
       }
-      if (ok) umma_commit(all_done);
+      if (ok) {
+        // all_done counts two commits: one per issuer, or both from one
+        umma_commit(all_done);
+        if (p.one_issuer) umma_commit(all_done);
+      }
       if (!ok) {
-        umma_commit(&drain[b]);
-        drain_wait(&drain[b], 0);
+        umma_commit(&drain[b0]);
+        drain_wait(&drain[b0], 0);
       }
     }
   } else {
@@ -888,6 +920,7 @@ int attention_bwd(const AttnBwdShape& sh, const void* qkv, const void* o, const 
   prm.dv_col = (int)sh.dv_col;
   prm.scale = 1.f / sqrtf((float)f.d);
   prm.scale_log2 = prm.scale * 1.4426950408889634f;
+  prm.one_issuer = sh.deterministic ? 1 : 0;
   prm.err = device_error_word();
   if (!prm.err) return 3;
   switch (f.d) {

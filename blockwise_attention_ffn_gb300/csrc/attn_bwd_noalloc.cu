@@ -22,6 +22,7 @@
 #include <atomic>
 
 #include "../../include/bpt.h"
+#include "internal.h"
 
 namespace {
 
@@ -70,5 +71,6 @@ extern "C" int bpt_attention_bwd_noalloc(const bpt_config* cfg, const void* qkv,
   int st = BPT_OK;
   void* scratch = scratch_on_current_device(&st);
   if (!scratch) return st;
-  return bpt_attention_bwd(cfg, qkv, o, lse, dout, dqkv, scratch, (size_t)BPT_NOALLOC_SCRATCH_BYTES, stream);
+  return bpt::attention_bwd_call(cfg, qkv, o, lse, dout, dqkv, scratch, (size_t)BPT_NOALLOC_SCRATCH_BYTES, stream,
+                                1);
 }

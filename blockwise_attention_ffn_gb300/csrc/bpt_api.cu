@@ -39,6 +39,8 @@ struct Dims {
   int64_t Uk;      // key/value heads per stage
   int64_t qkv_w;   // columns of the (stage) projection buffer
   float rope;      // rotary embedding base (0: none)
+  bool det;        // BPT_FLAG_DETERMINISTIC
+  bool debug;      // BPT_FLAG_DEBUG_CHECKS
 };
 
 int validate(const bpt_config* c, Dims* D) {
@@ -55,7 +57,8 @@ int validate(const bpt_config* c, Dims* D) {
   if (c->ffn_block < 0 || (c->ffn_block % c->q_block)) return BPT_EINVAL;
   if (!(c->norm_eps > 0.f)) return BPT_EINVAL;
   if (c->act == BPT_ACT_SWIGLU && (c->ffn_dim % 64)) return BPT_EINVAL;
-  if (c->flags & ~(BPT_FLAG_ACCUM_GRADS | BPT_FLAG_ONE_STREAM)) return BPT_EINVAL;
+  if (c->flags & ~(BPT_FLAG_ACCUM_GRADS | BPT_FLAG_ONE_STREAM | BPT_FLAG_DETERMINISTIC | BPT_FLAG_DEBUG_CHECKS))
+    return BPT_EINVAL;
   const int d = c->head_dim;
   if (d != 64 && d != 80 && d != 96 && d != 112 && d != 128) return BPT_EUNSUPPORTED;
   const int G = c->n_heads / c->n_kv_heads;
@@ -81,6 +84,8 @@ int validate(const bpt_config* c, Dims* D) {
   D->rows = D->b * D->s;
   D->qkv_w = (D->U + 2 * D->Uk) * d;
   D->rope = c->rope_base;
+  D->det = (c->flags & BPT_FLAG_DETERMINISTIC) != 0;
+  D->debug = (c->flags & BPT_FLAG_DEBUG_CHECKS) != 0;
   return BPT_OK;
 }
 
@@ -101,6 +106,56 @@ int check_weights(const bpt_config* c, const bpt_weights* w) {
     if (c->act != BPT_ACT_SWIGLU && (!w->b1 || !aligned16(w->b1))) return BPT_EINVAL;
   }
   return BPT_OK;
+}
+
+// ---------------------------------------------------------------- debug checks
+// BPT_FLAG_DEBUG_CHECKS: every pointer argument, with the bytes the call
+// touches through it, must lie inside one device allocation of the current
+// device; after the launches the call synchronises and reports the device
+// error word itself.
+struct Span {
+  const void* p;
+  int64_t bytes;
+};
+
+int check_spans(const Span* sp, int n) {
+  for (int i = 0; i < n; ++i)
+    if (sp[i].bytes > 0 && check_device_range(sp[i].p, (size_t)sp[i].bytes)) return BPT_EINVAL;
+  return BPT_OK;
+}
+
+// The parameters a config uses (bpt_weights / bpt_grads field order), `elem`
+// bytes per element; returns the count written to out[17].
+int param_spans(const bpt_config* c, const Dims& D, const void* const f[17], int elem, Span* out) {
+  const bool ln = c->norm == BPT_NORM_LAYER, hb = c->has_bias != 0, sw = c->act == BPT_ACT_SWIGLU;
+  const int64_t h = D.h, q = D.H * D.d, kv = D.Hkv * D.d, ff = D.f;
+  const int64_t n[17] = {h,          ln ? h : 0,  q * h,  hb ? q : 0,           kv * h, hb ? kv : 0,
+                         kv * h,     hb ? kv : 0, h * q,  hb ? h : 0,           h,      ln ? h : 0,
+                         ff * h,     hb && !sw ? ff : 0,  h * ff, hb ? h : 0,   sw ? ff * h : 0};
+  for (int i = 0; i < 17; ++i) out[i] = Span{f[i], n[i] * elem};
+  return 17;
+}
+
+int check_weights_range(const bpt_config* c, const Dims& D, const bpt_weights* w) {
+  const void* f[17] = {w->ln1_w, w->ln1_b, w->wq, w->bq, w->wk, w->bk, w->wv, w->bv, w->wo,
+                       w->bo,    w->ln2_w, w->ln2_b, w->w1, w->b1, w->w2, w->b2, w->w3};
+  Span sp[17];
+  return check_spans(sp, param_spans(c, D, f, 2, sp));
+}
+
+int check_grads_range(const bpt_config* c, const Dims& D, const bpt_grads* g) {
+  const void* f[17] = {g->ln1_w, g->ln1_b, g->wq, g->bq, g->wk, g->bk, g->wv, g->bv, g->wo,
+                       g->bo,    g->ln2_w, g->ln2_b, g->w1, g->b1, g->w2, g->b2, g->w3};
+  Span sp[17];
+  return check_spans(sp, param_spans(c, D, f, 4, sp));
+}
+
+// After the launches: wait for them and report the error word (which the
+// read clears) or the failure of the synchronisation itself.
+int debug_finish(cudaStream_t st) {
+  unsigned int e[4] = {0, 0, 0, 0};
+  if (read_device_error(st, e)) return BPT_ECUDA;
+  return e[0] ? BPT_ETIMEOUT : BPT_OK;
 }
 
 // ---------------------------------------------------------------- workspace
@@ -134,6 +189,9 @@ size_t plan_fwd(const Dims& D, void* base, FwdWs* w, bool need_lse) {
 struct BwdWs {
   void *xn, *qkv, *o, *x1, *x1n, *gd, *g, *u, *a, *dz, *dx1n, *dx1, *dO, *dqkv, *attn;
   float *dxn, *dx1f;
+  // fixed-order mode: per-block partial sums of the norm backward (main
+  // stream) and of the bias column sums (second stream); null otherwise
+  float *part_main, *part_side;
 };
 AttnBwdShape stage_bwd_shape(const Dims& D, int64_t k);
 size_t plan_bwd(const Dims& D, void* base, BwdWs* w) {
@@ -156,6 +214,12 @@ size_t plan_bwd(const Dims& D, void* base, BwdWs* w) {
   w->dqkv = c.take(D.rows * D.qkv_w * 2);
   w->dxn = reinterpret_cast<float*>(c.take(D.rows * D.h * 4));
   w->attn = c.take(attention_bwd_ws_bytes(stage_bwd_shape(D, 0)));
+  w->part_main = w->part_side = nullptr;
+  if (D.det) {
+    w->part_main = reinterpret_cast<float*>(c.take(norm_bwd_part_floats((int)D.h) * 4));
+    const int64_t widest = std::max(std::max(D.h, D.f), D.qkv_w);
+    w->part_side = reinterpret_cast<float*>(c.take(colsum_part_floats(widest) * 4));
+  }
   return c.off;
 }
 
@@ -304,6 +368,9 @@ int gemm_kseg(int64_t M, int64_t N, const MatView& A, const MatView* B, const in
   return 0;
 }
 
+int layer_fwd(const bpt_config* cfg, const Dims& D, const bpt_weights* w, const void* x, void* y, void* saved,
+              const FwdWs& W, cudaStream_t st);
+
 }  // namespace
 
 extern "C" {
@@ -370,8 +437,25 @@ int bpt_layer_fwd(const bpt_config* cfg, const bpt_weights* w, const void* x, vo
   FwdWs W;
   const size_t need = plan_fwd(D, nullptr, &W, saved == nullptr);
   if (ws_bytes < need) return BPT_ENOSPC;
+  if (D.debug) {
+    const int64_t act = D.rows * D.h * 2;
+    const Span sp[] = {{x, act}, {y, act}, {saved, saved ? D.b * D.H * D.s_pad * 4 : 0}, {ws, (int64_t)need}};
+    if (check_spans(sp, 4) || check_weights_range(cfg, D, w)) return BPT_EINVAL;
+  }
   plan_fwd(D, ws, &W, saved == nullptr);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  rc = layer_fwd(cfg, D, w, x, y, saved, W, st);
+  if (rc) return rc;
+  return D.debug ? debug_finish(st) : BPT_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+int layer_fwd(const bpt_config* cfg, const Dims& D, const bpt_weights* w, const void* x, void* y, void* saved,
+              const FwdWs& W, cudaStream_t st) {
+  int rc;
   float* lse = saved ? reinterpret_cast<float*>(saved) : W.lse;
   const bool hb = cfg->has_bias != 0;
   const int64_t h = D.h, f = D.f, Hd = D.H * D.d;
@@ -458,6 +542,10 @@ int bpt_layer_fwd(const bpt_config* cfg, const bpt_weights* w, const void* x, vo
   return BPT_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
 int bpt_attn_headchunk(const bpt_config* cfg, const bpt_weights* w, const void* xn, void* o, void* lse,
                        void* ws, size_t ws_bytes, void* stream) {
   Dims D;
@@ -467,7 +555,17 @@ int bpt_attn_headchunk(const bpt_config* cfg, const bpt_weights* w, const void* 
   if (cfg->has_bias && (!w->bq || !w->bk || !w->bv)) return BPT_EINVAL;
   if (!aligned16(xn) || !aligned16(o) || !aligned16(ws) || (lse && !aligned16(lse))) return BPT_EINVAL;
   void* qkv;
-  if (ws_bytes < plan_headchunk(D, nullptr, &qkv)) return BPT_ENOSPC;
+  const size_t need = plan_headchunk(D, nullptr, &qkv);
+  if (ws_bytes < need) return BPT_ENOSPC;
+  if (D.debug) {
+    const int64_t q = D.H * D.d, kv = D.Hkv * D.d, h = D.h;
+    const bool hb = cfg->has_bias != 0;
+    const Span sp[] = {{xn, D.rows * h * 2},      {o, D.rows * q * 2}, {lse, lse ? D.b * D.H * D.s_pad * 4 : 0},
+                       {ws, (int64_t)need},       {w->wq, q * h * 2},  {w->wk, kv * h * 2},
+                       {w->wv, kv * h * 2},       {w->bq, hb ? q * 2 : 0}, {w->bk, hb ? kv * 2 : 0},
+                       {w->bv, hb ? kv * 2 : 0}};
+    if (check_spans(sp, 10)) return BPT_EINVAL;
+  }
   plan_headchunk(D, ws, &qkv);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   for (int64_t k = 0; k < D.n_stages; ++k) {
@@ -475,7 +573,7 @@ int bpt_attn_headchunk(const bpt_config* cfg, const bpt_weights* w, const void* 
     AttnShape a = stage_attn_shape(D, k, cfg->causal);
     if ((rc = attention_fwd(a, qkv, o, reinterpret_cast<float*>(lse), st))) return rc;
   }
-  return BPT_OK;
+  return D.debug ? debug_finish(st) : BPT_OK;
 }
 
 int bpt_attention_fwd(const bpt_config* cfg, const void* qkv, void* o, void* lse, void* stream) {
@@ -487,8 +585,15 @@ int bpt_attention_fwd(const bpt_config* cfg, const void* qkv, void* o, void* lse
   F.U = D.H;
   F.Uk = D.Hkv;
   F.qkv_w = (D.H + 2 * D.Hkv) * D.d;
+  if (D.debug) {
+    const Span sp[] = {{qkv, D.rows * F.qkv_w * 2}, {o, D.rows * D.H * D.d * 2},
+                       {lse, lse ? D.b * D.H * D.s_pad * 4 : 0}};
+    if (check_spans(sp, 3)) return BPT_EINVAL;
+  }
   AttnShape a = stage_attn_shape(F, 0, cfg->causal);
-  return attention_fwd(a, qkv, o, reinterpret_cast<float*>(lse), reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if ((rc = attention_fwd(a, qkv, o, reinterpret_cast<float*>(lse), st))) return rc;
+  return D.debug ? debug_finish(st) : BPT_OK;
 }
 
 size_t bpt_attention_bwd_workspace_bytes(const bpt_config* cfg) {
@@ -505,6 +610,16 @@ size_t bpt_attention_bwd_workspace_bytes(const bpt_config* cfg) {
 
 int bpt_attention_bwd(const bpt_config* cfg, const void* qkv, const void* o, const void* lse, const void* dout,
                       void* dqkv, void* ws, size_t ws_bytes, void* stream) {
+  return bpt::attention_bwd_call(cfg, qkv, o, lse, dout, dqkv, ws, ws_bytes, stream, 0);
+}
+
+}  // extern "C"
+
+// The attention backward behind both entry points; ws_is_library: the
+// workspace is the library's own array (not checked under the debug flag).
+int bpt::attention_bwd_call(const bpt_config* cfg, const void* qkv, const void* o, const void* lse,
+                            const void* dout, void* dqkv, void* ws, size_t ws_bytes, void* stream,
+                            int ws_is_library) {
   Dims D;
   int rc = validate(cfg, &D);
   if (rc) return rc;
@@ -518,10 +633,21 @@ int bpt_attention_bwd(const bpt_config* cfg, const void* qkv, const void* o, con
   F.qkv_w = (D.H + 2 * D.Hkv) * D.d;
   AttnBwdShape s = stage_bwd_shape(F, 0);
   s.f.causal = cfg->causal;
-  if (ws_bytes < attention_bwd_ws_bytes(s)) return BPT_ENOSPC;
-  return attention_bwd(s, qkv, o, reinterpret_cast<const float*>(lse), dout, dqkv, ws,
-                       reinterpret_cast<cudaStream_t>(stream));
+  s.deterministic = D.det;
+  const size_t need = attention_bwd_ws_bytes(s);
+  if (ws_bytes < need) return BPT_ENOSPC;
+  if (D.debug) {
+    const int64_t packed = D.rows * F.qkv_w * 2, hd = D.rows * D.H * D.d * 2;
+    const Span sp[] = {{qkv, packed}, {o, hd}, {lse, D.b * D.H * D.s_pad * 4}, {dout, hd}, {dqkv, packed},
+                       {ws, ws_is_library ? 0 : (int64_t)need}};
+    if (check_spans(sp, 6)) return BPT_EINVAL;
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if ((rc = attention_bwd(s, qkv, o, reinterpret_cast<const float*>(lse), dout, dqkv, ws, st))) return rc;
+  return D.debug ? debug_finish(st) : BPT_OK;
 }
+
+extern "C" {
 
 int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, const void* saved, const void* dy,
                   void* dx, const bpt_grads* g, void* ws, size_t ws_bytes, void* stream) {
@@ -542,7 +668,13 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
       return BPT_EINVAL;
   }
   BwdWs W;
-  if (ws_bytes < plan_bwd(D, nullptr, &W)) return BPT_ENOSPC;
+  const size_t need = plan_bwd(D, nullptr, &W);
+  if (ws_bytes < need) return BPT_ENOSPC;
+  if (D.debug) {
+    const int64_t act = D.rows * D.h * 2;
+    const Span sp[] = {{x, act}, {dy, act}, {dx, act}, {saved, D.b * D.H * D.s_pad * 4}, {ws, (int64_t)need}};
+    if (check_spans(sp, 5) || check_weights_range(cfg, D, w) || check_grads_range(cfg, D, g)) return BPT_EINVAL;
+  }
   plan_bwd(D, ws, &W);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   Side* sd = side_stream();
@@ -589,6 +721,7 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
           MatView A{bf(W.o, row * Hd), nr, Hd, Hd};
           MatView B{w->wo, h, Hd, Hd};
           Epilogue e;
+          e.deterministic = D.det;
           e.kind = EPI_F32;  // x1 stays fp32: the residual stream is rounded once, at y
           e.out = W.x1;
           e.ldo = h;
@@ -606,6 +739,7 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
           MatView A{W.x1n, nr, h, h};
           MatView B{w->w1, f, h, h};
           Epilogue e;
+          e.deterministic = D.det;
           e.out = W.a;
           e.ldo = f;
           if (swiglu) {
@@ -633,18 +767,20 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
           MatView A{dyb, nr, h, h};     // MN-major: [K = rows, M = h]
           MatView B{W.a, nr, f, f};     // MN-major: [K = rows, N = f]
           Epilogue e;
+          e.deterministic = D.det;
           e.kind = EPI_F32;
           e.out = g->w2;
           e.ldo = f;
           e.beta = beta;
           if ((rc = gemm(h, f, nr, A, true, &B, &nr, 1, true, nullptr, e, ss))) return rc;
-          if (hb && (rc = colsum(nr, h, dyb, h, reinterpret_cast<float*>(g->b2), beta != 0.f, ss))) return rc;
+          if (hb && (rc = colsum(nr, h, dyb, h, reinterpret_cast<float*>(g->b2), beta != 0.f, ss, W.part_side))) return rc;
         }
         // dA = dy W2, fused with the activation gradient
         {
           MatView A{dyb, nr, h, h};
           MatView B{w->w2, h, f, f};  // [K = h rows, N = f cols]
           Epilogue e;
+          e.deterministic = D.det;
           if (swiglu) {
             e.kind = EPI_SWIGLU_BWD;
             e.aux = W.g;
@@ -672,6 +808,7 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
           const int64_t ldz = swiglu ? 2 * f : f;
           MatView B{W.x1n, nr, h, h};
           Epilogue e;
+          e.deterministic = D.det;
           e.kind = EPI_F32;
           e.ldo = h;
           e.beta = beta;
@@ -683,12 +820,13 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
             e.out = g->w3;
             if ((rc = gemm(f, h, nr, A2, true, &B, &nr, 1, true, nullptr, e, ss))) return rc;
           } else if (hb) {
-            if ((rc = colsum(nr, f, W.dz, f, reinterpret_cast<float*>(g->b1), beta != 0.f, ss))) return rc;
+            if ((rc = colsum(nr, f, W.dz, f, reinterpret_cast<float*>(g->b1), beta != 0.f, ss, W.part_side))) return rc;
           }
         }
         // dx1n = dz W1  (SwiGLU: dg Wg + du Wu)
         {
           Epilogue e;
+          e.deterministic = D.det;
           e.kind = EPI_BF16;
           e.out = W.dx1n;
           e.ldo = h;
@@ -711,7 +849,7 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
         {
           NormBwdIO io{W.dx1n, 0, h, W.x1, 1, h, dyb, 0, h, bfm(W.dx1, row * h), W.dx1f + row * h, h};
           if ((rc = norm_bwd(nr, (int)h, cfg->norm, cfg->norm_eps, io, w->ln2_w, reinterpret_cast<float*>(g->ln2_w),
-                             ln ? reinterpret_cast<float*>(g->ln2_b) : nullptr, st)))
+                             ln ? reinterpret_cast<float*>(g->ln2_b) : nullptr, st, W.part_main)))
             return rc;
         }
         first = false;
@@ -727,16 +865,18 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
       MatView A2{W.dx1, D.rows, h, h};
       MatView B2{W.o, D.rows, Hd, Hd};
       Epilogue e2;
+      e2.deterministic = D.det;
       e2.kind = EPI_F32;
       e2.out = g->wo;
       e2.ldo = Hd;
       e2.beta = accum ? 1.f : 0.f;
       const int64_t K = D.rows;
       if ((rc = gemm(h, Hd, K, A2, true, &B2, &K, 1, true, nullptr, e2, ss))) return rc;
-      if (hb && (rc = colsum(D.rows, h, W.dx1, h, reinterpret_cast<float*>(g->bo), accum, ss))) return rc;
+      if (hb && (rc = colsum(D.rows, h, W.dx1, h, reinterpret_cast<float*>(g->bo), accum, ss, W.part_side))) return rc;
       MatView A{W.dx1, D.rows, h, h};
       MatView B{w->wo, h, Hd, Hd};  // [K = h rows, N = Hd cols]
       Epilogue e;
+      e.deterministic = D.det;
       e.out = W.dO;
       e.ldo = Hd;
       if ((rc = gemm(D.rows, Hd, h, A, false, &B, &h, 1, true, nullptr, e, st))) return rc;
@@ -762,6 +902,7 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
       if (k > 0 && (rc = join())) return rc;
       AttnBwdShape sb = stage_bwd_shape(D, k);
       sb.f.causal = cfg->causal;
+      sb.deterministic = D.det;
       if ((rc = attention_bwd(sb, W.qkv, W.o, lse, W.dO, W.dqkv, W.attn, st))) return rc;
       // dQ, dK are gradients of the rotated heads: turn them back
       if (rope && (rc = rope_apply(D.rows, (int)D.s, W.dqkv, D.qkv_w, 0, (int)(D.U + D.Uk), (int)d, D.rope, 1, st)))
@@ -775,6 +916,7 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
             {bf(w->wq, q0 * h), nq, h, h}, {bf(w->wk, kv0 * h), nkv, h, h}, {bf(w->wv, kv0 * h), nkv, h, h}};
         int64_t ks[3] = {nq, nkv, nkv};
         Epilogue e;
+        e.deterministic = D.det;
         e.kind = EPI_F32;
         e.out = W.dxn;
         e.ldo = h;
@@ -795,13 +937,14 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
         for (auto& pc : pieces) {
           MatView A{bf(W.dqkv, pc.col), D.rows, pc.n, D.qkv_w};
           Epilogue e;
+          e.deterministic = D.det;
           e.kind = EPI_F32;
           e.out = f32(pc.G, pc.row0 * h);
           e.ldo = h;
           e.beta = accum ? 1.f : 0.f;
           if ((rc = gemm(pc.n, h, K, A, true, &B, &K, 1, true, nullptr, e, ss))) return rc;
           if (hb && (pc.Gb != g->bk || rope) &&
-              (rc = colsum(D.rows, pc.n, bf(W.dqkv, pc.col), D.qkv_w, f32(pc.Gb, pc.row0), accum, ss)))
+              (rc = colsum(D.rows, pc.n, bf(W.dqkv, pc.col), D.qkv_w, f32(pc.Gb, pc.row0), accum, ss, W.part_side)))
             return rc;
         }
       }
@@ -811,7 +954,7 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
     {
       NormBwdIO io{W.dxn, 1, h, x, 0, h, W.dx1f, 1, h, dx, nullptr, h};
       if ((rc = norm_bwd(D.rows, (int)h, cfg->norm, cfg->norm_eps, io, w->ln1_w, reinterpret_cast<float*>(g->ln1_w),
-                         ln ? reinterpret_cast<float*>(g->ln1_b) : nullptr, st)))
+                         ln ? reinterpret_cast<float*>(g->ln1_b) : nullptr, st, W.part_main)))
         return rc;
     }
     return BPT_OK;
@@ -820,7 +963,9 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
   // everything issued on the side stream is ordered before the caller's next
   // work on the main stream
   const int jr = join();
-  return rc ? rc : (jr ? BPT_ECUDA : BPT_OK);
+  if (rc) return rc;
+  if (jr) return BPT_ECUDA;
+  return D.debug ? debug_finish(st) : BPT_OK;
 }
 
 }  // extern "C"

@@ -733,7 +733,7 @@ int gemm(int64_t M, int64_t N, int64_t K, const MatView& A, bool a_mn, const Mat
     auto fill = [&](int64_t units) { return (double)units / (double)(((units + nsm - 1) / nsm) * nsm); };
     const bool aligned = (e.ldo % 4) == 0 && (reinterpret_cast<uintptr_t>(e.out) & 15) == 0;
     if (!dual && e.kind == EPI_F32 && !e.bias && !e.res && (e.beta == 0.f || e.beta == 1.f) && aligned && nsm > 0 &&
-        fill(tiles) < 0.8) {
+        !e.deterministic && fill(tiles) < 0.8) {
       for (int ks = 2; ks <= 8 && p.nkt / ks >= 16; ++ks)
         if (fill(tiles * ks) >= 0.9) {
           p.ksplit = ks;

@@ -161,6 +161,40 @@ __global__ void watchdog_selftest_kernel(unsigned int* err, int site) {
   asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(&bar)) : "memory");
 }
 
+// [p, p + bytes) inside one device allocation of the current device: the
+// runtime classifies the pointer (device or managed memory, on this device)
+// and the driver gives the allocation holding it (its base and size), taken
+// through the driver entry point like the tensor-map encoder.
+typedef CUresult (*PfnMemGetAddressRange)(CUdeviceptr*, size_t*, CUdeviceptr);
+
+int check_device_range(const void* p, size_t bytes) {
+  if (!p) return 1;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // the query's error is not the caller's
+    return 1;
+  }
+  if ((a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) || a.device != dev) return 1;
+  static std::atomic<PfnMemGetAddressRange> cached{nullptr};
+  PfnMemGetAddressRange fn = cached.load(std::memory_order_acquire);
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !f)
+      return 1;
+    fn = reinterpret_cast<PfnMemGetAddressRange>(f);
+    cached.store(fn, std::memory_order_release);
+  }
+  CUdeviceptr base = 0;
+  size_t size = 0;
+  if (fn(&base, &size, reinterpret_cast<CUdeviceptr>(p)) != CUDA_SUCCESS) return 1;
+  const uint64_t lo = reinterpret_cast<uint64_t>(p);
+  return (lo >= base && bytes <= size && lo - base <= size - bytes) ? 0 : 1;
+}
+
 // Reads and clears the error word (synchronising the stream first).
 int read_device_error(cudaStream_t st, unsigned int out[4]) {
   cudaError_t e = cudaStreamSynchronize(st);
@@ -178,6 +212,10 @@ int read_device_error(cudaStream_t st, unsigned int out[4]) {
 }  // namespace bpt
 
 extern "C" {
+
+int bpt_check_device_range(const void* ptr, size_t bytes) {
+  return bpt::check_device_range(ptr, bytes) ? BPT_EINVAL : BPT_OK;
+}
 
 int bpt_watchdog_selftest(void* stream) {
   unsigned int* err = bpt::device_error_word();

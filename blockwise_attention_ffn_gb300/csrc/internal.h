@@ -8,6 +8,8 @@
 
 #include <atomic>
 
+#include "../../include/bpt.h"
+
 namespace bpt {
 
 // ---------------------------------------------------------------- profiling
@@ -26,6 +28,9 @@ unsigned int* device_error_word();
 int read_device_error(cudaStream_t st, unsigned int out[4]);
 // streaming multiprocessors of the current device (0 on error), cached per device
 int sm_count();
+// 0 if [p, p + bytes) lies inside one device allocation of the current
+// device, else 1 (the debug checks of BPT_FLAG_DEBUG_CHECKS)
+int check_device_range(const void* p, size_t bytes);
 
 // Raises a kernel's dynamic shared-memory limit to `bytes` on the current
 // device, once per device (the attribute belongs to the kernel's instance in
@@ -90,6 +95,9 @@ struct Epilogue {
   const void* aux2 = nullptr;
   int64_t ldaux2 = 0;
   float beta = 0.f;
+  // fixed summation order: no K split (a split adds its K ranges' shares in
+  // L2 in whatever order they land)
+  int deterministic = 0;
 };
 
 // Returns 0 or a BPT_* status.
@@ -120,6 +128,9 @@ struct AttnBwdShape {
   AttnShape f;            // forward geometry (q_begin/q_end ignored: all rows)
   int64_t ld_do, do_col;  // dO [b*s, ld_do], head n at do_col + n*d
   int64_t ld_dqkv, dq_col, dk_col, dv_col;  // outputs, bf16
+  // one MMA-issuing thread per CTA, so every accumulator takes its products
+  // in a fixed order (the default two issuers add in arrival order)
+  int deterministic = 0;
 };
 // ws: fp32 dQ accumulator [b*s, H*d] followed by D [b, H, s_pad] fp32
 // (s_pad = s rounded up to 128); lse is [b, H_total, s_pad].
@@ -127,12 +138,21 @@ size_t attention_bwd_ws_bytes(const AttnBwdShape& sh);
 int attention_bwd(const AttnBwdShape& sh, const void* qkv, const void* o, const float* lse,
                   const void* dout, void* dqkv, void* ws, cudaStream_t st);
 
+// The checks and launches of bpt_attention_bwd with the workspace given;
+// ws_is_library: the workspace is the library's own array (the
+// no-allocation entry point), which the debug checks do not inspect.
+int attention_bwd_call(const bpt_config* cfg, const void* qkv, const void* o, const void* lse, const void* dout,
+                       void* dqkv, void* ws, size_t ws_bytes, void* stream, int ws_is_library);
+
 // ---------------------------------------------------------------- norms & misc
 // y = norm(x) * w (+ b), rows of width h; x is bf16 or (x_f32) fp32; y bf16.
 int norm_fwd(int64_t rows, int h, int kind, float eps, const void* x, int x_f32, int64_t ldx,
              const void* w, const void* b, void* y, int64_t ldy, cudaStream_t st);
 // dx = res + d/dx norm (given dy, x, w); dw/db partial sums accumulated into
-// the fp32 vectors with atomics (they must be zeroed or hold the running sum).
+// the fp32 vectors (they must be zeroed or hold the running sum): with
+// atomics, or, when `part` is given, written per block to part and added in
+// block order by a second kernel (a fixed summation order; part holds
+// norm_bwd_part_floats(h) floats).
 // dy, x and res are each bf16 or fp32 (the *_f32 flags); dx is written as
 // bf16 and, when dx_f32 is given, also as fp32 (same leading dimension).
 struct NormBwdIO {
@@ -142,10 +162,14 @@ struct NormBwdIO {
   void* dx; float* dx_f32; int64_t lddx;
 };
 int norm_bwd(int64_t rows, int h, int kind, float eps, const NormBwdIO& io, const void* w, float* dw,
-             float* db, cudaStream_t st);
-// out[n] (+)= sum over rows of in[row, n]  (bf16 in, fp32 out)
+             float* db, cudaStream_t st, float* part = nullptr);
+int64_t norm_bwd_part_floats(int h);
+// out[n] (+)= sum over rows of in[row, n]  (bf16 in, fp32 out); with atomics,
+// or, when `part` is given (colsum_part_floats(n) floats), per-band partial
+// sums added in band order by a second kernel
 int colsum(int64_t rows, int64_t n, const void* in, int64_t ld, float* out, int accumulate,
-           cudaStream_t st);
+           cudaStream_t st, float* part = nullptr);
+int64_t colsum_part_floats(int64_t n);
 // Rotary position embedding in place: n_heads heads of d columns from column
 // col0 of bf16 buf [rows, ld], row r at position r % s, pair (i, i + d/2)
 // turned by (r % s) * base^(-2i/d) (inverse: by minus that).  d % 4 == 0,

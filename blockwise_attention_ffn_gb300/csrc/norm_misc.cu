@@ -9,6 +9,8 @@
 // per row, 16-byte vector accesses; rows are re-read from L1/L2 between passes.
 #include <math.h>
 
+#include <algorithm>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -116,9 +118,11 @@ __global__ void norm_fwd_kernel(int64_t rows, int h, int kind, float eps, const 
 // The loops store through pointers the compiler must assume alias the
 // inputs, so they load a group of chunks (phase 1) or two rows (phase 2)
 // before any store: one load in flight per thread would leave HBM idle.
+// With `part` (the fixed-order mode) each block writes its column sums to
+// part[blockIdx.x][0, h) (dw) and [h, 2h) (db) instead of adding them.
 __global__ void __launch_bounds__(512) norm_bwd_kernel(int64_t rows, int h, int kind, float eps, NormBwdIO io,
                                                         const __nv_bfloat16* w, float* dw, float* db,
-                                                        int64_t band) {
+                                                        int64_t band, float* part) {
   extern __shared__ float stat[];  // [sub-band row][4]: mean, rstd, mean(g), mean(g * xhat)
   constexpr int NB1 = 2;           // chunk groups of phase 1 (the accumulators stay live)
   const int lane = threadIdx.x & 31;
@@ -231,10 +235,19 @@ __global__ void __launch_bounds__(512) norm_bwd_kernel(int64_t rows, int h, int 
       __syncthreads();
     }
     if (active) {
+      if (part) {
+        float* pw = part + (int64_t)blockIdx.x * 2 * h + c;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        if (dw) atomicAdd(&dw[c + k], adw[k]);
-        if (db) atomicAdd(&db[c + k], adb[k]);
+        for (int k = 0; k < 8; ++k) {
+          pw[k] = adw[k];
+          pw[h + k] = adb[k];
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (dw) atomicAdd(&dw[c + k], adw[k]);
+          if (db) atomicAdd(&db[c + k], adb[k]);
+        }
       }
     }
   }
@@ -245,11 +258,14 @@ __global__ void __launch_bounds__(512) norm_bwd_kernel(int64_t rows, int h, int 
 // A block covers 256 columns (8 per lane of a warp) and a band of rows; its 8
 // warps take every 8th row of the band, four rows in flight at a time, and
 // combine their partial sums in shared memory so the block issues one atomic
-// per column.  n and ld are multiples of 8 (16-byte row segments).
+// per column.  n and ld are multiples of 8 (16-byte row segments).  With
+// `part` (the fixed-order mode) the block's sums go to part[blockIdx.y][.]
+// instead.
 constexpr int COLSUM_WARPS = 8;
 __global__ void __launch_bounds__(32 * COLSUM_WARPS) colsum_kernel(int64_t rows, int64_t n, const __nv_bfloat16* in,
-                                                                   int64_t ld, int64_t band, float* out) {
-  __shared__ float part[COLSUM_WARPS][256 + 4];
+                                                                   int64_t ld, int64_t band, float* out, float* part) {
+  __shared__ float part_s[COLSUM_WARPS][256 + 4];
+  float* dst_part = part;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t c = (int64_t)blockIdx.x * 256 + lane * 8;
   const int64_t r0 = (int64_t)blockIdx.y * band;
@@ -274,16 +290,29 @@ __global__ void __launch_bounds__(32 * COLSUM_WARPS) colsum_kernel(int64_t rows,
     }
   }
 #pragma unroll
-  for (int k = 0; k < 8; ++k) part[w][lane * 8 + k] = acc[k];
+  for (int k = 0; k < 8; ++k) part_s[w][lane * 8 + k] = acc[k];
   __syncthreads();
   const int col = threadIdx.x;  // 256 threads, one column each
   const int64_t gc = (int64_t)blockIdx.x * 256 + col;
   if (gc < n) {
     float t = 0.f;
 #pragma unroll
-    for (int i = 0; i < COLSUM_WARPS; ++i) t += part[i][col];
-    atomicAdd(&out[gc], t);
+    for (int i = 0; i < COLSUM_WARPS; ++i) t += part_s[i][col];
+    if (dst_part)
+      dst_part[(int64_t)blockIdx.y * n + gc] = t;
+    else
+      atomicAdd(&out[gc], t);
   }
+}
+
+// out[c] += sum over p = 0, 1, ..., nparts - 1 (in that order) of
+// part[p * ldp + c]: the second half of the fixed-order column sums.
+__global__ void reduce_parts_kernel(int nparts, int64_t n, const float* part, int64_t ldp, float* out) {
+  const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= n) return;
+  float t = 0.f;
+  for (int p = 0; p < nparts; ++p) t += part[(int64_t)p * ldp + c];
+  out[c] += t;
 }
 
 __global__ void f32_to_bf16_kernel(int64_t rows, int64_t n, const float* src, int64_t lds,
@@ -421,8 +450,23 @@ int norm_fwd(int64_t rows, int h, int kind, float eps, const void* x, int x_f32,
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 
+// blocks of the fixed-order norm backward, whose partial sums (dw and db:
+// 2h floats per block) the caller's workspace holds
+constexpr int64_t NORM_DET_BLOCKS = 256;
+// bands (row ranges, one per block row) of the fixed-order column sums
+constexpr int64_t COLSUM_DET_BANDS = 64;
+
+int64_t norm_bwd_part_floats(int h) { return NORM_DET_BLOCKS * 2 * (int64_t)h; }
+int64_t colsum_part_floats(int64_t n) { return COLSUM_DET_BANDS * n; }
+
+int reduce_parts(int nparts, int64_t n, const float* part, int64_t ldp, float* out, cudaStream_t st) {
+  if (nparts <= 0 || n <= 0) return 0;
+  reduce_parts_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(nparts, n, part, ldp, out);
+  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
 int norm_bwd(int64_t rows, int h, int kind, float eps, const NormBwdIO& io, const void* w, float* dw,
-             float* db, cudaStream_t st) {
+             float* db, cudaStream_t st, float* part) {
   if (rows <= 0) return 0;
   // one thread per 8 columns (a whole row per block up to h = 4096), 64..512
   // threads
@@ -440,6 +484,8 @@ int norm_bwd(int64_t rows, int h, int kind, float eps, const NormBwdIO& io, cons
   int64_t band = (rows + nsm * per_sm - 1) / (nsm * per_sm);
   if (band < 8) band = 8;
   if (band > 2048) band = 2048;
+  // fixed order: at most NORM_DET_BLOCKS blocks, one partial row each
+  if (part) band = std::max<int64_t>(8, (rows + NORM_DET_BLOCKS - 1) / NORM_DET_BLOCKS);
   const int64_t grid = (rows + band - 1) / band;
   const size_t smem = (size_t)2 * (threads / 32) * 4 * sizeof(float);  // one sub-band of statistics
   ProfScope prof(PROF_NORM, 0.0,
@@ -447,12 +493,17 @@ int norm_bwd(int64_t rows, int h, int kind, float eps, const NormBwdIO& io, cons
                                      (io.dx_f32 ? 4 : 0)),
                  st);
   norm_bwd_kernel<<<(unsigned)grid, threads, smem, st>>>(rows, h, kind, eps, io, (const __nv_bfloat16*)w, dw, db,
-                                                         band);
-  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+                                                         band, part);
+  if (cudaGetLastError() != cudaSuccess) return 3;
+  if (part) {
+    if (dw && reduce_parts((int)grid, h, part, 2 * (int64_t)h, dw, st)) return 3;
+    if (db && reduce_parts((int)grid, h, part + h, 2 * (int64_t)h, db, st)) return 3;
+  }
+  return 0;
 }
 
 int colsum(int64_t rows, int64_t n, const void* in, int64_t ld, float* out, int accumulate,
-           cudaStream_t st) {
+           cudaStream_t st, float* part) {
   if (!accumulate && cudaMemsetAsync(out, 0, n * sizeof(float), st) != cudaSuccess) return 3;
   if (rows <= 0 || n <= 0) return 0;
   ProfScope prof(PROF_MISC, 0.0, (double)rows * n * 2, st);
@@ -460,13 +511,15 @@ int colsum(int64_t rows, int64_t n, const void* in, int64_t ld, float* out, int 
   const int nsm = sm_count();
   const int64_t gx = (n + 255) / 256;
   int64_t gy = (4 * (nsm > 0 ? nsm : 1) + gx - 1) / gx;
+  if (part) gy = std::min(gy, COLSUM_DET_BANDS);
   int64_t band = (rows + gy - 1) / gy;
   band = (band + COLSUM_WARPS - 1) / COLSUM_WARPS * COLSUM_WARPS;
   if (band < 4 * COLSUM_WARPS) band = 4 * COLSUM_WARPS;
   gy = (rows + band - 1) / band;
   dim3 grid((unsigned)gx, (unsigned)gy);
-  colsum_kernel<<<grid, 32 * COLSUM_WARPS, 0, st>>>(rows, n, (const __nv_bfloat16*)in, ld, band, out);
-  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+  colsum_kernel<<<grid, 32 * COLSUM_WARPS, 0, st>>>(rows, n, (const __nv_bfloat16*)in, ld, band, out, part);
+  if (cudaGetLastError() != cudaSuccess) return 3;
+  return part ? reduce_parts((int)gy, n, part, n, out, st) : 0;
 }
 
 int f32_to_bf16(int64_t rows, int64_t n, const float* src, int64_t ld_src, void* dst, int64_t ld_dst,

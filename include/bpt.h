@@ -73,7 +73,42 @@ enum {
 
 enum { BPT_NORM_LAYER = 0, BPT_NORM_RMS = 1 };
 enum { BPT_ACT_GELU_ERF = 0, BPT_ACT_GELU_TANH = 1, BPT_ACT_SWIGLU = 2 };
-enum { BPT_FLAG_ACCUM_GRADS = 1, BPT_FLAG_ONE_STREAM = 2 };
+/* Flags (bpt_config.flags, OR-ed):
+ *  BPT_FLAG_ACCUM_GRADS   weight gradients are added to (+=) instead of
+ *                         overwritten.
+ *  BPT_FLAG_ONE_STREAM    every launch of bpt_layer_bwd on the caller's
+ *                         stream, in issue order (no second stream).
+ *  BPT_FLAG_DETERMINISTIC every floating-point sum is taken in an order
+ *                         fixed by the shapes and the device's SM count, so
+ *                         two calls with the same inputs on the same device
+ *                         give bitwise equal results.  Without it, three
+ *                         kinds of sums follow the timing of the run: the
+ *                         attention backward's two MMA-issuing threads per
+ *                         CTA add into one TMEM accumulator in the order
+ *                         their products reach the tensor core; weight-
+ *                         gradient products split along K add their parts in
+ *                         L2; bias and norm-parameter gradients add per-block
+ *                         partial sums with atomics.  Each such result is
+ *                         then off by at most a rounding step of the
+ *                         summation order (one bf16 unit for dQ/dK/dV).  With
+ *                         the flag: one issuing thread per CTA, no K split,
+ *                         and per-block partial sums written to the workspace
+ *                         and added in block order by a second kernel.  The
+ *                         attention backward runs about a quarter slower.
+ *  BPT_FLAG_DEBUG_CHECKS  before any launch, every device pointer argument
+ *                         must lie, with the bytes the call touches through
+ *                         it, inside one device allocation of the current
+ *                         device (else BPT_EINVAL); after the launches the
+ *                         call synchronises `stream` and returns the device
+ *                         error word's status (BPT_ETIMEOUT) or a failed
+ *                         kernel's (BPT_ECUDA) itself.  The call is then
+ *                         synchronous: not for use under stream capture.  */
+enum {
+  BPT_FLAG_ACCUM_GRADS = 1,
+  BPT_FLAG_ONE_STREAM = 2,
+  BPT_FLAG_DETERMINISTIC = 4,
+  BPT_FLAG_DEBUG_CHECKS = 8
+};
 
 enum { BPT_PASS_FWD = 0, BPT_PASS_BWD = 1, BPT_PASS_HEADCHUNK = 2 };
 
@@ -201,8 +236,10 @@ int bpt_attention_fwd(const bpt_config* cfg, const void* qkv, void* o, void* lse
  *   both as bf16 (hi, lo) pairs for the dK/dV products: 24*b*H*s_pad bytes).
  *   b*H*s_pad above 2^31 - 1 returns BPT_EUNSUPPORTED.
  * Two kernels: dK/dV with the key/value tile outermost and dQ with the query
- * tile outermost, each accumulating in TMEM; no atomics, so the result is
- * deterministic. */
+ * tile outermost, each accumulating in TMEM (no atomics).  Each CTA has two
+ * MMA-issuing threads that add into the same accumulator, so the order of
+ * the fp32 sums, and with it the last bit of a bf16 result, follows the
+ * timing of the run; BPT_FLAG_DETERMINISTIC in cfg->flags fixes it. */
 size_t bpt_attention_bwd_workspace_bytes(const bpt_config* cfg);
 int bpt_attention_bwd(const bpt_config* cfg, const void* qkv, const void* o, const void* lse,
                       const void* dout, void* dqkv, void* ws, size_t ws_bytes, void* stream);
@@ -223,11 +260,14 @@ int bpt_attention_bwd(const bpt_config* cfg, const void* qkv, const void* o, con
  *    more scratch than BPT_NOALLOC_SCRATCH_BYTES (192 MiB: b*H*s_pad up to
  *    8M, e.g. 32 heads at s = 256K; 32 heads at s = 512K is too big).
  *  - The first call on a device looks up the array's device address (once
- *    per device, with that device current); make that first call before
- *    any stream capture.
- *  - Every call shares the one array and clears what must start at zero
- *    itself.  Calls that overlap on the GPU (other streams or host threads
- *    on the same device) race on it: serialise them.
+ *    per device, with that device current) and keeps it for the life of the
+ *    process; make that first call before any stream capture.  A device
+ *    reset (cudaDeviceReset) after it is not supported: the array would be
+ *    reloaded at another address.
+ *  - Every call shares the one array.  Nothing in it has to start at zero:
+ *    each call writes every byte of the array that it reads before reading
+ *    it.  Calls that overlap on the GPU (other streams or host threads on
+ *    the same device) race on it: serialise them.
  *  - It calls no cudaMalloc, cudaFree or other allocating routine. */
 #define BPT_NOALLOC_SCRATCH_BYTES (192u * 1024u * 1024u)
 int bpt_attention_bwd_noalloc(const bpt_config* cfg, const void* qkv, const void* o, const void* lse,
@@ -250,6 +290,16 @@ int bpt_profile_collect(int nkinds, double* ms, double* flops, double* bytes, in
  * (bpt_profile_collect does).  Returns the count, or minus a status code.
  * A diagnostic aid: the layer has no such step in the paper. */
 int bpt_profile_list(int max, int* kind, double* flops, double* bytes, double* ms);
+
+/* BPT_OK if the bytes [ptr, ptr + bytes) lie inside one device allocation
+ * (cudaMalloc, a memory pool's block, managed memory) of the current device,
+ * else BPT_EINVAL: host memory, another device's memory, or a range that runs
+ * past its allocation's end.  The check BPT_FLAG_DEBUG_CHECKS applies to
+ * every pointer argument.  Launches nothing; a diagnostic aid with no
+ * counterpart in the paper.  A caching allocator hands out pieces of larger
+ * allocations, so a range past the end of its piece but inside the
+ * allocation passes. */
+int bpt_check_device_range(const void* ptr, size_t bytes);
 
 /* Text of a status code (static storage). */
 const char* bpt_status_string(int status);

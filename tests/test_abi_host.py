@@ -104,7 +104,7 @@ def _call_fwd(cfg, x=1 << 20, y=1 << 20, ws=1 << 20, wsz=1 << 40):
 
 @pytest.mark.parametrize("bad", [
     dict(s=0), dict(h=100), dict(n_heads=5), dict(head_chunk=3), dict(q_block=64),
-    dict(ffn_block=100), dict(norm=2), dict(act=3), dict(norm_eps=0.0), dict(flags=8),
+    dict(ffn_block=100), dict(norm=2), dict(act=3), dict(norm_eps=0.0), dict(flags=16),
     dict(b=0), dict(causal=2), dict(has_bias=2), dict(n_kv_heads=0),
     dict(rope_base=0.5), dict(rope_base=-10000.0), dict(rope_base=float("nan")), dict(rope_base=float("inf")),
 ])
@@ -114,12 +114,39 @@ def test_invalid_config_rejected_before_launch(built, bad):
 
 
 def test_known_flags_accepted(built):
-    """Both defined flags pass validation and leave the workspace plan alone."""
+    """Every defined flag passes validation.  Accumulation, one stream and the
+    debug checks leave the workspace plan alone; the fixed-order mode adds
+    room for its per-block partial sums to the backward's workspace only."""
     base = bpt.bpt_workspace_bytes(presets.C1, bpt.BPT_PASS_BWD)
-    both = presets.C1.with_(flags=bpt.BPT_FLAG_ACCUM_GRADS | bpt.BPT_FLAG_ONE_STREAM)
+    plain = presets.C1.with_(flags=bpt.BPT_FLAG_ACCUM_GRADS | bpt.BPT_FLAG_ONE_STREAM | bpt.BPT_FLAG_DEBUG_CHECKS)
     assert base > 0
-    assert bpt.bpt_workspace_bytes(both, bpt.BPT_PASS_BWD) == base
-    assert bpt.bpt_workspace_bytes(presets.C1.with_(flags=4), bpt.BPT_PASS_BWD) == 0
+    assert bpt.bpt_workspace_bytes(plain, bpt.BPT_PASS_BWD) == base
+    det = presets.C1.with_(flags=bpt.BPT_FLAG_DETERMINISTIC)
+    for p in (bpt.BPT_PASS_FWD, bpt.BPT_PASS_HEADCHUNK):
+        assert bpt.bpt_workspace_bytes(det, p) == bpt.bpt_workspace_bytes(presets.C1, p)
+    # 256 blocks x (dw, db) x h floats for the norm backward, 64 bands x the
+    # widest column sum (f here) for the bias gradients
+    c = presets.C1
+    extra = 256 * 2 * c.h * 4 + 64 * max(c.h, c.ffn_dim, 3 * c.n_heads * c.head_dim) * 4
+    assert bpt.bpt_workspace_bytes(det, bpt.BPT_PASS_BWD) == base + extra
+    assert bpt.bpt_workspace_bytes(presets.C1.with_(flags=16), bpt.BPT_PASS_BWD) == 0
+
+
+def test_debug_checks_reject_pointers_outside_device_memory(built):
+    """BPT_FLAG_DEBUG_CHECKS refuses, before any launch, pointers that do not
+    lie in device memory of the current device (here: no device at all, or
+    host addresses)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present: the GPU test covers the debug checks")
+    L = bpt.lib()
+    dbg = presets.C1.with_(flags=bpt.BPT_FLAG_DEBUG_CHECKS)
+    assert _call_fwd(dbg) == bpt.BPT_EINVAL
+    c = bpt.make_config(dbg)
+    p = 1 << 20
+    assert L.bpt_attention_fwd(ctypes.byref(c), p, p, None, None) == bpt.BPT_EINVAL
+    assert bpt.bpt_check_device_range(p, 16) == bpt.BPT_EINVAL
+    assert L.bpt_check_device_range(None, 16) == bpt.BPT_EINVAL
 
 
 def test_rope_base_accepted_and_plan_unchanged(built):

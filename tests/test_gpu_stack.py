@@ -1,8 +1,20 @@
-"""The layer stack with a checkpoint every k layers on the GPU: for every k,
-its output equals chaining the layer calls by hand bit for bit, and its
-gradients equal the hand-chained backward up to the summation order of the
-weight-gradient reductions.  (The schedule itself is pinned against the
-oracle's stack on the CPU; each layer call against the oracle elsewhere.)"""
+"""The layer stack with a checkpoint every k layers on the GPU, against
+chaining the layer calls by hand.
+
+With BPT_FLAG_DETERMINISTIC every sum of a layer call is taken in a fixed
+order, and the stack repeats exactly the layer calls of the hand-chained
+backward on exactly the same values (the re-run forward of a segment gives
+its layer inputs bit for bit), so output, input gradient and every weight
+gradient are bitwise equal for every k.
+
+Without the flag the attention backward, the split weight-gradient products
+and the bias and norm gradients add in the order their parts arrive, so two
+calls on the same values may differ in the last bits of an fp32 sum and,
+after rounding, by one bf16 unit in dQ/dK/dV and dx.  That difference is
+bounded here by a tenth of the acceptance bound against the exact gradient
+that every layer call meets on its own (the parity tests), a margin that a
+wrong schedule (a stale or skipped segment) exceeds by orders of magnitude.
+(The schedule itself is pinned against the oracle's stack on the CPU.)"""
 import pytest
 import torch
 
@@ -10,6 +22,7 @@ import blockwise_attention_ffn_gb300 as bpt
 from blockwise_attention_ffn_gb300 import stack
 from blockwise_attention_ffn_gb300.presets import LayerConfig
 from blockwise_attention_ffn_gb300.synth import make_layer_inputs
+from tests.gpu_helpers import ATTN_GRAD_REL_FRO, ATTN_GRADS, REL_FRO
 
 pytestmark = pytest.mark.gpu
 
@@ -24,45 +37,59 @@ def _weights():
             for i in range(L)]
 
 
-def test_checkpointed_stack_equals_chained_layer_calls():
-    Ws = _weights()
-    inp = make_layer_inputs(CFG, seed=40, device="cpu")
-    x, dy = inp["x"].cuda(), inp["dy"].cuda()
-    ws = bpt.alloc_bytes(max(bpt.bpt_workspace_bytes(CFG, bpt.BPT_PASS_FWD),
-                             bpt.bpt_workspace_bytes(CFG, bpt.BPT_PASS_BWD)))
-    # by hand: every layer input kept
+def _hand_chained(cfg, Ws, x, dy, ws):
     xs, saved = [x], []
     for W in Ws:
         y = torch.empty_like(x)
-        sv = bpt.alloc_bytes(bpt.bpt_saved_bytes(CFG))
-        bpt.bpt_layer_fwd(CFG, W, xs[-1], y, sv, ws)
+        sv = bpt.alloc_bytes(bpt.bpt_saved_bytes(cfg))
+        bpt.bpt_layer_fwd(cfg, W, xs[-1], y, sv, ws)
         xs.append(y)
         saved.append(sv)
-    g, grads_ref = dy, [None] * L
+    g, grads = dy, [None] * L
     for i in range(L - 1, -1, -1):
         dx = torch.empty_like(x)
-        grads_ref[i] = bpt.alloc_grads(Ws[i])
-        bpt.bpt_layer_bwd(CFG, Ws[i], xs[i], saved[i], g, dx, grads_ref[i], ws)
+        grads[i] = bpt.alloc_grads(Ws[i])
+        bpt.bpt_layer_bwd(cfg, Ws[i], xs[i], saved[i], g, dx, grads[i], ws)
         g = dx
     torch.cuda.synchronize()
     assert bpt.bpt_last_device_error() == (bpt.BPT_OK, 0)
+    return xs[-1], g, grads
+
+
+@pytest.mark.parametrize("flags", [bpt.BPT_FLAG_DETERMINISTIC, 0], ids=["fixed order", "default"])
+def test_checkpointed_stack_equals_chained_layer_calls(flags):
+    cfg = CFG.with_(flags=flags)
+    Ws = _weights()
+    inp = make_layer_inputs(cfg, seed=40, device="cpu")
+    x, dy = inp["x"].cuda(), inp["dy"].cuda()
+    ws = bpt.alloc_bytes(max(bpt.bpt_workspace_bytes(cfg, bpt.BPT_PASS_FWD),
+                             bpt.bpt_workspace_bytes(cfg, bpt.BPT_PASS_BWD)))
+    y_ref, dx_ref, grads_ref = _hand_chained(cfg, Ws, x, dy, ws)
 
     for k in (1, 2, 3):
-        y, st = stack.stack_fwd(CFG, Ws, x, k, ws=ws)
-        assert torch.equal(y, xs[-1]), k
-        dx, grads = stack.stack_bwd(CFG, Ws, st, dy, ws=ws)
+        y, st = stack.stack_fwd(cfg, Ws, x, k, ws=ws)
+        assert torch.equal(y, y_ref), k
+        dx, grads = stack.stack_bwd(cfg, Ws, st, dy, ws=ws)
         torch.cuda.synchronize()
         assert bpt.bpt_last_device_error() == (bpt.BPT_OK, 0)
         assert st.peak_held == stack.held_inputs(L, k)
-        # dx: at most one bf16 unit apart (it is not reduced across CTAs, so
-        # normally identical)
-        d = (dx.float() - g.float()).abs()
-        assert torch.all(d <= 2.0 ** -7 * g.float().abs().clamp_min(2.0 ** -10)), (k, float(d.max()))
+        if flags & bpt.BPT_FLAG_DETERMINISTIC:
+            assert torch.equal(dx, dx_ref), k
+            for i in range(L):
+                for name, ref_g in grads_ref[i].items():
+                    if ref_g is not None:
+                        assert torch.equal(grads[i][name], ref_g), (k, i, name)
+            continue
+        rel = float((dx.float() - dx_ref.float()).norm() / dx_ref.float().norm())
+        print(f"k={k} dx rel {rel:.2e}")
+        assert rel <= 0.1 * REL_FRO, (k, rel)
         for i in range(L):
             for name, ref_g in grads_ref[i].items():
                 if ref_g is None:
                     continue
                 got = grads[i][name]
-                den = float(ref_g.norm()) or 1.0
-                rel = float((got - ref_g).norm()) / den
-                assert rel <= 1e-5, (k, i, name, rel)
+                den = float(ref_g.norm())
+                rel = float((got - ref_g).norm()) / den if den > 0 else float((got - ref_g).norm())
+                bound = 0.1 * (ATTN_GRAD_REL_FRO if name in ATTN_GRADS else REL_FRO)
+                print(f"k={k} layer {i} d{name} rel {rel:.2e} (bound {bound:.1e})")
+                assert rel <= bound, (k, i, name, rel)

@@ -479,6 +479,173 @@ def run_gpu(args, c):
     return 0
 
 
+def lm_flops(c) -> dict:
+    """Algorithmic FLOPs of the language-model loss step: the logits 2 n h V
+    in the forward; the backward rebuilds them and forms dx = dz W and
+    dW = dz^T x, 2 n h V each."""
+    f = 2.0 * c.n * c.h * c.vocab
+    return {"forward": f, "executed": 4 * f, "model": 3 * f}
+
+
+def describe_lm(c) -> dict:
+    return {"workload": c.name, "n": c.n, "h": c.h, "vocab": c.vocab,
+            "vocab_block": c.vocab_block or min(8192, (c.vocab + 255) // 256 * 256), "pass": "fwd+bwd",
+            "seed": c.seed, "l2": "no flush: x, W and dW alone are 0.9 GB, far larger than the 129 MB L2"}
+
+
+def cpu_baseline_lm(c, rows: int) -> dict:
+    import numpy as np  # noqa: F401
+
+    from blockwise_attention_ffn_gb300.synth import make_lm_inputs
+    from oracle import lm_loss
+    sc = c.with_(n=rows)
+    inp = make_lm_inputs(sc, seed=c.seed)
+    x, w, t = inp["x"].double().numpy(), inp["w"].double().numpy(), inp["targets"].numpy()
+    t0 = time.perf_counter()
+    lm_loss.lm_loss(x, w, t)
+    lm_loss.lm_loss_backward(x, w, t)
+    dt = time.perf_counter() - t0
+    fl = lm_flops(sc)["executed"]
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle", "seconds": dt,
+            "sample": f"fp64 NumPy oracle, loss and gradients of the first {rows} positions (same h and V), "
+                      f"{fl / 1e12:.3f} TFLOP of the same FLOP definition; cores = the BLAS threads"}
+
+
+def run_gpu_lm(args, c):
+    """One step = bpt_lm_loss_fwd + bpt_lm_loss_bwd of the loss workload."""
+    import torch
+    import torch.distributed as tdist
+
+    import blockwise_attention_ffn_gb300 as bpt
+    from blockwise_attention_ffn_gb300.synth import make_lm_inputs
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        init_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    bpt.lib()
+    inp = make_lm_inputs(c, seed=rank_seed(c, rank), device=dev)
+    x, w, t = inp["x"], inp["w"], inp["targets"]
+    loss = torch.empty(1, device=dev)
+    lse = torch.empty(c.n, device=dev)
+    dx = torch.empty_like(x)
+    dw = torch.empty(c.vocab, c.h, device=dev)
+    torch.cuda.synchronize()
+    base_mem = torch.cuda.memory_allocated(dev)
+    ws_bytes = max(bpt.bpt_lm_workspace_bytes(c, bpt.BPT_PASS_FWD), bpt.bpt_lm_workspace_bytes(c, bpt.BPT_PASS_BWD))
+    ws = bpt.alloc_bytes(ws_bytes, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        bpt.bpt_lm_loss_fwd(c, x, w, t, loss, lse, ws, stream)
+        bpt.bpt_lm_loss_bwd(c, x, w, t, lse, 1.0, dx, dw, ws, stream)
+
+    torch.cuda.reset_peak_memory_stats(dev)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if bpt.bpt_last_device_error(stream)[0] != bpt.BPT_OK:
+        raise RuntimeError("device error in the warm-up")
+    peak_mem = torch.cuda.max_memory_allocated(dev)
+    clocks = ClockSampler()
+    if rank == 0:
+        clocks.start()
+    if world > 1:
+        tdist.barrier()
+    torch.cuda.synchronize()
+    e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        tdist.barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    clk = clocks.stop() if rank == 0 else None
+    # the forward alone
+    e0.record(stream)
+    for _ in range(args.steps):
+        bpt.bpt_lm_loss_fwd(c, x, w, t, loss, lse, ws, stream)
+    e2.record(stream)
+    torch.cuda.synchronize()
+    fwd_ms = max_over_ranks(e0.elapsed_time(e2) / args.steps, world, dev)
+    fl = lm_flops(c)
+    value = job_throughput(fl["executed"], world, ms)
+    peaks = load_peaks()
+    bpt.bpt_profile_enable(True)
+    nprof = max(1, min(args.steps, 3))
+    for _ in range(nprof):
+        step()
+    torch.cuda.synchronize()
+    prof = bpt.bpt_profile_collect()
+    bpt.bpt_profile_enable(False)
+    tot_ms = sum(v["ms"] for v in prof.values())
+    kernels = {k: {"launches_per_step": v["launches"] / nprof, "ms_per_step": v["ms"] / nprof,
+                   "share": v["ms"] / tot_ms if tot_ms else None,
+                   "tflops": (v["flops"] / (v["ms"] * 1e-3) / 1e12) if v["flops"] else None,
+                   "gbs": (v["bytes"] / (v["ms"] * 1e-3) / 1e9) if v["bytes"] else None}
+               for k, v in prof.items() if v["launches"]}
+    g = prof["gemm"]
+    ach = g["flops"] / (g["ms"] * 1e-3) / 1e12
+    roof = {"kernel": "gemm", "bound": "tensor", "achieved": ach, "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
+            "frac": ach / peaks["bf16_sustained"], "frac_of_burst_peak": ach / peaks["bf16"],
+            "peak_note": f"{peaks['source']} bf16 sustained (kernel timed inside the long step)",
+            "per_launch_flops": g["flops"] / g["launches"], "avg_launch_ms": g["ms"] / g["launches"],
+            "traffic": load_traffic().get("lm_gemm")}
+    launches = sum(v["launches"] for v in prof.values()) / nprof
+    # end to end: x and the targets in from pinned host memory, dx and the
+    # loss back
+    xh, th = x.cpu().pin_memory(), t.cpu().pin_memory()
+    dxh, lh = torch.empty_like(xh).pin_memory(), torch.empty(1).pin_memory()
+
+    def step_e2e():
+        x.copy_(xh, non_blocking=True)
+        t.copy_(th, non_blocking=True)
+        step()
+        dxh.copy_(dx, non_blocking=True)
+        lh.copy_(loss, non_blocking=True)
+
+    for _ in range(max(1, args.warmup // 2)):
+        step_e2e()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step_e2e()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / args.steps, world, dev)
+    if reports(rank):
+        line = {
+            "metric": "blockwise LM loss (vocabulary projection + cross-entropy) fwd+bwd TFLOP/s and tokens/s",
+            "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) x, N(0,0.02) W, uniform targets)", "config": describe_lm(c),
+            "flops_per_step": fl, "tokens_per_s": c.n * world / (ms * 1e-3),
+            "pct_of_bf16_peak": 100 * value / (peaks["bf16"] * world),
+            "pct_of_bf16_peak_sustained": 100 * value / (peaks["bf16_sustained"] * world),
+            "peak_source": peaks["source"], "clocks": clk,
+            "passes": {"fwd_ms": fwd_ms, "fwd_tflops": job_throughput(fl["forward"], world, fwd_ms)},
+            "e2e": {"value": job_throughput(fl["executed"], world, e2e_ms), "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": xh.numel() * 2 + th.numel() * 4,
+                    "d2h_bytes_per_step": dxh.numel() * 2 + 4,
+                    "what": "pinned host x and targets copied in, loss fwd+bwd through the C ABI, dx and the loss out"},
+            "gpu_launches": int(round(launches * args.steps)), "roofline": roof, "kernels": kernels,
+            "memory": {"peak_device_bytes": peak_mem, "inputs_weights_grads_bytes": base_mem,
+                       "workspace_bytes": ws_bytes, "logits_bytes_bf16_not_held": 2 * c.n * c.vocab},
+        }
+        if not args.no_cpu_baseline and world == 1:
+            try:
+                line["cpu_baseline"] = cpu_baseline_lm(c, min(args.cpu_rows, c.n))
+            except Exception as e:  # noqa: BLE001 - reported in the line
+                line["cpu_baseline"] = {"error": repr(e), "kind": "oracle"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        tdist.barrier()
+        tdist.destroy_process_group()
+    return 0
+
+
 def run_one_kernel(args, c):
     """One launch of one component at the workload's shape with a shorter
     sequence (--seq), for profiler captures of a small case."""
@@ -518,7 +685,8 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="c3", help="c1..c5 (default c3, the s=32K workload)")
+    ap.add_argument("--config", default="c3",
+                    help="c1..c5 (default c3, the s=32K workload); lm3: the language-model loss after it")
     ap.add_argument("--ref-rows", type=int, default=1024,
                     help="positions of the workload the CPU oracle runs per step of --impl reference")
     ap.add_argument("--cpu-rows", type=int, default=4096,
@@ -532,7 +700,19 @@ def main():
     ap.add_argument("--seq", type=int, default=4096, help="sequence length for --profile-kernel")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
-    from blockwise_attention_ffn_gb300.presets import PRESETS
+    from blockwise_attention_ffn_gb300.presets import LM3, PRESETS
+    if args.config == "lm3":
+        if args.impl == "reference":
+            ws, rank, _ = dist_setup()
+            if reports(rank):
+                cb = cpu_baseline_lm(LM3, args.cpu_rows)
+                print(json.dumps({"impl": "reference", "metric": "blockwise LM loss fwd+bwd TFLOP/s",
+                                  "value": cb["value"], "unit": "TFLOP/s", "n_gpus": args.gpus,
+                                  "steps": 1, "warmup": 0, "ms_per_step": cb["seconds"] * 1e3,
+                                  "higher_is_better": True, "dtype": "f64", "config": describe_lm(LM3),
+                                  "cpu_baseline": cb}), flush=True)
+            return 0
+        return run_gpu_lm(args, LM3)
     c = PRESETS[args.config]
     if args.rope_base:
         c = c.with_(rope_base=args.rope_base)

@@ -7,6 +7,7 @@ or fails to load, importing the binding's entry points raises.
 
 Entry points keep the C names: bpt_layer_fwd, bpt_layer_bwd,
 bpt_attn_headchunk, bpt_attention_fwd, bpt_attention_bwd, bpt_attention_bwd_noalloc,
+bpt_lm_loss_fwd, bpt_lm_loss_bwd, bpt_lm_workspace_bytes,
 bpt_workspace_bytes, bpt_saved_bytes, bpt_attention_bwd_workspace_bytes,
 bpt_status_string, bpt_last_device_error, bpt_check_device_range, bpt_watchdog_selftest,
 bpt_profile_enable, bpt_profile_collect, bpt_profile_list.  The layer stack
@@ -47,6 +48,10 @@ class BptWeights(ctypes.Structure):
 
 class BptGrads(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_FIELDS]
+
+
+class BptLmConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("n", "h", "vocab", "vocab_block", "flags")]
 
 
 class BptError(RuntimeError):
@@ -91,6 +96,13 @@ def lib() -> ctypes.CDLL:
         L.bpt_status_string.restype = ctypes.c_char_p
         L.bpt_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
         L.bpt_last_device_error.restype = i32
+        lmp = ctypes.POINTER(BptLmConfig)
+        L.bpt_lm_workspace_bytes.argtypes = [lmp, i32]
+        L.bpt_lm_workspace_bytes.restype = sz
+        L.bpt_lm_loss_fwd.argtypes = [lmp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.bpt_lm_loss_fwd.restype = i32
+        L.bpt_lm_loss_bwd.argtypes = [lmp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, sz, vp]
+        L.bpt_lm_loss_bwd.restype = i32
         L.bpt_check_device_range.argtypes = [vp, sz]
         L.bpt_check_device_range.restype = i32
         L.bpt_watchdog_selftest.argtypes = [vp]
@@ -197,6 +209,34 @@ def bpt_attention_bwd(cfg, qkv, o, lse, dout, dqkv, ws, stream=None) -> None:
     _check(rc, "bpt_attention_bwd")
 
 
+def make_lm_config(c) -> BptLmConfig:
+    """BptLmConfig from an LmConfig (or any object with n, h, vocab,
+    vocab_block and flags)."""
+    return BptLmConfig(c.n, c.h, c.vocab, c.vocab_block, c.flags)
+
+
+def bpt_lm_workspace_bytes(cfg, pass_: int) -> int:
+    return int(lib().bpt_lm_workspace_bytes(ctypes.byref(make_lm_config(cfg)), int(pass_)))
+
+
+def bpt_lm_loss_fwd(cfg, x, w, targets, loss, lse, ws, stream=None) -> None:
+    """Mean token cross-entropy of x [n, h] through w [V, h] against int32
+    targets [n]: writes loss (one fp32 element) and lse [n] (optional)."""
+    c = make_lm_config(cfg)
+    rc = lib().bpt_lm_loss_fwd(ctypes.byref(c), _ptr(x), _ptr(w), _ptr(targets), _ptr(loss), _ptr(lse),
+                               _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    _check(rc, "bpt_lm_loss_fwd")
+
+
+def bpt_lm_loss_bwd(cfg, x, w, targets, lse, dloss, dx, dw, ws, stream=None) -> None:
+    """Gradients of dloss * loss: dx [n, h] bf16 and dw [V, h] fp32."""
+    c = make_lm_config(cfg)
+    rc = lib().bpt_lm_loss_bwd(ctypes.byref(c), _ptr(x), _ptr(w), _ptr(targets), _ptr(lse), float(dloss),
+                               _ptr(dx), _ptr(dw), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    _check(rc, "bpt_lm_loss_bwd")
+
+
+BPT_LM_BAD_TARGET_SITE = 950
 NOALLOC_SCRATCH_BYTES = 192 * 1024 * 1024
 
 

@@ -155,7 +155,8 @@ int check_grads_range(const bpt_config* c, const Dims& D, const bpt_grads* g) {
 int debug_finish(cudaStream_t st) {
   unsigned int e[4] = {0, 0, 0, 0};
   if (read_device_error(st, e)) return BPT_ECUDA;
-  return e[0] ? BPT_ETIMEOUT : BPT_OK;
+  if (!e[0]) return BPT_OK;
+  return e[0] == BPT_EINVAL ? BPT_EINVAL : BPT_ETIMEOUT;
 }
 
 // ---------------------------------------------------------------- workspace
@@ -396,7 +397,7 @@ int bpt_last_device_error(void* stream, int* detail) {
   }
   if (e[0]) {
     if (detail) *detail = (int)e[1];
-    return BPT_ETIMEOUT;
+    return e[0] == BPT_EINVAL ? BPT_EINVAL : BPT_ETIMEOUT;
   }
   if (detail) *detail = 0;
   return BPT_OK;

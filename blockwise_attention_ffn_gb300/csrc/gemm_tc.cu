@@ -17,6 +17,8 @@
 // its share in L2).  The epilogue moves whole 32-byte sectors per thread
 // where every operand allows it.
 #include <math.h>
+
+#include <algorithm>
 #include <string.h>
 
 #include "internal.h"
@@ -57,8 +59,14 @@ struct GemmParams {
   float beta;
   int mt, nt, ntiles;  // tile grid; ntiles counts work units (tiles x ksplit)
   int m_fast;          // walk tiles along M first
+  int group;           // > 0: bands of `group` tile rows (group_m) or tile
+  int group_m;         //      columns, each walked whole before the next
   int ksplit;          // K ranges per tile (> 1: EPI_F32 added atomically)
   int vec32;           // every epilogue operand allows 32-byte accesses
+  const float* rowf;   // loss epilogues: per-row log-sum-exp
+  const int* rowi;     // loss epilogues: per-row target id
+  float scale;
+  long long col0;      // vocabulary id of column 0
   unsigned int* err;
 };
 
@@ -292,6 +300,19 @@ __device__ __forceinline__ void epiw(const GemmParams& p, int m, int n, const fl
       storew_bf16<W>(reinterpret_cast<__nv_bfloat16*>(p.out2) + (long long)m * p.ldo2 + n, w2);
       break;
     }
+    case EPI_CE_GRAD: {
+      // (softmax - onehot) * scale from the logit and the row's log-sum-exp
+      const float l2 = p.rowf[m] * 1.4426950408889634f;
+      const long long t = (long long)p.rowi[m] - p.col0 - n;  // target column within the W
+#pragma unroll
+      for (int j = 0; j < W; ++j) {
+        float e;
+        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(fmaf(a[j], 1.4426950408889634f, -l2)));
+        v[j] = (e - (t == j ? 1.f : 0.f)) * p.scale;
+      }
+      storew_bf16<W>(reinterpret_cast<__nv_bfloat16*>(p.out) + (long long)m * p.ldo + n, v);
+      break;
+    }
     default: {  // EPI_F32
       float* o = reinterpret_cast<float*>(p.out) + (long long)m * p.ldo + n;
       float t[W];
@@ -370,6 +391,13 @@ __device__ __forceinline__ void epi1(const GemmParams& p, int m, int n, float a,
           __float2bfloat16(a * g * sg);
       break;
     }
+    case EPI_CE_GRAD: {
+      float e;
+      asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(fmaf(a, 1.4426950408889634f, -p.rowf[m] * 1.4426950408889634f)));
+      const float v = (e - ((long long)p.rowi[m] == p.col0 + n ? 1.f : 0.f)) * p.scale;
+      reinterpret_cast<__nv_bfloat16*>(p.out)[(long long)m * p.ldo + n] = __float2bfloat16(v);
+      break;
+    }
     default: {
       float* o = reinterpret_cast<float*>(p.out) + (long long)m * p.ldo + n;
       float v = a;
@@ -399,7 +427,20 @@ __device__ __forceinline__ void k_range(const GemmParams& p, int unit, int& kb, 
 __device__ __forceinline__ void tile_origin(const GemmParams& p, int unit, int bn, int& m0, int& n0) {
   const int tile = unit % (p.mt * p.nt);
   int mb, nb;
-  if (p.m_fast) {
+  if (p.group > 0) {
+    // a band of `group` tile rows (or columns) of the operand that would
+    // otherwise be re-read stays in L2 while the band is walked across the
+    // other dimension, its own dimension fastest; the other operand is read
+    // once per band
+    const int nmaj = p.group_m ? p.mt : p.nt;
+    const int nmin = p.group_m ? p.nt : p.mt;
+    const int g = tile / (p.group * nmin);
+    const int r = tile - g * (p.group * nmin);
+    const int gs = min(p.group, nmaj - g * p.group);
+    const int a = g * p.group + r % gs, b = r / gs;
+    mb = p.group_m ? a : b;
+    nb = p.group_m ? b : a;
+  } else if (p.m_fast) {
     mb = tile % p.mt;
     nb = tile / p.mt;
   } else {
@@ -578,6 +619,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       tile_origin(p, tile, BN, m0, n0);
       const int m = m0 + row;
       const uint32_t tbase = tmem + (uint32_t)(acc * ACC_COLS) + ((uint32_t)(q * 32) << 16);
+      if (!DUAL && p.epi == EPI_LSE) {
+        // this thread's row over its half of the tile: online max and sum of
+        // exp over the valid columns, 32 at a time, and the target's logit
+        float mx = -INFINITY, sm = 0.f;
+        const int t = m < p.M ? p.rowi[m] - (int)p.col0 : -1;
+#pragma unroll 1
+        for (int c = 0; c < EPI_COLS / 32; ++c) {
+          const int col = half * EPI_COLS + c * 32;
+          const int nb = n0 + col;
+          uint32_t ra[32];
+          tmem_ld32(tbase + col, ra);
+          float cm = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (nb + j < p.N) cm = fmaxf(cm, __uint_as_float(ra[j]));
+          if (cm > -INFINITY) {
+            const float nm = fmaxf(mx, cm);
+            const float nl2 = nm * 1.4426950408889634f;
+            float e, part = 0.f;
+            asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(fmaf(mx, 1.4426950408889634f, -nl2)));
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              float x;
+              asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(x) : "f"(fmaf(__uint_as_float(ra[j]), 1.4426950408889634f, -nl2)));
+              part += nb + j < p.N ? x : 0.f;
+            }
+            sm = fmaf(sm, e, part);
+            mx = nm;
+          }
+          if (m < p.M && t >= nb && t < nb + 32 && t < p.N) {
+            float z = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (t - nb == j) z = __uint_as_float(ra[j]);
+            reinterpret_cast<float*>(p.out2)[m] = z;
+          }
+        }
+        if (m < p.M) {
+          const long long part_idx = 2 * (long long)(n0 / BN) + half;
+          reinterpret_cast<float2*>(p.out)[part_idx * p.ldo + m] = make_float2(mx, sm);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        continue;
+      }
 #pragma unroll 1
       for (int c = 0; c < EPI_COLS / 32; ++c) {
         const int col = half * EPI_COLS + c * 32;
@@ -644,6 +731,25 @@ int launch(GemmParams& p, cudaStream_t st) {
   p.nt = (p.N + BN - 1) / BN;
   p.ntiles = p.mt * p.nt * p.ksplit;
   p.m_fast = p.M <= p.N;
+  {
+    // Both operands past what L2 keeps while the wave in flight uses them:
+    // walk bands of tiles instead.  Band along M (A's rows): A is read once,
+    // B once per band; along N the other way round.  The band's slice of its
+    // operand is kept to about a quarter of L2, and the side that moves fewer
+    // bytes in total is taken.
+    const double a_bytes = (double)p.M * p.K * 2, b_bytes = (double)p.N * p.K * 2 * (DUAL ? 2 : 1);
+    constexpr double L2_KEEP = 32.0 * 1024 * 1024;
+    p.group = 0;
+    if (a_bytes + b_bytes > 3 * L2_KEEP && p.mt > 1 && p.nt > 1) {
+      const double row_a = (double)BM * p.K * 2, row_b = (double)BN * p.K * 2 * (DUAL ? 2 : 1);
+      const int gm = (int)std::max(1.0, std::min((double)p.mt, L2_KEEP / row_a));
+      const int gn = (int)std::max(1.0, std::min((double)p.nt, L2_KEEP / row_b));
+      const double tm = a_bytes + b_bytes * ((p.mt + gm - 1) / gm);
+      const double tn = b_bytes + a_bytes * ((p.nt + gn - 1) / gn);
+      p.group_m = tm <= tn;
+      p.group = p.group_m ? gm : gn;
+    }
+  }
   const int grid = p.ntiles < nsm ? p.ntiles : nsm;
   kern<<<grid, NUM_THREADS, SMEM, st>>>(p);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
@@ -709,6 +815,10 @@ int gemm(int64_t M, int64_t N, int64_t K, const MatView& A, bool a_mn, const Mat
   p.aux2 = reinterpret_cast<const __nv_bfloat16*>(e.aux2);
   p.ldaux2 = e.ldaux2;
   p.beta = e.beta;
+  p.rowf = e.rowf;
+  p.rowi = e.rowi;
+  p.scale = e.scale;
+  p.col0 = e.col0;
   p.err = device_error_word();
   if (!p.err) return 3;
   {

@@ -75,6 +75,12 @@ enum EpiKind {
   EPI_GELU_BWD = 3,    // out = acc * aux[m, n] (aux = gelu'(z))          -> bf16
   EPI_SWIGLU_BWD = 4,  // acc = dA; g = aux, u = aux2: out = dA*u*silu'(g), out2 = dA*silu(g)
   EPI_F32 = 5,         // out = acc (+ bias) (+ res) + beta * out        -> fp32
+  // language-model loss, logits z = acc of column n (vocabulary id col0 + n):
+  EPI_LSE = 6,         // per row and tile half: (max z, sum exp(z - max)) over
+                       // the valid columns -> float2 out[part * ldo + m],
+                       // part = 2 * tile column + half; z of the row's target
+                       // rowi[m] (if in this tile) -> float out2[m]
+  EPI_CE_GRAD = 7,     // out = (exp(z - rowf[m]) - [col0 + n == rowi[m]]) * scale -> bf16
 };
 
 struct Epilogue {
@@ -98,6 +104,12 @@ struct Epilogue {
   // fixed summation order: no K split (a split adds its K ranges' shares in
   // L2 in whatever order they land)
   int deterministic = 0;
+  // per-row inputs of the loss epilogues: rowf fp32 [M] (log-sum-exp),
+  // rowi int32 [M] (target ids); scale; col0 = vocabulary id of column 0
+  const float* rowf = nullptr;
+  const int* rowi = nullptr;
+  float scale = 1.f;
+  int64_t col0 = 0;
 };
 
 // Returns 0 or a BPT_* status.

@@ -14,8 +14,9 @@ namespace bpt {
 
 // ---------------------------------------------------------------- error word
 // The device error word (4 x u32, one per device, address passed to every
-// kernel): [0] status (0 ok, 4 timeout), [1] wait-site id of the first
-// failure, [2] blockIdx.x of the first failure, [3] failure count.
+// kernel): [0] status of the first failure (0 ok, 4 timeout, 1 invalid data
+// such as a target id outside the vocabulary), [1] its site id, [2] its
+// blockIdx.x, [3] failure count.
 
 #ifndef BPT_WAIT_CYCLES
 #define BPT_WAIT_CYCLES (4000000000LL)  // about 2 s at the GB300 boost clock
@@ -26,6 +27,16 @@ __device__ __forceinline__ void report_timeout(unsigned int* err, int site) {
   printf("bpt: wait site %d timed out in block %d thread %d\n", site, (int)blockIdx.x, (int)threadIdx.x);
 #endif
   if (atomicCAS(&err[0], 0u, 4u) == 0u) {
+    err[1] = (unsigned)site;
+    err[2] = blockIdx.x;
+  }
+  atomicAdd(&err[3], 1u);
+}
+
+// Invalid input data found on the device (status 1, BPT_EINVAL), recorded
+// like a timeout; the kernel carries on with a defined substitute.
+__device__ __forceinline__ void report_bad_data(unsigned int* err, int site) {
+  if (atomicCAS(&err[0], 0u, 1u) == 0u) {
     err[1] = (unsigned)site;
     err[2] = blockIdx.x;
   }

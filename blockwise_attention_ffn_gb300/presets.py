@@ -52,3 +52,25 @@ C5 = LayerConfig(name="llama-8b s=65536 h=4096 32q/8kv x128 U=8", b=1, s=65536, 
                  ffn_block=4096, backward=True, seed=4)
 
 PRESETS = {"c1": C1, "c2": C2, "c3": C3, "c4": C4, "c5": C5}
+
+
+@dataclass(frozen=True)
+class LmConfig:
+    """The language-model loss after the last layer: n positions of width h
+    against a vocabulary of V tokens, the backward in blocks of vocab_block
+    vocabulary columns (0: the library's default)."""
+    n: int
+    h: int
+    vocab: int
+    vocab_block: int = 0
+    flags: int = 0
+    name: str = ""
+    seed: int = 0
+
+    def with_(self, **kw) -> "LmConfig":
+        return replace(self, **kw)
+
+
+# The loss after the GPT-3B-shaped layer at s = 32768, over the GPT-2 BPE
+# vocabulary of the OpenWebText models (50257 tokens).
+LM3 = LmConfig(name="gpt-3b lm head s=32768 h=2560 V=50257", n=32768, h=2560, vocab=50257, seed=5)

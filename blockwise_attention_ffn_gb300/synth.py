@@ -65,3 +65,19 @@ def make_layer_inputs(cfg, seed: int, device="cpu", with_dy=True, dtype=torch.bf
     if with_dy:
         out["dy"] = randn(cfg.b, cfg.s, cfg.h).to(dtype)
     return out
+
+
+def make_lm_inputs(cfg, seed: int, device="cpu", dtype=torch.bfloat16):
+    """Inputs of the language-model loss: dict(x=[n, h], w=[V, h],
+    targets=[n] int32).  x ~ N(0, 1) (the last layer's normalised output),
+    w ~ N(0, 0.02) like every other matrix (logits then have a standard
+    deviation of about 0.02 sqrt(h)), targets uniform over the vocabulary.
+    Drawn in that order from one generator seeded with ``seed``.
+
+    ``cfg`` is any object with fields n, h, vocab."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    x = torch.randn(cfg.n, cfg.h, generator=gen, device=device, dtype=torch.float32).to(dtype)
+    w = (torch.randn(cfg.vocab, cfg.h, generator=gen, device=device, dtype=torch.float32) * 0.02).to(dtype)
+    t = torch.randint(0, cfg.vocab, (cfg.n,), generator=gen, device=device, dtype=torch.int64).to(torch.int32)
+    return {"x": x, "w": w, "targets": t}

@@ -273,6 +273,58 @@ int bpt_attention_bwd(const bpt_config* cfg, const void* qkv, const void* o, con
 int bpt_attention_bwd_noalloc(const bpt_config* cfg, const void* qkv, const void* o, const void* lse,
                               const void* dout, void* dqkv, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Language-model loss after the last layer, blockwise.
+ *
+ * "Blockwise Parallel Transformer for Long Context Large Models", section 3
+ * (the note on the cross-entropy loss before Algorithm 1): the blockwise
+ * schedule covers the final loss as well; "Untied Ulysses ...", the
+ * paragraph on Arctic Long Sequence Training and its Table 1: this loss is
+ * the largest activation term (240 S d_model bytes) and is computed tiled.
+ * The pages do not write the loss out; it is taken as the mean token
+ * cross-entropy (natural log) of the logits z = x W^T through a bias-free
+ * vocabulary projection:
+ *   loss = (1/n) sum_i (logsumexp_v z_iv - z_i,t_i)
+ *   dz   = dloss * (softmax(z) - onehot(t)) / n,  dx = dz W,  dW = dz^T x
+ * The n x V logits never exist: the forward reduces each 256-column tile of
+ * them to per-row partial (max, sum exp) pairs in the GEMM epilogue, the
+ * backward rebuilds them one vocabulary block of c_v columns at a time.
+ *
+ *   n            positions (rows of x; b*s of the layer)
+ *   h            model width, a multiple of 8
+ *   vocab        V >= 1 (any value; the last tile and block are ragged)
+ *   vocab_block  c_v, vocabulary columns per backward block: a multiple of
+ *                256; 0 means min(8192, V rounded up to 256).  The
+ *                backward's workspace holds one n x c_v bf16 block.
+ *   flags        BPT_FLAG_ACCUM_GRADS (dW +=), BPT_FLAG_DETERMINISTIC,
+ *                BPT_FLAG_DEBUG_CHECKS (as for the layer); others rejected. */
+typedef struct {
+  int32_t n, h, vocab, vocab_block, flags;
+} bpt_lm_config;
+
+/* Workspace bytes of bpt_lm_loss_fwd (pass BPT_PASS_FWD: 16 n ceil(V/256)
+ * bytes of partial pairs plus 12 n; 4 n fewer when lse is given) or
+ * bpt_lm_loss_bwd (BPT_PASS_BWD: the n x c_v bf16 block, plus an fp32 n x h
+ * accumulator for dx when V spans more than one block).  0 if invalid. */
+size_t bpt_lm_workspace_bytes(const bpt_lm_config* cfg, int pass);
+
+/* Forward: x [n, h] bf16, w [V, h] bf16 (nn.Linear layout), targets [n]
+ * int32 in [0, V) (device).  Writes loss (one fp32, device) and, if lse is
+ * not NULL, the per-row log-sum-exp [n] fp32 that the backward takes.  A
+ * target outside [0, V) does not stop the call: the row's term is its
+ * log-sum-exp alone, and the device error word records BPT_EINVAL with site
+ * BPT_LM_BAD_TARGET_SITE (read with bpt_last_device_error).  The mean is
+ * summed in a fixed order (the forward is deterministic in every mode). */
+#define BPT_LM_BAD_TARGET_SITE 950
+int bpt_lm_loss_fwd(const bpt_lm_config* cfg, const void* x, const void* w, const int32_t* targets,
+                    float* loss, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward: the gradients of dloss * loss.  lse as the forward wrote it;
+ * dx [n, h] bf16 out; dw [V, h] fp32 out (+= with BPT_FLAG_ACCUM_GRADS). */
+int bpt_lm_loss_bwd(const bpt_lm_config* cfg, const void* x, const void* w, const int32_t* targets,
+                    const float* lse, float dloss, void* dx, float* dw, void* ws, size_t ws_bytes,
+                    void* stream);
+
 /* Opt-in launch profiler.  bpt_profile_enable(1) makes every later launch
  * of this process record a pair of CUDA events on its stream, tagged with
  * the launch's kind and its algorithmic work (FLOPs for tensor-core kernels,
@@ -306,8 +358,10 @@ const char* bpt_status_string(int status);
 
 /* Synchronises `stream`, then reads and clears the device error word.
  * Returns BPT_OK, BPT_ETIMEOUT (a bounded wait ran out; *detail = the wait
- * site id) or BPT_ECUDA (the synchronisation itself failed; *detail = the
- * cudaError_t).  detail may be NULL. */
+ * site id), BPT_EINVAL (a kernel met invalid input data; *detail = its site,
+ * e.g. BPT_LM_BAD_TARGET_SITE) or BPT_ECUDA (the synchronisation itself
+ * failed; *detail = the cudaError_t).  The first failure of either kind is
+ * kept until read.  detail may be NULL. */
 int bpt_last_device_error(void* stream, int* detail);
 
 /* Watchdog self-test: exercises the device-side wait limit without faulting

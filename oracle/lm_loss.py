@@ -59,6 +59,48 @@ def lm_loss_backward(x, W, targets):
     return dz @ W, dz.T @ x
 
 
+def row_logsumexp(x, W, rows=None, c=1024):
+    """log sum_v exp(z_iv) of the logits z = x W^T for the positions in
+    ``rows`` (all by default), formed c positions at a time so that a long
+    sequence never holds its whole logit matrix: the per-position quantity
+    the loss subtracts the target's logit from."""
+    x = np.asarray(x, F64)
+    W = np.asarray(W, F64)
+    idx = np.arange(x.shape[0]) if rows is None else np.asarray(rows)
+    out = np.empty(len(idx))
+    for r0 in range(0, len(idx), c):
+        out[r0:r0 + c] = _lse_rows(x[idx[r0:r0 + c]] @ W.T)
+    return out
+
+
+def lm_loss_and_lse(x, W, targets, c=1024):
+    """(loss, per-position log-sum-exp) in one pass over blocks of c
+    positions: the loss is the mean of lse_i - z_i,t_i."""
+    x = np.asarray(x, F64)
+    W = np.asarray(W, F64)
+    t = np.asarray(targets)
+    lse = np.empty(x.shape[0])
+    zt = np.empty(x.shape[0])
+    for r0 in range(0, x.shape[0], c):
+        z = x[r0:r0 + c] @ W.T
+        lse[r0:r0 + c] = _lse_rows(z)
+        zt[r0:r0 + c] = z[np.arange(z.shape[0]), t[r0:r0 + c]]
+    return float(np.mean(lse - zt)), lse
+
+
+def lm_dw_rows(x, W, targets, lse, vrows):
+    """Rows ``vrows`` of dW = dz^T x, with dz_iv = (exp(z_iv - lse_i) -
+    [t_i = v]) / s: only the logits of those vocabulary entries are formed,
+    given every position's log-sum-exp (from :func:`lm_loss_and_lse`)."""
+    x = np.asarray(x, F64)
+    W = np.asarray(W, F64)
+    t = np.asarray(targets)
+    v = np.asarray(vrows)
+    z = x @ W[v].T                                    # [s, len(v)]
+    dz = np.exp(z - np.asarray(lse, F64)[:, None]) - (t[:, None] == v[None, :])
+    return dz.T @ x / x.shape[0]
+
+
 def lm_loss_row_blocks(x, W, targets, c):
     """The page's form: positions in blocks of c, each block's logits formed,
     reduced to its loss terms and dropped before the next block."""

@@ -74,3 +74,33 @@ def test_position_blocks_equal_vanilla(c):
 def test_vocabulary_blocks_with_online_lse_equal_vanilla(c_v):
     x, W, t = _case(35, scale=4.0)   # large logits: the running max must do its job
     assert abs(L.lm_loss_vocab_blocks(x, W, t, c_v) - L.lm_loss(x, W, t)) < 1e-12
+
+
+def test_row_logsumexp_matches_scipy_and_the_loss():
+    """The per-position log-sum-exp equals SciPy's logsumexp of the logits
+    (a library routine), for all rows and for a sample in any order, and the
+    loss is the mean of it minus the target logits."""
+    from scipy.special import logsumexp
+    x, W, t = _case(36, scale=3.0)
+    z = x @ W.T
+    want = logsumexp(z, axis=1)
+    for c in (1, 4, 1024):
+        assert np.max(np.abs(L.row_logsumexp(x, W, c=c) - want)) < 1e-12
+    rows = np.array([5, 0, 22, 7])
+    assert np.max(np.abs(L.row_logsumexp(x, W, rows=rows) - want[rows])) < 1e-12
+    assert abs(np.mean(want - z[np.arange(len(t)), t]) - L.lm_loss(x, W, t)) < 1e-13
+
+
+@pytest.mark.parametrize("c", [1, 6, 1024])
+def test_one_pass_loss_and_lse_and_sampled_dw_rows(c):
+    """The one-pass (loss, lse) equals the vanilla loss and SciPy's
+    logsumexp; dW at chosen vocabulary rows, given that lse, equals those rows
+    of the full gradient (target rows and others, repeated and unordered)."""
+    from scipy.special import logsumexp
+    x, W, t = _case(37, scale=2.0)
+    loss, lse = L.lm_loss_and_lse(x, W, t, c=c)
+    assert abs(loss - L.lm_loss(x, W, t)) < 1e-13
+    assert np.max(np.abs(lse - logsumexp(x @ W.T, axis=1))) < 1e-12
+    _, dW = L.lm_loss_backward(x, W, t)
+    vrows = np.array([t[0], 0, 36, t[3], 5, t[0]])
+    assert np.max(np.abs(L.lm_dw_rows(x, W, t, lse, vrows) - dW[vrows])) < 1e-13

@@ -36,7 +36,9 @@ def flop_counts(c) -> dict:
     F_linear = 2 s h (H + 2 H_kv) d + 2 s H d h + 2 s h f n_mat
     F_attn   = 4 d H * (number of unmasked query/key pairs)   (~ 2 s^2 H d)
     forward  = F_linear + F_attn
-    executed (fwd + recompute bwd) = forward + (forward - fc2) + 2 F_linear + 2.5 F_attn
+    executed (fwd + recompute bwd) = forward + (forward - fc2) + 2 F_linear + 2.5 F_attn,
+               less the Q/K/V projection (save policy 1) and also the attention
+               forward (policy 2) that the backward then does not rebuild
     model    = 3 * forward"""
     s, h, H, Hk, d, f, b = c.s, c.h, c.n_heads, c.n_kv_heads, c.head_dim, c.ffn_dim, c.b
     n_mat = 3 if c.act == 2 else 2
@@ -48,9 +50,15 @@ def flop_counts(c) -> dict:
     if not c.backward:
         return {"forward": fwd, "executed": fwd, "model": fwd, "linear": lin, "attn": attn}
     executed = fwd + (fwd - fc2) + 2 * lin + 2.5 * attn
-    if c.head_chunk and c.head_chunk < H:
+    qkv = b * 2 * s * h * (H + 2 * Hk) * d
+    save = getattr(c, "save_policy", 0)
+    if c.head_chunk and c.head_chunk < H and save == 0:
         # Q/K/V of every stage is projected once more for the attention backward
-        executed += b * 2 * s * h * (H + 2 * Hk) * d
+        executed += qkv
+    if save >= 1:
+        executed -= qkv   # the backward takes the projections the forward kept
+    if save >= 2:
+        executed -= attn  # and the attention output
     return {"forward": fwd, "executed": executed, "model": 3 * fwd, "linear": lin, "attn": attn}
 
 
@@ -204,7 +212,9 @@ def describe(c) -> dict:
             "ffn_block": c.ffn_block, "head_chunk": c.head_chunk or c.n_heads,
             "pass": "fwd+bwd" if c.backward else "fwd", "seed": c.seed,
             "l2": "no flush: every step streams inputs and buffers far larger than the 129 MB L2",
-            **({"rope_base": c.rope_base} if c.rope_base else {})}
+            **({"rope_base": c.rope_base} if c.rope_base else {}),
+            **({"stage_order": ["contiguous", "interleaved"][c.stage_order]} if c.stage_order else {}),
+            **({"save_policy": ["log-sum-exp", "+ Q/K/V", "+ Q/K/V and O"][c.save_policy]} if c.save_policy else {})}
 
 
 # ----------------------------------------------------------------- CPU oracle leg
@@ -695,6 +705,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rope-base", type=float, default=0.0,
                     help="rotary position embedding base for the layer (0: none, the workloads' setting)")
+    ap.add_argument("--head-chunk", type=int, default=None,
+                    help="query heads per stage U (the workload's own by default)")
+    ap.add_argument("--stage-order", type=int, default=0, choices=[0, 1],
+                    help="head-chunk stage order: 0 contiguous, 1 interleaved over the key/value groups")
+    ap.add_argument("--save-policy", type=int, default=0, choices=[0, 1, 2],
+                    help="kept for the backward: 0 the log-sum-exp, 1 + Q/K/V, 2 + the attention output")
     ap.add_argument("--profile-kernel", choices=["attn_fwd", "attn_bwd", "layer"], default=None,
                     help="run one launch of this component (small case for profiler captures)")
     ap.add_argument("--seq", type=int, default=4096, help="sequence length for --profile-kernel")
@@ -716,6 +732,10 @@ def main():
     c = PRESETS[args.config]
     if args.rope_base:
         c = c.with_(rope_base=args.rope_base)
+    if args.head_chunk is not None:
+        c = c.with_(head_chunk=args.head_chunk)
+    if args.stage_order or args.save_policy:
+        c = c.with_(stage_order=args.stage_order, save_policy=args.save_policy)
     if args.profile_kernel:
         return run_one_kernel(args, c)
     if args.impl == "reference":

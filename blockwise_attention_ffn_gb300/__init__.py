@@ -26,6 +26,8 @@ LIB_PATH = os.path.join(_HERE, "libbpt.so")
 
 BPT_OK, BPT_EINVAL, BPT_ENOSPC, BPT_ECUDA, BPT_ETIMEOUT, BPT_EUNSUPPORTED = range(6)
 BPT_PASS_FWD, BPT_PASS_BWD, BPT_PASS_HEADCHUNK = 0, 1, 2
+BPT_STAGE_CONTIGUOUS, BPT_STAGE_INTERLEAVED = 0, 1
+BPT_SAVE_NOTHING, BPT_SAVE_PROJECTIONS, BPT_SAVE_ATTN_OUT = 0, 1, 2
 BPT_FLAG_ACCUM_GRADS = 1
 BPT_FLAG_ONE_STREAM = 2
 BPT_FLAG_DETERMINISTIC = 4
@@ -39,7 +41,8 @@ class BptConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "b", "s", "h", "n_heads", "n_kv_heads", "head_dim", "ffn_dim",
         "q_block", "kv_block", "ffn_block", "head_chunk", "causal", "norm", "act", "has_bias")] + \
-        [("norm_eps", ctypes.c_float), ("flags", ctypes.c_int32), ("rope_base", ctypes.c_float)]
+        [("norm_eps", ctypes.c_float), ("flags", ctypes.c_int32), ("rope_base", ctypes.c_float),
+         ("stage_order", ctypes.c_int32), ("save_policy", ctypes.c_int32)]
 
 
 class BptWeights(ctypes.Structure):
@@ -124,7 +127,8 @@ def make_config(c) -> BptConfig:
     """BptConfig from a LayerConfig (or any object with the same fields)."""
     return BptConfig(c.b, c.s, c.h, c.n_heads, c.n_kv_heads, c.head_dim, c.ffn_dim, c.q_block,
                      c.kv_block, c.ffn_block, c.head_chunk, c.causal, c.norm, c.act, c.has_bias,
-                     c.norm_eps, c.flags, float(getattr(c, "rope_base", 0.0)))
+                     c.norm_eps, c.flags, float(getattr(c, "rope_base", 0.0)),
+                     int(getattr(c, "stage_order", 0)), int(getattr(c, "save_policy", 0)))
 
 
 def _ptr(t):

@@ -47,6 +47,10 @@ struct AttnFwdParams {
   int o_col;
   float* lse;
   int H_total, lse_head0;
+  // output head of local head n (O column block and LSE row):
+  // (n / o_seg) * o_seg_stride + n % o_seg -- n itself unless the call's
+  // heads are spread over the output in segments (interleaved stages)
+  int o_seg, o_seg_stride;
   int qt_begin, n_qt, b;
   float scale_log2;  // log2(e) / sqrt(d)
   float scale;       // 1 / sqrt(d)
@@ -54,6 +58,10 @@ struct AttnFwdParams {
   long long ld_qkv;
   unsigned int* err;
 };
+
+__device__ __forceinline__ int out_head(const AttnFwdParams& p, int n) {
+  return (n / p.o_seg) * p.o_seg_stride + n % p.o_seg;
+}
 
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x,
                                             int y, int z) {
@@ -349,7 +357,7 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
     if (ok) {
       tc_fence_after();
       const bool valid = qpos < p.s;
-      __nv_bfloat16* orow = p.o + ((long long)bi * p.s + qpos - p.o_row0) * p.ld_o + p.o_col + (long long)n * D;
+      __nv_bfloat16* orow = p.o + ((long long)bi * p.s + qpos - p.o_row0) * p.ld_o + p.o_col + (long long)out_head(p, n) * D;
       uint32_t oall[D + EXT];
 #pragma unroll
       for (int cc = 0; cc < (D + EXT) / 16; ++cc) tmem_ld16_nw(tO + lane_off + cc * 16, oall + cc * 16);
@@ -363,7 +371,7 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
       // every row of the padded tile gets a finite value (rows past s see the
       // zero-filled query), so the backward pass never reads garbage
       if (p.lse)
-        p.lse[((long long)bi * p.H_total + p.lse_head0 + n) * p.s_pad + qpos] = m_run * p.scale + logf(l_run);
+        p.lse[((long long)bi * p.H_total + p.lse_head0 + out_head(p, n)) * p.s_pad + qpos] = m_run * p.scale + logf(l_run);
     }
   }
 
@@ -677,7 +685,7 @@ __global__ void __launch_bounds__(352, 1) attn_fwd_sk_kernel(const __grid_consta
       constexpr int NC0 = (NC + 1) / 2;
       const int cbeg = b == 0 ? 0 : NC0, cend = b == 0 ? NC0 : NC;
       const bool valid = qpos < p.s;
-      __nv_bfloat16* orow = p.o + ((long long)bi * p.s + qpos - p.o_row0) * p.ld_o + p.o_col + (long long)n * D;
+      __nv_bfloat16* orow = p.o + ((long long)bi * p.s + qpos - p.o_row0) * p.ld_o + p.o_col + (long long)out_head(p, n) * D;
       for (int cc = cbeg; cc < cend; ++cc) {
         uint32_t vs[16], vo[16];
         tmem_ld16_nw(tOb + lane_off + cc * 16, vs);
@@ -693,7 +701,7 @@ __global__ void __launch_bounds__(352, 1) attn_fwd_sk_kernel(const __grid_consta
       // every row of the padded tile gets a finite value (rows past s see the
       // zero-filled query), so the backward pass never reads garbage
       if (b == 0 && p.lse)
-        p.lse[((long long)bi * p.H_total + p.lse_head0 + n) * p.s_pad + qpos] = m * p.scale + logf(l);
+        p.lse[((long long)bi * p.H_total + p.lse_head0 + out_head(p, n)) * p.s_pad + qpos] = m * p.scale + logf(l);
     }
   }
 
@@ -750,6 +758,8 @@ int attention_fwd(const AttnShape& sh, const void* qkv, void* o, float* lse, cud
   prm.lse = lse;
   prm.H_total = sh.H_total;
   prm.lse_head0 = sh.lse_head0;
+  prm.o_seg = sh.o_seg > 0 ? sh.o_seg : sh.H;
+  prm.o_seg_stride = sh.o_seg > 0 ? sh.o_seg_stride : sh.H;
   prm.qt_begin = sh.q_begin / 128;
   prm.n_qt = (sh.q_end + 127) / 128 - prm.qt_begin;
   prm.b = sh.b;

@@ -41,6 +41,11 @@ struct Dims {
   float rope;      // rotary embedding base (0: none)
   bool det;        // BPT_FLAG_DETERMINISTIC
   bool debug;      // BPT_FLAG_DEBUG_CHECKS
+  bool interleave; // interleaved stages (chunked, BPT_STAGE_INTERLEAVED)
+  int64_t m;       // interleaved: query heads of each group per stage (U / H_kv)
+  int64_t iw;      // interleaved: columns of the stage buffer, U d + 2 H_kv d
+  int save;        // BPT_SAVE_*
+  int64_t full_w;  // columns of Q/K/V of every head, (H + 2 H_kv) d
 };
 
 int validate(const bpt_config* c, Dims* D) {
@@ -65,6 +70,9 @@ int validate(const bpt_config* c, Dims* D) {
   int U = c->head_chunk;
   if (U == 0) U = c->n_heads;
   if (U < 1 || (c->n_heads % U) || (U % G)) return BPT_EINVAL;
+  if (c->stage_order != BPT_STAGE_CONTIGUOUS && c->stage_order != BPT_STAGE_INTERLEAVED) return BPT_EINVAL;
+  if (c->stage_order == BPT_STAGE_INTERLEAVED && (U % c->n_kv_heads)) return BPT_EINVAL;
+  if (c->save_policy < BPT_SAVE_NOTHING || c->save_policy > BPT_SAVE_ATTN_OUT) return BPT_EINVAL;
   if ((int64_t)c->s * c->b >= (int64_t(1) << 31)) return BPT_EINVAL;
   D->b = c->b;
   D->s = c->s;
@@ -86,6 +94,11 @@ int validate(const bpt_config* c, Dims* D) {
   D->rope = c->rope_base;
   D->det = (c->flags & BPT_FLAG_DETERMINISTIC) != 0;
   D->debug = (c->flags & BPT_FLAG_DEBUG_CHECKS) != 0;
+  D->interleave = D->chunked && c->stage_order == BPT_STAGE_INTERLEAVED;
+  D->m = U / c->n_kv_heads;
+  D->iw = (U + 2 * (int64_t)c->n_kv_heads) * d;
+  D->save = c->save_policy;
+  D->full_w = (D->H + 2 * D->Hkv) * d;
   return BPT_OK;
 }
 
@@ -171,19 +184,42 @@ struct Carve {
   }
 };
 
+// What the forward keeps for the backward (the caller's `saved` buffer):
+// the log-sum-exp [b, H, s_pad] fp32, then with BPT_SAVE_PROJECTIONS Q, K, V
+// of every head [rows, (H + 2 H_kv) d] (the unchunked packed layout), then
+// with BPT_SAVE_ATTN_OUT the attention output O [rows, H d].
+struct Saved {
+  float* lse;
+  void *qkv, *o;
+};
+size_t plan_saved(const Dims& D, const void* base, Saved* sv) {
+  Carve c(const_cast<void*>(base));
+  sv->lse = reinterpret_cast<float*>(c.take(D.b * D.H * D.s_pad * 4));
+  sv->qkv = D.save >= BPT_SAVE_PROJECTIONS ? c.take(D.rows * D.full_w * 2) : nullptr;
+  sv->o = D.save >= BPT_SAVE_ATTN_OUT ? c.take(D.rows * D.H * D.d * 2) : nullptr;
+  return c.off;
+}
+
 struct FwdWs {
   void *xn, *qkv, *o, *x1, *x1n, *a;
   float* lse;
+  void *wq_perm, *bq_perm;  // interleaved stages: Wq (and bq) rows in stage order
 };
-size_t plan_fwd(const Dims& D, void* base, FwdWs* w, bool need_lse) {
+// saving: whether the call keeps the backward's activations (a `saved`
+// buffer is given); the projections and O then live there, not here
+size_t plan_fwd(const Dims& D, void* base, FwdWs* w, bool need_lse, bool saving) {
   Carve c(base);
+  const bool keep_qkv = saving && D.save >= BPT_SAVE_PROJECTIONS;
+  const bool keep_o = saving && D.save >= BPT_SAVE_ATTN_OUT;
   w->xn = c.take(D.rows * D.h * 2);
-  w->qkv = c.take(D.rows * D.qkv_w * 2);
-  w->o = c.take((D.chunked ? D.rows : D.cf) * D.H * D.d * 2);
+  w->qkv = D.interleave ? c.take(D.rows * D.iw * 2) : keep_qkv ? nullptr : c.take(D.rows * D.qkv_w * 2);
+  w->o = keep_o ? nullptr : c.take((D.chunked ? D.rows : D.cf) * D.H * D.d * 2);
   w->x1 = c.take(D.cf * D.h * 4);  // fp32 residual stream
   w->x1n = c.take(D.cf * D.h * 2);
   w->a = c.take(D.cf * D.f * 2);
   w->lse = reinterpret_cast<float*>(need_lse ? c.take(D.b * D.H * D.s_pad * 4) : nullptr);
+  w->wq_perm = D.interleave ? c.take(D.H * D.d * D.h * 2) : nullptr;
+  w->bq_perm = D.interleave ? c.take(D.H * D.d * 2) : nullptr;
   return c.off;
 }
 
@@ -197,10 +233,11 @@ struct BwdWs {
 AttnBwdShape stage_bwd_shape(const Dims& D, int64_t k);
 size_t plan_bwd(const Dims& D, void* base, BwdWs* w) {
   Carve c(base);
-  // the FFN block buffers are sized for the larger (SwiGLU) case
+  // the FFN block buffers are sized for the larger (SwiGLU) case; the
+  // projections and O come from the saved buffer when the forward kept them
   w->xn = c.take(D.rows * D.h * 2);
-  w->qkv = c.take(D.rows * D.qkv_w * 2);
-  w->o = c.take(D.rows * D.H * D.d * 2);
+  w->qkv = D.save >= BPT_SAVE_PROJECTIONS ? nullptr : c.take(D.rows * D.qkv_w * 2);
+  w->o = D.save >= BPT_SAVE_ATTN_OUT ? nullptr : c.take(D.rows * D.H * D.d * 2);
   w->x1 = c.take(D.cf * D.h * 4);  // fp32 residual stream
   w->x1n = c.take(D.cf * D.h * 2);
   w->gd = c.take(D.cf * D.f * 2);  // GeLU: gelu'(z) of the recompute; SwiGLU: gate g
@@ -224,9 +261,14 @@ size_t plan_bwd(const Dims& D, void* base, BwdWs* w) {
   return c.off;
 }
 
-size_t plan_headchunk(const Dims& D, void* base, void** qkv) {
+struct HcWs {
+  void *qkv, *wq_perm, *bq_perm;
+};
+size_t plan_headchunk(const Dims& D, void* base, HcWs* w) {
   Carve c(base);
-  *qkv = c.take(D.rows * D.qkv_w * 2);
+  w->qkv = c.take(D.rows * (D.interleave ? D.iw : D.qkv_w) * 2);
+  w->wq_perm = D.interleave ? c.take(D.H * D.d * D.h * 2) : nullptr;
+  w->bq_perm = D.interleave ? c.take(D.H * D.d * 2) : nullptr;
   return c.off;
 }
 
@@ -235,11 +277,40 @@ const uint8_t* bf(const void* p, int64_t elems) { return reinterpret_cast<const 
 uint8_t* bfm(void* p, int64_t elems) { return reinterpret_cast<uint8_t*>(p) + elems * 2; }
 float* f32(void* p, int64_t elems) { return reinterpret_cast<float*>(p) + elems; }
 
+// rows of xn projected through n_out rows of a weight matrix (+ bias):
+// out[:, 0:n_out] = xn W^T (+ bias), bf16 with row length ldo
+int project(const Dims& D, const void* xn, const void* W, const void* bias, int64_t n_out, void* out, int64_t ldo,
+            cudaStream_t st) {
+  MatView A{xn, D.rows, D.h, D.h};
+  MatView B{W, n_out, D.h, D.h};
+  Epilogue e;
+  e.kind = EPI_BF16;
+  e.out = out;
+  e.ldo = ldo;
+  e.bias = bias;
+  int64_t kseg = D.h;
+  return gemm(D.rows, n_out, D.h, A, false, &B, &kseg, 1, false, nullptr, e, st);
+}
+
+// Where a stage's projections live: a buffer, its row length, and the
+// columns of the stage's first query, key and value head.
+struct QkvBuf {
+  void* p;
+  int64_t ld, q_col, k_col, v_col;
+};
+// the per-stage buffer: Q of the U heads, then K and V of their U/G heads
+QkvBuf stage_buf(const Dims& D, void* p) { return QkvBuf{p, D.qkv_w, 0, D.U * D.d, (D.U + D.Uk) * D.d}; }
+// stage k's heads inside the buffer of every head's projections that the
+// forward keeps for the backward (BPT_SAVE_PROJECTIONS): [Q all | K all | V all]
+QkvBuf kept_buf(const Dims& D, void* p, int64_t k) {
+  return QkvBuf{p, D.full_w, k * D.U * D.d, D.H * D.d + k * D.Uk * D.d, (D.H + D.Hkv) * D.d + k * D.Uk * D.d};
+}
+
 // Q/K/V of stage k (all stages = one stage when not chunked) for all rows:
-// qkv[:, 0:U d] = xn Wq[kU d : (k+1)U d]^T (+ bq), then K, V of the stage's
-// U/G key/value heads.  With rotary embedding, the stage's query and key
-// heads (adjacent columns) are then rotated at their rows' positions.
-int stage_qkv(const Dims& D, const bpt_weights* w, bool has_bias, const void* xn, void* qkv, int64_t k,
+// Q = xn Wq[kU d : (k+1)U d]^T (+ bq), then K, V of the stage's U/G
+// key/value heads, into the columns `b` names.  With rotary embedding, the
+// stage's query and key heads are then rotated at their rows' positions.
+int stage_qkv(const Dims& D, const bpt_weights* w, bool has_bias, const void* xn, const QkvBuf& b, int64_t k,
               cudaStream_t st) {
   const int64_t d = D.d, h = D.h;
   const int64_t q0 = k * D.U * d, kv0 = k * D.Uk * d;
@@ -247,26 +318,22 @@ int stage_qkv(const Dims& D, const bpt_weights* w, bool has_bias, const void* xn
     const void* W;
     const void* bias;
     int64_t row0, n, col;
-  } pieces[3] = {{w->wq, w->bq, q0, D.U * d, 0},
-                 {w->wk, w->bk, kv0, D.Uk * d, D.U * d},
-                 {w->wv, w->bv, kv0, D.Uk * d, (D.U + D.Uk) * d}};
-  MatView A{xn, D.rows, h, h};
+  } pieces[3] = {{w->wq, w->bq, q0, D.U * d, b.q_col},
+                 {w->wk, w->bk, kv0, D.Uk * d, b.k_col},
+                 {w->wv, w->bv, kv0, D.Uk * d, b.v_col}};
   for (auto& pc : pieces) {
-    MatView B{bf(pc.W, pc.row0 * h), pc.n, h, h};
-    Epilogue e;
-    e.kind = EPI_BF16;
-    e.out = bfm(qkv, pc.col);
-    e.ldo = D.qkv_w;
-    e.bias = has_bias ? bf(pc.bias, pc.row0) : nullptr;
-    int64_t kseg = h;
-    int rc = gemm(D.rows, pc.n, h, A, false, &B, &kseg, 1, false, nullptr, e, st);
+    int rc = project(D, xn, bf(pc.W, pc.row0 * h), has_bias ? bf(pc.bias, pc.row0) : nullptr, pc.n,
+                     bfm(b.p, pc.col), b.ld, st);
     if (rc) return rc;
   }
-  if (D.rope != 0.f) return rope_apply(D.rows, (int)D.s, qkv, D.qkv_w, 0, (int)(D.U + D.Uk), (int)d, D.rope, 0, st);
-  return 0;
+  if (D.rope == 0.f) return 0;
+  if (b.k_col == b.q_col + D.U * d)  // query and key heads adjacent: one pass
+    return rope_apply(D.rows, (int)D.s, b.p, b.ld, (int)b.q_col, (int)(D.U + D.Uk), (int)d, D.rope, 0, st);
+  int rc = rope_apply(D.rows, (int)D.s, b.p, b.ld, (int)b.q_col, (int)D.U, (int)d, D.rope, 0, st);
+  return rc ? rc : rope_apply(D.rows, (int)D.s, b.p, b.ld, (int)b.k_col, (int)D.Uk, (int)d, D.rope, 0, st);
 }
 
-AttnShape stage_attn_shape(const Dims& D, int64_t k, int causal) {
+AttnShape stage_attn_shape(const Dims& D, int64_t k, int causal, const QkvBuf& b) {
   AttnShape a;
   a.b = (int)D.b;
   a.s = (int)D.s;
@@ -274,10 +341,10 @@ AttnShape stage_attn_shape(const Dims& D, int64_t k, int causal) {
   a.Hkv = (int)D.Uk;
   a.d = (int)D.d;
   a.causal = causal;
-  a.ld_qkv = D.qkv_w;
-  a.q_col = 0;
-  a.k_col = D.U * D.d;
-  a.v_col = (D.U + D.Uk) * D.d;
+  a.ld_qkv = b.ld;
+  a.q_col = b.q_col;
+  a.k_col = b.k_col;
+  a.v_col = b.v_col;
   a.ld_o = D.H * D.d;
   a.o_col = k * D.U * D.d;
   a.H_total = (int)D.H;
@@ -288,9 +355,9 @@ AttnShape stage_attn_shape(const Dims& D, int64_t k, int causal) {
   return a;
 }
 
-AttnBwdShape stage_bwd_shape(const Dims& D, int64_t k) {
+AttnBwdShape stage_bwd_shape(const Dims& D, int64_t k, const QkvBuf& b) {
   AttnBwdShape s;
-  s.f = stage_attn_shape(D, k, 1);
+  s.f = stage_attn_shape(D, k, 1, b);
   s.ld_do = D.H * D.d;
   s.do_col = k * D.U * D.d;
   s.ld_dqkv = D.qkv_w;
@@ -298,6 +365,76 @@ AttnBwdShape stage_bwd_shape(const Dims& D, int64_t k) {
   s.dk_col = D.U * D.d;
   s.dv_col = (D.U + D.Uk) * D.d;
   return s;
+}
+AttnBwdShape stage_bwd_shape(const Dims& D, int64_t k) { return stage_bwd_shape(D, k, stage_buf(D, nullptr)); }
+
+// Interleaved stages ("Untied Ulysses ...", section 4.1 "The GQA Scheduling
+// Algorithm"): stage k takes the m = U / H_kv query heads gG + km .. gG + km
+// + m - 1 of every group g.  Every stage needs every key/value head, so
+// those are projected once, before the stages, into columns U d .. of the
+// stage buffer and stay there; each stage projects only its query heads
+// (from a copy of Wq whose rows are in stage order, so one product covers
+// the stage) into columns 0 .. U d, and its attention writes O and the
+// log-sum-exp at the heads' own places (output head of local head g m + r:
+// g G + k m + r).  keep_qkv: every head's Q, K and V are also copied into the
+// kept buffer's layout for the backward.
+int interleaved_attention(const Dims& D, const bpt_weights* w, bool hb, const void* xn, void* buf, void* wq_perm,
+                          void* bq_perm, void* o, float* lse, int causal, void* keep_qkv, cudaStream_t st) {
+  const int64_t d = D.d, h = D.h, blk = D.m * d;
+  for (int64_t k = 0; k < D.n_stages; ++k)
+    for (int64_t g = 0; g < D.Hkv; ++g) {
+      const int64_t dst = (k * D.U + g * D.m) * d, src = (g * D.G + k * D.m) * d;  // rows of Wq
+      if (cudaMemcpyAsync(bfm(wq_perm, dst * h), bf(w->wq, src * h), (size_t)(blk * h * 2), cudaMemcpyDeviceToDevice,
+                          st) != cudaSuccess)
+        return BPT_ECUDA;
+      if (hb && cudaMemcpyAsync(bfm(bq_perm, dst), bf(w->bq, src), (size_t)(blk * 2), cudaMemcpyDeviceToDevice, st) !=
+                    cudaSuccess)
+        return BPT_ECUDA;
+    }
+  const int64_t kc = D.U * d, vc = kc + D.Hkv * d;
+  int rc;
+  if ((rc = project(D, xn, w->wk, hb ? w->bk : nullptr, D.Hkv * d, bfm(buf, kc), D.iw, st))) return rc;
+  if ((rc = project(D, xn, w->wv, hb ? w->bv : nullptr, D.Hkv * d, bfm(buf, vc), D.iw, st))) return rc;
+  if (D.rope != 0.f && (rc = rope_apply(D.rows, (int)D.s, buf, D.iw, (int)kc, (int)D.Hkv, (int)d, D.rope, 0, st)))
+    return rc;
+  if (keep_qkv && cudaMemcpy2DAsync(bfm(keep_qkv, D.H * d), (size_t)(D.full_w * 2), bf(buf, kc), (size_t)(D.iw * 2),
+                                    (size_t)(2 * D.Hkv * d * 2), (size_t)D.rows, cudaMemcpyDeviceToDevice,
+                                    st) != cudaSuccess)
+    return BPT_ECUDA;
+  for (int64_t k = 0; k < D.n_stages; ++k) {
+    if ((rc = project(D, xn, bf(wq_perm, k * D.U * d * h), hb ? bf(bq_perm, k * D.U * d) : nullptr, D.U * d, buf,
+                      D.iw, st)))
+      return rc;
+    if (D.rope != 0.f && (rc = rope_apply(D.rows, (int)D.s, buf, D.iw, 0, (int)D.U, (int)d, D.rope, 0, st))) return rc;
+    if (keep_qkv)
+      for (int64_t g = 0; g < D.Hkv; ++g)
+        if (cudaMemcpy2DAsync(bfm(keep_qkv, (g * D.G + k * D.m) * d), (size_t)(D.full_w * 2), bf(buf, g * blk),
+                              (size_t)(D.iw * 2), (size_t)(blk * 2), (size_t)D.rows, cudaMemcpyDeviceToDevice,
+                              st) != cudaSuccess)
+          return BPT_ECUDA;
+    AttnShape a;
+    a.b = (int)D.b;
+    a.s = (int)D.s;
+    a.H = (int)D.U;
+    a.Hkv = (int)D.Hkv;
+    a.d = (int)d;
+    a.causal = causal;
+    a.ld_qkv = D.iw;
+    a.q_col = 0;
+    a.k_col = kc;
+    a.v_col = vc;
+    a.ld_o = D.H * d;
+    a.o_col = k * blk;
+    a.o_seg = (int)D.m;
+    a.o_seg_stride = (int)D.G;
+    a.H_total = (int)D.H;
+    a.lse_head0 = (int)(k * D.m);
+    a.q_begin = 0;
+    a.q_end = (int)D.s;
+    a.o_row0 = 0;
+    if ((rc = attention_fwd(a, buf, o, lse, st))) return rc;
+  }
+  return 0;
 }
 
 // out[M, N] (fp32, beta) = sum_i A[:, Kseg_i] B_i  with MN-major B segments;
@@ -406,7 +543,8 @@ int bpt_last_device_error(void* stream, int* detail) {
 size_t bpt_saved_bytes(const bpt_config* cfg) {
   Dims D;
   if (validate(cfg, &D)) return 0;
-  return (size_t)(D.b * D.H * D.s_pad * 4);
+  Saved sv;
+  return plan_saved(D, nullptr, &sv);
 }
 
 size_t bpt_workspace_bytes(const bpt_config* cfg, int pass) {
@@ -414,15 +552,15 @@ size_t bpt_workspace_bytes(const bpt_config* cfg, int pass) {
   if (validate(cfg, &D)) return 0;
   if (pass == BPT_PASS_FWD) {
     FwdWs w;
-    return plan_fwd(D, nullptr, &w, true);
+    return plan_fwd(D, nullptr, &w, true, false);  // enough with or without `saved`
   }
   if (pass == BPT_PASS_BWD) {
     BwdWs w;
     return plan_bwd(D, nullptr, &w);
   }
   if (pass == BPT_PASS_HEADCHUNK) {
-    void* q;
-    return plan_headchunk(D, nullptr, &q);
+    HcWs w;
+    return plan_headchunk(D, nullptr, &w);
   }
   return 0;
 }
@@ -436,14 +574,15 @@ int bpt_layer_fwd(const bpt_config* cfg, const bpt_weights* w, const void* x, vo
   if (!x || !y || !ws || !aligned16(x) || !aligned16(y) || !aligned16(ws) || (saved && !aligned16(saved)))
     return BPT_EINVAL;
   FwdWs W;
-  const size_t need = plan_fwd(D, nullptr, &W, saved == nullptr);
+  const size_t need = plan_fwd(D, nullptr, &W, saved == nullptr, saved != nullptr);
   if (ws_bytes < need) return BPT_ENOSPC;
   if (D.debug) {
-    const int64_t act = D.rows * D.h * 2;
-    const Span sp[] = {{x, act}, {y, act}, {saved, saved ? D.b * D.H * D.s_pad * 4 : 0}, {ws, (int64_t)need}};
+    Saved sv;
+    const int64_t act = D.rows * D.h * 2, kept = (int64_t)plan_saved(D, nullptr, &sv);
+    const Span sp[] = {{x, act}, {y, act}, {saved, saved ? kept : 0}, {ws, (int64_t)need}};
     if (check_spans(sp, 4) || check_weights_range(cfg, D, w)) return BPT_EINVAL;
   }
-  plan_fwd(D, ws, &W, saved == nullptr);
+  plan_fwd(D, ws, &W, saved == nullptr, saved != nullptr);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   rc = layer_fwd(cfg, D, w, x, y, saved, W, st);
   if (rc) return rc;
@@ -457,21 +596,32 @@ namespace {
 int layer_fwd(const bpt_config* cfg, const Dims& D, const bpt_weights* w, const void* x, void* y, void* saved,
               const FwdWs& W, cudaStream_t st) {
   int rc;
-  float* lse = saved ? reinterpret_cast<float*>(saved) : W.lse;
+  Saved sv{nullptr, nullptr, nullptr};
+  if (saved) plan_saved(D, saved, &sv);
+  float* lse = saved ? sv.lse : W.lse;
+  // the projections and O go where the backward will find them when the
+  // save policy keeps them
+  void* obuf = sv.o ? sv.o : W.o;
+  const QkvBuf b0 = sv.qkv ? kept_buf(D, sv.qkv, 0) : stage_buf(D, W.qkv);
   const bool hb = cfg->has_bias != 0;
   const int64_t h = D.h, f = D.f, Hd = D.H * D.d;
 
   // N1 over the whole sequence
   if ((rc = norm_fwd(D.rows, (int)h, cfg->norm, cfg->norm_eps, x, 0, h, w->ln1_w, w->ln1_b, W.xn, h, st)))
     return rc;
-  if (D.chunked) {
+  if (D.interleave) {
+    if ((rc = interleaved_attention(D, w, hb, W.xn, W.qkv, W.wq_perm, W.bq_perm, obuf, lse, cfg->causal, sv.qkv,
+                                    st)))
+      return rc;
+  } else if (D.chunked) {
     for (int64_t k = 0; k < D.n_stages; ++k) {
-      if ((rc = stage_qkv(D, w, hb, W.xn, W.qkv, k, st))) return rc;
-      AttnShape a = stage_attn_shape(D, k, cfg->causal);
-      if ((rc = attention_fwd(a, W.qkv, W.o, lse, st))) return rc;
+      const QkvBuf b = sv.qkv ? kept_buf(D, sv.qkv, k) : stage_buf(D, W.qkv);
+      if ((rc = stage_qkv(D, w, hb, W.xn, b, k, st))) return rc;
+      AttnShape a = stage_attn_shape(D, k, cfg->causal, b);
+      if ((rc = attention_fwd(a, b.p, obuf, lse, st))) return rc;
     }
   } else {
-    if ((rc = stage_qkv(D, w, hb, W.xn, W.qkv, 0, st))) return rc;
+    if ((rc = stage_qkv(D, w, hb, W.xn, b0, 0, st))) return rc;
   }
 
   for (int64_t bi = 0; bi < D.b; ++bi) {
@@ -480,17 +630,18 @@ int layer_fwd(const bpt_config* cfg, const Dims& D, const bpt_weights* w, const 
       const int64_t row = bi * D.s + r0;
       const void* oblk;
       if (D.chunked) {
-        oblk = bf(W.o, row * Hd);
+        oblk = bf(obuf, row * Hd);
       } else {
-        // attention of this block's query rows, all heads
-        AttnShape a = stage_attn_shape(D, 0, cfg->causal);
+        // attention of this block's query rows, all heads: into the block
+        // buffer, or into the kept O at the rows' own place
+        AttnShape a = stage_attn_shape(D, 0, cfg->causal, b0);
         a.b = 1;
         a.q_begin = (int)r0;
         a.q_end = (int)(r0 + nr);
-        a.o_row0 = r0;
-        if ((rc = attention_fwd(a, bf(W.qkv, bi * D.s * D.qkv_w), W.o, lse + bi * D.H * D.s_pad, st)))
-          return rc;
-        oblk = W.o;
+        a.o_row0 = sv.o ? 0 : r0;
+        void* odst = sv.o ? bfm(sv.o, bi * D.s * Hd) : W.o;
+        if ((rc = attention_fwd(a, bf(b0.p, bi * D.s * b0.ld), odst, lse + bi * D.H * D.s_pad, st))) return rc;
+        oblk = sv.o ? bf(sv.o, row * Hd) : W.o;
       }
       // x1 = x + O Wo^T + bo
       {
@@ -555,8 +706,8 @@ int bpt_attn_headchunk(const bpt_config* cfg, const bpt_weights* w, const void* 
   if (!w || !w->wq || !w->wk || !w->wv || !xn || !o || !ws) return BPT_EINVAL;
   if (cfg->has_bias && (!w->bq || !w->bk || !w->bv)) return BPT_EINVAL;
   if (!aligned16(xn) || !aligned16(o) || !aligned16(ws) || (lse && !aligned16(lse))) return BPT_EINVAL;
-  void* qkv;
-  const size_t need = plan_headchunk(D, nullptr, &qkv);
+  HcWs hc;
+  const size_t need = plan_headchunk(D, nullptr, &hc);
   if (ws_bytes < need) return BPT_ENOSPC;
   if (D.debug) {
     const int64_t q = D.H * D.d, kv = D.Hkv * D.d, h = D.h;
@@ -567,12 +718,20 @@ int bpt_attn_headchunk(const bpt_config* cfg, const bpt_weights* w, const void* 
                        {w->bv, hb ? kv * 2 : 0}};
     if (check_spans(sp, 10)) return BPT_EINVAL;
   }
-  plan_headchunk(D, ws, &qkv);
+  plan_headchunk(D, ws, &hc);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  for (int64_t k = 0; k < D.n_stages; ++k) {
-    if ((rc = stage_qkv(D, w, cfg->has_bias != 0, xn, qkv, k, st))) return rc;
-    AttnShape a = stage_attn_shape(D, k, cfg->causal);
-    if ((rc = attention_fwd(a, qkv, o, reinterpret_cast<float*>(lse), st))) return rc;
+  const bool hb = cfg->has_bias != 0;
+  if (D.interleave) {
+    if ((rc = interleaved_attention(D, w, hb, xn, hc.qkv, hc.wq_perm, hc.bq_perm, o, reinterpret_cast<float*>(lse),
+                                    cfg->causal, nullptr, st)))
+      return rc;
+  } else {
+    for (int64_t k = 0; k < D.n_stages; ++k) {
+      const QkvBuf b = stage_buf(D, hc.qkv);
+      if ((rc = stage_qkv(D, w, hb, xn, b, k, st))) return rc;
+      AttnShape a = stage_attn_shape(D, k, cfg->causal, b);
+      if ((rc = attention_fwd(a, hc.qkv, o, reinterpret_cast<float*>(lse), st))) return rc;
+    }
   }
   return D.debug ? debug_finish(st) : BPT_OK;
 }
@@ -591,7 +750,7 @@ int bpt_attention_fwd(const bpt_config* cfg, const void* qkv, void* o, void* lse
                        {lse, lse ? D.b * D.H * D.s_pad * 4 : 0}};
     if (check_spans(sp, 3)) return BPT_EINVAL;
   }
-  AttnShape a = stage_attn_shape(F, 0, cfg->causal);
+  AttnShape a = stage_attn_shape(F, 0, cfg->causal, stage_buf(F, const_cast<void*>(qkv)));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if ((rc = attention_fwd(a, qkv, o, reinterpret_cast<float*>(lse), st))) return rc;
   return D.debug ? debug_finish(st) : BPT_OK;
@@ -673,7 +832,9 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
   if (ws_bytes < need) return BPT_ENOSPC;
   if (D.debug) {
     const int64_t act = D.rows * D.h * 2;
-    const Span sp[] = {{x, act}, {dy, act}, {dx, act}, {saved, D.b * D.H * D.s_pad * 4}, {ws, (int64_t)need}};
+    Saved kv;
+    const int64_t kept = (int64_t)plan_saved(D, nullptr, &kv);
+    const Span sp[] = {{x, act}, {dy, act}, {dx, act}, {saved, kept}, {ws, (int64_t)need}};
     if (check_spans(sp, 5) || check_weights_range(cfg, D, w) || check_grads_range(cfg, D, g)) return BPT_EINVAL;
   }
   plan_bwd(D, ws, &W);
@@ -686,7 +847,13 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
   cudaStream_t ss = one ? st : sd->s;
   auto fork = [&]() { return one ? 0 : fork_side(st, sd); };
   auto join = [&]() { return one ? 0 : join_side(st, sd); };
-  const float* lse = reinterpret_cast<const float*>(saved);
+  Saved sv;
+  plan_saved(D, saved, &sv);
+  const float* lse = sv.lse;
+  // O and the projections: kept by the forward (save policy) or rebuilt into
+  // the workspace
+  void* obuf = sv.o ? sv.o : W.o;
+  auto qbuf = [&](int64_t k) { return sv.qkv ? kept_buf(D, sv.qkv, k) : stage_buf(D, W.qkv); };
   const bool hb = cfg->has_bias != 0;
   const bool accum = (cfg->flags & BPT_FLAG_ACCUM_GRADS) != 0;
   const bool swiglu = cfg->act == BPT_ACT_SWIGLU;
@@ -702,13 +869,18 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
         return BPT_ECUDA;
     }
 
-    // ---- recompute N1, Q/K/V and attention (the saved LSE is not rewritten)
+    // ---- recompute N1, Q/K/V and attention (the saved LSE is not rewritten);
+    // what the forward kept is taken from `saved` instead (always contiguous
+    // stages here: the result does not depend on the stage order)
     if ((rc = norm_fwd(D.rows, (int)h, cfg->norm, cfg->norm_eps, x, 0, h, w->ln1_w, w->ln1_b, W.xn, h, st)))
       return rc;
-    for (int64_t k = 0; k < D.n_stages; ++k) {
-      if ((rc = stage_qkv(D, w, hb, W.xn, W.qkv, k, st))) return rc;
-      AttnShape a = stage_attn_shape(D, k, cfg->causal);
-      if ((rc = attention_fwd(a, W.qkv, W.o, nullptr, st))) return rc;
+    if (!sv.o) {
+      for (int64_t k = 0; k < D.n_stages; ++k) {
+        const QkvBuf b = qbuf(k);
+        if (!sv.qkv && (rc = stage_qkv(D, w, hb, W.xn, b, k, st))) return rc;
+        AttnShape a = stage_attn_shape(D, k, cfg->causal, b);
+        if ((rc = attention_fwd(a, b.p, obuf, nullptr, st))) return rc;
+      }
     }
 
     // ---- FFN blocks: rebuild x1, N2, fc1 and form the FFN / N2 gradients
@@ -719,7 +891,7 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
         const int64_t row = bi * D.s + r0;
         const float beta = (accum || !first) ? 1.f : 0.f;
         {
-          MatView A{bf(W.o, row * Hd), nr, Hd, Hd};
+          MatView A{bf(obuf, row * Hd), nr, Hd, Hd};
           MatView B{w->wo, h, Hd, Hd};
           Epilogue e;
           e.deterministic = D.det;
@@ -864,7 +1036,7 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
       // side stream: dWo and dbo need only dx1 and O, and run beside dO and
       // the attention backward
       MatView A2{W.dx1, D.rows, h, h};
-      MatView B2{W.o, D.rows, Hd, Hd};
+      MatView B2{obuf, D.rows, Hd, Hd};
       Epilogue e2;
       e2.deterministic = D.det;
       e2.kind = EPI_F32;
@@ -897,14 +1069,18 @@ int bpt_layer_bwd(const bpt_config* cfg, const bpt_weights* w, const void* x, co
         cudaMemsetAsync(g->bk, 0, (size_t)(D.Hkv * D.d) * sizeof(float), st) != cudaSuccess)
       return BPT_ECUDA;
     for (int64_t k = 0; k < D.n_stages; ++k) {
-      if (D.chunked && (rc = stage_qkv(D, w, hb, W.xn, W.qkv, k, st))) return rc;
+      const QkvBuf b = qbuf(k);
+      // the projections of stage k: kept by the forward, still in the stage
+      // buffer (one stage), or rebuilt (the recompute above made the last
+      // stage's, or none of them if O was kept)
+      if (!sv.qkv && (D.chunked || sv.o) && (rc = stage_qkv(D, w, hb, W.xn, b, k, st))) return rc;
       // the previous stage's weight gradients (side stream) read dqkv, which
       // this stage's attention backward rewrites
       if (k > 0 && (rc = join())) return rc;
-      AttnBwdShape sb = stage_bwd_shape(D, k);
+      AttnBwdShape sb = stage_bwd_shape(D, k, b);
       sb.f.causal = cfg->causal;
       sb.deterministic = D.det;
-      if ((rc = attention_bwd(sb, W.qkv, W.o, lse, W.dO, W.dqkv, W.attn, st))) return rc;
+      if ((rc = attention_bwd(sb, b.p, obuf, lse, W.dO, W.dqkv, W.attn, st))) return rc;
       // dQ, dK are gradients of the rotated heads: turn them back
       if (rope && (rc = rope_apply(D.rows, (int)D.s, W.dqkv, D.qkv_w, 0, (int)(D.U + D.Uk), (int)d, D.rope, 1, st)))
         return rc;

@@ -133,6 +133,10 @@ struct AttnShape {
   // buffer that holds only the processed block)
   int q_begin, q_end;
   int64_t o_row0;
+  // heads spread over the output (interleaved stages): local head n goes to
+  // output head (n / o_seg) * o_seg_stride + n % o_seg (O columns and LSE
+  // rows, both after o_col / lse_head0); o_seg = 0: output head n
+  int o_seg = 0, o_seg_stride = 0;
 };
 int attention_fwd(const AttnShape& sh, const void* qkv, void* o, float* lse, cudaStream_t st);
 

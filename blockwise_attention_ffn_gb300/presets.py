@@ -30,6 +30,8 @@ class LayerConfig:
     norm_eps: float = 1e-5
     flags: int = 0
     rope_base: float = 0.0  # rotary position embedding base; 0 = none
+    stage_order: int = 0    # head-chunk stages: 0 contiguous, 1 interleaved over the groups
+    save_policy: int = 0    # kept for the backward: 0 log-sum-exp, 1 + Q/K/V, 2 + attention output
     name: str = ""
     backward: bool = False  # the workload includes the backward pass
     seed: int = 0

@@ -111,6 +111,8 @@ enum {
 };
 
 enum { BPT_PASS_FWD = 0, BPT_PASS_BWD = 1, BPT_PASS_HEADCHUNK = 2 };
+enum { BPT_STAGE_CONTIGUOUS = 0, BPT_STAGE_INTERLEAVED = 1 };
+enum { BPT_SAVE_NOTHING = 0, BPT_SAVE_PROJECTIONS = 1, BPT_SAVE_ATTN_OUT = 2 };
 
 /* Shape and schedule of one layer.
  *   b, s, h            batch, sequence length, model width
@@ -139,7 +141,35 @@ enum { BPT_PASS_FWD = 0, BPT_PASS_BWD = 1, BPT_PASS_HEADCHUNK = 2 };
  *                      position p (the row's index within its sequence)
  *                      turns by p * rope_base^(-2i/d).  The layer calls and
  *                      bpt_attn_headchunk apply it; the attention-only calls
- *                      take Q/K as given.                                    */
+ *                      take Q/K as given.
+ *   stage_order        head-chunk stage order ("Untied Ulysses ...", section
+ *                      4.1 "The GQA Scheduling Algorithm"):
+ *                      BPT_STAGE_CONTIGUOUS (0): stage k takes query heads
+ *                      kU .. kU+U-1 and projects their U/G key/value heads
+ *                      itself;
+ *                      BPT_STAGE_INTERLEAVED (1): stage k takes the m = U/H_kv
+ *                      query heads gG + km .. gG + km + m-1 of every group g,
+ *                      and the key/value projections of all H_kv heads are made
+ *                      once and stay resident for every stage (U must be a
+ *                      multiple of H_kv).  Same result; the forward holds
+ *                      U d + 2 H_kv d columns of projections instead of
+ *                      (U + 2U/G) d.  The backward always runs the contiguous
+ *                      stages.  No effect without chunking.
+ *   save_policy        what the forward keeps for the backward, besides the
+ *                      log-sum-exp ("Blockwise Parallel Transformer ...",
+ *                      Appendix A.2 / Figure 3 notes: the checkpoint policies
+ *                      searched for attention; the FFN always recomputes):
+ *                      BPT_SAVE_NOTHING (0): nothing else; the backward
+ *                      rebuilds N1, Q/K/V and the attention output;
+ *                      BPT_SAVE_PROJECTIONS (1): also Q, K, V of every head
+ *                      (the contractions without batch dimensions), so the
+ *                      backward skips their projection;
+ *                      BPT_SAVE_ATTN_OUT (2): also the attention output O
+ *                      (the attention's dot products, combined across key
+ *                      blocks), so the backward skips the attention forward.
+ *                      The per-block score matrices are never kept: together
+ *                      they would be the s x s matrix the method avoids.
+ *                      bpt_saved_bytes grows accordingly.                    */
 typedef struct {
   int32_t b, s, h, n_heads, n_kv_heads, head_dim, ffn_dim;
   int32_t q_block, kv_block, ffn_block, head_chunk;
@@ -150,6 +180,8 @@ typedef struct {
   float norm_eps;
   int32_t flags;
   float rope_base;
+  int32_t stage_order;
+  int32_t save_policy;
 } bpt_config;
 
 /* bf16 device pointers, nn.Linear [out, in]; NULL where the variant has none
@@ -171,8 +203,10 @@ typedef struct {
 size_t bpt_workspace_bytes(const bpt_config* cfg, int pass);
 
 /* Bytes the forward pass saves for the backward pass: the log-sum-exp of
- * every attention row, fp32 [b, H, s_pad] (the only activation kept besides
- * the layer input x, which the caller keeps). */
+ * every attention row, fp32 [b, H, s_pad] (with BPT_SAVE_NOTHING the only
+ * activation kept besides the layer input x, which the caller keeps); with
+ * BPT_SAVE_PROJECTIONS also Q, K, V [b*s, (H + 2 H_kv) d] bf16, with
+ * BPT_SAVE_ATTN_OUT also O [b*s, H d] bf16 (each region 256-byte aligned). */
 size_t bpt_saved_bytes(const bpt_config* cfg);
 
 /* Forward pass of one layer.

@@ -107,6 +107,9 @@ def _call_fwd(cfg, x=1 << 20, y=1 << 20, ws=1 << 20, wsz=1 << 40):
     dict(ffn_block=100), dict(norm=2), dict(act=3), dict(norm_eps=0.0), dict(flags=16),
     dict(b=0), dict(causal=2), dict(has_bias=2), dict(n_kv_heads=0),
     dict(rope_base=0.5), dict(rope_base=-10000.0), dict(rope_base=float("nan")), dict(rope_base=float("inf")),
+    dict(stage_order=2), dict(stage_order=-1), dict(save_policy=3), dict(save_policy=-1),
+    # interleaved stages need whole groups: U = 2 over H_kv = 4 key/value heads
+    dict(n_heads=4, n_kv_heads=4, head_chunk=2, stage_order=1),
 ])
 def test_invalid_config_rejected_before_launch(built, bad):
     cfg = presets.C1.with_(**bad)
@@ -286,3 +289,35 @@ def test_missing_library_raises(monkeypatch):
         bpt.lib()
     with pytest.raises(RuntimeError):
         bpt.bpt_workspace_bytes(presets.C1, bpt.BPT_PASS_FWD)
+
+
+def test_schedule_options_sizes(built):
+    """The interleaved order keeps every key/value head resident (forward and
+    head-chunk workspaces grow by the difference, plus a copy of Wq in stage
+    order); the save policies grow the saved bytes by Q/K/V and O of every
+    row and leave the forward's workspace size (with or without a saved
+    buffer) alone, while the backward's shrinks."""
+    c5 = presets.C5                      # 32 over 8 heads of 128, U = 8
+    il = c5.with_(stage_order=bpt.BPT_STAGE_INTERLEAVED)
+    rows, d, h, H, Hk, U = c5.b * c5.s, c5.head_dim, c5.h, c5.n_heads, c5.n_kv_heads, c5.head_chunk
+
+    def up(n):
+        return (n + 255) // 256 * 256
+    contiguous_stage = up(rows * (U + 2 * U // (H // Hk)) * d * 2)
+    interleaved_stage = up(rows * (U + 2 * Hk) * d * 2)
+    wq_copy = up(H * d * h * 2) + up(H * d * 2)
+    assert (bpt.bpt_workspace_bytes(il, bpt.BPT_PASS_HEADCHUNK) ==
+            bpt.bpt_workspace_bytes(c5, bpt.BPT_PASS_HEADCHUNK) - contiguous_stage + interleaved_stage + wq_copy)
+    assert (bpt.bpt_workspace_bytes(il, bpt.BPT_PASS_FWD) ==
+            bpt.bpt_workspace_bytes(c5, bpt.BPT_PASS_FWD) - contiguous_stage + interleaved_stage + wq_copy)
+    assert bpt.bpt_workspace_bytes(il, bpt.BPT_PASS_BWD) == bpt.bpt_workspace_bytes(c5, bpt.BPT_PASS_BWD)
+    c3 = presets.C3
+    lse = bpt.bpt_saved_bytes(c3)
+    qkv = up(c3.s * (c3.n_heads + 2 * c3.n_kv_heads) * c3.head_dim * 2)
+    o = up(c3.s * c3.n_heads * c3.head_dim * 2)
+    assert bpt.bpt_saved_bytes(c3.with_(save_policy=1)) == up(lse) + qkv
+    assert bpt.bpt_saved_bytes(c3.with_(save_policy=2)) == up(lse) + qkv + o
+    for p in (1, 2):
+        assert bpt.bpt_workspace_bytes(c3.with_(save_policy=p), 0) == bpt.bpt_workspace_bytes(c3, 0)
+    assert bpt.bpt_workspace_bytes(c3.with_(save_policy=1), 1) == bpt.bpt_workspace_bytes(c3, 1) - qkv
+    assert bpt.bpt_workspace_bytes(c3.with_(save_policy=2), 1) == bpt.bpt_workspace_bytes(c3, 1) - qkv - o

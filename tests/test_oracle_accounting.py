@@ -129,3 +129,25 @@ def test_bench_flop_count_matches_oracle_accounting(name):
     want_exec = (2 * want["forward"] - want["fc2"] + 2 * want["linear"] + 2.5 * want["attn"]
                  + (2 + 2.5) * want["attn"] * (exact - 1) + extra)
     assert got["executed"] == pytest.approx(want_exec, rel=1e-12)
+
+
+@pytest.mark.parametrize("name,policy", [("c3", 1), ("c3", 2), ("c5", 1), ("c5", 2)])
+def test_bench_flop_count_drops_what_the_kept_activations_save(name, policy):
+    """With a save policy the backward does not rebuild the Q/K/V projection
+    (policy 1), nor the attention forward (policy 2): the executed count
+    drops by exactly those terms of the oracle's accounting; the model count
+    (3 forwards) does not change."""
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    from blockwise_attention_ffn_gb300.presets import PRESETS
+    from tests.oracle_helpers import oracle_cfg
+    c = PRESETS[name]
+    base = bench.flop_counts(c)
+    got = bench.flop_counts(c.with_(save_policy=policy))
+    want = A.step_flops(oracle_cfg(c))
+    exact = 1 + 1 / c.s
+    chunk_extra = want["qkv"] if c.head_chunk and c.head_chunk < c.n_heads else 0
+    drop = chunk_extra + want["qkv"] + (want["attn"] * exact if policy == 2 else 0)
+    assert got["executed"] == pytest.approx(base["executed"] - drop, rel=1e-12)
+    assert got["model"] == base["model"]

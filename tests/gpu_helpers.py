@@ -12,12 +12,20 @@ from blockwise_attention_ffn_gb300.synth import make_layer_inputs
 # max abs error <= 2e-2 and relative Frobenius error <= 5e-3.
 MAX_ABS = 2e-2
 REL_FRO = 5e-3
-# The gradients that flow back through the attention probabilities into the
-# Q/K/V and output projections and the first norm carry the error of the bf16
-# operands any tensor-core implementation must use (xn, Q, K, V above all);
-# tests/test_bf16_floor.py emulates that floor (0.55-0.75% at the GPT-3B and
-# Llama-8B shapes) and derives this bound for exactly those tensors.
-ATTN_GRAD_REL_FRO = 1.2e-2
+# The tensors whose error floor exceeds REL_FRO.  Any bf16-operand
+# implementation rounds xn, Q, K, V, P, O, dO, dS and dQ/dK/dV; emulating
+# exactly the roundings these kernels make around the exact fp64 layer
+# (tests/bf16_emulation.py; values in tests/golden/bf16_floor.json) puts the
+# relative Frobenius floor of these tensors above 5e-3 at a workload shape:
+# dWq 6.5e-3 (GPT-3B, s = 2048) and 8.0e-3 (Llama-8B, s = 1024), dWk alike,
+# dbq 6.2e-3, the N1 scale 7.7e-3, dWv 7.2e-3, dWo 7.1e-3, and dx 5.5e-3
+# (Llama-8B); with rotary embedding the key-bias gradient (identically zero
+# without it) 8.5e-3.  Every other tensor's floor is below 5e-3 (at most
+# 4.4e-3) and keeps REL_FRO.  tests/test_bf16_floor.py checks both sets
+# against the emulation.
+WIDE_TENSORS = ("wq", "bq", "wk", "bk", "wv", "wo", "ln1_w", "dx")
+# at least 1.5 times the largest floor of those tensors (8.5e-3)
+ATTN_GRAD_REL_FRO = 1.3e-2
 # The log-sum-exp is m + ln(l) with l the fp32 sum of the bf16-rounded
 # probabilities (the same values whose products with V form the numerator).
 # Each carries at most 2^-8 relative rounding (bf16 keeps 8 significant
@@ -25,7 +33,12 @@ ATTN_GRAD_REL_FRO = 1.2e-2
 # the bound adds fp32 noise on top.
 LSE_MAX_ABS = 4.1e-3
 LSE_REL_FRO = 2e-4
-ATTN_GRADS = ("wq", "bq", "wk", "bk", "wv", "bv", "wo", "bo", "ln1_w", "ln1_b")
+ATTN_GRADS = WIDE_TENSORS  # the weight gradients among them
+
+
+def rel_bound(name):
+    """Relative Frobenius bound of tensor `name` (a weight name or "dx")."""
+    return ATTN_GRAD_REL_FRO if name in WIDE_TENSORS else REL_FRO
 
 
 def half_ulp_bf16(x):
@@ -65,6 +78,7 @@ def assert_close(got, want, what, max_abs=MAX_ABS, rel_fro=REL_FRO, bf16_out=Tru
     elif rms_scale and want.size:
         scale = max(1.0, float(np.sqrt(np.mean(want * want))))
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    print(f"  {what}: max_abs(excess) {ma:.3e} (bound {max_abs * scale:.3e})  rel_fro {rf:.3e} (bound {rel_fro:.1e})")
     assert ma <= max_abs * scale and rf <= rel_fro, \
         f"{what}: max_abs(excess)={ma:.3e} (bound {max_abs * scale:.3e}) rel_fro={rf:.3e}"
     return ma, rf
@@ -75,15 +89,14 @@ def assert_close_grad(got, want, what, name=None):
     error in units of the tensor's largest entry when that exceeds 1.  A
     gradient that is exactly zero in exact arithmetic (the key bias: softmax
     is shift-invariant along a row) is checked for max abs error only.  The
-    gradients in ATTN_GRADS use the derived ATTN_GRAD_REL_FRO bound."""
+    gradients in WIDE_TENSORS use the derived ATTN_GRAD_REL_FRO bound."""
     want = np.asarray(want, np.float64)
     if np.max(np.abs(want), initial=0.0) < 1e-9:
         got = np.asarray(got, np.float64)
         assert np.all(np.isfinite(got)) and np.max(np.abs(got)) <= MAX_ABS, \
             f"{what}: exact value 0, max |got| = {np.max(np.abs(got)):.3e}"
         return float(np.max(np.abs(got))), 0.0
-    rf = ATTN_GRAD_REL_FRO if name in ATTN_GRADS else REL_FRO
-    return assert_close(got, want, what, rel_fro=rf, bf16_out=False, grad=True)
+    return assert_close(got, want, what, rel_fro=rel_bound(name), bf16_out=False, grad=True)
 
 
 def to64(t):

@@ -14,8 +14,8 @@ import torch
 
 from blockwise_attention_ffn_gb300.presets import PRESETS
 from oracle import sampled
-from tests.gpu_helpers import (ATTN_GRAD_REL_FRO, assert_close, assert_close_grad, device_inputs, run_bwd,
-                               run_fwd, to64)
+from tests.gpu_helpers import (assert_close, assert_close_grad, device_inputs, rel_bound, run_bwd, run_fwd,
+                               to64)
 from tests.oracle_helpers import inputs_to_oracle, oracle_cfg
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
@@ -54,6 +54,6 @@ def test_backward_sparse_upstream_gradient(name):
     o = inputs_to_oracle(inp)
     dx_ref, g_ref = sampled.backward_sparse_dy(o["x"], o["W"], to64(inp["dy"])[0, rows], rows,
                                                oracle_cfg(cfg))
-    assert_close(to64(dx)[0], dx_ref, f"{name} dx", grad=True, rel_fro=ATTN_GRAD_REL_FRO)
+    assert_close(to64(dx)[0], dx_ref, f"{name} dx", grad=True, rel_fro=rel_bound("dx"))
     for k, v in g_ref.items():
         assert_close_grad(to64(grads[k]), v, f"{name} d{k}", name=k)

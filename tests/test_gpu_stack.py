@@ -22,7 +22,7 @@ import blockwise_attention_ffn_gb300 as bpt
 from blockwise_attention_ffn_gb300 import stack
 from blockwise_attention_ffn_gb300.presets import LayerConfig
 from blockwise_attention_ffn_gb300.synth import make_layer_inputs
-from tests.gpu_helpers import ATTN_GRAD_REL_FRO, ATTN_GRADS, REL_FRO
+from tests.gpu_helpers import REL_FRO, rel_bound
 
 pytestmark = pytest.mark.gpu
 
@@ -90,6 +90,6 @@ def test_checkpointed_stack_equals_chained_layer_calls(flags):
                 got = grads[i][name]
                 den = float(ref_g.norm())
                 rel = float((got - ref_g).norm()) / den if den > 0 else float((got - ref_g).norm())
-                bound = 0.1 * (ATTN_GRAD_REL_FRO if name in ATTN_GRADS else REL_FRO)
+                bound = 0.1 * rel_bound(name)
                 print(f"k={k} layer {i} d{name} rel {rel:.2e} (bound {bound:.1e})")
                 assert rel <= bound, (k, i, name, rel)

@@ -57,3 +57,40 @@ def test_backward_sparse_upstream_gradient(name):
     assert_close(to64(dx)[0], dx_ref, f"{name} dx", grad=True, rel_fro=rel_bound("dx"))
     for k, v in g_ref.items():
         assert_close_grad(to64(grads[k]), v, f"{name} d{k}", name=k)
+
+
+# Rotary embedding at full length: at s = 131072 the highest-frequency pair
+# turns by up to 1.3e5 rad, where the kernel's fp64 angle reduction matters
+# (an fp32 product would be ~4e-3 rad off at the last rows).  The sampled
+# rows include the last two positions.  Bases: 10000 (the GPT-NeoX / Llama-2
+# value) for the long GPT layer, 500000 (Llama-3's) for the Llama-8B layer.
+ROPE_CASES = [("c4", 10000.0), ("c5", 500000.0)]
+
+
+@pytest.mark.parametrize("name,base", ROPE_CASES, ids=[c for c, _ in ROPE_CASES])
+def test_rope_forward_sampled_rows(name, base):
+    cfg = PRESETS[name].with_(rope_base=base)
+    inp, dev = device_inputs(cfg, seed=cfg.seed + 10, with_dy=False)
+    y, _ = run_fwd(cfg, dev)
+    rows = _rows(cfg.s, cfg.seed + 10)
+    o = inputs_to_oracle(inp)
+    want = sampled.forward_rows(o["x"], o["W"], oracle_cfg(cfg), rows)
+    got = to64(y[0, torch.as_tensor(rows, device=y.device)])
+    assert_close(got, want, f"{name} rope y[rows]", rms_scale=True)
+
+
+def test_rope_backward_sparse_upstream_gradient_llama():
+    cfg = PRESETS["c5"].with_(rope_base=500000.0)
+    inp, dev = device_inputs(cfg, seed=cfg.seed + 11)
+    rows = _rows(cfg.s, cfg.seed + 12)
+    mask = torch.zeros(cfg.s, dtype=torch.bool)
+    mask[torch.as_tensor(rows)] = True
+    dy_sparse = inp["dy"].clone()
+    dy_sparse[0, ~mask] = 0
+    _, saved = run_fwd(cfg, dev)
+    dx, grads = run_bwd(cfg, dev, saved, dy=dy_sparse.cuda())
+    o = inputs_to_oracle(inp)
+    dx_ref, g_ref = sampled.backward_sparse_dy(o["x"], o["W"], to64(inp["dy"])[0, rows], rows, oracle_cfg(cfg))
+    assert_close(to64(dx)[0], dx_ref, "c5 rope dx", grad=True, rel_fro=rel_bound("dx"))
+    for k, v in g_ref.items():
+        assert_close_grad(to64(grads[k]), v, f"c5 rope d{k}", name=k)

@@ -436,8 +436,13 @@ __global__ void __launch_bounds__(352, 1) attn_dkdv_hs_kernel(const __grid_const
       // P^T in fp32 (for dS^T) and as bf16 pairs (the dV operand)
       float pe[64];
       if (!edge) {
+        const uint64_t c2 = f2(c, c);
 #pragma unroll
-        for (int k = 0; k < 64; ++k) pe[k] = ex2(__uint_as_float(sv[k]) * c);
+        for (int k = 0; k < 64; k += 2) {
+          const float2 e = f2split(mul2(f2(__uint_as_float(sv[k]), __uint_as_float(sv[k + 1])), c2));
+          pe[k] = ex2(e.x);
+          pe[k + 1] = ex2(e.y);
+        }
       } else {
 #pragma unroll
         for (int k = 0; k < 64; ++k) pe[k] = (k < lo || k >= hi) ? 0.f : ex2(__uint_as_float(sv[k]) * c);
@@ -460,8 +465,10 @@ __global__ void __launch_bounds__(352, 1) attn_dkdv_hs_kernel(const __grid_const
       tmem_wait_ld(dr);
       uint32_t o[32];
 #pragma unroll
-      for (int k = 0; k < 64; k += 2)
-        o[k / 2] = pack_bf16(pe[k] * __uint_as_float(dr[k]), pe[k + 1] * __uint_as_float(dr[k + 1]));
+      for (int k = 0; k < 64; k += 2) {
+        const float2 v = f2split(mul2(f2(pe[k], pe[k + 1]), f2(__uint_as_float(dr[k]), __uint_as_float(dr[k + 1]))));
+        o[k / 2] = pack_bf16(v.x, v.y);
+      }
       tmem_st32(tdPb + lane_off, o);
       tmem_st_wait();
       tc_fence_before();
@@ -767,8 +774,13 @@ __global__ void __launch_bounds__(352, 1) attn_dq_hs_kernel(const __grid_constan
       // P stays in fp32 registers: no product here reads it, only dS
       float pe[64];
       if (hi >= 64) {
+        const uint64_t c2 = f2(c, c), nl2 = f2(nl, nl);
 #pragma unroll
-        for (int k = 0; k < 64; ++k) pe[k] = ex2(fmaf(__uint_as_float(sv[k]), c, nl));
+        for (int k = 0; k < 64; k += 2) {
+          const float2 e = f2split(fma2(f2(__uint_as_float(sv[k]), __uint_as_float(sv[k + 1])), c2, nl2));
+          pe[k] = ex2(e.x);
+          pe[k + 1] = ex2(e.y);
+        }
       } else {
 #pragma unroll
         for (int k = 0; k < 64; ++k) pe[k] = k < hi ? ex2(fmaf(__uint_as_float(sv[k]), c, nl)) : 0.f;
@@ -782,9 +794,13 @@ __global__ void __launch_bounds__(352, 1) attn_dq_hs_kernel(const __grid_constan
       tmem_ld32_nw(tdPb + lane_off + 32, dr + 32);
       tmem_wait_ld(dr);
       uint32_t o[32];
+      const uint64_t ds2 = f2(dsum, dsum);
 #pragma unroll
-      for (int k = 0; k < 64; k += 2)
-        o[k / 2] = pack_bf16(pe[k] * (__uint_as_float(dr[k]) - dsum), pe[k + 1] * (__uint_as_float(dr[k + 1]) - dsum));
+      for (int k = 0; k < 64; k += 2) {
+        const float2 v = f2split(
+            mul2(f2(pe[k], pe[k + 1]), sub2(f2(__uint_as_float(dr[k]), __uint_as_float(dr[k + 1])), ds2)));
+        o[k / 2] = pack_bf16(v.x, v.y);
+      }
       tmem_st32(tdPb + lane_off, o);
       tmem_st_wait();
       tc_fence_before();

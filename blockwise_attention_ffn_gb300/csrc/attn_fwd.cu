@@ -618,9 +618,12 @@ __global__ void __launch_bounds__(352, 1) attn_fwd_sk_kernel(const __grid_consta
       const float mc = (m_run == NEG_INF) ? 0.f : m_run * c;
       uint32_t pk[32];
       if (!edge) {
+        const uint64_t c2 = f2(c, c), nmc2 = f2(-mc, -mc);
 #pragma unroll
-        for (int i = 0; i < 64; i += 2)
-          pk[i / 2] = pack_bf16(ex2(fmaf(__uint_as_float(sv[i]), c, -mc)), ex2(fmaf(__uint_as_float(sv[i + 1]), c, -mc)));
+        for (int i = 0; i < 64; i += 2) {
+          const float2 e = f2split(fma2(f2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), c2, nmc2));
+          pk[i / 2] = pack_bf16(ex2(e.x), ex2(e.y));
+        }
       } else {
 #pragma unroll
         for (int i = 0; i < 64; i += 2) {

@@ -253,9 +253,10 @@ __global__ void __launch_bounds__(352, 1) attn_dkdv_hs_kernel(const __grid_const
       }
     }
   } else if (warp == 1 || warp == 10) {
-    // one issuer (fixed-order mode): warp 1 issues every sub-tile's products
+    // the whole warp runs the issue loop, one elected lane issues.  One
+    // issuer (fixed-order mode): warp 1 issues every sub-tile's products
     // in sub-tile order, so dV and dK take their products in a fixed order
-    if (lane == 0 && !(p.one_issuer && warp == 10)) {
+    if (!(p.one_issuer && warp == 10)) {
       // ------------------------------------------------ MMA issuers
       const int b0 = warp == 1 ? 0 : 1;  // this issuer's first sub-tile
       const int ustep = p.one_issuer ? 1 : 2;
@@ -276,14 +277,14 @@ __global__ void __launch_bounds__(352, 1) attn_dkdv_hs_kernel(const __grid_const
         const uint32_t uA = stage_u(u) + 2 * T::TILE + 64 * 16 * b;
         if constexpr (C::KV_TMEM) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a(tSb, tKA + kk * 8, T::kmajor(uQ, kk), ID_S, kk > 0);
-          umma_bf16_tmem_a(tSb, tKA + D / 2, sdesc(uA, uZero - uA, 128, 0u), ID_S, 1);
+          for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a_w(tSb, tKA + kk * 8, T::kmajor(uQ, kk), ID_S, kk > 0);
+          umma_bf16_tmem_a_w(tSb, tKA + D / 2, sdesc(uA, uZero - uA, 128, 0u), ID_S, 1);
         } else {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) umma_bf16(tSb, T::kmajor(uK, kk), T::kmajor(uQ, kk), ID_S, kk > 0);
-          umma_bf16(tSb, sdesc(uKx, uZero - uKx, 128, 0u), sdesc(uA, uZero - uA, 128, 0u), ID_S, 1);
+          for (int kk = 0; kk < D / 16; ++kk) umma_bf16_w(tSb, T::kmajor(uK, kk), T::kmajor(uQ, kk), ID_S, kk > 0);
+          umma_bf16_w(tSb, sdesc(uKx, uZero - uKx, 128, 0u), sdesc(uA, uZero - uA, 128, 0u), ID_S, 1);
         }
-        umma_commit(&s_full[b]);
+        umma_commit_w(&s_full[b]);
       };
       auto issue_dp = [&](int u) {
         const int b = u & 1;
@@ -293,21 +294,21 @@ __global__ void __launch_bounds__(352, 1) attn_dkdv_hs_kernel(const __grid_const
         if constexpr (C::KV_TMEM) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            umma_bf16_tmem_a(tdPb, tVA + kk * 8, T::kmajor(udO, kk), ID_S, kk > 0);
-          umma_bf16_tmem_a(tdPb, tVA + D / 2, sdesc(uA, uZero - uA, 128, 0u), ID_S, 1);
+            umma_bf16_tmem_a_w(tdPb, tVA + kk * 8, T::kmajor(udO, kk), ID_S, kk > 0);
+          umma_bf16_tmem_a_w(tdPb, tVA + D / 2, sdesc(uA, uZero - uA, 128, 0u), ID_S, 1);
         } else {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) umma_bf16(tdPb, T::kmajor(uV, kk), T::kmajor(udO, kk), ID_S, kk > 0);
-          umma_bf16(tdPb, sdesc(uVx, uZero - uVx, 128, 0u), sdesc(uA, uZero - uA, 128, 0u), ID_S, 1);
+          for (int kk = 0; kk < D / 16; ++kk) umma_bf16_w(tdPb, T::kmajor(uV, kk), T::kmajor(udO, kk), ID_S, kk > 0);
+          umma_bf16_w(tdPb, sdesc(uVx, uZero - uVx, 128, 0u), sdesc(uA, uZero - uA, 128, 0u), ID_S, 1);
         }
-        umma_commit(&dp_full[b]);
+        umma_commit_w(&dp_full[b]);
       };
       auto wait_stage = [&](int u) {
         const int t = u >> 1;
-        return bounded_wait(&qdo_full[t % QS], (t / QS) & 1, abort_flag, 641, p.err);
+        return bounded_wait_w(&qdo_full[t % QS], (t / QS) & 1, abort_flag, 641, p.err);
       };
-      bool ok = bounded_wait(kv_ready, 0, abort_flag, 642, p.err) &&
-                (C::KV_TMEM || bounded_wait(kv_full, 0, abort_flag, 646, p.err)) && wait_stage(b0);
+      bool ok = bounded_wait_w(kv_ready, 0, abort_flag, 642, p.err) &&
+                (C::KV_TMEM || bounded_wait_w(kv_full, 0, abort_flag, 646, p.err)) && wait_stage(b0);
       if (ok) {
         tc_fence_after();
         // sub-tiles 0 and 1 share stage 0 (U is even)
@@ -325,11 +326,11 @@ __global__ void __launch_bounds__(352, 1) attn_dkdv_hs_kernel(const __grid_const
         const bool more = u + 2 < U;
         // dV += P^T(u) dO(u): the P^T pairs sit over the first 32 columns of
         // buffer b; dO rows 64b.. are K blocks 4b..4b+3 of the stage's tile
-        if (!bounded_wait(&p_full[b], (u >> 1) & 1, abort_flag, 643, p.err)) { ok = false; break; }
+        if (!bounded_wait_w(&p_full[b], (u >> 1) & 1, abort_flag, 643, p.err)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          umma_bf16_tmem_a(tdV, tSb + kk * 8, T::mnmajor(udO, 4 * b + kk), ID_KV, 1);
+          umma_bf16_tmem_a_w(tdV, tSb + kk * 8, T::mnmajor(udO, 4 * b + kk), ID_KV, 1);
         if (more) {
           // S(u+2) overwrites P^T(u), after dV(u) in issue order
           if (!wait_stage(u + 2)) { ok = false; break; }
@@ -337,28 +338,28 @@ __global__ void __launch_bounds__(352, 1) attn_dkdv_hs_kernel(const __grid_const
           issue_s(u + 2);
         }
         // dK += dS^T(u) Q(u)
-        if (!bounded_wait(&ds_full[b], (u >> 1) & 1, abort_flag, 644, p.err)) { ok = false; break; }
+        if (!bounded_wait_w(&ds_full[b], (u >> 1) & 1, abort_flag, 644, p.err)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          umma_bf16_tmem_a(tdK, tdPb + kk * 8, T::mnmajor(uQ, 4 * b + kk), ID_KV, 1);
-        umma_commit(&qdo_empty[st]);
+          umma_bf16_tmem_a_w(tdK, tdPb + kk * 8, T::mnmajor(uQ, 4 * b + kk), ID_KV, 1);
+        umma_commit_w(&qdo_empty[st]);
         // dP(u+2) overwrites dS^T(u), after dK(u) in issue order
         if (more) issue_dp(u + 2);
       }
       if (ok) {
         // all_done counts two commits: one per issuer, or both from one
-        umma_commit(all_done);
-        if (p.one_issuer) umma_commit(all_done);
+        umma_commit_w(all_done);
+        if (p.one_issuer) umma_commit_w(all_done);
       }
       if (!ok) {
-        umma_commit(&drain[b0]);
+        umma_commit_w(&drain[b0]);
         drain_wait(&drain[b0], 0);
       }
     }
   } else {
     // ------------------------------------------------ compute (warps 2..9;
-    // lanes 1..31 of the issuer warps fall through to the final barrier)
+    // warp 10 in the one-issuer mode falls through to the final barrier)
     const int quarter = warp & 3;
     const int b = (warp - 2) >> 2;  // group = buffer = sub-tile parity
     const int r = quarter * 32 + lane;
@@ -637,9 +638,10 @@ __global__ void __launch_bounds__(352, 1) attn_dq_hs_kernel(const __grid_constan
       }
     }
   } else if (warp == 1 || warp == 10) {
-    // one issuer (fixed-order mode): warp 1 issues every sub-tile's products
+    // the whole warp runs the issue loop, one elected lane issues.  One
+    // issuer (fixed-order mode): warp 1 issues every sub-tile's products
     // in sub-tile order, so dQ takes its products in a fixed order
-    if (lane == 0 && !(p.one_issuer && warp == 10)) {
+    if (!(p.one_issuer && warp == 10)) {
       // ------------------------------------------------ MMA issuers
       const int b0 = warp == 1 ? 0 : 1;  // this issuer's first sub-tile
       const int ustep = p.one_issuer ? 1 : 2;
@@ -653,22 +655,22 @@ __global__ void __launch_bounds__(352, 1) attn_dq_hs_kernel(const __grid_constan
         const uint32_t tSb = tS + 64 * b;
         const uint32_t k = uK(u) + 64 * T::SWB * b;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a(tSb, tQA + kk * 8, T::kmajor(k, kk), ID_S, kk > 0);
-        umma_commit(&s_full[b]);
+        for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a_w(tSb, tQA + kk * 8, T::kmajor(k, kk), ID_S, kk > 0);
+        umma_commit_w(&s_full[b]);
       };
       auto issue_dp = [&](int u) {
         const int b = u & 1;
         const uint32_t tdPb = tdP + 64 * b;
         const uint32_t v = uK(u) + T::TILE + 64 * T::SWB * b;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a(tdPb, tOA + kk * 8, T::kmajor(v, kk), ID_S, kk > 0);
-        umma_commit(&dp_full[b]);
+        for (int kk = 0; kk < D / 16; ++kk) umma_bf16_tmem_a_w(tdPb, tOA + kk * 8, T::kmajor(v, kk), ID_S, kk > 0);
+        umma_commit_w(&dp_full[b]);
       };
       auto wait_stage = [&](int u) {
         const int jt = u >> 1;
-        return bounded_wait(&kv_full[jt % KVS], (jt / KVS) & 1, abort_flag, 671, p.err);
+        return bounded_wait_w(&kv_full[jt % KVS], (jt / KVS) & 1, abort_flag, 671, p.err);
       };
-      bool ok = bounded_wait(qo_ready, 0, abort_flag, 672, p.err) && wait_stage(b0);
+      bool ok = bounded_wait_w(qo_ready, 0, abort_flag, 672, p.err) && wait_stage(b0);
       if (ok) {
         tc_fence_after();
         // sub-tiles 0 and 1 share stage 0 (U is even)
@@ -684,7 +686,7 @@ __global__ void __launch_bounds__(352, 1) attn_dq_hs_kernel(const __grid_constan
         const bool more = u + 2 < U;
         if (more) {
           // S(u+2) once the group has read S(u)
-          if (!bounded_wait(&s_free[b], (u >> 1) & 1, abort_flag, 673, p.err) || !wait_stage(u + 2)) {
+          if (!bounded_wait_w(&s_free[b], (u >> 1) & 1, abort_flag, 673, p.err) || !wait_stage(u + 2)) {
             ok = false;
             break;
           }
@@ -692,28 +694,28 @@ __global__ void __launch_bounds__(352, 1) attn_dq_hs_kernel(const __grid_constan
           issue_s(u + 2);
         }
         // dQ += dS(u) K_u: key rows 64b.. are K blocks 4b..4b+3 of the tile
-        if (!bounded_wait(&ds_full[b], (u >> 1) & 1, abort_flag, 674, p.err)) { ok = false; break; }
+        if (!bounded_wait_w(&ds_full[b], (u >> 1) & 1, abort_flag, 674, p.err)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          umma_bf16_tmem_a(tdQ, tdPb + kk * 8, T::mnmajor(uK(u), 4 * b + kk), ID_DQ, 1);
-        umma_commit(&kv_empty[st]);
+          umma_bf16_tmem_a_w(tdQ, tdPb + kk * 8, T::mnmajor(uK(u), 4 * b + kk), ID_DQ, 1);
+        umma_commit_w(&kv_empty[st]);
         // dP(u+2) overwrites dS(u), after dQ(u) in issue order
         if (more) issue_dp(u + 2);
       }
       if (ok) {
         // all_done counts two commits: one per issuer, or both from one
-        umma_commit(all_done);
-        if (p.one_issuer) umma_commit(all_done);
+        umma_commit_w(all_done);
+        if (p.one_issuer) umma_commit_w(all_done);
       }
       if (!ok) {
-        umma_commit(&drain[b0]);
+        umma_commit_w(&drain[b0]);
         drain_wait(&drain[b0], 0);
       }
     }
   } else {
     // ------------------------------------------------ compute (warps 2..9;
-    // lanes 1..31 of the issuer warps fall through to the final barrier)
+    // warp 10 in the one-issuer mode falls through to the final barrier)
     const int quarter = warp & 3;
     const int b = (warp - 2) >> 2;  // group = buffer = sub-tile parity
     const int r = quarter * 32 + lane;

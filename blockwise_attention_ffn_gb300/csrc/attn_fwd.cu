@@ -198,37 +198,36 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------ MMA issuer
-      // order: S(0); per j: S(j+1), PV(j).  S(j+1) overwrites the buffer of
-      // P(j-1) after PV(j-1) in issue order.
-      const uint32_t uKV = smem_u32(sKV);
-      auto issue_s = [&](int j) -> bool {
-        if (!bounded_wait(&kv_full[j % KVS], (j / KVS) & 1, abort_flag, 213, p.err)) return false;
-        tc_fence_after();
-        const uint32_t kt = uKV + (j % KVS) * STAGE;
+    // ------------------------------------------------ MMA issuer (the
+    // whole warp runs the loop, one elected lane issues)
+    // order: S(0); per j: S(j+1), PV(j).  S(j+1) overwrites the buffer of
+    // P(j-1) after PV(j-1) in issue order.
+    const uint32_t uKV = smem_u32(sKV);
+    auto issue_s = [&](int j) -> bool {
+      if (!bounded_wait_w(&kv_full[j % KVS], (j / KVS) & 1, abort_flag, 213, p.err)) return false;
+      tc_fence_after();
+      const uint32_t kt = uKV + (j % KVS) * STAGE;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_bf16_tmem_a(tS + (j & 1) * 128, tQA + kk * 8, T::kmajor(kt, kk), IDESC_S, kk > 0);
-        umma_commit(&s_full[j & 1]);
-        return true;
-      };
-      bool ok = bounded_wait(q_ready, 0, abort_flag, 211, p.err) && issue_s(0);
-      for (int j = 0; ok && j < nkv; ++j) {
-        if (j + 1 < nkv && !issue_s(j + 1)) { ok = false; break; }
-        if (!bounded_wait(&p_full[j & 1], (j >> 1) & 1, abort_flag, 212, p.err)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t vt = uKV + (j % KVS) * STAGE + T::TILE;
+      for (int kk = 0; kk < D / 16; ++kk)
+        umma_bf16_tmem_a_w(tS + (j & 1) * 128, tQA + kk * 8, T::kmajor(kt, kk), IDESC_S, kk > 0);
+      umma_commit_w(&s_full[j & 1]);
+      return true;
+    };
+    bool ok = bounded_wait_w(q_ready, 0, abort_flag, 211, p.err) && issue_s(0);
+    for (int j = 0; ok && j < nkv; ++j) {
+      if (j + 1 < nkv && !issue_s(j + 1)) { ok = false; break; }
+      if (!bounded_wait_w(&p_full[j & 1], (j >> 1) & 1, abort_flag, 212, p.err)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t vt = uKV + (j % KVS) * STAGE + T::TILE;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_tmem_a(tO, tS + (j & 1) * 128 + kk * 8, T::mnmajor(vt, kk), IDESC_PV, (j > 0 || kk > 0));
-        umma_commit(&kv_empty[j % KVS]);
-        umma_commit(pv_done);
-      }
-      if (!ok) {
-        umma_commit(drain);
-        drain_wait(drain, 0);
-      }
+      for (int kk = 0; kk < 8; ++kk)
+        umma_bf16_tmem_a_w(tO, tS + (j & 1) * 128 + kk * 8, T::mnmajor(vt, kk), IDESC_PV, (j > 0 || kk > 0));
+      umma_commit_w(&kv_empty[j % KVS]);
+      umma_commit_w(pv_done);
+    }
+    if (!ok) {
+      umma_commit_w(drain);
+      drain_wait(drain, 0);
     }
   } else {
     // ------------------------------------------------ softmax (warps 2..5)
@@ -276,18 +275,12 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
       const bool edge = hi < 128;
       float mx = NEG_INF;
       if (!edge) {
-        if constexpr (EXT > 0) {
-          // two chains of three-input maxima (measured faster here; slower
-          // in the d = 128 instance, which keeps the plain chain)
-          float m2[2] = {NEG_INF, NEG_INF};
+        // four independent chains of three-input maxima
+        float m4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
 #pragma unroll
-          for (int i = 0; i < 128; i += 2)
-            m2[(i >> 1) & 1] = max3f(m2[(i >> 1) & 1], __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
-          mx = fmaxf(m2[0], m2[1]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 128; ++i) mx = fmaxf(mx, __uint_as_float(sv[i]));
-        }
+        for (int i = 0; i < 128; i += 2)
+          m4[(i >> 1) & 3] = max3f(m4[(i >> 1) & 3], __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
+        mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       } else {
 #pragma unroll
         for (int i = 0; i < 128; ++i)
@@ -327,9 +320,12 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
       // P over the first 64 columns of its own S buffer (all read above)
       tmem_st32(tb, *reinterpret_cast<const uint32_t(*)[32]>(pk));
       tmem_st32(tb + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
-      // PV(j-1) must be done before O is rescaled; waiting for it every step
-      // keeps these warps within one phase of pv_done
-      if (j > 0) {
+      // PV(j-1) must be done before O is rescaled.  Having seen S(j), which
+      // was issued after PV(j-2), these warps know pv_done is in phase j-1
+      // or j (PV(j) waits for this step's P), so a wait on the parity of
+      // j - 1 is exact however many phases went by unwaited.  The last step
+      // always waits, so the wait after the loop is exact too.
+      if (j > 0 && (rescale || j == nkv - 1)) {
         ok = bounded_wait(pv_done, (j - 1) & 1, abort_flag, 222, p.err);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
@@ -510,41 +506,40 @@ __global__ void __launch_bounds__(352, 1) attn_fwd_sk_kernel(const __grid_consta
       }
     }
   } else if (warp == 1 || warp == 10) {
-    if (lane == 0) {
-      // ------------------------------------------------ MMA issuers
-      // group b's products: S_b(j+1) = Q K_j[64b..]^T into its buffer
-      // (j+1) % 2, then O_b += P_b(j) V_j[64b..] (+ the row-sum chunk).
-      // S_b(j+1) overwrites P_b(j-1) after PV_b(j-1) from the same thread.
-      const int b = warp == 1 ? 0 : 1;
-      const uint32_t uKV = smem_u32(sKV);
-      const uint32_t tSb = tmem + 128 * b;
-      const uint32_t tOb = tmem + C::COL_O + b * C::OW;
-      auto issue_s = [&](int j) -> bool {
-        if (!bounded_wait(&kv_full[j % KVS], (j / KVS) & 1, abort_flag, 233, p.err)) return false;
-        tc_fence_after();
-        const uint32_t kt = uKV + (j % KVS) * STAGE + 64 * T::SWB * b;
+    // ------------------------------------------------ MMA issuers (the
+    // whole warp runs the loop, one elected lane issues)
+    // group b's products: S_b(j+1) = Q K_j[64b..]^T into its buffer
+    // (j+1) % 2, then O_b += P_b(j) V_j[64b..] (+ the row-sum chunk).
+    // S_b(j+1) overwrites P_b(j-1) after PV_b(j-1) from the same thread.
+    const int b = warp == 1 ? 0 : 1;
+    const uint32_t uKV = smem_u32(sKV);
+    const uint32_t tSb = tmem + 128 * b;
+    const uint32_t tOb = tmem + C::COL_O + b * C::OW;
+    auto issue_s = [&](int j) -> bool {
+      if (!bounded_wait_w(&kv_full[j % KVS], (j / KVS) & 1, abort_flag, 233, p.err)) return false;
+      tc_fence_after();
+      const uint32_t kt = uKV + (j % KVS) * STAGE + 64 * T::SWB * b;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_bf16_tmem_a(tSb + (j & 1) * 64, tQA + kk * 8, T::kmajor(kt, kk), IDESC_S, kk > 0);
-        umma_commit(&s_full[2 * b + (j & 1)]);
-        return true;
-      };
-      bool ok = bounded_wait(q_ready, 0, abort_flag, 234, p.err) && issue_s(0);
-      for (int j = 0; ok && j < nkv; ++j) {
-        if (j + 1 < nkv && !issue_s(j + 1)) { ok = false; break; }
-        if (!bounded_wait(&p_full[2 * b + (j & 1)], (j >> 1) & 1, abort_flag, 235, p.err)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t vt = uKV + (j % KVS) * STAGE + T::TILE;
+      for (int kk = 0; kk < D / 16; ++kk)
+        umma_bf16_tmem_a_w(tSb + (j & 1) * 64, tQA + kk * 8, T::kmajor(kt, kk), IDESC_S, kk > 0);
+      umma_commit_w(&s_full[2 * b + (j & 1)]);
+      return true;
+    };
+    bool ok = bounded_wait_w(q_ready, 0, abort_flag, 234, p.err) && issue_s(0);
+    for (int j = 0; ok && j < nkv; ++j) {
+      if (j + 1 < nkv && !issue_s(j + 1)) { ok = false; break; }
+      if (!bounded_wait_w(&p_full[2 * b + (j & 1)], (j >> 1) & 1, abort_flag, 235, p.err)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t vt = uKV + (j % KVS) * STAGE + T::TILE;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_bf16_tmem_a(tOb, tSb + (j & 1) * 64 + kk * 8, T::mnmajor(vt, 4 * b + kk), IDESC_PV, (j > 0 || kk > 0));
-        umma_commit(&kv_empty[j % KVS]);
-        umma_commit(&pv_done[b]);
-      }
-      if (!ok) {
-        umma_commit(&drain[b]);
-        drain_wait(&drain[b], 0);
-      }
+      for (int kk = 0; kk < 4; ++kk)
+        umma_bf16_tmem_a_w(tOb, tSb + (j & 1) * 64 + kk * 8, T::mnmajor(vt, 4 * b + kk), IDESC_PV, (j > 0 || kk > 0));
+      umma_commit_w(&kv_empty[j % KVS]);
+      umma_commit_w(&pv_done[b]);
+    }
+    if (!ok) {
+      umma_commit_w(&drain[b]);
+      drain_wait(&drain[b], 0);
     }
   } else {
     // ------------------------------------------------ softmax (warps 2..9)
@@ -595,11 +590,11 @@ __global__ void __launch_bounds__(352, 1) attn_fwd_sk_kernel(const __grid_consta
       const bool edge = hi < 64;
       float mx = NEG_INF;
       if (!edge) {
-        float m2[2] = {NEG_INF, NEG_INF};
+        float m4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
 #pragma unroll
         for (int i = 0; i < 64; i += 2)
-          m2[(i >> 1) & 1] = max3f(m2[(i >> 1) & 1], __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
-        mx = fmaxf(m2[0], m2[1]);
+          m4[(i >> 1) & 3] = max3f(m4[(i >> 1) & 3], __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
+        mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       } else {
 #pragma unroll
         for (int i = 0; i < 64; ++i)
@@ -634,9 +629,9 @@ __global__ void __launch_bounds__(352, 1) attn_fwd_sk_kernel(const __grid_consta
       }
       // P over the first 32 columns of its own S buffer (all read above)
       tmem_st32(tb, pk);
-      // PV(j-1) must be done before O is rescaled; waiting for it every step
-      // keeps these warps within one phase of pv_done
-      if (j > 0) {
+      // PV(j-1) must be done before O is rescaled; the wait is exact
+      // without the skipped ones, as in the one-group kernel
+      if (j > 0 && (rescale || j == nkv - 1)) {
         ok = bounded_wait(&pv_done[b], (j - 1) & 1, abort_flag, 242, p.err);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();

@@ -189,6 +189,46 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
       : "memory");
 }
 
+// Warp-wide forms, for an issuing warp whose 32 lanes all run the issue loop:
+// the loop stays convergent, so its counters and the descriptors it builds
+// are warp-uniform values, and one lane chosen by elect.sync issues the
+// instruction.  (With the loop inside a one-lane branch every product took
+// about 100 issuing-thread cycles, more than a 128 x 64 x 16 product takes on
+// the tensor core.)  Every lane of the warp must make the call.
+__device__ __forceinline__ void umma_bf16_w(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_bf16_tmem_a_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                                   uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit_w(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+// bounded_wait by every lane of a warp, with one verdict for all of them
+__device__ __forceinline__ bool bounded_wait_w(uint64_t* bar, uint32_t parity, volatile int* abort, int site,
+                                               unsigned int* err) {
+  return __all_sync(0xffffffffu, bounded_wait(bar, parity, abort, site, err));
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B and an fp32 accumulator.
 // a_mn / b_mn: operand is MN-major (contiguous along M resp. N) instead of
 // K-major.

@@ -5,7 +5,8 @@
 //
 // Persistent: one CTA per SM walks 128 x BN tiles of C.  Warp roles:
 //   warp 0      TMA producer: K-tiles of A and B into a 4-stage smem ring
-//   warp 1      TMEM owner and single-thread MMA issuer (M=128, N=BN, K=16)
+//   warp 1      TMEM owner and MMA issuer (M=128, N=BN, K=16): the warp runs
+//               the loop, one elected lane issues
 //               into one of two 256-column accumulators
 //   warps 2..9  epilogue: TMEM -> registers (one row per thread, half the
 //               columns per warp) -> fused bias / residual / activation ->
@@ -553,53 +554,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------ MMA issuer
-      const uint32_t smem_base = smem_u32(smem);
-      uint32_t it = 0;
-      int tc = 0;  // tiles done by this CTA
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++tc) {
-        const int acc = tc & 1;
-        // the epilogue must have drained this accumulator's previous tile
-        if (tc >= 2 && !bounded_wait(&acc_empty[acc], ((tc >> 1) - 1) & 1, abort_flag, 106, p.err)) {
+    // ------------------------------------------------ MMA issuer
+    const uint32_t smem_base = smem_u32(smem);
+    uint32_t it = 0;
+    int tc = 0;  // tiles done by this CTA
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++tc) {
+      const int acc = tc & 1;
+      // the epilogue must have drained this accumulator's previous tile
+      if (tc >= 2 && !bounded_wait_w(&acc_empty[acc], ((tc >> 1) - 1) & 1, abort_flag, 106, p.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d = tmem + (uint32_t)(acc * ACC_COLS);
+      int kb, ke;
+      k_range(p, tile, kb, ke);
+      for (int kt = kb; kt < ke; ++kt) {
+        const int s = it % STAGES;
+        if (!bounded_wait_w(&full[s], (it / STAGES) & 1, abort_flag, 103, p.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(acc * ACC_COLS);
-        int kb, ke;
-        k_range(p, tile, kb, ke);
-        for (int kt = kb; kt < ke; ++kt) {
-          const int s = it % STAGES;
-          if (!bounded_wait(&full[s], (it / STAGES) & 1, abort_flag, 103, p.err)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sa = smem_base + s * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
+        const uint32_t sa = smem_base + s * STAGE_BYTES;
+        const uint32_t sb = sa + A_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = A_MN ? sdesc(sa + kk * 2048, 8192, 1024, 2) : sdesc(sa + kk * 32, 16, 1024, 2);
-            const uint64_t bd = B_MN ? sdesc(sb + kk * 2048, 8192, 1024, 2) : sdesc(sb + kk * 32, 16, 1024, 2);
-            const bool accum = kt != kb || kk != 0;
-            umma_bf16(d, ad, bd, IDESC, accum);
-            if (DUAL) {
-              const uint64_t bd2 = sdesc(sb + BN * BK * 2 + kk * 32, 16, 1024, 2);
-              umma_bf16(d + BN, ad, bd2, IDESC, accum);
-            }
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint64_t ad = A_MN ? sdesc(sa + kk * 2048, 8192, 1024, 2) : sdesc(sa + kk * 32, 16, 1024, 2);
+          const uint64_t bd = B_MN ? sdesc(sb + kk * 2048, 8192, 1024, 2) : sdesc(sb + kk * 32, 16, 1024, 2);
+          const bool accum = kt != kb || kk != 0;
+          umma_bf16_w(d, ad, bd, IDESC, accum);
+          if (DUAL) {
+            const uint64_t bd2 = sdesc(sb + BN * BK * 2 + kk * 32, 16, 1024, 2);
+            umma_bf16_w(d + BN, ad, bd2, IDESC, accum);
           }
-          umma_commit(&empty[s]);
-          ++it;
         }
-        if (!ok) break;
-        umma_commit(&acc_full[acc]);
+        umma_commit_w(&empty[s]);
+        ++it;
       }
-      if (!ok) {
-        umma_commit(drain);  // wait until nothing issued is still in flight
-        drain_wait(drain, 0);
-      }
+      if (!ok) break;
+      umma_commit_w(&acc_full[acc]);
+    }
+    if (!ok) {
+      umma_commit_w(drain);  // wait until nothing issued is still in flight
+      drain_wait(drain, 0);
     }
   } else {
     // ------------------------------------------------ epilogue (warps 2..9)

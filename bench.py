@@ -427,17 +427,40 @@ def run_gpu(args, c):
                 "per_launch_bytes": dv["bytes"] / dv["launches"],
                 "avg_launch_ms": dv["ms"] / dv["launches"], "traffic": traffic}
 
-    # end to end through the C ABI from pinned host buffers
+    # end to end through the C ABI from pinned host buffers.  Every step
+    # copies its x and dy in and its dx out inside the timed region; dy
+    # travels on a second stream while the forward runs (the backward waits
+    # for it), and dx leaves on that stream while the next step's x copy and
+    # forward run (the next backward, which overwrites dx, waits for it)
     xh = x.cpu().pin_memory()
     dyh = dy.cpu().pin_memory() if c.backward else None
     outh = torch.empty_like(xh).pin_memory()
+    copy_st = torch.cuda.Stream(dev)
+    ev_in, ev_used, ev_out = (torch.cuda.Event() for _ in range(3))
+    n_e2e = [0]
 
     def step_e2e():
         x.copy_(xh, non_blocking=True)
-        if c.backward:
+        if not c.backward:
+            bpt.bpt_layer_fwd(c, W, x, y, saved, ws, stream)
+            outh.copy_(y, non_blocking=True)
+            return
+        if n_e2e[0]:
+            copy_st.wait_event(ev_used)  # the previous backward has read dy
+        with torch.cuda.stream(copy_st):
             dy.copy_(dyh, non_blocking=True)
-        step()
-        outh.copy_(dx if c.backward else y, non_blocking=True)
+            ev_in.record(copy_st)
+        bpt.bpt_layer_fwd(c, W, x, y, saved, ws, stream)
+        stream.wait_event(ev_in)
+        if n_e2e[0]:
+            stream.wait_event(ev_out)  # the previous dx has been copied out
+        bpt.bpt_layer_bwd(c, W, x, saved, dy, dx, grads, ws, stream)
+        ev_used.record(stream)
+        copy_st.wait_event(ev_used)
+        with torch.cuda.stream(copy_st):
+            outh.copy_(dx, non_blocking=True)
+            ev_out.record(copy_st)
+        n_e2e[0] += 1
 
     for _ in range(max(1, args.warmup // 2)):
         step_e2e()
@@ -607,15 +630,28 @@ def run_gpu_lm(args, c):
     launches = sum(v["launches"] for v in prof.values()) / nprof
     # end to end: x and the targets in from pinned host memory, dx and the
     # loss back
+    # dx leaves on a second stream while the next step's copies in and
+    # forward run; the next backward, which overwrites dx, waits for it
     xh, th = x.cpu().pin_memory(), t.cpu().pin_memory()
     dxh, lh = torch.empty_like(xh).pin_memory(), torch.empty(1).pin_memory()
+    copy_st = torch.cuda.Stream(dev)
+    ev_used, ev_out = torch.cuda.Event(), torch.cuda.Event()
+    n_e2e = [0]
 
     def step_e2e():
         x.copy_(xh, non_blocking=True)
         t.copy_(th, non_blocking=True)
-        step()
-        dxh.copy_(dx, non_blocking=True)
-        lh.copy_(loss, non_blocking=True)
+        bpt.bpt_lm_loss_fwd(c, x, w, t, loss, lse, ws, stream)
+        if n_e2e[0]:
+            stream.wait_event(ev_out)
+        bpt.bpt_lm_loss_bwd(c, x, w, t, lse, 1.0, dx, dw, ws, stream)
+        lh.copy_(loss, non_blocking=True)  # on this stream: the next forward rewrites it
+        ev_used.record(stream)
+        copy_st.wait_event(ev_used)
+        with torch.cuda.stream(copy_st):
+            dxh.copy_(dx, non_blocking=True)
+            ev_out.record(copy_st)
+        n_e2e[0] += 1
 
     for _ in range(max(1, args.warmup // 2)):
         step_e2e()

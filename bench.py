@@ -69,6 +69,56 @@ def vanilla_activation_bytes(c) -> int:
     return 34 * c.s * c.b * c.h + 5 * c.n_heads * c.s * c.s * c.b
 
 
+def vanilla_layer_bytes(c, inp, dev):
+    """Device bytes of the plain materialised layer, for the memory
+    comparison only (never for results): the layer written with PyTorch ops
+    on the GPU in bf16, Q K^T and the probabilities materialised per head,
+    every activation kept by autograd for a backward.  Returns the peak
+    during the forward and the bytes still held after it, both above the
+    inputs and weights."""
+    import torch
+    import torch.nn.functional as F
+
+    W = {k: (None if v is None else v.detach().clone().requires_grad_(True)) for k, v in inp["weights"].items()}
+    x = inp["x"].detach().clone().requires_grad_(True)
+    b, s, h, H, Hk, d = c.b, c.s, c.h, c.n_heads, c.n_kv_heads, c.head_dim
+
+    def norm(t, w, bias):
+        if c.norm == 0:
+            return F.layer_norm(t, (h,), w, bias, 1e-5)
+        return t * torch.rsqrt(t.float().pow(2).mean(-1, keepdim=True) + 1e-5).to(t.dtype) * w
+
+    def lin(t, w, bias=None):
+        return F.linear(t, W[w], W[bias] if bias and W.get(bias) is not None else None)
+
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats(dev)
+    base = torch.cuda.memory_allocated(dev)
+    xn = norm(x, W["ln1_w"], W.get("ln1_b"))
+    q = lin(xn, "wq", "bq").view(b, s, H, d).transpose(1, 2)
+    k = lin(xn, "wk", "bk").view(b, s, Hk, d).transpose(1, 2).repeat_interleave(H // Hk, dim=1)
+    v = lin(xn, "wv", "bv").view(b, s, Hk, d).transpose(1, 2).repeat_interleave(H // Hk, dim=1)
+    sc = (q @ k.transpose(-1, -2)) * (1.0 / d ** 0.5)
+    if c.causal:
+        sc = sc.masked_fill(torch.ones(s, s, dtype=torch.bool, device=dev).triu(1), float("-inf"))
+    o = (torch.softmax(sc, dim=-1) @ v).transpose(1, 2).reshape(b, s, H * d)
+    x1 = x + lin(o, "wo", "bo")
+    x1n = norm(x1, W["ln2_w"], W.get("ln2_b"))
+    if c.act == 2:
+        a = F.silu(lin(x1n, "w1")) * lin(x1n, "w3")
+    else:
+        a = F.gelu(lin(x1n, "w1", "b1"), approximate="tanh" if c.act == 1 else "none")
+    y = x1 + lin(a, "w2", "b2")
+    torch.cuda.synchronize()
+    peak = torch.cuda.max_memory_allocated(dev) - base
+    held = torch.cuda.memory_allocated(dev) - base
+    del y, a, x1n, x1, o, sc, q, k, v, xn
+    torch.cuda.synchronize()
+    return {"peak_bytes": int(peak), "held_after_forward_bytes": int(held),
+            "what": "plain PyTorch bf16 layer on the GPU, scores and probabilities materialised, "
+                    "activations kept for a backward (memory comparison only)"}
+
+
 # ----------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -498,6 +548,13 @@ def run_gpu(args, c):
                        "workspace_bytes": ws_bytes, "saved_bytes": bpt.bpt_saved_bytes(c),
                        "vanilla_layer_activation_bytes_analytic": vanilla_activation_bytes(c)},
         }
+        # the materialised layer where it fits comfortably (the analytic
+        # estimate under 32 GB: the forward-only workloads)
+        if vanilla_activation_bytes(c) < 32 * 2 ** 30:
+            try:
+                line["memory"]["vanilla_layer_measured"] = vanilla_layer_bytes(c, inp, dev)
+            except Exception as e:  # noqa: BLE001 - reported in the line
+                line["memory"]["vanilla_layer_measured"] = {"error": repr(e)}
         if not args.no_cpu_baseline and world == 1:
             # a reported baseline, not the measurement: a failure here must not
             # cost the line

@@ -802,6 +802,8 @@ def main():
                     help="query heads per stage U (the workload's own by default)")
     ap.add_argument("--stage-order", type=int, default=0, choices=[0, 1],
                     help="head-chunk stage order: 0 contiguous, 1 interleaved over the key/value groups")
+    ap.add_argument("--ffn-block", type=int, default=None,
+                    help="rows per FFN block c_f (the workload's own by default)")
     ap.add_argument("--save-policy", type=int, default=0, choices=[0, 1, 2],
                     help="kept for the backward: 0 the log-sum-exp, 1 + Q/K/V, 2 + the attention output")
     ap.add_argument("--profile-kernel", choices=["attn_fwd", "attn_bwd", "layer"], default=None,
@@ -827,6 +829,8 @@ def main():
         c = c.with_(rope_base=args.rope_base)
     if args.head_chunk is not None:
         c = c.with_(head_chunk=args.head_chunk)
+    if args.ffn_block is not None:
+        c = c.with_(ffn_block=args.ffn_block)
     if args.stage_order or args.save_policy:
         c = c.with_(stage_order=args.stage_order, save_policy=args.save_policy)
     if args.profile_kernel:

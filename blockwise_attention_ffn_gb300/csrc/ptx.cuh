@@ -159,42 +159,17 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]^T, bf16 inputs, fp32 accumulate.
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// D[tmem] (+)= A[tmem] * B[smem desc]^T: A (M = 128 lanes, K along the
-// columns, two bf16 per 32-bit column, the lower K index in the low half)
-// read from tensor memory.
-__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                                 uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// Arrives once on `bar` when every MMA this thread issued so far has completed.
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-
-// Warp-wide forms, for an issuing warp whose 32 lanes all run the issue loop:
-// the loop stays convergent, so its counters and the descriptors it builds
-// are warp-uniform values, and one lane chosen by elect.sync issues the
-// instruction.  (With the loop inside a one-lane branch every product took
-// about 100 issuing-thread cycles, more than a 128 x 64 x 16 product takes on
-// the tensor core.)  Every lane of the warp must make the call.
+// tcgen05 products and commits, issued by a warp whose 32 lanes all run the
+// issue loop: the loop stays convergent, so its counters and the descriptors
+// it builds are warp-uniform values, and one lane chosen by elect.sync issues
+// the instruction.  (With the loop inside a one-lane branch every product
+// took about 100 issuing-thread cycles, more than a 128 x 64 x 16 product
+// takes on the tensor core.)  Every lane of the warp must make the call.
+// umma_bf16_w: D[tmem] (+)= A[smem desc] * B[smem desc]^T, bf16 inputs, fp32
+// accumulate; umma_bf16_tmem_a_w: A (M = 128 lanes, K along the columns, two
+// bf16 per 32-bit column, the lower K index in the low half) from tensor
+// memory; umma_commit_w: arrives once on `bar` when every product the warp
+// issued so far has completed.
 __device__ __forceinline__ void umma_bf16_w(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(

@@ -91,13 +91,13 @@ enum { BPT_ACT_GELU_ERF = 0, BPT_ACT_GELU_TANH = 1, BPT_ACT_SWIGLU = 2 };
  *                         partial sums with atomics.  Each such result is
  *                         then off by at most a rounding step of the
  *                         summation order (one bf16 unit for dQ/dK/dV).  With
- *                         the flag: one issuing thread per CTA, no K split,
+ *                         the flag: one issuing warp per CTA, no K split,
  *                         and per-block partial sums written to the workspace
  *                         and added in block order by a second kernel.  The
- *                         attention backward then takes about 1.6-1.7 times
- *                         as long, the layer backward about 1.3 times
- *                         (measured: 32.1 -> 43.5 ms at the GPT-3B workload,
- *                         176 -> 224 ms at the Llama-8B one).
+ *                         attention backward then takes about 1.35-1.5 times
+ *                         as long, the layer backward about 1.15-1.25 times
+ *                         (measured: 29.1 -> 36.0 ms at the GPT-3B workload,
+ *                         166.6 -> 190.8 ms at the Llama-8B one).
  *  BPT_FLAG_DEBUG_CHECKS  before any launch, every device pointer argument
  *                         must lie, with the bytes the call touches through
  *                         it, inside one device allocation of the current

@@ -15,7 +15,7 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libbpt.so")
-SOURCES = ["bpt_api.cu", "gemm_tc.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_bwd_noalloc.cu", "norm_misc.cu",
+SOURCES = ["bpt_api.cu", "gemm_tc.cu", "gemm_pair.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_bwd_noalloc.cu", "norm_misc.cu",
            "host_util.cu", "lm_loss.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]

@@ -1,7 +1,7 @@
 // ptx.cuh -- thin inline-PTX wrappers for the sm_103a features the kernels use:
-// mbarriers, TMA tensor loads (no multicast), bulk reductions, and the 5th
+// mbarriers, TMA tensor loads (no multicast), bulk reductions, the 5th
 // generation tensor core (tcgen05: TMEM allocation, MMA, commit, TMEM loads and
-// stores).  Every wait is bounded (see bounded_wait) so a kernel can never spin
+// stores), and the same for two CTAs sharing one product.  Every wait is bounded (see bounded_wait) so a kernel can never spin
 // forever: it records an error in the device error word and unwinds.
 #pragma once
 
@@ -370,6 +370,111 @@ __device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool pred) {
 }
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------- CTA pairs
+// A cluster of two CTAs on two SMs that share one tensor-core product
+// (cta_group::2, M = 256): each CTA stages its 128 rows of A and half of B's
+// rows in its own shared memory at the same offsets, and holds its 128 rows
+// of the accumulator in its own TMEM at the same columns; rank 0 issues the
+// products.  Every tcgen05 instruction of such a kernel names cta_group::2.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// shared::cluster address of the object at shared::cta address `saddr` in
+// the cluster's CTA `rank`
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+// every thread of every CTA of the cluster (also a barrier of this CTA)
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// arrive on an mbarrier given by its shared::cluster address (either CTA)
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cl_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// bounded_wait on a barrier that the other CTA of the pair arrives on, by
+// every lane of a warp, one verdict for all of them
+__device__ __forceinline__ bool bounded_wait_cluster_w(uint64_t* bar, uint32_t parity, volatile int* abort, int site,
+                                                       unsigned int* err) {
+  bool ok = mbar_try_wait_cluster(bar, parity);
+  if (!ok) {
+    const long long t0 = clock64();
+    while (true) {
+      if (mbar_try_wait_cluster(bar, parity)) {
+        ok = true;
+        break;
+      }
+      if (*abort) break;
+      if (clock64() - t0 > BPT_WAIT_CYCLES) {
+        report_timeout(err, site);
+        *abort = 1;
+        break;
+      }
+    }
+  }
+  return __all_sync(0xffffffffu, ok);
+}
+// TMA load into this CTA's shared memory whose completion (bytes) is counted
+// on an mbarrier of either CTA of the pair (shared::cluster address)
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar_cl, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cl), "r"(x), "r"(y)
+      : "memory");
+}
+// TMEM allocation for the pair: one warp of each CTA makes the call
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// umma_bf16_w over the pair (issued by rank 0): rows 0..127 of A and the
+// first half of B's rows from rank 0's shared memory, the rest from rank 1's
+__device__ __forceinline__ void umma_bf16_pair_w(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// arrives once on the mbarrier at shared::cta address of `bar` in each CTA of
+// the pair named by `mask` (bit r: rank r) when the pair's products issued so
+// far have completed
+__device__ __forceinline__ void umma_commit_pair_w(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(
+          smem_u32(bar)),
+      "h"(mask)
+      : "memory");
 }
 
 }  // namespace bpt

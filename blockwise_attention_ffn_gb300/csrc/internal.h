@@ -78,7 +78,8 @@ enum EpiKind {
   // language-model loss, logits z = acc of column n (vocabulary id col0 + n):
   EPI_LSE = 6,         // per row and tile half: (max z, sum exp(z - max)) over
                        // the valid columns -> float2 out[part * ldo + m],
-                       // part = 2 * tile column + half; z of the row's target
+                       // part = 2 * tile column + half (tiles are 256 columns
+                       // wide, so part = column / 128); z of the row's target
                        // rowi[m] (if in this tile) -> float out2[m]
   EPI_CE_GRAD = 7,     // out = (exp(z - rowf[m]) - [col0 + n == rowi[m]]) * scale -> bf16
 };

@@ -253,6 +253,207 @@ __global__ void __launch_bounds__(512) norm_bwd_kernel(int64_t rows, int h, int 
   }
 }
 
+// The same backward with its rows staged in shared memory by the copy engine.
+// A block takes a contiguous band of rows in groups of R; `ns` ring stages of
+// R rows (x, dy and res of each row side by side) are filled by 1-D bulk
+// copies issued by thread 0, ns - 1 groups ahead of the group being
+// processed, so the loads stay in flight however few warps the block has.
+// Per group:
+//  1. the rows' statistics from shared memory, as the forward computes them
+//     (mean, then the centred sums), and the two row sums of the gradient,
+//     each row split over P = warps / R warps whose partial sums are
+//     combined in a fixed order;
+//  2. each thread owns 8 columns: for every row of the group it forms dx
+//     (stored straight to global memory, a row per block-wide access) and
+//     accumulates dw, db in registers.
+// Every row is read from HBM once.  Rows, the row strides and every pointer
+// are 16-byte aligned (the host checks; it takes norm_bwd_kernel otherwise).
+__global__ void __launch_bounds__(512, 1) norm_bwd_staged_kernel(int64_t rows, int h, int kind, float eps,
+                                                                 NormBwdIO io, const __nv_bfloat16* w, float* dw,
+                                                                 float* db, int64_t band, float* part, int R, int ns,
+                                                                 unsigned int* err) {
+  extern __shared__ __align__(128) uint8_t sm[];
+  const int xe = io.x_f32 ? 4 : 2, de = io.dy_f32 ? 4 : 2, re = io.res ? (io.res_f32 ? 4 : 2) : 0;
+  const int xb = h * xe, dyb = h * de, rb = h * re;
+  const int row_bytes = xb + dyb + rb;
+  const int stage_bytes = R * row_bytes;
+  float* stat = reinterpret_cast<float*>(sm + (size_t)ns * stage_bytes);  // [R][4]
+  float* red = stat + 4 * ((R + 1) & ~1);                                  // [R][P][3] partial sums
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + 48);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + ns);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarp = blockDim.x >> 5;  // at most 16
+  const int P = nwarp / R;             // warps per row for the statistics (R <= warps)
+  const int64_t r0 = (int64_t)blockIdx.x * band;
+  const int64_t r1 = min(rows, r0 + band);
+  const int ngroups = r0 < r1 ? (int)((r1 - r0 + R - 1) / R) : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ns; ++s) mbar_init(&full[s], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // group g into stage g % ns (thread 0)
+  auto issue = [&](int g) {
+    const int s = g % ns;
+    const int64_t gr = r0 + (int64_t)g * R;
+    const int nr = (int)min((int64_t)R, r1 - gr);
+    uint8_t* base = sm + (size_t)s * stage_bytes;
+    mbar_expect_tx(&full[s], (uint32_t)(nr * row_bytes));
+    for (int i = 0; i < nr; ++i) {
+      uint8_t* rp = base + (size_t)i * row_bytes;
+      const int64_t r = gr + i;
+      bulk_load(rp, reinterpret_cast<const uint8_t*>(io.x) + r * io.ldx * xe, (uint32_t)xb, &full[s]);
+      bulk_load(rp + xb, reinterpret_cast<const uint8_t*>(io.dy) + r * io.lddy * de, (uint32_t)dyb, &full[s]);
+      if (rb) bulk_load(rp + xb + dyb, reinterpret_cast<const uint8_t*>(io.res) + r * io.ldres * re, (uint32_t)rb,
+                        &full[s]);
+    }
+  };
+  if (threadIdx.x == 0)
+    for (int g = 0; g < min(ns, ngroups); ++g) issue(g);
+
+  const int c = threadIdx.x * 8;
+  const bool active = c < h;
+  float adw[8], adb[8], wv[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) adw[k] = adb[k] = wv[k] = 0.f;
+  if (active) ld8(w + c, wv);
+  int g = 0;
+  for (; g < ngroups; ++g) {
+    const int s = g % ns;
+    const int64_t gr = r0 + (int64_t)g * R;
+    const int nr = (int)min((int64_t)R, r1 - gr);
+    const bool ok = __syncthreads_and(bounded_wait(&full[s], (uint32_t)(g / ns) & 1u, abort_flag, 301, err));
+    if (!ok) break;
+    const uint8_t* base = sm + (size_t)s * stage_bytes;
+    // 1. statistics: P warps per row (warp w takes part w % P of row w / P,
+    //    every P-th 256-column chunk), partial sums combined in a fixed order
+    {
+      const int i = warp / P, p = warp % P;
+      const bool mine = i < nr;
+      const uint8_t* xs = base + (size_t)i * row_bytes;
+      const uint8_t* ds = xs + xb;
+      if (kind == 0) {
+        float sx = 0.f;
+        if (mine)
+          for (int c0 = (p * 32 + lane) * 8; c0 < h; c0 += P * 256) {
+            float v[8];
+            ld8x(xs, io.x_f32, c0, v);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) sx += v[k];
+          }
+        sx = warp_sum(sx);
+        if (mine && lane == 0) red[(i * P + p) * 3] = sx;
+        __syncthreads();
+        if ((int)threadIdx.x < nr) {
+          float t = 0.f;
+          for (int u = 0; u < P; ++u) t += red[((int)threadIdx.x * P + u) * 3];
+          stat[threadIdx.x * 4] = t / h;
+        }
+        __syncthreads();
+      }
+      const float mean = (kind == 0 && mine) ? stat[i * 4] : 0.f;
+      float q = 0.f, sg = 0.f, sgx = 0.f;
+      if (mine)
+        for (int c0 = (p * 32 + lane) * 8; c0 < h; c0 += P * 256) {
+          float v[8], gv[8], w8[8];
+          ld8x(xs, io.x_f32, c0, v);
+          ld8x(ds, io.dy_f32, c0, gv);
+          ld8(w + c0, w8);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float t = v[k] - mean;
+            const float gg = gv[k] * w8[k];
+            q += t * t;
+            sg += gg;
+            sgx += gg * t;
+          }
+        }
+      q = warp_sum(q);
+      sg = warp_sum(sg);
+      sgx = warp_sum(sgx);
+      if (mine && lane == 0) {
+        float* o = red + (i * P + p) * 3;
+        o[0] = q;
+        o[1] = sg;
+        o[2] = sgx;
+      }
+      __syncthreads();
+      if ((int)threadIdx.x < nr) {
+        float Q = 0.f, SG = 0.f, SGX = 0.f;
+        for (int u = 0; u < P; ++u) {
+          const float* o = red + ((int)threadIdx.x * P + u) * 3;
+          Q += o[0];
+          SG += o[1];
+          SGX += o[2];
+        }
+        const float rstd = rsqrtf(Q / h + eps);
+        float* o = stat + threadIdx.x * 4;
+        if (kind != 0) o[0] = 0.f;
+        o[1] = rstd;
+        o[2] = (kind == 0) ? SG / h : 0.f;
+        o[3] = SGX * rstd / h;
+      }
+    }
+    __syncthreads();
+    // 2. dx and the scale/shift gradients, 8 columns per thread
+    if (active) {
+      for (int i = 0; i < nr; ++i) {
+        const uint8_t* xs = base + (size_t)i * row_bytes;
+        const float4 s4 = *reinterpret_cast<const float4*>(stat + i * 4);
+        float v[8], gv[8], rv[8];
+        ld8x(xs, io.x_f32, c, v);
+        ld8x(xs + xb, io.dy_f32, c, gv);
+        if (rb) ld8x(xs + xb + dyb, io.res_f32, c, rv);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float xh = (v[k] - s4.x) * s4.y;
+          adw[k] += gv[k] * xh;
+          adb[k] += gv[k];
+          v[k] = s4.y * (gv[k] * wv[k] - s4.z - xh * s4.w) + (rb ? rv[k] : 0.f);
+        }
+        const int64_t r = gr + i;
+        st8(reinterpret_cast<__nv_bfloat16*>(io.dx) + r * io.lddx + c, v);
+        if (io.dx_f32) {
+          float4* o = reinterpret_cast<float4*>(io.dx_f32 + r * io.lddx + c);
+          o[0] = make_float4(v[0], v[1], v[2], v[3]);
+          o[1] = make_float4(v[4], v[5], v[6], v[7]);
+        }
+      }
+    }
+    // stage s and the statistics are free again
+    __syncthreads();
+    if (threadIdx.x == 0 && g + ns < ngroups) {
+      fence_proxy_async_smem();
+      issue(g + ns);
+    }
+  }
+  if (g < ngroups) {
+    // gave up waiting: let the copies already issued land before the block
+    // (and its shared memory) goes away
+    if (threadIdx.x == 0)
+      for (int j = g; j < min(ngroups, g + ns); ++j) drain_wait(&full[j % ns], (uint32_t)(j / ns) & 1u);
+    return;
+  }
+  if (active) {
+    if (part) {
+      float* pw = part + (int64_t)blockIdx.x * 2 * h + c;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        pw[k] = adw[k];
+        pw[h + k] = adb[k];
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (dw) atomicAdd(&dw[c + k], adw[k]);
+        if (db) atomicAdd(&db[c + k], adb[k]);
+      }
+    }
+  }
+}
+
 // out[n] += sum_r in[r, n]; 8 columns per thread, rows split over gridDim.y
 // Column sums of a bf16 [rows x n] matrix, added atomically into fp32 out.
 // A block covers 256 columns (8 per lane of a warp) and a band of rows; its 8
@@ -465,9 +666,64 @@ int reduce_parts(int nparts, int64_t n, const float* part, int64_t ldp, float* o
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 
+// The staged form when every row starts on a 16-byte boundary and at least
+// two ring stages of a row each fit the shared-memory budget; returns -1
+// when it does not apply.
+static int norm_bwd_staged(int64_t rows, int h, int kind, float eps, const NormBwdIO& io, const void* w,
+                           float* dw, float* db, cudaStream_t st, float* part) {
+  constexpr int BUDGET = 200 * 1024;  // bytes of ring stages per block (one block per SM)
+  auto al = [](const void* p, int64_t ld, int elem) {
+    return p == nullptr || ((reinterpret_cast<uintptr_t>(p) & 15) == 0 && ((ld * elem) & 15) == 0);
+  };
+  const int xe = io.x_f32 ? 4 : 2, de = io.dy_f32 ? 4 : 2, re = io.res ? (io.res_f32 ? 4 : 2) : 0;
+  if (h % 8 || h > 4096 || !al(io.x, io.ldx, xe) || !al(io.dy, io.lddy, de) || !al(io.res, io.ldres, re ? re : 2))
+    return -1;
+  const int row_bytes = h * (xe + de + re);
+  // groups of up to 4 rows (no more than the block's warps: each row's
+  // statistics take at least one) with at least three stages, or single rows
+  const int threads = std::max(64, (h / 8 + 31) / 32 * 32);
+  int R = std::min(4, threads / 32);
+  while (R > 1 && 3 * R * row_bytes > BUDGET) --R;
+  const int ns = std::min(8, BUDGET / (R * row_bytes));
+  if (ns < 2) return -1;
+  const int smem = ns * R * row_bytes + 16 * ((R + 1) & ~1) + 4 * 48 + 8 * ns + 16;
+  // the limit is raised once per device, to the largest size any call asks for
+  static std::atomic<uint64_t> attr{0};
+  if (smem_limit_once(reinterpret_cast<const void*>(norm_bwd_staged_kernel), BUDGET + 1024, &attr)) return 3;
+  const int64_t nsm = sm_count() > 0 ? sm_count() : 1;
+  // one block per SM, contiguous bands of rows; the fixed-order mode keeps
+  // the unstaged kernel's bands (at most NORM_DET_BLOCKS partial sums)
+  int64_t band;
+  if (part) {
+    band = std::max<int64_t>(8, (rows + NORM_DET_BLOCKS - 1) / NORM_DET_BLOCKS);
+  } else {
+    const int64_t g0 = std::min<int64_t>(nsm, (rows + R - 1) / R);
+    band = (rows + g0 - 1) / g0;
+  }
+  const int64_t grid = (rows + band - 1) / band;
+  unsigned int* err = device_error_word();
+  if (!err) return 3;
+  ProfScope prof(PROF_NORM, 0.0,
+                 (double)rows * h * ((io.dy_f32 ? 4 : 2) + (io.x_f32 ? 4 : 2) + (io.res ? (io.res_f32 ? 4 : 2) : 0) + 2 +
+                                     (io.dx_f32 ? 4 : 0)),
+                 st);
+  norm_bwd_staged_kernel<<<(unsigned)grid, threads, smem, st>>>(rows, h, kind, eps, io, (const __nv_bfloat16*)w,
+                                                                dw, db, band, part, R, ns, err);
+  if (cudaGetLastError() != cudaSuccess) return 3;
+  if (part) {
+    if (dw && reduce_parts((int)grid, h, part, 2 * (int64_t)h, dw, st)) return 3;
+    if (db && reduce_parts((int)grid, h, part + h, 2 * (int64_t)h, db, st)) return 3;
+  }
+  return 0;
+}
+
 int norm_bwd(int64_t rows, int h, int kind, float eps, const NormBwdIO& io, const void* w, float* dw,
              float* db, cudaStream_t st, float* part) {
   if (rows <= 0) return 0;
+  {
+    const int rc = norm_bwd_staged(rows, h, kind, eps, io, w, dw, db, st, part);
+    if (rc >= 0) return rc;
+  }
   // one thread per 8 columns (a whole row per block up to h = 4096), 64..512
   // threads
   int threads = (h / 8 + 31) / 32 * 32;

@@ -253,36 +253,55 @@ __global__ void __launch_bounds__(512) norm_bwd_kernel(int64_t rows, int h, int 
   }
 }
 
+// rows per group of the staged norm backward, at most
+constexpr int NB_MAX_R = 8;
+
+// 4 consecutive values of a bf16 or fp32 row (8- or 16-byte accesses)
+__device__ __forceinline__ void ld4x(const void* base, int f32, int64_t idx, float (&v)[4]) {
+  if (f32) {
+    const float4 a = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + idx);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  } else {
+    const uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(base) + idx);
+    v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x);
+    v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
+  }
+}
+
 // The same backward with its rows staged in shared memory by the copy engine.
 // A block takes a contiguous band of rows in groups of R; `ns` ring stages of
 // R rows (x, dy and res of each row side by side) are filled by 1-D bulk
 // copies issued by thread 0, ns - 1 groups ahead of the group being
-// processed, so the loads stay in flight however few warps the block has.
-// Per group:
+// processed, so the loads stay in flight whatever the block does meanwhile.
+// Each thread owns 4 consecutive columns (h / 4 threads, up to 1024), so a
+// warp's shared-memory accesses are contiguous 8- or 16-byte pieces, free of
+// bank conflicts.  Per group:
 //  1. the rows' statistics from shared memory, as the forward computes them
 //     (mean, then the centred sums), and the two row sums of the gradient,
-//     each row split over P = warps / R warps whose partial sums are
-//     combined in a fixed order;
-//  2. each thread owns 8 columns: for every row of the group it forms dx
-//     (stored straight to global memory, a row per block-wide access) and
-//     accumulates dw, db in registers.
+//     each row split over P = warps / R warps whose partial sums are added
+//     in a fixed order (each warp adds its row's partial sums of x itself,
+//     one thread per row the rest);
+//  2. for every row of the group each thread forms dx for its columns
+//     (stored straight to global memory) and accumulates dw, db in
+//     registers.
 // Every row is read from HBM once.  Rows, the row strides and every pointer
 // are 16-byte aligned (the host checks; it takes norm_bwd_kernel otherwise).
-__global__ void __launch_bounds__(512, 1) norm_bwd_staged_kernel(int64_t rows, int h, int kind, float eps,
-                                                                 NormBwdIO io, const __nv_bfloat16* w, float* dw,
-                                                                 float* db, int64_t band, float* part, int R, int ns,
-                                                                 unsigned int* err) {
+__global__ void __launch_bounds__(1024, 1) norm_bwd_staged_kernel(int64_t rows, int h, int kind, float eps,
+                                                                  NormBwdIO io, const __nv_bfloat16* w, float* dw,
+                                                                  float* db, int64_t band, float* part, int R, int ns,
+                                                                  unsigned int* err) {
   extern __shared__ __align__(128) uint8_t sm[];
   const int xe = io.x_f32 ? 4 : 2, de = io.dy_f32 ? 4 : 2, re = io.res ? (io.res_f32 ? 4 : 2) : 0;
   const int xb = h * xe, dyb = h * de, rb = h * re;
   const int row_bytes = xb + dyb + rb;
   const int stage_bytes = R * row_bytes;
   float* stat = reinterpret_cast<float*>(sm + (size_t)ns * stage_bytes);  // [R][4]
-  float* red = stat + 4 * ((R + 1) & ~1);                                  // [R][P][3] partial sums
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + 48);
+  float* red = stat + 4 * NB_MAX_R;                                       // [R][P][3] partial sums
+  float* red1 = red + 3 * 32;                                             // [R][P] partial sums of x
+  uint64_t* full = reinterpret_cast<uint64_t*>(red1 + 32);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(full + ns);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nwarp = blockDim.x >> 5;  // at most 16
+  const int nwarp = blockDim.x >> 5;  // at most 32
   const int P = nwarp / R;             // warps per row for the statistics (R <= warps)
   const int64_t r0 = (int64_t)blockIdx.x * band;
   const int64_t r1 = min(rows, r0 + band);
@@ -313,22 +332,25 @@ __global__ void __launch_bounds__(512, 1) norm_bwd_staged_kernel(int64_t rows, i
   if (threadIdx.x == 0)
     for (int g = 0; g < min(ns, ngroups); ++g) issue(g);
 
-  const int c = threadIdx.x * 8;
+  const int c = threadIdx.x * 4;
   const bool active = c < h;
-  float adw[8], adb[8], wv[8];
+  float adw[4], adb[4], wv[4];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) adw[k] = adb[k] = wv[k] = 0.f;
-  if (active) ld8(w + c, wv);
+  for (int k = 0; k < 4; ++k) adw[k] = adb[k] = wv[k] = 0.f;
+  if (active) ld4x(w, 0, c, wv);
   int g = 0;
   for (; g < ngroups; ++g) {
     const int s = g % ns;
     const int64_t gr = r0 + (int64_t)g * R;
     const int nr = (int)min((int64_t)R, r1 - gr);
-    const bool ok = __syncthreads_and(bounded_wait(&full[s], (uint32_t)(g / ns) & 1u, abort_flag, 301, err));
+    // one warp polls the stage's barrier, the others wait at the block
+    // barrier (and see the copied rows through it)
+    const bool ok =
+        __syncthreads_and(warp != 0 || bounded_wait(&full[s], (uint32_t)(g / ns) & 1u, abort_flag, 301, err));
     if (!ok) break;
     const uint8_t* base = sm + (size_t)s * stage_bytes;
     // 1. statistics: P warps per row (warp w takes part w % P of row w / P,
-    //    every P-th 256-column chunk), partial sums combined in a fixed order
+    //    every P-th 128-column chunk), partial sums combined in a fixed order
     {
       const int i = warp / P, p = warp % P;
       const bool mine = i < nr;
@@ -337,34 +359,33 @@ __global__ void __launch_bounds__(512, 1) norm_bwd_staged_kernel(int64_t rows, i
       if (kind == 0) {
         float sx = 0.f;
         if (mine)
-          for (int c0 = (p * 32 + lane) * 8; c0 < h; c0 += P * 256) {
-            float v[8];
-            ld8x(xs, io.x_f32, c0, v);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) sx += v[k];
+          for (int c0 = (p * 32 + lane) * 4; c0 < h; c0 += P * 128) {
+            float v[4];
+            ld4x(xs, io.x_f32, c0, v);
+            sx += (v[0] + v[1]) + (v[2] + v[3]);
           }
         sx = warp_sum(sx);
-        if (mine && lane == 0) red[(i * P + p) * 3] = sx;
-        __syncthreads();
-        if ((int)threadIdx.x < nr) {
-          float t = 0.f;
-          for (int u = 0; u < P; ++u) t += red[((int)threadIdx.x * P + u) * 3];
-          stat[threadIdx.x * 4] = t / h;
-        }
+        if (mine && lane == 0) red1[i * P + p] = sx;
         __syncthreads();
       }
-      const float mean = (kind == 0 && mine) ? stat[i * 4] : 0.f;
+      // each warp of a row adds the row's partial sums itself (same order);
+      // red1 is rewritten only after the barrier that ends the group
+      float mean = 0.f;
+      if (kind == 0 && mine) {
+        for (int u = 0; u < P; ++u) mean += red1[i * P + u];
+        mean /= h;
+      }
       float q = 0.f, sg = 0.f, sgx = 0.f;
       if (mine)
-        for (int c0 = (p * 32 + lane) * 8; c0 < h; c0 += P * 256) {
-          float v[8], gv[8], w8[8];
-          ld8x(xs, io.x_f32, c0, v);
-          ld8x(ds, io.dy_f32, c0, gv);
-          ld8(w + c0, w8);
+        for (int c0 = (p * 32 + lane) * 4; c0 < h; c0 += P * 128) {
+          float v[4], gv[4], w4[4];
+          ld4x(xs, io.x_f32, c0, v);
+          ld4x(ds, io.dy_f32, c0, gv);
+          ld4x(w, 0, c0, w4);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
+          for (int k = 0; k < 4; ++k) {
             const float t = v[k] - mean;
-            const float gg = gv[k] * w8[k];
+            const float gg = gv[k] * w4[k];
             q += t * t;
             sg += gg;
             sgx += gg * t;
@@ -381,45 +402,44 @@ __global__ void __launch_bounds__(512, 1) norm_bwd_staged_kernel(int64_t rows, i
       }
       __syncthreads();
       if ((int)threadIdx.x < nr) {
-        float Q = 0.f, SG = 0.f, SGX = 0.f;
+        const int r = threadIdx.x;
+        float M = 0.f, Q = 0.f, SG = 0.f, SGX = 0.f;
         for (int u = 0; u < P; ++u) {
-          const float* o = red + ((int)threadIdx.x * P + u) * 3;
+          const float* o = red + (r * P + u) * 3;
+          if (kind == 0) M += red1[r * P + u];
           Q += o[0];
           SG += o[1];
           SGX += o[2];
         }
         const float rstd = rsqrtf(Q / h + eps);
-        float* o = stat + threadIdx.x * 4;
-        if (kind != 0) o[0] = 0.f;
+        float* o = stat + r * 4;
+        o[0] = (kind == 0) ? M / h : 0.f;
         o[1] = rstd;
         o[2] = (kind == 0) ? SG / h : 0.f;
         o[3] = SGX * rstd / h;
       }
     }
     __syncthreads();
-    // 2. dx and the scale/shift gradients, 8 columns per thread
+    // 2. dx and the scale/shift gradients, 4 columns per thread
     if (active) {
       for (int i = 0; i < nr; ++i) {
         const uint8_t* xs = base + (size_t)i * row_bytes;
         const float4 s4 = *reinterpret_cast<const float4*>(stat + i * 4);
-        float v[8], gv[8], rv[8];
-        ld8x(xs, io.x_f32, c, v);
-        ld8x(xs + xb, io.dy_f32, c, gv);
-        if (rb) ld8x(xs + xb + dyb, io.res_f32, c, rv);
+        float v[4], gv[4], rv[4];
+        ld4x(xs, io.x_f32, c, v);
+        ld4x(xs + xb, io.dy_f32, c, gv);
+        if (rb) ld4x(xs + xb + dyb, io.res_f32, c, rv);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < 4; ++k) {
           const float xh = (v[k] - s4.x) * s4.y;
           adw[k] += gv[k] * xh;
           adb[k] += gv[k];
           v[k] = s4.y * (gv[k] * wv[k] - s4.z - xh * s4.w) + (rb ? rv[k] : 0.f);
         }
         const int64_t r = gr + i;
-        st8(reinterpret_cast<__nv_bfloat16*>(io.dx) + r * io.lddx + c, v);
-        if (io.dx_f32) {
-          float4* o = reinterpret_cast<float4*>(io.dx_f32 + r * io.lddx + c);
-          o[0] = make_float4(v[0], v[1], v[2], v[3]);
-          o[1] = make_float4(v[4], v[5], v[6], v[7]);
-        }
+        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(io.dx) + r * io.lddx + c) =
+            make_uint2(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]));
+        if (io.dx_f32) *reinterpret_cast<float4*>(io.dx_f32 + r * io.lddx + c) = make_float4(v[0], v[1], v[2], v[3]);
       }
     }
     // stage s and the statistics are free again
@@ -440,13 +460,13 @@ __global__ void __launch_bounds__(512, 1) norm_bwd_staged_kernel(int64_t rows, i
     if (part) {
       float* pw = part + (int64_t)blockIdx.x * 2 * h + c;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < 4; ++k) {
         pw[k] = adw[k];
         pw[h + k] = adb[k];
       }
     } else {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < 4; ++k) {
         if (dw) atomicAdd(&dw[c + k], adw[k]);
         if (db) atomicAdd(&db[c + k], adb[k]);
       }
@@ -679,14 +699,16 @@ static int norm_bwd_staged(int64_t rows, int h, int kind, float eps, const NormB
   if (h % 8 || h > 4096 || !al(io.x, io.ldx, xe) || !al(io.dy, io.lddy, de) || !al(io.res, io.ldres, re ? re : 2))
     return -1;
   const int row_bytes = h * (xe + de + re);
-  // groups of up to 4 rows (no more than the block's warps: each row's
-  // statistics take at least one) with at least three stages, or single rows
-  const int threads = std::max(64, (h / 8 + 31) / 32 * 32);
-  int R = std::min(4, threads / 32);
-  while (R > 1 && 3 * R * row_bytes > BUDGET) --R;
-  const int ns = std::min(8, BUDGET / (R * row_bytes));
-  if (ns < 2) return -1;
-  const int smem = ns * R * row_bytes + 16 * ((R + 1) & ~1) + 4 * 48 + 8 * ns + 16;
+  // one thread per 4 columns; two stages of as many rows as fit (never more
+  // rows than warps: each row's statistics take at least one).  Larger groups
+  // beat deeper rings: a group costs four or five block barriers whatever its size
+  // (measured per GPT-3B s=32K step: 1.01 ms of norms with two stages of 5
+  // and 4 rows, 1.14 with three of 3 and 2, 1.60 with single rows).
+  const int threads = std::max(64, (h / 4 + 31) / 32 * 32);
+  const int R = std::min(std::min(NB_MAX_R, threads / 32), BUDGET / (2 * row_bytes));
+  const int ns = 2;
+  if (R < 1) return -1;
+  const int smem = ns * R * row_bytes + 16 * NB_MAX_R + 4 * 4 * 32 + 8 * ns + 16;
   // the limit is raised once per device, to the largest size any call asks for
   static std::atomic<uint64_t> attr{0};
   if (smem_limit_once(reinterpret_cast<const void*>(norm_bwd_staged_kernel), BUDGET + 1024, &attr)) return 3;

@@ -696,7 +696,8 @@ static int norm_bwd_staged(int64_t rows, int h, int kind, float eps, const NormB
     return p == nullptr || ((reinterpret_cast<uintptr_t>(p) & 15) == 0 && ((ld * elem) & 15) == 0);
   };
   const int xe = io.x_f32 ? 4 : 2, de = io.dy_f32 ? 4 : 2, re = io.res ? (io.res_f32 ? 4 : 2) : 0;
-  if (h % 8 || h > 4096 || !al(io.x, io.ldx, xe) || !al(io.dy, io.lddy, de) || !al(io.res, io.ldres, re ? re : 2))
+  if (h % 8 || h > 4096 || !al(io.x, io.ldx, xe) || !al(io.dy, io.lddy, de) || !al(io.res, io.ldres, re ? re : 2) ||
+      !al(io.dx, io.lddx, 2) || !al(io.dx_f32, io.lddx, 4) || (reinterpret_cast<uintptr_t>(w) & 7))
     return -1;
   const int row_bytes = h * (xe + de + re);
   // one thread per 4 columns; two stages of as many rows as fit (never more

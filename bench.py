@@ -478,38 +478,52 @@ def run_gpu(args, c):
                 "avg_launch_ms": dv["ms"] / dv["launches"], "traffic": traffic}
 
     # end to end through the C ABI from pinned host buffers.  Every step
-    # copies its x and dy in and its dx out inside the timed region; dy
-    # travels on a second stream while the forward runs (the backward waits
-    # for it), and dx leaves on that stream while the next step's x copy and
-    # forward run (the next backward, which overwrites dx, waits for it)
+    # copies its x and dy in and its dx out inside the timed region, the way
+    # a training loop prefetches its next batch: x alternates between two
+    # device buffers, and the next step's x comes in on a copy stream while
+    # this step's backward runs; dy comes in on that stream while the forward
+    # runs (after the previous backward has read it), and dx goes out on a
+    # third stream while the next step's forward runs (the next backward,
+    # which overwrites dx, waits for it).
     xh = x.cpu().pin_memory()
     dyh = dy.cpu().pin_memory() if c.backward else None
     outh = torch.empty_like(xh).pin_memory()
-    copy_st = torch.cuda.Stream(dev)
-    ev_in, ev_used, ev_out = (torch.cuda.Event() for _ in range(3))
+    xs = [x, torch.empty_like(x)] if c.backward else [x]
+    h2d_st, d2h_st = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_x = [torch.cuda.Event() for _ in xs]
+    ev_dy, ev_bwd, ev_out = (torch.cuda.Event() for _ in range(3))
     n_e2e = [0]
 
     def step_e2e():
-        x.copy_(xh, non_blocking=True)
         if not c.backward:
+            x.copy_(xh, non_blocking=True)
             bpt.bpt_layer_fwd(c, W, x, y, saved, ws, stream)
             outh.copy_(y, non_blocking=True)
             return
-        if n_e2e[0]:
-            copy_st.wait_event(ev_used)  # the previous backward has read dy
-        with torch.cuda.stream(copy_st):
+        k = n_e2e[0]
+        xk = xs[k % 2]
+        if k == 0:
+            with torch.cuda.stream(h2d_st):
+                xk.copy_(xh, non_blocking=True)
+                ev_x[0].record(h2d_st)
+        stream.wait_event(ev_x[k % 2])
+        bpt.bpt_layer_fwd(c, W, xk, y, saved, ws, stream)
+        if k:
+            h2d_st.wait_event(ev_bwd)  # the previous backward has read dy and the other x
+        with torch.cuda.stream(h2d_st):
             dy.copy_(dyh, non_blocking=True)
-            ev_in.record(copy_st)
-        bpt.bpt_layer_fwd(c, W, x, y, saved, ws, stream)
-        stream.wait_event(ev_in)
-        if n_e2e[0]:
+            ev_dy.record(h2d_st)
+            xs[(k + 1) % 2].copy_(xh, non_blocking=True)  # the next step's x
+            ev_x[(k + 1) % 2].record(h2d_st)
+        stream.wait_event(ev_dy)
+        if k:
             stream.wait_event(ev_out)  # the previous dx has been copied out
-        bpt.bpt_layer_bwd(c, W, x, saved, dy, dx, grads, ws, stream)
-        ev_used.record(stream)
-        copy_st.wait_event(ev_used)
-        with torch.cuda.stream(copy_st):
+        bpt.bpt_layer_bwd(c, W, xk, saved, dy, dx, grads, ws, stream)
+        ev_bwd.record(stream)
+        d2h_st.wait_event(ev_bwd)
+        with torch.cuda.stream(d2h_st):
             outh.copy_(dx, non_blocking=True)
-            ev_out.record(copy_st)
+            ev_out.record(d2h_st)
         n_e2e[0] += 1
 
     for _ in range(max(1, args.warmup // 2)):
@@ -541,7 +555,8 @@ def run_gpu(args, c):
             "clocks": clk,
             "e2e": {"value": job_throughput(fl["executed"], world, e2e_ms), "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "what": "pinned host x (and dy) copied in, fwd+bwd through the C ABI, dx copied out"},
+                    "what": "pinned host x (and dy) copied in, fwd+bwd through the C ABI, dx copied out; the next "
+                            "step's x comes in during this step's backward, into the other of two device buffers"},
             "gpu_launches": int(round(launches_per_step * args.steps)),
             "roofline": roof, "kernels": kernels, "passes": passes,
             "memory": {"peak_device_bytes": peak_mem, "inputs_weights_grads_bytes": base_mem,

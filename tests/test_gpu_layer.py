@@ -29,7 +29,16 @@ GPT_B2 = LayerConfig(b=2, s=200, h=256, n_heads=2, n_kv_heads=2, head_dim=128, f
 GPT_MANY_TILES = LayerConfig(b=1, s=2500, h=384, n_heads=6, n_kv_heads=6, head_dim=64, ffn_dim=8192,
                              name="gpt many tiles")
 
-LAYERS = [GPT_SMALL, GPT_D80, LLAMA_SMALL, GPT_B2, GPT_MANY_TILES]
+# model width above 4096 (attention narrower than the model): the norms'
+# unstaged backward kernel, which takes the rows the shared-memory-staged one
+# does not, and N = 4352 products; only the tensors of WIDE_TENSORS have an
+# emulated bf16 floor above 5e-3 at these shapes (at most 7.1e-3)
+GPT_WIDE = LayerConfig(b=1, s=160, h=4352, n_heads=4, n_kv_heads=4, head_dim=64, ffn_dim=256, ffn_block=128,
+                       name="gpt h4352")
+LLAMA_WIDE = LayerConfig(b=1, s=160, h=4352, n_heads=4, n_kv_heads=2, head_dim=64, ffn_dim=256, ffn_block=128,
+                         norm=1, act=2, has_bias=0, name="llama h4352")
+
+LAYERS = [GPT_SMALL, GPT_D80, LLAMA_SMALL, GPT_B2, GPT_MANY_TILES, GPT_WIDE, LLAMA_WIDE]
 
 
 @pytest.mark.parametrize("cfg", LAYERS, ids=lambda c: c.name)

@@ -884,8 +884,12 @@ int launch(GemmParams& p, cudaStream_t st) {
   }
 }
 
-// The pair-of-SMs launches (gemm_pair.cu).
+// The pair-of-SMs launches (gemm_pair.cu), and the pairs of CTAs the
+// device holds at once (every pair instance has the same shared memory and
+// threads; 0 when the device cannot hold one, and then gemm() takes the
+// one-SM form).
 int launch_pair(GemmParams& p, bool a_mn, bool b_mn, bool dual, cudaStream_t st);
+int pair_units();
 
 }  // namespace gk
 }  // namespace bpt

@@ -31,8 +31,10 @@ int gemm(int64_t M, int64_t N, int64_t K, const MatView& A, bool a_mn, const Mat
     if (acc != K) return 1;
   }
   const int BN = dual ? 128 : 256;
-  // a pair of SMs per 256-row tile wherever there are two row tiles
-  const bool pair = M > BM;
+  // a pair of SMs per 256-row tile wherever there are two row tiles (and
+  // the device can hold a pair of CTAs)
+  const int pairs = M > BM ? pair_units() : 0;
+  const bool pair = pairs > 0;
   const int TM = pair ? 2 * BM : BM;
   const int BNS = pair ? BN / 2 : BN;  // rows of each B one CTA stages
   // A
@@ -92,7 +94,7 @@ int gemm(int64_t M, int64_t N, int64_t K, const MatView& A, bool a_mn, const Mat
   // unless accumulating).
   p.ksplit = 1;
   {
-    const int nsm = pair ? sm_count() / 2 : sm_count();  // units in flight
+    const int nsm = pair ? pairs : sm_count();  // units in flight
     const int64_t tiles = ((M + TM - 1) / TM) * ((N + BN - 1) / BN);
     auto fill = [&](int64_t units) { return (double)units / (double)(((units + nsm - 1) / nsm) * nsm); };
     const bool aligned = (e.ldo % 4) == 0 && (reinterpret_cast<uintptr_t>(e.out) & 15) == 0;

@@ -705,11 +705,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           ++it;
         }
       }
-      if (*abort_flag && rank == 0) {
+      if (*abort_flag) {
         // let every load issued land before the CTA goes away (a pair's
         // rank 1 waits at the final cluster barrier meanwhile)
-        for (uint32_t j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
-          drain_wait(&full[j % STAGES], (j / STAGES) & 1);
+        if (rank == 0)
+          for (uint32_t j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+            drain_wait(&full[j % STAGES], (j / STAGES) & 1);
+        // a pair: the loads of rank 1 complete on rank 0's barriers, so
+        // neither side can wait for the other's stragglers; both give them
+        // a fixed 10^6 cycles (about half a millisecond) before the final
+        // cluster barrier
+        if (PAIR) {
+          const long long t0 = clock64();
+          while (clock64() - t0 < 1000000) {
+          }
+        }
       }
     }
   } else if (warp == 1) {
